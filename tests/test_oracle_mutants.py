@@ -1,0 +1,123 @@
+"""Planted mistakes in the oracle (on the CPU): each mutant replaces one
+oracle function with a plausible wrong version, and at least one pin in
+test_oracle_pins.py must then fail.  This shows the pins are discriminating,
+not restatements of the oracle's own formulas."""
+import numpy as np
+import pytest
+
+import oracle as O
+import oracle.coda_oracle as OC
+from tests import test_oracle_pins as P
+
+
+def _patch(monkeypatch, name, fn):
+    monkeypatch.setattr(OC, name, fn)
+    monkeypatch.setattr(O, name, fn)
+
+
+def _fails(check, *args):
+    with pytest.raises((AssertionError, ValueError, IndexError)):
+        check(*args)
+
+
+def test_mutant_rstd_sum_instead_of_mean(monkeypatch):
+    _patch(monkeypatch, "rms_rstd",
+           lambda h, eps=1e-5: 1.0 / np.sqrt(np.sum(np.asarray(h) ** 2, axis=1) + eps))
+    _fails(P.test_rstd_constant_row, 0.5)
+
+
+def test_mutant_eps_outside_sqrt(monkeypatch):
+    _patch(monkeypatch, "rms_rstd",
+           lambda h, eps=1e-5: 1.0 / (np.sqrt(np.mean(np.asarray(h) ** 2, axis=1)) + eps))
+    _fails(P.test_rstd_constant_row, 0.0)
+
+
+def test_mutant_fold_on_wrong_axis(monkeypatch):
+    _patch(monkeypatch, "fold_weight",
+           lambda W2t, g: np.asarray(W2t) * np.asarray(g)[: np.asarray(W2t).shape[0], None])
+    _fails(P.test_fold_and_rowscale_commute)
+
+
+def test_mutant_swiglu_halves_swapped(monkeypatch):
+    def bad(z):
+        F = z.shape[1] // 2
+        return OC.silu(z[:, F:]) * z[:, :F]
+    _patch(monkeypatch, "swiglu", bad)
+    _fails(P.test_swiglu_halves)
+
+
+def test_mutant_matmul_not_transposed(monkeypatch):
+    _patch(monkeypatch, "matmul_nt", lambda A, Bt: np.asarray(A) @ np.asarray(Bt))
+    _fails(P.test_matmul_bruteforce)
+
+
+def _bad_block_backward(drop_projection=False, flip_sign=False):
+    good = OC.block_backward
+
+    def bad(X, W1t, R, g, W2t, dY, eps=1e-5, swiglu_act=True):
+        out = good(X, W1t, R, g, W2t, dY, eps, swiglu_act)
+        h, r = out["h"], out["rstd"]
+        d = h.shape[1]
+        dN = out["dZ"] @ np.asarray(W2t)
+        dn = dN * np.asarray(g)[None, :]
+        proj = np.sum(dn * h, axis=1)
+        if drop_projection:
+            dh = r[:, None] * dn
+        else:
+            dh = r[:, None] * dn + (r ** 3 / d)[:, None] * h * proj[:, None]
+        out = dict(out)
+        out["dh"] = out["dR"] = dh
+        out["dX"] = dh @ np.asarray(W1t)
+        out["dW1t"] = dh.T @ np.asarray(X)
+        return out
+    return bad
+
+
+def test_mutant_rmsnorm_bwd_missing_projection(monkeypatch):
+    _patch(monkeypatch, "block_backward", _bad_block_backward(drop_projection=True))
+    _fails(P.test_block_backward_finite_difference, True)
+
+
+def test_mutant_rmsnorm_bwd_sign(monkeypatch):
+    _patch(monkeypatch, "block_backward", _bad_block_backward(flip_sign=True))
+    _fails(P.test_block_backward_finite_difference, False)
+
+
+def test_mutant_c_missing_over_d(monkeypatch):
+    good = OC.stage_swiglu_bwd
+    _patch(monkeypatch, "stage_swiglu_bwd",
+           lambda dY, z, rstd, d: (lambda a: (a[0], a[1] * d))(good(dY, z, rstd, d)))
+    _fails(P.test_fused_stages_compose_to_textbook_backward)
+
+
+def test_mutant_dg_with_extra_g(monkeypatch):
+    good = OC.stage_dgrad2_rmsbwd
+
+    def bad(dP, W2t, g, h, c):
+        dh, dg = good(dP, W2t, g, h, c)
+        return dh, dg * np.asarray(g)
+    _patch(monkeypatch, "stage_dgrad2_rmsbwd", bad)
+    _fails(P.test_fused_stages_compose_to_textbook_backward)
+
+
+def test_mutant_lse_combine_unweighted(monkeypatch):
+    _patch(monkeypatch, "lse_combine",
+           lambda mx, se: np.max(mx, axis=1) + np.log(np.sum(se, axis=1)))
+    _fails(P.test_lse_combine_identity, 7)
+
+
+def test_mutant_argmax_highest_on_tie(monkeypatch):
+    _patch(monkeypatch, "argmax_lowest",
+           lambda L: (L.shape[1] - 1 - np.argmax(L[:, ::-1], axis=1)).astype(np.int64))
+    _fails(P.test_ce_argmax_tie_lowest_index)
+
+
+def test_mutant_ce_grad_missing_mean(monkeypatch):
+    good = OC.ce_backward
+
+    def bad(H, Wt, labels, row_chunk=256):
+        out = good(H, Wt, labels, row_chunk)
+        M = np.asarray(H).shape[0]
+        return {"dH": out["dH"] * M, "dWt": out["dWt"] * M}
+    _patch(monkeypatch, "ce_backward", bad)
+    _fails(P.test_ce_backward_finite_difference_and_row_sum)

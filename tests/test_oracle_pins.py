@@ -1,0 +1,327 @@
+"""Pins for the fp64 oracle: every check here is independent of the oracle's
+own formulas (brute force, closed forms, finite differences, an independent
+autograd library, hand-worked fixtures), so a dropped term, a wrong sign or
+index, or a transposed operand in the oracle fails at least one of them.
+
+Method: "CODA: Rewriting Transformer Blocks as GEMM-Epilogue Programs" as
+summarised by the Synced article (sections 尾声 and 五种积木).
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle as O
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def rng(seed=0):
+    return np.random.default_rng(seed)
+
+
+# --------------------------------------------------------------------------
+# GEMM
+# --------------------------------------------------------------------------
+
+def brute_nt(A, Bt):
+    M, K = A.shape
+    N = Bt.shape[0]
+    C = np.zeros((M, N))
+    for m in range(M):
+        for n in range(N):
+            s = 0.0
+            for k in range(K):
+                s += A[m, k] * Bt[n, k]
+            C[m, n] = s
+    return C
+
+
+def test_matmul_bruteforce():
+    r = rng(1)
+    A = r.standard_normal((3, 5))
+    Bt = r.standard_normal((4, 5))
+    np.testing.assert_allclose(O.matmul_nt(A, Bt), brute_nt(A, Bt), rtol=1e-13, atol=1e-13)
+
+
+def test_gemm_integer_known_answer():
+    # integer-valued operands: the exact result is an integer matrix
+    A = np.array([[1, 2, 3], [0, -1, 4]], float)
+    Bt = np.array([[1, 0, 0], [0, 1, 0], [1, 1, 1], [2, -1, 0]], float)
+    expect = np.array([[1, 2, 6, 0], [0, -1, 3, 1]], float)
+    assert np.array_equal(O.matmul_nt(A, Bt), expect)
+    R = np.ones((2, 4))
+    assert np.array_equal(O.gemm_residual(A, Bt, R), expect + 1)
+
+
+# --------------------------------------------------------------------------
+# RMSNorm, partial RMS and the combine
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("c", [0.0, 0.5, 3.0, -2.0])
+def test_rstd_constant_row(c):
+    eps = 1e-5
+    h = np.full((2, 37), c)
+    np.testing.assert_allclose(O.rms_rstd(h, eps), 1.0 / math.sqrt(c * c + eps), rtol=1e-15)
+
+
+def test_rstd_bruteforce_mean_not_sum():
+    h = np.array([[3.0, 4.0, 0.0, 0.0]])
+    # mean of squares = 25/4
+    assert O.rms_rstd(h, 0.0)[0] == pytest.approx(1.0 / 2.5, rel=1e-15)
+
+
+@pytest.mark.parametrize("bn", [1, 16, 100, 128, 300])
+def test_partial_sumsq_tiling_invariance(bn):
+    h = rng(2).standard_normal((5, 300))
+    ps = O.partial_sumsq(h, bn)
+    assert ps.shape == (5, -(-300 // bn))
+    np.testing.assert_allclose(ps.sum(axis=1), (h * h).sum(axis=1), rtol=1e-13)
+    # brute force of each block
+    for j in range(ps.shape[1]):
+        for m in range(5):
+            s = 0.0
+            for k in range(j * bn, min(300, (j + 1) * bn)):
+                s += h[m, k] ** 2
+            assert ps[m, j] == pytest.approx(s, rel=1e-13)
+
+
+def test_rstd_from_partials_matches_rstd():
+    h = rng(3).standard_normal((7, 96)) * 2
+    for bn in (8, 32, 96):
+        np.testing.assert_allclose(O.rstd_from_partials(O.partial_sumsq(h, bn), 96, 1e-5),
+                                   O.rms_rstd(h, 1e-5), rtol=1e-14)
+
+
+def test_rmsnorm_unit_rms():
+    h = rng(4).standard_normal((6, 64)) * 7
+    n = O.rmsnorm(h, np.ones(64), eps=0.0)
+    np.testing.assert_allclose(np.mean(n * n, axis=1), 1.0, rtol=1e-13)
+
+
+# --------------------------------------------------------------------------
+# the re-parameterisation: fold g, defer r past the second GEMM
+# --------------------------------------------------------------------------
+
+def test_fold_and_rowscale_commute():
+    r = rng(5)
+    M, d, N2 = 6, 10, 14          # d != N2 so a transposed g would not broadcast
+    h = r.standard_normal((M, d))
+    g = r.uniform(0.5, 1.5, d)
+    W2t = r.standard_normal((N2, d))
+    rstd = O.rms_rstd(h, 1e-5)
+    z_fused = O.rowscale_gemm(h, O.fold_weight(W2t, g), rstd)
+    # unfused: explicit normalised activation, then a brute-force GEMM
+    n = np.array([[h[m, k] * rstd[m] * g[k] for k in range(d)] for m in range(M)])
+    np.testing.assert_allclose(z_fused, brute_nt(n, W2t), rtol=1e-12, atol=1e-13)
+
+
+def test_fold_weight_bruteforce():
+    W2t = np.arange(12, dtype=float).reshape(3, 4)
+    g = np.array([1.0, 2.0, 0.5, -1.0])
+    expect = np.array([[W2t[i, k] * g[k] for k in range(4)] for i in range(3)])
+    assert np.array_equal(O.fold_weight(W2t, g), expect)
+
+
+# --------------------------------------------------------------------------
+# SwiGLU
+# --------------------------------------------------------------------------
+
+def test_silu_special_values():
+    assert O.silu(0.0) == 0.0
+    assert O.silu(1.0) == pytest.approx(1.0 / (1.0 + math.exp(-1.0)), rel=1e-15)
+    assert O.silu(40.0) == pytest.approx(40.0, rel=1e-15)
+    assert abs(O.silu(-40.0)) < 1e-15
+    assert O.silu_grad(0.0) == pytest.approx(0.5, rel=1e-15)
+
+
+def test_silu_grad_finite_difference():
+    x = np.linspace(-6, 6, 41)
+    e = 1e-6
+    fd = (O.silu(x + e) - O.silu(x - e)) / (2 * e)
+    np.testing.assert_allclose(O.silu_grad(x), fd, rtol=1e-8, atol=1e-9)
+
+
+def test_swiglu_halves():
+    z = np.array([[0.0, 2.0, 5.0, 7.0],      # gate=[0,2], up=[5,7]
+                  [30.0, -30.0, 3.0, 4.0]])
+    out = O.swiglu(z)
+    assert out.shape == (2, 2)
+    assert out[0, 0] == 0.0                   # silu(0) * 5
+    assert out[0, 1] == pytest.approx(2.0 / (1 + math.exp(-2.0)) * 7.0, rel=1e-15)
+    assert out[1, 0] == pytest.approx(30.0 * 3.0, rel=1e-12)
+    assert out[1, 1] == pytest.approx(-30.0 / (1 + math.exp(30.0)) * 4.0, rel=1e-12)
+
+
+# --------------------------------------------------------------------------
+# backward: finite differences and an independent autograd
+# --------------------------------------------------------------------------
+
+def _tiny_block(seed, swiglu_act=True, M=3, K1=4, d=5, F=3):
+    r = rng(seed)
+    N2 = 2 * F if swiglu_act else F
+    return dict(X=r.standard_normal((M, K1)), W1t=r.standard_normal((d, K1)) * 0.5,
+                R=r.standard_normal((M, d)), g=r.uniform(0.5, 1.5, d),
+                W2t=r.standard_normal((N2, d)) * 0.5, dY=r.standard_normal((M, F)))
+
+
+def _loss(p, swiglu_act):
+    fw = O.block_forward(p["X"], p["W1t"], p["R"], p["g"], p["W2t"], 1e-5, swiglu_act)
+    return float(np.sum(fw["out"] * p["dY"]))
+
+
+@pytest.mark.parametrize("swiglu_act", [True, False])
+def test_block_backward_finite_difference(swiglu_act):
+    p = _tiny_block(7, swiglu_act)
+    gr = O.block_backward(p["X"], p["W1t"], p["R"], p["g"], p["W2t"], p["dY"], 1e-5, swiglu_act)
+    names = {"X": "dX", "W1t": "dW1t", "R": "dR", "g": "dg", "W2t": "dW2t"}
+    e = 1e-6
+    for k, gk in names.items():
+        a = p[k]
+        fd = np.zeros_like(a)
+        for idx in np.ndindex(a.shape):
+            old = a[idx]
+            a[idx] = old + e
+            lp = _loss(p, swiglu_act)
+            a[idx] = old - e
+            lm = _loss(p, swiglu_act)
+            a[idx] = old
+            fd[idx] = (lp - lm) / (2 * e)
+        np.testing.assert_allclose(gr[gk], fd, rtol=1e-6, atol=1e-7, err_msg=k)
+
+
+def test_block_backward_matches_torch_autograd():
+    torch = pytest.importorskip("torch")
+    p = _tiny_block(11, True, M=4, K1=6, d=8, F=5)
+    t = {k: torch.tensor(v, dtype=torch.float64, requires_grad=True) for k, v in p.items()}
+    h = t["X"] @ t["W1t"].T + t["R"]
+    n = torch.nn.functional.rms_norm(h, (8,), weight=t["g"], eps=1e-5)
+    z = n @ t["W2t"].T
+    out = torch.nn.functional.silu(z[:, :5]) * z[:, 5:]
+    (out * t["dY"]).sum().backward()
+    gr = O.block_backward(p["X"], p["W1t"], p["R"], p["g"], p["W2t"], p["dY"], 1e-5, True)
+    for k, gk in {"X": "dX", "W1t": "dW1t", "R": "dR", "g": "dg", "W2t": "dW2t"}.items():
+        np.testing.assert_allclose(gr[gk], t[k].grad.numpy(), rtol=1e-11, atol=1e-12, err_msg=k)
+    np.testing.assert_allclose(O.block_forward(p["X"], p["W1t"], p["R"], p["g"], p["W2t"])["out"],
+                               out.detach().numpy(), rtol=1e-12, atol=1e-13)
+
+
+def test_fused_stages_compose_to_textbook_backward():
+    """The fused stage definitions (dP, c, dh = g*acc - c*h, dg = sum acc*h,
+    dW2 = g * h^T dP) reproduce the chain-rule backward exactly in fp64."""
+    p = _tiny_block(13, True, M=6, K1=7, d=9, F=4)
+    ref = O.block_backward(p["X"], p["W1t"], p["R"], p["g"], p["W2t"], p["dY"])
+    h = O.gemm_residual(p["X"], p["W1t"], p["R"])
+    rstd = O.rstd_from_partials(O.partial_sumsq(h, 4), 9, 1e-5)
+    z = O.rowscale_gemm(h, O.fold_weight(p["W2t"], p["g"]), rstd)
+    np.testing.assert_allclose(O.swiglu(z), ref["out"], rtol=1e-12, atol=1e-13)
+    dP, c = O.stage_swiglu_bwd(p["dY"], z, rstd, 9)
+    dh, dg = O.stage_dgrad2_rmsbwd(dP, p["W2t"], p["g"], h, c)
+    np.testing.assert_allclose(dh, ref["dh"], rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(dg, ref["dg"], rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(O.stage_wgrad2(h, dP, p["g"]), ref["dW2t"], rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(O.stage_dgrad1(dh, p["W1t"]), ref["dX"], rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(O.stage_wgrad1(dh, p["X"]), ref["dW1t"], rtol=1e-11, atol=1e-12)
+
+
+# --------------------------------------------------------------------------
+# blocked log-sum-exp and cross-entropy
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("bn", [1, 7, 64, 200])
+def test_lse_combine_identity(bn):
+    L = rng(17).standard_normal((4, 200)) * 5
+    mx, se = O.lse_tile_partials(L, bn)
+    direct = np.log(np.sum(np.exp(L), axis=1))
+    np.testing.assert_allclose(O.lse_combine(mx, se), direct, rtol=1e-13)
+    np.testing.assert_allclose(O.lse_rows(L), direct, rtol=1e-13)
+
+
+def test_lse_large_values_and_constant_row():
+    L = np.full((1, 10), 1000.0)
+    assert O.lse_rows(L)[0] == pytest.approx(1000.0 + math.log(10.0), rel=1e-15)
+    mx, se = O.lse_tile_partials(L, 3)
+    assert O.lse_combine(mx, se)[0] == pytest.approx(1000.0 + math.log(10.0), rel=1e-15)
+
+
+def test_ce_uniform_logits_is_log_v():
+    V, d, M = 37, 8, 5
+    out = O.ce_forward(rng(1).standard_normal((M, d)), np.zeros((V, d)), np.arange(M) % V)
+    assert out["loss"] == pytest.approx(math.log(V), rel=1e-15)
+
+
+def test_ce_argmax_tie_lowest_index():
+    H = np.array([[1.0, 2.0]])
+    Wt = np.array([[0.0, 0.0], [1.0, 1.0], [-1.0, 0.0], [1.0, 1.0]])  # columns 1 and 3 tie
+    out = O.ce_forward(H, Wt, np.array([2]))
+    assert out["argmax"][0] == 1
+
+
+def test_ce_backward_finite_difference_and_row_sum():
+    r = rng(19)
+    M, d, V = 3, 4, 6
+    H = r.standard_normal((M, d))
+    Wt = r.standard_normal((V, d))
+    y = np.array([0, 5, 2])
+    gr = O.ce_backward(H, Wt, y, row_chunk=2)
+    e = 1e-6
+    for a, ga in ((H, gr["dH"]), (Wt, gr["dWt"])):
+        fd = np.zeros_like(a)
+        for idx in np.ndindex(a.shape):
+            old = a[idx]
+            a[idx] = old + e
+            lp = O.ce_forward(H, Wt, y, row_chunk=2)["loss"]
+            a[idx] = old - e
+            lm = O.ce_forward(H, Wt, y, row_chunk=2)["loss"]
+            a[idx] = old
+            fd[idx] = (lp - lm) / (2 * e)
+        np.testing.assert_allclose(ga, fd, rtol=1e-6, atol=1e-9)
+    # softmax minus one-hot sums to zero per row: with Wt = I columns, dH rows sum to 0
+    Wi = np.eye(V)
+    g2 = O.ce_backward(r.standard_normal((M, V)), Wi, y)
+    np.testing.assert_allclose(g2["dH"].sum(axis=1), 0.0, atol=1e-15)
+
+
+def test_ce_expected_loss_statistics():
+    """L = H W with H ~ N(0,1), W ~ N(0, 0.02), d = 2048: logits are
+    N(0, s^2), s^2 = d * 0.02^2 = 0.8192, so E[lse] ~= ln V + s^2/2 for large V
+    and E[loss] ~= ln V + s^2 / 2."""
+    r = rng(23)
+    M, d, V = 64, 2048, 8192
+    H = r.standard_normal((M, d))
+    Wt = r.standard_normal((V, d)) * 0.02
+    y = r.integers(0, V, M)
+    loss = O.ce_forward(H, Wt, y, row_chunk=64)["loss"]
+    assert loss == pytest.approx(math.log(V) + 0.8192 / 2, abs=0.25)
+
+
+# --------------------------------------------------------------------------
+# hand-worked fixtures
+# --------------------------------------------------------------------------
+
+def test_golden_block_forward_worked_example():
+    f = json.load(open(os.path.join(GOLD, "block_fwd_worked.json")))
+    arr = {k: np.array(f[k], float) for k in ("X", "W1t", "R", "g", "W2t")}
+    fw = O.block_forward(arr["X"], arr["W1t"], arr["R"], arr["g"], arr["W2t"], f["eps"], True)
+    for k, v in f["expect"].items():
+        np.testing.assert_allclose(fw[k], np.array(v), rtol=1e-14, atol=1e-15, err_msg=k)
+    # the fused route reaches the same numbers
+    h = O.gemm_residual(arr["X"], arr["W1t"], arr["R"])
+    rstd = O.rstd_from_partials(O.partial_sumsq(h, 1), 2, f["eps"])
+    z = O.rowscale_gemm(h, O.fold_weight(arr["W2t"], arr["g"]), rstd)
+    np.testing.assert_allclose(O.swiglu(z), np.array(f["expect"]["out"]), rtol=1e-14)
+
+
+def test_golden_ce_worked_example():
+    f = json.load(open(os.path.join(GOLD, "ce_worked.json")))
+    H, Wt, y = np.array(f["H"], float), np.array(f["Wt"], float), np.array(f["labels"])
+    fw = O.ce_forward(H, Wt, y)
+    ex = f["expect"]
+    assert fw["loss"] == pytest.approx(ex["loss"], rel=1e-14)
+    np.testing.assert_allclose(fw["lse"], ex["lse"], rtol=1e-14)
+    assert list(fw["argmax"]) == ex["argmax"]
+    bw = O.ce_backward(H, Wt, y)
+    np.testing.assert_allclose(bw["dH"], ex["dH"], rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(bw["dWt"], ex["dWt"], rtol=1e-13, atol=1e-15)
