@@ -1,0 +1,355 @@
+"""Python binding of libcoda (include/coda.h): Transformer-block memory-bound
+operations run as GEMM epilogues on sm_103a.
+
+Argument marshalling only: every function here takes torch tensors already
+on the GPU, checks dtype/shape/contiguity, and calls the C entry point of the
+same name with raw pointers and extents on the current torch stream.  All
+arithmetic runs in the library's CUDA kernels.  There is no fallback: if
+libcoda.so is missing or cannot be loaded, importing the binding's entry
+points raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libcoda.so")
+
+CODA_EPI_SWIGLU = 0
+CODA_EPI_PLAIN = 1
+
+STATUS_NAMES = {
+    0: "CODA_OK", 1: "CODA_ERR_INVALID_ARG", 2: "CODA_ERR_ALIGNMENT", 3: "CODA_ERR_UNSUPPORTED",
+    4: "CODA_ERR_WORKSPACE_TOO_SMALL", 5: "CODA_ERR_CUDA", 6: "CODA_ERR_TIMEOUT", 7: "CODA_ERR_LABEL_RANGE",
+}
+
+
+class CodaError(RuntimeError):
+    def __init__(self, code: int, where: str, msg: str):
+        super().__init__(f"{where}: {STATUS_NAMES.get(code, code)} ({msg})")
+        self.code = code
+
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_U64 = ctypes.c_uint64
+_U32 = ctypes.c_uint32
+_INT = ctypes.c_int
+_F32 = ctypes.c_float
+_SZ = ctypes.c_size_t
+
+# name -> (restype, argtypes), mirroring include/coda.h
+SIGNATURES = {
+    "coda_create": (_INT, [ctypes.POINTER(_P), _INT]),
+    "coda_destroy": (_INT, [_P]),
+    "coda_status_string": (ctypes.c_char_p, [_INT]),
+    "coda_sync_status": (_INT, [_P, _P, ctypes.POINTER(ctypes.c_int32)]),
+    "coda_set_wait_timeout_ns": (_INT, [_P, _U64]),
+    "coda_prms_num_tiles": (_I64, [_I64]),
+    "coda_dgpart_rows": (_I64, [_I64]),
+    "coda_gemm": (_INT, [_P, _P, _INT, _P, _INT, _P, _I64, _I64, _I64, _P, _P, _P]),
+    "coda_fold_rmsnorm_weight": (_INT, [_P, _P, _P, _P, _I64, _I64, _P]),
+    "coda_gemm_res_prms": (_INT, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
+    "coda_rstd_combine": (_INT, [_P, _P, _I64, _I64, _I64, _F32, _P, _P]),
+    "coda_gemm_rowscale_swiglu": (_INT, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _U32, _P]),
+    "coda_swiglu_bwd": (_INT, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
+    "coda_gemm_dgrad_rmsbwd": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
+    "coda_dg_combine": (_INT, [_P, _P, _I64, _I64, _P, _P]),
+    "coda_gemm_wgrad_gscale": (_INT, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
+    "coda_bwd_workspace_bytes": (_SZ, [_I64, _I64, _I64]),
+    "coda_gemm_rowscale_swiglu_bwd": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
+                                             _I64, _I64, _I64, _P]),
+    "coda_gemm_res_prms_bwd": (_INT, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
+    "coda_lmhead_ce_workspace_bytes": (_SZ, [_I64, _I64, _I64, _INT]),
+    "coda_lmhead_ce": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I64, _I64, _I64, _P]),
+    "coda_unfused_workspace_bytes": (_SZ, [_I64, _I64, _I64]),
+    "coda_unfused_fwd": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
+                                _I64, _I64, _I64, _I64, _F32, _U32, _P]),
+    "coda_unfused_bwd": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
+                                _I64, _I64, _I64, _I64, _P]),
+}
+
+_lib = None
+_lib_lock = threading.Lock()
+_handles: dict[int, int] = {}
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libcoda.so (built by gemm_epilogue_transformer_tma_gb300.build) and
+    declare every entry point's signature.  Raises if it is missing."""
+    global _lib
+    with _lib_lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise ImportError(f"{path} is missing: build it with "
+                              "`python -m gemm_epilogue_transformer_tma_gb300.build`")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+def _check(code: int, where: str):
+    if code != 0:
+        msg = load_library().coda_status_string(code).decode()
+        raise CodaError(code, where, msg)
+
+
+def handle(device: int | None = None) -> int:
+    """The library handle of a CUDA device (created once per device)."""
+    lib = load_library()
+    dev = torch.cuda.current_device() if device is None else int(device)
+    h = _handles.get(dev)
+    if h is None:
+        hp = _P()
+        _check(lib.coda_create(ctypes.byref(hp), dev), "coda_create")
+        h = hp.value
+        _handles[dev] = h
+    return h
+
+
+def _stream(stream=None) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _ptr(t: torch.Tensor | None, dtype=None, name="tensor") -> int | None:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _shape(t, shape, name):
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+BF = torch.bfloat16
+F32 = torch.float32
+I32 = torch.int32
+
+
+def _h(t: torch.Tensor) -> int:
+    return handle(t.device.index)
+
+
+# ---------------------------------------------------------------------------
+def coda_sync_status(device: int | None = None, stream=None) -> tuple[int, int]:
+    """Synchronise the stream, read and clear the device status word.
+    Returns (status, raw_bits); does not raise."""
+    lib = load_library()
+    bits = ctypes.c_int32(0)
+    st = lib.coda_sync_status(handle(device), _stream(stream), ctypes.byref(bits))
+    return st, bits.value
+
+
+def coda_set_wait_timeout_ns(ns: int, device: int | None = None):
+    _check(load_library().coda_set_wait_timeout_ns(handle(device), ns), "coda_set_wait_timeout_ns")
+
+
+def coda_prms_num_tiles(d: int) -> int:
+    return load_library().coda_prms_num_tiles(d)
+
+
+def coda_dgpart_rows(M: int) -> int:
+    return load_library().coda_dgpart_rows(M)
+
+
+def coda_gemm(A, a_mn_major: bool, B, b_mn_major: bool, C, M: int, N: int, K: int,
+              row_scale=None, col_scale=None, stream=None):
+    """C[M,N] = row_scale * col_scale * A B (see include/coda.h)."""
+    _shape(A, (K, M) if a_mn_major else (M, K), "A")
+    _shape(B, (K, N) if b_mn_major else (N, K), "B")
+    _shape(C, (M, N), "C")
+    if row_scale is not None:
+        _shape(row_scale, (M,), "row_scale")
+    if col_scale is not None:
+        _shape(col_scale, (N,), "col_scale")
+    _check(load_library().coda_gemm(_h(C), _ptr(A, BF, "A"), int(a_mn_major), _ptr(B, BF, "B"), int(b_mn_major),
+                                    _ptr(C, BF, "C"), M, N, K, _ptr(row_scale, F32, "row_scale"),
+                                    _ptr(col_scale, BF, "col_scale"), _stream(stream)), "coda_gemm")
+
+
+def coda_fold_rmsnorm_weight(W2t, g, W2gt, stream=None):
+    N2, d = W2t.shape
+    _shape(g, (d,), "g")
+    _shape(W2gt, (N2, d), "W2gt")
+    _check(load_library().coda_fold_rmsnorm_weight(_h(W2t), _ptr(W2t, BF, "W2t"), _ptr(g, BF, "g"),
+                                                   _ptr(W2gt, BF, "W2gt"), N2, d, _stream(stream)),
+           "coda_fold_rmsnorm_weight")
+
+
+def coda_gemm_res_prms(X, W1t, R, H, psum, stream=None):
+    M, K1 = X.shape
+    d = W1t.shape[0]
+    _shape(W1t, (d, K1), "W1t")
+    _shape(R, (M, d), "R")
+    _shape(H, (M, d), "H")
+    _shape(psum, (M, coda_prms_num_tiles(d)), "psum")
+    _check(load_library().coda_gemm_res_prms(_h(X), _ptr(X, BF, "X"), _ptr(W1t, BF, "W1t"), _ptr(R, BF, "R"),
+                                             _ptr(H, BF, "H"), _ptr(psum, F32, "psum"), M, K1, d, _stream(stream)),
+           "coda_gemm_res_prms")
+
+
+def coda_rstd_combine(psum, d: int, eps: float, rstd, stream=None):
+    M, T = psum.shape
+    _shape(rstd, (M,), "rstd")
+    _check(load_library().coda_rstd_combine(_h(psum), _ptr(psum, F32, "psum"), M, T, d, eps,
+                                            _ptr(rstd, F32, "rstd"), _stream(stream)), "coda_rstd_combine")
+
+
+def coda_gemm_rowscale_swiglu(H, W2gt, rstd, out, z_save=None, flags=CODA_EPI_SWIGLU, stream=None):
+    M, d = H.shape
+    N2 = W2gt.shape[0]
+    _shape(W2gt, (N2, d), "W2gt")
+    _shape(rstd, (M,), "rstd")
+    _shape(out, (M, N2 // 2 if flags == CODA_EPI_SWIGLU else N2), "out")
+    if z_save is not None:
+        _shape(z_save, (M, N2), "z_save")
+    _check(load_library().coda_gemm_rowscale_swiglu(_h(H), _ptr(H, BF, "H"), _ptr(W2gt, BF, "W2gt"),
+                                                    _ptr(rstd, F32, "rstd"), _ptr(out, BF, "out"),
+                                                    _ptr(z_save, BF, "z_save"), M, d, N2, flags, _stream(stream)),
+           "coda_gemm_rowscale_swiglu")
+
+
+def coda_swiglu_bwd(dY, z, rstd, dP, c, d: int, stream=None):
+    M, F = dY.shape
+    _shape(z, (M, 2 * F), "z")
+    _shape(rstd, (M,), "rstd")
+    _shape(dP, (M, 2 * F), "dP")
+    _shape(c, (M,), "c")
+    _check(load_library().coda_swiglu_bwd(_h(dY), _ptr(dY, BF, "dY"), _ptr(z, BF, "z"), _ptr(rstd, F32, "rstd"),
+                                          _ptr(dP, BF, "dP"), _ptr(c, F32, "c"), M, F, d, _stream(stream)),
+           "coda_swiglu_bwd")
+
+
+def coda_gemm_dgrad_rmsbwd(dP, W2t, H, g, c, dH, dgpart, stream=None):
+    M, N2 = dP.shape
+    d = W2t.shape[1]
+    _shape(W2t, (N2, d), "W2t")
+    _shape(H, (M, d), "H")
+    _shape(g, (d,), "g")
+    _shape(c, (M,), "c")
+    _shape(dH, (M, d), "dH")
+    _shape(dgpart, (coda_dgpart_rows(M), d), "dgpart")
+    _check(load_library().coda_gemm_dgrad_rmsbwd(_h(dP), _ptr(dP, BF, "dP"), _ptr(W2t, BF, "W2t"), _ptr(H, BF, "H"),
+                                                 _ptr(g, BF, "g"), _ptr(c, F32, "c"), _ptr(dH, BF, "dH"),
+                                                 _ptr(dgpart, F32, "dgpart"), M, N2, d, _stream(stream)),
+           "coda_gemm_dgrad_rmsbwd")
+
+
+def coda_dg_combine(dgpart, dg, stream=None):
+    rows, d = dgpart.shape
+    _shape(dg, (d,), "dg")
+    _check(load_library().coda_dg_combine(_h(dg), _ptr(dgpart, F32, "dgpart"), rows, d, _ptr(dg, F32, "dg"),
+                                          _stream(stream)), "coda_dg_combine")
+
+
+def coda_gemm_wgrad_gscale(H, dP, g, dW2t, stream=None):
+    M, d = H.shape
+    N2 = dP.shape[1]
+    _shape(dP, (M, N2), "dP")
+    _shape(g, (d,), "g")
+    _shape(dW2t, (N2, d), "dW2t")
+    _check(load_library().coda_gemm_wgrad_gscale(_h(H), _ptr(H, BF, "H"), _ptr(dP, BF, "dP"), _ptr(g, BF, "g"),
+                                                 _ptr(dW2t, BF, "dW2t"), M, N2, d, _stream(stream)),
+           "coda_gemm_wgrad_gscale")
+
+
+def coda_bwd_workspace_bytes(M: int, d: int, N2: int) -> int:
+    return load_library().coda_bwd_workspace_bytes(M, d, N2)
+
+
+def coda_gemm_rowscale_swiglu_bwd(dY, z, rstd, H, W2t, g, dH, dW2t, dg, ws, stream=None):
+    M, d = H.shape
+    N2 = W2t.shape[0]
+    _shape(dY, (M, N2 // 2), "dY")
+    _shape(z, (M, N2), "z")
+    _shape(rstd, (M,), "rstd")
+    _shape(W2t, (N2, d), "W2t")
+    _shape(g, (d,), "g")
+    _shape(dH, (M, d), "dH")
+    _shape(dW2t, (N2, d), "dW2t")
+    _shape(dg, (d,), "dg")
+    _check(load_library().coda_gemm_rowscale_swiglu_bwd(
+        _h(H), _ptr(dY, BF, "dY"), _ptr(z, BF, "z"), _ptr(rstd, F32, "rstd"), _ptr(H, BF, "H"),
+        _ptr(W2t, BF, "W2t"), _ptr(g, BF, "g"), _ptr(dH, BF, "dH"), _ptr(dW2t, BF, "dW2t"), _ptr(dg, F32, "dg"),
+        _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), M, d, N2, _stream(stream)),
+        "coda_gemm_rowscale_swiglu_bwd")
+
+
+def coda_gemm_res_prms_bwd(dH, X, W1t, dX, dW1t, dR=None, stream=None):
+    M, K1 = X.shape
+    d = W1t.shape[0]
+    _shape(dH, (M, d), "dH")
+    _shape(W1t, (d, K1), "W1t")
+    _shape(dX, (M, K1), "dX")
+    _shape(dW1t, (d, K1), "dW1t")
+    if dR is not None:
+        _shape(dR, (M, d), "dR")
+    _check(load_library().coda_gemm_res_prms_bwd(_h(X), _ptr(dH, BF, "dH"), _ptr(X, BF, "X"), _ptr(W1t, BF, "W1t"),
+                                                 _ptr(dX, BF, "dX"), _ptr(dW1t, BF, "dW1t"), _ptr(dR, BF, "dR"),
+                                                 M, K1, d, _stream(stream)), "coda_gemm_res_prms_bwd")
+
+
+def coda_lmhead_ce_workspace_bytes(M: int, d: int, V: int, with_grads: bool) -> int:
+    return load_library().coda_lmhead_ce_workspace_bytes(M, d, V, int(with_grads))
+
+
+def coda_lmhead_ce(Hs, Wt, labels, loss, lse, argmax, dHs, dWt, ws, stream=None):
+    M, d = Hs.shape
+    V = Wt.shape[0]
+    _shape(Wt, (V, d), "Wt")
+    _shape(labels, (M,), "labels")
+    _shape(loss, (1,), "loss")
+    _shape(lse, (M,), "lse")
+    if argmax is not None:
+        _shape(argmax, (M,), "argmax")
+    if dHs is not None:
+        _shape(dHs, (M, d), "dHs")
+        _shape(dWt, (V, d), "dWt")
+    _check(load_library().coda_lmhead_ce(
+        _h(Hs), _ptr(Hs, BF, "Hs"), _ptr(Wt, BF, "Wt"), _ptr(labels, I32, "labels"), _ptr(loss, F32, "loss"),
+        _ptr(lse, F32, "lse"), _ptr(argmax, I32, "argmax"), _ptr(dHs, BF, "dHs"), _ptr(dWt, BF, "dWt"),
+        _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), M, d, V, _stream(stream)), "coda_lmhead_ce")
+
+
+def coda_unfused_workspace_bytes(M: int, d: int, N2: int) -> int:
+    return load_library().coda_unfused_workspace_bytes(M, d, N2)
+
+
+def coda_unfused_fwd(X, W1t, R, g, W2t, H, rstd, Nrm, z, out, ws, eps=1e-5, flags=CODA_EPI_SWIGLU, stream=None):
+    M, K1 = X.shape
+    d = W1t.shape[0]
+    N2 = W2t.shape[0]
+    _check(load_library().coda_unfused_fwd(
+        _h(X), _ptr(X, BF, "X"), _ptr(W1t, BF, "W1t"), _ptr(R, BF, "R"), _ptr(g, BF, "g"), _ptr(W2t, BF, "W2t"),
+        _ptr(H, BF, "H"), _ptr(rstd, F32, "rstd"), _ptr(Nrm, BF, "Nrm"), _ptr(z, BF, "z"), _ptr(out, BF, "out"),
+        _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), M, K1, d, N2, eps, flags, _stream(stream)),
+        "coda_unfused_fwd")
+
+
+def coda_unfused_bwd(dY, X, W1t, g, W2t, H, rstd, Nrm, z, dH, dX, dW1t, dW2t, dg, ws, stream=None):
+    M, K1 = X.shape
+    d = W1t.shape[0]
+    N2 = W2t.shape[0]
+    _check(load_library().coda_unfused_bwd(
+        _h(X), _ptr(dY, BF, "dY"), _ptr(X, BF, "X"), _ptr(W1t, BF, "W1t"), _ptr(g, BF, "g"), _ptr(W2t, BF, "W2t"),
+        _ptr(H, BF, "H"), _ptr(rstd, F32, "rstd"), _ptr(Nrm, BF, "Nrm"), _ptr(z, BF, "z"), _ptr(dH, BF, "dH"),
+        _ptr(dX, BF, "dX"), _ptr(dW1t, BF, "dW1t"), _ptr(dW2t, BF, "dW2t"), _ptr(dg, F32, "dg"),
+        _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), M, K1, d, N2, _stream(stream)),
+        "coda_unfused_bwd")

@@ -1,0 +1,91 @@
+// Host-side plumbing shared by the translation units of libcoda: tensor-map
+// construction, the launch context, and the internal launchers each .cu file
+// provides.  Not part of the public ABI (that is include/coda.h).
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace coda {
+
+struct LaunchCtx {
+  int num_sms;
+  int* status;          // device status word
+  uint64_t timeout_ns;  // bound on every in-kernel wait
+  cudaStream_t stream;
+};
+
+// 2-D bf16 tensor map with 128-byte swizzle.  The tensor is `outer` rows of
+// `inner` contiguous elements with a row pitch of `ld` elements; the box is
+// box_inner x box_outer elements (box_inner * 2 bytes must be <= 128).
+// Returns false if the driver rejects it.
+bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t ld,
+                    uint32_t box_inner, uint32_t box_outer);
+
+// ---- GEMM launchers (gemm_*.cu) --------------------------------------------
+// Operand majors: A K-major = [M][K], MN-major = [K][M]; B K-major = [N][K],
+// MN-major = [K][N].  All row pitches equal the extents (dense tensors).
+
+// C = bf16(row_scale[m] * col_scale[n] * sum_k A B); scales may be null.
+cudaError_t gemm_store(const LaunchCtx& c, const __nv_bfloat16* A, bool a_mn, const __nv_bfloat16* B, bool b_mn,
+                       __nv_bfloat16* C, int M, int N, int K, const float* row_scale,
+                       const __nv_bfloat16* col_scale);
+
+// C (fp32) = A B  or  C += A B.
+cudaError_t gemm_store_f32(const LaunchCtx& c, const __nv_bfloat16* A, bool a_mn, const __nv_bfloat16* B, bool b_mn,
+                           float* C, int M, int N, int K, bool accumulate);
+
+// h = bf16(X W1 + R); psum[m, j] = sum of h^2 over column tile j.
+cudaError_t gemm_res_prms(const LaunchCtx& c, const __nv_bfloat16* X, const __nv_bfloat16* W1t,
+                          const __nv_bfloat16* R, __nv_bfloat16* H, float* psum, int M, int K1, int d, int T);
+
+// z = rstd * (H W2g); out = silu(z_gate) * z_up (swiglu) or z (plain).
+cudaError_t gemm_rowscale_swiglu(const LaunchCtx& c, const __nv_bfloat16* H, const __nv_bfloat16* W2gt,
+                                 const float* rstd, __nv_bfloat16* out, __nv_bfloat16* zsave, int M, int d, int N2,
+                                 bool swiglu);
+
+// acc = dP W2^T; dH = g*acc - c*h; dgpart[4*tm+q, n] = sum_rows acc*h.
+cudaError_t gemm_dgrad_rms(const LaunchCtx& c, const __nv_bfloat16* dP, const __nv_bfloat16* W2t,
+                           const __nv_bfloat16* H, const __nv_bfloat16* g, const float* cvec, __nv_bfloat16* dH,
+                           float* dgpart, int M, int N2, int d);
+
+// per (row, vocab tile) max / sum-exp / argmax, label logit.
+cudaError_t gemm_ce_stats(const LaunchCtx& c, const __nv_bfloat16* H, const __nv_bfloat16* Wt, const int32_t* labels,
+                          float* pmax, float* psum, int32_t* parg, float* zy, int M, int d, int V, int T);
+
+// dL chunk = (softmax - onehot) / M for vocabulary rows [v0, v0 + Vc).
+cudaError_t gemm_ce_grad(const LaunchCtx& c, const __nv_bfloat16* H, const __nv_bfloat16* Wt_chunk,
+                         const int32_t* labels, const float* lse, __nv_bfloat16* dL, int M, int d, int Vc, int v0,
+                         float inv_M);
+
+int ce_tile_cols();    // vocabulary columns per CE statistics tile
+int prms_tile_cols();  // columns per partial-RMS tile of GEMM1
+
+// ---- memory-bound kernels (mem_kernels.cu) ---------------------------------
+cudaError_t launch_fold(const LaunchCtx& c, const __nv_bfloat16* W2t, const __nv_bfloat16* g, __nv_bfloat16* W2gt,
+                        int64_t N2, int64_t d);
+cudaError_t launch_rstd_combine(const LaunchCtx& c, const float* psum, int64_t M, int64_t T, int64_t d, float eps,
+                                float* rstd);
+cudaError_t launch_swiglu_bwd(const LaunchCtx& c, const __nv_bfloat16* dY, const __nv_bfloat16* z,
+                              const float* rstd, __nv_bfloat16* dP, float* cvec, int64_t M, int64_t F, int64_t d);
+cudaError_t launch_col_combine(const LaunchCtx& c, const float* part, int64_t rows, int64_t d, float* out);
+cudaError_t launch_ce_combine(const LaunchCtx& c, const float* pmax, const float* psum, const int32_t* parg,
+                              const float* zy, const int32_t* labels, int64_t M, int64_t T, int64_t V, float* lse,
+                              int32_t* argmax, float* row_loss);
+cudaError_t launch_mean(const LaunchCtx& c, const float* v, int64_t n, float* out);
+cudaError_t launch_f32_to_bf16(const LaunchCtx& c, const float* in, __nv_bfloat16* out, int64_t n);
+// unfused ablation kernels
+cudaError_t launch_add_rmsnorm(const LaunchCtx& c, const __nv_bfloat16* A, const __nv_bfloat16* R,
+                               const __nv_bfloat16* g, __nv_bfloat16* H, float* rstd, __nv_bfloat16* Nrm, int64_t M,
+                               int64_t d, float eps);
+cudaError_t launch_swiglu(const LaunchCtx& c, const __nv_bfloat16* z, __nv_bfloat16* out, int64_t M, int64_t F);
+cudaError_t launch_swiglu_bwd_plain(const LaunchCtx& c, const __nv_bfloat16* dY, const __nv_bfloat16* z,
+                                    __nv_bfloat16* dZ, int64_t M, int64_t F);
+cudaError_t launch_rmsnorm_bwd(const LaunchCtx& c, const __nv_bfloat16* dN, const __nv_bfloat16* H,
+                               const float* rstd, const __nv_bfloat16* g, __nv_bfloat16* dH, int64_t M, int64_t d);
+cudaError_t launch_rmsnorm_bwd_dg(const LaunchCtx& c, const __nv_bfloat16* dN, const __nv_bfloat16* H,
+                                  const float* rstd, float* dgpart, int64_t M, int64_t d, int64_t rows_per_part);
+
+}  // namespace coda

@@ -1,0 +1,24 @@
+// Backward GEMM instantiation: the second GEMM's data gradient with the
+// RMSNorm backward (dh = g*acc - c*h, dg partial sums) in its epilogue.
+#include "gemm_launch.cuh"
+
+namespace coda {
+
+namespace {
+constexpr int kBN = 256;
+constexpr int kStages = 4;
+}  // namespace
+
+cudaError_t gemm_dgrad_rms(const LaunchCtx& c, const __nv_bfloat16* dP, const __nv_bfloat16* W2t,
+                           const __nv_bfloat16* H, const __nv_bfloat16* g, const float* cvec, __nv_bfloat16* dH,
+                           float* dgpart, int M, int N2, int d) {
+  // acc[m, k] = sum_n dP[m, n] W2t[n, k]: A = dP K-major (K = N2), B = W2t
+  // stored [K][N] (MN-major).
+  CUtensorMap ta, tb;
+  if (!make_operand_maps(&ta, &tb, dP, false, W2t, true, M, d, N2, kBN)) return cudaErrorInvalidValue;
+  EpiDgradRms::Params ep{H, d, g, cvec, dH, d, dgpart};
+  return launch_gemm_kernel<kBN, kStages, false, true, false, EpiDgradRms>(c, ta, tb, tb, M, d, N2,
+                                                                            (d + kBN - 1) / kBN, ep);
+}
+
+}  // namespace coda

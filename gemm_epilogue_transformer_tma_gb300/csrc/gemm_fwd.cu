@@ -1,0 +1,67 @@
+// Forward GEMM instantiations: GEMM1 with the residual + partial-RMS epilogue,
+// GEMM2 with the deferred row scale + SwiGLU epilogue, and the plain GEMM.
+#include "gemm_launch.cuh"
+
+namespace coda {
+
+namespace {
+constexpr int kBN = 256;
+constexpr int kStages = 4;
+}  // namespace
+
+int prms_tile_cols() { return kBN; }
+
+cudaError_t gemm_res_prms(const LaunchCtx& c, const __nv_bfloat16* X, const __nv_bfloat16* W1t,
+                          const __nv_bfloat16* R, __nv_bfloat16* H, float* psum, int M, int K1, int d, int T) {
+  CUtensorMap ta, tb;
+  if (!make_operand_maps(&ta, &tb, X, false, W1t, false, M, d, K1, kBN)) return cudaErrorInvalidValue;
+  EpiResPrms::Params ep{R, d, H, d, psum, T};
+  return launch_gemm_kernel<kBN, kStages, false, false, false, EpiResPrms>(c, ta, tb, tb, M, d, K1,
+                                                                            (d + kBN - 1) / kBN, ep);
+}
+
+cudaError_t gemm_rowscale_swiglu(const LaunchCtx& c, const __nv_bfloat16* H, const __nv_bfloat16* W2gt,
+                                 const float* rstd, __nv_bfloat16* out, __nv_bfloat16* zsave, int M, int d, int N2,
+                                 bool swiglu) {
+  CUtensorMap ta, tb, tb2;
+  if (!swiglu) {
+    if (!make_operand_maps(&ta, &tb, H, false, W2gt, false, M, N2, d, kBN)) return cudaErrorInvalidValue;
+    EpiStore::Params ep{out, N2, rstd, nullptr};
+    return launch_gemm_kernel<kBN, kStages, false, false, false, EpiStore>(c, ta, tb, tb, M, N2, d,
+                                                                            (N2 + kBN - 1) / kBN, ep);
+  }
+  const int F = N2 / 2;
+  if (!make_tmap_bf16(&ta, H, d, M, d, 64, BM)) return cudaErrorInvalidValue;
+  // gate rows [0, F) and up rows [F, 2F) of W2gt as two separate tensors so
+  // each half is zero-filled past its own end
+  if (!make_tmap_bf16(&tb, W2gt, d, F, d, 64, kBN / 2)) return cudaErrorInvalidValue;
+  if (!make_tmap_bf16(&tb2, W2gt + static_cast<int64_t>(F) * d, d, F, d, 64, kBN / 2)) return cudaErrorInvalidValue;
+  EpiRowscaleSwiglu::Params ep{rstd, out, F, zsave, N2, F};
+  return launch_gemm_kernel<kBN, kStages, false, false, true, EpiRowscaleSwiglu>(c, ta, tb, tb2, M, F, d,
+                                                                                 (F + kBN / 2 - 1) / (kBN / 2), ep);
+}
+
+cudaError_t gemm_store(const LaunchCtx& c, const __nv_bfloat16* A, bool a_mn, const __nv_bfloat16* B, bool b_mn,
+                       __nv_bfloat16* C, int M, int N, int K, const float* row_scale,
+                       const __nv_bfloat16* col_scale) {
+  CUtensorMap ta, tb;
+  if (!make_operand_maps(&ta, &tb, A, a_mn, B, b_mn, M, N, K, kBN)) return cudaErrorInvalidValue;
+  EpiStore::Params ep{C, N, row_scale, col_scale};
+  const int tn = (N + kBN - 1) / kBN;
+  if (!a_mn && !b_mn) return launch_gemm_kernel<kBN, kStages, false, false, false, EpiStore>(c, ta, tb, tb, M, N, K, tn, ep);
+  if (!a_mn && b_mn) return launch_gemm_kernel<kBN, kStages, false, true, false, EpiStore>(c, ta, tb, tb, M, N, K, tn, ep);
+  if (a_mn && b_mn) return launch_gemm_kernel<kBN, kStages, true, true, false, EpiStore>(c, ta, tb, tb, M, N, K, tn, ep);
+  return cudaErrorNotSupported;  // MN-major A with K-major B is not used on this path
+}
+
+cudaError_t gemm_store_f32(const LaunchCtx& c, const __nv_bfloat16* A, bool a_mn, const __nv_bfloat16* B, bool b_mn,
+                           float* C, int M, int N, int K, bool accumulate) {
+  if (a_mn || !b_mn) return cudaErrorNotSupported;  // only [M][K] x [K][N] is used
+  CUtensorMap ta, tb;
+  if (!make_operand_maps(&ta, &tb, A, a_mn, B, b_mn, M, N, K, kBN)) return cudaErrorInvalidValue;
+  EpiStoreF32::Params ep{C, N, accumulate ? 1 : 0};
+  return launch_gemm_kernel<kBN, kStages, false, true, false, EpiStoreF32>(c, ta, tb, tb, M, N, K,
+                                                                            (N + kBN - 1) / kBN, ep);
+}
+
+}  // namespace coda

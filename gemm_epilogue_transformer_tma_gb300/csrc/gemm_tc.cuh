@@ -1,0 +1,621 @@
+// Persistent, warp-specialised bf16 GEMM for sm_103a with a programmable
+// epilogue.
+//
+//   C[m, n] = sum_k A[m, k] * B[k, n]          (fp32 accumulate in TMEM)
+//
+// The mainloop is fixed; what happens to the accumulator before it leaves
+// the chip is a template policy ("epilogue program").  This is the split the
+// CODA write-up describes (section 尾声: a GEMM kernel = mainloop + epilogue,
+// and the epilogue runs while the result is still on chip; section 五种积木:
+// the epilogue exposes elementwise, vector load/store, tile load/store,
+// block-reduction and stateful primitives).
+//
+// CTA = 6 warps:
+//   warp 0       TMA producer: fills a STAGES-deep shared-memory ring with A
+//                and B tiles (128-byte swizzle), completion on mbarriers.
+//   warp 1       TMEM allocator and MMA issuer: one elected thread issues
+//                tcgen05.mma (M=128, N=BN, K=16) into one of two TMEM
+//                accumulator buffers and commits to mbarriers.
+//   warps 2..5   epilogue: tcgen05.ld the accumulator (one row per thread),
+//                run the epilogue program, store to HBM, release the buffer.
+// Two TMEM buffers let the epilogue of tile i overlap the mainloop of i+1.
+//
+// Operand layouts (row-major storage, element = bf16):
+//   A K-major : A stored [M][K]          A MN-major : A stored [K][M]
+//   B K-major : B stored [N][K]          B MN-major : B stored [K][N]
+// B_DUAL (K-major only): the B tile is two half-height boxes from two tensor
+// maps (used for the gate / up halves of a SwiGLU projection).
+//
+// Every mbarrier wait is bounded (wall-clock limit); on expiry the kernel
+// records an error bit in the device status word, tells the other roles to
+// stop, waits (bounded) for its own copies and MMAs in flight, frees TMEM and
+// returns.
+#pragma once
+
+#include "ptx.cuh"
+
+namespace coda {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int UMMA_K = 16;
+constexpr int GEMM_THREADS = 192;
+constexpr int EPI_THREADS = 128;
+
+struct GemmShape {
+  int M, N, K;        // logical problem (N = output columns the epilogue sees)
+  int tiles_m, tiles_n;
+  int num_kb;
+  int group_m;        // tile raster: groups of group_m M-tiles sweep all N-tiles
+};
+
+struct KernelCtl {
+  int* status;        // device status word (atomicOr of DEV_ERR_* bits)
+  uint64_t timeout_ns;
+};
+
+struct EpiCtx {
+  int M, N;
+  int tm, tn;
+  int row;            // row inside the tile, 0..127 (= TMEM lane)
+  int m;              // global row
+  int quad;           // TMEM lane quadrant of this warp, 0..3
+  int lane;
+  uint32_t taddr;     // TMEM address of (first lane of quadrant, column 0 of this accumulator)
+};
+
+template <int BN, int STAGES>
+struct GemmSmem {
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
+  static constexpr int BAR_BYTES = 256;
+  static constexpr int TOTAL = RING_BYTES + BAR_BYTES + 1024;  // + alignment slack
+  static constexpr int TMEM_COLS = 2 * BN;                      // double-buffered accumulator
+  static_assert(TMEM_COLS <= 512, "TMEM has 512 columns");
+  static_assert((2 * STAGES + 5) * 8 + 8 <= BAR_BYTES, "barrier area too small");
+};
+
+__device__ __forceinline__ void tile_coords(int t, const GemmShape& s, int& tm, int& tn) {
+  const int group_tiles = s.group_m * s.tiles_n;
+  const int group = t / group_tiles;
+  const int first_m = group * s.group_m;
+  const int gm = min(s.tiles_m - first_m, s.group_m);
+  const int r = t - group * group_tiles;
+  tm = first_m + r % gm;
+  tn = r / gm;
+}
+
+__device__ __forceinline__ void raise_error(const KernelCtl& ctl, volatile int* abort_flag, int bit) {
+  atomicOr(ctl.status, bit);
+  *abort_flag = 1;
+}
+
+template <int BN, int STAGES, bool A_MN, bool B_MN, bool B_DUAL, class Epi>
+__global__ void __launch_bounds__(GEMM_THREADS, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmB2, const GemmShape sh, const KernelCtl ctl,
+                   const typename Epi::Params ep) {
+  using L = GemmSmem<BN, STAGES>;
+  static_assert(!(B_DUAL && B_MN), "dual-box B is K-major only");
+  static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
+  constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, A_MN, B_MN);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::RING_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], EPI_THREADS);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    if (B_DUAL) tma_prefetch_desc(&tmB2);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, L::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int num_tiles = sh.tiles_m * sh.tiles_n;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      long issued = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        int tm, tn;
+        tile_coords(t, sh, tm, tn);
+        for (int kb = 0; kb < sh.num_kb; ++kb) {
+          if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, ctl.timeout_ns)) {
+            if (!*abort_flag) raise_error(ctl, abort_flag, DEV_ERR_TIMEOUT_PRODUCER);
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + stage * L::STAGE_BYTES;
+          uint8_t* sb = sa + L::A_BYTES;
+          mbar_arrive_expect_tx(&full[stage], L::STAGE_BYTES);
+          if (!A_MN) {
+            tma_load_2d(sa, &tmA, &full[stage], kb * BK, tm * BM);
+          } else {
+#pragma unroll
+            for (int i = 0; i < BM / 64; ++i) tma_load_2d(sa + i * 8192, &tmA, &full[stage], tm * BM + i * 64, kb * BK);
+          }
+          if (B_DUAL) {
+            tma_load_2d(sb, &tmB, &full[stage], kb * BK, tn * (BN / 2));
+            tma_load_2d(sb + (BN / 2) * 128, &tmB2, &full[stage], kb * BK, tn * (BN / 2));
+          } else if (!B_MN) {
+            tma_load_2d(sb, &tmB, &full[stage], kb * BK, tn * BN);
+          } else {
+#pragma unroll
+            for (int i = 0; i < BN / 64; ++i) tma_load_2d(sb + i * 8192, &tmB, &full[stage], tn * BN + i * 64, kb * BK);
+          }
+          ++issued;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        // let every copy this thread started land before shared memory is released
+        const long n_wait = issued < STAGES ? issued : STAGES;
+        for (long j = 1; j <= n_wait; ++j) {
+          const long n = issued - j;
+          if (!mbar_wait_timeout(&full[n % STAGES], static_cast<uint32_t>((n / STAGES) & 1), ctl.timeout_ns))
+            atomicOr(ctl.status, DEV_ERR_TIMEOUT_DRAIN);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++it) {
+        const int acc = it & 1;
+        const uint32_t acc_phase = (it >> 1) & 1;
+        if (!mbar_wait_bounded(&tempty[acc], acc_phase ^ 1u, abort_flag, ctl.timeout_ns)) {
+          if (!*abort_flag) raise_error(ctl, abort_flag, DEV_ERR_TIMEOUT_MMA);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < sh.num_kb; ++kb) {
+          if (!mbar_wait_bounded(&full[stage], phase, abort_flag, ctl.timeout_ns)) {
+            if (!*abort_flag) raise_error(ctl, abort_flag, DEV_ERR_TIMEOUT_MMA);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * L::STAGE_BYTES);
+          const uint32_t sb = sa + L::A_BYTES;
+#pragma unroll
+          for (int k = 0; k < BK / UMMA_K; ++k) {
+            const uint64_t ad = A_MN ? sdesc_sw128(sa + k * 2048, 8192, 1024) : sdesc_sw128(sa + k * 32, 16, 1024);
+            const uint64_t bd = B_MN ? sdesc_sw128(sb + k * 2048, 8192, 1024) : sdesc_sw128(sb + k * 32, 16, 1024);
+            umma_bf16(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
+          }
+          umma_commit(&empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&tfull[acc]);
+      }
+      // wait for every MMA this thread issued before TMEM can be freed
+      umma_commit(drain);
+      if (!mbar_wait_timeout(drain, 0, ctl.timeout_ns)) atomicOr(ctl.status, DEV_ERR_TIMEOUT_DRAIN);
+    }
+  } else {
+    // ------------------------------------------------------------- epilogue
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    int it = 0;
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
+      int tm, tn;
+      tile_coords(t, sh, tm, tn);
+      const int acc = it & 1;
+      const uint32_t acc_phase = (it >> 1) & 1;
+      bool ok = mbar_wait_bounded(&tfull[acc], acc_phase, abort_flag, ctl.timeout_ns);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) {
+        if (lane == 0 && !*abort_flag) raise_error(ctl, abort_flag, DEV_ERR_TIMEOUT_EPILOGUE);
+        break;
+      }
+      tc_fence_after();
+      EpiCtx c;
+      c.M = sh.M;
+      c.N = sh.N;
+      c.tm = tm;
+      c.tn = tn;
+      c.row = row;
+      c.m = tm * BM + row;
+      c.quad = quad;
+      c.lane = lane;
+      c.taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      Epi::template run<BN>(ep, c);
+      tc_fence_before();
+      mbar_arrive(&tempty[acc]);
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, L::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// epilogue helpers: 32-column row segments, groups of 8 bf16 (16 bytes);
+// every extent on the boundary is a multiple of 8 so groups are all-or-none.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* p, int nvalid, float (&f)[32]) {
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    if (g * 8 < nvalid) {
+      const uint4 q = __ldg(reinterpret_cast<const uint4*>(p + g * 8));
+      unpack_bf16x8(q, &f[g * 8]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) f[g * 8 + i] = 0.f;
+    }
+  }
+}
+
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* p, int nvalid, const float (&f)[32]) {
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    if (g * 8 < nvalid) {
+      uint4 q;
+      q.x = pack_bf16x2(f[g * 8 + 0], f[g * 8 + 1]);
+      q.y = pack_bf16x2(f[g * 8 + 2], f[g * 8 + 3]);
+      q.z = pack_bf16x2(f[g * 8 + 4], f[g * 8 + 5]);
+      q.w = pack_bf16x2(f[g * 8 + 6], f[g * 8 + 7]);
+      *reinterpret_cast<uint4*>(p + g * 8) = q;
+    }
+  }
+}
+
+// lane l ends with sum over the 32 lanes of v[l]  (31 shuffles)
+__device__ __forceinline__ float warp_transpose_sum32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    const bool upper = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < off; ++i) {
+      const float send = upper ? v[i] : v[i + off];
+      const float keep = upper ? v[i + off] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+    }
+  }
+  return v[0];
+}
+
+// ---------------------------------------------------------------------------
+// Epilogue programs
+// ---------------------------------------------------------------------------
+
+// C = bf16(row_scale[m] * col_scale[n] * acc); both scales optional.
+struct EpiStore {
+  struct Params {
+    __nv_bfloat16* out;
+    int64_t ldo;
+    const float* row_scale;
+    const __nv_bfloat16* col_scale;
+  };
+  template <int BN>
+  static __device__ __forceinline__ void run(const Params& p, const EpiCtx& c) {
+    const bool row_ok = c.m < c.M;
+    const float rs = (p.row_scale != nullptr && row_ok) ? p.row_scale[c.m] : 1.f;
+#pragma unroll 1
+    for (int cc = 0; cc < BN; cc += 32) {
+      float v[32];
+      tmem_ld32(c.taddr + cc, v);
+      const int n0 = c.tn * BN + cc;
+      if (row_ok && n0 < c.N) {
+        if (p.col_scale != nullptr) {
+          float s[32];
+          load_bf16x32(p.col_scale + n0, c.N - n0, s);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] *= s[i];
+        }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] *= rs;
+        store_bf16x32(p.out + static_cast<int64_t>(c.m) * p.ldo + n0, c.N - n0, v);
+      }
+    }
+  }
+};
+
+// fp32 output, overwrite (beta = 0) or accumulate (beta = 1).
+struct EpiStoreF32 {
+  struct Params {
+    float* out;
+    int64_t ldo;
+    int beta;
+  };
+  template <int BN>
+  static __device__ __forceinline__ void run(const Params& p, const EpiCtx& c) {
+    const bool row_ok = c.m < c.M;
+#pragma unroll 1
+    for (int cc = 0; cc < BN; cc += 32) {
+      float v[32];
+      tmem_ld32(c.taddr + cc, v);
+      const int n0 = c.tn * BN + cc;
+      if (row_ok && n0 < c.N) {
+        float* o = p.out + static_cast<int64_t>(c.m) * p.ldo + n0;
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+          if (g * 4 < c.N - n0) {
+            float4 w = make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+            if (p.beta) {
+              const float4 old = *reinterpret_cast<const float4*>(o + 4 * g);
+              w.x += old.x;
+              w.y += old.y;
+              w.z += old.z;
+              w.w += old.w;
+            }
+            *reinterpret_cast<float4*>(o + 4 * g) = w;
+          }
+        }
+      }
+    }
+  }
+};
+
+// GEMM1 epilogue: h = bf16(acc + R); store h; psum[m, tn] = sum over the
+// tile's columns of h^2 (h as stored, i.e. after rounding to bf16).
+struct EpiResPrms {
+  struct Params {
+    const __nv_bfloat16* R;
+    int64_t ldr;
+    __nv_bfloat16* H;
+    int64_t ldh;
+    float* psum;
+    int T;  // psum columns
+  };
+  template <int BN>
+  static __device__ __forceinline__ void run(const Params& p, const EpiCtx& c) {
+    const bool row_ok = c.m < c.M;
+    float ss = 0.f;
+#pragma unroll 1
+    for (int cc = 0; cc < BN; cc += 32) {
+      float v[32];
+      tmem_ld32(c.taddr + cc, v);
+      const int n0 = c.tn * BN + cc;
+      if (row_ok && n0 < c.N) {
+        float r[32];
+        load_bf16x32(p.R + static_cast<int64_t>(c.m) * p.ldr + n0, c.N - n0, r);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float hb = bf16_round(v[i] + r[i]);
+          v[i] = hb;
+          ss = fmaf(hb, hb, ss);
+        }
+        store_bf16x32(p.H + static_cast<int64_t>(c.m) * p.ldh + n0, c.N - n0, v);
+      }
+    }
+    if (row_ok) p.psum[static_cast<int64_t>(c.m) * p.T + c.tn] = ss;
+  }
+};
+
+// GEMM2 epilogue: the accumulator holds [gate | up] halves of BN/2 columns
+// (two B boxes).  z = rstd[m] * acc; out = silu(z_gate) * z_up; optionally
+// save z (bf16) for the backward.  In plain mode (swiglu == 0, single box)
+// out = rstd[m] * acc.
+struct EpiRowscaleSwiglu {
+  struct Params {
+    const float* rstd;
+    __nv_bfloat16* out;
+    int64_t ldo;
+    __nv_bfloat16* zsave;  // may be null
+    int64_t ldz;
+    int F;                 // gate (= up) width; output columns
+  };
+  template <int BN>
+  static __device__ __forceinline__ void run(const Params& p, const EpiCtx& c) {
+    constexpr int HB = BN / 2;
+    const bool row_ok = c.m < c.M;
+    const float r = row_ok ? p.rstd[c.m] : 0.f;
+#pragma unroll 1
+    for (int cc = 0; cc < HB; cc += 32) {
+      float g[32], u[32];
+      tmem_ld32(c.taddr + cc, g);
+      tmem_ld32(c.taddr + HB + cc, u);
+      const int j0 = c.tn * HB + cc;
+      if (row_ok && j0 < p.F) {
+        const int nv = p.F - j0;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          g[i] *= r;
+          u[i] *= r;
+        }
+        if (p.zsave != nullptr) {
+          store_bf16x32(p.zsave + static_cast<int64_t>(c.m) * p.ldz + j0, nv, g);
+          store_bf16x32(p.zsave + static_cast<int64_t>(c.m) * p.ldz + p.F + j0, nv, u);
+        }
+        float o[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] = silu_f(g[i]) * u[i];
+        store_bf16x32(p.out + static_cast<int64_t>(c.m) * p.ldo + j0, nv, o);
+      }
+    }
+  }
+};
+
+// Data gradient of GEMM2 with the RMSNorm backward in its epilogue:
+//   acc = dP W2^T ; dh = g * acc - c[m] * h ; dgpart[4*tm + quad, n] =
+//   sum over the warp's 32 rows of acc * h  (block reduction across lanes).
+struct EpiDgradRms {
+  struct Params {
+    const __nv_bfloat16* H;
+    int64_t ldh;
+    const __nv_bfloat16* g;
+    const float* c;
+    __nv_bfloat16* dH;
+    int64_t lddh;
+    float* dgpart;  // [4 * tiles_m, N]
+  };
+  template <int BN>
+  static __device__ __forceinline__ void run(const Params& p, const EpiCtx& c) {
+    const bool row_ok = c.m < c.M;
+    const float cm = row_ok ? p.c[c.m] : 0.f;
+#pragma unroll 1
+    for (int cc = 0; cc < BN; cc += 32) {
+      float a[32];
+      tmem_ld32(c.taddr + cc, a);
+      const int n0 = c.tn * BN + cc;
+      if (n0 < c.N) {
+        float h[32], gv[32];
+        load_bf16x32(p.H + static_cast<int64_t>(c.m) * p.ldh + n0, row_ok ? c.N - n0 : 0, h);
+        load_bf16x32(p.g + n0, c.N - n0, gv);
+        if (row_ok) {
+          float dh[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) dh[i] = fmaf(gv[i], a[i], -cm * h[i]);
+          store_bf16x32(p.dH + static_cast<int64_t>(c.m) * p.lddh + n0, c.N - n0, dh);
+        }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) a[i] *= h[i];
+        const float s = warp_transpose_sum32(a, c.lane);
+        if (n0 + c.lane < c.N)
+          p.dgpart[static_cast<int64_t>(c.tm * 4 + c.quad) * c.N + n0 + c.lane] = s;
+      }
+    }
+  }
+};
+
+// LM-head forward epilogue: per (row, N-tile) running max and sum of
+// exp(L - max) (online rescaling across 32-column chunks), the tile argmax
+// (lowest column on ties), and the label logit when the label falls in the
+// tile.  Columns >= N (vocabulary tail) are masked out.
+struct EpiCeStats {
+  struct Params {
+    const int32_t* labels;
+    float* pmax;
+    float* psum;
+    int32_t* parg;
+    float* zy;
+    int T;
+    int* status;
+  };
+  template <int BN>
+  static __device__ __forceinline__ void run(const Params& p, const EpiCtx& c) {
+    const bool row_ok = c.m < c.M;
+    const int y = row_ok ? p.labels[c.m] : -1;
+    if (row_ok && c.tn == 0 && (y < 0 || y >= c.N)) atomicOr(p.status, DEV_ERR_LABEL_RANGE);
+    float mx = -INFINITY, se = 0.f, zy = 0.f;
+    int am = -1;
+    bool found = false;
+#pragma unroll 1
+    for (int cc = 0; cc < BN; cc += 32) {
+      float v[32];
+      tmem_ld32(c.taddr + cc, v);
+      const int n0 = c.tn * BN + cc;
+      if (row_ok && n0 < c.N) {
+        const int nv = c.N - n0;
+        float cmax = -INFINITY;
+        int carg = -1;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          if (i < nv && v[i] > cmax) {
+            cmax = v[i];
+            carg = n0 + i;
+          }
+        }
+        if (cmax > mx) {
+          se *= __expf(mx - cmax);
+          mx = cmax;
+          am = carg;
+        }
+        float s = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (i < nv) s += __expf(v[i] - mx);
+        se += s;
+        if (y >= n0 && y < n0 + 32) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (n0 + i == y) zy = v[i];
+          found = true;
+        }
+      }
+    }
+    if (row_ok) {
+      const int64_t o = static_cast<int64_t>(c.m) * p.T + c.tn;
+      p.pmax[o] = mx;
+      p.psum[o] = se;
+      p.parg[o] = am;
+      if (found) p.zy[c.m] = zy;
+    }
+  }
+};
+
+// LM-head backward epilogue: dL = (exp(L - lse[m]) - [n == y_m]) / M as bf16
+// into a vocabulary-chunk buffer (column n of the chunk = vocabulary v0 + n).
+struct EpiCeGrad {
+  struct Params {
+    const int32_t* labels;
+    const float* lse;
+    __nv_bfloat16* dL;
+    int64_t ldd;
+    float inv_M;
+    int v0;
+  };
+  template <int BN>
+  static __device__ __forceinline__ void run(const Params& p, const EpiCtx& c) {
+    const bool row_ok = c.m < c.M;
+    const float l = row_ok ? p.lse[c.m] : 0.f;
+    const int y = row_ok ? p.labels[c.m] - p.v0 : -1;
+#pragma unroll 1
+    for (int cc = 0; cc < BN; cc += 32) {
+      float v[32];
+      tmem_ld32(c.taddr + cc, v);
+      const int n0 = c.tn * BN + cc;
+      if (row_ok && n0 < c.N) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float e = __expf(v[i] - l) - ((n0 + i == y) ? 1.f : 0.f);
+          v[i] = e * p.inv_M;
+        }
+        store_bf16x32(p.dL + static_cast<int64_t>(c.m) * p.ldd + n0, c.N - n0, v);
+      }
+    }
+  }
+};
+
+}  // namespace coda

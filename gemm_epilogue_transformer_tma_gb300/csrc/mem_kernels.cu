@@ -1,0 +1,428 @@
+// Memory-bound kernels of the path: folding the RMSNorm weight into W2, the
+// light partial-RMS combine, the SwiGLU backward stream, column combines, the
+// blocked log-sum-exp combine, and the unfused ablation's standalone
+// add+RMSNorm / SwiGLU / SwiGLU-bwd / RMSNorm-bwd kernels.
+//
+// All accesses are 16-byte vectors (8 bf16 or 4 fp32) along the contiguous
+// dimension; every extent on the boundary is a multiple of 8 elements.
+#include <cfloat>
+
+#include "coda_internal.h"
+#include "ptx.cuh"
+
+namespace coda {
+
+namespace {
+
+__device__ __forceinline__ uint4 pack8(const float* f) {
+  uint4 q;
+  q.x = pack_bf16x2(f[0], f[1]);
+  q.y = pack_bf16x2(f[2], f[3]);
+  q.z = pack_bf16x2(f[4], f[5]);
+  q.w = pack_bf16x2(f[6], f[7]);
+  return q;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// block-wide sum for blockDim.x == 256; result valid in every thread
+__device__ __forceinline__ float block_sum_256(float v, float* red) {
+  v = warp_sum(v);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) red[w] = v;
+  __syncthreads();
+  float t = (l < 8) ? red[l] : 0.f;
+  return warp_sum(t);
+}
+
+int grid_for(const LaunchCtx& c, int64_t work_items, int threads) {
+  const int64_t need = (work_items + threads - 1) / threads;
+  const int64_t cap = static_cast<int64_t>(c.num_sms) * 8;
+  return static_cast<int>(need < cap ? (need > 0 ? need : 1) : cap);
+}
+
+// ---------------------------------------------------------------------------
+// W2gt[n, k] = bf16(W2t[n, k] * g[k])
+__global__ void fold_kernel(const uint4* __restrict__ W2t, const uint4* __restrict__ g8, uint4* __restrict__ out,
+                            int64_t n8, int64_t d8) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n8;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    float w[8], g[8], o[8];
+    unpack_bf16x8(W2t[i], w);
+    unpack_bf16x8(__ldg(&g8[i % d8]), g);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) o[j] = w[j] * g[j];
+    out[i] = pack8(o);
+  }
+}
+
+// rstd[m] = 1 / sqrt(sum_j psum[m, j] / d + eps): one warp per row
+__global__ void rstd_combine_kernel(const float* __restrict__ psum, int64_t M, int64_t T, float inv_d, float eps,
+                                    float* __restrict__ rstd) {
+  const int64_t row = blockIdx.x * static_cast<int64_t>(blockDim.x / 32) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= M) return;
+  float s = 0.f;
+  for (int64_t j = lane; j < T; j += 32) s += psum[row * T + j];
+  s = warp_sum(s);
+  if (lane == 0) rstd[row] = 1.0f / sqrtf(s * inv_d + eps);
+}
+
+// SwiGLU backward with the deferred row scale: one CTA (256 threads) per row.
+//   s = sigmoid(zg); dZg = dY*zu*s*(1 + zg*(1-s)); dZu = dY*zg*s
+//   dP = bf16(r * dZ); c[m] = r^2/d * sum(dZg*zg + dZu*zu)
+__global__ void __launch_bounds__(256) swiglu_bwd_kernel(const __nv_bfloat16* __restrict__ dY,
+                                                         const __nv_bfloat16* __restrict__ z,
+                                                         const float* __restrict__ rstd,
+                                                         __nv_bfloat16* __restrict__ dP, float* __restrict__ cvec,
+                                                         int64_t F, float inv_d) {
+  __shared__ float red[8];
+  const int64_t m = blockIdx.x;
+  const float r = rstd[m];
+  const uint4* dy8 = reinterpret_cast<const uint4*>(dY + m * F);
+  const uint4* zg8 = reinterpret_cast<const uint4*>(z + m * 2 * F);
+  const uint4* zu8 = reinterpret_cast<const uint4*>(z + m * 2 * F + F);
+  uint4* pg8 = reinterpret_cast<uint4*>(dP + m * 2 * F);
+  uint4* pu8 = reinterpret_cast<uint4*>(dP + m * 2 * F + F);
+  float dot = 0.f;
+  for (int64_t j = threadIdx.x; j < F / 8; j += blockDim.x) {
+    float dy[8], zg[8], zu[8], og[8], ou[8];
+    unpack_bf16x8(dy8[j], dy);
+    unpack_bf16x8(zg8[j], zg);
+    unpack_bf16x8(zu8[j], zu);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float s = 1.0f / (1.0f + __expf(-zg[i]));
+      const float dzu = dy[i] * zg[i] * s;
+      const float dzg = dy[i] * zu[i] * s * (1.0f + zg[i] * (1.0f - s));
+      dot = fmaf(dzg, zg[i], fmaf(dzu, zu[i], dot));
+      og[i] = r * dzg;
+      ou[i] = r * dzu;
+    }
+    pg8[j] = pack8(og);
+    pu8[j] = pack8(ou);
+  }
+  const float tot = block_sum_256(dot, red);
+  if (threadIdx.x == 0) cvec[m] = r * r * inv_d * tot;
+}
+
+// out[k] = sum_r part[r, k]; block = 32 columns x 8 row groups
+__global__ void col_combine_kernel(const float* __restrict__ part, int64_t rows, int64_t d, float* __restrict__ out) {
+  __shared__ float red[8][33];
+  const int64_t k = blockIdx.x * 32 + threadIdx.x;
+  float s = 0.f;
+  if (k < d)
+    for (int64_t r = threadIdx.y; r < rows; r += 8) s += part[r * d + k];
+  red[threadIdx.y][threadIdx.x] = s;
+  __syncthreads();
+  if (threadIdx.y == 0 && k < d) {
+    float t = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) t += red[i][threadIdx.x];
+    out[k] = t;
+  }
+}
+
+// Blocked log-sum-exp combine, one warp per row:
+//   m* = max_j mx_j ; lse = m* + log(sum_j se_j * exp(mx_j - m*))
+//   argmax = column of the largest tile max (lowest column on ties)
+//   row_loss = lse - z_y (0 and a status bit if the label is out of range)
+__global__ void ce_combine_kernel(const float* __restrict__ pmax, const float* __restrict__ psum,
+                                  const int32_t* __restrict__ parg, const float* __restrict__ zy,
+                                  const int32_t* __restrict__ labels, int64_t M, int64_t T, int64_t V,
+                                  float* __restrict__ lse, int32_t* __restrict__ argmax, float* __restrict__ row_loss,
+                                  int* status) {
+  const int64_t row = blockIdx.x * static_cast<int64_t>(blockDim.x / 32) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= M) return;
+  const float* mx = pmax + row * T;
+  const float* se = psum + row * T;
+  const int32_t* ag = parg + row * T;
+  float best = -INFINITY;
+  int bidx = 0x7fffffff;
+  for (int64_t j = lane; j < T; j += 32) {
+    const float v = mx[j];
+    const int a = ag[j];
+    if (v > best || (v == best && a < bidx)) {
+      best = v;
+      bidx = a;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+    const int oa = __shfl_xor_sync(0xffffffffu, bidx, o);
+    if (ov > best || (ov == best && oa < bidx)) {
+      best = ov;
+      bidx = oa;
+    }
+  }
+  float s = 0.f;
+  for (int64_t j = lane; j < T; j += 32) s += se[j] * __expf(mx[j] - best);
+  s = warp_sum(s);
+  if (lane == 0) {
+    const float l = best + logf(s);
+    lse[row] = l;
+    if (argmax != nullptr) argmax[row] = bidx;
+    const int y = labels[row];
+    if (y < 0 || y >= V) {
+      atomicOr(status, DEV_ERR_LABEL_RANGE);
+      row_loss[row] = 0.f;
+    } else {
+      row_loss[row] = l - zy[row];
+    }
+  }
+}
+
+// out = mean(v) with a fixed summation order (one CTA of 1024 threads)
+__global__ void __launch_bounds__(1024) mean_kernel(const float* __restrict__ v, int64_t n, float* __restrict__ out) {
+  __shared__ float red[32];
+  float s = 0.f;
+  for (int64_t i = threadIdx.x; i < n; i += blockDim.x) s += v[i];
+  s = warp_sum(s);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = s;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float t = warp_sum(red[threadIdx.x]);
+    if (threadIdx.x == 0) *out = t / static_cast<float>(n);
+  }
+}
+
+__global__ void f32_to_bf16_kernel(const float4* __restrict__ in, uint2* __restrict__ out, int64_t n4) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n4;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const float4 f = in[i];
+    out[i] = make_uint2(pack_bf16x2(f.x, f.y), pack_bf16x2(f.z, f.w));
+  }
+}
+
+// ---------------------------------------------------------------------------
+// unfused ablation kernels
+
+// h = bf16(A + R); rstd = 1/sqrt(mean h^2 + eps); Nrm = bf16(h * rstd * g)
+__global__ void __launch_bounds__(256) add_rmsnorm_kernel(const __nv_bfloat16* __restrict__ A,
+                                                          const __nv_bfloat16* __restrict__ R,
+                                                          const __nv_bfloat16* __restrict__ g,
+                                                          __nv_bfloat16* __restrict__ H, float* __restrict__ rstd,
+                                                          __nv_bfloat16* __restrict__ Nrm, int64_t d, float eps) {
+  __shared__ float red[8];
+  const int64_t m = blockIdx.x;
+  const uint4* a8 = reinterpret_cast<const uint4*>(A + m * d);
+  const uint4* r8 = reinterpret_cast<const uint4*>(R + m * d);
+  uint4* h8 = reinterpret_cast<uint4*>(H + m * d);
+  float ss = 0.f;
+  for (int64_t j = threadIdx.x; j < d / 8; j += blockDim.x) {
+    float a[8], r[8], h[8];
+    unpack_bf16x8(a8[j], a);
+    unpack_bf16x8(r8[j], r);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      h[i] = bf16_round(a[i] + r[i]);
+      ss = fmaf(h[i], h[i], ss);
+    }
+    h8[j] = pack8(h);
+  }
+  const float tot = block_sum_256(ss, red);
+  const float rs = 1.0f / sqrtf(tot / static_cast<float>(d) + eps);
+  if (threadIdx.x == 0) rstd[m] = rs;
+  const uint4* g8 = reinterpret_cast<const uint4*>(g);
+  uint4* n8 = reinterpret_cast<uint4*>(Nrm + m * d);
+  for (int64_t j = threadIdx.x; j < d / 8; j += blockDim.x) {
+    float h[8], gg[8], o[8];
+    unpack_bf16x8(h8[j], h);
+    unpack_bf16x8(__ldg(&g8[j]), gg);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] = h[i] * rs * gg[i];
+    n8[j] = pack8(o);
+  }
+}
+
+__global__ void swiglu_kernel(const __nv_bfloat16* __restrict__ z, __nv_bfloat16* __restrict__ out, int64_t M,
+                              int64_t F) {
+  const int64_t f8 = F / 8;
+  const int64_t n = M * f8;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t m = i / f8, j = i - m * f8;
+    float zg[8], zu[8], o[8];
+    unpack_bf16x8(reinterpret_cast<const uint4*>(z + m * 2 * F)[j], zg);
+    unpack_bf16x8(reinterpret_cast<const uint4*>(z + m * 2 * F + F)[j], zu);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) o[k] = silu_f(zg[k]) * zu[k];
+    reinterpret_cast<uint4*>(out + m * F)[j] = pack8(o);
+  }
+}
+
+__global__ void swiglu_bwd_plain_kernel(const __nv_bfloat16* __restrict__ dY, const __nv_bfloat16* __restrict__ z,
+                                        __nv_bfloat16* __restrict__ dZ, int64_t M, int64_t F) {
+  const int64_t f8 = F / 8;
+  const int64_t n = M * f8;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t m = i / f8, j = i - m * f8;
+    float dy[8], zg[8], zu[8], og[8], ou[8];
+    unpack_bf16x8(reinterpret_cast<const uint4*>(dY + m * F)[j], dy);
+    unpack_bf16x8(reinterpret_cast<const uint4*>(z + m * 2 * F)[j], zg);
+    unpack_bf16x8(reinterpret_cast<const uint4*>(z + m * 2 * F + F)[j], zu);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float s = 1.0f / (1.0f + __expf(-zg[k]));
+      og[k] = dy[k] * zu[k] * s * (1.0f + zg[k] * (1.0f - s));
+      ou[k] = dy[k] * zg[k] * s;
+    }
+    reinterpret_cast<uint4*>(dZ + m * 2 * F)[j] = pack8(og);
+    reinterpret_cast<uint4*>(dZ + m * 2 * F + F)[j] = pack8(ou);
+  }
+}
+
+// textbook RMSNorm backward for one row per CTA:
+//   dn = g * dN ; dh = r*dn - (r^3/d) * h * sum(dn*h)
+__global__ void __launch_bounds__(256) rmsnorm_bwd_kernel(const __nv_bfloat16* __restrict__ dN,
+                                                          const __nv_bfloat16* __restrict__ H,
+                                                          const float* __restrict__ rstd,
+                                                          const __nv_bfloat16* __restrict__ g,
+                                                          __nv_bfloat16* __restrict__ dH, int64_t d) {
+  __shared__ float red[8];
+  const int64_t m = blockIdx.x;
+  const float r = rstd[m];
+  const uint4* dn8 = reinterpret_cast<const uint4*>(dN + m * d);
+  const uint4* h8 = reinterpret_cast<const uint4*>(H + m * d);
+  const uint4* g8 = reinterpret_cast<const uint4*>(g);
+  float dot = 0.f;
+  for (int64_t j = threadIdx.x; j < d / 8; j += blockDim.x) {
+    float a[8], h[8], gg[8];
+    unpack_bf16x8(dn8[j], a);
+    unpack_bf16x8(h8[j], h);
+    unpack_bf16x8(__ldg(&g8[j]), gg);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) dot = fmaf(a[i] * gg[i], h[i], dot);
+  }
+  const float tot = block_sum_256(dot, red);
+  const float coef = r * r * r * tot / static_cast<float>(d);
+  uint4* o8 = reinterpret_cast<uint4*>(dH + m * d);
+  for (int64_t j = threadIdx.x; j < d / 8; j += blockDim.x) {
+    float a[8], h[8], gg[8], o[8];
+    unpack_bf16x8(dn8[j], a);
+    unpack_bf16x8(h8[j], h);
+    unpack_bf16x8(__ldg(&g8[j]), gg);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] = r * gg[i] * a[i] - coef * h[i];
+    o8[j] = pack8(o);
+  }
+}
+
+// dgpart[p, k] = sum over rows [p*rows_per_part, ...) of dN[m,k] * h[m,k] * r[m]
+__global__ void rmsnorm_bwd_dg_kernel(const __nv_bfloat16* __restrict__ dN, const __nv_bfloat16* __restrict__ H,
+                                      const float* __restrict__ rstd, float* __restrict__ dgpart, int64_t M, int64_t d,
+                                      int64_t rows_per_part) {
+  __shared__ float red[8][33];
+  const int64_t k = blockIdx.x * 32 + threadIdx.x;
+  const int64_t r0 = blockIdx.y * rows_per_part;
+  const int64_t r1 = min(M, r0 + rows_per_part);
+  float s = 0.f;
+  if (k < d)
+    for (int64_t m = r0 + threadIdx.y; m < r1; m += 8)
+      s += __bfloat162float(dN[m * d + k]) * __bfloat162float(H[m * d + k]) * rstd[m];
+  red[threadIdx.y][threadIdx.x] = s;
+  __syncthreads();
+  if (threadIdx.y == 0 && k < d) {
+    float t = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) t += red[i][threadIdx.x];
+    dgpart[blockIdx.y * d + k] = t;
+  }
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// launchers
+cudaError_t launch_fold(const LaunchCtx& c, const __nv_bfloat16* W2t, const __nv_bfloat16* g, __nv_bfloat16* W2gt,
+                        int64_t N2, int64_t d) {
+  const int64_t n8 = N2 * d / 8;
+  fold_kernel<<<grid_for(c, n8, 256), 256, 0, c.stream>>>(reinterpret_cast<const uint4*>(W2t),
+                                                          reinterpret_cast<const uint4*>(g),
+                                                          reinterpret_cast<uint4*>(W2gt), n8, d / 8);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rstd_combine(const LaunchCtx& c, const float* psum, int64_t M, int64_t T, int64_t d, float eps,
+                                float* rstd) {
+  const int rows_per_block = 8;
+  const int64_t grid = (M + rows_per_block - 1) / rows_per_block;
+  rstd_combine_kernel<<<static_cast<unsigned>(grid), 32 * rows_per_block, 0, c.stream>>>(
+      psum, M, T, 1.0f / static_cast<float>(d), eps, rstd);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_swiglu_bwd(const LaunchCtx& c, const __nv_bfloat16* dY, const __nv_bfloat16* z,
+                              const float* rstd, __nv_bfloat16* dP, float* cvec, int64_t M, int64_t F, int64_t d) {
+  swiglu_bwd_kernel<<<static_cast<unsigned>(M), 256, 0, c.stream>>>(dY, z, rstd, dP, cvec, F,
+                                                                    1.0f / static_cast<float>(d));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_col_combine(const LaunchCtx& c, const float* part, int64_t rows, int64_t d, float* out) {
+  col_combine_kernel<<<static_cast<unsigned>((d + 31) / 32), dim3(32, 8), 0, c.stream>>>(part, rows, d, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ce_combine(const LaunchCtx& c, const float* pmax, const float* psum, const int32_t* parg,
+                              const float* zy, const int32_t* labels, int64_t M, int64_t T, int64_t V, float* lse,
+                              int32_t* argmax, float* row_loss) {
+  const int rows_per_block = 8;
+  ce_combine_kernel<<<static_cast<unsigned>((M + rows_per_block - 1) / rows_per_block), 32 * rows_per_block, 0,
+                      c.stream>>>(pmax, psum, parg, zy, labels, M, T, V, lse, argmax, row_loss, c.status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mean(const LaunchCtx& c, const float* v, int64_t n, float* out) {
+  mean_kernel<<<1, 1024, 0, c.stream>>>(v, n, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_f32_to_bf16(const LaunchCtx& c, const float* in, __nv_bfloat16* out, int64_t n) {
+  const int64_t n4 = n / 4;
+  f32_to_bf16_kernel<<<grid_for(c, n4, 256), 256, 0, c.stream>>>(reinterpret_cast<const float4*>(in),
+                                                                 reinterpret_cast<uint2*>(out), n4);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_add_rmsnorm(const LaunchCtx& c, const __nv_bfloat16* A, const __nv_bfloat16* R,
+                               const __nv_bfloat16* g, __nv_bfloat16* H, float* rstd, __nv_bfloat16* Nrm, int64_t M,
+                               int64_t d, float eps) {
+  add_rmsnorm_kernel<<<static_cast<unsigned>(M), 256, 0, c.stream>>>(A, R, g, H, rstd, Nrm, d, eps);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_swiglu(const LaunchCtx& c, const __nv_bfloat16* z, __nv_bfloat16* out, int64_t M, int64_t F) {
+  swiglu_kernel<<<grid_for(c, M * F / 8, 256), 256, 0, c.stream>>>(z, out, M, F);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_swiglu_bwd_plain(const LaunchCtx& c, const __nv_bfloat16* dY, const __nv_bfloat16* z,
+                                    __nv_bfloat16* dZ, int64_t M, int64_t F) {
+  swiglu_bwd_plain_kernel<<<grid_for(c, M * F / 8, 256), 256, 0, c.stream>>>(dY, z, dZ, M, F);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rmsnorm_bwd(const LaunchCtx& c, const __nv_bfloat16* dN, const __nv_bfloat16* H,
+                               const float* rstd, const __nv_bfloat16* g, __nv_bfloat16* dH, int64_t M, int64_t d) {
+  rmsnorm_bwd_kernel<<<static_cast<unsigned>(M), 256, 0, c.stream>>>(dN, H, rstd, g, dH, d);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rmsnorm_bwd_dg(const LaunchCtx& c, const __nv_bfloat16* dN, const __nv_bfloat16* H,
+                                  const float* rstd, float* dgpart, int64_t M, int64_t d, int64_t rows_per_part) {
+  const dim3 grid(static_cast<unsigned>((d + 31) / 32),
+                  static_cast<unsigned>((M + rows_per_part - 1) / rows_per_part));
+  rmsnorm_bwd_dg_kernel<<<grid, dim3(32, 8), 0, c.stream>>>(dN, H, rstd, dgpart, M, d, rows_per_part);
+  return cudaGetLastError();
+}
+
+}  // namespace coda

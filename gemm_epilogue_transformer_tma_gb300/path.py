@@ -1,0 +1,110 @@
+"""One pass of the hot path through the C ABI: device buffers for a
+GEMM-Residual-PartialRMS-GEMM(+SwiGLU) block and the call sequence of its
+forward and backward, fused or unfused (ablation).
+
+Orchestration only: buffer allocation (torch, on the device) and the order of
+library calls.  No arithmetic happens here.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import (CODA_EPI_PLAIN, CODA_EPI_SWIGLU, coda_bwd_workspace_bytes, coda_dg_combine,
+               coda_dgpart_rows, coda_fold_rmsnorm_weight, coda_gemm_dgrad_rmsbwd, coda_gemm_res_prms,
+               coda_gemm_res_prms_bwd, coda_gemm_rowscale_swiglu, coda_gemm_rowscale_swiglu_bwd,
+               coda_gemm_wgrad_gscale, coda_prms_num_tiles, coda_rstd_combine, coda_swiglu_bwd,
+               coda_unfused_bwd, coda_unfused_fwd, coda_unfused_workspace_bytes)
+
+BF = torch.bfloat16
+F32 = torch.float32
+
+
+class BlockBuffers:
+    """All tensors of one block problem on one device.
+
+    inputs: X[M,K1], W1t[d,K1], R[M,d], g[d], W2t[N2,d], dY[M,F] (backward)
+    forward: W2gt, H, psum, rstd, z (saved), out
+    backward: dP, c, dgpart (stages), dH (= dR), dX, dW1t, dW2t, dg
+    """
+
+    def __init__(self, inputs: dict, swiglu: bool = True, backward: bool = True, eps: float = 1e-5,
+                 unfused: bool = False):
+        dev = inputs["X"].device
+        self.swiglu = swiglu
+        self.eps = eps
+        self.with_backward = backward
+        self.unfused = unfused
+        for k, v in inputs.items():
+            setattr(self, k, v.contiguous())
+        self.M, self.K1 = self.X.shape
+        self.d = self.W1t.shape[0]
+        self.N2 = self.W2t.shape[0]
+        self.F = self.N2 // 2 if swiglu else self.N2
+        M, d, N2 = self.M, self.d, self.N2
+        e = dict(device=dev)
+        self.W2gt = torch.empty(N2, d, dtype=BF, **e)
+        self.H = torch.empty(M, d, dtype=BF, **e)
+        self.psum = torch.empty(M, coda_prms_num_tiles(d), dtype=F32, **e)
+        self.rstd = torch.empty(M, dtype=F32, **e)
+        self.z = torch.empty(M, N2, dtype=BF, **e)
+        self.out = torch.empty(M, self.F, dtype=BF, **e) if swiglu else self.z
+        if unfused:
+            self.Nrm = torch.empty(M, d, dtype=BF, **e)
+            self.ws_unfused = torch.empty(max(1, coda_unfused_workspace_bytes(M, d, N2)), dtype=torch.uint8, **e)
+        if backward:
+            self.dP = torch.empty(M, N2, dtype=BF, **e)
+            self.c = torch.empty(M, dtype=F32, **e)
+            self.dgpart = torch.empty(max(1, coda_dgpart_rows(M)), d, dtype=F32, **e)
+            self.dH = torch.empty(M, d, dtype=BF, **e)
+            self.dX = torch.empty(M, self.K1, dtype=BF, **e)
+            self.dW1t = torch.empty(d, self.K1, dtype=BF, **e)
+            self.dW2t = torch.empty(N2, d, dtype=BF, **e)
+            self.dg = torch.empty(d, dtype=F32, **e)
+            self.ws = torch.empty(max(1, coda_bwd_workspace_bytes(M, d, N2)), dtype=torch.uint8, **e)
+
+    # -- fused path ----------------------------------------------------------
+    def forward(self, save_z: bool = True):
+        """fold g -> GEMM1 + residual + partial RMS -> rstd combine ->
+        GEMM2 + row scale + SwiGLU (z saved for the backward)."""
+        if self.unfused:
+            return self.forward_unfused()
+        coda_fold_rmsnorm_weight(self.W2t, self.g, self.W2gt)
+        coda_gemm_res_prms(self.X, self.W1t, self.R, self.H, self.psum)
+        coda_rstd_combine(self.psum, self.d, self.eps, self.rstd)
+        if self.swiglu:
+            coda_gemm_rowscale_swiglu(self.H, self.W2gt, self.rstd, self.out,
+                                      self.z if save_z else None, CODA_EPI_SWIGLU)
+        else:
+            coda_gemm_rowscale_swiglu(self.H, self.W2gt, self.rstd, self.z, None, CODA_EPI_PLAIN)
+
+    def backward_stages(self):
+        """The backward as separate stage calls (dP, c, dgpart stay visible)."""
+        coda_swiglu_bwd(self.dY, self.z, self.rstd, self.dP, self.c, self.d)
+        coda_gemm_dgrad_rmsbwd(self.dP, self.W2t, self.H, self.g, self.c, self.dH, self.dgpart)
+        coda_dg_combine(self.dgpart, self.dg)
+        coda_gemm_wgrad_gscale(self.H, self.dP, self.g, self.dW2t)
+        coda_gemm_res_prms_bwd(self.dH, self.X, self.W1t, self.dX, self.dW1t, self.dH)
+
+    def backward(self):
+        """SwiGLU bwd -> dgrad2 + RMSNorm bwd -> dg combine -> wgrad2 ->
+        dgrad1 -> wgrad1 (composite calls)."""
+        if self.unfused:
+            return self.backward_unfused()
+        coda_gemm_rowscale_swiglu_bwd(self.dY, self.z, self.rstd, self.H, self.W2t, self.g, self.dH,
+                                      self.dW2t, self.dg, self.ws)
+        coda_gemm_res_prms_bwd(self.dH, self.X, self.W1t, self.dX, self.dW1t, self.dH)
+
+    def step(self):
+        """One pass of the whole path: forward, then backward if requested."""
+        self.forward()
+        if self.with_backward:
+            self.backward()
+
+    # -- unfused ablation -----------------------------------------------------
+    def forward_unfused(self):
+        coda_unfused_fwd(self.X, self.W1t, self.R, self.g, self.W2t, self.H, self.rstd, self.Nrm, self.z,
+                         self.out, self.ws_unfused, self.eps, CODA_EPI_SWIGLU if self.swiglu else CODA_EPI_PLAIN)
+
+    def backward_unfused(self):
+        coda_unfused_bwd(self.dY, self.X, self.W1t, self.g, self.W2t, self.H, self.rstd, self.Nrm, self.z,
+                         self.dH, self.dX, self.dW1t, self.dW2t, self.dg, self.ws_unfused)

@@ -1,0 +1,262 @@
+/*
+ * coda.h -- C ABI of libcoda: a Transformer block's memory-bound operations
+ * run as GEMM epilogues on sm_103a (GB300).
+ *
+ * Method: "CODA: Rewriting Transformer Blocks as GEMM-Epilogue Programs"
+ * (arXiv 2605.19269), as described by the Synced / KuCoin write-up:
+ *   - section 尾声 / 尾聲: a GEMM is a mainloop plus an epilogue; the RMSNorm
+ *     row scale r commutes with the next GEMM, so it is deferred into that
+ *     GEMM's epilogue, while the first GEMM's epilogue only emits per-tile
+ *     partial RMS that a very light auxiliary kernel merges; the same holds
+ *     for SwiGLU, cross-entropy and the backward pass;
+ *   - section 五种积木 / 五種積木: the epilogue primitives (elementwise,
+ *     vector load/store, tile load/store, block reduction such as partial RMS
+ *     and block log-sum-exp, stateful running max / sum-exp).
+ *
+ * Conventions for every call below.
+ *   - Tensors are dense, row-major, with the leading dimension equal to the
+ *     last extent.  "bf16" tensors are IEEE bfloat16 (passed as void*).
+ *     Weights use nn.Linear layout: W1t[d][K1], W2t[N2][d], Wt[V][d].  For
+ *     SwiGLU, rows [0, F) of W2t are the gate projection and rows [F, 2F) the
+ *     up projection (N2 = 2F).
+ *   - Every pointer is caller-owned CUDA device memory on the handle's device
+ *     (except the handle itself and the out-parameters of coda_create and
+ *     coda_sync_status, which are host memory).  Device pointers must be
+ *     16-byte aligned.  The library never allocates after coda_create and
+ *     only reads or writes the buffers it is given; scratch space is passed
+ *     in as a caller-owned workspace whose size a *_workspace_bytes call
+ *     returns.
+ *   - Extents are int64_t.  Every contiguous extent (K1, d, N2, F, V) must be
+ *     a positive multiple of 8 and every extent below 2^31.  M == 0 is a
+ *     valid empty problem: nothing is launched and CODA_OK is returned.
+ *   - Every compute call is asynchronous on `stream` (a cudaStream_t, NULL =
+ *     legacy default stream).  The return value reports argument, alignment,
+ *     shape and launch errors synchronously; nothing is launched when it is
+ *     not CODA_OK.  Conditions detected on the device (a bounded wait that
+ *     expired, a label out of range) are recorded in the handle's device
+ *     status word and reported by coda_sync_status.
+ *   - A handle may be used from one host thread at a time.
+ */
+#ifndef CODA_H_
+#define CODA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum coda_status {
+  CODA_OK = 0,
+  CODA_ERR_INVALID_ARG = 1,        /* null pointer, non-positive or too large extent */
+  CODA_ERR_ALIGNMENT = 2,          /* pointer not 16-byte aligned or extent not a multiple of 8 */
+  CODA_ERR_UNSUPPORTED = 3,        /* shape or flag combination this library does not implement */
+  CODA_ERR_WORKSPACE_TOO_SMALL = 4,
+  CODA_ERR_CUDA = 5,               /* a CUDA runtime/driver call failed (launch, tensor map) */
+  CODA_ERR_TIMEOUT = 6,            /* device: an in-kernel wait hit its time limit */
+  CODA_ERR_LABEL_RANGE = 7         /* device: a label outside [0, V) */
+} coda_status_t;
+
+typedef struct coda_handle_s* coda_handle_t;
+
+/* flags of coda_gemm_rowscale_swiglu */
+#define CODA_EPI_SWIGLU 0u /* out = silu(z[:, :F]) * z[:, F:], N2 = 2F */
+#define CODA_EPI_PLAIN 1u  /* out = z (row scale only), N2 output columns */
+
+/* ------------------------------------------------------------------------ */
+/* handle, status                                                            */
+/* ------------------------------------------------------------------------ */
+
+/* Create a handle on CUDA device `device`: allocates the 4-byte device status
+ * word (the only allocation the library makes).  *out receives the handle. */
+coda_status_t coda_create(coda_handle_t* out, int device);
+
+/* Free the handle and its status word.  NULL is accepted. */
+coda_status_t coda_destroy(coda_handle_t h);
+
+/* Static English description of a status code. */
+const char* coda_status_string(coda_status_t s);
+
+/* Synchronise `stream`, read and clear the device status word.  Returns
+ * CODA_ERR_TIMEOUT or CODA_ERR_LABEL_RANGE if a kernel recorded that
+ * condition since the last call, else CODA_OK.  If device_bits is not NULL it
+ * receives the raw bit mask (bits 0-3: which wait timed out; bit 8: label
+ * range). */
+coda_status_t coda_sync_status(coda_handle_t h, void* stream, int32_t* device_bits);
+
+/* Wall-clock limit, in nanoseconds, of every wait inside the library's GEMM
+ * kernels (default 4e9).  On expiry the kernel records CODA_ERR_TIMEOUT, lets
+ * its in-flight copies and MMAs finish, frees its tensor memory and returns.
+ * 0 restores the default. */
+coda_status_t coda_set_wait_timeout_ns(coda_handle_t h, uint64_t ns);
+
+/* Columns of the partial-RMS buffer for hidden width d: ceil(d / BN1). */
+int64_t coda_prms_num_tiles(int64_t d);
+
+/* Rows of the dg partial buffer of coda_gemm_dgrad_rmsbwd: 4 * ceil(M/128). */
+int64_t coda_dgpart_rows(int64_t M);
+
+/* ------------------------------------------------------------------------ */
+/* the fixed mainloop with a plain epilogue                                  */
+/* ------------------------------------------------------------------------ */
+
+/* C[M][N] = bf16( row_scale[m] * col_scale[n] * sum_k A(m,k) B(k,n) ).
+ * The mainloop of the write-up's section 尾声, epilogue = scale + store.
+ * A is [M][K] (a_mn_major = 0) or stored transposed as [K][M] (a_mn_major = 1);
+ * B is [N][K] (b_mn_major = 0) or [K][N] (b_mn_major = 1).  Supported
+ * combinations: (0,0), (0,1), (1,1).  row_scale (fp32 [M]) and col_scale
+ * (bf16 [N]) may be NULL.  M, N, K multiples of 8. */
+coda_status_t coda_gemm(coda_handle_t h, const void* A, int a_mn_major, const void* B, int b_mn_major, void* C,
+                        int64_t M, int64_t N, int64_t K, const float* row_scale, const void* col_scale,
+                        void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* forward: GEMM-Residual-PartialRMS-GEMM (+SwiGLU)                           */
+/* ------------------------------------------------------------------------ */
+
+/* W2gt[n][k] = bf16(W2t[n][k] * g[k]) -- the RMSNorm weight g (bf16 [d]) folded
+ * into the second GEMM's B operand (section 尾声: r and g are per-row /
+ * per-column scales that commute with the contraction; section 五种积木:
+ * vector load of the RMSNorm weight).  W2t, W2gt: bf16 [N2][d]; may not
+ * alias. */
+coda_status_t coda_fold_rmsnorm_weight(coda_handle_t h, const void* W2t, const void* g, void* W2gt, int64_t N2,
+                                       int64_t d, void* stream);
+
+/* GEMM1 with the residual + partial-RMS epilogue (section 尾声):
+ *   H[m][n] = bf16( sum_k X[m][k] W1t[n][k] + R[m][n] )
+ *   psum[m][j] = sum over n in column tile j of H[m][n]^2   (fp32, H as stored)
+ * X bf16 [M][K1], W1t bf16 [d][K1], R bf16 [M][d], H bf16 [M][d],
+ * psum fp32 [M][coda_prms_num_tiles(d)].  H may not alias R. */
+coda_status_t coda_gemm_res_prms(coda_handle_t h, const void* X, const void* W1t, const void* R, void* H,
+                                 float* psum, int64_t M, int64_t K1, int64_t d, void* stream);
+
+/* The light auxiliary combine (section 尾声):
+ *   rstd[m] = 1 / sqrt( sum_j psum[m][j] / d + eps )
+ * psum fp32 [M][T], rstd fp32 [M]. */
+coda_status_t coda_rstd_combine(coda_handle_t h, const float* psum, int64_t M, int64_t T, int64_t d, float eps,
+                                float* rstd, void* stream);
+
+/* GEMM2 with the deferred row scale and SwiGLU epilogue (section 尾声, and the
+ * SwiGLU re-parameterisation it lists):
+ *   z[m][n] = rstd[m] * sum_k H[m][k] W2gt[n][k]
+ *   CODA_EPI_SWIGLU: out[m][j] = silu(z[m][j]) * z[m][F + j], out bf16 [M][F],
+ *                    N2 = 2F; if z_save is not NULL it receives z (bf16
+ *                    [M][N2], the tile store that saves activations for the
+ *                    backward).
+ *   CODA_EPI_PLAIN:  out[m][n] = z[m][n], out bf16 [M][N2]; z_save must be
+ *                    NULL.
+ * H bf16 [M][d], W2gt bf16 [N2][d] (from coda_fold_rmsnorm_weight), rstd fp32
+ * [M].  N2 (and F for SwiGLU) multiples of 8. */
+coda_status_t coda_gemm_rowscale_swiglu(coda_handle_t h, const void* H, const void* W2gt, const float* rstd,
+                                        void* out, void* z_save, int64_t M, int64_t d, int64_t N2, uint32_t flags,
+                                        void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* backward (section 尾声: the backward of a block-local epilogue is itself    */
+/* block-local)                                                              */
+/* ------------------------------------------------------------------------ */
+
+/* SwiGLU backward with the row scale folded in:
+ *   dZ = d(silu(zg) * zu) applied to dY;  dP = bf16(rstd[m] * dZ)
+ *   c[m] = rstd[m]^2 / d * sum_n dZ[m][n] z[m][n]
+ * dY bf16 [M][F], z bf16 [M][2F] (from the forward), rstd fp32 [M],
+ * dP bf16 [M][2F], c fp32 [M]; d is the hidden width. */
+coda_status_t coda_swiglu_bwd(coda_handle_t h, const void* dY, const void* z, const float* rstd, void* dP,
+                              float* c, int64_t M, int64_t F, int64_t d, void* stream);
+
+/* Data gradient of GEMM2 with the RMSNorm backward in its epilogue:
+ *   acc[m][k] = sum_n dP[m][n] W2t[n][k]
+ *   dH[m][k]  = bf16( g[k] * acc[m][k] - c[m] * H[m][k] )
+ *   dgpart[r][k] = sum over rows m of block r (32 rows) of acc[m][k] * H[m][k]
+ * dP bf16 [M][N2], W2t bf16 [N2][d] (unfolded), H bf16 [M][d], g bf16 [d],
+ * c fp32 [M], dH bf16 [M][d], dgpart fp32 [coda_dgpart_rows(M)][d]. */
+coda_status_t coda_gemm_dgrad_rmsbwd(coda_handle_t h, const void* dP, const void* W2t, const void* H,
+                                     const void* g, const float* c, void* dH, float* dgpart, int64_t M, int64_t N2,
+                                     int64_t d, void* stream);
+
+/* dg[k] = sum_r dgpart[r][k] (fixed order).  dgpart fp32 [rows][d], dg fp32 [d]. */
+coda_status_t coda_dg_combine(coda_handle_t h, const float* dgpart, int64_t rows, int64_t d, float* dg,
+                              void* stream);
+
+/* Weight gradient of GEMM2 with the folded g applied per column:
+ *   dW2t[n][k] = bf16( g[k] * sum_m dP[m][n] H[m][k] )
+ * H bf16 [M][d], dP bf16 [M][N2], g bf16 [d], dW2t bf16 [N2][d]. */
+coda_status_t coda_gemm_wgrad_gscale(coda_handle_t h, const void* H, const void* dP, const void* g, void* dW2t,
+                                     int64_t M, int64_t N2, int64_t d, void* stream);
+
+/* Workspace of coda_gemm_rowscale_swiglu_bwd: dP bf16 [M][N2], c fp32 [M],
+ * dgpart fp32 [coda_dgpart_rows(M)][d], each 256-byte aligned. */
+size_t coda_bwd_workspace_bytes(int64_t M, int64_t d, int64_t N2);
+
+/* Backward of GEMM2 + deferred RMSNorm + SwiGLU, chaining coda_swiglu_bwd,
+ * coda_gemm_dgrad_rmsbwd, coda_dg_combine and coda_gemm_wgrad_gscale:
+ * outputs dH (bf16 [M][d], = dR = dA of the residual stream), dW2t (bf16
+ * [N2][d]) and dg (fp32 [d]).  Inputs as the stage calls; SwiGLU only. */
+coda_status_t coda_gemm_rowscale_swiglu_bwd(coda_handle_t h, const void* dY, const void* z, const float* rstd,
+                                            const void* H, const void* W2t, const void* g, void* dH, void* dW2t,
+                                            float* dg, void* ws, size_t ws_bytes, int64_t M, int64_t d, int64_t N2,
+                                            void* stream);
+
+/* Backward of GEMM1 + residual: dX = dH W1 (bf16 [M][K1]), dW1t = dH^T X
+ * (bf16 [d][K1]).  dR: NULL, or == dH (aliased: nothing is written, since
+ * dR = dH), or a distinct bf16 [M][d] buffer that receives a copy of dH. */
+coda_status_t coda_gemm_res_prms_bwd(coda_handle_t h, const void* dH, const void* X, const void* W1t, void* dX,
+                                     void* dW1t, void* dR, int64_t M, int64_t K1, int64_t d, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* LM head: blocked log-sum-exp cross-entropy epilogue (section 五种积木:     */
+/* block reduction "block log-sum-exp", stateful max / sum-exp)              */
+/* ------------------------------------------------------------------------ */
+
+/* Workspace of coda_lmhead_ce (with_grads = 0: forward only). */
+size_t coda_lmhead_ce_workspace_bytes(int64_t M, int64_t d, int64_t V, int with_grads);
+
+/* Mean softmax cross-entropy of the logits L = Hs Wt^T against labels,
+ * without ever writing an [M][V] logits tensor:
+ *   per (row, 256-column vocabulary tile): max, sum exp(L - max), argmax,
+ *   label logit (GEMM epilogue); combine: lse[m] = log sum_v exp L[m][v];
+ *   loss = mean_m (lse[m] - L[m][y_m]); argmax[m] = first maximal column.
+ * If dHs is not NULL the gradients are produced too, vocabulary chunk by
+ * chunk: dL = (softmax - onehot)/M recomputed in a GEMM epilogue into a
+ * workspace chunk, dHs = dL Wt (fp32 accumulation across chunks), dWt =
+ * dL^T Hs.
+ * Hs bf16 [M][d], Wt bf16 [V][d], labels int32 [M] in [0, V) (a label outside
+ * sets CODA_ERR_LABEL_RANGE in the status word and its row contributes 0 to
+ * the sum), loss fp32 [1], lse fp32 [M], argmax int32 [M] or NULL,
+ * dHs bf16 [M][d] or NULL, dWt bf16 [V][d] (required iff dHs != NULL). */
+coda_status_t coda_lmhead_ce(coda_handle_t h, const void* Hs, const void* Wt, const int32_t* labels, float* loss,
+                             float* lse, int32_t* argmax, void* dHs, void* dWt, void* ws, size_t ws_bytes, int64_t M,
+                             int64_t d, int64_t V, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* unfused ablation: the same GEMM kernel with standalone memory-bound       */
+/* kernels in between (the "three separate operators" baseline of section    */
+/* 尾声)                                                                      */
+/* ------------------------------------------------------------------------ */
+
+/* Workspace of coda_unfused_fwd / coda_unfused_bwd. */
+size_t coda_unfused_workspace_bytes(int64_t M, int64_t d, int64_t N2);
+
+/* A = X W1 (GEMM) ; H = bf16(A + R), rstd, Nrm = bf16(H rstd g) (one kernel) ;
+ * z = Nrm W2 (GEMM, bf16 [M][N2]) ; out = silu(z_gate) z_up (kernel) or out = z
+ * when flags == CODA_EPI_PLAIN (then `out` may equal `z`).  Nrm bf16 [M][d] is
+ * kept for the backward. */
+coda_status_t coda_unfused_fwd(coda_handle_t h, const void* X, const void* W1t, const void* R, const void* g,
+                               const void* W2t, void* H, float* rstd, void* Nrm, void* z, void* out, void* ws,
+                               size_t ws_bytes, int64_t M, int64_t K1, int64_t d, int64_t N2, float eps,
+                               uint32_t flags, void* stream);
+
+/* dZ = SwiGLU'(dY) (kernel) ; dN = dZ W2^T (GEMM) ; dH = RMSNorm'(dN) (kernel),
+ * dg (kernel + combine) ; dW2t = dZ^T Nrm (GEMM) ; dX, dW1t (GEMMs).
+ * SwiGLU only. */
+coda_status_t coda_unfused_bwd(coda_handle_t h, const void* dY, const void* X, const void* W1t, const void* g,
+                               const void* W2t, const void* H, const float* rstd, const void* Nrm, const void* z,
+                               void* dH, void* dX, void* dW1t, void* dW2t, float* dg, void* ws, size_t ws_bytes,
+                               int64_t M, int64_t K1, int64_t d, int64_t N2, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CODA_H_ */

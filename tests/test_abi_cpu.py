@@ -1,0 +1,64 @@
+"""Host-only checks of the C ABI: the library loads, exports every entry
+point include/coda.h declares with the binding's signature table matching,
+and the pure host queries (tile counts, workspace sizes, status strings)
+answer without a GPU."""
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "coda.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from gemm_epilogue_transformer_tma_gb300 import build
+    build.build()
+    import gemm_epilogue_transformer_tma_gb300 as C
+    return C.load_library()
+
+
+def declared():
+    src = open(HEADER).read()
+    return set(re.findall(r"^\s*(?:coda_status_t|const char\*|int64_t|size_t)\s+(coda_\w+)\s*\(", src, re.M))
+
+
+def test_header_declares_the_named_entry_points():
+    names = declared()
+    for n in ("coda_gemm_res_prms", "coda_rstd_combine", "coda_gemm_rowscale_swiglu",
+              "coda_gemm_rowscale_swiglu_bwd", "coda_gemm_res_prms_bwd", "coda_lmhead_ce"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    import gemm_epilogue_transformer_tma_gb300 as C
+    names = declared()
+    assert names == set(C.SIGNATURES), (names ^ set(C.SIGNATURES))
+    out = subprocess.run(["nm", "-D", "--defined-only", C.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r" T (coda_\w+)", out))
+    assert names <= exported, names - exported
+    for n in names:
+        assert hasattr(lib, n)
+
+
+def test_host_queries(lib):
+    assert lib.coda_prms_num_tiles(4096) == 16
+    assert lib.coda_prms_num_tiles(328) == 2
+    assert lib.coda_dgpart_rows(300) == 12
+    assert lib.coda_bwd_workspace_bytes(0, 64, 128) == 0
+    M, d, N2 = 8192, 4096, 28672
+    assert lib.coda_bwd_workspace_bytes(M, d, N2) >= M * N2 * 2 + M * 4 + 4 * (M // 128) * d * 4
+    assert lib.coda_lmhead_ce_workspace_bytes(8192, 2048, 128256, 0) >= 3 * 8192 * 501 * 4
+    assert lib.coda_lmhead_ce_workspace_bytes(8192, 2048, 128256, 1) > lib.coda_lmhead_ce_workspace_bytes(
+        8192, 2048, 128256, 0)
+    assert lib.coda_status_string(0) == b"ok"
+    assert b"time limit" in lib.coda_status_string(6)
+
+
+def test_null_handle_is_rejected_without_a_gpu(lib):
+    # validation runs before any CUDA call
+    assert lib.coda_set_wait_timeout_ns(None, 1) == 1
+    assert lib.coda_gemm(None, None, 0, None, 0, None, 8, 8, 8, None, None, None) == 1
+    assert lib.coda_destroy(None) == 0
