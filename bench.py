@@ -1,0 +1,386 @@
+"""Benchmark: fused GEMM-RMSNorm-GEMM (+SwiGLU) forward + backward on GB300.
+
+One step = one pass of the block's hot path over one batch of synthetic
+input: fold g -> GEMM1 + residual + partial RMS -> rstd combine -> GEMM2 +
+row scale + SwiGLU -> SwiGLU backward -> dgrad2 + RMSNorm backward -> dg
+combine -> wgrad2 -> dgrad1 -> wgrad1, all through the C ABI.
+
+Default workload: the 7B-size block (M=8192 tokens, d=4096, ffn 14336),
+bf16 inputs/outputs, fp32 accumulation.  The metric counts 2*M*N*K per GEMM
+for the forward, data-gradient and weight-gradient GEMMs (3x the forward).
+
+Also reported on the same line: the unfused ablation (same GEMM kernel with
+standalone add+RMSNorm / SwiGLU / SwiGLU-bwd / RMSNorm-bwd kernels), the
+LM-head blocked-LSE cross-entropy forward+backward, the dominant kernel's
+roofline, an end-to-end number through the public API with host buffers,
+and the fp64 oracle timed on the host cores (cpu_baseline).
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--config 7b|70b]
+       [--impl reference]
+Under torchrun (N > 1) every rank runs an independent replica (the method is
+single-GPU; there is no exchange step), rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from coda_inputs import B7, B70, LMHEAD, BlockShape, block_inputs, ce_inputs  # noqa: E402
+
+METRIC = "fused GEMM-RMSNorm-GEMM fwd+bwd TFLOP/s and % of GB300 bf16 dense peak"
+UNIT = "TFLOP/s"
+CONFIGS = {"7b": B7, "70b": B70}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return {"hbm_gbs": j["hbm_gbs"], "bf16_tflops": j["bf16_tflops"],
+                "bf16_tflops_sustained": j.get("bf16_tflops_sustained", j["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.path is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        busy = [s for s in sm if s > 0.5 * (max(mx) if mx else 1)] or sm
+        return {"sm_mhz": statistics.median(busy) if busy else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+class FusedStep:
+    """The fused path's calls with CUDA events between stages."""
+    STAGES = ["fold", "gemm1_res_prms", "rstd_combine", "gemm2_rowscale_swiglu", "swiglu_bwd",
+              "dgrad2_rmsbwd", "dg_combine", "wgrad2_gscale", "dgrad1", "wgrad1"]
+
+    def __init__(self, C, b):
+        self.C, self.b = C, b
+        s = b
+        self.flops = {
+            "gemm1_res_prms": 2.0 * s.M * s.d * s.K1,
+            "gemm2_rowscale_swiglu": 2.0 * s.M * s.N2 * s.d,
+            "dgrad2_rmsbwd": 2.0 * s.M * s.N2 * s.d,
+            "wgrad2_gscale": 2.0 * s.M * s.N2 * s.d,
+            "dgrad1": 2.0 * s.M * s.d * s.K1,
+            "wgrad1": 2.0 * s.M * s.d * s.K1,
+        }
+
+    def calls(self):
+        C, b = self.C, self.b
+        return [
+            lambda: C.coda_fold_rmsnorm_weight(b.W2t, b.g, b.W2gt),
+            lambda: C.coda_gemm_res_prms(b.X, b.W1t, b.R, b.H, b.psum),
+            lambda: C.coda_rstd_combine(b.psum, b.d, b.eps, b.rstd),
+            lambda: C.coda_gemm_rowscale_swiglu(b.H, b.W2gt, b.rstd, b.out, b.z, C.CODA_EPI_SWIGLU),
+            lambda: C.coda_swiglu_bwd(b.dY, b.z, b.rstd, b.dP, b.c, b.d),
+            lambda: C.coda_gemm_dgrad_rmsbwd(b.dP, b.W2t, b.H, b.g, b.c, b.dH, b.dgpart),
+            lambda: C.coda_dg_combine(b.dgpart, b.dg),
+            lambda: C.coda_gemm_wgrad_gscale(b.H, b.dP, b.g, b.dW2t),
+            lambda: C.coda_gemm(b.dH, False, b.W1t, True, b.dX, b.M, b.K1, b.d),
+            lambda: C.coda_gemm(b.dH, True, b.X, True, b.dW1t, b.d, b.K1, b.M),
+        ]
+
+
+def time_steps(calls, steps, warmup, stage_events=True):
+    """Run warmup + timed steps; return (total_ms, per-stage ms lists)."""
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        for f in calls:
+            f()
+    torch.cuda.synchronize()
+    n = len(calls)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n + 1)] for _ in range(steps)] if stage_events else None
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for s in range(steps):
+        for i, f in enumerate(calls):
+            if stage_events:
+                evs[s][i].record(stream)
+            f()
+        if stage_events:
+            evs[s][n].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    total = t0.elapsed_time(t1)
+    per = None
+    if stage_events:
+        per = [[evs[s][i].elapsed_time(evs[s][i + 1]) for s in range(steps)] for i in range(n)]
+    return total, per
+
+
+def cpu_oracle_baseline(shape: BlockShape, target_s: float = 12.0, max_rows: int = 1024):
+    """fp64 oracle fwd+bwd of the block on a row sample of the workload (full
+    weights), timed on the host cores.  Returns a cpu_baseline dict."""
+    import numpy as np
+
+    import oracle as O
+    from coda_inputs import to_f64
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    full = block_inputs(BlockShape(shape.name, max_rows, shape.K1, shape.d, shape.N2), 0, "cpu")
+    W = {k: to_f64(full[k]) for k in ("W1t", "g", "W2t")}
+    rows = 32
+    while True:
+        A = {k: to_f64(full[k][:rows]) for k in ("X", "R", "dY")}
+        t = time.perf_counter()
+        O.block_backward(A["X"], W["W1t"], A["R"], W["g"], W["W2t"], A["dY"], shape.eps, True)
+        dt = time.perf_counter() - t
+        if dt >= target_s or rows >= max_rows:
+            break
+        rows = min(max_rows, max(rows * 2, int(rows * target_s / max(dt, 1e-3))))
+        rows = max(8, (rows // 8) * 8)
+    flops = 3.0 * (2.0 * rows * shape.d * shape.K1 + 2.0 * rows * shape.N2 * shape.d)
+    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"fp64 numpy oracle block fwd+bwd on {rows} of {shape.M} token rows of the "
+                      f"{shape.name} workload (full weights), {dt:.1f} s wall", "seconds": dt,
+            "rows": rows}
+
+
+def run_reference(args, shape):
+    """The oracle as the reference arm: timed on the host cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    per_step = []
+    res = None
+    for i in range(args.warmup + args.steps):
+        res = cpu_oracle_baseline(shape, target_s=max(2.0, 60.0 / (args.warmup + args.steps + 1)), max_rows=256)
+        if i >= args.warmup:
+            per_step.append(res)
+    v = statistics.median([r["value"] for r in per_step])
+    secs = statistics.median([r["seconds"] for r in per_step])
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": shape.name, "M": shape.M, "K1": shape.K1, "d": shape.d, "ffn": shape.N2 // 2,
+                       "sample_rows": res["rows"]},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": res["cores"], "kind": "oracle",
+                             "sample": res["sample"]},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def bench_lmhead(C, steps, warmup):
+    s = LMHEAD
+    x = ce_inputs(s, 0, "cuda")
+    ws = torch.empty(C.coda_lmhead_ce_workspace_bytes(s.M, s.d, s.V, True), dtype=torch.uint8, device="cuda")
+    loss = torch.empty(1, device="cuda")
+    lse = torch.empty(s.M, device="cuda")
+    am = torch.empty(s.M, dtype=torch.int32, device="cuda")
+    dH = torch.empty(s.M, s.d, dtype=torch.bfloat16, device="cuda")
+    dW = torch.empty(s.V, s.d, dtype=torch.bfloat16, device="cuda")
+    fwd = [lambda: C.coda_lmhead_ce(x["H"], x["Wt"], x["labels"], loss, lse, am, None, None, ws)]
+    both = [lambda: C.coda_lmhead_ce(x["H"], x["Wt"], x["labels"], loss, lse, am, dH, dW, ws)]
+    tf, _ = time_steps(fwd, max(1, steps // 2), 1, stage_events=False)
+    tb, _ = time_steps(both, max(1, steps // 2), 1, stage_events=False)
+    n = max(1, steps // 2)
+    g = s.gemm_flops()
+    ms_f, ms_b = tf / n, tb / n
+    out = {"workload": s.name, "M": s.M, "d": s.d, "V": s.V, "fwd_ms": ms_f, "fwdbwd_ms": ms_b,
+           "fwd_tflops": g / ms_f / 1e9, "fwdbwd_tflops_counted": 3 * g / ms_b / 1e9,
+           "fwdbwd_tflops_executed": 4 * g / ms_b / 1e9, "loss": loss.item()}
+    del x, ws, dH, dW
+    return out
+
+
+def e2e_step(C, b, host, stream):
+    """Public-API step with host buffers: H2D of the step's activations and
+    upstream gradient from pinned memory, the fused fwd+bwd, D2H of dX."""
+    b.X.copy_(host["X"], non_blocking=True)
+    b.R.copy_(host["R"], non_blocking=True)
+    b.dY.copy_(host["dY"], non_blocking=True)
+    b.forward()
+    b.backward()
+    host["dX"].copy_(b.dX, non_blocking=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="7b", choices=sorted(CONFIGS))
+    ap.add_argument("--impl", default="fused", choices=["fused", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="skip ablation, LM-head and e2e legs")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    shape = CONFIGS[args.config]
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        return run_reference(args, shape)
+
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    import gemm_epilogue_transformer_tma_gb300 as C
+    from gemm_epilogue_transformer_tma_gb300.path import BlockBuffers
+    peaks = load_peaks()
+
+    x = block_inputs(shape, seed=rank, device="cuda")
+    b = BlockBuffers(x)
+    fs = FusedStep(C, b)
+    calls = fs.calls()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # warmup + timed region (clock sampling during it)
+    for _ in range(args.warmup):
+        for f in calls:
+            f()
+    barrier()
+    with ClockSampler(local) as clk:
+        total_ms, per = time_steps(calls, args.steps, 0)
+    barrier()
+    st, bits = C.coda_sync_status()
+    if st != 0:
+        raise RuntimeError(f"device status {C.STATUS_NAMES.get(st)} bits={bits:#x}")
+    ms = total_ms / args.steps
+    if dist is not None:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = t.item()
+    step_flops = shape.fwdbwd_flops()
+    value = world * step_flops / (ms * 1e-3) / 1e12
+    stage_ms = {name: statistics.mean(per[i]) for i, name in enumerate(FusedStep.STAGES)}
+    dom = max(fs.flops, key=lambda k: stage_ms[k])
+    dom_ach = fs.flops[dom] / (stage_ms[dom] * 1e-3) / 1e12
+    peak = peaks["bf16_tflops_sustained"]
+    clocks = clk.summary()
+
+    extras = {}
+    if not args.no_extras and rank == 0:
+        # unfused ablation, same workload and timing rules
+        bu = BlockBuffers(x, unfused=True)
+        ucalls = [bu.forward_unfused, bu.backward_unfused]
+        u_ms, _ = time_steps(ucalls, max(3, args.steps // 2), args.warmup, stage_events=False)
+        u_ms /= max(3, args.steps // 2)
+        extras["ablation_unfused"] = {"ms_per_step": u_ms, "tflops": step_flops / (u_ms * 1e-3) / 1e12,
+                                      "fused_speedup": u_ms / ms}
+        del bu
+        torch.cuda.empty_cache()
+        # end to end through the public API with host buffers
+        host = {k: torch.empty_like(x[k], device="cpu").pin_memory() for k in ("X", "R", "dY")}
+        for k in host:
+            host[k].copy_(x[k])
+        host["dX"] = torch.empty_like(b.dX, device="cpu").pin_memory()
+        stream = torch.cuda.current_stream()
+        for _ in range(2):
+            e2e_step(C, b, host, stream)
+        torch.cuda.synchronize()
+        n_e2e = max(3, args.steps // 2)
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            e2e_step(C, b, host, stream)
+        torch.cuda.synchronize()
+        e2e_ms = (time.perf_counter() - t0) * 1e3 / n_e2e
+        h2d = sum(host[k].numel() * host[k].element_size() for k in ("X", "R", "dY"))
+        d2h = host["dX"].numel() * host["dX"].element_size()
+        extras["e2e"] = {"value": step_flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e2e_ms,
+                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+        del host
+        del b, x, fs, calls
+        torch.cuda.empty_cache()
+        extras["lmhead_ce"] = bench_lmhead(C, args.steps, args.warmup)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1)/N(0,0.02)/U(0.5,1.5))",
+            "config": {"workload": shape.name, "M": shape.M, "K1": shape.K1, "d": shape.d, "ffn": shape.N2 // 2,
+                       "eps": shape.eps, "parallelism": "replicas" if world > 1 else "single-gpu",
+                       "l2": "inputs larger than L2 (W2 alone is %d MB), no flush" % (shape.N2 * shape.d * 2 >> 20)},
+            "pct_of_peak": 100.0 * value / world / peak,
+            "peak": {"bf16_tflops_sustained": peak, "bf16_tflops_burst": peaks["bf16_tflops"],
+                     "source": peaks["source"]},
+            "roofline": {"kernel": dom, "bound": "tensor", "achieved": dom_ach, "peak": peak, "unit": "TFLOP/s",
+                         "frac": dom_ach / peak, "traffic": None,
+                         "note": "peak = sustained bf16 of %s (kernel timed inside a long step)" % peaks["source"]},
+            "stage_ms": stage_ms,
+            "gpu_launches": len(calls) * args.steps,
+            "clocks": clocks,
+        }
+        if "e2e" in extras:
+            line["e2e"] = extras.pop("e2e")
+        line.update(extras)
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_oracle_baseline(shape)
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
