@@ -318,6 +318,7 @@ def main():
     peak = peaks["bf16_tflops_sustained"]
     clocks = clk.summary()
 
+    launches = len(calls) * args.steps
     extras = {}
     if not args.no_extras and rank == 0:
         # unfused ablation, same workload and timing rules
@@ -368,7 +369,7 @@ def main():
                          "frac": dom_ach / peak, "traffic": None,
                          "note": "peak = sustained bf16 of %s (kernel timed inside a long step)" % peaks["source"]},
             "stage_ms": stage_ms,
-            "gpu_launches": len(calls) * args.steps,
+            "gpu_launches": launches,
             "clocks": clocks,
         }
         if "e2e" in extras:

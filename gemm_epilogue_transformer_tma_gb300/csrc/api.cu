@@ -220,8 +220,8 @@ coda_status_t coda_fold_rmsnorm_weight(coda_handle_t h, const void* W2t, const v
 coda_status_t coda_gemm_res_prms(coda_handle_t h, const void* X, const void* W1t, const void* R, void* H,
                                  float* psum, int64_t M, int64_t K1, int64_t d, void* stream) {
   CODA_TRY(Check().handle(h).rows(M).mptr(X, M).ptr(W1t).mptr(R, M).mptr(H, M).mptr(psum, M).cols(K1).cols(d).st);
-  if (R == H) return CODA_ERR_INVALID_ARG;
   if (M == 0) return CODA_OK;
+  if (R == H) return CODA_ERR_INVALID_ARG;
   return from_cuda(gemm_res_prms(ctx_of(h, stream), static_cast<const bf16*>(X), static_cast<const bf16*>(W1t),
                                  static_cast<const bf16*>(R), static_cast<bf16*>(H), psum, int(M), int(K1), int(d),
                                  int(coda_prms_num_tiles(d))));

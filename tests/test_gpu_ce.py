@@ -1,0 +1,97 @@
+"""LM-head cross-entropy with the blocked log-sum-exp epilogue vs the fp64
+oracle (Synced write-up, section 五种积木: block reduction "block
+log-sum-exp" and the stateful max / sum-exp statistics).
+
+Small vocabularies that still span several 256-column tiles with a ragged
+last tile, plus several 16384-column backward chunks."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from coda_inputs import CEShape, ce_inputs
+from tests._parity import assert_device_ok, assert_elem, assert_frob, f64
+
+pytestmark = pytest.mark.gpu
+
+C = pytest.importorskip("gemm_epilogue_transformer_tma_gb300")
+
+
+def run_ce(H, Wt, labels, grads=True):
+    M, d = H.shape
+    V = Wt.shape[0]
+    ws = torch.empty(C.coda_lmhead_ce_workspace_bytes(M, d, V, grads), dtype=torch.uint8, device="cuda")
+    out = dict(loss=torch.empty(1, device="cuda"), lse=torch.empty(M, device="cuda"),
+               argmax=torch.empty(M, dtype=torch.int32, device="cuda"))
+    dH = torch.empty(M, d, dtype=torch.bfloat16, device="cuda") if grads else None
+    dW = torch.empty(V, d, dtype=torch.bfloat16, device="cuda") if grads else None
+    C.coda_lmhead_ce(H, Wt, labels, out["loss"], out["lse"], out["argmax"], dH, dW, ws)
+    out["dH"], out["dW"] = dH, dW
+    return out
+
+
+def check_argmax(gpu_am, H, Wt, tol_gap=1e-3):
+    L = O.logits_rows(H, Wt)
+    ref = O.argmax_lowest(L)
+    srt = np.sort(L, axis=1)
+    gap = srt[:, -1] - srt[:, -2]
+    decided = gap > tol_gap
+    got = gpu_am.cpu().numpy().astype(np.int64)
+    assert np.array_equal(got[decided], ref[decided])
+    # undecided rows: the GPU's choice must be a maximal column within the gap
+    for m in np.where(~decided)[0]:
+        assert L[m, got[m]] >= srt[m, -1] - tol_gap
+
+
+@pytest.mark.parametrize("M,d,V", [(200, 136, 1000), (128, 64, 256), (37, 256, 40000)])
+def test_ce_parity(M, d, V):
+    s = CEShape("t", M, d, V)
+    x = {k: v.cuda() for k, v in ce_inputs(s, 0).items()}
+    o = run_ce(x["H"], x["Wt"], x["labels"])
+    assert_device_ok()
+    H, Wt, y = f64(x["H"]), f64(x["Wt"]), x["labels"].cpu().numpy()
+    fw = O.ce_forward(H, Wt, y)
+    bw = O.ce_backward(H, Wt, y)
+    assert_elem(o["lse"], fw["lse"], "lse", tol=1e-4)
+    assert abs(o["loss"].item() - fw["loss"]) <= 1e-4 * abs(fw["loss"])
+    check_argmax(o["argmax"], H, Wt)
+    assert_frob(o["dH"], bw["dH"], "dH")
+    assert_frob(o["dW"], bw["dWt"], "dW")
+
+
+def test_ce_forward_only_and_label_range():
+    s = CEShape("t", 64, 64, 512)
+    x = {k: v.cuda() for k, v in ce_inputs(s, 1).items()}
+    lab = x["labels"].clone()
+    lab[3] = 512          # out of range
+    lab[5] = -1
+    o = run_ce(x["H"], x["Wt"], lab, grads=False)
+    st, bits = C.coda_sync_status()
+    assert st == 7 and (bits & 0x100)
+    H, Wt = f64(x["H"]), f64(x["Wt"])
+    lse = O.lse_rows(O.logits_rows(H, Wt))
+    assert_elem(o["lse"], lse, "lse", tol=1e-4)
+    ok = np.ones(64, bool)
+    ok[[3, 5]] = False
+    L = O.logits_rows(H, Wt)
+    yy = lab.cpu().numpy()
+    per_row = np.where(ok, lse - L[np.arange(64), np.clip(yy, 0, 511)], 0.0)
+    assert abs(o["loss"].item() - per_row.mean()) <= 1e-4 * abs(per_row.mean())
+    assert_device_ok()
+
+
+def test_ce_argmax_ties_pick_lowest_column():
+    M, d, V = 16, 64, 1024
+    g = torch.Generator().manual_seed(3)
+    H = torch.randn(M, d, generator=g).to(torch.bfloat16)
+    Wt = (torch.randn(V, d, generator=g) * 0.02).to(torch.bfloat16)
+    # exact duplicates of the winning column, in a later tile and in the same tile
+    L = f64(H) @ f64(Wt).T
+    win = O.argmax_lowest(L)
+    for m in range(M):
+        Wt[(win[m] + 300 + m) % V] = Wt[win[m]]
+    L = f64(H) @ f64(Wt).T
+    lab = torch.zeros(M, dtype=torch.int32)
+    o = run_ce(H.cuda(), Wt.cuda(), lab.cuda(), grads=False)
+    assert_device_ok()
+    assert np.array_equal(o["argmax"].cpu().numpy(), O.argmax_lowest(L))
