@@ -58,6 +58,7 @@ SIGNATURES = {
     "coda_gemm_rowscale_swiglu": (_INT, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _U32, _P]),
     "coda_swiglu_bwd": (_INT, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "coda_gemm_dgrad_rmsbwd": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
+    "coda_gemm_dgrad_rmsbwd_noalloc": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "coda_dg_combine": (_INT, [_P, _P, _I64, _I64, _P, _P]),
     "coda_gemm_wgrad_gscale": (_INT, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "coda_bwd_workspace_bytes": (_SZ, [_I64, _I64, _I64]),
@@ -250,6 +251,23 @@ def coda_gemm_dgrad_rmsbwd(dP, W2t, H, g, c, dH, dgpart, stream=None):
                                                  _ptr(g, BF, "g"), _ptr(c, F32, "c"), _ptr(dH, BF, "dH"),
                                                  _ptr(dgpart, F32, "dgpart"), M, N2, d, _stream(stream)),
            "coda_gemm_dgrad_rmsbwd")
+
+
+def coda_gemm_dgrad_rmsbwd_noalloc(dP, W2t, H, g, c, dH, dg, stream=None):
+    """coda_gemm_dgrad_rmsbwd + coda_dg_combine without any device allocation:
+    the dg partial sums live in the library's own fixed 8 MiB array."""
+    M, N2 = dP.shape
+    d = W2t.shape[1]
+    _shape(W2t, (N2, d), "W2t")
+    _shape(H, (M, d), "H")
+    _shape(g, (d,), "g")
+    _shape(c, (M,), "c")
+    _shape(dH, (M, d), "dH")
+    _shape(dg, (d,), "dg")
+    _check(load_library().coda_gemm_dgrad_rmsbwd_noalloc(_h(dP), _ptr(dP, BF, "dP"), _ptr(W2t, BF, "W2t"),
+                                                         _ptr(H, BF, "H"), _ptr(g, BF, "g"), _ptr(c, F32, "c"),
+                                                         _ptr(dH, BF, "dH"), _ptr(dg, F32, "dg"), M, N2, d,
+                                                         _stream(stream)), "coda_gemm_dgrad_rmsbwd_noalloc")
 
 
 def coda_dg_combine(dgpart, dg, stream=None):

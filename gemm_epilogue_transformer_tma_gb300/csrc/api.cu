@@ -108,6 +108,12 @@ bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t o
   return r == CUDA_SUCCESS;
 }
 
+LaunchCtx launch_ctx_of_handle(void* handle, void* stream) {
+  return ctx_of(static_cast<coda_handle_t>(handle), stream);
+}
+
+int device_of_handle(void* handle) { return static_cast<coda_handle_t>(handle)->device; }
+
 }  // namespace coda
 
 using namespace coda;

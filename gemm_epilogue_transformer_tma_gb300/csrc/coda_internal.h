@@ -24,6 +24,11 @@ struct LaunchCtx {
 bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t ld,
                     uint32_t box_inner, uint32_t box_outer);
 
+// Handle accessors (api.cu), for translation units that only see the
+// opaque coda_handle_t.
+LaunchCtx launch_ctx_of_handle(void* handle, void* stream);
+int device_of_handle(void* handle);
+
 // ---- GEMM launchers (gemm_*.cu) --------------------------------------------
 // Operand majors: A K-major = [M][K], MN-major = [K][M]; B K-major = [N][K],
 // MN-major = [K][N].  All row pitches equal the extents (dense tensors).

@@ -175,6 +175,32 @@ coda_status_t coda_gemm_dgrad_rmsbwd(coda_handle_t h, const void* dP, const void
                                      const void* g, const float* c, void* dH, float* dgpart, int64_t M, int64_t N2,
                                      int64_t d, void* stream);
 
+/* Allocation-free form of coda_gemm_dgrad_rmsbwd followed by coda_dg_combine:
+ * the same dH and dg, but the dg partial sums live in an array compiled into
+ * the library instead of a caller buffer.  The CODA write-up has no
+ * counterpart to this call; it exists for callers that cannot allocate device
+ * memory at all -- for example a host framework that passes a plugin only its
+ * input and output tensors while its own pool owns the rest of the device, or
+ * a latency-critical caller that must not pay for, or synchronise on, an
+ * allocation.  It calls no cudaMalloc, cudaFree or allocating library routine.
+ *   Inputs and outputs as coda_gemm_dgrad_rmsbwd; dg fp32 [d] receives the
+ *   column sums directly.
+ *   Limit: coda_dgpart_rows(M) * d * 4 bytes must not exceed 8 MiB (e.g. M up
+ *   to 8192 at d = 8192, or 16384 at d = 4096); larger problems are rejected
+ *   with CODA_ERR_WORKSPACE_TOO_SMALL before anything is launched.  The 8 MiB
+ *   array is held on every GPU that loads the library until the process
+ *   exits.
+ *   The first call on a device looks up the array's device address (with that
+ *   device current) and caches it; make that first call before any stream
+ *   capture.
+ *   All calls share the one array per device: calls that may overlap on the
+ *   GPU (different streams, or different host threads) race on it and must be
+ *   serialised by the caller.  Every partial a call reads is written earlier
+ *   in the same call, so what a previous call left there is never used. */
+coda_status_t coda_gemm_dgrad_rmsbwd_noalloc(coda_handle_t h, const void* dP, const void* W2t, const void* H,
+                                             const void* g, const float* c, void* dH, float* dg, int64_t M,
+                                             int64_t N2, int64_t d, void* stream);
+
 /* dg[k] = sum_r dgpart[r][k] (fixed order).  dgpart fp32 [rows][d], dg fp32 [d]. */
 coda_status_t coda_dg_combine(coda_handle_t h, const float* dgpart, int64_t rows, int64_t d, float* dg,
                               void* stream);
