@@ -262,10 +262,14 @@ def main():
     ap.add_argument("--impl", default="fused", choices=["fused", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip ablation, LM-head and e2e legs")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="override the token count M (smaller cases for profiler captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     shape = CONFIGS[args.config]
+    if args.tokens:
+        shape = BlockShape(f"{shape.name}_m{args.tokens}", args.tokens, shape.K1, shape.d, shape.N2)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
