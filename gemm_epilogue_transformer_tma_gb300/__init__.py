@@ -49,6 +49,7 @@ SIGNATURES = {
     "coda_status_string": (ctypes.c_char_p, [_INT]),
     "coda_sync_status": (_INT, [_P, _P, ctypes.POINTER(ctypes.c_int32)]),
     "coda_set_wait_timeout_ns": (_INT, [_P, _U64]),
+    "coda_debug_skip_first_stage": (_INT, [_P, _INT]),
     "coda_prms_num_tiles": (_I64, [_I64]),
     "coda_dgpart_rows": (_I64, [_I64]),
     "coda_gemm": (_INT, [_P, _P, _INT, _P, _INT, _P, _I64, _I64, _I64, _P, _P, _P]),
@@ -160,6 +161,11 @@ def coda_sync_status(device: int | None = None, stream=None) -> tuple[int, int]:
 
 def coda_set_wait_timeout_ns(ns: int, device: int | None = None):
     _check(load_library().coda_set_wait_timeout_ns(handle(device), ns), "coda_set_wait_timeout_ns")
+
+
+def coda_debug_skip_first_stage(enable: bool, device: int | None = None):
+    """Failure-detection test hook (see include/coda.h)."""
+    _check(load_library().coda_debug_skip_first_stage(handle(device), int(enable)), "coda_debug_skip_first_stage")
 
 
 def coda_prms_num_tiles(d: int) -> int:

@@ -18,6 +18,7 @@ struct coda_handle_s {
   int num_sms;
   int* status;  // device status word
   uint64_t timeout_ns;
+  int skip_first_stage;  // test hook for the bounded waits (coda_debug_skip_first_stage)
 };
 
 namespace coda {
@@ -45,6 +46,7 @@ LaunchCtx ctx_of(coda_handle_t h, void* stream) {
   c.status = h->status;
   c.timeout_ns = h->timeout_ns;
   c.stream = static_cast<cudaStream_t>(stream);
+  c.skip_first_stage = h->skip_first_stage;
   return c;
 }
 
@@ -141,6 +143,7 @@ coda_status_t coda_create(coda_handle_t* out, int device) {
   coda_handle_s* h = new coda_handle_s;
   h->device = device;
   h->timeout_ns = kDefaultTimeoutNs;
+  h->skip_first_stage = 0;
   h->status = nullptr;
   coda_status_t st = CODA_OK;
   if (cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
@@ -195,6 +198,12 @@ coda_status_t coda_sync_status(coda_handle_t h, void* stream, int32_t* device_bi
 coda_status_t coda_set_wait_timeout_ns(coda_handle_t h, uint64_t ns) {
   CODA_TRY(Check().handle(h).st);
   h->timeout_ns = ns == 0 ? kDefaultTimeoutNs : ns;
+  return CODA_OK;
+}
+
+coda_status_t coda_debug_skip_first_stage(coda_handle_t h, int enable) {
+  CODA_TRY(Check().handle(h).st);
+  h->skip_first_stage = enable != 0;
   return CODA_OK;
 }
 

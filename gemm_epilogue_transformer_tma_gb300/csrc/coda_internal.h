@@ -15,6 +15,7 @@ struct LaunchCtx {
   int* status;          // device status word
   uint64_t timeout_ns;  // bound on every in-kernel wait
   cudaStream_t stream;
+  int skip_first_stage;  // test hook, see coda_debug_skip_first_stage
 };
 
 // 2-D bf16 tensor map with 128-byte swizzle.  The tensor is `outer` rows of

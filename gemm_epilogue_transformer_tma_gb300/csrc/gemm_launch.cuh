@@ -25,7 +25,7 @@ cudaError_t launch_gemm_kernel(const LaunchCtx& c, const CUtensorMap& ta, const 
   sh.tiles_n = tiles_n;
   sh.num_kb = (K + BK - 1) / BK;
   sh.group_m = 8;
-  KernelCtl ctl{c.status, c.timeout_ns};
+  KernelCtl ctl{c.status, c.timeout_ns, c.skip_first_stage};
   const int tiles = sh.tiles_m * sh.tiles_n;
   const int grid = std::max(1, std::min(tiles, c.num_sms));
   kern<<<grid, GEMM_THREADS, L::TOTAL, c.stream>>>(ta, tb, tb2, sh, ctl, ep);

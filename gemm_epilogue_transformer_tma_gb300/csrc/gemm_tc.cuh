@@ -52,6 +52,7 @@ struct GemmShape {
 struct KernelCtl {
   int* status;        // device status word (atomicOr of DEV_ERR_* bits)
   uint64_t timeout_ns;
+  int skip_first_stage;  // test hook: CTA 0's producer never fills its first stage
 };
 
 struct EpiCtx {
@@ -147,8 +148,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      long issued = 0;
+      uint32_t pending = 0;  // bit s: stage s has been filled at least once
+      uint32_t parity = 0;   // bit s: phase parity of the last fill of stage s
       bool ok = true;
+      bool skip = ctl.skip_first_stage != 0 && blockIdx.x == 0;
       for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
         int tm, tn;
         tile_coords(t, sh, tm, tn);
@@ -158,25 +161,31 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             ok = false;
             break;
           }
-          uint8_t* sa = smem + stage * L::STAGE_BYTES;
-          uint8_t* sb = sa + L::A_BYTES;
-          mbar_arrive_expect_tx(&full[stage], L::STAGE_BYTES);
-          if (!A_MN) {
-            tma_load_2d(sa, &tmA, &full[stage], kb * BK, tm * BM);
+          if (skip) {
+            // test hook: leave this stage unfilled so the MMA's wait on it expires
+            skip = false;
           } else {
+            uint8_t* sa = smem + stage * L::STAGE_BYTES;
+            uint8_t* sb = sa + L::A_BYTES;
+            mbar_arrive_expect_tx(&full[stage], L::STAGE_BYTES);
+            if (!A_MN) {
+              tma_load_2d(sa, &tmA, &full[stage], kb * BK, tm * BM);
+            } else {
 #pragma unroll
-            for (int i = 0; i < BM / 64; ++i) tma_load_2d(sa + i * 8192, &tmA, &full[stage], tm * BM + i * 64, kb * BK);
-          }
-          if (B_DUAL) {
-            tma_load_2d(sb, &tmB, &full[stage], kb * BK, tn * (BN / 2));
-            tma_load_2d(sb + (BN / 2) * 128, &tmB2, &full[stage], kb * BK, tn * (BN / 2));
-          } else if (!B_MN) {
-            tma_load_2d(sb, &tmB, &full[stage], kb * BK, tn * BN);
-          } else {
+              for (int i = 0; i < BM / 64; ++i) tma_load_2d(sa + i * 8192, &tmA, &full[stage], tm * BM + i * 64, kb * BK);
+            }
+            if (B_DUAL) {
+              tma_load_2d(sb, &tmB, &full[stage], kb * BK, tn * (BN / 2));
+              tma_load_2d(sb + (BN / 2) * 128, &tmB2, &full[stage], kb * BK, tn * (BN / 2));
+            } else if (!B_MN) {
+              tma_load_2d(sb, &tmB, &full[stage], kb * BK, tn * BN);
+            } else {
 #pragma unroll
-            for (int i = 0; i < BN / 64; ++i) tma_load_2d(sb + i * 8192, &tmB, &full[stage], tn * BN + i * 64, kb * BK);
+              for (int i = 0; i < BN / 64; ++i) tma_load_2d(sb + i * 8192, &tmB, &full[stage], tn * BN + i * 64, kb * BK);
+            }
+            pending |= 1u << stage;
+            parity = (parity & ~(1u << stage)) | (phase << stage);
           }
-          ++issued;
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -185,12 +194,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       }
       if (!ok) {
         // let every copy this thread started land before shared memory is released
-        const long n_wait = issued < STAGES ? issued : STAGES;
-        for (long j = 1; j <= n_wait; ++j) {
-          const long n = issued - j;
-          if (!mbar_wait_timeout(&full[n % STAGES], static_cast<uint32_t>((n / STAGES) & 1), ctl.timeout_ns))
-            atomicOr(ctl.status, DEV_ERR_TIMEOUT_DRAIN);
-        }
+        for (int st = 0; st < STAGES; ++st)
+          if ((pending >> st) & 1u)
+            if (!mbar_wait_timeout(&full[st], (parity >> st) & 1u, ctl.timeout_ns))
+              atomicOr(ctl.status, DEV_ERR_TIMEOUT_DRAIN);
       }
     }
   } else if (warp == 1) {

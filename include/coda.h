@@ -91,6 +91,14 @@ coda_status_t coda_sync_status(coda_handle_t h, void* stream, int32_t* device_bi
  * 0 restores the default. */
 coda_status_t coda_set_wait_timeout_ns(coda_handle_t h, uint64_t ns);
 
+/* Failure-detection test hook.  While enabled, every GEMM launched through
+ * this handle leaves the first shared-memory stage of its first CTA unfilled,
+ * so that CTA's MMA wait cannot complete and must hit the wait limit: the
+ * launch then records CODA_ERR_TIMEOUT (reported by coda_sync_status), its
+ * results are invalid, and the context stays usable.  Pair it with a short
+ * coda_set_wait_timeout_ns.  Not for production use. */
+coda_status_t coda_debug_skip_first_stage(coda_handle_t h, int enable);
+
 /* Columns of the partial-RMS buffer for hidden width d: ceil(d / BN1). */
 int64_t coda_prms_num_tiles(int64_t d);
 

@@ -22,7 +22,7 @@ __all__ = [
     "block_backward", "stage_swiglu_bwd", "stage_dgrad2_rmsbwd",
     "stage_wgrad2", "stage_dgrad1", "stage_wgrad1", "logits_rows",
     "lse_rows", "lse_tile_partials", "lse_combine", "ce_forward",
-    "ce_backward", "argmax_lowest",
+    "ce_backward", "argmax_lowest", "ce_weight_grad_given_lse",
 ]
 
 
@@ -307,3 +307,15 @@ def ce_backward(H, Wt, labels, row_chunk: int = 256):
         dH[s:s + row_chunk] = P @ Wt
         dWt += P.T @ H[s:s + row_chunk]
     return {"dH": dH, "dWt": dWt}
+
+
+def ce_weight_grad_given_lse(H, Wt_cols, cols, labels, lse, M: int):
+    """Rows `cols` of dWt given each row's log-sum-exp:
+    dWt[v] = sum_m ((exp(L[m,v] - lse[m]) - [y_m == v]) / M) H[m], with
+    L[m,v] = H[m] . Wt[v].  Wt_cols holds the rows `cols` of Wt; M is the
+    batch size of the mean (the rows of H may be all of them)."""
+    H = np.asarray(H, np.float64)
+    L = H @ np.asarray(Wt_cols, np.float64).T
+    P = np.exp(L - np.asarray(lse, np.float64)[:, None])
+    P -= (np.asarray(labels, np.int64)[:, None] == np.asarray(cols, np.int64)[None, :])
+    return (P / M).T @ H

@@ -325,3 +325,16 @@ def test_golden_ce_worked_example():
     bw = O.ce_backward(H, Wt, y)
     np.testing.assert_allclose(bw["dH"], ex["dH"], rtol=1e-13, atol=1e-15)
     np.testing.assert_allclose(bw["dWt"], ex["dWt"], rtol=1e-13, atol=1e-15)
+
+
+def test_ce_weight_grad_given_lse_matches_full_backward():
+    r = rng(29)
+    M, d, V = 6, 5, 40
+    H = r.standard_normal((M, d))
+    Wt = r.standard_normal((V, d))
+    y = np.array([0, 3, 3, 39, 7, 12])
+    full = O.ce_backward(H, Wt, y)["dWt"]
+    cols = np.array([3, 12, 0, 25])
+    lse = O.lse_rows(O.logits_rows(H, Wt))
+    np.testing.assert_allclose(O.ce_weight_grad_given_lse(H, Wt[cols], cols, y, lse, M), full[cols],
+                               rtol=1e-12, atol=1e-14)
