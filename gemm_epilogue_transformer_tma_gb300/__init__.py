@@ -50,6 +50,7 @@ SIGNATURES = {
     "coda_sync_status": (_INT, [_P, _P, ctypes.POINTER(ctypes.c_int32)]),
     "coda_set_wait_timeout_ns": (_INT, [_P, _U64]),
     "coda_debug_skip_first_stage": (_INT, [_P, _INT]),
+    "coda_set_sm_pairing": (_INT, [_P, _INT]),
     "coda_prms_num_tiles": (_I64, [_I64]),
     "coda_dgpart_rows": (_I64, [_I64]),
     "coda_gemm": (_INT, [_P, _P, _INT, _P, _INT, _P, _I64, _I64, _I64, _P, _P, _P]),
@@ -161,6 +162,11 @@ def coda_sync_status(device: int | None = None, stream=None) -> tuple[int, int]:
 
 def coda_set_wait_timeout_ns(ns: int, device: int | None = None):
     _check(load_library().coda_set_wait_timeout_ns(handle(device), ns), "coda_set_wait_timeout_ns")
+
+
+def coda_set_sm_pairing(enable: bool, device: int | None = None):
+    """GEMMs on SM pairs (2-SM MMA, default) or one SM per tile."""
+    _check(load_library().coda_set_sm_pairing(handle(device), int(enable)), "coda_set_sm_pairing")
 
 
 def coda_debug_skip_first_stage(enable: bool, device: int | None = None):

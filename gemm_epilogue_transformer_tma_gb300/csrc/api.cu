@@ -19,6 +19,7 @@ struct coda_handle_s {
   int* status;  // device status word
   uint64_t timeout_ns;
   int skip_first_stage;  // test hook for the bounded waits (coda_debug_skip_first_stage)
+  int pair;              // GEMMs on SM pairs (coda_set_sm_pairing)
 };
 
 namespace coda {
@@ -47,6 +48,7 @@ LaunchCtx ctx_of(coda_handle_t h, void* stream) {
   c.timeout_ns = h->timeout_ns;
   c.stream = static_cast<cudaStream_t>(stream);
   c.skip_first_stage = h->skip_first_stage;
+  c.pair = h->pair;
   return c;
 }
 
@@ -144,6 +146,7 @@ coda_status_t coda_create(coda_handle_t* out, int device) {
   h->device = device;
   h->timeout_ns = kDefaultTimeoutNs;
   h->skip_first_stage = 0;
+  h->pair = 1;
   h->status = nullptr;
   coda_status_t st = CODA_OK;
   if (cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
@@ -198,6 +201,12 @@ coda_status_t coda_sync_status(coda_handle_t h, void* stream, int32_t* device_bi
 coda_status_t coda_set_wait_timeout_ns(coda_handle_t h, uint64_t ns) {
   CODA_TRY(Check().handle(h).st);
   h->timeout_ns = ns == 0 ? kDefaultTimeoutNs : ns;
+  return CODA_OK;
+}
+
+coda_status_t coda_set_sm_pairing(coda_handle_t h, int enable) {
+  CODA_TRY(Check().handle(h).st);
+  h->pair = enable != 0;
   return CODA_OK;
 }
 

@@ -16,6 +16,7 @@ struct LaunchCtx {
   uint64_t timeout_ns;  // bound on every in-kernel wait
   cudaStream_t stream;
   int skip_first_stage;  // test hook, see coda_debug_skip_first_stage
+  int pair;              // 1: 2-SM GEMM kernel (CTA pairs), 0: 1-SM kernel
 };
 
 // 2-D bf16 tensor map with 128-byte swizzle.  The tensor is `outer` rows of

@@ -6,7 +6,6 @@ namespace coda {
 
 namespace {
 constexpr int kBN = 256;
-constexpr int kStages = 4;
 }  // namespace
 
 cudaError_t gemm_dgrad_rms(const LaunchCtx& c, const __nv_bfloat16* dP, const __nv_bfloat16* W2t,
@@ -15,10 +14,9 @@ cudaError_t gemm_dgrad_rms(const LaunchCtx& c, const __nv_bfloat16* dP, const __
   // acc[m, k] = sum_n dP[m, n] W2t[n, k]: A = dP K-major (K = N2), B = W2t
   // stored [K][N] (MN-major).
   CUtensorMap ta, tb;
-  if (!make_operand_maps(&ta, &tb, dP, false, W2t, true, M, d, N2, kBN)) return cudaErrorInvalidValue;
+  if (!make_operand_maps(&ta, &tb, dP, false, W2t, true, M, d, N2, b_box_rows(c))) return cudaErrorInvalidValue;
   EpiDgradRms::Params ep{H, d, g, cvec, dH, d, dgpart};
-  return launch_gemm_kernel<kBN, kStages, false, true, false, EpiDgradRms>(c, ta, tb, tb, M, d, N2,
-                                                                            (d + kBN - 1) / kBN, ep);
+  return run_gemm<false, true, false, EpiDgradRms>(c, ta, tb, tb, M, d, N2, (d + kBN - 1) / kBN, ep);
 }
 
 }  // namespace coda

@@ -6,7 +6,6 @@ namespace coda {
 
 namespace {
 constexpr int kBN = 256;
-constexpr int kStages = 4;
 }  // namespace
 
 int prms_tile_cols() { return kBN; }
@@ -14,10 +13,9 @@ int prms_tile_cols() { return kBN; }
 cudaError_t gemm_res_prms(const LaunchCtx& c, const __nv_bfloat16* X, const __nv_bfloat16* W1t,
                           const __nv_bfloat16* R, __nv_bfloat16* H, float* psum, int M, int K1, int d, int T) {
   CUtensorMap ta, tb;
-  if (!make_operand_maps(&ta, &tb, X, false, W1t, false, M, d, K1, kBN)) return cudaErrorInvalidValue;
+  if (!make_operand_maps(&ta, &tb, X, false, W1t, false, M, d, K1, b_box_rows(c))) return cudaErrorInvalidValue;
   EpiResPrms::Params ep{R, d, H, d, psum, T};
-  return launch_gemm_kernel<kBN, kStages, false, false, false, EpiResPrms>(c, ta, tb, tb, M, d, K1,
-                                                                            (d + kBN - 1) / kBN, ep);
+  return run_gemm<false, false, false, EpiResPrms>(c, ta, tb, tb, M, d, K1, (d + kBN - 1) / kBN, ep);
 }
 
 cudaError_t gemm_rowscale_swiglu(const LaunchCtx& c, const __nv_bfloat16* H, const __nv_bfloat16* W2gt,
@@ -25,10 +23,9 @@ cudaError_t gemm_rowscale_swiglu(const LaunchCtx& c, const __nv_bfloat16* H, con
                                  bool swiglu) {
   CUtensorMap ta, tb, tb2;
   if (!swiglu) {
-    if (!make_operand_maps(&ta, &tb, H, false, W2gt, false, M, N2, d, kBN)) return cudaErrorInvalidValue;
+    if (!make_operand_maps(&ta, &tb, H, false, W2gt, false, M, N2, d, b_box_rows(c))) return cudaErrorInvalidValue;
     EpiStore::Params ep{out, N2, rstd, nullptr};
-    return launch_gemm_kernel<kBN, kStages, false, false, false, EpiStore>(c, ta, tb, tb, M, N2, d,
-                                                                            (N2 + kBN - 1) / kBN, ep);
+    return run_gemm<false, false, false, EpiStore>(c, ta, tb, tb, M, N2, d, (N2 + kBN - 1) / kBN, ep);
   }
   const int F = N2 / 2;
   if (!make_tmap_bf16(&ta, H, d, M, d, 64, BM)) return cudaErrorInvalidValue;
@@ -37,20 +34,19 @@ cudaError_t gemm_rowscale_swiglu(const LaunchCtx& c, const __nv_bfloat16* H, con
   if (!make_tmap_bf16(&tb, W2gt, d, F, d, 64, kBN / 2)) return cudaErrorInvalidValue;
   if (!make_tmap_bf16(&tb2, W2gt + static_cast<int64_t>(F) * d, d, F, d, 64, kBN / 2)) return cudaErrorInvalidValue;
   EpiRowscaleSwiglu::Params ep{rstd, out, F, zsave, N2, F};
-  return launch_gemm_kernel<kBN, kStages, false, false, true, EpiRowscaleSwiglu>(c, ta, tb, tb2, M, F, d,
-                                                                                 (F + kBN / 2 - 1) / (kBN / 2), ep);
+  return run_gemm<false, false, true, EpiRowscaleSwiglu>(c, ta, tb, tb2, M, F, d, (F + kBN / 2 - 1) / (kBN / 2), ep);
 }
 
 cudaError_t gemm_store(const LaunchCtx& c, const __nv_bfloat16* A, bool a_mn, const __nv_bfloat16* B, bool b_mn,
                        __nv_bfloat16* C, int M, int N, int K, const float* row_scale,
                        const __nv_bfloat16* col_scale) {
   CUtensorMap ta, tb;
-  if (!make_operand_maps(&ta, &tb, A, a_mn, B, b_mn, M, N, K, kBN)) return cudaErrorInvalidValue;
+  if (!make_operand_maps(&ta, &tb, A, a_mn, B, b_mn, M, N, K, b_box_rows(c))) return cudaErrorInvalidValue;
   EpiStore::Params ep{C, N, row_scale, col_scale};
   const int tn = (N + kBN - 1) / kBN;
-  if (!a_mn && !b_mn) return launch_gemm_kernel<kBN, kStages, false, false, false, EpiStore>(c, ta, tb, tb, M, N, K, tn, ep);
-  if (!a_mn && b_mn) return launch_gemm_kernel<kBN, kStages, false, true, false, EpiStore>(c, ta, tb, tb, M, N, K, tn, ep);
-  if (a_mn && b_mn) return launch_gemm_kernel<kBN, kStages, true, true, false, EpiStore>(c, ta, tb, tb, M, N, K, tn, ep);
+  if (!a_mn && !b_mn) return run_gemm<false, false, false, EpiStore>(c, ta, tb, tb, M, N, K, tn, ep);
+  if (!a_mn && b_mn) return run_gemm<false, true, false, EpiStore>(c, ta, tb, tb, M, N, K, tn, ep);
+  if (a_mn && b_mn) return run_gemm<true, true, false, EpiStore>(c, ta, tb, tb, M, N, K, tn, ep);
   return cudaErrorNotSupported;  // MN-major A with K-major B is not used on this path
 }
 
@@ -58,10 +54,9 @@ cudaError_t gemm_store_f32(const LaunchCtx& c, const __nv_bfloat16* A, bool a_mn
                            float* C, int M, int N, int K, bool accumulate) {
   if (a_mn || !b_mn) return cudaErrorNotSupported;  // only [M][K] x [K][N] is used
   CUtensorMap ta, tb;
-  if (!make_operand_maps(&ta, &tb, A, a_mn, B, b_mn, M, N, K, kBN)) return cudaErrorInvalidValue;
+  if (!make_operand_maps(&ta, &tb, A, a_mn, B, b_mn, M, N, K, b_box_rows(c))) return cudaErrorInvalidValue;
   EpiStoreF32::Params ep{C, N, accumulate ? 1 : 0};
-  return launch_gemm_kernel<kBN, kStages, false, true, false, EpiStoreF32>(c, ta, tb, tb, M, N, K,
-                                                                            (N + kBN - 1) / kBN, ep);
+  return run_gemm<false, true, false, EpiStoreF32>(c, ta, tb, tb, M, N, K, (N + kBN - 1) / kBN, ep);
 }
 
 }  // namespace coda

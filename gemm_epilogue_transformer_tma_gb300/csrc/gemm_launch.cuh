@@ -6,6 +6,7 @@
 
 #include "coda_internal.h"
 #include "gemm_tc.cuh"
+#include "gemm_tc2.cuh"
 
 namespace coda {
 
@@ -31,6 +32,64 @@ cudaError_t launch_gemm_kernel(const LaunchCtx& c, const CUtensorMap& ta, const 
   kern<<<grid, GEMM_THREADS, L::TOTAL, c.stream>>>(ta, tb, tb2, sh, ctl, ep);
   return cudaGetLastError();
 }
+
+template <int BN, int STAGES, bool A_MN, bool B_MN, bool B_DUAL, class Epi>
+cudaError_t launch_gemm2_kernel(const LaunchCtx& c, const CUtensorMap& ta, const CUtensorMap& tb,
+                                const CUtensorMap& tb2, int M, int N, int K, int tiles_n,
+                                const typename Epi::Params& ep) {
+  using L = Gemm2Smem<BN, STAGES>;
+  auto kern = gemm_tc2_kernel<BN, STAGES, A_MN, B_MN, B_DUAL, Epi>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL);
+  if (e != cudaSuccess) return e;
+  GemmShape sh;
+  sh.M = M;
+  sh.N = N;
+  sh.K = K;
+  sh.tiles_m = (M + BM2 - 1) / BM2;
+  sh.tiles_n = tiles_n;
+  sh.num_kb = (K + BK - 1) / BK;
+  sh.group_m = 4;
+  KernelCtl ctl{c.status, c.timeout_ns, c.skip_first_stage};
+  // co-resident SM pairs for this kernel (not every TPC need have both SMs
+  // enabled); queried once per instantiation and device
+  static int max_pairs[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (max_pairs[dev] == 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (c.num_sms / 2), 1, 1);
+    cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = L::TOTAL;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    max_pairs[dev] = std::max(1, std::min(n, c.num_sms / 2));
+  }
+  const int tiles = sh.tiles_m * sh.tiles_n;
+  const int clusters = std::max(1, std::min(tiles, max_pairs[dev]));
+  kern<<<2 * clusters, GEMM_THREADS, L::TOTAL, c.stream>>>(ta, tb, tb2, sh, ctl, ep);
+  return cudaGetLastError();
+}
+
+// The 2-SM pair kernel (default) or the 1-SM kernel, 256-column tiles.
+template <bool A_MN, bool B_MN, bool B_DUAL, class Epi>
+cudaError_t run_gemm(const LaunchCtx& c, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tb2, int M,
+                     int N, int K, int tiles_n, const typename Epi::Params& ep) {
+  if (c.pair) return launch_gemm2_kernel<256, 6, A_MN, B_MN, B_DUAL, Epi>(c, ta, tb, tb2, M, N, K, tiles_n, ep);
+  return launch_gemm_kernel<256, 4, A_MN, B_MN, B_DUAL, Epi>(c, ta, tb, tb2, M, N, K, tiles_n, ep);
+}
+
+// Rows of one K-major B box: a whole 256-row tile (1-SM) or the half a CTA
+// of the pair holds.
+inline int b_box_rows(const LaunchCtx& c) { return c.pair ? 128 : 256; }
 
 // Tensor maps for the two operands given their majors.
 inline bool make_operand_maps(CUtensorMap* ta, CUtensorMap* tb, const __nv_bfloat16* A, bool a_mn,

@@ -519,7 +519,9 @@ struct EpiDgradRms {
 #pragma unroll
         for (int i = 0; i < 32; ++i) a[i] *= h[i];
         const float s = warp_transpose_sum32(a, c.lane);
-        if (n0 + c.lane < c.N)
+        // 128-row blocks wholly past M (the second half of a CTA-pair tile)
+        // have no rows and no partial
+        if (n0 + c.lane < c.N && c.tm * 128 < c.M)
           p.dgpart[static_cast<int64_t>(c.tm * 4 + c.quad) * c.N + n0 + c.lane] = s;
       }
     }

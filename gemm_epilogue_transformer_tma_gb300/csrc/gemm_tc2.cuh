@@ -1,0 +1,282 @@
+// 2-SM form of the persistent bf16 GEMM: a cluster of two CTAs (an SM pair)
+// computes one 256 x BN output tile with tcgen05.mma.cta_group::2.
+//
+// Each CTA loads only its own half of the operands -- 128 rows of A and BN/2
+// rows (columns) of B -- so per SM the shared-memory traffic per MMA is half
+// of the 1-SM kernel's B traffic, which leaves room for a deeper ring (6
+// stages of 32 KB).  The accumulator of each CTA holds its 128 output rows x
+// BN columns in its own TMEM, so the epilogue programs of gemm_tc.cuh run
+// unchanged (EpiCtx.tm is the 128-row block index).
+//
+// Roles, per CTA of the pair (rank 0 = leader, rank 1 = peer):
+//   warp 0       TMA producer for this CTA's halves; completion on this
+//                CTA's own full[] barrier.
+//   warp 1       leader: MMA issuer.  It waits for its own full[s] and for
+//                peer_full[s] (the peer's relay), issues the 2-SM MMAs, and
+//                commits to empty[s] / tfull[] of both CTAs (multicast).
+//                peer: relay -- waits for its own full[s] and arrives on the
+//                leader's peer_full[s].  Both CTAs' warp 1 allocate TMEM
+//                together (cta_group::2).
+//   warps 2..5   epilogue on this CTA's 128 rows; release the accumulator by
+//                arriving on the leader's tempty[].
+// Every copy completes on a barrier of the CTA that issued it, so each CTA
+// can always wait for its own copies on the way out.  All waits are bounded
+// as in the 1-SM kernel.
+#pragma once
+
+#include "gemm_tc.cuh"
+
+namespace coda {
+
+constexpr int BM2 = 256;  // output rows per CTA pair
+
+template <int BN, int STAGES>
+struct Gemm2Smem {
+  static constexpr int A_BYTES = 128 * BK * 2;        // this CTA's 128 rows of A
+  static constexpr int B_BYTES = (BN / 2) * BK * 2;   // this CTA's BN/2 rows of B
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
+  static constexpr int BAR_BYTES = 512;
+  static constexpr int TOTAL = RING_BYTES + BAR_BYTES + 1024;
+  static constexpr int TMEM_COLS = 2 * BN;
+  static_assert(TMEM_COLS <= 512, "TMEM has 512 columns");
+  static_assert((3 * STAGES + 5) * 8 + 8 <= BAR_BYTES, "barrier area too small");
+  static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "1 KB aligned halves");
+};
+
+template <int BN, int STAGES, bool A_MN, bool B_MN, bool B_DUAL, class Epi>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
+    gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmB2, const GemmShape sh, const KernelCtl ctl,
+                    const typename Epi::Params ep) {
+  using L = Gemm2Smem<BN, STAGES>;
+  static_assert(!(B_DUAL && B_MN), "dual-box B is K-major only");
+  static_assert(BN == 256, "the pair kernel is instantiated for 256-column tiles");
+  constexpr int HB = BN / 2;  // B rows held by one CTA
+  constexpr uint32_t IDESC = idesc_bf16_f32(BM2, BN, A_MN, B_MN);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::RING_BYTES);
+  uint64_t* peer_full = full + STAGES;  // leader only: the peer's stage s has landed
+  uint64_t* empty = peer_full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;  // leader only: both CTAs' epilogues released the buffer
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int cluster_id = blockIdx.x >> 1;
+  const int num_clusters = gridDim.x >> 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&peer_full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 8);  // lane 0 of the 4 epilogue warps of each CTA
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    if (B_DUAL) tma_prefetch_desc(&tmB2);
+  }
+  // barriers of both CTAs initialised before anyone signals across the pair
+  cluster_sync_all();
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, L::TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync_all();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int num_tiles = sh.tiles_m * sh.tiles_n;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t pending = 0, parity = 0;
+      bool ok = true;
+      bool skip = ctl.skip_first_stage != 0 && cluster_id == 0 && leader;
+      for (int t = cluster_id; t < num_tiles && ok; t += num_clusters) {
+        int tm, tn;
+        tile_coords(t, sh, tm, tn);
+        const int m0 = tm * BM2 + static_cast<int>(rank) * 128;  // this CTA's A rows
+        for (int kb = 0; kb < sh.num_kb; ++kb) {
+          if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, ctl.timeout_ns)) {
+            if (!*abort_flag) raise_error(ctl, abort_flag, DEV_ERR_TIMEOUT_PRODUCER);
+            ok = false;
+            break;
+          }
+          if (skip) {
+            skip = false;  // test hook: leave this stage unfilled
+          } else {
+            uint8_t* sa = smem + stage * L::STAGE_BYTES;
+            uint8_t* sb = sa + L::A_BYTES;
+            mbar_arrive_expect_tx(&full[stage], L::STAGE_BYTES);
+            if (!A_MN) {
+              tma_load_2d(sa, &tmA, &full[stage], kb * BK, m0);
+            } else {
+              tma_load_2d(sa, &tmA, &full[stage], m0, kb * BK);
+              tma_load_2d(sa + 8192, &tmA, &full[stage], m0 + 64, kb * BK);
+            }
+            if (B_DUAL) {
+              // leader: gate rows of the tile, peer: the matching up rows
+              tma_load_2d(sb, leader ? &tmB : &tmB2, &full[stage], kb * BK, tn * HB);
+            } else if (!B_MN) {
+              tma_load_2d(sb, &tmB, &full[stage], kb * BK, tn * BN + static_cast<int>(rank) * HB);
+            } else {
+#pragma unroll
+              for (int i = 0; i < HB / 64; ++i)
+                tma_load_2d(sb + i * 8192, &tmB, &full[stage], tn * BN + static_cast<int>(rank) * HB + i * 64,
+                            kb * BK);
+            }
+            pending |= 1u << stage;
+            parity = (parity & ~(1u << stage)) | (phase << stage);
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        for (int st = 0; st < STAGES; ++st)
+          if ((pending >> st) & 1u)
+            if (!mbar_wait_timeout(&full[st], (parity >> st) & 1u, ctl.timeout_ns))
+              atomicOr(ctl.status, DEV_ERR_TIMEOUT_DRAIN);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      if (leader) {
+        // -------------------------------------------------------------- MMA
+        int stage = 0;
+        uint32_t phase = 0;
+        int it = 0;
+        bool ok = true;
+        bool issued_any = false;
+        for (int t = cluster_id; t < num_tiles && ok; t += num_clusters, ++it) {
+          const int acc = it & 1;
+          const uint32_t acc_phase = (it >> 1) & 1;
+          if (!mbar_wait_bounded_cluster(&tempty[acc], acc_phase ^ 1u, abort_flag, ctl.timeout_ns)) {
+            if (!*abort_flag) raise_error(ctl, abort_flag, DEV_ERR_TIMEOUT_MMA);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+          for (int kb = 0; kb < sh.num_kb; ++kb) {
+            if (!mbar_wait_bounded(&full[stage], phase, abort_flag, ctl.timeout_ns) ||
+                !mbar_wait_bounded_cluster(&peer_full[stage], phase, abort_flag, ctl.timeout_ns)) {
+              if (!*abort_flag) raise_error(ctl, abort_flag, DEV_ERR_TIMEOUT_MMA);
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t sa = smem_u32(smem + stage * L::STAGE_BYTES);
+            const uint32_t sb = sa + L::A_BYTES;
+#pragma unroll
+            for (int k = 0; k < BK / UMMA_K; ++k) {
+              const uint64_t ad = A_MN ? sdesc_sw128(sa + k * 2048, 8192, 1024) : sdesc_sw128(sa + k * 32, 16, 1024);
+              const uint64_t bd = B_MN ? sdesc_sw128(sb + k * 2048, 8192, 1024) : sdesc_sw128(sb + k * 32, 16, 1024);
+              umma_bf16_pair(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
+            }
+            issued_any = true;
+            umma_commit_pair_multicast(&empty[stage], 0x3);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (!ok) break;
+          umma_commit_pair_multicast(&tfull[acc], 0x3);
+        }
+        // every MMA this thread issued has completed before TMEM is freed
+        if (issued_any) {
+          umma_commit_pair_local(drain);
+          if (!mbar_wait_timeout(drain, 0, ctl.timeout_ns)) atomicOr(ctl.status, DEV_ERR_TIMEOUT_DRAIN);
+        }
+      } else {
+        // ------------------------------------------------------------ relay
+        const uint32_t leader_peer_full = mapa_shared(smem_u32(peer_full), 0);
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        bool skip = false;  // the test hook only touches the leader's stage
+        (void)skip;
+        for (int t = cluster_id; t < num_tiles && ok; t += num_clusters) {
+          for (int kb = 0; kb < sh.num_kb; ++kb) {
+            if (!mbar_wait_bounded(&full[stage], phase, abort_flag, ctl.timeout_ns)) {
+              if (!*abort_flag) raise_error(ctl, abort_flag, DEV_ERR_TIMEOUT_MMA);
+              ok = false;
+              break;
+            }
+            mbar_arrive_cluster(leader_peer_full + static_cast<uint32_t>(stage * 8));
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------- epilogue
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const uint32_t leader_tempty = mapa_shared(smem_u32(tempty), 0);
+    int it = 0;
+    for (int t = cluster_id; t < num_tiles; t += num_clusters, ++it) {
+      int tm, tn;
+      tile_coords(t, sh, tm, tn);
+      const int acc = it & 1;
+      const uint32_t acc_phase = (it >> 1) & 1;
+      bool ok = mbar_wait_bounded(&tfull[acc], acc_phase, abort_flag, ctl.timeout_ns);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) {
+        if (lane == 0 && !*abort_flag) raise_error(ctl, abort_flag, DEV_ERR_TIMEOUT_EPILOGUE);
+        break;
+      }
+      tc_fence_after();
+      EpiCtx c;
+      c.M = sh.M;
+      c.N = sh.N;
+      c.tm = tm * 2 + static_cast<int>(rank);
+      c.tn = tn;
+      c.row = row;
+      c.m = c.tm * 128 + row;
+      c.quad = quad;
+      c.lane = lane;
+      c.taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      Epi::template run<BN>(ep, c);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(leader_tempty + static_cast<uint32_t>(acc * 8));
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  // both CTAs done with the pair's TMEM and with each other's barriers
+  cluster_sync_all();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, L::TMEM_COLS);
+  }
+}
+
+}  // namespace coda

@@ -91,6 +91,13 @@ coda_status_t coda_sync_status(coda_handle_t h, void* stream, int32_t* device_bi
  * 0 restores the default. */
 coda_status_t coda_set_wait_timeout_ns(coda_handle_t h, uint64_t ns);
 
+/* GEMM kernel form for every later call on this handle.  enable = 1 (the
+ * default): each 256 x 256 output tile is computed by a pair of SMs with the
+ * 2-SM tcgen05 MMA, each SM loading half of the operands; enable = 0: one SM
+ * per 128 x 256 tile.  Results are identical up to fp32 summation order
+ * inside the tensor core; the choice only affects speed. */
+coda_status_t coda_set_sm_pairing(coda_handle_t h, int enable);
+
 /* Failure-detection test hook.  While enabled, every GEMM launched through
  * this handle leaves the first shared-memory stage of its first CTA unfilled,
  * so that CTA's MMA wait cannot complete and must hit the wait limit: the

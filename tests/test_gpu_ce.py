@@ -17,6 +17,13 @@ pytestmark = pytest.mark.gpu
 C = pytest.importorskip("gemm_epilogue_transformer_tma_gb300")
 
 
+@pytest.fixture(params=[True, False], ids=["sm_pair", "single_sm"])
+def pairing(request):
+    C.coda_set_sm_pairing(request.param)
+    yield request.param
+    C.coda_set_sm_pairing(True)
+
+
 def run_ce(H, Wt, labels, grads=True):
     M, d = H.shape
     V = Wt.shape[0]
@@ -44,7 +51,7 @@ def check_argmax(gpu_am, H, Wt, tol_gap=1e-3):
 
 
 @pytest.mark.parametrize("M,d,V", [(200, 136, 1000), (128, 64, 256), (37, 256, 40000)])
-def test_ce_parity(M, d, V):
+def test_ce_parity(M, d, V, pairing):
     s = CEShape("t", M, d, V)
     x = {k: v.cuda() for k, v in ce_inputs(s, 0).items()}
     o = run_ce(x["H"], x["Wt"], x["labels"])

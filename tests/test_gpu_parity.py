@@ -31,6 +31,14 @@ SHAPES = {
 }
 
 
+@pytest.fixture(params=[True, False], ids=["sm_pair", "single_sm"])
+def pairing(request):
+    """Run the test with the 2-SM pair GEMM kernel and with the 1-SM one."""
+    C.coda_set_sm_pairing(request.param)
+    yield request.param
+    C.coda_set_sm_pairing(True)
+
+
 def dev_inputs(s, seed=0):
     return {k: v.cuda() for k, v in block_inputs(s, seed, "cpu", with_dy=s.swiglu).items()}
 
@@ -41,7 +49,7 @@ def dev_inputs(s, seed=0):
 
 @pytest.mark.parametrize("a_mn,b_mn", [(False, False), (False, True), (True, True)])
 @pytest.mark.parametrize("M,N,K", [(200, 328, 136), (128, 256, 64), (8, 8, 8), (520, 776, 1000)])
-def test_gemm_layouts(a_mn, b_mn, M, N, K):
+def test_gemm_layouts(a_mn, b_mn, M, N, K, pairing):
     # fan-in scaled operands (as in the block workloads) so outputs are O(1)
     # and the elementwise bar's 1e-3 floor is on the data's own scale
     g = torch.Generator().manual_seed(M * 7 + N + K)
@@ -55,7 +63,7 @@ def test_gemm_layouts(a_mn, b_mn, M, N, K):
     assert_elem(Cd, O.matmul_nt(f64(A), f64(B)), "C")
 
 
-def test_gemm_row_and_col_scale():
+def test_gemm_row_and_col_scale(pairing):
     M, N, K = 264, 264, 192
     g = torch.Generator().manual_seed(5)
     A = torch.randn(M, K, generator=g).to(torch.bfloat16)
@@ -94,7 +102,7 @@ def check_forward(s: BlockShape, b: BlockBuffers, x: dict):
 
 
 @pytest.mark.parametrize("name", ["ragged", "whole", "one_row"])
-def test_forward_parity(name):
+def test_forward_parity(name, pairing):
     s = SHAPES[name]
     x = dev_inputs(s)
     b = BlockBuffers(x, swiglu=True, backward=False)
@@ -103,7 +111,7 @@ def test_forward_parity(name):
     check_forward(s, b, x)
 
 
-def test_tiny_config_plain():
+def test_tiny_config_plain(pairing):
     """configs[0]-style tiny problem: X[256,512], W1, W2 [512,512], PLAIN
     epilogue (row scale only), outputs h, rstd, out[256,512]."""
     x = dev_inputs(TINY)
@@ -132,7 +140,7 @@ def check_backward_stages(s, b, x):
 
 
 @pytest.mark.parametrize("name", ["ragged", "whole", "one_row"])
-def test_backward_stage_parity(name):
+def test_backward_stage_parity(name, pairing):
     s = SHAPES[name]
     x = dev_inputs(s)
     b = BlockBuffers(x)
@@ -169,7 +177,7 @@ def test_composite_backward_equals_stages_and_is_deterministic():
             assert torch.equal(getattr(a, k), v), k
 
 
-def test_unfused_ablation_matches_oracle():
+def test_unfused_ablation_matches_oracle(pairing):
     s = SHAPES["ragged"]
     x = dev_inputs(s)
     b = BlockBuffers(x, unfused=True)

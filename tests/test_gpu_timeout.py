@@ -27,8 +27,10 @@ def _gemm(M, N, K, seed):
     return A, B, Cd
 
 
-def test_expired_wait_is_reported_and_the_context_survives():
+@pytest.mark.parametrize("pair", [True, False], ids=["sm_pair", "single_sm"])
+def test_expired_wait_is_reported_and_the_context_survives(pair):
     assert_device_ok()
+    C.coda_set_sm_pairing(pair)
     C.coda_set_wait_timeout_ns(50_000_000)  # 50 ms
     C.coda_debug_skip_first_stage(True)
     try:
@@ -37,12 +39,15 @@ def test_expired_wait_is_reported_and_the_context_survives():
     finally:
         C.coda_debug_skip_first_stage(False)
         C.coda_set_wait_timeout_ns(0)
+        C.coda_set_sm_pairing(True)
     assert st == 6, f"expected CODA_ERR_TIMEOUT, got {C.STATUS_NAMES.get(st)} bits={bits:#x}"
     # the MMA warp waits on the unfilled stage, and the producer waits for the
     # MMA to release it: whichever limit is noticed first raises the abort
     assert bits & TIMEOUT_BITS, f"a bounded wait should have expired (bits={bits:#x})"
     assert not bits & DRAIN_BIT, f"in-flight copies did not drain (bits={bits:#x})"
     # the status word was cleared by the read, and the context still works
+    C.coda_set_sm_pairing(pair)
     A, B, Cd = _gemm(264, 520, 200, 2)
+    C.coda_set_sm_pairing(True)
     assert_device_ok()
     assert_elem(Cd, O.matmul_nt(f64(A), f64(B)), "C after timeout")
