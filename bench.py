@@ -262,6 +262,8 @@ def main():
     ap.add_argument("--impl", default="fused", choices=["fused", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip ablation, LM-head and e2e legs")
+    ap.add_argument("--single-sm", action="store_true",
+                    help="GEMMs on one SM per tile instead of SM pairs")
     ap.add_argument("--tokens", type=int, default=0,
                     help="override the token count M (smaller cases for profiler captures)")
     args = ap.parse_args()
@@ -287,6 +289,7 @@ def main():
     import gemm_epilogue_transformer_tma_gb300 as C
     from gemm_epilogue_transformer_tma_gb300.path import BlockBuffers
     peaks = load_peaks()
+    C.coda_set_sm_pairing(not args.single_sm)
 
     x = block_inputs(shape, seed=rank, device="cuda")
     b = BlockBuffers(x)
@@ -371,6 +374,7 @@ def main():
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1)/N(0,0.02)/U(0.5,1.5))",
             "config": {"workload": shape.name, "M": shape.M, "K1": shape.K1, "d": shape.d, "ffn": shape.N2 // 2,
                        "eps": shape.eps, "parallelism": "replicas" if world > 1 else "single-gpu",
+                       "gemm": "1-SM tiles" if args.single_sm else "SM-pair tiles",
                        "l2": "inputs larger than L2 (W2 alone is %d MB), no flush" % (shape.N2 * shape.d * 2 >> 20)},
             "pct_of_peak": 100.0 * value / world / peak,
             "pct_of_sustained_peak": 100.0 * value / world / peaks["bf16_tflops_sustained"],

@@ -9,19 +9,19 @@
 // unchanged (EpiCtx.tm is the 128-row block index).
 //
 // Roles, per CTA of the pair (rank 0 = leader, rank 1 = peer):
-//   warp 0       TMA producer for this CTA's halves; completion on this
-//                CTA's own full[] barrier.
-//   warp 1       leader: MMA issuer.  It waits for its own full[s] and for
-//                peer_full[s] (the peer's relay), issues the 2-SM MMAs, and
-//                commits to empty[s] / tfull[] of both CTAs (multicast).
-//                peer: relay -- waits for its own full[s] and arrives on the
-//                leader's peer_full[s].  Both CTAs' warp 1 allocate TMEM
-//                together (cta_group::2).
+//   warp 0       TMA producer for this CTA's halves.  Both CTAs' copies of a
+//                stage complete on the leader's full[s] barrier, which the
+//                leader arms for the bytes of both halves.
+//   warp 1       leader: MMA issuer.  It waits for full[s], issues the 2-SM
+//                MMAs, and commits to empty[s] / tfull[] of both CTAs
+//                (multicast).  Both CTAs' warp 1 allocate TMEM together
+//                (cta_group::2).
 //   warps 2..5   epilogue on this CTA's 128 rows; release the accumulator by
 //                arriving on the leader's tempty[].
-// Every copy completes on a barrier of the CTA that issued it, so each CTA
-// can always wait for its own copies on the way out.  All waits are bounded
-// as in the 1-SM kernel.
+// All waits are bounded as in the 1-SM kernel.  After an abort the leader
+// waits (bounded) for every stage it armed, which counts the peer's bytes
+// too; the peer cannot observe its own copies, so it waits a fixed grace
+// period far longer than a copy's latency before releasing its memory.
 #pragma once
 
 #include "gemm_tc.cuh"
@@ -40,7 +40,7 @@ struct Gemm2Smem {
   static constexpr int TOTAL = RING_BYTES + BAR_BYTES + 1024;
   static constexpr int TMEM_COLS = 2 * BN;
   static_assert(TMEM_COLS <= 512, "TMEM has 512 columns");
-  static_assert((3 * STAGES + 5) * 8 + 8 <= BAR_BYTES, "barrier area too small");
+  static_assert((2 * STAGES + 5) * 8 + 8 <= BAR_BYTES, "barrier area too small");
   static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "1 KB aligned halves");
 };
 
@@ -57,9 +57,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::RING_BYTES);
-  uint64_t* peer_full = full + STAGES;  // leader only: the peer's stage s has landed
-  uint64_t* empty = peer_full + STAGES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::RING_BYTES);  // leader's counts both halves
+  uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;  // leader only: both CTAs' epilogues released the buffer
   uint64_t* drain = tempty + 2;
@@ -76,7 +75,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&peer_full[s], 1);
       mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -106,9 +104,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA
     if (lane == 0) {
+      const uint32_t leader_full = mapa_shared(smem_u32(full), 0);
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t pending = 0, parity = 0;
+      uint32_t pending = 0, parity = 0;  // leader: stages it armed
       bool ok = true;
       bool skip = ctl.skip_first_stage != 0 && cluster_id == 0 && leader;
       for (int t = cluster_id; t < num_tiles && ok; t += num_clusters) {
@@ -122,30 +121,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
             break;
           }
           if (skip) {
-            skip = false;  // test hook: leave this stage unfilled
+            skip = false;  // test hook: the leader never arms this stage
           } else {
             uint8_t* sa = smem + stage * L::STAGE_BYTES;
             uint8_t* sb = sa + L::A_BYTES;
-            mbar_arrive_expect_tx(&full[stage], L::STAGE_BYTES);
+            const uint32_t bar = leader_full + static_cast<uint32_t>(stage * 8);
+            if (leader) {
+              mbar_arrive_expect_tx(&full[stage], 2 * L::STAGE_BYTES);
+              pending |= 1u << stage;
+              parity = (parity & ~(1u << stage)) | (phase << stage);
+            }
             if (!A_MN) {
-              tma_load_2d(sa, &tmA, &full[stage], kb * BK, m0);
+              tma_load_2d_pair(sa, &tmA, bar, kb * BK, m0);
             } else {
-              tma_load_2d(sa, &tmA, &full[stage], m0, kb * BK);
-              tma_load_2d(sa + 8192, &tmA, &full[stage], m0 + 64, kb * BK);
+              tma_load_2d_pair(sa, &tmA, bar, m0, kb * BK);
+              tma_load_2d_pair(sa + 8192, &tmA, bar, m0 + 64, kb * BK);
             }
             if (B_DUAL) {
               // leader: gate rows of the tile, peer: the matching up rows
-              tma_load_2d(sb, leader ? &tmB : &tmB2, &full[stage], kb * BK, tn * HB);
+              tma_load_2d_pair(sb, leader ? &tmB : &tmB2, bar, kb * BK, tn * HB);
             } else if (!B_MN) {
-              tma_load_2d(sb, &tmB, &full[stage], kb * BK, tn * BN + static_cast<int>(rank) * HB);
+              tma_load_2d_pair(sb, &tmB, bar, kb * BK, tn * BN + static_cast<int>(rank) * HB);
             } else {
 #pragma unroll
               for (int i = 0; i < HB / 64; ++i)
-                tma_load_2d(sb + i * 8192, &tmB, &full[stage], tn * BN + static_cast<int>(rank) * HB + i * 64,
-                            kb * BK);
+                tma_load_2d_pair(sb + i * 8192, &tmB, bar, tn * BN + static_cast<int>(rank) * HB + i * 64, kb * BK);
             }
-            pending |= 1u << stage;
-            parity = (parity & ~(1u << stage)) | (phase << stage);
           }
           if (++stage == STAGES) {
             stage = 0;
@@ -154,10 +155,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
         }
       }
       if (!ok) {
-        for (int st = 0; st < STAGES; ++st)
-          if ((pending >> st) & 1u)
-            if (!mbar_wait_timeout(&full[st], (parity >> st) & 1u, ctl.timeout_ns))
-              atomicOr(ctl.status, DEV_ERR_TIMEOUT_DRAIN);
+        if (leader) {
+          for (int st = 0; st < STAGES; ++st)
+            if ((pending >> st) & 1u)
+              if (!mbar_wait_timeout(&full[st], (parity >> st) & 1u, ctl.timeout_ns))
+                atomicOr(ctl.status, DEV_ERR_TIMEOUT_DRAIN);
+        } else {
+          // the peer's copies complete on the leader's barrier: give any that
+          // are still in flight a grace period (copies take microseconds)
+          const uint64_t t0 = globaltimer_ns();
+          while (globaltimer_ns() - t0 < 2000000ull) {
+          }
+        }
       }
     }
   } else if (warp == 1) {
@@ -180,8 +189,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
           for (int kb = 0; kb < sh.num_kb; ++kb) {
-            if (!mbar_wait_bounded(&full[stage], phase, abort_flag, ctl.timeout_ns) ||
-                !mbar_wait_bounded_cluster(&peer_full[stage], phase, abort_flag, ctl.timeout_ns)) {
+            if (!mbar_wait_bounded_cluster(&full[stage], phase, abort_flag, ctl.timeout_ns)) {
               if (!*abort_flag) raise_error(ctl, abort_flag, DEV_ERR_TIMEOUT_MMA);
               ok = false;
               break;
@@ -209,28 +217,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
         if (issued_any) {
           umma_commit_pair_local(drain);
           if (!mbar_wait_timeout(drain, 0, ctl.timeout_ns)) atomicOr(ctl.status, DEV_ERR_TIMEOUT_DRAIN);
-        }
-      } else {
-        // ------------------------------------------------------------ relay
-        const uint32_t leader_peer_full = mapa_shared(smem_u32(peer_full), 0);
-        int stage = 0;
-        uint32_t phase = 0;
-        bool ok = true;
-        bool skip = false;  // the test hook only touches the leader's stage
-        (void)skip;
-        for (int t = cluster_id; t < num_tiles && ok; t += num_clusters) {
-          for (int kb = 0; kb < sh.num_kb; ++kb) {
-            if (!mbar_wait_bounded(&full[stage], phase, abort_flag, ctl.timeout_ns)) {
-              if (!*abort_flag) raise_error(ctl, abort_flag, DEV_ERR_TIMEOUT_MMA);
-              ok = false;
-              break;
-            }
-            mbar_arrive_cluster(leader_peer_full + static_cast<uint32_t>(stage * 8));
-            if (++stage == STAGES) {
-              stage = 0;
-              phase ^= 1u;
-            }
-          }
         }
       }
     }
