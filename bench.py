@@ -43,6 +43,36 @@ UNIT = "TFLOP/s"
 CONFIGS = {"7b": B7, "70b": B70}
 
 
+KERNEL_SOURCES = ["ptx.cuh", "gemm_tc.cuh", "gemm_tc2.cuh", "gemm_launch.cuh", "gemm_fwd.cu", "gemm_bwd.cu"]
+
+
+def kernel_sources_sha256():
+    import hashlib
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "gemm_epilogue_transformer_tma_gb300", "csrc")
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def measured_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch of `kernel` on `workload` from the ncu record in
+    profiles/traffic.txt, or None if there is none or the kernel sources have
+    changed since it was taken."""
+    p = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(p):
+        return None
+    sha = kernel_sources_sha256()
+    with open(p) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) == 4 and not line.startswith("#") and parts[0] == workload and parts[1] == kernel \
+                    and parts[3] == sha:
+                return float(parts[2])
+    return None
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -381,7 +411,7 @@ def main():
             "peak": {"used": peak_kind, "bf16_tflops_burst": peaks["bf16_tflops"],
                      "bf16_tflops_sustained": peaks["bf16_tflops_sustained"], "source": peaks["source"]},
             "roofline": {"kernel": dom, "bound": "tensor", "achieved": dom_ach, "peak": peak, "unit": "TFLOP/s",
-                         "frac": dom_ach / peak, "traffic": None,
+                         "frac": dom_ach / peak, "traffic": measured_traffic(shape.name, dom),
                          "note": "peak = %s bf16 of %s (SM clock %s of max %s MHz)" % (
                              peak_kind, peaks["source"], clocks.get("sm_mhz"), clocks.get("sm_max_mhz"))},
             "stage_ms": stage_ms,
