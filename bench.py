@@ -36,11 +36,11 @@ sys.path.insert(0, ROOT)
 
 import torch  # noqa: E402
 
-from coda_inputs import B7, B70, LMHEAD, BlockShape, block_inputs, ce_inputs  # noqa: E402
+from coda_inputs import B1, B7, B70, LMHEAD, BlockShape, block_inputs, ce_inputs  # noqa: E402
 
 METRIC = "fused GEMM-RMSNorm-GEMM fwd+bwd TFLOP/s and % of GB300 bf16 dense peak"
 UNIT = "TFLOP/s"
-CONFIGS = {"7b": B7, "70b": B70}
+CONFIGS = {"7b": B7, "70b": B70, "1b": B1}  # 1b: forward only
 
 
 KERNEL_SOURCES = ["ptx.cuh", "gemm_tc.cuh", "gemm_tc2.cuh", "gemm_launch.cuh", "gemm_fwd.cu", "gemm_bwd.cu"]
@@ -170,6 +170,21 @@ class FusedStep:
         ]
 
 
+def max_over_ranks(ms: float, dist=None, device="cpu") -> float:
+    """The slowest rank's time per step (every rank calls this)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_value(step_flops: float, ms: float, world: int) -> float:
+    """Whole-job TFLOP/s: every rank runs one independent replica of the step
+    (weak scaling), timed by the slowest rank."""
+    return world * step_flops / (ms * 1e-3) / 1e12
+
+
 def time_steps(calls, steps, warmup, stage_events=True):
     """Run warmup + timed steps; return (total_ms, per-stage ms lists)."""
     stream = torch.cuda.current_stream()
@@ -272,15 +287,59 @@ def bench_lmhead(C, steps, warmup):
     return out
 
 
-def e2e_step(C, b, host, stream):
-    """Public-API step with host buffers: H2D of the step's activations and
-    upstream gradient from pinned memory, the fused fwd+bwd, D2H of dX."""
-    b.X.copy_(host["X"], non_blocking=True)
-    b.R.copy_(host["R"], non_blocking=True)
-    b.dY.copy_(host["dY"], non_blocking=True)
-    b.forward()
-    b.backward()
-    host["dX"].copy_(b.dX, non_blocking=True)
+class E2EPipeline:
+    """The fused step through the public API with host buffers, as a training
+    loop would drive it: each step's activations and upstream gradient are
+    copied from pinned host memory and its dX is read back, with two device
+    buffer sets so that step i+1's H2D copy and step i's D2H read overlap
+    step i's compute (separate copy streams, event-ordered)."""
+
+    def __init__(self, C, b0, host):
+        from gemm_epilogue_transformer_tma_gb300.path import BlockBuffers
+        self.host = host
+        shared = {k: getattr(b0, k) for k in ("W1t", "g", "W2t")}
+        second = dict(shared, X=torch.empty_like(b0.X), R=torch.empty_like(b0.R))
+        if b0.with_backward:
+            second["dY"] = torch.empty_like(b0.dY)
+        self.bufs = [b0, BlockBuffers(second, backward=b0.with_backward)]
+        self.inputs = ("X", "R", "dY") if b0.with_backward else ("X", "R")
+        self.result = "dX" if b0.with_backward else "out"
+        self.compute = torch.cuda.current_stream()
+        self.h2d = torch.cuda.Stream()
+        self.d2h = torch.cuda.Stream()
+        ev = lambda: [torch.cuda.Event(), torch.cuda.Event()]  # noqa: E731
+        self.ev_in, self.ev_comp, self.ev_out = ev(), ev(), ev()
+        self.fresh = [True, True]
+
+    def _load(self, slot):
+        b = self.bufs[slot]
+        with torch.cuda.stream(self.h2d):
+            if not self.fresh[slot]:
+                self.h2d.wait_event(self.ev_comp[slot])  # the previous step on this slot read it
+            for k in self.inputs:
+                getattr(b, k).copy_(self.host[k], non_blocking=True)
+            self.ev_in[slot].record(self.h2d)
+
+    def run(self, n):
+        self._load(0)
+        for i in range(n):
+            slot = i & 1
+            b = self.bufs[slot]
+            self.compute.wait_event(self.ev_in[slot])
+            if not self.fresh[slot]:
+                self.compute.wait_event(self.ev_out[slot])  # dX of step i-2 read back
+            b.forward()
+            if b.with_backward:
+                b.backward()
+            self.ev_comp[slot].record(self.compute)
+            self.fresh[slot] = False
+            if i + 1 < n:
+                self._load(slot ^ 1)
+            with torch.cuda.stream(self.d2h):
+                self.d2h.wait_event(self.ev_comp[slot])
+                self.host[self.result].copy_(getattr(b, self.result), non_blocking=True)
+                self.ev_out[slot].record(self.d2h)
+        torch.cuda.synchronize()
 
 
 def main():
@@ -301,7 +360,8 @@ def main():
         args.warmup = 3
     shape = CONFIGS[args.config]
     if args.tokens:
-        shape = BlockShape(f"{shape.name}_m{args.tokens}", args.tokens, shape.K1, shape.d, shape.N2)
+        shape = BlockShape(f"{shape.name}_m{args.tokens}", args.tokens, shape.K1, shape.d, shape.N2,
+                           backward=shape.backward)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -322,9 +382,9 @@ def main():
     C.coda_set_sm_pairing(not args.single_sm)
 
     x = block_inputs(shape, seed=rank, device="cuda")
-    b = BlockBuffers(x)
+    b = BlockBuffers(x, backward=shape.backward)
     fs = FusedStep(C, b)
-    calls = fs.calls()
+    calls = fs.calls() if shape.backward else fs.calls()[:4]
 
     def barrier():
         if dist is not None:
@@ -342,15 +402,11 @@ def main():
     st, bits = C.coda_sync_status()
     if st != 0:
         raise RuntimeError(f"device status {C.STATUS_NAMES.get(st)} bits={bits:#x}")
-    ms = total_ms / args.steps
-    if dist is not None:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = t.item()
-    step_flops = shape.fwdbwd_flops()
-    value = world * step_flops / (ms * 1e-3) / 1e12
-    stage_ms = {name: statistics.mean(per[i]) for i, name in enumerate(FusedStep.STAGES)}
-    dom = max(fs.flops, key=lambda k: stage_ms[k])
+    ms = max_over_ranks(total_ms / args.steps, dist, "cuda")
+    step_flops = shape.fwdbwd_flops() if shape.backward else shape.fwd_flops()
+    value = aggregate_value(step_flops, ms, world)
+    stage_ms = {name: statistics.mean(per[i]) for i, name in enumerate(FusedStep.STAGES[:len(calls)])}
+    dom = max((k for k in fs.flops if k in stage_ms), key=lambda k: stage_ms[k])
     dom_ach = fs.flops[dom] / (stage_ms[dom] * 1e-3) / 1e12
     clocks = clk.summary()
     # The peak that matches the conditions the kernels ran under: the burst
@@ -365,8 +421,8 @@ def main():
     extras = {}
     if not args.no_extras and rank == 0:
         # unfused ablation, same workload and timing rules
-        bu = BlockBuffers(x, unfused=True)
-        ucalls = [bu.forward_unfused, bu.backward_unfused]
+        bu = BlockBuffers(x, unfused=True, backward=shape.backward)
+        ucalls = [bu.forward_unfused, bu.backward_unfused] if shape.backward else [bu.forward_unfused]
         u_ms, _ = time_steps(ucalls, max(3, args.steps // 2), args.warmup, stage_events=False)
         u_ms /= max(3, args.steps // 2)
         extras["ablation_unfused"] = {"ms_per_step": u_ms, "tflops": step_flops / (u_ms * 1e-3) / 1e12,
@@ -374,25 +430,26 @@ def main():
         del bu
         torch.cuda.empty_cache()
         # end to end through the public API with host buffers
-        host = {k: torch.empty_like(x[k], device="cpu").pin_memory() for k in ("X", "R", "dY")}
+        ins = ("X", "R", "dY") if shape.backward else ("X", "R")
+        res = "dX" if shape.backward else "out"
+        host = {k: torch.empty_like(x[k], device="cpu").pin_memory() for k in ins}
         for k in host:
             host[k].copy_(x[k])
-        host["dX"] = torch.empty_like(b.dX, device="cpu").pin_memory()
-        stream = torch.cuda.current_stream()
-        for _ in range(2):
-            e2e_step(C, b, host, stream)
-        torch.cuda.synchronize()
+        host[res] = torch.empty_like(getattr(b, res), device="cpu").pin_memory()
+        pipe = E2EPipeline(C, b, host)
+        pipe.run(3)
         n_e2e = max(3, args.steps // 2)
-        t0 = time.perf_counter()
-        for _ in range(n_e2e):
-            e2e_step(C, b, host, stream)
         torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        pipe.run(n_e2e)
         e2e_ms = (time.perf_counter() - t0) * 1e3 / n_e2e
-        h2d = sum(host[k].numel() * host[k].element_size() for k in ("X", "R", "dY"))
-        d2h = host["dX"].numel() * host["dX"].element_size()
+        h2d = sum(host[k].numel() * host[k].element_size() for k in ins)
+        d2h = host[res].numel() * host[res].element_size()
         extras["e2e"] = {"value": step_flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e2e_ms,
-                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
-        del host
+                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                         "timing": "host wall clock over the whole run, synchronize at both ends; copies of "
+                                   "step i+1 (H2D) and i (D2H) overlap step i's compute"}
+        del host, pipe
         del b, x, fs, calls
         torch.cuda.empty_cache()
         extras["lmhead_ce"] = bench_lmhead(C, args.steps, args.warmup)
