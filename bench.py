@@ -138,36 +138,48 @@ class ClockSampler:
 
 # ---------------------------------------------------------------------------
 class FusedStep:
-    """The fused path's calls with CUDA events between stages."""
-    STAGES = ["fold", "gemm1_res_prms", "rstd_combine", "gemm2_rowscale_swiglu", "swiglu_bwd",
-              "dgrad2_rmsbwd", "dg_combine", "wgrad2_gscale", "dgrad1", "wgrad1"]
+    """The fused path's calls (stage name, call); CUDA events go between them.
+    With fuse_rstd the light combine runs inside GEMM2's epilogue."""
 
-    def __init__(self, C, b):
+    def __init__(self, C, b, fuse_rstd=False):
         self.C, self.b = C, b
         s = b
+        gemm2 = "gemm2_prms_rowscale_swiglu" if fuse_rstd else "gemm2_rowscale_swiglu"
         self.flops = {
             "gemm1_res_prms": 2.0 * s.M * s.d * s.K1,
-            "gemm2_rowscale_swiglu": 2.0 * s.M * s.N2 * s.d,
+            gemm2: 2.0 * s.M * s.N2 * s.d,
             "dgrad2_rmsbwd": 2.0 * s.M * s.N2 * s.d,
             "wgrad2_gscale": 2.0 * s.M * s.N2 * s.d,
             "dgrad1": 2.0 * s.M * s.d * s.K1,
             "wgrad1": 2.0 * s.M * s.d * s.K1,
         }
+        fwd = [
+            ("fold", lambda: C.coda_fold_rmsnorm_weight(b.W2t, b.g, b.W2gt)),
+            ("gemm1_res_prms", lambda: C.coda_gemm_res_prms(b.X, b.W1t, b.R, b.H, b.psum)),
+        ]
+        if fuse_rstd:
+            fwd.append((gemm2, lambda: C.coda_gemm_prms_rowscale_swiglu(b.H, b.W2gt, b.psum, b.eps, b.rstd, b.out,
+                                                                        b.z, C.CODA_EPI_SWIGLU)))
+        else:
+            fwd += [
+                ("rstd_combine", lambda: C.coda_rstd_combine(b.psum, b.d, b.eps, b.rstd)),
+                (gemm2, lambda: C.coda_gemm_rowscale_swiglu(b.H, b.W2gt, b.rstd, b.out, b.z, C.CODA_EPI_SWIGLU)),
+            ]
+        bwd = [
+            ("swiglu_bwd", lambda: C.coda_swiglu_bwd(b.dY, b.z, b.rstd, b.dP, b.c, b.d)),
+            ("dgrad2_rmsbwd", lambda: C.coda_gemm_dgrad_rmsbwd(b.dP, b.W2t, b.H, b.g, b.c, b.dH, b.dgpart)),
+            ("dg_combine", lambda: C.coda_dg_combine(b.dgpart, b.dg)),
+            ("wgrad2_gscale", lambda: C.coda_gemm_wgrad_gscale(b.H, b.dP, b.g, b.dW2t)),
+            ("dgrad1", lambda: C.coda_gemm(b.dH, False, b.W1t, True, b.dX, b.M, b.K1, b.d)),
+            ("wgrad1", lambda: C.coda_gemm(b.dH, True, b.X, True, b.dW1t, b.d, b.K1, b.M)),
+        ]
+        self.stages = fwd + (bwd if b.with_backward else [])
+
+    def names(self):
+        return [n for n, _ in self.stages]
 
     def calls(self):
-        C, b = self.C, self.b
-        return [
-            lambda: C.coda_fold_rmsnorm_weight(b.W2t, b.g, b.W2gt),
-            lambda: C.coda_gemm_res_prms(b.X, b.W1t, b.R, b.H, b.psum),
-            lambda: C.coda_rstd_combine(b.psum, b.d, b.eps, b.rstd),
-            lambda: C.coda_gemm_rowscale_swiglu(b.H, b.W2gt, b.rstd, b.out, b.z, C.CODA_EPI_SWIGLU),
-            lambda: C.coda_swiglu_bwd(b.dY, b.z, b.rstd, b.dP, b.c, b.d),
-            lambda: C.coda_gemm_dgrad_rmsbwd(b.dP, b.W2t, b.H, b.g, b.c, b.dH, b.dgpart),
-            lambda: C.coda_dg_combine(b.dgpart, b.dg),
-            lambda: C.coda_gemm_wgrad_gscale(b.H, b.dP, b.g, b.dW2t),
-            lambda: C.coda_gemm(b.dH, False, b.W1t, True, b.dX, b.M, b.K1, b.d),
-            lambda: C.coda_gemm(b.dH, True, b.X, True, b.dW1t, b.d, b.K1, b.M),
-        ]
+        return [f for _, f in self.stages]
 
 
 def max_over_ranks(ms: float, dist=None, device="cpu") -> float:
@@ -301,7 +313,7 @@ class E2EPipeline:
         second = dict(shared, X=torch.empty_like(b0.X), R=torch.empty_like(b0.R))
         if b0.with_backward:
             second["dY"] = torch.empty_like(b0.dY)
-        self.bufs = [b0, BlockBuffers(second, backward=b0.with_backward)]
+        self.bufs = [b0, BlockBuffers(second, backward=b0.with_backward, fuse_rstd=b0.fuse_rstd)]
         self.inputs = ("X", "R", "dY") if b0.with_backward else ("X", "R")
         self.result = "dX" if b0.with_backward else "out"
         self.compute = torch.cuda.current_stream()
@@ -351,6 +363,8 @@ def main():
     ap.add_argument("--impl", default="fused", choices=["fused", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip ablation, LM-head and e2e legs")
+    ap.add_argument("--fuse-rstd", action="store_true",
+                    help="fold the rstd combine into GEMM2's epilogue (one launch fewer)")
     ap.add_argument("--single-sm", action="store_true",
                     help="GEMMs on one SM per tile instead of SM pairs")
     ap.add_argument("--tokens", type=int, default=0,
@@ -382,9 +396,9 @@ def main():
     C.coda_set_sm_pairing(not args.single_sm)
 
     x = block_inputs(shape, seed=rank, device="cuda")
-    b = BlockBuffers(x, backward=shape.backward)
-    fs = FusedStep(C, b)
-    calls = fs.calls() if shape.backward else fs.calls()[:4]
+    b = BlockBuffers(x, backward=shape.backward, fuse_rstd=args.fuse_rstd)
+    fs = FusedStep(C, b, fuse_rstd=args.fuse_rstd)
+    calls = fs.calls()
 
     def barrier():
         if dist is not None:
@@ -405,7 +419,7 @@ def main():
     ms = max_over_ranks(total_ms / args.steps, dist, "cuda")
     step_flops = shape.fwdbwd_flops() if shape.backward else shape.fwd_flops()
     value = aggregate_value(step_flops, ms, world)
-    stage_ms = {name: statistics.mean(per[i]) for i, name in enumerate(FusedStep.STAGES[:len(calls)])}
+    stage_ms = {name: statistics.mean(per[i]) for i, name in enumerate(fs.names())}
     dom = max((k for k in fs.flops if k in stage_ms), key=lambda k: stage_ms[k])
     dom_ach = fs.flops[dom] / (stage_ms[dom] * 1e-3) / 1e12
     clocks = clk.summary()
@@ -462,6 +476,7 @@ def main():
             "config": {"workload": shape.name, "M": shape.M, "K1": shape.K1, "d": shape.d, "ffn": shape.N2 // 2,
                        "eps": shape.eps, "parallelism": "replicas" if world > 1 else "single-gpu",
                        "gemm": "1-SM tiles" if args.single_sm else "SM-pair tiles",
+                       "rstd": "in GEMM2's epilogue" if args.fuse_rstd else "separate combine kernel",
                        "l2": "inputs larger than L2 (W2 alone is %d MB), no flush" % (shape.N2 * shape.d * 2 >> 20)},
             "pct_of_peak": 100.0 * value / world / peak,
             "pct_of_sustained_peak": 100.0 * value / world / peaks["bf16_tflops_sustained"],

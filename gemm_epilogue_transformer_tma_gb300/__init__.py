@@ -58,6 +58,7 @@ SIGNATURES = {
     "coda_gemm_res_prms": (_INT, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "coda_rstd_combine": (_INT, [_P, _P, _I64, _I64, _I64, _F32, _P, _P]),
     "coda_gemm_rowscale_swiglu": (_INT, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _U32, _P]),
+    "coda_gemm_prms_rowscale_swiglu": (_INT, [_P, _P, _P, _P, _I64, _F32, _P, _P, _P, _I64, _I64, _I64, _U32, _P]),
     "coda_swiglu_bwd": (_INT, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "coda_gemm_dgrad_rmsbwd": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "coda_gemm_dgrad_rmsbwd_noalloc": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
@@ -237,6 +238,27 @@ def coda_gemm_rowscale_swiglu(H, W2gt, rstd, out, z_save=None, flags=CODA_EPI_SW
                                                     _ptr(rstd, F32, "rstd"), _ptr(out, BF, "out"),
                                                     _ptr(z_save, BF, "z_save"), M, d, N2, flags, _stream(stream)),
            "coda_gemm_rowscale_swiglu")
+
+
+def coda_gemm_prms_rowscale_swiglu(H, W2gt, psum, eps, rstd, out, z_save=None, flags=CODA_EPI_SWIGLU,
+                                   stream=None):
+    """GEMM2 with the row scale derived from GEMM1's partial sums in its
+    epilogue (no separate combine launch); rstd may be None."""
+    M, d = H.shape
+    N2 = W2gt.shape[0]
+    T = psum.shape[1]
+    _shape(W2gt, (N2, d), "W2gt")
+    _shape(psum, (M, T), "psum")
+    if rstd is not None:
+        _shape(rstd, (M,), "rstd")
+    _shape(out, (M, N2 // 2 if flags == CODA_EPI_SWIGLU else N2), "out")
+    if z_save is not None:
+        _shape(z_save, (M, N2), "z_save")
+    _check(load_library().coda_gemm_prms_rowscale_swiglu(_h(H), _ptr(H, BF, "H"), _ptr(W2gt, BF, "W2gt"),
+                                                         _ptr(psum, F32, "psum"), T, eps, _ptr(rstd, F32, "rstd"),
+                                                         _ptr(out, BF, "out"), _ptr(z_save, BF, "z_save"),
+                                                         M, d, N2, flags, _stream(stream)),
+           "coda_gemm_prms_rowscale_swiglu")
 
 
 def coda_swiglu_bwd(dY, z, rstd, dP, c, d: int, stream=None):

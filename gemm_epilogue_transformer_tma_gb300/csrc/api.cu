@@ -273,6 +273,33 @@ coda_status_t coda_gemm_rowscale_swiglu(coda_handle_t h, const void* H, const vo
                                         static_cast<bf16*>(z_save), int(M), int(d), int(N2), swiglu));
 }
 
+coda_status_t coda_gemm_prms_rowscale_swiglu(coda_handle_t h, const void* H, const void* W2gt, const float* psum,
+                                             int64_t T, float eps, float* rstd, void* out, void* z_save, int64_t M,
+                                             int64_t d, int64_t N2, uint32_t flags, void* stream) {
+  CODA_TRY(Check()
+               .handle(h)
+               .rows(M)
+               .mptr(H, M)
+               .ptr(W2gt)
+               .mptr(psum, M)
+               .opt_ptr(rstd)
+               .mptr(out, M)
+               .opt_ptr(z_save)
+               .cols(d)
+               .cols(N2)
+               .st);
+  if (flags != CODA_EPI_SWIGLU && flags != CODA_EPI_PLAIN) return CODA_ERR_UNSUPPORTED;
+  const bool swiglu = flags == CODA_EPI_SWIGLU;
+  if (swiglu && (N2 / 2) % 8 != 0) return CODA_ERR_ALIGNMENT;
+  if (!swiglu && z_save != nullptr) return CODA_ERR_INVALID_ARG;
+  if (T <= 0 || T > kMaxExtent || !(eps >= 0.f)) return CODA_ERR_INVALID_ARG;
+  if (M == 0) return CODA_OK;
+  return from_cuda(gemm_rowscale_swiglu(ctx_of(h, stream), static_cast<const bf16*>(H),
+                                        static_cast<const bf16*>(W2gt), nullptr, static_cast<bf16*>(out),
+                                        static_cast<bf16*>(z_save), int(M), int(d), int(N2), swiglu, psum, int(T), eps,
+                                        rstd));
+}
+
 // ---------------------------------------------------------------------------
 coda_status_t coda_swiglu_bwd(coda_handle_t h, const void* dY, const void* z, const float* rstd, void* dP,
                               float* c, int64_t M, int64_t F, int64_t d, void* stream) {

@@ -26,6 +26,26 @@ struct LaunchCtx {
 bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t ld,
                     uint32_t box_inner, uint32_t box_outer);
 
+// Launch `kern` on c.stream with programmatic stream serialization: its
+// prologue may overlap the tail of the previous kernel in the stream.  Every
+// library kernel calls griddep_wait() before its first global-memory access,
+// so the ordering of memory effects is that of a plain stream launch.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_chained(const LaunchCtx& c, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                           Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = c.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // Handle accessors (api.cu), for translation units that only see the
 // opaque coda_handle_t.
 LaunchCtx launch_ctx_of_handle(void* handle, void* stream);
@@ -49,9 +69,13 @@ cudaError_t gemm_res_prms(const LaunchCtx& c, const __nv_bfloat16* X, const __nv
                           const __nv_bfloat16* R, __nv_bfloat16* H, float* psum, int M, int K1, int d, int T);
 
 // z = rstd * (H W2g); out = silu(z_gate) * z_up (swiglu) or z (plain).
+// With psum != null the row scale comes from the partial sums of squares
+// (1 / sqrt(sum_j psum / d + eps)) instead of rstd, and is also written to
+// rstd_out when that is not null.
 cudaError_t gemm_rowscale_swiglu(const LaunchCtx& c, const __nv_bfloat16* H, const __nv_bfloat16* W2gt,
                                  const float* rstd, __nv_bfloat16* out, __nv_bfloat16* zsave, int M, int d, int N2,
-                                 bool swiglu);
+                                 bool swiglu, const float* psum = nullptr, int T = 0, float eps = 0.f,
+                                 float* rstd_out = nullptr);
 
 // acc = dP W2^T; dH = g*acc - c*h; dgpart[4*tm+q, n] = sum_rows acc*h.
 cudaError_t gemm_dgrad_rms(const LaunchCtx& c, const __nv_bfloat16* dP, const __nv_bfloat16* W2t,

@@ -20,11 +20,12 @@ cudaError_t gemm_res_prms(const LaunchCtx& c, const __nv_bfloat16* X, const __nv
 
 cudaError_t gemm_rowscale_swiglu(const LaunchCtx& c, const __nv_bfloat16* H, const __nv_bfloat16* W2gt,
                                  const float* rstd, __nv_bfloat16* out, __nv_bfloat16* zsave, int M, int d, int N2,
-                                 bool swiglu) {
+                                 bool swiglu, const float* psum, int T, float eps, float* rstd_out) {
+  const float inv_d = 1.0f / static_cast<float>(d);
   CUtensorMap ta, tb, tb2;
   if (!swiglu) {
     if (!make_operand_maps(&ta, &tb, H, false, W2gt, false, M, N2, d, b_box_rows(c))) return cudaErrorInvalidValue;
-    EpiStore::Params ep{out, N2, rstd, nullptr};
+    EpiStore::Params ep{out, N2, rstd, nullptr, psum, T, inv_d, eps, rstd_out};
     return run_gemm<false, false, false, EpiStore>(c, ta, tb, tb, M, N2, d, (N2 + kBN - 1) / kBN, ep);
   }
   const int F = N2 / 2;
@@ -33,7 +34,7 @@ cudaError_t gemm_rowscale_swiglu(const LaunchCtx& c, const __nv_bfloat16* H, con
   // each half is zero-filled past its own end
   if (!make_tmap_bf16(&tb, W2gt, d, F, d, 64, kBN / 2)) return cudaErrorInvalidValue;
   if (!make_tmap_bf16(&tb2, W2gt + static_cast<int64_t>(F) * d, d, F, d, 64, kBN / 2)) return cudaErrorInvalidValue;
-  EpiRowscaleSwiglu::Params ep{rstd, out, F, zsave, N2, F};
+  EpiRowscaleSwiglu::Params ep{rstd, out, F, zsave, N2, F, psum, T, inv_d, eps, rstd_out};
   return run_gemm<false, false, true, EpiRowscaleSwiglu>(c, ta, tb, tb2, M, F, d, (F + kBN / 2 - 1) / (kBN / 2), ep);
 }
 
@@ -42,7 +43,7 @@ cudaError_t gemm_store(const LaunchCtx& c, const __nv_bfloat16* A, bool a_mn, co
                        const __nv_bfloat16* col_scale) {
   CUtensorMap ta, tb;
   if (!make_operand_maps(&ta, &tb, A, a_mn, B, b_mn, M, N, K, b_box_rows(c))) return cudaErrorInvalidValue;
-  EpiStore::Params ep{C, N, row_scale, col_scale};
+  EpiStore::Params ep{C, N, row_scale, col_scale, nullptr, 0, 0.f, 0.f, nullptr};
   const int tn = (N + kBN - 1) / kBN;
   if (!a_mn && !b_mn) return run_gemm<false, false, false, EpiStore>(c, ta, tb, tb, M, N, K, tn, ep);
   if (!a_mn && b_mn) return run_gemm<false, true, false, EpiStore>(c, ta, tb, tb, M, N, K, tn, ep);

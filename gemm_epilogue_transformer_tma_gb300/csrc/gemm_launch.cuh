@@ -29,8 +29,7 @@ cudaError_t launch_gemm_kernel(const LaunchCtx& c, const CUtensorMap& ta, const 
   KernelCtl ctl{c.status, c.timeout_ns, c.skip_first_stage};
   const int tiles = sh.tiles_m * sh.tiles_n;
   const int grid = std::max(1, std::min(tiles, c.num_sms));
-  kern<<<grid, GEMM_THREADS, L::TOTAL, c.stream>>>(ta, tb, tb2, sh, ctl, ep);
-  return cudaGetLastError();
+  return launch_chained(c, kern, dim3(grid), dim3(GEMM_THREADS), L::TOTAL, ta, tb, tb2, sh, ctl, ep);
 }
 
 template <int BN, int STAGES, bool A_MN, bool B_MN, bool B_DUAL, class Epi>
@@ -75,8 +74,7 @@ cudaError_t launch_gemm2_kernel(const LaunchCtx& c, const CUtensorMap& ta, const
   }
   const int tiles = sh.tiles_m * sh.tiles_n;
   const int clusters = std::max(1, std::min(tiles, max_pairs[dev]));
-  kern<<<2 * clusters, GEMM_THREADS, L::TOTAL, c.stream>>>(ta, tb, tb2, sh, ctl, ep);
-  return cudaGetLastError();
+  return launch_chained(c, kern, dim3(2 * clusters), dim3(GEMM_THREADS), L::TOTAL, ta, tb, tb2, sh, ctl, ep);
 }
 
 // The 2-SM pair kernel (default) or the 1-SM kernel, 256-column tiles.

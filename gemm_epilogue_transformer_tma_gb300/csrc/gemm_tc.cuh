@@ -140,6 +140,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // the set-up above may overlap the previous kernel; operands and outputs
+  // are touched only after it has completed
+  griddep_launch_dependents();
+  griddep_wait();
 
   const int num_tiles = sh.tiles_m * sh.tiles_n;
 
@@ -336,6 +340,19 @@ __device__ __forceinline__ float warp_transpose_sum32(float (&v)[32], int lane) 
 // Epilogue programs
 // ---------------------------------------------------------------------------
 
+// The RMSNorm row scale of row c.m taken straight from the partial sums of
+// squares of the first GEMM: r = 1 / sqrt(sum_j psum[m, j] * inv_d + eps).
+// The tile in column 0 also stores r (for the backward) when rstd_out is set.
+__device__ __forceinline__ float rstd_from_psum(const float* psum, int T, float inv_d, float eps, float* rstd_out,
+                                                const EpiCtx& c) {
+  const float* p = psum + static_cast<int64_t>(c.m) * T;
+  float acc = 0.f;
+  for (int j = 0; j < T; ++j) acc += p[j];
+  const float r = 1.0f / sqrtf(acc * inv_d + eps);
+  if (rstd_out != nullptr && c.tn == 0) rstd_out[c.m] = r;
+  return r;
+}
+
 // C = bf16(row_scale[m] * col_scale[n] * acc); both scales optional.
 struct EpiStore {
   struct Params {
@@ -343,11 +360,23 @@ struct EpiStore {
     int64_t ldo;
     const float* row_scale;
     const __nv_bfloat16* col_scale;
+    // optional: the row scale from first-GEMM partial sums instead of row_scale
+    const float* psum;
+    int T;
+    float inv_d;
+    float eps;
+    float* rstd_out;
   };
   template <int BN>
   static __device__ __forceinline__ void run(const Params& p, const EpiCtx& c) {
     const bool row_ok = c.m < c.M;
-    const float rs = (p.row_scale != nullptr && row_ok) ? p.row_scale[c.m] : 1.f;
+    float rs = 1.f;
+    if (row_ok) {
+      if (p.psum != nullptr)
+        rs = rstd_from_psum(p.psum, p.T, p.inv_d, p.eps, p.rstd_out, c);
+      else if (p.row_scale != nullptr)
+        rs = p.row_scale[c.m];
+    }
 #pragma unroll 1
     for (int cc = 0; cc < BN; cc += 32) {
       float v[32];
@@ -452,12 +481,19 @@ struct EpiRowscaleSwiglu {
     __nv_bfloat16* zsave;  // may be null
     int64_t ldz;
     int F;                 // gate (= up) width; output columns
+    // optional: the row scale from first-GEMM partial sums instead of rstd
+    const float* psum;
+    int T;
+    float inv_d;
+    float eps;
+    float* rstd_out;
   };
   template <int BN>
   static __device__ __forceinline__ void run(const Params& p, const EpiCtx& c) {
     constexpr int HB = BN / 2;
     const bool row_ok = c.m < c.M;
-    const float r = row_ok ? p.rstd[c.m] : 0.f;
+    float r = 0.f;
+    if (row_ok) r = p.psum != nullptr ? rstd_from_psum(p.psum, p.T, p.inv_d, p.eps, p.rstd_out, c) : p.rstd[c.m];
 #pragma unroll 1
     for (int cc = 0; cc < HB; cc += 32) {
       float g[32], u[32];

@@ -98,6 +98,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
   cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // the set-up above may overlap the previous kernel; operands and outputs
+  // are touched only after it has completed
+  griddep_launch_dependents();
+  griddep_wait();
 
   const int num_tiles = sh.tiles_m * sh.tiles_n;
 

@@ -50,6 +50,8 @@ int grid_for(const LaunchCtx& c, int64_t work_items, int threads) {
 // W2gt[n, k] = bf16(W2t[n, k] * g[k])
 __global__ void fold_kernel(const uint4* __restrict__ W2t, const uint4* __restrict__ g8, uint4* __restrict__ out,
                             int64_t n8, int64_t d8) {
+  griddep_wait();
+  griddep_launch_dependents();
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n8;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     float w[8], g[8], o[8];
@@ -64,6 +66,8 @@ __global__ void fold_kernel(const uint4* __restrict__ W2t, const uint4* __restri
 // rstd[m] = 1 / sqrt(sum_j psum[m, j] / d + eps): one warp per row
 __global__ void rstd_combine_kernel(const float* __restrict__ psum, int64_t M, int64_t T, float inv_d, float eps,
                                     float* __restrict__ rstd) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int64_t row = blockIdx.x * static_cast<int64_t>(blockDim.x / 32) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= M) return;
@@ -81,6 +85,8 @@ __global__ void __launch_bounds__(256) swiglu_bwd_kernel(const __nv_bfloat16* __
                                                          const float* __restrict__ rstd,
                                                          __nv_bfloat16* __restrict__ dP, float* __restrict__ cvec,
                                                          int64_t F, float inv_d) {
+  griddep_wait();
+  griddep_launch_dependents();
   __shared__ float red[8];
   const int64_t m = blockIdx.x;
   const float r = rstd[m];
@@ -113,6 +119,8 @@ __global__ void __launch_bounds__(256) swiglu_bwd_kernel(const __nv_bfloat16* __
 
 // out[k] = sum_r part[r, k]; block = 32 columns x 8 row groups
 __global__ void col_combine_kernel(const float* __restrict__ part, int64_t rows, int64_t d, float* __restrict__ out) {
+  griddep_wait();
+  griddep_launch_dependents();
   __shared__ float red[8][33];
   const int64_t k = blockIdx.x * 32 + threadIdx.x;
   float s = 0.f;
@@ -137,6 +145,8 @@ __global__ void ce_combine_kernel(const float* __restrict__ pmax, const float* _
                                   const int32_t* __restrict__ labels, int64_t M, int64_t T, int64_t V,
                                   float* __restrict__ lse, int32_t* __restrict__ argmax, float* __restrict__ row_loss,
                                   int* status) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int64_t row = blockIdx.x * static_cast<int64_t>(blockDim.x / 32) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= M) return;
@@ -181,6 +191,8 @@ __global__ void ce_combine_kernel(const float* __restrict__ pmax, const float* _
 
 // out = mean(v) with a fixed summation order (one CTA of 1024 threads)
 __global__ void __launch_bounds__(1024) mean_kernel(const float* __restrict__ v, int64_t n, float* __restrict__ out) {
+  griddep_wait();
+  griddep_launch_dependents();
   __shared__ float red[32];
   float s = 0.f;
   for (int64_t i = threadIdx.x; i < n; i += blockDim.x) s += v[i];
@@ -194,6 +206,8 @@ __global__ void __launch_bounds__(1024) mean_kernel(const float* __restrict__ v,
 }
 
 __global__ void f32_to_bf16_kernel(const float4* __restrict__ in, uint2* __restrict__ out, int64_t n4) {
+  griddep_wait();
+  griddep_launch_dependents();
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n4;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const float4 f = in[i];
@@ -210,6 +224,8 @@ __global__ void __launch_bounds__(256) add_rmsnorm_kernel(const __nv_bfloat16* _
                                                           const __nv_bfloat16* __restrict__ g,
                                                           __nv_bfloat16* __restrict__ H, float* __restrict__ rstd,
                                                           __nv_bfloat16* __restrict__ Nrm, int64_t d, float eps) {
+  griddep_wait();
+  griddep_launch_dependents();
   __shared__ float red[8];
   const int64_t m = blockIdx.x;
   const uint4* a8 = reinterpret_cast<const uint4*>(A + m * d);
@@ -244,6 +260,8 @@ __global__ void __launch_bounds__(256) add_rmsnorm_kernel(const __nv_bfloat16* _
 
 __global__ void swiglu_kernel(const __nv_bfloat16* __restrict__ z, __nv_bfloat16* __restrict__ out, int64_t M,
                               int64_t F) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int64_t f8 = F / 8;
   const int64_t n = M * f8;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
@@ -260,6 +278,8 @@ __global__ void swiglu_kernel(const __nv_bfloat16* __restrict__ z, __nv_bfloat16
 
 __global__ void swiglu_bwd_plain_kernel(const __nv_bfloat16* __restrict__ dY, const __nv_bfloat16* __restrict__ z,
                                         __nv_bfloat16* __restrict__ dZ, int64_t M, int64_t F) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int64_t f8 = F / 8;
   const int64_t n = M * f8;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
@@ -287,6 +307,8 @@ __global__ void __launch_bounds__(256) rmsnorm_bwd_kernel(const __nv_bfloat16* _
                                                           const float* __restrict__ rstd,
                                                           const __nv_bfloat16* __restrict__ g,
                                                           __nv_bfloat16* __restrict__ dH, int64_t d) {
+  griddep_wait();
+  griddep_launch_dependents();
   __shared__ float red[8];
   const int64_t m = blockIdx.x;
   const float r = rstd[m];
@@ -320,6 +342,8 @@ __global__ void __launch_bounds__(256) rmsnorm_bwd_kernel(const __nv_bfloat16* _
 __global__ void rmsnorm_bwd_dg_kernel(const __nv_bfloat16* __restrict__ dN, const __nv_bfloat16* __restrict__ H,
                                       const float* __restrict__ rstd, float* __restrict__ dgpart, int64_t M, int64_t d,
                                       int64_t rows_per_part) {
+  griddep_wait();
+  griddep_launch_dependents();
   __shared__ float red[8][33];
   const int64_t k = blockIdx.x * 32 + threadIdx.x;
   const int64_t r0 = blockIdx.y * rows_per_part;
@@ -345,84 +369,70 @@ __global__ void rmsnorm_bwd_dg_kernel(const __nv_bfloat16* __restrict__ dN, cons
 cudaError_t launch_fold(const LaunchCtx& c, const __nv_bfloat16* W2t, const __nv_bfloat16* g, __nv_bfloat16* W2gt,
                         int64_t N2, int64_t d) {
   const int64_t n8 = N2 * d / 8;
-  fold_kernel<<<grid_for(c, n8, 256), 256, 0, c.stream>>>(reinterpret_cast<const uint4*>(W2t),
+  return launch_chained(c, fold_kernel, dim3(grid_for(c, n8, 256)), dim3(256), 0, reinterpret_cast<const uint4*>(W2t),
                                                           reinterpret_cast<const uint4*>(g),
                                                           reinterpret_cast<uint4*>(W2gt), n8, d / 8);
-  return cudaGetLastError();
 }
 
 cudaError_t launch_rstd_combine(const LaunchCtx& c, const float* psum, int64_t M, int64_t T, int64_t d, float eps,
                                 float* rstd) {
   const int rows_per_block = 8;
   const int64_t grid = (M + rows_per_block - 1) / rows_per_block;
-  rstd_combine_kernel<<<static_cast<unsigned>(grid), 32 * rows_per_block, 0, c.stream>>>(
-      psum, M, T, 1.0f / static_cast<float>(d), eps, rstd);
-  return cudaGetLastError();
+  return launch_chained(c, rstd_combine_kernel, dim3(static_cast<unsigned>(grid)), dim3(32 * rows_per_block), 0, psum, M, T, 1.0f / static_cast<float>(d), eps, rstd);
 }
 
 cudaError_t launch_swiglu_bwd(const LaunchCtx& c, const __nv_bfloat16* dY, const __nv_bfloat16* z,
                               const float* rstd, __nv_bfloat16* dP, float* cvec, int64_t M, int64_t F, int64_t d) {
-  swiglu_bwd_kernel<<<static_cast<unsigned>(M), 256, 0, c.stream>>>(dY, z, rstd, dP, cvec, F,
+  return launch_chained(c, swiglu_bwd_kernel, dim3(static_cast<unsigned>(M)), dim3(256), 0, dY, z, rstd, dP, cvec, F,
                                                                     1.0f / static_cast<float>(d));
-  return cudaGetLastError();
 }
 
 cudaError_t launch_col_combine(const LaunchCtx& c, const float* part, int64_t rows, int64_t d, float* out) {
-  col_combine_kernel<<<static_cast<unsigned>((d + 31) / 32), dim3(32, 8), 0, c.stream>>>(part, rows, d, out);
-  return cudaGetLastError();
+  return launch_chained(c, col_combine_kernel, dim3(static_cast<unsigned>((d + 31) / 32)), dim3(dim3(32, 8)), 0, part, rows, d, out);
 }
 
 cudaError_t launch_ce_combine(const LaunchCtx& c, const float* pmax, const float* psum, const int32_t* parg,
                               const float* zy, const int32_t* labels, int64_t M, int64_t T, int64_t V, float* lse,
                               int32_t* argmax, float* row_loss) {
   const int rows_per_block = 8;
-  ce_combine_kernel<<<static_cast<unsigned>((M + rows_per_block - 1) / rows_per_block), 32 * rows_per_block, 0,
-                      c.stream>>>(pmax, psum, parg, zy, labels, M, T, V, lse, argmax, row_loss, c.status);
-  return cudaGetLastError();
+  return launch_chained(c, ce_combine_kernel, dim3(static_cast<unsigned>((M + rows_per_block - 1) / rows_per_block)), dim3(32 * rows_per_block), 0, pmax, psum, parg, zy, labels, M, T, V, lse, argmax, row_loss, c.status);
 }
 
 cudaError_t launch_mean(const LaunchCtx& c, const float* v, int64_t n, float* out) {
-  mean_kernel<<<1, 1024, 0, c.stream>>>(v, n, out);
-  return cudaGetLastError();
+  return launch_chained(c, mean_kernel, dim3(1), dim3(1024), 0, v, n, out);
 }
 
 cudaError_t launch_f32_to_bf16(const LaunchCtx& c, const float* in, __nv_bfloat16* out, int64_t n) {
   const int64_t n4 = n / 4;
-  f32_to_bf16_kernel<<<grid_for(c, n4, 256), 256, 0, c.stream>>>(reinterpret_cast<const float4*>(in),
+  return launch_chained(c, f32_to_bf16_kernel, dim3(grid_for(c, n4, 256)), dim3(256), 0, reinterpret_cast<const float4*>(in),
                                                                  reinterpret_cast<uint2*>(out), n4);
-  return cudaGetLastError();
 }
 
 cudaError_t launch_add_rmsnorm(const LaunchCtx& c, const __nv_bfloat16* A, const __nv_bfloat16* R,
                                const __nv_bfloat16* g, __nv_bfloat16* H, float* rstd, __nv_bfloat16* Nrm, int64_t M,
                                int64_t d, float eps) {
-  add_rmsnorm_kernel<<<static_cast<unsigned>(M), 256, 0, c.stream>>>(A, R, g, H, rstd, Nrm, d, eps);
-  return cudaGetLastError();
+  return launch_chained(c, add_rmsnorm_kernel, dim3(static_cast<unsigned>(M)), dim3(256), 0, A, R, g, H, rstd, Nrm, d, eps);
 }
 
 cudaError_t launch_swiglu(const LaunchCtx& c, const __nv_bfloat16* z, __nv_bfloat16* out, int64_t M, int64_t F) {
-  swiglu_kernel<<<grid_for(c, M * F / 8, 256), 256, 0, c.stream>>>(z, out, M, F);
-  return cudaGetLastError();
+  return launch_chained(c, swiglu_kernel, dim3(grid_for(c, M * F / 8, 256)), dim3(256), 0, z, out, M, F);
 }
 
 cudaError_t launch_swiglu_bwd_plain(const LaunchCtx& c, const __nv_bfloat16* dY, const __nv_bfloat16* z,
                                     __nv_bfloat16* dZ, int64_t M, int64_t F) {
-  swiglu_bwd_plain_kernel<<<grid_for(c, M * F / 8, 256), 256, 0, c.stream>>>(dY, z, dZ, M, F);
-  return cudaGetLastError();
+  return launch_chained(c, swiglu_bwd_plain_kernel, dim3(grid_for(c, M * F / 8, 256)), dim3(256), 0, dY, z, dZ, M, F);
 }
 
 cudaError_t launch_rmsnorm_bwd(const LaunchCtx& c, const __nv_bfloat16* dN, const __nv_bfloat16* H,
                                const float* rstd, const __nv_bfloat16* g, __nv_bfloat16* dH, int64_t M, int64_t d) {
-  rmsnorm_bwd_kernel<<<static_cast<unsigned>(M), 256, 0, c.stream>>>(dN, H, rstd, g, dH, d);
-  return cudaGetLastError();
+  return launch_chained(c, rmsnorm_bwd_kernel, dim3(static_cast<unsigned>(M)), dim3(256), 0, dN, H, rstd, g, dH, d);
 }
 
 cudaError_t launch_rmsnorm_bwd_dg(const LaunchCtx& c, const __nv_bfloat16* dN, const __nv_bfloat16* H,
                                   const float* rstd, float* dgpart, int64_t M, int64_t d, int64_t rows_per_part) {
   const dim3 grid(static_cast<unsigned>((d + 31) / 32),
                   static_cast<unsigned>((M + rows_per_part - 1) / rows_per_part));
-  rmsnorm_bwd_dg_kernel<<<grid, dim3(32, 8), 0, c.stream>>>(dN, H, rstd, dgpart, M, d, rows_per_part);
-  return cudaGetLastError();
+  return launch_chained(c, rmsnorm_bwd_dg_kernel, dim3(grid), dim3(dim3(32, 8)), 0, dN, H, rstd, dgpart, M, d, rows_per_part);
 }
 
 }  // namespace coda

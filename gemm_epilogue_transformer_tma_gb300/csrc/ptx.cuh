@@ -32,6 +32,19 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 }
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch: a kernel launched with the programmatic
+// stream-serialization attribute may start before the previous kernel in the
+// stream has finished; griddep_wait() blocks until that kernel has completed
+// and its memory is visible, griddep_launch_dependents() lets the next kernel
+// start launching.  Both are no-ops in a normal launch.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

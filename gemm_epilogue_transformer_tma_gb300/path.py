@@ -10,7 +10,8 @@ from __future__ import annotations
 import torch
 
 from . import (CODA_EPI_PLAIN, CODA_EPI_SWIGLU, coda_bwd_workspace_bytes, coda_dg_combine,
-               coda_dgpart_rows, coda_fold_rmsnorm_weight, coda_gemm_dgrad_rmsbwd, coda_gemm_res_prms,
+               coda_dgpart_rows, coda_fold_rmsnorm_weight, coda_gemm_dgrad_rmsbwd, coda_gemm_prms_rowscale_swiglu,
+               coda_gemm_res_prms,
                coda_gemm_res_prms_bwd, coda_gemm_rowscale_swiglu, coda_gemm_rowscale_swiglu_bwd,
                coda_gemm_wgrad_gscale, coda_prms_num_tiles, coda_rstd_combine, coda_swiglu_bwd,
                coda_unfused_bwd, coda_unfused_fwd, coda_unfused_workspace_bytes)
@@ -28,12 +29,13 @@ class BlockBuffers:
     """
 
     def __init__(self, inputs: dict, swiglu: bool = True, backward: bool = True, eps: float = 1e-5,
-                 unfused: bool = False):
+                 unfused: bool = False, fuse_rstd: bool = False):
         dev = inputs["X"].device
         self.swiglu = swiglu
         self.eps = eps
         self.with_backward = backward
         self.unfused = unfused
+        self.fuse_rstd = fuse_rstd
         for k, v in inputs.items():
             setattr(self, k, v.contiguous())
         self.M, self.K1 = self.X.shape
@@ -70,6 +72,13 @@ class BlockBuffers:
             return self.forward_unfused()
         coda_fold_rmsnorm_weight(self.W2t, self.g, self.W2gt)
         coda_gemm_res_prms(self.X, self.W1t, self.R, self.H, self.psum)
+        if self.fuse_rstd:
+            # the combine runs inside GEMM2's epilogue, which also stores rstd
+            flags = CODA_EPI_SWIGLU if self.swiglu else CODA_EPI_PLAIN
+            coda_gemm_prms_rowscale_swiglu(self.H, self.W2gt, self.psum, self.eps, self.rstd,
+                                           self.out if self.swiglu else self.z,
+                                           (self.z if save_z else None) if self.swiglu else None, flags)
+            return
         coda_rstd_combine(self.psum, self.d, self.eps, self.rstd)
         if self.swiglu:
             coda_gemm_rowscale_swiglu(self.H, self.W2gt, self.rstd, self.out,

@@ -167,6 +167,19 @@ coda_status_t coda_gemm_rowscale_swiglu(coda_handle_t h, const void* H, const vo
                                         void* out, void* z_save, int64_t M, int64_t d, int64_t N2, uint32_t flags,
                                         void* stream);
 
+/* The same GEMM2 with the light combine folded into its epilogue: each output
+ * tile derives its rows' scale from GEMM1's partial sums,
+ *   rstd[m] = 1 / sqrt( sum_j psum[m][j] / d + eps ),
+ * so the separate coda_rstd_combine launch disappears (its work is T loads per
+ * row per tile, read from L2).  psum fp32 [M][T] (from coda_gemm_res_prms),
+ * rstd fp32 [M] receives the row scale for the backward (may be NULL); the
+ * other arguments, flags and outputs are those of coda_gemm_rowscale_swiglu.
+ * The row sum runs in a different order than coda_rstd_combine's, so rstd can
+ * differ in the last bit. */
+coda_status_t coda_gemm_prms_rowscale_swiglu(coda_handle_t h, const void* H, const void* W2gt, const float* psum,
+                                             int64_t T, float eps, float* rstd, void* out, void* z_save, int64_t M,
+                                             int64_t d, int64_t N2, uint32_t flags, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* backward (section 尾声: the backward of a block-local epilogue is itself    */
 /* block-local)                                                              */

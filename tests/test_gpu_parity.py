@@ -227,3 +227,38 @@ def test_argument_errors():
         C.coda_gemm(d, False, d, False, out, 64, 64, 64, row_scale=torch.empty(64, device="cuda"),
                     col_scale=torch.empty(64, device="cuda", dtype=torch.float32))
     assert_device_ok()
+
+
+# --------------------------------------------------------------------------
+# the light combine folded into GEMM2's epilogue (row scale from the partial
+# sums, no separate combine launch)
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", ["ragged", "whole", "one_row"])
+def test_forward_fused_rstd_parity(name, pairing):
+    s = SHAPES[name]
+    x = dev_inputs(s)
+    b = BlockBuffers(x, swiglu=True, backward=False, fuse_rstd=True)
+    b.forward()
+    assert_device_ok()
+    check_forward(s, b, x)
+
+
+def test_tiny_config_plain_fused_rstd():
+    x = dev_inputs(TINY)
+    b = BlockBuffers(x, swiglu=False, backward=False, fuse_rstd=True)
+    b.forward()
+    assert_device_ok()
+    check_forward(TINY, b, x)
+
+
+def test_fwd_bwd_end_to_end_fused_rstd():
+    s = SHAPES["ragged"]
+    x = dev_inputs(s)
+    b = BlockBuffers(x, fuse_rstd=True)
+    b.step()
+    assert_device_ok()
+    ref = O.block_backward(*(f64(x[k]) for k in ("X", "W1t", "R", "g", "W2t", "dY")), EPS, True)
+    for k_gpu, k_ref in (("out", "out"), ("rstd", "rstd"), ("dH", "dR"), ("dX", "dX"), ("dW1t", "dW1t"),
+                         ("dW2t", "dW2t"), ("dg", "dg")):
+        assert_frob(getattr(b, k_gpu), ref[k_ref], f"{k_gpu} e2e")
