@@ -36,7 +36,7 @@ sys.path.insert(0, ROOT)
 
 import torch  # noqa: E402
 
-from coda_inputs import B1, B7, B70, LMHEAD, BlockShape, block_inputs, ce_inputs  # noqa: E402
+from coda_inputs import B1, B7, B70, LMHEAD, BlockShape, block_inputs, ce_inputs, down_proj_inputs  # noqa: E402
 
 METRIC = "fused GEMM-RMSNorm-GEMM fwd+bwd TFLOP/s and % of GB300 bf16 dense peak"
 UNIT = "TFLOP/s"
@@ -276,6 +276,32 @@ def run_reference(args, shape):
     print(json.dumps(line), flush=True)
 
 
+def bench_down_proj_swiglu_bwd(C, b, shape, steps, warmup):
+    """The SwiGLU backward fed by a down projection's data gradient:
+    dY = dYb W3 through HBM (plain GEMM + streaming SwiGLU-backward kernel +
+    dgrad2 with c) against dY kept on chip (GEMM with the SwiGLU-backward
+    epilogue + dgrad2 forming c from the epilogue's partial sums)."""
+    dp = down_proj_inputs(shape, 0, "cuda")
+    dY = torch.empty(shape.M, shape.F, dtype=torch.bfloat16, device="cuda")
+    cpart = torch.empty(shape.M, C.coda_prms_num_tiles(shape.F), device="cuda")
+    through_hbm = [
+        lambda: C.coda_gemm(dp["dYb"], False, dp["W3t"], True, dY, shape.M, shape.F, shape.d),
+        lambda: C.coda_swiglu_bwd(dY, b.z, b.rstd, b.dP, b.c, shape.d),
+        lambda: C.coda_gemm_dgrad_rmsbwd(b.dP, b.W2t, b.H, b.g, b.c, b.dH, b.dgpart),
+    ]
+    on_chip = [
+        lambda: C.coda_gemm_dgrad_swiglu_bwd(dp["dYb"], dp["W3t"], b.z, b.rstd, b.dP, cpart),
+        lambda: C.coda_gemm_dgrad_rmsbwd_cpart(b.dP, b.W2t, b.H, b.g, b.rstd, cpart, b.dH, b.dgpart),
+    ]
+    n = max(3, steps // 2)
+    t_hbm, _ = time_steps(through_hbm, n, warmup, stage_events=False)
+    t_chip, _ = time_steps(on_chip, n, warmup, stage_events=False)
+    flops = 2.0 * shape.M * shape.F * shape.d + 2.0 * shape.M * shape.N2 * shape.d
+    return {"what": "down-proj dgrad + SwiGLU bwd + dgrad2/RMSNorm bwd", "dY_through_hbm_ms": t_hbm / n,
+            "dY_on_chip_ms": t_chip / n, "speedup": t_hbm / t_chip,
+            "on_chip_tflops": flops / (t_chip / n * 1e-3) / 1e12}
+
+
 def bench_lmhead(C, steps, warmup):
     s = LMHEAD
     x = ce_inputs(s, 0, "cuda")
@@ -411,7 +437,12 @@ def main():
             f()
     barrier()
     with ClockSampler(local) as clk:
-        total_ms, per = time_steps(calls, args.steps, 0)
+        # headline: events only around the whole region, so nothing sits
+        # between launches (an event between kernels would also stop the
+        # next kernel's prologue from overlapping the previous one's tail)
+        total_ms, _ = time_steps(calls, args.steps, 0, stage_events=False)
+        # per-stage breakdown: a second pass with an event between stages
+        _, per = time_steps(calls, args.steps, 0, stage_events=True)
     barrier()
     st, bits = C.coda_sync_status()
     if st != 0:
@@ -443,6 +474,10 @@ def main():
                                       "fused_speedup": u_ms / ms}
         del bu
         torch.cuda.empty_cache()
+        if shape.backward:
+            extras["next_swiglu_bwd_in_down_proj_dgrad"] = bench_down_proj_swiglu_bwd(C, b, shape, args.steps,
+                                                                                    args.warmup)
+            torch.cuda.empty_cache()
         # end to end through the public API with host buffers
         ins = ("X", "R", "dY") if shape.backward else ("X", "R")
         res = "dX" if shape.backward else "out"

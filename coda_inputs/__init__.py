@@ -28,7 +28,7 @@ import math
 import torch
 
 # order in which tensors draw their seeds
-_ORDER = {"X": 0, "W1": 1, "R": 2, "g": 3, "W2": 4, "dY": 5, "H": 6, "W": 7, "labels": 8}
+_ORDER = {"X": 0, "W1": 1, "R": 2, "g": 3, "W2": 4, "dY": 5, "H": 6, "W": 7, "labels": 8, "W3": 9, "dYb": 10}
 
 
 @dataclasses.dataclass(frozen=True)
@@ -122,6 +122,14 @@ def block_inputs(s: BlockShape, seed: int = 0, device="cpu", with_dy=None) -> di
     if with_dy if with_dy is not None else s.backward:
         x["dY"] = normal_bf16((s.M, s.out_cols), 1.0, seed, "dY", device)
     return x
+
+
+def down_proj_inputs(s: BlockShape, seed: int = 0, device="cpu") -> dict:
+    """For a block whose SwiGLU output feeds a down projection y = out W3:
+    W3t[d, F] ~ N(0, w_std) (nn.Linear layout) and the upstream gradient
+    dYb[M, d] ~ N(0, 1)."""
+    return {"W3t": normal_bf16((s.d, s.F), s.w_std, seed, "W3", device),
+            "dYb": normal_bf16((s.M, s.d), 1.0, seed, "dYb", device)}
 
 
 def ce_inputs(s: CEShape, seed: int = 0, device="cpu") -> dict:

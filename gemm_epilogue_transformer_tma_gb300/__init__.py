@@ -62,6 +62,8 @@ SIGNATURES = {
     "coda_swiglu_bwd": (_INT, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "coda_gemm_dgrad_rmsbwd": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "coda_gemm_dgrad_rmsbwd_noalloc": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
+    "coda_gemm_dgrad_swiglu_bwd": (_INT, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
+    "coda_gemm_dgrad_rmsbwd_cpart": (_INT, [_P, _P, _P, _P, _P, _P, _P, _I64, _P, _P, _I64, _I64, _I64, _P]),
     "coda_dg_combine": (_INT, [_P, _P, _I64, _I64, _P, _P]),
     "coda_gemm_wgrad_gscale": (_INT, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "coda_bwd_workspace_bytes": (_SZ, [_I64, _I64, _I64]),
@@ -302,6 +304,39 @@ def coda_gemm_dgrad_rmsbwd_noalloc(dP, W2t, H, g, c, dH, dg, stream=None):
                                                          _ptr(H, BF, "H"), _ptr(g, BF, "g"), _ptr(c, F32, "c"),
                                                          _ptr(dH, BF, "dH"), _ptr(dg, F32, "dg"), M, N2, d,
                                                          _stream(stream)), "coda_gemm_dgrad_rmsbwd_noalloc")
+
+
+def coda_gemm_dgrad_swiglu_bwd(dYb, W3t, z, rstd, dP, cpart, stream=None):
+    """dY = dYb W3 on chip, SwiGLU backward in the epilogue: dP and the c
+    partial sums (see include/coda.h)."""
+    M, d = dYb.shape
+    F = W3t.shape[1]
+    _shape(W3t, (d, F), "W3t")
+    _shape(z, (M, 2 * F), "z")
+    _shape(rstd, (M,), "rstd")
+    _shape(dP, (M, 2 * F), "dP")
+    _shape(cpart, (M, coda_prms_num_tiles(F)), "cpart")
+    _check(load_library().coda_gemm_dgrad_swiglu_bwd(_h(dYb), _ptr(dYb, BF, "dYb"), _ptr(W3t, BF, "W3t"),
+                                                     _ptr(z, BF, "z"), _ptr(rstd, F32, "rstd"), _ptr(dP, BF, "dP"),
+                                                     _ptr(cpart, F32, "cpart"), M, d, F, _stream(stream)),
+           "coda_gemm_dgrad_swiglu_bwd")
+
+
+def coda_gemm_dgrad_rmsbwd_cpart(dP, W2t, H, g, rstd, cpart, dH, dgpart, stream=None):
+    M, N2 = dP.shape
+    d = W2t.shape[1]
+    Tc = cpart.shape[1]
+    _shape(W2t, (N2, d), "W2t")
+    _shape(H, (M, d), "H")
+    _shape(g, (d,), "g")
+    _shape(rstd, (M,), "rstd")
+    _shape(cpart, (M, Tc), "cpart")
+    _shape(dH, (M, d), "dH")
+    _shape(dgpart, (coda_dgpart_rows(M), d), "dgpart")
+    _check(load_library().coda_gemm_dgrad_rmsbwd_cpart(
+        _h(dP), _ptr(dP, BF, "dP"), _ptr(W2t, BF, "W2t"), _ptr(H, BF, "H"), _ptr(g, BF, "g"),
+        _ptr(rstd, F32, "rstd"), _ptr(cpart, F32, "cpart"), Tc, _ptr(dH, BF, "dH"), _ptr(dgpart, F32, "dgpart"),
+        M, N2, d, _stream(stream)), "coda_gemm_dgrad_rmsbwd_cpart")
 
 
 def coda_dg_combine(dgpart, dg, stream=None):

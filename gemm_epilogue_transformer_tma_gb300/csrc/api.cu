@@ -319,6 +319,52 @@ coda_status_t coda_gemm_dgrad_rmsbwd(coda_handle_t h, const void* dP, const void
                                   dgpart, int(M), int(N2), int(d)));
 }
 
+coda_status_t coda_gemm_dgrad_swiglu_bwd(coda_handle_t h, const void* dYb, const void* W3t, const void* z,
+                                         const float* rstd, void* dP, float* cpart, int64_t M, int64_t d, int64_t F,
+                                         void* stream) {
+  CODA_TRY(Check()
+               .handle(h)
+               .rows(M)
+               .mptr(dYb, M)
+               .ptr(W3t)
+               .mptr(z, M)
+               .mptr(rstd, M)
+               .mptr(dP, M)
+               .mptr(cpart, M)
+               .cols(d)
+               .cols(F)
+               .st);
+  if (M == 0) return CODA_OK;
+  return from_cuda(gemm_dgrad_swiglu_bwd(ctx_of(h, stream), static_cast<const bf16*>(dYb),
+                                         static_cast<const bf16*>(W3t), static_cast<const bf16*>(z), rstd,
+                                         static_cast<bf16*>(dP), cpart, int(M), int(d), int(F),
+                                         int(coda_prms_num_tiles(F))));
+}
+
+coda_status_t coda_gemm_dgrad_rmsbwd_cpart(coda_handle_t h, const void* dP, const void* W2t, const void* H,
+                                           const void* g, const float* rstd, const float* cpart, int64_t Tc,
+                                           void* dH, float* dgpart, int64_t M, int64_t N2, int64_t d, void* stream) {
+  CODA_TRY(Check()
+               .handle(h)
+               .rows(M)
+               .mptr(dP, M)
+               .ptr(W2t)
+               .mptr(H, M)
+               .ptr(g)
+               .mptr(rstd, M)
+               .mptr(cpart, M)
+               .mptr(dH, M)
+               .mptr(dgpart, M)
+               .cols(N2)
+               .cols(d)
+               .st);
+  if (Tc <= 0 || Tc > kMaxExtent) return CODA_ERR_INVALID_ARG;
+  if (M == 0) return CODA_OK;
+  return from_cuda(gemm_dgrad_rms(ctx_of(h, stream), static_cast<const bf16*>(dP), static_cast<const bf16*>(W2t),
+                                  static_cast<const bf16*>(H), static_cast<const bf16*>(g), nullptr,
+                                  static_cast<bf16*>(dH), dgpart, int(M), int(N2), int(d), cpart, int(Tc), rstd));
+}
+
 coda_status_t coda_dg_combine(coda_handle_t h, const float* dgpart, int64_t rows, int64_t d, float* dg,
                               void* stream) {
   CODA_TRY(Check().handle(h).rows(rows).mptr(dgpart, rows).ptr(dg).st);

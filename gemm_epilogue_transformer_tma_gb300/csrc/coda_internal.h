@@ -78,9 +78,18 @@ cudaError_t gemm_rowscale_swiglu(const LaunchCtx& c, const __nv_bfloat16* H, con
                                  float* rstd_out = nullptr);
 
 // acc = dP W2^T; dH = g*acc - c*h; dgpart[4*tm+q, n] = sum_rows acc*h.
+// With cpart != null, c comes from the SwiGLU-backward epilogue's partial
+// sums: c[m] = rstd[m]^2 / d * sum_j cpart[m, j] (Tc columns); cvec unused.
 cudaError_t gemm_dgrad_rms(const LaunchCtx& c, const __nv_bfloat16* dP, const __nv_bfloat16* W2t,
                            const __nv_bfloat16* H, const __nv_bfloat16* g, const float* cvec, __nv_bfloat16* dH,
-                           float* dgpart, int M, int N2, int d);
+                           float* dgpart, int M, int N2, int d, const float* cpart = nullptr, int Tc = 0,
+                           const float* rstd = nullptr);
+
+// dY = dYb W3 computed on chip, then the SwiGLU backward in the epilogue:
+// dP = bf16(rstd dZ), cpart[m, j] = sum over 256-column tile j of dZ z.
+cudaError_t gemm_dgrad_swiglu_bwd(const LaunchCtx& c, const __nv_bfloat16* dYb, const __nv_bfloat16* W3t,
+                                  const __nv_bfloat16* z, const float* rstd, __nv_bfloat16* dP, float* cpart, int M,
+                                  int d, int F, int T);
 
 // per (row, vocab tile) max / sum-exp / argmax, label logit.
 cudaError_t gemm_ce_stats(const LaunchCtx& c, const __nv_bfloat16* H, const __nv_bfloat16* Wt, const int32_t* labels,

@@ -532,11 +532,28 @@ struct EpiDgradRms {
     __nv_bfloat16* dH;
     int64_t lddh;
     float* dgpart;  // [4 * tiles_m, N]
+    // optional: c from the SwiGLU-backward epilogue's partial sums,
+    // c[m] = rstd[m]^2 * inv_d * sum_j cpart[m, j], instead of the c vector
+    const float* cpart;
+    int Tc;
+    const float* rstd;
+    float inv_d;
   };
   template <int BN>
   static __device__ __forceinline__ void run(const Params& p, const EpiCtx& c) {
     const bool row_ok = c.m < c.M;
-    const float cm = row_ok ? p.c[c.m] : 0.f;
+    float cm = 0.f;
+    if (row_ok) {
+      if (p.cpart != nullptr) {
+        const float* cp = p.cpart + static_cast<int64_t>(c.m) * p.Tc;
+        float acc = 0.f;
+        for (int j = 0; j < p.Tc; ++j) acc += cp[j];
+        const float r = p.rstd[c.m];
+        cm = r * r * p.inv_d * acc;
+      } else {
+        cm = p.c[c.m];
+      }
+    }
 #pragma unroll 1
     for (int cc = 0; cc < BN; cc += 32) {
       float a[32];
@@ -561,6 +578,56 @@ struct EpiDgradRms {
           p.dgpart[static_cast<int64_t>(c.tm * 4 + c.quad) * c.N + n0 + c.lane] = s;
       }
     }
+  }
+};
+
+// Data gradient of a down projection y = out W3 with the SwiGLU backward in
+// its epilogue: the accumulator holds dY (gate-column indices j); with
+// s = sigmoid(z_gate):
+//   dZ_gate = dY z_up s (1 + z_gate (1 - s)),  dZ_up = dY z_gate s,
+//   dP = bf16(rstd[m] dZ) into the gate / up halves,
+//   cpart[m, tn] = sum over the tile's columns of dZ_gate z_gate + dZ_up z_up
+// (a block reduction the RMSNorm backward later merges into c).  dY itself
+// never leaves the chip.
+struct EpiSwigluBwd {
+  struct Params {
+    const __nv_bfloat16* z;  // [M, 2F]
+    const float* rstd;
+    __nv_bfloat16* dP;       // [M, 2F]
+    float* cpart;            // [M, T]
+    int T;
+    int F;
+  };
+  template <int BN>
+  static __device__ __forceinline__ void run(const Params& p, const EpiCtx& c) {
+    const bool row_ok = c.m < c.M;
+    const float r = row_ok ? p.rstd[c.m] : 0.f;
+    const int64_t row = static_cast<int64_t>(c.m) * 2 * p.F;
+    float cp = 0.f;
+#pragma unroll 1
+    for (int cc = 0; cc < BN; cc += 32) {
+      float dy[32];
+      tmem_ld32(c.taddr + cc, dy);
+      const int j0 = c.tn * BN + cc;
+      if (row_ok && j0 < p.F) {
+        const int nv = p.F - j0;
+        float zg[32], zu[32];
+        load_bf16x32(p.z + row + j0, nv, zg);
+        load_bf16x32(p.z + row + p.F + j0, nv, zu);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float s = 1.0f / (1.0f + __expf(-zg[i]));
+          const float dzu = dy[i] * zg[i] * s;
+          const float dzg = dy[i] * zu[i] * s * (1.0f + zg[i] * (1.0f - s));
+          cp = fmaf(dzg, zg[i], fmaf(dzu, zu[i], cp));
+          zg[i] = r * dzg;
+          zu[i] = r * dzu;
+        }
+        store_bf16x32(p.dP + row + j0, nv, zg);
+        store_bf16x32(p.dP + row + p.F + j0, nv, zu);
+      }
+    }
+    if (row_ok) p.cpart[static_cast<int64_t>(c.m) * p.T + c.tn] = cp;
   }
 };
 

@@ -11,7 +11,7 @@ import torch
 
 from . import (CODA_EPI_PLAIN, CODA_EPI_SWIGLU, coda_bwd_workspace_bytes, coda_dg_combine,
                coda_dgpart_rows, coda_fold_rmsnorm_weight, coda_gemm_dgrad_rmsbwd, coda_gemm_prms_rowscale_swiglu,
-               coda_gemm_res_prms,
+               coda_gemm_dgrad_rmsbwd_cpart, coda_gemm_dgrad_swiglu_bwd, coda_gemm_res_prms,
                coda_gemm_res_prms_bwd, coda_gemm_rowscale_swiglu, coda_gemm_rowscale_swiglu_bwd,
                coda_gemm_wgrad_gscale, coda_prms_num_tiles, coda_rstd_combine, coda_swiglu_bwd,
                coda_unfused_bwd, coda_unfused_fwd, coda_unfused_workspace_bytes)
@@ -108,6 +108,21 @@ class BlockBuffers:
         self.forward()
         if self.with_backward:
             self.backward()
+
+    # -- backward from the down projection's upstream gradient ---------------
+    def backward_from_down_proj(self, dYb, W3t):
+        """The backward when the block's output feeds a down projection
+        y = out W3 (W3t[d, F]) with upstream gradient dYb[M, d]: dY stays on
+        chip -- the down projection's data-gradient GEMM runs the SwiGLU
+        backward in its epilogue, and dgrad2's epilogue forms c from its
+        partial sums."""
+        if not hasattr(self, "cpart"):
+            self.cpart = torch.empty(self.M, coda_prms_num_tiles(self.F), dtype=F32, device=self.X.device)
+        coda_gemm_dgrad_swiglu_bwd(dYb, W3t, self.z, self.rstd, self.dP, self.cpart)
+        coda_gemm_dgrad_rmsbwd_cpart(self.dP, self.W2t, self.H, self.g, self.rstd, self.cpart, self.dH, self.dgpart)
+        coda_dg_combine(self.dgpart, self.dg)
+        coda_gemm_wgrad_gscale(self.H, self.dP, self.g, self.dW2t)
+        coda_gemm_res_prms_bwd(self.dH, self.X, self.W1t, self.dX, self.dW1t, self.dH)
 
     # -- unfused ablation -----------------------------------------------------
     def forward_unfused(self):

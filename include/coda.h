@@ -229,6 +229,29 @@ coda_status_t coda_gemm_dgrad_rmsbwd_noalloc(coda_handle_t h, const void* dP, co
                                              const void* g, const float* c, void* dH, float* dg, int64_t M,
                                              int64_t N2, int64_t d, void* stream);
 
+/* SwiGLU backward in the epilogue of the down projection's data gradient
+ * (the first "next" row: the upstream gradient dY of the SwiGLU output is
+ * never written to HBM).  With the down projection y = out W3 (nn.Linear
+ * layout W3t[d][F]) and its upstream gradient dYb:
+ *   dY[m][j] = sum_k dYb[m][k] W3t[k][j]                 (mainloop, on chip)
+ *   dP = bf16(rstd[m] * dZ), dZ = d(silu(z_gate) * z_up) applied to dY
+ *   cpart[m][t] = sum over the gate columns j of 256-column tile t (and their
+ *                 up columns) of dZ * z                  (block reduction)
+ * so that c[m] = rstd[m]^2 / d * sum_t cpart[m][t] (coda_swiglu_bwd's c).
+ * dYb bf16 [M][d], W3t bf16 [d][F], z bf16 [M][2F], rstd fp32 [M],
+ * dP bf16 [M][2F], cpart fp32 [M][coda_prms_num_tiles(F)]. */
+coda_status_t coda_gemm_dgrad_swiglu_bwd(coda_handle_t h, const void* dYb, const void* W3t, const void* z,
+                                         const float* rstd, void* dP, float* cpart, int64_t M, int64_t d, int64_t F,
+                                         void* stream);
+
+/* coda_gemm_dgrad_rmsbwd with c formed in its epilogue from the partial sums
+ * of coda_gemm_dgrad_swiglu_bwd: c[m] = rstd[m]^2 / d * sum_t cpart[m][t]
+ * (Tc = coda_prms_num_tiles(F) columns); everything else as
+ * coda_gemm_dgrad_rmsbwd. */
+coda_status_t coda_gemm_dgrad_rmsbwd_cpart(coda_handle_t h, const void* dP, const void* W2t, const void* H,
+                                           const void* g, const float* rstd, const float* cpart, int64_t Tc,
+                                           void* dH, float* dgpart, int64_t M, int64_t N2, int64_t d, void* stream);
+
 /* dg[k] = sum_r dgpart[r][k] (fixed order).  dgpart fp32 [rows][d], dg fp32 [d]. */
 coda_status_t coda_dg_combine(coda_handle_t h, const float* dgpart, int64_t rows, int64_t d, float* dg,
                               void* stream);

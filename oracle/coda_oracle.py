@@ -22,7 +22,8 @@ __all__ = [
     "block_backward", "stage_swiglu_bwd", "stage_dgrad2_rmsbwd",
     "stage_wgrad2", "stage_dgrad1", "stage_wgrad1", "logits_rows",
     "lse_rows", "lse_tile_partials", "lse_combine", "ce_forward",
-    "ce_backward", "argmax_lowest", "ce_weight_grad_given_lse",
+    "ce_backward", "argmax_lowest", "ce_weight_grad_given_lse", "down_proj_dgrad",
+    "swiglu_c_partials",
 ]
 
 
@@ -196,6 +197,26 @@ def stage_swiglu_bwd(dY, z, rstd, d: int):
     r = np.asarray(rstd, np.float64)
     zz = np.asarray(z, np.float64)
     return r[:, None] * dZ, (r * r / d) * np.sum(dZ * zz, axis=1)
+
+
+def down_proj_dgrad(dYb, W3t):
+    """Gradient reaching the SwiGLU output through a down projection
+    y = out W3 (nn.Linear layout W3t[d, F]): dY[m, j] = sum_k dYb[m, k]
+    W3t[k, j]."""
+    return np.asarray(dYb, np.float64) @ np.asarray(W3t, np.float64)
+
+
+def swiglu_c_partials(dY, z, bn: int):
+    """Per (row, tile of bn gate columns) partial sums of dZ * z over the gate
+    columns of the tile and the matching up columns: the block reduction a
+    SwiGLU-backward epilogue emits; sum_j of them times r^2 / d is c of
+    stage_swiglu_bwd."""
+    z = np.asarray(z, np.float64)
+    F = z.shape[1] // 2
+    dZ = swiglu_backward(dY, z)
+    prod = dZ[:, :F] * z[:, :F] + dZ[:, F:] * z[:, F:]
+    T = -(-F // bn)
+    return np.stack([prod[:, j * bn:(j + 1) * bn].sum(axis=1) for j in range(T)], axis=1)
 
 
 def stage_dgrad2_rmsbwd(dP, W2t, g, h, c):

@@ -1,0 +1,100 @@
+"""The "next" rows built on the hot path, against the fp64 oracle:
+
+* the SwiGLU backward in the epilogue of the down projection's data-gradient
+  GEMM (dY stays on chip; c is formed from per-tile partial sums inside the
+  RMSNorm-backward epilogue of dgrad2);
+
+graded per stage on the GPU's own stage inputs (elementwise) and end to end
+against the chain rule (Frobenius).  Synced write-up, section 尾声 (the
+re-parameterisation holds for SwiGLU and for the backward) and 实验结果
+(SwiGLU backward)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from coda_inputs import BlockShape, block_inputs, down_proj_inputs
+from tests._parity import assert_device_ok, assert_elem, assert_frob, f64
+
+pytestmark = pytest.mark.gpu
+
+C = pytest.importorskip("gemm_epilogue_transformer_tma_gb300")
+from gemm_epilogue_transformer_tma_gb300.path import BlockBuffers  # noqa: E402
+
+SHAPES = {
+    "ragged": BlockShape("ragged", 300, 200, 328, 528),
+    "whole": BlockShape("whole", 384, 256, 512, 1024),
+}
+
+
+@pytest.fixture(params=[True, False], ids=["sm_pair", "single_sm"])
+def pairing(request):
+    C.coda_set_sm_pairing(request.param)
+    yield request.param
+    C.coda_set_sm_pairing(True)
+
+
+def _setup(s):
+    x = {k: v.cuda() for k, v in block_inputs(s, 0, "cpu", with_dy=False).items()}
+    dp = {k: v.cuda() for k, v in down_proj_inputs(s, 0, "cpu").items()}
+    b = BlockBuffers(dict(x, dY=torch.empty(s.M, s.F, dtype=torch.bfloat16, device="cuda")))
+    b.forward()
+    return x, dp, b
+
+
+@pytest.mark.parametrize("name", ["ragged", "whole"])
+def test_down_proj_dgrad_swiglu_bwd_stage(name, pairing):
+    s = SHAPES[name]
+    x, dp, b = _setup(s)
+    cpart = torch.empty(s.M, C.coda_prms_num_tiles(s.F), device="cuda")
+    C.coda_gemm_dgrad_swiglu_bwd(dp["dYb"], dp["W3t"], b.z, b.rstd, b.dP, cpart)
+    assert_device_ok()
+    dY = O.down_proj_dgrad(f64(dp["dYb"]), f64(dp["W3t"]))
+    z, rstd = f64(b.z), f64(b.rstd)
+    dP_ref, c_ref = O.stage_swiglu_bwd(dY, z, rstd, s.d)
+    assert_elem(b.dP, dP_ref, "dP")
+    cp_ref = O.swiglu_c_partials(dY, z, 256)
+    assert_elem(cpart, cp_ref, "cpart")
+    assert_elem(f64(cpart).sum(axis=1) * rstd ** 2 / s.d, c_ref, "c from cpart")
+
+
+@pytest.mark.parametrize("name", ["ragged", "whole"])
+def test_dgrad_rmsbwd_with_cpart_stage(name, pairing):
+    s = SHAPES[name]
+    x, dp, b = _setup(s)
+    cpart = torch.empty(s.M, C.coda_prms_num_tiles(s.F), device="cuda")
+    C.coda_gemm_dgrad_swiglu_bwd(dp["dYb"], dp["W3t"], b.z, b.rstd, b.dP, cpart)
+    C.coda_gemm_dgrad_rmsbwd_cpart(b.dP, b.W2t, b.H, b.g, b.rstd, cpart, b.dH, b.dgpart)
+    C.coda_dg_combine(b.dgpart, b.dg)
+    assert_device_ok()
+    c = f64(cpart).sum(axis=1) * f64(b.rstd) ** 2 / s.d
+    dH_ref, dg_ref = O.stage_dgrad2_rmsbwd(f64(b.dP), f64(x["W2t"]), f64(x["g"]), f64(b.H), c)
+    assert_elem(b.dH, dH_ref, "dH")
+    assert_elem(b.dg, dg_ref, "dg")
+
+
+def test_backward_from_down_proj_end_to_end():
+    s = SHAPES["ragged"]
+    x, dp, b = _setup(s)
+    b.backward_from_down_proj(dp["dYb"], dp["W3t"])
+    assert_device_ok()
+    dY = O.down_proj_dgrad(f64(dp["dYb"]), f64(dp["W3t"]))
+    ref = O.block_backward(*(f64(x[k]) for k in ("X", "W1t", "R", "g", "W2t")), dY, s.eps, True)
+    for k_gpu, k_ref in (("dH", "dR"), ("dX", "dX"), ("dW1t", "dW1t"), ("dW2t", "dW2t"), ("dg", "dg")):
+        assert_frob(getattr(b, k_gpu), ref[k_ref], f"{k_gpu} e2e")
+
+
+def test_fused_matches_unfused_route():
+    """dY through HBM (plain GEMM to bf16 + the streaming SwiGLU backward) vs
+    on chip: same dP up to the bf16 rounding of dY."""
+    s = SHAPES["whole"]
+    x, dp, b = _setup(s)
+    cpart = torch.empty(s.M, C.coda_prms_num_tiles(s.F), device="cuda")
+    C.coda_gemm_dgrad_swiglu_bwd(dp["dYb"], dp["W3t"], b.z, b.rstd, b.dP, cpart)
+    dP_fused = b.dP.clone()
+    dY = torch.empty(s.M, s.F, dtype=torch.bfloat16, device="cuda")
+    C.coda_gemm(dp["dYb"], False, dp["W3t"], True, dY, s.M, s.F, s.d)
+    C.coda_swiglu_bwd(dY, b.z, b.rstd, b.dP, b.c, s.d)
+    assert_device_ok()
+    assert_frob(dP_fused, f64(b.dP), "dP fused vs unfused", tol=1e-2)
+    np.testing.assert_allclose(f64(cpart).sum(axis=1) * f64(b.rstd) ** 2 / s.d, f64(b.c), rtol=2e-2, atol=1e-6)

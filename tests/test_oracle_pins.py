@@ -338,3 +338,33 @@ def test_ce_weight_grad_given_lse_matches_full_backward():
     lse = O.lse_rows(O.logits_rows(H, Wt))
     np.testing.assert_allclose(O.ce_weight_grad_given_lse(H, Wt[cols], cols, y, lse, M), full[cols],
                                rtol=1e-12, atol=1e-14)
+
+
+def test_down_proj_dgrad_bruteforce():
+    r = rng(31)
+    dYb = r.standard_normal((3, 4))
+    W3t = r.standard_normal((4, 5))
+    ref = np.array([[sum(dYb[m, k] * W3t[k, j] for k in range(4)) for j in range(5)] for m in range(3)])
+    np.testing.assert_allclose(O.down_proj_dgrad(dYb, W3t), ref, rtol=1e-13, atol=1e-14)
+
+
+@pytest.mark.parametrize("bn", [1, 3, 8, 11])
+def test_swiglu_c_partials_sum_to_c(bn):
+    """the partials, brute-forced per tile, reproduce stage_swiglu_bwd's c"""
+    r = rng(37)
+    M, F, d = 4, 11, 7
+    z = r.standard_normal((M, 2 * F))
+    dY = r.standard_normal((M, F))
+    rstd = r.uniform(0.5, 2.0, M)
+    cp = O.swiglu_c_partials(dY, z, bn)
+    assert cp.shape == (M, -(-F // bn))
+    _, c = O.stage_swiglu_bwd(dY, z, rstd, d)
+    np.testing.assert_allclose(cp.sum(axis=1) * rstd ** 2 / d, c, rtol=1e-12)
+    # brute force of one tile from the SwiGLU derivative's closed form
+    m, j = 2, 0
+    tot = 0.0
+    for n in range(0, min(bn, F)):
+        zg, zu, dy = z[m, n], z[m, F + n], dY[m, n]
+        s = 1 / (1 + math.exp(-zg))
+        tot += dy * zu * s * (1 + zg * (1 - s)) * zg + dy * zg * s * zu
+    assert cp[m, j] == pytest.approx(tot, rel=1e-12)
