@@ -21,6 +21,9 @@ LIB_PATH = os.path.join(_HERE, "libcoda.so")
 
 CODA_EPI_SWIGLU = 0
 CODA_EPI_PLAIN = 1
+# columns covered by one block-reduction partial (psum, CE statistics, c
+# partials): partial j of a row covers columns [128 j, 128 j + 128)
+PARTIAL_COLS = 128
 
 STATUS_NAMES = {
     0: "CODA_OK", 1: "CODA_ERR_INVALID_ARG", 2: "CODA_ERR_ALIGNMENT", 3: "CODA_ERR_UNSUPPORTED",

@@ -8,7 +8,7 @@ namespace {
 constexpr int kBN = 256;
 }  // namespace
 
-int ce_tile_cols() { return kBN; }
+int ce_tile_cols() { return PART_COLS; }
 
 cudaError_t gemm_ce_stats(const LaunchCtx& c, const __nv_bfloat16* H, const __nv_bfloat16* Wt, const int32_t* labels,
                           float* pmax, float* psum, int32_t* parg, float* zy, int M, int d, int V, int T) {

@@ -8,7 +8,7 @@ namespace {
 constexpr int kBN = 256;
 }  // namespace
 
-int prms_tile_cols() { return kBN; }
+int prms_tile_cols() { return PART_COLS; }
 
 cudaError_t gemm_res_prms(const LaunchCtx& c, const __nv_bfloat16* X, const __nv_bfloat16* W1t,
                           const __nv_bfloat16* R, __nv_bfloat16* H, float* psum, int M, int K1, int d, int T) {

@@ -10,14 +10,18 @@
 // the epilogue exposes elementwise, vector load/store, tile load/store,
 // block-reduction and stateful primitives).
 //
-// CTA = 6 warps:
+// CTA = 10 warps:
 //   warp 0       TMA producer: fills a STAGES-deep shared-memory ring with A
 //                and B tiles (128-byte swizzle), completion on mbarriers.
 //   warp 1       TMEM allocator and MMA issuer: one elected thread issues
 //                tcgen05.mma (M=128, N=BN, K=16) into one of two TMEM
 //                accumulator buffers and commits to mbarriers.
-//   warps 2..5   epilogue: tcgen05.ld the accumulator (one row per thread),
-//                run the epilogue program, store to HBM, release the buffer.
+//   warps 2..9   epilogue: tcgen05.ld the accumulator (one row per thread;
+//                two warps per TMEM lane quadrant, each taking half of the
+//                tile's columns), run the epilogue program, store to HBM,
+//                release the buffer.  Block reductions along a row (partial
+//                RMS, CE statistics, SwiGLU-backward partials) are therefore
+//                per half tile (PART_COLS columns).
 // Two TMEM buffers let the epilogue of tile i overlap the mainloop of i+1.
 //
 // Operand layouts (row-major storage, element = bf16):
@@ -39,8 +43,9 @@ namespace coda {
 constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int UMMA_K = 16;
-constexpr int GEMM_THREADS = 192;
-constexpr int EPI_THREADS = 128;
+constexpr int GEMM_THREADS = 320;  // producer, MMA, 8 epilogue warps
+constexpr int EPI_THREADS = 256;
+constexpr int PART_COLS = 128;     // columns per block-reduction partial (half a tile)
 
 struct GemmShape {
   int M, N, K;        // logical problem (N = output columns the epilogue sees)
@@ -62,6 +67,8 @@ struct EpiCtx {
   int m;              // global row
   int quad;           // TMEM lane quadrant of this warp, 0..3
   int lane;
+  int c0, c1;         // this thread's columns of the tile: [c0, c1)
+  int part;           // index of its half-tile partial along the row (tn * 2 + half)
   uint32_t taddr;     // TMEM address of (first lane of quadrant, column 0 of this accumulator)
 };
 
@@ -252,6 +259,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   } else {
     // ------------------------------------------------------------- epilogue
     const int quad = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int row = quad * 32 + lane;
     int it = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
@@ -275,6 +283,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       c.m = tm * BM + row;
       c.quad = quad;
       c.lane = lane;
+      c.c0 = half * (BN / 2);
+      c.c1 = c.c0 + BN / 2;
+      c.part = tn * 2 + half;
       c.taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN);
       Epi::template run<BN>(ep, c);
       tc_fence_before();
@@ -349,7 +360,7 @@ __device__ __forceinline__ float rstd_from_psum(const float* psum, int T, float 
   float acc = 0.f;
   for (int j = 0; j < T; ++j) acc += p[j];
   const float r = 1.0f / sqrtf(acc * inv_d + eps);
-  if (rstd_out != nullptr && c.tn == 0) rstd_out[c.m] = r;
+  if (rstd_out != nullptr && c.tn == 0 && c.c0 == 0) rstd_out[c.m] = r;
   return r;
 }
 
@@ -378,7 +389,7 @@ struct EpiStore {
         rs = p.row_scale[c.m];
     }
 #pragma unroll 1
-    for (int cc = 0; cc < BN; cc += 32) {
+    for (int cc = c.c0; cc < c.c1; cc += 32) {
       float v[32];
       tmem_ld32(c.taddr + cc, v);
       const int n0 = c.tn * BN + cc;
@@ -408,7 +419,7 @@ struct EpiStoreF32 {
   static __device__ __forceinline__ void run(const Params& p, const EpiCtx& c) {
     const bool row_ok = c.m < c.M;
 #pragma unroll 1
-    for (int cc = 0; cc < BN; cc += 32) {
+    for (int cc = c.c0; cc < c.c1; cc += 32) {
       float v[32];
       tmem_ld32(c.taddr + cc, v);
       const int n0 = c.tn * BN + cc;
@@ -449,7 +460,7 @@ struct EpiResPrms {
     const bool row_ok = c.m < c.M;
     float ss = 0.f;
 #pragma unroll 1
-    for (int cc = 0; cc < BN; cc += 32) {
+    for (int cc = c.c0; cc < c.c1; cc += 32) {
       float v[32];
       tmem_ld32(c.taddr + cc, v);
       const int n0 = c.tn * BN + cc;
@@ -465,7 +476,7 @@ struct EpiResPrms {
         store_bf16x32(p.H + static_cast<int64_t>(c.m) * p.ldh + n0, c.N - n0, v);
       }
     }
-    if (row_ok) p.psum[static_cast<int64_t>(c.m) * p.T + c.tn] = ss;
+    if (row_ok && c.tn * BN + c.c0 < c.N) p.psum[static_cast<int64_t>(c.m) * p.T + c.part] = ss;
   }
 };
 
@@ -495,7 +506,7 @@ struct EpiRowscaleSwiglu {
     float r = 0.f;
     if (row_ok) r = p.psum != nullptr ? rstd_from_psum(p.psum, p.T, p.inv_d, p.eps, p.rstd_out, c) : p.rstd[c.m];
 #pragma unroll 1
-    for (int cc = 0; cc < HB; cc += 32) {
+    for (int cc = c.c0 / 2; cc < c.c1 / 2; cc += 32) {
       float g[32], u[32];
       tmem_ld32(c.taddr + cc, g);
       tmem_ld32(c.taddr + HB + cc, u);
@@ -555,7 +566,7 @@ struct EpiDgradRms {
       }
     }
 #pragma unroll 1
-    for (int cc = 0; cc < BN; cc += 32) {
+    for (int cc = c.c0; cc < c.c1; cc += 32) {
       float a[32];
       tmem_ld32(c.taddr + cc, a);
       const int n0 = c.tn * BN + cc;
@@ -605,7 +616,7 @@ struct EpiSwigluBwd {
     const int64_t row = static_cast<int64_t>(c.m) * 2 * p.F;
     float cp = 0.f;
 #pragma unroll 1
-    for (int cc = 0; cc < BN; cc += 32) {
+    for (int cc = c.c0; cc < c.c1; cc += 32) {
       float dy[32];
       tmem_ld32(c.taddr + cc, dy);
       const int j0 = c.tn * BN + cc;
@@ -627,7 +638,7 @@ struct EpiSwigluBwd {
         store_bf16x32(p.dP + row + p.F + j0, nv, zu);
       }
     }
-    if (row_ok) p.cpart[static_cast<int64_t>(c.m) * p.T + c.tn] = cp;
+    if (row_ok && c.tn * BN + c.c0 < p.F) p.cpart[static_cast<int64_t>(c.m) * p.T + c.part] = cp;
   }
 };
 
@@ -649,12 +660,12 @@ struct EpiCeStats {
   static __device__ __forceinline__ void run(const Params& p, const EpiCtx& c) {
     const bool row_ok = c.m < c.M;
     const int y = row_ok ? p.labels[c.m] : -1;
-    if (row_ok && c.tn == 0 && (y < 0 || y >= c.N)) atomicOr(p.status, DEV_ERR_LABEL_RANGE);
+    if (row_ok && c.tn == 0 && c.c0 == 0 && (y < 0 || y >= c.N)) atomicOr(p.status, DEV_ERR_LABEL_RANGE);
     float mx = -INFINITY, se = 0.f, zy = 0.f;
     int am = -1;
     bool found = false;
 #pragma unroll 1
-    for (int cc = 0; cc < BN; cc += 32) {
+    for (int cc = c.c0; cc < c.c1; cc += 32) {
       float v[32];
       tmem_ld32(c.taddr + cc, v);
       const int n0 = c.tn * BN + cc;
@@ -687,8 +698,8 @@ struct EpiCeStats {
         }
       }
     }
-    if (row_ok) {
-      const int64_t o = static_cast<int64_t>(c.m) * p.T + c.tn;
+    if (row_ok && c.tn * BN + c.c0 < c.N) {
+      const int64_t o = static_cast<int64_t>(c.m) * p.T + c.part;
       p.pmax[o] = mx;
       p.psum[o] = se;
       p.parg[o] = am;
@@ -714,7 +725,7 @@ struct EpiCeGrad {
     const float l = row_ok ? p.lse[c.m] : 0.f;
     const int y = row_ok ? p.labels[c.m] - p.v0 : -1;
 #pragma unroll 1
-    for (int cc = 0; cc < BN; cc += 32) {
+    for (int cc = c.c0; cc < c.c1; cc += 32) {
       float v[32];
       tmem_ld32(c.taddr + cc, v);
       const int n0 = c.tn * BN + cc;

@@ -106,7 +106,10 @@ coda_status_t coda_set_sm_pairing(coda_handle_t h, int enable);
  * coda_set_wait_timeout_ns.  Not for production use. */
 coda_status_t coda_debug_skip_first_stage(coda_handle_t h, int enable);
 
-/* Columns of the partial-RMS buffer for hidden width d: ceil(d / BN1). */
+/* Columns of a block-reduction partial buffer over n columns: ceil(n / 128).
+ * Partial j of a row covers columns [128 j, 128 j + 128) (half of a 256-column
+ * output tile).  Used for the partial RMS (n = d), the SwiGLU-backward c
+ * partials (n = F) and the LM-head statistics (n = V). */
 int64_t coda_prms_num_tiles(int64_t d);
 
 /* Rows of the dg partial buffer of coda_gemm_dgrad_rmsbwd: 4 * ceil(M/128). */
@@ -140,7 +143,7 @@ coda_status_t coda_fold_rmsnorm_weight(coda_handle_t h, const void* W2t, const v
 
 /* GEMM1 with the residual + partial-RMS epilogue (section 尾声):
  *   H[m][n] = bf16( sum_k X[m][k] W1t[n][k] + R[m][n] )
- *   psum[m][j] = sum over n in column tile j of H[m][n]^2   (fp32, H as stored)
+ *   psum[m][j] = sum over n in [128 j, 128 j + 128) of H[m][n]^2  (fp32, H as stored)
  * X bf16 [M][K1], W1t bf16 [d][K1], R bf16 [M][d], H bf16 [M][d],
  * psum fp32 [M][coda_prms_num_tiles(d)].  H may not alias R. */
 coda_status_t coda_gemm_res_prms(coda_handle_t h, const void* X, const void* W1t, const void* R, void* H,
@@ -235,7 +238,7 @@ coda_status_t coda_gemm_dgrad_rmsbwd_noalloc(coda_handle_t h, const void* dP, co
  * layout W3t[d][F]) and its upstream gradient dYb:
  *   dY[m][j] = sum_k dYb[m][k] W3t[k][j]                 (mainloop, on chip)
  *   dP = bf16(rstd[m] * dZ), dZ = d(silu(z_gate) * z_up) applied to dY
- *   cpart[m][t] = sum over the gate columns j of 256-column tile t (and their
+ *   cpart[m][t] = sum over the gate columns j in [128 t, 128 t + 128) (and their
  *                 up columns) of dZ * z                  (block reduction)
  * so that c[m] = rstd[m]^2 / d * sum_t cpart[m][t] (coda_swiglu_bwd's c).
  * dYb bf16 [M][d], W3t bf16 [d][F], z bf16 [M][2F], rstd fp32 [M],
@@ -291,7 +294,7 @@ size_t coda_lmhead_ce_workspace_bytes(int64_t M, int64_t d, int64_t V, int with_
 
 /* Mean softmax cross-entropy of the logits L = Hs Wt^T against labels,
  * without ever writing an [M][V] logits tensor:
- *   per (row, 256-column vocabulary tile): max, sum exp(L - max), argmax,
+ *   per (row, 128-column vocabulary block): max, sum exp(L - max), argmax,
  *   label logit (GEMM epilogue); combine: lse[m] = log sum_v exp L[m][v];
  *   loss = mean_m (lse[m] - L[m][y_m]); argmax[m] = first maximal column.
  * If dHs is not NULL the gradients are produced too, vocabulary chunk by

@@ -44,13 +44,13 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_host_queries(lib):
-    assert lib.coda_prms_num_tiles(4096) == 16
-    assert lib.coda_prms_num_tiles(328) == 2
+    assert lib.coda_prms_num_tiles(4096) == 32   # 128-column partials
+    assert lib.coda_prms_num_tiles(328) == 3
     assert lib.coda_dgpart_rows(300) == 12
     assert lib.coda_bwd_workspace_bytes(0, 64, 128) == 0
     M, d, N2 = 8192, 4096, 28672
     assert lib.coda_bwd_workspace_bytes(M, d, N2) >= M * N2 * 2 + M * 4 + 4 * (M // 128) * d * 4
-    assert lib.coda_lmhead_ce_workspace_bytes(8192, 2048, 128256, 0) >= 3 * 8192 * 501 * 4
+    assert lib.coda_lmhead_ce_workspace_bytes(8192, 2048, 128256, 0) >= 3 * 8192 * 1002 * 4
     assert lib.coda_lmhead_ce_workspace_bytes(8192, 2048, 128256, 1) > lib.coda_lmhead_ce_workspace_bytes(
         8192, 2048, 128256, 0)
     assert lib.coda_status_string(0) == b"ok"

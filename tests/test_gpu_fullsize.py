@@ -70,7 +70,7 @@ def check_block(shape, backward: bool):
     # a2 GEMM1 + residual, partial RMS
     H = rows_of(b.H, rows)
     assert_elem(H, O.gemm_residual(rows_of(b.X, rows), W1t, rows_of(b.R, rows)), "H")
-    assert_elem(rows_of(b.psum, rows), O.partial_sumsq(H, 256), "psum", tol=1e-4)
+    assert_elem(rows_of(b.psum, rows), O.partial_sumsq(H, C.PARTIAL_COLS), "psum", tol=1e-4)
     # a3 combine
     rstd = f64(b.rstd)[rows]
     assert_elem(rstd, O.rstd_from_partials(rows_of(b.psum, rows), d, shape.eps), "rstd", tol=1e-5)

@@ -53,7 +53,7 @@ def test_down_proj_dgrad_swiglu_bwd_stage(name, pairing):
     z, rstd = f64(b.z), f64(b.rstd)
     dP_ref, c_ref = O.stage_swiglu_bwd(dY, z, rstd, s.d)
     assert_elem(b.dP, dP_ref, "dP")
-    cp_ref = O.swiglu_c_partials(dY, z, 256)
+    cp_ref = O.swiglu_c_partials(dY, z, C.PARTIAL_COLS)
     assert_elem(cpart, cp_ref, "cpart")
     assert_elem(f64(cpart).sum(axis=1) * rstd ** 2 / s.d, c_ref, "c from cpart")
 

@@ -86,7 +86,7 @@ def check_forward(s: BlockShape, b: BlockBuffers, x: dict):
     H = f64(b.H)
     assert_elem(b.W2gt, O.fold_weight(W2t, g), "W2gt")
     assert_elem(b.H, O.gemm_residual(X, W1t, R), "H")
-    bn = 256
+    bn = C.PARTIAL_COLS
     assert_elem(b.psum, O.partial_sumsq(H, bn), "psum", tol=1e-4)
     assert_elem(b.rstd, O.rstd_from_partials(f64(b.psum), s.d, EPS), "rstd", tol=1e-5)
     z_ref = O.rowscale_gemm(H, f64(b.W2gt), f64(b.rstd))
