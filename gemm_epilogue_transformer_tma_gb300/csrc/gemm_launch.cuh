@@ -29,7 +29,7 @@ cudaError_t launch_gemm_kernel(const LaunchCtx& c, const CUtensorMap& ta, const 
   KernelCtl ctl{c.status, c.timeout_ns, c.skip_first_stage};
   const int tiles = sh.tiles_m * sh.tiles_n;
   const int grid = std::max(1, std::min(tiles, c.num_sms));
-  return launch_chained(c, kern, dim3(grid), dim3(GEMM_THREADS), L::TOTAL, ta, tb, tb2, sh, ctl, ep);
+  return launch_chained(c, kern, dim3(grid), dim3(gemm_threads<Epi>()), L::TOTAL, ta, tb, tb2, sh, ctl, ep);
 }
 
 template <int BN, int STAGES, bool A_MN, bool B_MN, bool B_DUAL, class Epi>
@@ -58,7 +58,7 @@ cudaError_t launch_gemm2_kernel(const LaunchCtx& c, const CUtensorMap& ta, const
   if (max_pairs[dev] == 0) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * (c.num_sms / 2), 1, 1);
-    cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
+    cfg.blockDim = dim3(gemm_threads<Epi>(), 1, 1);
     cfg.dynamicSmemBytes = L::TOTAL;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
@@ -74,7 +74,7 @@ cudaError_t launch_gemm2_kernel(const LaunchCtx& c, const CUtensorMap& ta, const
   }
   const int tiles = sh.tiles_m * sh.tiles_n;
   const int clusters = std::max(1, std::min(tiles, max_pairs[dev]));
-  return launch_chained(c, kern, dim3(2 * clusters), dim3(GEMM_THREADS), L::TOTAL, ta, tb, tb2, sh, ctl, ep);
+  return launch_chained(c, kern, dim3(2 * clusters), dim3(gemm_threads<Epi>()), L::TOTAL, ta, tb, tb2, sh, ctl, ep);
 }
 
 // The 2-SM pair kernel (default) or the 1-SM kernel, 256-column tiles.

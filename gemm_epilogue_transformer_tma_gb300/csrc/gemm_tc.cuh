@@ -10,18 +10,22 @@
 // the epilogue exposes elementwise, vector load/store, tile load/store,
 // block-reduction and stateful primitives).
 //
-// CTA = 10 warps:
+// CTA = 2 + E warps (E = 4 or 8 epilogue warps, a trait of the epilogue program):
 //   warp 0       TMA producer: fills a STAGES-deep shared-memory ring with A
 //                and B tiles (128-byte swizzle), completion on mbarriers.
 //   warp 1       TMEM allocator and MMA issuer: one elected thread issues
 //                tcgen05.mma (M=128, N=BN, K=16) into one of two TMEM
 //                accumulator buffers and commits to mbarriers.
-//   warps 2..9   epilogue: tcgen05.ld the accumulator (one row per thread;
-//                two warps per TMEM lane quadrant, each taking half of the
-//                tile's columns), run the epilogue program, store to HBM,
-//                release the buffer.  Block reductions along a row (partial
-//                RMS, CE statistics, SwiGLU-backward partials) are therefore
-//                per half tile (PART_COLS columns).
+//   warps 2..    epilogue: tcgen05.ld the accumulator (one row per thread),
+//                run the epilogue program, store to HBM, release the buffer.
+//                The program runs once per 128-column half of the tile: with
+//                8 warps, two per TMEM lane quadrant take one half each; with
+//                4 warps, each warp runs both halves in turn.  Block
+//                reductions along a row (partial RMS, CE statistics,
+//                SwiGLU-backward partials) are therefore per half tile
+//                (PART_COLS columns).  Memory-heavy epilogues use 8 warps for
+//                more loads in flight; the others use 4, which leaves the
+//                producer's and MMA issuer's sub-partitions less crowded.
 // Two TMEM buffers let the epilogue of tile i overlap the mainloop of i+1.
 //
 // Operand layouts (row-major storage, element = bf16):
@@ -43,8 +47,9 @@ namespace coda {
 constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int UMMA_K = 16;
-constexpr int GEMM_THREADS = 320;  // producer, MMA, 8 epilogue warps
-constexpr int EPI_THREADS = 256;
+// CTA size for an epilogue program with kEpiWarps epilogue warps (4 or 8)
+template <class Epi>
+constexpr int gemm_threads() { return 64 + 32 * Epi::kEpiWarps; }
 constexpr int PART_COLS = 128;     // columns per block-reduction partial (half a tile)
 
 struct GemmShape {
@@ -101,7 +106,7 @@ __device__ __forceinline__ void raise_error(const KernelCtl& ctl, volatile int* 
 }
 
 template <int BN, int STAGES, bool A_MN, bool B_MN, bool B_DUAL, class Epi>
-__global__ void __launch_bounds__(GEMM_THREADS, 1)
+__global__ void __launch_bounds__(gemm_threads<Epi>(), 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmB2, const GemmShape sh, const KernelCtl ctl,
                    const typename Epi::Params ep) {
@@ -130,7 +135,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], EPI_THREADS);
+      mbar_init(&tempty[a], 32 * Epi::kEpiWarps);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -258,8 +263,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------- epilogue
+    constexpr int HALVES = 8 / Epi::kEpiWarps;  // halves of the tile per warp
     const int quad = warp & 3;
-    const int half = (warp - 2) >> 2;
+    const int first_half = HALVES == 1 ? (warp - 2) >> 2 : 0;
     const int row = quad * 32 + lane;
     int it = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
@@ -283,11 +289,15 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       c.m = tm * BM + row;
       c.quad = quad;
       c.lane = lane;
-      c.c0 = half * (BN / 2);
-      c.c1 = c.c0 + BN / 2;
-      c.part = tn * 2 + half;
       c.taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN);
-      Epi::template run<BN>(ep, c);
+#pragma unroll 1
+      for (int hh = 0; hh < HALVES; ++hh) {
+        const int half = first_half + hh;
+        c.c0 = half * (BN / 2);
+        c.c1 = c.c0 + BN / 2;
+        c.part = tn * 2 + half;
+        Epi::template run<BN>(ep, c);
+      }
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
     }
@@ -366,6 +376,7 @@ __device__ __forceinline__ float rstd_from_psum(const float* psum, int T, float 
 
 // C = bf16(row_scale[m] * col_scale[n] * acc); both scales optional.
 struct EpiStore {
+  static constexpr int kEpiWarps = 4;
   struct Params {
     __nv_bfloat16* out;
     int64_t ldo;
@@ -410,6 +421,7 @@ struct EpiStore {
 
 // fp32 output, overwrite (beta = 0) or accumulate (beta = 1).
 struct EpiStoreF32 {
+  static constexpr int kEpiWarps = 4;
   struct Params {
     float* out;
     int64_t ldo;
@@ -447,6 +459,7 @@ struct EpiStoreF32 {
 // GEMM1 epilogue: h = bf16(acc + R); store h; psum[m, tn] = sum over the
 // tile's columns of h^2 (h as stored, i.e. after rounding to bf16).
 struct EpiResPrms {
+  static constexpr int kEpiWarps = 4;
   struct Params {
     const __nv_bfloat16* R;
     int64_t ldr;
@@ -485,6 +498,7 @@ struct EpiResPrms {
 // save z (bf16) for the backward.  In plain mode (swiglu == 0, single box)
 // out = rstd[m] * acc.
 struct EpiRowscaleSwiglu {
+  static constexpr int kEpiWarps = 4;
   struct Params {
     const float* rstd;
     __nv_bfloat16* out;
@@ -535,6 +549,7 @@ struct EpiRowscaleSwiglu {
 //   acc = dP W2^T ; dh = g * acc - c[m] * h ; dgpart[4*tm + quad, n] =
 //   sum over the warp's 32 rows of acc * h  (block reduction across lanes).
 struct EpiDgradRms {
+  static constexpr int kEpiWarps = 4;
   struct Params {
     const __nv_bfloat16* H;
     int64_t ldh;
@@ -601,6 +616,7 @@ struct EpiDgradRms {
 // (a block reduction the RMSNorm backward later merges into c).  dY itself
 // never leaves the chip.
 struct EpiSwigluBwd {
+  static constexpr int kEpiWarps = 8;  // loads z and stores dP: more loads in flight
   struct Params {
     const __nv_bfloat16* z;  // [M, 2F]
     const float* rstd;
@@ -647,6 +663,7 @@ struct EpiSwigluBwd {
 // (lowest column on ties), and the label logit when the label falls in the
 // tile.  Columns >= N (vocabulary tail) are masked out.
 struct EpiCeStats {
+  static constexpr int kEpiWarps = 4;
   struct Params {
     const int32_t* labels;
     float* pmax;
@@ -711,6 +728,7 @@ struct EpiCeStats {
 // LM-head backward epilogue: dL = (exp(L - lse[m]) - [n == y_m]) / M as bf16
 // into a vocabulary-chunk buffer (column n of the chunk = vocabulary v0 + n).
 struct EpiCeGrad {
+  static constexpr int kEpiWarps = 4;
   struct Params {
     const int32_t* labels;
     const float* lse;

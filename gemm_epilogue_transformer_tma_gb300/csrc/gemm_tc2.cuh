@@ -16,8 +16,8 @@
 //                MMAs, and commits to empty[s] / tfull[] of both CTAs
 //                (multicast).  Both CTAs' warp 1 allocate TMEM together
 //                (cta_group::2).
-//   warps 2..9   epilogue on this CTA's 128 rows (two warps per lane quadrant,
-//                each on half of the columns); release the accumulator by
+//   warps 2..    epilogue on this CTA's 128 rows (4 or 8 warps, see
+//                gemm_tc.cuh); release the accumulator by
 //                arriving on the leader's tempty[].
 // All waits are bounded as in the 1-SM kernel.  After an abort the leader
 // waits (bounded) for every stage it armed, which counts the peer's bytes
@@ -46,7 +46,7 @@ struct Gemm2Smem {
 };
 
 template <int BN, int STAGES, bool A_MN, bool B_MN, bool B_DUAL, class Epi>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi>(), 1)
     gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmB2, const GemmShape sh, const KernelCtl ctl,
                     const typename Epi::Params ep) {
@@ -80,7 +80,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 16);  // lane 0 of the 8 epilogue warps of each CTA
+      mbar_init(&tempty[a], 2 * Epi::kEpiWarps);  // lane 0 of every epilogue warp of both CTAs
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -227,8 +227,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------- epilogue
+    constexpr int HALVES = 8 / Epi::kEpiWarps;
     const int quad = warp & 3;
-    const int half = (warp - 2) >> 2;
+    const int first_half = HALVES == 1 ? (warp - 2) >> 2 : 0;
     const int row = quad * 32 + lane;
     const uint32_t leader_tempty = mapa_shared(smem_u32(tempty), 0);
     int it = 0;
@@ -253,11 +254,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
       c.m = c.tm * 128 + row;
       c.quad = quad;
       c.lane = lane;
-      c.c0 = half * (BN / 2);
-      c.c1 = c.c0 + BN / 2;
-      c.part = tn * 2 + half;
       c.taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN);
-      Epi::template run<BN>(ep, c);
+#pragma unroll 1
+      for (int hh = 0; hh < HALVES; ++hh) {
+        const int half = first_half + hh;
+        c.c0 = half * (BN / 2);
+        c.c1 = c.c0 + BN / 2;
+        c.part = tn * 2 + half;
+        Epi::template run<BN>(ep, c);
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(leader_tempty + static_cast<uint32_t>(acc * 8));
