@@ -302,6 +302,29 @@ def bench_down_proj_swiglu_bwd(C, b, shape, steps, warmup):
             "on_chip_tflops": flops / (t_chip / n * 1e-3) / 1e12}
 
 
+def bench_qkv_rope(C, steps, warmup, M=8192, S=2048, d=4096, n_heads=32):
+    """QKV projection of the 7B-size block (MHA, 32 heads of 128) with RoPE
+    in the epilogue, against the plain GEMM followed by a standalone RoPE
+    kernel."""
+    g = torch.Generator(device="cuda").manual_seed(11)
+    X = torch.randn(M, d, generator=g, device="cuda").to(torch.bfloat16)
+    W = (torch.randn(3 * n_heads * 128, d, generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+    cos_t = torch.empty(S, 64, device="cuda")
+    sin_t = torch.empty(S, 64, device="cuda")
+    C.coda_rope_table(cos_t, sin_t)
+    N = 3 * n_heads * 128
+    qkv = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    fused = [lambda: C.coda_gemm_qkv_rope(X, W, cos_t, sin_t, qkv, n_heads, n_heads)]
+    unfused = [lambda: C.coda_gemm(X, False, W, False, qkv, M, N, d),
+               lambda: C.coda_rope_apply(qkv, cos_t, sin_t, n_heads, n_heads)]
+    n = max(3, steps)
+    t_f, _ = time_steps(fused, n, warmup, stage_events=False)
+    t_u, _ = time_steps(unfused, n, warmup, stage_events=False)
+    flops = 2.0 * M * N * d
+    return {"M": M, "d": d, "heads": n_heads, "head_dim": 128, "seq": S, "fused_ms": t_f / n,
+            "unfused_ms": t_u / n, "speedup": t_u / t_f, "fused_tflops": flops / (t_f / n * 1e-3) / 1e12}
+
+
 def bench_lmhead(C, steps, warmup):
     s = LMHEAD
     x = ce_inputs(s, 0, "cuda")
@@ -502,6 +525,8 @@ def main():
         del b, x, fs, calls
         torch.cuda.empty_cache()
         extras["lmhead_ce"] = bench_lmhead(C, args.steps, args.warmup)
+        torch.cuda.empty_cache()
+        extras["next_qkv_rope"] = bench_qkv_rope(C, args.steps, args.warmup)
 
     if rank == 0:
         line = {

@@ -73,6 +73,9 @@ SIGNATURES = {
     "coda_gemm_rowscale_swiglu_bwd": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
                                              _I64, _I64, _I64, _P]),
     "coda_gemm_res_prms_bwd": (_INT, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
+    "coda_rope_table": (_INT, [_P, _P, _P, _I64, _I64, _F32, _P]),
+    "coda_gemm_qkv_rope": (_INT, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64, _P]),
+    "coda_rope_apply": (_INT, [_P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _P]),
     "coda_lmhead_ce_workspace_bytes": (_SZ, [_I64, _I64, _I64, _INT]),
     "coda_lmhead_ce": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I64, _I64, _I64, _P]),
     "coda_unfused_workspace_bytes": (_SZ, [_I64, _I64, _I64]),
@@ -394,6 +397,39 @@ def coda_gemm_res_prms_bwd(dH, X, W1t, dX, dW1t, dR=None, stream=None):
     _check(load_library().coda_gemm_res_prms_bwd(_h(X), _ptr(dH, BF, "dH"), _ptr(X, BF, "X"), _ptr(W1t, BF, "W1t"),
                                                  _ptr(dX, BF, "dX"), _ptr(dW1t, BF, "dW1t"), _ptr(dR, BF, "dR"),
                                                  M, K1, d, _stream(stream)), "coda_gemm_res_prms_bwd")
+
+
+def coda_rope_table(cos_t, sin_t, base=10000.0, stream=None):
+    """cos / sin tables [S, head_dim / 2] of the rotary embedding."""
+    S, half = cos_t.shape
+    _shape(sin_t, (S, half), "sin_t")
+    _check(load_library().coda_rope_table(_h(cos_t), _ptr(cos_t, F32, "cos_t"), _ptr(sin_t, F32, "sin_t"), S,
+                                          2 * half, base, _stream(stream)), "coda_rope_table")
+
+
+def coda_gemm_qkv_rope(X, Wqkv_t, cos_t, sin_t, qkv, n_q_heads, n_kv_heads, head_dim=128, stream=None):
+    """qkv = X Wqkv with RoPE on the q and k heads in the GEMM epilogue."""
+    M, d = X.shape
+    N = (n_q_heads + 2 * n_kv_heads) * head_dim
+    S = cos_t.shape[0]
+    _shape(Wqkv_t, (N, d), "Wqkv_t")
+    _shape(qkv, (M, N), "qkv")
+    _shape(cos_t, (S, head_dim // 2), "cos_t")
+    _check(load_library().coda_gemm_qkv_rope(_h(X), _ptr(X, BF, "X"), _ptr(Wqkv_t, BF, "Wqkv_t"),
+                                             _ptr(cos_t, F32, "cos_t"), _ptr(sin_t, F32, "sin_t"),
+                                             _ptr(qkv, BF, "qkv"), M, d, n_q_heads, n_kv_heads, head_dim, S,
+                                             _stream(stream)), "coda_gemm_qkv_rope")
+
+
+def coda_rope_apply(qkv, cos_t, sin_t, n_q_heads, n_kv_heads, head_dim=128, stream=None):
+    """Standalone in-place RoPE on an existing qkv (the unfused baseline)."""
+    M, N = qkv.shape
+    S = cos_t.shape[0]
+    if N != (n_q_heads + 2 * n_kv_heads) * head_dim:
+        raise ValueError("qkv width does not match the head counts")
+    _check(load_library().coda_rope_apply(_h(qkv), _ptr(qkv, BF, "qkv"), _ptr(cos_t, F32, "cos_t"),
+                                          _ptr(sin_t, F32, "sin_t"), M, n_q_heads, n_kv_heads, head_dim, S,
+                                          _stream(stream)), "coda_rope_apply")
 
 
 def coda_lmhead_ce_workspace_bytes(M: int, d: int, V: int, with_grads: bool) -> int:

@@ -451,6 +451,47 @@ coda_status_t coda_gemm_res_prms_bwd(coda_handle_t h, const void* dH, const void
 }
 
 // ---------------------------------------------------------------------------
+coda_status_t coda_rope_table(coda_handle_t h, float* cos_t, float* sin_t, int64_t S, int64_t head_dim, float base,
+                              void* stream) {
+  CODA_TRY(Check().handle(h).ptr(cos_t).ptr(sin_t).st);
+  if (S <= 0 || S > kMaxExtent || head_dim <= 0 || !(base > 1.f)) return CODA_ERR_INVALID_ARG;
+  if (head_dim % 16 != 0) return CODA_ERR_ALIGNMENT;
+  return from_cuda(launch_rope_table(ctx_of(h, stream), cos_t, sin_t, S, head_dim, static_cast<double>(base)));
+}
+
+namespace {
+coda_status_t check_heads(int64_t n_q, int64_t n_kv, int64_t head_dim, int64_t S) {
+  if (n_q <= 0 || n_kv < 0 || head_dim <= 0 || S <= 0 || S > kMaxExtent) return CODA_ERR_INVALID_ARG;
+  if ((n_q + 2 * n_kv) * head_dim > kMaxExtent) return CODA_ERR_INVALID_ARG;
+  if (head_dim % 16 != 0) return CODA_ERR_ALIGNMENT;
+  return CODA_OK;
+}
+}  // namespace
+
+coda_status_t coda_gemm_qkv_rope(coda_handle_t h, const void* X, const void* Wqkv_t, const float* cos_t,
+                                 const float* sin_t, void* qkv, int64_t M, int64_t d, int64_t n_q_heads,
+                                 int64_t n_kv_heads, int64_t head_dim, int64_t S, void* stream) {
+  CODA_TRY(Check().handle(h).rows(M).mptr(X, M).ptr(Wqkv_t).ptr(cos_t).ptr(sin_t).mptr(qkv, M).cols(d).st);
+  CODA_TRY(check_heads(n_q_heads, n_kv_heads, head_dim, S));
+  if (head_dim != 128) return CODA_ERR_UNSUPPORTED;
+  if (M == 0) return CODA_OK;
+  const int64_t N = (n_q_heads + 2 * n_kv_heads) * head_dim;
+  return from_cuda(gemm_qkv_rope(ctx_of(h, stream), static_cast<const bf16*>(X), static_cast<const bf16*>(Wqkv_t),
+                                 cos_t, sin_t, static_cast<bf16*>(qkv), int(M), int(d), int(N),
+                                 int((n_q_heads + n_kv_heads) * head_dim), int(S)));
+}
+
+coda_status_t coda_rope_apply(coda_handle_t h, void* qkv, const float* cos_t, const float* sin_t, int64_t M,
+                              int64_t n_q_heads, int64_t n_kv_heads, int64_t head_dim, int64_t S, void* stream) {
+  CODA_TRY(Check().handle(h).rows(M).mptr(qkv, M).ptr(cos_t).ptr(sin_t).st);
+  CODA_TRY(check_heads(n_q_heads, n_kv_heads, head_dim, S));
+  if (M == 0) return CODA_OK;
+  const int64_t N = (n_q_heads + 2 * n_kv_heads) * head_dim;
+  return from_cuda(launch_rope_apply(ctx_of(h, stream), static_cast<bf16*>(qkv), cos_t, sin_t, M, N,
+                                     (n_q_heads + n_kv_heads) * head_dim, head_dim, S));
+}
+
+// ---------------------------------------------------------------------------
 namespace {
 struct CeWs {
   float* pmax;

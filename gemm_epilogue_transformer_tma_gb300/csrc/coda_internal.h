@@ -100,6 +100,11 @@ cudaError_t gemm_ce_grad(const LaunchCtx& c, const __nv_bfloat16* H, const __nv_
                          const int32_t* labels, const float* lse, __nv_bfloat16* dL, int M, int d, int Vc, int v0,
                          float inv_M);
 
+// qkv = X Wqkv with RoPE (head_dim 128) on the first rot_cols columns.
+cudaError_t gemm_qkv_rope(const LaunchCtx& c, const __nv_bfloat16* X, const __nv_bfloat16* Wqkv_t,
+                          const float* cos_t, const float* sin_t, __nv_bfloat16* qkv, int M, int d, int N,
+                          int rot_cols, int S);
+
 int ce_tile_cols();    // vocabulary columns per CE statistics tile
 int prms_tile_cols();  // columns per partial-RMS tile of GEMM1
 
@@ -116,6 +121,11 @@ cudaError_t launch_ce_combine(const LaunchCtx& c, const float* pmax, const float
                               int32_t* argmax, float* row_loss);
 cudaError_t launch_mean(const LaunchCtx& c, const float* v, int64_t n, float* out);
 cudaError_t launch_f32_to_bf16(const LaunchCtx& c, const float* in, __nv_bfloat16* out, int64_t n);
+// cos / sin tables [S, head_dim/2] of the rotary embedding, computed in fp64
+cudaError_t launch_rope_table(const LaunchCtx& c, float* cos_t, float* sin_t, int64_t S, int64_t head_dim, double base);
+// RoPE in place on the first rot_cols columns of qkv [M, N] (standalone, unfused)
+cudaError_t launch_rope_apply(const LaunchCtx& c, __nv_bfloat16* qkv, const float* cos_t, const float* sin_t,
+                              int64_t M, int64_t N, int64_t rot_cols, int64_t head_dim, int64_t S);
 // unfused ablation kernels
 cudaError_t launch_add_rmsnorm(const LaunchCtx& c, const __nv_bfloat16* A, const __nv_bfloat16* R,
                                const __nv_bfloat16* g, __nv_bfloat16* H, float* rstd, __nv_bfloat16* Nrm, int64_t M,

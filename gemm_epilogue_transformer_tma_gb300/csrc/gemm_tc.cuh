@@ -658,6 +658,59 @@ struct EpiSwigluBwd {
   }
 };
 
+// QKV projection with rotary position embedding in the epilogue (rotate-half
+// pairing, head_dim 128 = one 128-column half tile = one head): for a q or k
+// head at position p = m mod S, out_i = x_i cos - x_{i+64} sin and
+// out_{i+64} = x_{i+64} cos + x_i sin with cos/sin read from [S, 64] tables
+// (the vector-load primitive); v heads (columns >= rot_cols) pass through.
+struct EpiRope {
+  static constexpr int kEpiWarps = 4;
+  struct Params {
+    __nv_bfloat16* out;
+    int64_t ldo;
+    const float* cos_t;  // [S, 64]
+    const float* sin_t;  // [S, 64]
+    int S;
+    int rot_cols;        // (heads of q + heads of k) * 128
+  };
+  template <int BN>
+  static __device__ __forceinline__ void run(const Params& p, const EpiCtx& c) {
+    const int nh = c.tn * BN + c.c0;  // first column of this half tile's head
+    if (nh >= c.N) return;            // the same for every lane of the warp
+    const bool row_ok = c.m < c.M;
+    const bool rot = nh < p.rot_cols;
+    const int64_t tab = row_ok ? static_cast<int64_t>(c.m % p.S) * 64 : 0;
+    __nv_bfloat16* o = p.out + static_cast<int64_t>(c.m) * p.ldo + nh;
+#pragma unroll 1
+    for (int cc = 0; cc < 64; cc += 32) {
+      float x1[32], x2[32];
+      tmem_ld32(c.taddr + c.c0 + cc, x1);
+      tmem_ld32(c.taddr + c.c0 + 64 + cc, x2);
+      if (row_ok) {
+        if (rot) {
+          const float4* cs4 = reinterpret_cast<const float4*>(p.cos_t + tab + cc);
+          const float4* sn4 = reinterpret_cast<const float4*>(p.sin_t + tab + cc);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float4 cq = __ldg(cs4 + q), sq = __ldg(sn4 + q);
+            const float cv[4] = {cq.x, cq.y, cq.z, cq.w};
+            const float sv[4] = {sq.x, sq.y, sq.z, sq.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int i = 4 * q + k;
+              const float a = x1[i], b = x2[i];
+              x1[i] = fmaf(a, cv[k], -b * sv[k]);
+              x2[i] = fmaf(b, cv[k], a * sv[k]);
+            }
+          }
+        }
+        store_bf16x32(o + cc, c.N - (nh + cc), x1);
+        store_bf16x32(o + 64 + cc, c.N - (nh + 64 + cc), x2);
+      }
+    }
+  }
+};
+
 // LM-head forward epilogue: per (row, N-tile) running max and sum of
 // exp(L - max) (online rescaling across 32-column chunks), the tile argmax
 // (lowest column on ties), and the label logit when the label falls in the

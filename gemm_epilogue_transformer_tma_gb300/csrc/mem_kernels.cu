@@ -215,6 +215,54 @@ __global__ void f32_to_bf16_kernel(const float4* __restrict__ in, uint2* __restr
   }
 }
 
+// cos / sin of theta[p, i] = p * base^(-2 i / D), in double precision
+__global__ void rope_table_kernel(float* __restrict__ cos_t, float* __restrict__ sin_t, int64_t S, int half,
+                                  double base) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int64_t n = S * half;
+  for (int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; t < n;
+       t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t pos = t / half;
+    const int i = static_cast<int>(t - pos * half);
+    const double th = static_cast<double>(pos) * pow(base, -2.0 * i / (2.0 * half));
+    double sv, cv;
+    sincos(th, &sv, &cv);
+    cos_t[t] = static_cast<float>(cv);
+    sin_t[t] = static_cast<float>(sv);
+  }
+}
+
+// standalone RoPE (rotate-half) in place; one thread per 8 pairs of a head
+__global__ void rope_apply_kernel(__nv_bfloat16* __restrict__ qkv, const float* __restrict__ cos_t,
+                                  const float* __restrict__ sin_t, int64_t M, int64_t N, int64_t rot_heads,
+                                  int half, int64_t S) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int g8 = half / 8;
+  const int64_t n = M * rot_heads * g8;
+  for (int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; t < n;
+       t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t m = t / (rot_heads * g8);
+    const int64_t r = t - m * rot_heads * g8;
+    const int64_t head = r / g8;
+    const int i0 = static_cast<int>(r - head * g8) * 8;
+    __nv_bfloat16* x = qkv + m * N + head * 2 * half;
+    const float* cs = cos_t + (m % S) * half + i0;
+    const float* sn = sin_t + (m % S) * half + i0;
+    float a[8], b[8], o1[8], o2[8];
+    unpack_bf16x8(*reinterpret_cast<const uint4*>(x + i0), a);
+    unpack_bf16x8(*reinterpret_cast<const uint4*>(x + half + i0), b);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      o1[k] = fmaf(a[k], cs[k], -b[k] * sn[k]);
+      o2[k] = fmaf(b[k], cs[k], a[k] * sn[k]);
+    }
+    *reinterpret_cast<uint4*>(x + i0) = pack8(o1);
+    *reinterpret_cast<uint4*>(x + half + i0) = pack8(o2);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // unfused ablation kernels
 
@@ -406,6 +454,21 @@ cudaError_t launch_f32_to_bf16(const LaunchCtx& c, const float* in, __nv_bfloat1
   const int64_t n4 = n / 4;
   return launch_chained(c, f32_to_bf16_kernel, dim3(grid_for(c, n4, 256)), dim3(256), 0, reinterpret_cast<const float4*>(in),
                                                                  reinterpret_cast<uint2*>(out), n4);
+}
+
+cudaError_t launch_rope_table(const LaunchCtx& c, float* cos_t, float* sin_t, int64_t S, int64_t head_dim,
+                              double base) {
+  const int half = static_cast<int>(head_dim / 2);
+  return launch_chained(c, rope_table_kernel, dim3(grid_for(c, S * half, 256)), dim3(256), 0, cos_t, sin_t, S, half,
+                        base);
+}
+
+cudaError_t launch_rope_apply(const LaunchCtx& c, __nv_bfloat16* qkv, const float* cos_t, const float* sin_t,
+                              int64_t M, int64_t N, int64_t rot_cols, int64_t head_dim, int64_t S) {
+  const int half = static_cast<int>(head_dim / 2);
+  const int64_t rot_heads = rot_cols / head_dim;
+  return launch_chained(c, rope_apply_kernel, dim3(grid_for(c, M * rot_heads * (half / 8), 256)), dim3(256), 0, qkv,
+                        cos_t, sin_t, M, N, rot_heads, half, S);
 }
 
 cudaError_t launch_add_rmsnorm(const LaunchCtx& c, const __nv_bfloat16* A, const __nv_bfloat16* R,

@@ -285,6 +285,38 @@ coda_status_t coda_gemm_res_prms_bwd(coda_handle_t h, const void* dH, const void
                                      void* dW1t, void* dR, int64_t M, int64_t K1, int64_t d, void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* rotary position embedding on the QKV projection (section 五种积木: RoPE  */
+/* among the elementwise epilogue transforms)                                */
+/* ------------------------------------------------------------------------ */
+
+/* cos_t[p][i] = cos(p * base^(-2 i / head_dim)), sin_t likewise, for
+ * positions p < S and i < head_dim / 2, computed in double precision and
+ * stored fp32.  cos_t, sin_t fp32 [S][head_dim / 2]; head_dim a positive
+ * multiple of 16. */
+coda_status_t coda_rope_table(coda_handle_t h, float* cos_t, float* sin_t, int64_t S, int64_t head_dim, float base,
+                              void* stream);
+
+/* QKV projection with RoPE in the epilogue:
+ *   qkv[m][n] = sum_k X[m][k] Wqkv_t[n][k], columns [q heads | k heads | v heads]
+ *   then every q and k head (columns < (n_q_heads + n_kv_heads) * head_dim)
+ *   is rotated at position p = m mod S with rotate-half pairing:
+ *   out_i = x_i cos - x_{i+D/2} sin, out_{i+D/2} = x_{i+D/2} cos + x_i sin.
+ * X bf16 [M][d] (rows batch-major, S positions per sequence), Wqkv_t bf16
+ * [(n_q_heads + 2 n_kv_heads) * head_dim][d], cos_t/sin_t from
+ * coda_rope_table, qkv bf16 [M][(n_q_heads + 2 n_kv_heads) * head_dim].
+ * head_dim must be 128 (one head = half an output tile): other values
+ * return CODA_ERR_UNSUPPORTED. */
+coda_status_t coda_gemm_qkv_rope(coda_handle_t h, const void* X, const void* Wqkv_t, const float* cos_t,
+                                 const float* sin_t, void* qkv, int64_t M, int64_t d, int64_t n_q_heads,
+                                 int64_t n_kv_heads, int64_t head_dim, int64_t S, void* stream);
+
+/* The same rotation as a standalone in-place kernel on an existing qkv (the
+ * unfused baseline): qkv bf16 [M][(n_q_heads + 2 n_kv_heads) * head_dim],
+ * head_dim a multiple of 16. */
+coda_status_t coda_rope_apply(coda_handle_t h, void* qkv, const float* cos_t, const float* sin_t, int64_t M,
+                              int64_t n_q_heads, int64_t n_kv_heads, int64_t head_dim, int64_t S, void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* LM head: blocked log-sum-exp cross-entropy epilogue (section 五种积木:     */
 /* block reduction "block log-sum-exp", stateful max / sum-exp)              */
 /* ------------------------------------------------------------------------ */

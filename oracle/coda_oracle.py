@@ -23,7 +23,7 @@ __all__ = [
     "stage_wgrad2", "stage_dgrad1", "stage_wgrad1", "logits_rows",
     "lse_rows", "lse_tile_partials", "lse_combine", "ce_forward",
     "ce_backward", "argmax_lowest", "ce_weight_grad_given_lse", "down_proj_dgrad",
-    "swiglu_c_partials",
+    "swiglu_c_partials", "rope_angles", "rope_rotate_half", "qkv_rope",
 ]
 
 
@@ -340,3 +340,45 @@ def ce_weight_grad_given_lse(H, Wt_cols, cols, labels, lse, M: int):
     P = np.exp(L - np.asarray(lse, np.float64)[:, None])
     P -= (np.asarray(labels, np.int64)[:, None] == np.asarray(cols, np.int64)[None, :])
     return (P / M).T @ H
+
+
+# ----------------------------------------------------------------------------
+# rotary position embedding on the QKV projection (an elementwise epilogue
+# transform in the write-up's 五种积木 section)
+# ----------------------------------------------------------------------------
+
+def rope_angles(positions, head_dim: int, base: float = 10000.0):
+    """theta[p, i] = position_p * base^(-2 i / head_dim), i < head_dim / 2."""
+    pos = np.asarray(positions, np.float64)
+    i = np.arange(head_dim // 2, dtype=np.float64)
+    return pos[:, None] * base ** (-2.0 * i / head_dim)[None, :]
+
+
+def rope_rotate_half(x, positions, head_dim: int, base: float = 10000.0):
+    """Rotate each head of x[M, heads * head_dim] (rotate-half pairing: element
+    i pairs with i + head_dim/2): out_i = x_i cos - x_{i+D/2} sin,
+    out_{i+D/2} = x_{i+D/2} cos + x_i sin, angles from row m's position."""
+    x = np.asarray(x, np.float64)
+    M, n = x.shape
+    h = head_dim // 2
+    th = rope_angles(positions, head_dim, base)
+    cos, sin = np.cos(th), np.sin(th)
+    out = np.empty_like(x)
+    for s0 in range(0, n, head_dim):
+        a = x[:, s0:s0 + h]
+        b = x[:, s0 + h:s0 + head_dim]
+        out[:, s0:s0 + h] = a * cos - b * sin
+        out[:, s0 + h:s0 + head_dim] = b * cos + a * sin
+    return out
+
+
+def qkv_rope(X, Wqkv_t, n_q_heads: int, n_kv_heads: int, head_dim: int, seq_len: int, base: float = 10000.0):
+    """qkv = X Wqkv (nn.Linear layout Wqkv_t[(Hq + 2 Hkv) D, d], columns q | k |
+    v), then RoPE on the q and k heads at position m mod seq_len; v as is."""
+    qkv = matmul_nt(X, Wqkv_t)
+    M = qkv.shape[0]
+    pos = np.arange(M) % seq_len
+    rot = (n_q_heads + n_kv_heads) * head_dim
+    out = qkv.copy()
+    out[:, :rot] = rope_rotate_half(qkv[:, :rot], pos, head_dim, base)
+    return out

@@ -100,3 +100,66 @@ def test_fused_matches_unfused_route():
     # c is a sum with cancellation: the bf16 rounding of dY on the HBM route
     # moves rows near zero by ~1e-5 absolute, so compare on c's own scale
     assert_frob(f64(cpart).sum(axis=1) * f64(b.rstd) ** 2 / s.d, f64(b.c), "c fused vs unfused", tol=2e-2)
+
+
+# --------------------------------------------------------------------------
+# RoPE in the QKV projection's epilogue (rotate-half, head_dim 128)
+# --------------------------------------------------------------------------
+
+def _rope_inputs(M, d, n_heads, seed):
+    g = torch.Generator().manual_seed(seed)
+    X = torch.randn(M, d, generator=g).to(torch.bfloat16)
+    W = (torch.randn(n_heads * 128, d, generator=g) * 0.02).to(torch.bfloat16)
+    return X.cuda(), W.cuda()
+
+
+def _tables(S, base=10000.0):
+    cos_t = torch.empty(S, 64, device="cuda")
+    sin_t = torch.empty(S, 64, device="cuda")
+    C.coda_rope_table(cos_t, sin_t, base)
+    return cos_t, sin_t
+
+
+def test_rope_table():
+    cos_t, sin_t = _tables(2048)
+    assert_device_ok()
+    th = O.rope_angles(np.arange(2048), 128)
+    assert_elem(cos_t, np.cos(th), "cos", tol=1e-5)
+    assert_elem(sin_t, np.sin(th), "sin", tol=1e-5)
+
+
+@pytest.mark.parametrize("M,d,Hq,Hkv,S", [(300, 328, 4, 2, 128), (512, 512, 2, 1, 512), (264, 136, 3, 0, 100),
+                                          (256, 256, 2, 2, 64)])
+def test_gemm_qkv_rope_parity(M, d, Hq, Hkv, S, pairing):
+    X, W = _rope_inputs(M, d, Hq + 2 * Hkv, M + d)
+    cos_t, sin_t = _tables(S)
+    qkv = torch.empty(M, (Hq + 2 * Hkv) * 128, dtype=torch.bfloat16, device="cuda")
+    C.coda_gemm_qkv_rope(X, W, cos_t, sin_t, qkv, Hq, Hkv)
+    assert_device_ok()
+    ref = O.qkv_rope(f64(X), f64(W), Hq, Hkv, 128, S)
+    assert_elem(qkv, ref, "qkv")
+    assert_frob(qkv, ref, "qkv")
+
+
+def test_rope_apply_standalone_and_fused_agree():
+    M, d, Hq, Hkv, S = 512, 512, 4, 2, 128
+    X, W = _rope_inputs(M, d, Hq + 2 * Hkv, 7)
+    cos_t, sin_t = _tables(S)
+    N = (Hq + 2 * Hkv) * 128
+    plain = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    C.coda_gemm(X, False, W, False, plain, M, N, d)
+    ref = O.rope_rotate_half(f64(plain)[:, :(Hq + Hkv) * 128], np.arange(M) % S, 128)
+    C.coda_rope_apply(plain, cos_t, sin_t, Hq, Hkv)
+    fused = torch.empty_like(plain)
+    C.coda_gemm_qkv_rope(X, W, cos_t, sin_t, fused, Hq, Hkv)
+    assert_device_ok()
+    assert_elem(plain[:, :(Hq + Hkv) * 128], ref, "standalone RoPE")
+    assert_frob(fused, f64(plain), "fused vs unfused", tol=1e-2)
+
+
+def test_rope_rejects_other_head_dims():
+    lib = C.load_library()
+    p = torch.empty(16, device="cuda").data_ptr()
+    st = lib.coda_gemm_qkv_rope(C.handle(), p, p, p, p, p, 128, 128, 2, 1, 64, 16,
+                                torch.cuda.current_stream().cuda_stream)
+    assert st == 3

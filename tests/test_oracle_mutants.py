@@ -121,3 +121,34 @@ def test_mutant_ce_grad_missing_mean(monkeypatch):
         return {"dH": out["dH"] * M, "dWt": out["dWt"] * M}
     _patch(monkeypatch, "ce_backward", bad)
     _fails(P.test_ce_backward_finite_difference_and_row_sum)
+
+
+def test_mutant_rope_interleaved_pairs(monkeypatch):
+    """pairing (2i, 2i+1) instead of (i, i + D/2) must be caught"""
+    def bad(x, positions, head_dim, base=10000.0):
+        x = np.asarray(x, np.float64)
+        th = OC.rope_angles(positions, head_dim, base)
+        out = x.copy()
+        for s0 in range(0, x.shape[1], head_dim):
+            a = x[:, s0:s0 + head_dim:2]
+            b = x[:, s0 + 1:s0 + head_dim:2]
+            out[:, s0:s0 + head_dim:2] = a * np.cos(th) - b * np.sin(th)
+            out[:, s0 + 1:s0 + head_dim:2] = b * np.cos(th) + a * np.sin(th)
+        return out
+    _patch(monkeypatch, "rope_rotate_half", bad)
+    _fails(P.test_rope_two_dim_closed_form)
+
+
+def test_mutant_rope_rotation_sign(monkeypatch):
+    good = OC.rope_rotate_half
+    _patch(monkeypatch, "rope_rotate_half",
+           lambda x, positions, head_dim, base=10000.0: good(x, -np.asarray(positions, float), head_dim, base))
+    _fails(P.test_rope_two_dim_closed_form)
+
+
+def test_mutant_rope_exponent(monkeypatch):
+    """theta_i = p base^(-i/D) instead of base^(-2i/D)"""
+    _patch(monkeypatch, "rope_angles",
+           lambda positions, head_dim, base=10000.0: np.asarray(positions, float)[:, None]
+           * base ** (-np.arange(head_dim // 2) / head_dim)[None, :])
+    _fails(P.test_rope_two_dim_closed_form)

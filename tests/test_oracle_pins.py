@@ -368,3 +368,60 @@ def test_swiglu_c_partials_sum_to_c(bn):
         s = 1 / (1 + math.exp(-zg))
         tot += dy * zu * s * (1 + zg * (1 - s)) * zg + dy * zg * s * zu
     assert cp[m, j] == pytest.approx(tot, rel=1e-12)
+
+
+# --------------------------------------------------------------------------
+# RoPE
+# --------------------------------------------------------------------------
+
+def test_rope_position_zero_is_identity_and_norm_preserved():
+    r = rng(41)
+    x = r.standard_normal((5, 3 * 8))
+    np.testing.assert_array_equal(O.rope_rotate_half(x, np.zeros(5), 8), x)
+    y = O.rope_rotate_half(x, np.arange(5) * 37, 8)
+    for s0 in range(0, 24, 8):
+        for i in range(4):
+            n_in = x[:, s0 + i] ** 2 + x[:, s0 + i + 4] ** 2
+            n_out = y[:, s0 + i] ** 2 + y[:, s0 + i + 4] ** 2
+            np.testing.assert_allclose(n_out, n_in, rtol=1e-13)
+
+
+def test_rope_two_dim_closed_form():
+    # head_dim 2: one pair, angle = position (base^0 = 1)
+    x = np.array([[1.0, 2.0]])
+    p = 0.7
+    y = O.rope_rotate_half(x, np.array([p]), 2)
+    np.testing.assert_allclose(y, [[math.cos(p) - 2 * math.sin(p), 2 * math.cos(p) + math.sin(p)]], rtol=1e-15)
+    # head_dim 4, base 100: angles p and p / 10, pairs (0, 2) and (1, 3)
+    th = O.rope_angles([3.0], 4, 100.0)
+    np.testing.assert_allclose(th, [[3.0, 0.3]], rtol=1e-15)
+    x = np.array([[1.0, 2.0, 3.0, 4.0]])
+    a, b = 3.0, 0.3
+    expect = [1 * math.cos(a) - 3 * math.sin(a), 2 * math.cos(b) - 4 * math.sin(b),
+              3 * math.cos(a) + 1 * math.sin(a), 4 * math.cos(b) + 2 * math.sin(b)]
+    np.testing.assert_allclose(O.rope_rotate_half(x, [3.0], 4, 100.0), [expect], rtol=1e-14)
+
+
+def test_rope_scores_depend_only_on_relative_position():
+    r = rng(43)
+    q = r.standard_normal((1, 16))
+    k = r.standard_normal((1, 16))
+    def score(m, n):
+        return float((O.rope_rotate_half(q, [m], 16) @ O.rope_rotate_half(k, [n], 16).T).item())
+    for m, n, t in ((5, 2, 11), (100, 7, 1000), (0, 9, 3)):
+        assert score(m, n) == pytest.approx(score(m + t, n + t), rel=1e-10, abs=1e-12)
+
+
+def test_qkv_rope_rotates_q_and_k_only():
+    r = rng(47)
+    M, d, D, Hq, Hkv, S = 6, 8, 4, 2, 1, 3
+    X = r.standard_normal((M, d))
+    W = r.standard_normal(((Hq + 2 * Hkv) * D, d))
+    out = O.qkv_rope(X, W, Hq, Hkv, D, S)
+    plain = X @ W.T
+    rot = (Hq + Hkv) * D
+    np.testing.assert_allclose(out[:, rot:], plain[:, rot:], rtol=1e-14)
+    pos = np.arange(M) % S
+    np.testing.assert_allclose(out[:, :rot], O.rope_rotate_half(plain[:, :rot], pos, D), rtol=1e-13)
+    # rows at position 0 (m = 0, 3) are not rotated
+    np.testing.assert_allclose(out[[0, 3]], plain[[0, 3]], rtol=1e-14)
