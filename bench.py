@@ -141,7 +141,7 @@ class FusedStep:
     """The fused path's calls (stage name, call); CUDA events go between them.
     With fuse_rstd the light combine runs inside GEMM2's epilogue."""
 
-    def __init__(self, C, b, fuse_rstd=False):
+    def __init__(self, C, b, fuse_rstd=False, g_on_activation=False):
         self.C, self.b = C, b
         s = b
         gemm2 = "gemm2_prms_rowscale_swiglu" if fuse_rstd else "gemm2_rowscale_swiglu"
@@ -153,17 +153,24 @@ class FusedStep:
             "dgrad1": 2.0 * s.M * s.d * s.K1,
             "wgrad1": 2.0 * s.M * s.d * s.K1,
         }
-        fwd = [
-            ("fold", lambda: C.coda_fold_rmsnorm_weight(b.W2t, b.g, b.W2gt)),
-            ("gemm1_res_prms", lambda: C.coda_gemm_res_prms(b.X, b.W1t, b.R, b.H, b.psum)),
-        ]
+        if g_on_activation:
+            # g broadcast in GEMM1's epilogue (Hg), GEMM2 on the unfolded W2
+            fwd = [("gemm1_res_prms_g", lambda: C.coda_gemm_res_prms_g(b.X, b.W1t, b.R, b.g, b.H, b.Hg, b.psum))]
+            A2, B2 = b.Hg, b.W2t
+            self.flops["gemm1_res_prms_g"] = self.flops.pop("gemm1_res_prms")
+        else:
+            fwd = [
+                ("fold", lambda: C.coda_fold_rmsnorm_weight(b.W2t, b.g, b.W2gt)),
+                ("gemm1_res_prms", lambda: C.coda_gemm_res_prms(b.X, b.W1t, b.R, b.H, b.psum)),
+            ]
+            A2, B2 = b.H, b.W2gt
         if fuse_rstd:
-            fwd.append((gemm2, lambda: C.coda_gemm_prms_rowscale_swiglu(b.H, b.W2gt, b.psum, b.eps, b.rstd, b.out,
-                                                                        b.z, C.CODA_EPI_SWIGLU)))
+            fwd.append((gemm2, lambda: C.coda_gemm_prms_rowscale_swiglu(A2, B2, b.psum, b.eps, b.rstd, b.out, b.z,
+                                                                        C.CODA_EPI_SWIGLU)))
         else:
             fwd += [
                 ("rstd_combine", lambda: C.coda_rstd_combine(b.psum, b.d, b.eps, b.rstd)),
-                (gemm2, lambda: C.coda_gemm_rowscale_swiglu(b.H, b.W2gt, b.rstd, b.out, b.z, C.CODA_EPI_SWIGLU)),
+                (gemm2, lambda: C.coda_gemm_rowscale_swiglu(A2, B2, b.rstd, b.out, b.z, C.CODA_EPI_SWIGLU)),
             ]
         bwd = [
             ("swiglu_bwd", lambda: C.coda_swiglu_bwd(b.dY, b.z, b.rstd, b.dP, b.c, b.d)),
@@ -362,7 +369,8 @@ class E2EPipeline:
         second = dict(shared, X=torch.empty_like(b0.X), R=torch.empty_like(b0.R))
         if b0.with_backward:
             second["dY"] = torch.empty_like(b0.dY)
-        self.bufs = [b0, BlockBuffers(second, backward=b0.with_backward, fuse_rstd=b0.fuse_rstd)]
+        self.bufs = [b0, BlockBuffers(second, backward=b0.with_backward, fuse_rstd=b0.fuse_rstd,
+                                      g_on_activation=b0.g_on_activation)]
         self.inputs = ("X", "R", "dY") if b0.with_backward else ("X", "R")
         self.result = "dX" if b0.with_backward else "out"
         self.compute = torch.cuda.current_stream()
@@ -414,6 +422,8 @@ def main():
     ap.add_argument("--no-extras", action="store_true", help="skip ablation, LM-head and e2e legs")
     ap.add_argument("--fuse-rstd", action="store_true",
                     help="fold the rstd combine into GEMM2's epilogue (one launch fewer)")
+    ap.add_argument("--g-on-activation", action="store_true",
+                    help="apply the RMSNorm weight in GEMM1's epilogue (Hg) instead of folding it into W2")
     ap.add_argument("--single-sm", action="store_true",
                     help="GEMMs on one SM per tile instead of SM pairs")
     ap.add_argument("--tokens", type=int, default=0,
@@ -445,8 +455,8 @@ def main():
     C.coda_set_sm_pairing(not args.single_sm)
 
     x = block_inputs(shape, seed=rank, device="cuda")
-    b = BlockBuffers(x, backward=shape.backward, fuse_rstd=args.fuse_rstd)
-    fs = FusedStep(C, b, fuse_rstd=args.fuse_rstd)
+    b = BlockBuffers(x, backward=shape.backward, fuse_rstd=args.fuse_rstd, g_on_activation=args.g_on_activation)
+    fs = FusedStep(C, b, fuse_rstd=args.fuse_rstd, g_on_activation=args.g_on_activation)
     calls = fs.calls()
 
     def barrier():
@@ -537,6 +547,7 @@ def main():
                        "eps": shape.eps, "parallelism": "replicas" if world > 1 else "single-gpu",
                        "gemm": "1-SM tiles" if args.single_sm else "SM-pair tiles",
                        "rstd": "in GEMM2's epilogue" if args.fuse_rstd else "separate combine kernel",
+                       "g": "on the activation (GEMM1 epilogue)" if args.g_on_activation else "folded into W2",
                        "l2": "inputs larger than L2 (W2 alone is %d MB), no flush" % (shape.N2 * shape.d * 2 >> 20)},
             "pct_of_peak": 100.0 * value / world / peak,
             "pct_of_sustained_peak": 100.0 * value / world / peaks["bf16_tflops_sustained"],

@@ -59,6 +59,7 @@ SIGNATURES = {
     "coda_gemm": (_INT, [_P, _P, _INT, _P, _INT, _P, _I64, _I64, _I64, _P, _P, _P]),
     "coda_fold_rmsnorm_weight": (_INT, [_P, _P, _P, _P, _I64, _I64, _P]),
     "coda_gemm_res_prms": (_INT, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
+    "coda_gemm_res_prms_g": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "coda_rstd_combine": (_INT, [_P, _P, _I64, _I64, _I64, _F32, _P, _P]),
     "coda_gemm_rowscale_swiglu": (_INT, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _U32, _P]),
     "coda_gemm_prms_rowscale_swiglu": (_INT, [_P, _P, _P, _P, _I64, _F32, _P, _P, _P, _I64, _I64, _I64, _U32, _P]),
@@ -225,6 +226,23 @@ def coda_gemm_res_prms(X, W1t, R, H, psum, stream=None):
     _check(load_library().coda_gemm_res_prms(_h(X), _ptr(X, BF, "X"), _ptr(W1t, BF, "W1t"), _ptr(R, BF, "R"),
                                              _ptr(H, BF, "H"), _ptr(psum, F32, "psum"), M, K1, d, _stream(stream)),
            "coda_gemm_res_prms")
+
+
+def coda_gemm_res_prms_g(X, W1t, R, g, H, Hg, psum, stream=None):
+    """coda_gemm_res_prms that also writes Hg = bf16(H * g) (the RMSNorm
+    weight applied on the activation side)."""
+    M, K1 = X.shape
+    d = W1t.shape[0]
+    _shape(W1t, (d, K1), "W1t")
+    _shape(R, (M, d), "R")
+    _shape(g, (d,), "g")
+    _shape(H, (M, d), "H")
+    _shape(Hg, (M, d), "Hg")
+    _shape(psum, (M, coda_prms_num_tiles(d)), "psum")
+    _check(load_library().coda_gemm_res_prms_g(_h(X), _ptr(X, BF, "X"), _ptr(W1t, BF, "W1t"), _ptr(R, BF, "R"),
+                                               _ptr(g, BF, "g"), _ptr(H, BF, "H"), _ptr(Hg, BF, "Hg"),
+                                               _ptr(psum, F32, "psum"), M, K1, d, _stream(stream)),
+           "coda_gemm_res_prms_g")
 
 
 def coda_rstd_combine(psum, d: int, eps: float, rstd, stream=None):

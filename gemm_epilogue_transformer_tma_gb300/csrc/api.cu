@@ -251,6 +251,28 @@ coda_status_t coda_gemm_res_prms(coda_handle_t h, const void* X, const void* W1t
                                  int(coda_prms_num_tiles(d))));
 }
 
+coda_status_t coda_gemm_res_prms_g(coda_handle_t h, const void* X, const void* W1t, const void* R, const void* g,
+                                   void* H, void* Hg, float* psum, int64_t M, int64_t K1, int64_t d, void* stream) {
+  CODA_TRY(Check()
+               .handle(h)
+               .rows(M)
+               .mptr(X, M)
+               .ptr(W1t)
+               .mptr(R, M)
+               .ptr(g)
+               .mptr(H, M)
+               .mptr(Hg, M)
+               .mptr(psum, M)
+               .cols(K1)
+               .cols(d)
+               .st);
+  if (M == 0) return CODA_OK;
+  if (R == H || R == Hg || H == Hg) return CODA_ERR_INVALID_ARG;
+  return from_cuda(gemm_res_prms(ctx_of(h, stream), static_cast<const bf16*>(X), static_cast<const bf16*>(W1t),
+                                 static_cast<const bf16*>(R), static_cast<bf16*>(H), psum, int(M), int(K1), int(d),
+                                 int(coda_prms_num_tiles(d)), static_cast<const bf16*>(g), static_cast<bf16*>(Hg)));
+}
+
 coda_status_t coda_rstd_combine(coda_handle_t h, const float* psum, int64_t M, int64_t T, int64_t d, float eps,
                                 float* rstd, void* stream) {
   CODA_TRY(Check().handle(h).rows(M).mptr(psum, M).mptr(rstd, M).st);

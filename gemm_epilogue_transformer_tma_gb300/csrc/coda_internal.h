@@ -64,9 +64,11 @@ cudaError_t gemm_store(const LaunchCtx& c, const __nv_bfloat16* A, bool a_mn, co
 cudaError_t gemm_store_f32(const LaunchCtx& c, const __nv_bfloat16* A, bool a_mn, const __nv_bfloat16* B, bool b_mn,
                            float* C, int M, int N, int K, bool accumulate);
 
-// h = bf16(X W1 + R); psum[m, j] = sum of h^2 over column tile j.
+// h = bf16(X W1 + R); psum[m, j] = sum of h^2 over column block j; with
+// Hg != null also Hg = bf16(h * g).
 cudaError_t gemm_res_prms(const LaunchCtx& c, const __nv_bfloat16* X, const __nv_bfloat16* W1t,
-                          const __nv_bfloat16* R, __nv_bfloat16* H, float* psum, int M, int K1, int d, int T);
+                          const __nv_bfloat16* R, __nv_bfloat16* H, float* psum, int M, int K1, int d, int T,
+                          const __nv_bfloat16* g = nullptr, __nv_bfloat16* Hg = nullptr);
 
 // z = rstd * (H W2g); out = silu(z_gate) * z_up (swiglu) or z (plain).
 // With psum != null the row scale comes from the partial sums of squares

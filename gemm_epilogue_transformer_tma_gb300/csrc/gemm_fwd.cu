@@ -11,10 +11,11 @@ constexpr int kBN = 256;
 int prms_tile_cols() { return PART_COLS; }
 
 cudaError_t gemm_res_prms(const LaunchCtx& c, const __nv_bfloat16* X, const __nv_bfloat16* W1t,
-                          const __nv_bfloat16* R, __nv_bfloat16* H, float* psum, int M, int K1, int d, int T) {
+                          const __nv_bfloat16* R, __nv_bfloat16* H, float* psum, int M, int K1, int d, int T,
+                          const __nv_bfloat16* g, __nv_bfloat16* Hg) {
   CUtensorMap ta, tb;
   if (!make_operand_maps(&ta, &tb, X, false, W1t, false, M, d, K1, b_box_rows(c))) return cudaErrorInvalidValue;
-  EpiResPrms::Params ep{R, d, H, d, psum, T};
+  EpiResPrms::Params ep{R, d, H, d, psum, T, g, Hg};
   return run_gemm<false, false, false, EpiResPrms>(c, ta, tb, tb, M, d, K1, (d + kBN - 1) / kBN, ep);
 }
 

@@ -467,6 +467,11 @@ struct EpiResPrms {
     int64_t ldh;
     float* psum;
     int T;  // psum columns
+    // optional: the RMSNorm weight broadcast along the row (vector load) and
+    // a second output Hg = bf16(H * g), the second GEMM's A operand when g is
+    // applied on the activation side instead of being folded into W2
+    const __nv_bfloat16* g;
+    __nv_bfloat16* Hg;
   };
   template <int BN>
   static __device__ __forceinline__ void run(const Params& p, const EpiCtx& c) {
@@ -487,6 +492,12 @@ struct EpiResPrms {
           ss = fmaf(hb, hb, ss);
         }
         store_bf16x32(p.H + static_cast<int64_t>(c.m) * p.ldh + n0, c.N - n0, v);
+        if (p.Hg != nullptr) {
+          load_bf16x32(p.g + n0, c.N - n0, r);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] *= r[i];
+          store_bf16x32(p.Hg + static_cast<int64_t>(c.m) * p.ldh + n0, c.N - n0, v);
+        }
       }
     }
     if (row_ok && c.tn * BN + c.c0 < c.N) p.psum[static_cast<int64_t>(c.m) * p.T + c.part] = ss;

@@ -11,7 +11,7 @@ import torch
 
 from . import (CODA_EPI_PLAIN, CODA_EPI_SWIGLU, coda_bwd_workspace_bytes, coda_dg_combine,
                coda_dgpart_rows, coda_fold_rmsnorm_weight, coda_gemm_dgrad_rmsbwd, coda_gemm_prms_rowscale_swiglu,
-               coda_gemm_dgrad_rmsbwd_cpart, coda_gemm_dgrad_swiglu_bwd, coda_gemm_res_prms,
+               coda_gemm_dgrad_rmsbwd_cpart, coda_gemm_dgrad_swiglu_bwd, coda_gemm_res_prms, coda_gemm_res_prms_g,
                coda_gemm_res_prms_bwd, coda_gemm_rowscale_swiglu, coda_gemm_rowscale_swiglu_bwd,
                coda_gemm_wgrad_gscale, coda_prms_num_tiles, coda_rstd_combine, coda_swiglu_bwd,
                coda_unfused_bwd, coda_unfused_fwd, coda_unfused_workspace_bytes)
@@ -29,13 +29,14 @@ class BlockBuffers:
     """
 
     def __init__(self, inputs: dict, swiglu: bool = True, backward: bool = True, eps: float = 1e-5,
-                 unfused: bool = False, fuse_rstd: bool = False):
+                 unfused: bool = False, fuse_rstd: bool = False, g_on_activation: bool = False):
         dev = inputs["X"].device
         self.swiglu = swiglu
         self.eps = eps
         self.with_backward = backward
         self.unfused = unfused
         self.fuse_rstd = fuse_rstd
+        self.g_on_activation = g_on_activation
         for k, v in inputs.items():
             setattr(self, k, v.contiguous())
         self.M, self.K1 = self.X.shape
@@ -46,6 +47,7 @@ class BlockBuffers:
         e = dict(device=dev)
         self.W2gt = torch.empty(N2, d, dtype=BF, **e)
         self.H = torch.empty(M, d, dtype=BF, **e)
+        self.Hg = torch.empty(M, d, dtype=BF, **e) if g_on_activation else None
         self.psum = torch.empty(M, coda_prms_num_tiles(d), dtype=F32, **e)
         self.rstd = torch.empty(M, dtype=F32, **e)
         self.z = torch.empty(M, N2, dtype=BF, **e)
@@ -70,21 +72,26 @@ class BlockBuffers:
         GEMM2 + row scale + SwiGLU (z saved for the backward)."""
         if self.unfused:
             return self.forward_unfused()
-        coda_fold_rmsnorm_weight(self.W2t, self.g, self.W2gt)
-        coda_gemm_res_prms(self.X, self.W1t, self.R, self.H, self.psum)
+        if self.g_on_activation:
+            # g broadcast in GEMM1's epilogue: GEMM2 takes Hg and the unfolded W2
+            coda_gemm_res_prms_g(self.X, self.W1t, self.R, self.g, self.H, self.Hg, self.psum)
+            A2, B2 = self.Hg, self.W2t
+        else:
+            coda_fold_rmsnorm_weight(self.W2t, self.g, self.W2gt)
+            coda_gemm_res_prms(self.X, self.W1t, self.R, self.H, self.psum)
+            A2, B2 = self.H, self.W2gt
         if self.fuse_rstd:
             # the combine runs inside GEMM2's epilogue, which also stores rstd
             flags = CODA_EPI_SWIGLU if self.swiglu else CODA_EPI_PLAIN
-            coda_gemm_prms_rowscale_swiglu(self.H, self.W2gt, self.psum, self.eps, self.rstd,
+            coda_gemm_prms_rowscale_swiglu(A2, B2, self.psum, self.eps, self.rstd,
                                            self.out if self.swiglu else self.z,
                                            (self.z if save_z else None) if self.swiglu else None, flags)
             return
         coda_rstd_combine(self.psum, self.d, self.eps, self.rstd)
         if self.swiglu:
-            coda_gemm_rowscale_swiglu(self.H, self.W2gt, self.rstd, self.out,
-                                      self.z if save_z else None, CODA_EPI_SWIGLU)
+            coda_gemm_rowscale_swiglu(A2, B2, self.rstd, self.out, self.z if save_z else None, CODA_EPI_SWIGLU)
         else:
-            coda_gemm_rowscale_swiglu(self.H, self.W2gt, self.rstd, self.z, None, CODA_EPI_PLAIN)
+            coda_gemm_rowscale_swiglu(A2, B2, self.rstd, self.z, None, CODA_EPI_PLAIN)
 
     def backward_stages(self):
         """The backward as separate stage calls (dP, c, dgpart stay visible)."""

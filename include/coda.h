@@ -149,6 +149,17 @@ coda_status_t coda_fold_rmsnorm_weight(coda_handle_t h, const void* W2t, const v
 coda_status_t coda_gemm_res_prms(coda_handle_t h, const void* X, const void* W1t, const void* R, void* H,
                                  float* psum, int64_t M, int64_t K1, int64_t d, void* stream);
 
+/* coda_gemm_res_prms that also applies the RMSNorm weight on the activation
+ * side: the epilogue broadcasts g along each row (section 五种积木: vector
+ * load of the RMSNorm weight) and writes a second output
+ *   Hg[m][n] = bf16( H[m][n] * g[n] )
+ * which the second GEMM then takes as its A operand with the unfolded W2t
+ * (coda_gemm_rowscale_swiglu(Hg, W2t, ...)).  This replaces the per-step
+ * coda_fold_rmsnorm_weight pass over W2 with one extra [M][d] write.  g bf16
+ * [d], Hg bf16 [M][d]; the rest as coda_gemm_res_prms. */
+coda_status_t coda_gemm_res_prms_g(coda_handle_t h, const void* X, const void* W1t, const void* R, const void* g,
+                                   void* H, void* Hg, float* psum, int64_t M, int64_t K1, int64_t d, void* stream);
+
 /* The light auxiliary combine (section 尾声):
  *   rstd[m] = 1 / sqrt( sum_j psum[m][j] / d + eps )
  * psum fp32 [M][T], rstd fp32 [M]. */

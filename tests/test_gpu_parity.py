@@ -262,3 +262,41 @@ def test_fwd_bwd_end_to_end_fused_rstd():
     for k_gpu, k_ref in (("out", "out"), ("rstd", "rstd"), ("dH", "dR"), ("dX", "dX"), ("dW1t", "dW1t"),
                          ("dW2t", "dW2t"), ("dg", "dg")):
         assert_frob(getattr(b, k_gpu), ref[k_ref], f"{k_gpu} e2e")
+
+
+# --------------------------------------------------------------------------
+# RMSNorm weight applied on the activation side (Hg written by GEMM1's
+# epilogue, GEMM2 on the unfolded W2): no per-step fold pass over W2
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", ["ragged", "whole", "one_row"])
+@pytest.mark.parametrize("fuse_rstd", [False, True])
+def test_forward_g_on_activation(name, fuse_rstd, pairing):
+    s = SHAPES[name]
+    x = dev_inputs(s)
+    b = BlockBuffers(x, swiglu=True, backward=False, g_on_activation=True, fuse_rstd=fuse_rstd)
+    b.forward()
+    assert_device_ok()
+    X, W1t, R, g, W2t = (f64(x[k]) for k in ("X", "W1t", "R", "g", "W2t"))
+    H = f64(b.H)
+    assert_elem(b.H, O.gemm_residual(X, W1t, R), "H")
+    assert_elem(b.Hg, H * g[None, :], "Hg")
+    assert_elem(b.psum, O.partial_sumsq(H, C.PARTIAL_COLS), "psum", tol=1e-4)
+    assert_elem(b.rstd, O.rstd_from_partials(f64(b.psum), s.d, EPS), "rstd", tol=1e-5)
+    z_ref = O.rowscale_gemm(f64(b.Hg), W2t, f64(b.rstd))
+    assert_elem(b.z, z_ref, "z")
+    assert_elem(b.out, O.swiglu(z_ref), "out")
+    full = O.block_forward(X, W1t, R, g, W2t, EPS, True)
+    assert_frob(b.out, full["out"], "out e2e")
+
+
+def test_fwd_bwd_end_to_end_g_on_activation():
+    s = SHAPES["ragged"]
+    x = dev_inputs(s)
+    b = BlockBuffers(x, g_on_activation=True, fuse_rstd=True)
+    b.step()
+    assert_device_ok()
+    ref = O.block_backward(*(f64(x[k]) for k in ("X", "W1t", "R", "g", "W2t", "dY")), EPS, True)
+    for k_gpu, k_ref in (("out", "out"), ("dH", "dR"), ("dX", "dX"), ("dW1t", "dW1t"), ("dW2t", "dW2t"),
+                         ("dg", "dg")):
+        assert_frob(getattr(b, k_gpu), ref[k_ref], f"{k_gpu} e2e")
