@@ -498,6 +498,21 @@ def main():
     launches = len(calls) * args.steps
     extras = {}
     if not args.no_extras and rank == 0:
+        # the same step with g broadcast in GEMM1's epilogue (no fold pass over
+        # W2) and the combine inside GEMM2's epilogue, timed the same way
+        if not args.g_on_activation or not args.fuse_rstd:
+            bv = BlockBuffers(x, backward=shape.backward, fuse_rstd=True, g_on_activation=True)
+            vcalls = FusedStep(C, bv, fuse_rstd=True, g_on_activation=True).calls()
+            for _ in range(args.warmup):
+                for f in vcalls:
+                    f()
+            v_ms, _ = time_steps(vcalls, args.steps, 0, stage_events=False)
+            v_ms /= args.steps
+            extras["variant_g_on_activation_fused_rstd"] = {
+                "ms_per_step": v_ms, "value": step_flops / (v_ms * 1e-3) / 1e12,
+                "pct_of_peak": 100.0 * step_flops / (v_ms * 1e-3) / 1e12 / peak, "launches_per_step": len(vcalls)}
+            del bv, vcalls
+            torch.cuda.empty_cache()
         # unfused ablation, same workload and timing rules
         bu = BlockBuffers(x, unfused=True, backward=shape.backward)
         ucalls = [bu.forward_unfused, bu.backward_unfused] if shape.backward else [bu.forward_unfused]
