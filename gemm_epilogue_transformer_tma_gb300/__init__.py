@@ -77,6 +77,9 @@ SIGNATURES = {
     "coda_rope_table": (_INT, [_P, _P, _P, _I64, _I64, _F32, _P]),
     "coda_gemm_qkv_rope": (_INT, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64, _P]),
     "coda_rope_apply": (_INT, [_P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _P]),
+    "coda_fp8_quantize": (_INT, [_P, _P, _P, _P, _P, _I64, _I64, _P]),
+    "coda_gemm_res_prms_fp8": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
+    "coda_gemm_rowscale_swiglu_fp8": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _U32, _P]),
     "coda_lmhead_ce_workspace_bytes": (_SZ, [_I64, _I64, _I64, _INT]),
     "coda_lmhead_ce": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I64, _I64, _I64, _P]),
     "coda_unfused_workspace_bytes": (_SZ, [_I64, _I64, _I64]),
@@ -448,6 +451,52 @@ def coda_rope_apply(qkv, cos_t, sin_t, n_q_heads, n_kv_heads, head_dim=128, stre
     _check(load_library().coda_rope_apply(_h(qkv), _ptr(qkv, BF, "qkv"), _ptr(cos_t, F32, "cos_t"),
                                           _ptr(sin_t, F32, "sin_t"), M, n_q_heads, n_kv_heads, head_dim, S,
                                           _stream(stream)), "coda_rope_apply")
+
+
+U8 = torch.uint8
+
+
+def coda_fp8_quantize(src, dst, amax_scale, g=None, stream=None):
+    """Per-tensor e4m3 quantisation of src (times g per column if given);
+    dst: uint8 codes of src's shape; amax_scale: fp32 [2] <- {amax, scale}."""
+    rows, cols = src.shape
+    _shape(dst, (rows, cols), "dst")
+    _shape(amax_scale, (2,), "amax_scale")
+    if g is not None:
+        _shape(g, (cols,), "g")
+    _check(load_library().coda_fp8_quantize(_h(src), _ptr(src, BF, "src"), _ptr(g, BF, "g"),
+                                            _ptr(amax_scale, F32, "amax_scale"), _ptr(dst, U8, "dst"), rows, cols,
+                                            _stream(stream)), "coda_fp8_quantize")
+
+
+def coda_gemm_res_prms_fp8(Xq, sX, W1q, sW1, R, H, psum, stream=None):
+    """GEMM1 + residual + partial RMS on e4m3 operands (scales: 1-element
+    fp32 device tensors, e.g. amax_scale[1:])."""
+    M, K1 = Xq.shape
+    d = W1q.shape[0]
+    _shape(W1q, (d, K1), "W1q")
+    _shape(R, (M, d), "R")
+    _shape(H, (M, d), "H")
+    _shape(psum, (M, coda_prms_num_tiles(d)), "psum")
+    _check(load_library().coda_gemm_res_prms_fp8(_h(Xq), _ptr(Xq, U8, "Xq"), _ptr(sX, F32, "sX"),
+                                                 _ptr(W1q, U8, "W1q"), _ptr(sW1, F32, "sW1"), _ptr(R, BF, "R"),
+                                                 _ptr(H, BF, "H"), _ptr(psum, F32, "psum"), M, K1, d,
+                                                 _stream(stream)), "coda_gemm_res_prms_fp8")
+
+
+def coda_gemm_rowscale_swiglu_fp8(Hq, sH, W2gq, sW2, rstd, out, z_save=None, flags=CODA_EPI_SWIGLU, stream=None):
+    M, d = Hq.shape
+    N2 = W2gq.shape[0]
+    _shape(W2gq, (N2, d), "W2gq")
+    _shape(rstd, (M,), "rstd")
+    _shape(out, (M, N2 // 2 if flags == CODA_EPI_SWIGLU else N2), "out")
+    if z_save is not None:
+        _shape(z_save, (M, N2), "z_save")
+    _check(load_library().coda_gemm_rowscale_swiglu_fp8(_h(Hq), _ptr(Hq, U8, "Hq"), _ptr(sH, F32, "sH"),
+                                                        _ptr(W2gq, U8, "W2gq"), _ptr(sW2, F32, "sW2"),
+                                                        _ptr(rstd, F32, "rstd"), _ptr(out, BF, "out"),
+                                                        _ptr(z_save, BF, "z_save"), M, d, N2, flags,
+                                                        _stream(stream)), "coda_gemm_rowscale_swiglu_fp8")
 
 
 def coda_lmhead_ce_workspace_bytes(M: int, d: int, V: int, with_grads: bool) -> int:

@@ -49,6 +49,8 @@ LaunchCtx ctx_of(coda_handle_t h, void* stream) {
   c.stream = static_cast<cudaStream_t>(stream);
   c.skip_first_stage = h->skip_first_stage;
   c.pair = h->pair;
+  c.scale_a = nullptr;
+  c.scale_b = nullptr;
   return c;
 }
 
@@ -117,6 +119,20 @@ LaunchCtx launch_ctx_of_handle(void* handle, void* stream) {
 }
 
 int device_of_handle(void* handle) { return static_cast<coda_handle_t>(handle)->device; }
+
+bool make_tmap_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t ld, uint32_t box_inner,
+                  uint32_t box_outer) {
+  std::call_once(g_encode_once, resolve_encode);
+  if (g_encode == nullptr) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {ld};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
 
 }  // namespace coda
 
@@ -511,6 +527,72 @@ coda_status_t coda_rope_apply(coda_handle_t h, void* qkv, const float* cos_t, co
   const int64_t N = (n_q_heads + 2 * n_kv_heads) * head_dim;
   return from_cuda(launch_rope_apply(ctx_of(h, stream), static_cast<bf16*>(qkv), cos_t, sin_t, M, N,
                                      (n_q_heads + n_kv_heads) * head_dim, head_dim, S));
+}
+
+// ---------------------------------------------------------------------------
+coda_status_t coda_fp8_quantize(coda_handle_t h, const void* src, const void* g, float* amax_scale, void* dst,
+                                int64_t rows, int64_t cols, void* stream) {
+  CODA_TRY(Check().handle(h).rows(rows).mptr(src, rows).opt_ptr(g).ptr(amax_scale).mptr(dst, rows).cols(cols).st);
+  if (cols % 16 != 0) return CODA_ERR_ALIGNMENT;
+  if (rows == 0) {
+    const float init[2] = {0.f, 1.f};
+    return from_cuda(cudaMemcpyAsync(amax_scale, init, sizeof(init), cudaMemcpyHostToDevice,
+                                     static_cast<cudaStream_t>(stream)));
+  }
+  return from_cuda(launch_fp8_quantize(ctx_of(h, stream), static_cast<const bf16*>(src), rows, cols,
+                                       static_cast<const bf16*>(g), amax_scale, static_cast<uint8_t*>(dst)));
+}
+
+coda_status_t coda_gemm_res_prms_fp8(coda_handle_t h, const void* Xq, const float* sX, const void* W1q,
+                                     const float* sW1, const void* R, void* H, float* psum, int64_t M, int64_t K1,
+                                     int64_t d, void* stream) {
+  CODA_TRY(Check()
+               .handle(h)
+               .rows(M)
+               .mptr(Xq, M)
+               .ptr(sX)
+               .ptr(W1q)
+               .ptr(sW1)
+               .mptr(R, M)
+               .mptr(H, M)
+               .mptr(psum, M)
+               .cols(K1)
+               .cols(d)
+               .st);
+  if (K1 % 16 != 0) return CODA_ERR_ALIGNMENT;
+  if (M == 0) return CODA_OK;
+  if (R == H) return CODA_ERR_INVALID_ARG;
+  return from_cuda(gemm_res_prms_fp8(ctx_of(h, stream), static_cast<const uint8_t*>(Xq), sX,
+                                     static_cast<const uint8_t*>(W1q), sW1, static_cast<const bf16*>(R),
+                                     static_cast<bf16*>(H), psum, int(M), int(K1), int(d),
+                                     int(coda_prms_num_tiles(d))));
+}
+
+coda_status_t coda_gemm_rowscale_swiglu_fp8(coda_handle_t h, const void* Hq, const float* sH, const void* W2gq,
+                                            const float* sW2, const float* rstd, void* out, void* z_save, int64_t M,
+                                            int64_t d, int64_t N2, uint32_t flags, void* stream) {
+  CODA_TRY(Check()
+               .handle(h)
+               .rows(M)
+               .mptr(Hq, M)
+               .ptr(sH)
+               .ptr(W2gq)
+               .ptr(sW2)
+               .mptr(rstd, M)
+               .mptr(out, M)
+               .opt_ptr(z_save)
+               .cols(d)
+               .cols(N2)
+               .st);
+  if (d % 16 != 0) return CODA_ERR_ALIGNMENT;
+  if (flags != CODA_EPI_SWIGLU && flags != CODA_EPI_PLAIN) return CODA_ERR_UNSUPPORTED;
+  const bool swiglu = flags == CODA_EPI_SWIGLU;
+  if (swiglu && (N2 / 2) % 16 != 0) return CODA_ERR_ALIGNMENT;
+  if (!swiglu && z_save != nullptr) return CODA_ERR_INVALID_ARG;
+  if (M == 0) return CODA_OK;
+  return from_cuda(gemm_rowscale_swiglu_fp8(ctx_of(h, stream), static_cast<const uint8_t*>(Hq), sH,
+                                            static_cast<const uint8_t*>(W2gq), sW2, rstd, static_cast<bf16*>(out),
+                                            static_cast<bf16*>(z_save), int(M), int(d), int(N2), swiglu));
 }
 
 // ---------------------------------------------------------------------------

@@ -17,6 +17,8 @@ struct LaunchCtx {
   cudaStream_t stream;
   int skip_first_stage;  // test hook, see coda_debug_skip_first_stage
   int pair;              // 1: 2-SM GEMM kernel (CTA pairs), 0: 1-SM kernel
+  const float* scale_a;  // FP8 operands: device pointers to the per-tensor scales
+  const float* scale_b;
 };
 
 // 2-D bf16 tensor map with 128-byte swizzle.  The tensor is `outer` rows of
@@ -25,6 +27,9 @@ struct LaunchCtx {
 // Returns false if the driver rejects it.
 bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t ld,
                     uint32_t box_inner, uint32_t box_outer);
+// The same for 1-byte elements (e4m3 codes): box_inner <= 128.
+bool make_tmap_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t ld, uint32_t box_inner,
+                  uint32_t box_outer);
 
 // Launch `kern` on c.stream with programmatic stream serialization: its
 // prologue may overlap the tail of the previous kernel in the stream.  Every
@@ -107,6 +112,15 @@ cudaError_t gemm_qkv_rope(const LaunchCtx& c, const __nv_bfloat16* X, const __nv
                           const float* cos_t, const float* sin_t, __nv_bfloat16* qkv, int M, int d, int N,
                           int rot_cols, int S);
 
+// FP8 (e4m3, per-tensor scales sa / sb) forms of the forward GEMMs; operands
+// K-major: A [M][K] codes, B [N][K] codes.
+cudaError_t gemm_res_prms_fp8(const LaunchCtx& c, const uint8_t* Xq, const float* sX, const uint8_t* W1q,
+                              const float* sW1, const __nv_bfloat16* R, __nv_bfloat16* H, float* psum, int M, int K1,
+                              int d, int T);
+cudaError_t gemm_rowscale_swiglu_fp8(const LaunchCtx& c, const uint8_t* Hq, const float* sH, const uint8_t* W2q,
+                                     const float* sW2, const float* rstd, __nv_bfloat16* out, __nv_bfloat16* zsave,
+                                     int M, int d, int N2, bool swiglu);
+
 int ce_tile_cols();    // vocabulary columns per CE statistics tile
 int prms_tile_cols();  // columns per partial-RMS tile of GEMM1
 
@@ -128,6 +142,10 @@ cudaError_t launch_rope_table(const LaunchCtx& c, float* cos_t, float* sin_t, in
 // RoPE in place on the first rot_cols columns of qkv [M, N] (standalone, unfused)
 cudaError_t launch_rope_apply(const LaunchCtx& c, __nv_bfloat16* qkv, const float* cos_t, const float* sin_t,
                               int64_t M, int64_t N, int64_t rot_cols, int64_t head_dim, int64_t S);
+// per-tensor e4m3 quantisation: ws[0] = amax of src (times g[col] if g),
+// ws[1] = scale = amax / 448 (1 if amax == 0); dst = e4m3(src * g / scale)
+cudaError_t launch_fp8_quantize(const LaunchCtx& c, const __nv_bfloat16* src, int64_t rows, int64_t cols,
+                                const __nv_bfloat16* g, float* ws, uint8_t* dst);
 // unfused ablation kernels
 cudaError_t launch_add_rmsnorm(const LaunchCtx& c, const __nv_bfloat16* A, const __nv_bfloat16* R,
                                const __nv_bfloat16* g, __nv_bfloat16* H, float* rstd, __nv_bfloat16* Nrm, int64_t M,

@@ -10,12 +10,12 @@
 
 namespace coda {
 
-template <int BN, int STAGES, bool A_MN, bool B_MN, bool B_DUAL, class Epi>
+template <int BN, int STAGES, bool A_MN, bool B_MN, bool B_DUAL, class Epi, bool FP8 = false>
 cudaError_t launch_gemm_kernel(const LaunchCtx& c, const CUtensorMap& ta, const CUtensorMap& tb,
                                const CUtensorMap& tb2, int M, int N, int K, int tiles_n,
                                const typename Epi::Params& ep) {
   using L = GemmSmem<BN, STAGES>;
-  auto kern = gemm_tc_kernel<BN, STAGES, A_MN, B_MN, B_DUAL, Epi>;
+  auto kern = gemm_tc_kernel<BN, STAGES, A_MN, B_MN, B_DUAL, Epi, FP8>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL);
   if (e != cudaSuccess) return e;
   GemmShape sh;
@@ -24,20 +24,20 @@ cudaError_t launch_gemm_kernel(const LaunchCtx& c, const CUtensorMap& ta, const 
   sh.K = K;
   sh.tiles_m = (M + BM - 1) / BM;
   sh.tiles_n = tiles_n;
-  sh.num_kb = (K + BK - 1) / BK;
+  sh.num_kb = (K + (FP8 ? 128 : BK) - 1) / (FP8 ? 128 : BK);
   sh.group_m = 8;
-  KernelCtl ctl{c.status, c.timeout_ns, c.skip_first_stage};
+  KernelCtl ctl{c.status, c.timeout_ns, c.skip_first_stage, c.scale_a, c.scale_b};
   const int tiles = sh.tiles_m * sh.tiles_n;
   const int grid = std::max(1, std::min(tiles, c.num_sms));
   return launch_chained(c, kern, dim3(grid), dim3(gemm_threads<Epi>()), L::TOTAL, ta, tb, tb2, sh, ctl, ep);
 }
 
-template <int BN, int STAGES, bool A_MN, bool B_MN, bool B_DUAL, class Epi>
+template <int BN, int STAGES, bool A_MN, bool B_MN, bool B_DUAL, class Epi, bool FP8 = false>
 cudaError_t launch_gemm2_kernel(const LaunchCtx& c, const CUtensorMap& ta, const CUtensorMap& tb,
                                 const CUtensorMap& tb2, int M, int N, int K, int tiles_n,
                                 const typename Epi::Params& ep) {
   using L = Gemm2Smem<BN, STAGES>;
-  auto kern = gemm_tc2_kernel<BN, STAGES, A_MN, B_MN, B_DUAL, Epi>;
+  auto kern = gemm_tc2_kernel<BN, STAGES, A_MN, B_MN, B_DUAL, Epi, FP8>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL);
   if (e != cudaSuccess) return e;
   GemmShape sh;
@@ -46,9 +46,9 @@ cudaError_t launch_gemm2_kernel(const LaunchCtx& c, const CUtensorMap& ta, const
   sh.K = K;
   sh.tiles_m = (M + BM2 - 1) / BM2;
   sh.tiles_n = tiles_n;
-  sh.num_kb = (K + BK - 1) / BK;
+  sh.num_kb = (K + (FP8 ? 128 : BK) - 1) / (FP8 ? 128 : BK);
   sh.group_m = 4;
-  KernelCtl ctl{c.status, c.timeout_ns, c.skip_first_stage};
+  KernelCtl ctl{c.status, c.timeout_ns, c.skip_first_stage, c.scale_a, c.scale_b};
   // co-resident SM pairs for this kernel (not every TPC need have both SMs
   // enabled); queried once per instantiation and device
   static int max_pairs[64] = {};
@@ -78,11 +78,11 @@ cudaError_t launch_gemm2_kernel(const LaunchCtx& c, const CUtensorMap& ta, const
 }
 
 // The 2-SM pair kernel (default) or the 1-SM kernel, 256-column tiles.
-template <bool A_MN, bool B_MN, bool B_DUAL, class Epi>
+template <bool A_MN, bool B_MN, bool B_DUAL, class Epi, bool FP8 = false>
 cudaError_t run_gemm(const LaunchCtx& c, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tb2, int M,
                      int N, int K, int tiles_n, const typename Epi::Params& ep) {
-  if (c.pair) return launch_gemm2_kernel<256, 6, A_MN, B_MN, B_DUAL, Epi>(c, ta, tb, tb2, M, N, K, tiles_n, ep);
-  return launch_gemm_kernel<256, 4, A_MN, B_MN, B_DUAL, Epi>(c, ta, tb, tb2, M, N, K, tiles_n, ep);
+  if (c.pair) return launch_gemm2_kernel<256, 6, A_MN, B_MN, B_DUAL, Epi, FP8>(c, ta, tb, tb2, M, N, K, tiles_n, ep);
+  return launch_gemm_kernel<256, 4, A_MN, B_MN, B_DUAL, Epi, FP8>(c, ta, tb, tb2, M, N, K, tiles_n, ep);
 }
 
 // Rows of one K-major B box: a whole 256-row tile (1-SM) or the half a CTA

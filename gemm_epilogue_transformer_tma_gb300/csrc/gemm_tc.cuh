@@ -63,7 +63,19 @@ struct KernelCtl {
   int* status;        // device status word (atomicOr of DEV_ERR_* bits)
   uint64_t timeout_ns;
   int skip_first_stage;  // test hook: CTA 0's producer never fills its first stage
+  const float* scale_a;  // FP8 operands: per-tensor dequantisation scales (null = 1)
+  const float* scale_b;
 };
+
+// The accumulator's scale: the product of the operands' per-tensor scales
+// (1 for bf16 operands).  Read after griddep_wait (a previous kernel may have
+// produced the scales).
+__device__ __forceinline__ float acc_scale_of(const KernelCtl& ctl) {
+  float s = 1.f;
+  if (ctl.scale_a != nullptr) s *= *ctl.scale_a;
+  if (ctl.scale_b != nullptr) s *= *ctl.scale_b;
+  return s;
+}
 
 struct EpiCtx {
   int M, N;
@@ -74,6 +86,7 @@ struct EpiCtx {
   int lane;
   int c0, c1;         // this thread's columns of the tile: [c0, c1)
   int part;           // index of its half-tile partial along the row (tn * 2 + half)
+  float acc_scale;    // multiply the accumulator by this (FP8 operand scales; 1 for bf16)
   uint32_t taddr;     // TMEM address of (first lane of quadrant, column 0 of this accumulator)
 };
 
@@ -105,7 +118,7 @@ __device__ __forceinline__ void raise_error(const KernelCtl& ctl, volatile int* 
   *abort_flag = 1;
 }
 
-template <int BN, int STAGES, bool A_MN, bool B_MN, bool B_DUAL, class Epi>
+template <int BN, int STAGES, bool A_MN, bool B_MN, bool B_DUAL, class Epi, bool FP8 = false>
 __global__ void __launch_bounds__(gemm_threads<Epi>(), 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmB2, const GemmShape sh, const KernelCtl ctl,
@@ -113,7 +126,9 @@ __global__ void __launch_bounds__(gemm_threads<Epi>(), 1)
   using L = GemmSmem<BN, STAGES>;
   static_assert(!(B_DUAL && B_MN), "dual-box B is K-major only");
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
-  constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, A_MN, B_MN);
+  static_assert(!FP8 || (!A_MN && !B_MN), "FP8 operands are K-major");
+  constexpr uint32_t IDESC = FP8 ? idesc_e4m3_f32(BM, BN) : idesc_bf16_f32(BM, BN, A_MN, B_MN);
+  constexpr int BKE = FP8 ? 128 : BK;  // elements per 128-byte k-block row
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -156,6 +171,7 @@ __global__ void __launch_bounds__(gemm_threads<Epi>(), 1)
   // are touched only after it has completed
   griddep_launch_dependents();
   griddep_wait();
+  const float acc_scale = acc_scale_of(ctl);
 
   const int num_tiles = sh.tiles_m * sh.tiles_n;
 
@@ -185,16 +201,16 @@ __global__ void __launch_bounds__(gemm_threads<Epi>(), 1)
             uint8_t* sb = sa + L::A_BYTES;
             mbar_arrive_expect_tx(&full[stage], L::STAGE_BYTES);
             if (!A_MN) {
-              tma_load_2d(sa, &tmA, &full[stage], kb * BK, tm * BM);
+              tma_load_2d(sa, &tmA, &full[stage], kb * BKE, tm * BM);
             } else {
 #pragma unroll
               for (int i = 0; i < BM / 64; ++i) tma_load_2d(sa + i * 8192, &tmA, &full[stage], tm * BM + i * 64, kb * BK);
             }
             if (B_DUAL) {
-              tma_load_2d(sb, &tmB, &full[stage], kb * BK, tn * (BN / 2));
-              tma_load_2d(sb + (BN / 2) * 128, &tmB2, &full[stage], kb * BK, tn * (BN / 2));
+              tma_load_2d(sb, &tmB, &full[stage], kb * BKE, tn * (BN / 2));
+              tma_load_2d(sb + (BN / 2) * 128, &tmB2, &full[stage], kb * BKE, tn * (BN / 2));
             } else if (!B_MN) {
-              tma_load_2d(sb, &tmB, &full[stage], kb * BK, tn * BN);
+              tma_load_2d(sb, &tmB, &full[stage], kb * BKE, tn * BN);
             } else {
 #pragma unroll
               for (int i = 0; i < BN / 64; ++i) tma_load_2d(sb + i * 8192, &tmB, &full[stage], tn * BN + i * 64, kb * BK);
@@ -246,7 +262,10 @@ __global__ void __launch_bounds__(gemm_threads<Epi>(), 1)
           for (int k = 0; k < BK / UMMA_K; ++k) {
             const uint64_t ad = A_MN ? sdesc_sw128(sa + k * 2048, 8192, 1024) : sdesc_sw128(sa + k * 32, 16, 1024);
             const uint64_t bd = B_MN ? sdesc_sw128(sb + k * 2048, 8192, 1024) : sdesc_sw128(sb + k * 32, 16, 1024);
-            umma_bf16(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
+            if (FP8)
+              umma_e4m3(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
+            else
+              umma_bf16(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
           }
           umma_commit(&empty[stage]);
           if (++stage == STAGES) {
@@ -289,6 +308,7 @@ __global__ void __launch_bounds__(gemm_threads<Epi>(), 1)
       c.m = tm * BM + row;
       c.quad = quad;
       c.lane = lane;
+      c.acc_scale = acc_scale;
       c.taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN);
 #pragma unroll 1
       for (int hh = 0; hh < HALVES; ++hh) {
@@ -399,6 +419,7 @@ struct EpiStore {
       else if (p.row_scale != nullptr)
         rs = p.row_scale[c.m];
     }
+    rs *= c.acc_scale;
 #pragma unroll 1
     for (int cc = c.c0; cc < c.c1; cc += 32) {
       float v[32];
@@ -487,7 +508,7 @@ struct EpiResPrms {
         load_bf16x32(p.R + static_cast<int64_t>(c.m) * p.ldr + n0, c.N - n0, r);
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const float hb = bf16_round(v[i] + r[i]);
+          const float hb = bf16_round(fmaf(v[i], c.acc_scale, r[i]));
           v[i] = hb;
           ss = fmaf(hb, hb, ss);
         }
@@ -530,6 +551,7 @@ struct EpiRowscaleSwiglu {
     const bool row_ok = c.m < c.M;
     float r = 0.f;
     if (row_ok) r = p.psum != nullptr ? rstd_from_psum(p.psum, p.T, p.inv_d, p.eps, p.rstd_out, c) : p.rstd[c.m];
+    r *= c.acc_scale;
 #pragma unroll 1
     for (int cc = c.c0 / 2; cc < c.c1 / 2; cc += 32) {
       float g[32], u[32];

@@ -45,7 +45,7 @@ struct Gemm2Smem {
   static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "1 KB aligned halves");
 };
 
-template <int BN, int STAGES, bool A_MN, bool B_MN, bool B_DUAL, class Epi>
+template <int BN, int STAGES, bool A_MN, bool B_MN, bool B_DUAL, class Epi, bool FP8 = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi>(), 1)
     gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmB2, const GemmShape sh, const KernelCtl ctl,
@@ -53,8 +53,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi>(),
   using L = Gemm2Smem<BN, STAGES>;
   static_assert(!(B_DUAL && B_MN), "dual-box B is K-major only");
   static_assert(BN == 256, "the pair kernel is instantiated for 256-column tiles");
+  static_assert(!FP8 || (!A_MN && !B_MN), "FP8 operands are K-major");
   constexpr int HB = BN / 2;  // B rows held by one CTA
-  constexpr uint32_t IDESC = idesc_bf16_f32(BM2, BN, A_MN, B_MN);
+  constexpr uint32_t IDESC = FP8 ? idesc_e4m3_f32(BM2, BN) : idesc_bf16_f32(BM2, BN, A_MN, B_MN);
+  constexpr int BKE = FP8 ? 128 : BK;  // elements per 128-byte k-block row
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -103,6 +105,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi>(),
   // are touched only after it has completed
   griddep_launch_dependents();
   griddep_wait();
+  const float acc_scale = acc_scale_of(ctl);
 
   const int num_tiles = sh.tiles_m * sh.tiles_n;
 
@@ -137,16 +140,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi>(),
               parity = (parity & ~(1u << stage)) | (phase << stage);
             }
             if (!A_MN) {
-              tma_load_2d_pair(sa, &tmA, bar, kb * BK, m0);
+              tma_load_2d_pair(sa, &tmA, bar, kb * BKE, m0);
             } else {
               tma_load_2d_pair(sa, &tmA, bar, m0, kb * BK);
               tma_load_2d_pair(sa + 8192, &tmA, bar, m0 + 64, kb * BK);
             }
             if (B_DUAL) {
               // leader: gate rows of the tile, peer: the matching up rows
-              tma_load_2d_pair(sb, leader ? &tmB : &tmB2, bar, kb * BK, tn * HB);
+              tma_load_2d_pair(sb, leader ? &tmB : &tmB2, bar, kb * BKE, tn * HB);
             } else if (!B_MN) {
-              tma_load_2d_pair(sb, &tmB, bar, kb * BK, tn * BN + static_cast<int>(rank) * HB);
+              tma_load_2d_pair(sb, &tmB, bar, kb * BKE, tn * BN + static_cast<int>(rank) * HB);
             } else {
 #pragma unroll
               for (int i = 0; i < HB / 64; ++i)
@@ -206,7 +209,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi>(),
             for (int k = 0; k < BK / UMMA_K; ++k) {
               const uint64_t ad = A_MN ? sdesc_sw128(sa + k * 2048, 8192, 1024) : sdesc_sw128(sa + k * 32, 16, 1024);
               const uint64_t bd = B_MN ? sdesc_sw128(sb + k * 2048, 8192, 1024) : sdesc_sw128(sb + k * 32, 16, 1024);
-              umma_bf16_pair(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
+              if (FP8)
+                umma_e4m3_pair(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
+              else
+                umma_bf16_pair(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
             }
             issued_any = true;
             umma_commit_pair_multicast(&empty[stage], 0x3);
@@ -254,6 +260,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi>(),
       c.m = c.tm * 128 + row;
       c.quad = quad;
       c.lane = lane;
+      c.acc_scale = acc_scale;
       c.taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN);
 #pragma unroll 1
       for (int hh = 0; hh < HALVES; ++hh) {

@@ -6,6 +6,7 @@
 // All accesses are 16-byte vectors (8 bf16 or 4 fp32) along the contiguous
 // dimension; every extent on the boundary is a multiple of 8 elements.
 #include <cfloat>
+#include <cuda_fp8.h>
 
 #include "coda_internal.h"
 #include "ptx.cuh"
@@ -263,6 +264,66 @@ __global__ void rope_apply_kernel(__nv_bfloat16* __restrict__ qkv, const float* 
   }
 }
 
+// per-tensor amax of src (* g[col] when g is given): block maxima combined
+// with atomicMax on the bit patterns (non-negative floats order as integers)
+__global__ void amax_kernel(const uint4* __restrict__ src, const uint4* __restrict__ g8, int64_t n8, int64_t c8,
+                            unsigned int* __restrict__ amax_bits) {
+  griddep_wait();
+  griddep_launch_dependents();
+  __shared__ float red[32];
+  float mx = 0.f;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n8;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    float v[8], gg[8];
+    unpack_bf16x8(src[i], v);
+    if (g8 != nullptr) {
+      unpack_bf16x8(__ldg(&g8[i % c8]), gg);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) v[k] *= gg[k];
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) mx = fmaxf(mx, fabsf(v[k]));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float t = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, o));
+    if (threadIdx.x == 0) atomicMax(amax_bits, __float_as_uint(t));
+  }
+}
+
+// dst = e4m3(src * g / scale), scale = amax / 448 (1 for an all-zero tensor);
+// saturating round-to-nearest-even conversion.  ws[1] receives the scale.
+__global__ void fp8_quantize_kernel(const uint4* __restrict__ src, const uint4* __restrict__ g8, int64_t n8,
+                                    int64_t c8, float* __restrict__ ws, uint2* __restrict__ dst) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const float amax = ws[0];
+  const float scale = amax > 0.f ? amax / 448.0f : 1.0f;
+  if (blockIdx.x == 0 && threadIdx.x == 0) ws[1] = scale;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n8;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    float v[8], gg[8];
+    unpack_bf16x8(src[i], v);
+    if (g8 != nullptr) {
+      unpack_bf16x8(__ldg(&g8[i % c8]), gg);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) v[k] *= gg[k];
+    }
+    uint32_t w[2] = {0u, 0u};
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint32_t b = __nv_cvt_float_to_fp8(v[k] / scale, __NV_SATFINITE, __NV_E4M3);
+      w[k >> 2] |= (b & 0xFFu) << (8 * (k & 3));
+    }
+    dst[i] = make_uint2(w[0], w[1]);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // unfused ablation kernels
 
@@ -469,6 +530,19 @@ cudaError_t launch_rope_apply(const LaunchCtx& c, __nv_bfloat16* qkv, const floa
   const int64_t rot_heads = rot_cols / head_dim;
   return launch_chained(c, rope_apply_kernel, dim3(grid_for(c, M * rot_heads * (half / 8), 256)), dim3(256), 0, qkv,
                         cos_t, sin_t, M, N, rot_heads, half, S);
+}
+
+cudaError_t launch_fp8_quantize(const LaunchCtx& c, const __nv_bfloat16* src, int64_t rows, int64_t cols,
+                                const __nv_bfloat16* g, float* ws, uint8_t* dst) {
+  const int64_t n8 = rows * cols / 8;
+  cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(float), c.stream);
+  if (e != cudaSuccess) return e;
+  const uint4* g8 = reinterpret_cast<const uint4*>(g);
+  e = launch_chained(c, amax_kernel, dim3(grid_for(c, n8, 256)), dim3(256), 0, reinterpret_cast<const uint4*>(src), g8,
+                     n8, cols / 8, reinterpret_cast<unsigned int*>(ws));
+  if (e != cudaSuccess) return e;
+  return launch_chained(c, fp8_quantize_kernel, dim3(grid_for(c, n8, 256)), dim3(256), 0,
+                        reinterpret_cast<const uint4*>(src), g8, n8, cols / 8, ws, reinterpret_cast<uint2*>(dst));
 }
 
 cudaError_t launch_add_rmsnorm(const LaunchCtx& c, const __nv_bfloat16* A, const __nv_bfloat16* R,

@@ -328,6 +328,39 @@ coda_status_t coda_rope_apply(coda_handle_t h, void* qkv, const float* cos_t, co
                               int64_t n_q_heads, int64_t n_kv_heads, int64_t head_dim, int64_t S, void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* FP8 operands (the write-up's 背景 section: FP8 speeds up the matmul, which  */
+/* raises the relative cost of the memory-bound operations the epilogues     */
+/* absorb): e4m3 codes with one fp32 scale per tensor                        */
+/* ------------------------------------------------------------------------ */
+
+/* Per-tensor e4m3 quantisation:
+ *   amax = max |src[r][c] * g[c]|  (g = 1 when NULL; the product in fp32)
+ *   scale = amax / 448 (1 when amax == 0)
+ *   dst[r][c] = e4m3( src[r][c] * g[c] / scale ), round to nearest even,
+ *               saturating at +-448
+ * src bf16 [rows][cols], g bf16 [cols] or NULL (with g = the RMSNorm weight
+ * and src = W2t this folds g into W2 while quantising), amax_scale fp32 [2]
+ * receives {amax, scale}, dst e4m3 codes [rows][cols] (1 byte each).  cols a
+ * multiple of 16. */
+coda_status_t coda_fp8_quantize(coda_handle_t h, const void* src, const void* g, float* amax_scale, void* dst,
+                                int64_t rows, int64_t cols, void* stream);
+
+/* coda_gemm_res_prms on e4m3 operands: H = bf16( sX * sW1 * sum_k Xq[m][k]
+ * W1q[n][k] + R ), psum as before.  Xq codes [M][K1], W1q codes [d][K1], sX /
+ * sW1 device pointers to the tensors' scales (amax_scale + 1 of
+ * coda_fp8_quantize).  K1 and d multiples of 16. */
+coda_status_t coda_gemm_res_prms_fp8(coda_handle_t h, const void* Xq, const float* sX, const void* W1q,
+                                     const float* sW1, const void* R, void* H, float* psum, int64_t M, int64_t K1,
+                                     int64_t d, void* stream);
+
+/* coda_gemm_rowscale_swiglu on e4m3 operands: z = rstd[m] * sH * sW2 *
+ * sum_k Hq[m][k] W2gq[n][k], then the same SwiGLU / PLAIN epilogue.  Hq codes
+ * [M][d], W2gq codes [N2][d] (e.g. coda_fp8_quantize of W2t with g). */
+coda_status_t coda_gemm_rowscale_swiglu_fp8(coda_handle_t h, const void* Hq, const float* sH, const void* W2gq,
+                                            const float* sW2, const float* rstd, void* out, void* z_save, int64_t M,
+                                            int64_t d, int64_t N2, uint32_t flags, void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* LM head: blocked log-sum-exp cross-entropy epilogue (section 五种积木:     */
 /* block reduction "block log-sum-exp", stateful max / sum-exp)              */
 /* ------------------------------------------------------------------------ */

@@ -23,7 +23,8 @@ __all__ = [
     "stage_wgrad2", "stage_dgrad1", "stage_wgrad1", "logits_rows",
     "lse_rows", "lse_tile_partials", "lse_combine", "ce_forward",
     "ce_backward", "argmax_lowest", "ce_weight_grad_given_lse", "down_proj_dgrad",
-    "swiglu_c_partials", "rope_angles", "rope_rotate_half", "qkv_rope",
+    "swiglu_c_partials", "rope_angles", "rope_rotate_half", "qkv_rope", "e4m3_round", "e4m3_encode",
+    "e4m3_decode", "fp8_scale", "fp8_quantize",
 ]
 
 
@@ -382,3 +383,68 @@ def qkv_rope(X, Wqkv_t, n_q_heads: int, n_kv_heads: int, head_dim: int, seq_len:
     out = qkv.copy()
     out[:, :rot] = rope_rotate_half(qkv[:, :rot], pos, head_dim, base)
     return out
+
+
+# ----------------------------------------------------------------------------
+# FP8 (e4m3) operands with per-tensor scaling (the write-up's 背景 section:
+# FP8 makes the matmul faster, raising the relative cost of the memory-bound
+# operations the epilogues absorb)
+# ----------------------------------------------------------------------------
+# e4m3: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits; normal numbers
+# 2^-6 .. 448, subnormals k * 2^-9; no infinities (saturating conversion).
+
+E4M3_MAX = 448.0
+
+
+def e4m3_round(x):
+    """Round to the nearest e4m3 value, ties to even, saturating at +-448.
+    Input: float64 array (the value to convert, already in the precision
+    the conversion sees)."""
+    x = np.asarray(x, np.float64)
+    a = np.abs(x)
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    e = np.clip(e, -6, 8)                       # below 2^-6: subnormal quantum 2^-9
+    quantum = np.exp2(e - 3)
+    q = np.round(a / quantum) * quantum         # np.round: half to even
+    q = np.minimum(q, E4M3_MAX)
+    return np.where(a > 0, np.sign(x) * q, 0.0 * x)
+
+
+def e4m3_encode(v):
+    """Byte encoding of e4m3 values (exactly representable, |v| <= 448)."""
+    v = np.asarray(v, np.float64)
+    sign = (np.signbit(v)).astype(np.uint8) << 7
+    a = np.abs(v)
+    out = np.zeros(a.shape, np.uint8)
+    sub = (a > 0) & (a < 2.0 ** -6)
+    out[sub] = (a[sub] / 2.0 ** -9).astype(np.uint8)
+    nrm = a >= 2.0 ** -6
+    e = np.floor(np.log2(a[nrm]))
+    man = a[nrm] / np.exp2(e) - 1.0
+    out[nrm] = ((e + 7).astype(np.uint8) << 3) | np.round(man * 8).astype(np.uint8)
+    return out | sign
+
+
+def e4m3_decode(b):
+    """Value of e4m3 byte codes (the NaN codes 0x7f / 0xff are not produced
+    by a saturating conversion)."""
+    b = np.asarray(b, np.uint8).astype(np.int64)
+    sign = np.where(b & 0x80, -1.0, 1.0)
+    e = (b >> 3) & 0xF
+    m = b & 0x7
+    val = np.where(e == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    return sign * val
+
+
+def fp8_scale(x):
+    """Per-tensor scale that maps the tensor's largest magnitude onto the
+    top of the e4m3 range: amax / 448 (1 for an all-zero tensor), in fp32."""
+    amax = np.float32(np.max(np.abs(np.asarray(x, np.float32)))) if np.size(x) else np.float32(0)
+    return np.float32(amax / np.float32(E4M3_MAX)) if amax > 0 else np.float32(1.0)
+
+
+def fp8_quantize(x, scale):
+    """Codes of x / scale rounded to e4m3; the division is done in fp32, the
+    precision the conversion sees."""
+    q = np.asarray(x, np.float32) / np.float32(scale)
+    return e4m3_encode(e4m3_round(q.astype(np.float64)))

@@ -152,3 +152,18 @@ def test_mutant_rope_exponent(monkeypatch):
            lambda positions, head_dim, base=10000.0: np.asarray(positions, float)[:, None]
            * base ** (-np.arange(head_dim // 2) / head_dim)[None, :])
     _fails(P.test_rope_two_dim_closed_form)
+
+
+def test_mutant_e4m3_ties_away_from_zero(monkeypatch):
+    good = OC.e4m3_round
+
+    def bad(x):
+        x = np.asarray(x, np.float64)
+        a = np.abs(x)
+        e = np.clip(np.floor(np.log2(np.where(a > 0, a, 1.0))), -6, 8)
+        quantum = np.exp2(e - 3)
+        q = np.minimum(np.floor(a / quantum + 0.5) * quantum, 448.0)
+        return np.where(a > 0, np.sign(x) * q, 0.0 * x)
+    _patch(monkeypatch, "e4m3_round", bad)
+    _fails(P.test_e4m3_rounding_rules)
+    assert good is not bad

@@ -425,3 +425,55 @@ def test_qkv_rope_rotates_q_and_k_only():
     np.testing.assert_allclose(out[:, :rot], O.rope_rotate_half(plain[:, :rot], pos, D), rtol=1e-13)
     # rows at position 0 (m = 0, 3) are not rotated
     np.testing.assert_allclose(out[[0, 3]], plain[[0, 3]], rtol=1e-14)
+
+
+# --------------------------------------------------------------------------
+# e4m3 (FP8) rounding and encoding, from the format's definition
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("v,code", [(1.0, 0x38), (-1.0, 0xB8), (448.0, 0x7E), (2.0 ** -6, 0x08),
+                                    (2.0 ** -9, 0x01), (0.875 * 2.0 ** -6, 0x07), (1.125, 0x39), (0.0, 0x00),
+                                    (240.0, 0x77), (3.5, 0x46)])
+def test_e4m3_known_encodings(v, code):
+    assert int(O.e4m3_encode(np.array([v]))[0]) == code
+    assert O.e4m3_decode(np.array([code], np.uint8))[0] == v
+
+
+def test_e4m3_every_code_round_trips():
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], np.uint8)   # skip the NaN codes
+    vals = O.e4m3_decode(codes)
+    assert np.array_equal(O.e4m3_round(vals), vals)
+    back = O.e4m3_encode(vals)
+    # +0 and -0 both decode to zero; everything else is exact
+    nz = codes != 0x80
+    assert np.array_equal(back[nz], codes[nz])
+
+
+def test_e4m3_rounding_rules():
+    # ties to even: 1 + 1/16 lies halfway between 1 and 1.125 -> 1 (even mantissa)
+    assert O.e4m3_round(1.0625) == 1.0
+    assert O.e4m3_round(1.1875) == 1.25          # halfway 1.125 / 1.25 -> even mantissa 2
+    # half the smallest subnormal rounds to 0, a hair above rounds up
+    assert O.e4m3_round(2.0 ** -10) == 0.0
+    assert O.e4m3_round(2.0 ** -10 * 1.001) == 2.0 ** -9
+    # saturation
+    assert O.e4m3_round(1000.0) == 448.0 and O.e4m3_round(-465.0) == -448.0
+    # relative error of normal numbers <= 2^-4
+    x = np.random.default_rng(5).uniform(2.0 ** -6, 448, 10000)
+    assert np.max(np.abs(O.e4m3_round(x) - x) / x) <= 2.0 ** -4 + 1e-15
+    # nearest: no representable value is closer
+    grid = np.unique(np.abs(O.e4m3_decode(np.arange(0, 127, dtype=np.uint8))))
+    for v in np.random.default_rng(6).uniform(0, 448, 500):
+        best = grid[np.argmin(np.abs(grid - v))]
+        assert abs(O.e4m3_round(v) - v) <= abs(best - v) + 1e-15
+
+
+def test_fp8_scale_and_quantize():
+    x = np.array([[0.5, -3.0], [1.5, 0.25]], np.float32)
+    s = O.fp8_scale(x)
+    assert s == np.float32(3.0 / 448.0)
+    q = O.fp8_quantize(x, s)
+    # the largest magnitude maps to +-448
+    assert int(q[0, 1]) == 0xFE
+    np.testing.assert_allclose(O.e4m3_decode(q) * s, x, rtol=2.0 ** -4)
+    assert O.fp8_scale(np.zeros((2, 2))) == 1.0
