@@ -55,8 +55,8 @@ def test_quantize_codes_bit_exact(shape, scale):
 
 def test_quantize_with_folded_weight_bit_exact():
     g = torch.Generator().manual_seed(3)
-    W = (torch.randn(528, 328, generator=g) * 0.02).to(torch.bfloat16)
-    gw = (torch.rand(328, generator=g) + 0.5).to(torch.bfloat16)
+    W = (torch.randn(528, 336, generator=g) * 0.02).to(torch.bfloat16)
+    gw = (torch.rand(336, generator=g) + 0.5).to(torch.bfloat16)
     q, s = quantize(W.cuda(), gw.cuda())
     assert_device_ok()
     v = W.float().numpy() * gw.float().numpy()[None, :]      # exact in fp32
