@@ -72,6 +72,15 @@ struct Check {
     return *this;
   }
   Check& opt_ptr(const void* p) { return p == nullptr ? *this : ptr(p); }
+  // a pointer to fp32 scalars: natural (4-byte) alignment
+  Check& sptr(const void* p) {
+    if (st != CODA_OK) return *this;
+    if (p == nullptr)
+      st = CODA_ERR_INVALID_ARG;
+    else if (reinterpret_cast<uintptr_t>(p) % 4 != 0)
+      st = CODA_ERR_ALIGNMENT;
+    return *this;
+  }
   // a tensor with a token-count (M) extent: may be empty (NULL) when M == 0
   Check& mptr(const void* p, int64_t M) { return M == 0 ? opt_ptr(p) : ptr(p); }
   // the token count M: 0 <= M < 2^31
@@ -532,7 +541,7 @@ coda_status_t coda_rope_apply(coda_handle_t h, void* qkv, const float* cos_t, co
 // ---------------------------------------------------------------------------
 coda_status_t coda_fp8_quantize(coda_handle_t h, const void* src, const void* g, float* amax_scale, void* dst,
                                 int64_t rows, int64_t cols, void* stream) {
-  CODA_TRY(Check().handle(h).rows(rows).mptr(src, rows).opt_ptr(g).ptr(amax_scale).mptr(dst, rows).cols(cols).st);
+  CODA_TRY(Check().handle(h).rows(rows).mptr(src, rows).opt_ptr(g).sptr(amax_scale).mptr(dst, rows).cols(cols).st);
   if (cols % 16 != 0) return CODA_ERR_ALIGNMENT;
   if (rows == 0) {
     const float init[2] = {0.f, 1.f};
@@ -550,9 +559,9 @@ coda_status_t coda_gemm_res_prms_fp8(coda_handle_t h, const void* Xq, const floa
                .handle(h)
                .rows(M)
                .mptr(Xq, M)
-               .ptr(sX)
+               .sptr(sX)
                .ptr(W1q)
-               .ptr(sW1)
+               .sptr(sW1)
                .mptr(R, M)
                .mptr(H, M)
                .mptr(psum, M)
@@ -575,9 +584,9 @@ coda_status_t coda_gemm_rowscale_swiglu_fp8(coda_handle_t h, const void* Hq, con
                .handle(h)
                .rows(M)
                .mptr(Hq, M)
-               .ptr(sH)
+               .sptr(sH)
                .ptr(W2gq)
-               .ptr(sW2)
+               .sptr(sW2)
                .mptr(rstd, M)
                .mptr(out, M)
                .opt_ptr(z_save)

@@ -348,7 +348,8 @@ coda_status_t coda_fp8_quantize(coda_handle_t h, const void* src, const void* g,
 /* coda_gemm_res_prms on e4m3 operands: H = bf16( sX * sW1 * sum_k Xq[m][k]
  * W1q[n][k] + R ), psum as before.  Xq codes [M][K1], W1q codes [d][K1], sX /
  * sW1 device pointers to the tensors' scales (amax_scale + 1 of
- * coda_fp8_quantize).  K1 and d multiples of 16. */
+ * coda_fp8_quantize; scalar pointers need only 4-byte alignment).  K1 and d
+ * multiples of 16. */
 coda_status_t coda_gemm_res_prms_fp8(coda_handle_t h, const void* Xq, const float* sX, const void* W1q,
                                      const float* sW1, const void* R, void* H, float* psum, int64_t M, int64_t K1,
                                      int64_t d, void* stream);
