@@ -309,6 +309,44 @@ def bench_down_proj_swiglu_bwd(C, b, shape, steps, warmup):
             "on_chip_tflops": flops / (t_chip / n * 1e-3) / 1e12}
 
 
+def bench_fp8_forward(C, b, shape, steps, warmup, peak_bf16):
+    """The block forward with e4m3 operands (per-tensor scales; activations X
+    and H quantised in the step, weights once beforehand, their cost reported
+    apart) against the same forward in bf16."""
+    u8 = torch.uint8
+    dev = "cuda"
+    Xq = torch.empty(shape.M, shape.K1, dtype=u8, device=dev)
+    Hq = torch.empty(shape.M, shape.d, dtype=u8, device=dev)
+    W1q = torch.empty(shape.d, shape.K1, dtype=u8, device=dev)
+    W2q = torch.empty(shape.N2, shape.d, dtype=u8, device=dev)
+    sc = torch.empty(4, 2, device=dev)
+    weights = [lambda: C.coda_fp8_quantize(b.W1t, W1q, sc[1]),
+               lambda: C.coda_fp8_quantize(b.W2t, W2q, sc[2], b.g)]
+    fp8 = [
+        lambda: C.coda_fp8_quantize(b.X, Xq, sc[0]),
+        lambda: C.coda_gemm_res_prms_fp8(Xq, sc[0, 1:], W1q, sc[1, 1:], b.R, b.H, b.psum),
+        lambda: C.coda_rstd_combine(b.psum, b.d, b.eps, b.rstd),
+        lambda: C.coda_fp8_quantize(b.H, Hq, sc[3]),
+        lambda: C.coda_gemm_rowscale_swiglu_fp8(Hq, sc[3, 1:], W2q, sc[2, 1:], b.rstd, b.out, b.z),
+    ]
+    bf16 = FusedStep(C, b).calls()[:4]
+    n = max(3, steps)
+    t_w, _ = time_steps(weights, n, warmup, stage_events=False)
+    t_8, per8 = time_steps(fp8, n, warmup, stage_events=True)
+    t_8, _ = time_steps(fp8, n, 0, stage_events=False)
+    t_16, _ = time_steps(bf16, n, warmup, stage_events=False)
+    fl = shape.fwd_flops()
+    names = ["quantize_X", "gemm1_res_prms_fp8", "rstd_combine", "quantize_H", "gemm2_rowscale_swiglu_fp8"]
+    g2 = statistics.mean(per8[4])
+    return {"workload": shape.name + " forward", "fp8_fwd_ms": t_8 / n, "bf16_fwd_ms": t_16 / n,
+            "speedup": t_16 / t_8, "fp8_fwd_tflops": fl / (t_8 / n * 1e-3) / 1e12,
+            "weight_quantize_ms": t_w / n, "stage_ms": {k: statistics.mean(v) for k, v in zip(names, per8)},
+            "gemm2_fp8_tflops": 2.0 * shape.M * shape.N2 * shape.d / (g2 * 1e-3) / 1e12,
+            "fp8_peak_tflops": 2 * peak_bf16,
+            "gemm2_frac_of_fp8_peak": 2.0 * shape.M * shape.N2 * shape.d / (g2 * 1e-3) / 1e12 / (2 * peak_bf16),
+            "peak_note": "fp8 dense peak taken as 2x the measured bf16 peak (nominal ratio 4.5 / 2.25 PFLOP/s)"}
+
+
 def bench_qkv_rope(C, steps, warmup, M=8192, S=2048, d=4096, n_heads=32):
     """QKV projection of the 7B-size block (MHA, 32 heads of 128) with RoPE
     in the epilogue, against the plain GEMM followed by a standalone RoPE
@@ -547,6 +585,8 @@ def main():
                          "timing": "host wall clock over the whole run, synchronize at both ends; copies of "
                                    "step i+1 (H2D) and i (D2H) overlap step i's compute"}
         del host, pipe
+        extras["next_fp8_forward"] = bench_fp8_forward(C, b, shape, args.steps, args.warmup, peak)
+        torch.cuda.empty_cache()
         del b, x, fs, calls
         torch.cuda.empty_cache()
         extras["lmhead_ce"] = bench_lmhead(C, args.steps, args.warmup)
