@@ -47,7 +47,7 @@ cudaError_t launch_gemm2_kernel(const LaunchCtx& c, const CUtensorMap& ta, const
   sh.tiles_m = (M + BM2 - 1) / BM2;
   sh.tiles_n = tiles_n;
   sh.num_kb = (K + (FP8 ? 128 : BK) - 1) / (FP8 ? 128 : BK);
-  sh.group_m = 4;
+  sh.group_m = 8;
   KernelCtl ctl{c.status, c.timeout_ns, c.skip_first_stage, c.scale_a, c.scale_b};
   // co-resident SM pairs for this kernel (not every TPC need have both SMs
   // enabled); queried once per instantiation and device
