@@ -48,19 +48,39 @@ int grid_for(const LaunchCtx& c, int64_t work_items, int threads) {
 }
 
 // ---------------------------------------------------------------------------
-// W2gt[n, k] = bf16(W2t[n, k] * g[k])
-__global__ void fold_kernel(const uint4* __restrict__ W2t, const uint4* __restrict__ g8, uint4* __restrict__ out,
-                            int64_t n8, int64_t d8) {
+// W2gt[n, k] = bf16(W2t[n, k] * g[k]).  A thread owns one 8-column chunk
+// (its g values stay in registers) and kFoldRows rows of it: all of its row
+// loads are issued before the first product, so each SM keeps enough bytes
+// in flight to cover HBM latency.
+constexpr int kFoldRows = 8;
+
+__global__ void __launch_bounds__(256) fold_kernel(const uint4* __restrict__ W2t, const uint4* __restrict__ g8,
+                                                   uint4* __restrict__ out, int64_t rows, int64_t d8) {
   griddep_wait();
   griddep_launch_dependents();
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n8;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    float w[8], g[8], o[8];
-    unpack_bf16x8(W2t[i], w);
-    unpack_bf16x8(__ldg(&g8[i % d8]), g);
+  const int64_t j = blockIdx.x * 256LL + threadIdx.x;
+  if (j >= d8) return;
+  float g[8];
+  unpack_bf16x8(__ldg(&g8[j]), g);
+  for (int64_t r0 = blockIdx.y * static_cast<int64_t>(kFoldRows); r0 < rows;
+       r0 += static_cast<int64_t>(gridDim.y) * kFoldRows) {
+    const uint4* src = W2t + r0 * d8 + j;
+    uint4* dst = out + r0 * d8 + j;
+    const int nr = static_cast<int>(rows - r0 < kFoldRows ? rows - r0 : kFoldRows);
+    uint4 v[kFoldRows];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) o[j] = w[j] * g[j];
-    out[i] = pack8(o);
+    for (int r = 0; r < kFoldRows; ++r)
+      if (r < nr) v[r] = src[r * d8];
+#pragma unroll
+    for (int r = 0; r < kFoldRows; ++r) {
+      if (r < nr) {
+        float w[8], o[8];
+        unpack_bf16x8(v[r], w);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o[i] = w[i] * g[i];
+        dst[r * d8] = pack8(o);
+      }
+    }
   }
 }
 
@@ -81,6 +101,29 @@ __global__ void rstd_combine_kernel(const float* __restrict__ psum, int64_t M, i
 // SwiGLU backward with the deferred row scale: one CTA (256 threads) per row.
 //   s = sigmoid(zg); dZg = dY*zu*s*(1 + zg*(1-s)); dZu = dY*zg*s
 //   dP = bf16(r * dZ); c[m] = r^2/d * sum(dZg*zg + dZu*zu)
+// Each thread loads two 8-column chunks (six 16-byte loads) before computing
+// either, to keep enough bytes in flight.
+__device__ __forceinline__ float swiglu_bwd_chunk(const uint4& dyq, const uint4& zgq, const uint4& zuq, float r,
+                                                  uint4& pg, uint4& pu) {
+  float dy[8], zg[8], zu[8], og[8], ou[8];
+  unpack_bf16x8(dyq, dy);
+  unpack_bf16x8(zgq, zg);
+  unpack_bf16x8(zuq, zu);
+  float dot = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float s = 1.0f / (1.0f + __expf(-zg[i]));
+    const float dzu = dy[i] * zg[i] * s;
+    const float dzg = dy[i] * zu[i] * s * (1.0f + zg[i] * (1.0f - s));
+    dot = fmaf(dzg, zg[i], fmaf(dzu, zu[i], dot));
+    og[i] = r * dzg;
+    ou[i] = r * dzu;
+  }
+  pg = pack8(og);
+  pu = pack8(ou);
+  return dot;
+}
+
 __global__ void __launch_bounds__(256) swiglu_bwd_kernel(const __nv_bfloat16* __restrict__ dY,
                                                          const __nv_bfloat16* __restrict__ z,
                                                          const float* __restrict__ rstd,
@@ -96,23 +139,27 @@ __global__ void __launch_bounds__(256) swiglu_bwd_kernel(const __nv_bfloat16* __
   const uint4* zu8 = reinterpret_cast<const uint4*>(z + m * 2 * F + F);
   uint4* pg8 = reinterpret_cast<uint4*>(dP + m * 2 * F);
   uint4* pu8 = reinterpret_cast<uint4*>(dP + m * 2 * F + F);
+  const int64_t F8 = F / 8;
   float dot = 0.f;
-  for (int64_t j = threadIdx.x; j < F / 8; j += blockDim.x) {
-    float dy[8], zg[8], zu[8], og[8], ou[8];
-    unpack_bf16x8(dy8[j], dy);
-    unpack_bf16x8(zg8[j], zg);
-    unpack_bf16x8(zu8[j], zu);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float s = 1.0f / (1.0f + __expf(-zg[i]));
-      const float dzu = dy[i] * zg[i] * s;
-      const float dzg = dy[i] * zu[i] * s * (1.0f + zg[i] * (1.0f - s));
-      dot = fmaf(dzg, zg[i], fmaf(dzu, zu[i], dot));
-      og[i] = r * dzg;
-      ou[i] = r * dzu;
+  for (int64_t j0 = threadIdx.x; j0 < F8; j0 += 2 * 256) {
+    const int64_t j1 = j0 + 256;
+    const bool two = j1 < F8;
+    const uint4 a0 = dy8[j0], b0 = zg8[j0], c0 = zu8[j0];
+    uint4 a1 = a0, b1 = b0, c1 = c0;
+    if (two) {
+      a1 = dy8[j1];
+      b1 = zg8[j1];
+      c1 = zu8[j1];
     }
-    pg8[j] = pack8(og);
-    pu8[j] = pack8(ou);
+    uint4 pg, pu;
+    dot += swiglu_bwd_chunk(a0, b0, c0, r, pg, pu);
+    pg8[j0] = pg;
+    pu8[j0] = pu;
+    if (two) {
+      dot += swiglu_bwd_chunk(a1, b1, c1, r, pg, pu);
+      pg8[j1] = pg;
+      pu8[j1] = pu;
+    }
   }
   const float tot = block_sum_256(dot, red);
   if (threadIdx.x == 0) cvec[m] = r * r * inv_d * tot;
@@ -477,10 +524,11 @@ __global__ void rmsnorm_bwd_dg_kernel(const __nv_bfloat16* __restrict__ dN, cons
 // launchers
 cudaError_t launch_fold(const LaunchCtx& c, const __nv_bfloat16* W2t, const __nv_bfloat16* g, __nv_bfloat16* W2gt,
                         int64_t N2, int64_t d) {
-  const int64_t n8 = N2 * d / 8;
-  return launch_chained(c, fold_kernel, dim3(grid_for(c, n8, 256)), dim3(256), 0, reinterpret_cast<const uint4*>(W2t),
-                                                          reinterpret_cast<const uint4*>(g),
-                                                          reinterpret_cast<uint4*>(W2gt), n8, d / 8);
+  const int64_t d8 = d / 8;
+  const int64_t row_blocks = (N2 + kFoldRows - 1) / kFoldRows;
+  const dim3 grid(static_cast<unsigned>((d8 + 255) / 256), static_cast<unsigned>(row_blocks < 65535 ? row_blocks : 65535));
+  return launch_chained(c, fold_kernel, grid, dim3(256), 0, reinterpret_cast<const uint4*>(W2t),
+                        reinterpret_cast<const uint4*>(g), reinterpret_cast<uint4*>(W2gt), N2, d8);
 }
 
 cudaError_t launch_rstd_combine(const LaunchCtx& c, const float* psum, int64_t M, int64_t T, int64_t d, float eps,
