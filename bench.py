@@ -370,6 +370,34 @@ def bench_qkv_rope(C, steps, warmup, M=8192, S=2048, d=4096, n_heads=32):
             "unfused_ms": t_u / n, "speedup": t_u / t_f, "fused_tflops": flops / (t_f / n * 1e-3) / 1e12}
 
 
+def bench_plain_vs_cublas(C, shape, steps, warmup):
+    """The library's plain GEMM (K-major operands, bf16 store, no epilogue
+    work) against cuBLAS (torch.matmul) on the GEMM shapes of the step, same
+    operands, interleaved.  Context for the roofline: the denominator is a
+    cuBLAS figure taken on its own best shape."""
+    out = {}
+    n = max(3, steps // 2)
+    for name, (M, N, K) in {"gemm2": (shape.M, shape.N2, shape.d), "dgrad2": (shape.M, shape.d, shape.N2),
+                            "gemm1": (shape.M, shape.d, shape.K1)}.items():
+        g = torch.Generator(device="cuda").manual_seed(0)
+        A = torch.randn(M, K, device="cuda", generator=g).to(torch.bfloat16)
+        B = (torch.randn(N, K, device="cuda", generator=g) / K ** 0.5).to(torch.bfloat16)
+        Cd = torch.empty(M, N, device="cuda", dtype=torch.bfloat16)
+        ours = [lambda: C.coda_gemm(A, False, B, False, Cd, M, N, K)]
+        lib = [lambda: torch.matmul(A, B.t(), out=Cd)]
+        t_o, t_l = [], []
+        for _ in range(2):
+            t_o.append(time_steps(ours, n, warmup, stage_events=False)[0] / n)
+            t_l.append(time_steps(lib, n, warmup, stage_events=False)[0] / n)
+        fl = 2.0 * M * N * K
+        out[name] = {"M": M, "N": N, "K": K, "coda_ms": min(t_o), "cublas_ms": min(t_l),
+                     "coda_tflops": fl / min(t_o) / 1e9, "cublas_tflops": fl / min(t_l) / 1e9,
+                     "ratio": min(t_l) / min(t_o)}
+        del A, B, Cd
+        torch.cuda.empty_cache()
+    return out
+
+
 def bench_lmhead(C, steps, warmup):
     s = LMHEAD
     x = ce_inputs(s, 0, "cuda")
@@ -589,6 +617,7 @@ def main():
         torch.cuda.empty_cache()
         del b, x, fs, calls
         torch.cuda.empty_cache()
+        extras["plain_gemm_vs_cublas"] = bench_plain_vs_cublas(C, shape, args.steps, args.warmup)
         extras["lmhead_ce"] = bench_lmhead(C, args.steps, args.warmup)
         torch.cuda.empty_cache()
         extras["next_qkv_rope"] = bench_qkv_rope(C, args.steps, args.warmup)
