@@ -123,6 +123,30 @@ bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t o
   return r == CUDA_SUCCESS;
 }
 
+namespace {
+bool make_tmap_store(CUtensorMap* m, CUtensorMapDataType type, uint32_t esize, CUtensorMapSwizzle swz,
+                     const void* base, uint64_t cols, uint64_t rows, uint64_t ld) {
+  std::call_once(g_encode_once, resolve_encode);
+  if (g_encode == nullptr) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {ld * esize};
+  const cuuint32_t box[2] = {32, 32};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = g_encode(m, type, 2, const_cast<void*>(base), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+}  // namespace
+
+bool make_tmap_store_bf16(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t ld) {
+  return make_tmap_store(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, CU_TENSOR_MAP_SWIZZLE_64B, base, cols, rows, ld);
+}
+
+bool make_tmap_store_f32(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t ld) {
+  return make_tmap_store(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, CU_TENSOR_MAP_SWIZZLE_128B, base, cols, rows, ld);
+}
+
 LaunchCtx launch_ctx_of_handle(void* handle, void* stream) {
   return ctx_of(static_cast<coda_handle_t>(handle), stream);
 }

@@ -27,6 +27,11 @@ struct LaunchCtx {
 // Returns false if the driver rejects it.
 bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t ld,
                     uint32_t box_inner, uint32_t box_outer);
+// Tensor maps for the epilogue's TMA stores: `rows` x `cols` elements with a
+// row pitch of `ld` elements, 32 x 32 boxes (bf16: 64-byte swizzle; fp32:
+// 128-byte swizzle), matching the staging layout of the GEMM epilogue.
+bool make_tmap_store_bf16(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t ld);
+bool make_tmap_store_f32(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t ld);
 // The same for 1-byte elements (e4m3 codes): box_inner <= 128.
 bool make_tmap_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t ld, uint32_t box_inner,
                   uint32_t box_outer);

@@ -15,7 +15,17 @@ cudaError_t gemm_dgrad_rms(const LaunchCtx& c, const __nv_bfloat16* dP, const __
   // stored [K][N] (MN-major).
   CUtensorMap ta, tb;
   if (!make_operand_maps(&ta, &tb, dP, false, W2t, true, M, d, N2, b_box_rows(c))) return cudaErrorInvalidValue;
-  EpiDgradRms::Params ep{H, d, g, cvec, dH, d, dgpart, cpart, Tc, rstd, 1.0f / static_cast<float>(d)};
+  EpiDgradRms::Params ep{};
+  if (!make_tmap_store_bf16(&ep.dH, dH, d, M, d)) return cudaErrorInvalidValue;
+  ep.H = H;
+  ep.ldh = d;
+  ep.g = g;
+  ep.c = cvec;
+  ep.dgpart = dgpart;
+  ep.cpart = cpart;
+  ep.Tc = Tc;
+  ep.rstd = rstd;
+  ep.inv_d = 1.0f / static_cast<float>(d);
   return run_gemm<false, true, false, EpiDgradRms>(c, ta, tb, tb, M, d, N2, (d + kBN - 1) / kBN, ep);
 }
 
@@ -30,7 +40,14 @@ cudaError_t gemm_dgrad_swiglu_bwd(const LaunchCtx& c, const __nv_bfloat16* dYb, 
   // stored [K][N] (MN-major), N = F gate columns
   CUtensorMap ta, tb;
   if (!make_operand_maps(&ta, &tb, dYb, false, W3t, true, M, F, d, b_box_rows(c))) return cudaErrorInvalidValue;
-  EpiSwigluBwd::Params ep{z, rstd, dP, cpart, T, F};
+  EpiSwigluBwd::Params ep{};
+  if (!make_tmap_store_bf16(&ep.dPg, dP, F, M, 2 * static_cast<uint64_t>(F))) return cudaErrorInvalidValue;
+  if (!make_tmap_store_bf16(&ep.dPu, dP + F, F, M, 2 * static_cast<uint64_t>(F))) return cudaErrorInvalidValue;
+  ep.z = z;
+  ep.rstd = rstd;
+  ep.cpart = cpart;
+  ep.T = T;
+  ep.F = F;
   return run_gemm<false, true, false, EpiSwigluBwd>(c, ta, tb, tb, M, F, d, (F + 255) / 256, ep);
 }
 

@@ -23,7 +23,12 @@ cudaError_t gemm_ce_grad(const LaunchCtx& c, const __nv_bfloat16* H, const __nv_
                          float inv_M) {
   CUtensorMap ta, tb;
   if (!make_operand_maps(&ta, &tb, H, false, Wt_chunk, false, M, Vc, d, b_box_rows(c))) return cudaErrorInvalidValue;
-  EpiCeGrad::Params ep{labels, lse, dL, Vc, inv_M, v0};
+  EpiCeGrad::Params ep{};
+  if (!make_tmap_store_bf16(&ep.dL, dL, Vc, M, Vc)) return cudaErrorInvalidValue;
+  ep.labels = labels;
+  ep.lse = lse;
+  ep.inv_M = inv_M;
+  ep.v0 = v0;
   return run_gemm<false, false, false, EpiCeGrad>(c, ta, tb, tb, M, Vc, d, (Vc + kBN - 1) / kBN, ep);
 }
 

@@ -23,7 +23,12 @@ cudaError_t gemm_res_prms_fp8(const LaunchCtx& c0, const uint8_t* Xq, const floa
   c.scale_b = sW1;
   CUtensorMap ta, tb;
   if (!make_fp8_maps(&ta, &tb, Xq, W1q, M, d, K1, b_box_rows(c))) return cudaErrorInvalidValue;
-  EpiResPrms::Params ep{R, d, H, d, psum, T, nullptr, nullptr};
+  EpiResPrms::Params ep{};
+  if (!make_tmap_store_bf16(&ep.H, H, d, M, d)) return cudaErrorInvalidValue;
+  ep.R = R;
+  ep.ldr = d;
+  ep.psum = psum;
+  ep.T = T;
   return run_gemm<false, false, false, EpiResPrms, true>(c, ta, tb, tb, M, d, K1, (d + kBN - 1) / kBN, ep);
 }
 
@@ -36,14 +41,24 @@ cudaError_t gemm_rowscale_swiglu_fp8(const LaunchCtx& c0, const uint8_t* Hq, con
   CUtensorMap ta, tb, tb2;
   if (!swiglu) {
     if (!make_fp8_maps(&ta, &tb, Hq, W2q, M, N2, d, b_box_rows(c))) return cudaErrorInvalidValue;
-    EpiStore::Params ep{out, N2, rstd, nullptr, nullptr, 0, 0.f, 0.f, nullptr};
+    EpiStore::Params ep{};
+    if (!make_tmap_store_bf16(&ep.out, out, N2, M, N2)) return cudaErrorInvalidValue;
+    ep.row_scale = rstd;
     return run_gemm<false, false, false, EpiStore, true>(c, ta, tb, tb, M, N2, d, (N2 + kBN - 1) / kBN, ep);
   }
   const int F = N2 / 2;
   if (!make_tmap_u8(&ta, Hq, d, M, d, 128, BM)) return cudaErrorInvalidValue;
   if (!make_tmap_u8(&tb, W2q, d, F, d, 128, kBN / 2)) return cudaErrorInvalidValue;
   if (!make_tmap_u8(&tb2, W2q + static_cast<int64_t>(F) * d, d, F, d, 128, kBN / 2)) return cudaErrorInvalidValue;
-  EpiRowscaleSwiglu::Params ep{rstd, out, F, zsave, N2, F, nullptr, 0, 0.f, 0.f, nullptr};
+  EpiRowscaleSwiglu::Params ep{};
+  if (!make_tmap_store_bf16(&ep.out, out, F, M, F)) return cudaErrorInvalidValue;
+  if (zsave != nullptr) {
+    if (!make_tmap_store_bf16(&ep.zg, zsave, F, M, N2)) return cudaErrorInvalidValue;
+    if (!make_tmap_store_bf16(&ep.zu, zsave + F, F, M, N2)) return cudaErrorInvalidValue;
+  }
+  ep.save_z = zsave != nullptr;
+  ep.rstd = rstd;
+  ep.F = F;
   return run_gemm<false, false, true, EpiRowscaleSwiglu, true>(c, ta, tb, tb2, M, F, d,
                                                                (F + kBN / 2 - 1) / (kBN / 2), ep);
 }

@@ -15,7 +15,14 @@ cudaError_t gemm_res_prms(const LaunchCtx& c, const __nv_bfloat16* X, const __nv
                           const __nv_bfloat16* g, __nv_bfloat16* Hg) {
   CUtensorMap ta, tb;
   if (!make_operand_maps(&ta, &tb, X, false, W1t, false, M, d, K1, b_box_rows(c))) return cudaErrorInvalidValue;
-  EpiResPrms::Params ep{R, d, H, d, psum, T, g, Hg};
+  EpiResPrms::Params ep{};
+  if (!make_tmap_store_bf16(&ep.H, H, d, M, d)) return cudaErrorInvalidValue;
+  if (Hg != nullptr && !make_tmap_store_bf16(&ep.Hg, Hg, d, M, d)) return cudaErrorInvalidValue;
+  ep.R = R;
+  ep.ldr = d;
+  ep.psum = psum;
+  ep.T = T;
+  ep.g = Hg != nullptr ? g : nullptr;
   return run_gemm<false, false, false, EpiResPrms>(c, ta, tb, tb, M, d, K1, (d + kBN - 1) / kBN, ep);
 }
 
@@ -26,7 +33,14 @@ cudaError_t gemm_rowscale_swiglu(const LaunchCtx& c, const __nv_bfloat16* H, con
   CUtensorMap ta, tb, tb2;
   if (!swiglu) {
     if (!make_operand_maps(&ta, &tb, H, false, W2gt, false, M, N2, d, b_box_rows(c))) return cudaErrorInvalidValue;
-    EpiStore::Params ep{out, N2, rstd, nullptr, psum, T, inv_d, eps, rstd_out};
+    EpiStore::Params ep{};
+    if (!make_tmap_store_bf16(&ep.out, out, N2, M, N2)) return cudaErrorInvalidValue;
+    ep.row_scale = rstd;
+    ep.psum = psum;
+    ep.T = T;
+    ep.inv_d = inv_d;
+    ep.eps = eps;
+    ep.rstd_out = rstd_out;
     return run_gemm<false, false, false, EpiStore>(c, ta, tb, tb, M, N2, d, (N2 + kBN - 1) / kBN, ep);
   }
   const int F = N2 / 2;
@@ -35,7 +49,20 @@ cudaError_t gemm_rowscale_swiglu(const LaunchCtx& c, const __nv_bfloat16* H, con
   // each half is zero-filled past its own end
   if (!make_tmap_bf16(&tb, W2gt, d, F, d, 64, kBN / 2)) return cudaErrorInvalidValue;
   if (!make_tmap_bf16(&tb2, W2gt + static_cast<int64_t>(F) * d, d, F, d, 64, kBN / 2)) return cudaErrorInvalidValue;
-  EpiRowscaleSwiglu::Params ep{rstd, out, F, zsave, N2, F, psum, T, inv_d, eps, rstd_out};
+  EpiRowscaleSwiglu::Params ep{};
+  if (!make_tmap_store_bf16(&ep.out, out, F, M, F)) return cudaErrorInvalidValue;
+  if (zsave != nullptr) {
+    if (!make_tmap_store_bf16(&ep.zg, zsave, F, M, N2)) return cudaErrorInvalidValue;
+    if (!make_tmap_store_bf16(&ep.zu, zsave + F, F, M, N2)) return cudaErrorInvalidValue;
+  }
+  ep.save_z = zsave != nullptr;
+  ep.rstd = rstd;
+  ep.F = F;
+  ep.psum = psum;
+  ep.T = T;
+  ep.inv_d = inv_d;
+  ep.eps = eps;
+  ep.rstd_out = rstd_out;
   return run_gemm<false, false, true, EpiRowscaleSwiglu>(c, ta, tb, tb2, M, F, d, (F + kBN / 2 - 1) / (kBN / 2), ep);
 }
 
@@ -44,7 +71,10 @@ cudaError_t gemm_store(const LaunchCtx& c, const __nv_bfloat16* A, bool a_mn, co
                        const __nv_bfloat16* col_scale) {
   CUtensorMap ta, tb;
   if (!make_operand_maps(&ta, &tb, A, a_mn, B, b_mn, M, N, K, b_box_rows(c))) return cudaErrorInvalidValue;
-  EpiStore::Params ep{C, N, row_scale, col_scale, nullptr, 0, 0.f, 0.f, nullptr};
+  EpiStore::Params ep{};
+  if (!make_tmap_store_bf16(&ep.out, C, N, M, N)) return cudaErrorInvalidValue;
+  ep.row_scale = row_scale;
+  ep.col_scale = col_scale;
   const int tn = (N + kBN - 1) / kBN;
   if (!a_mn && !b_mn) return run_gemm<false, false, false, EpiStore>(c, ta, tb, tb, M, N, K, tn, ep);
   if (!a_mn && b_mn) return run_gemm<false, true, false, EpiStore>(c, ta, tb, tb, M, N, K, tn, ep);
@@ -57,7 +87,9 @@ cudaError_t gemm_store_f32(const LaunchCtx& c, const __nv_bfloat16* A, bool a_mn
   if (a_mn || !b_mn) return cudaErrorNotSupported;  // only [M][K] x [K][N] is used
   CUtensorMap ta, tb;
   if (!make_operand_maps(&ta, &tb, A, a_mn, B, b_mn, M, N, K, b_box_rows(c))) return cudaErrorInvalidValue;
-  EpiStoreF32::Params ep{C, N, accumulate ? 1 : 0};
+  EpiStoreF32::Params ep{};
+  if (!make_tmap_store_f32(&ep.out, C, N, M, N)) return cudaErrorInvalidValue;
+  ep.beta = accumulate ? 1 : 0;
   return run_gemm<false, true, false, EpiStoreF32>(c, ta, tb, tb, M, N, K, (N + kBN - 1) / kBN, ep);
 }
 

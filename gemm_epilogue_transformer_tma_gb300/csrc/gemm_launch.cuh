@@ -14,7 +14,7 @@ template <int BN, int STAGES, bool A_MN, bool B_MN, bool B_DUAL, class Epi, bool
 cudaError_t launch_gemm_kernel(const LaunchCtx& c, const CUtensorMap& ta, const CUtensorMap& tb,
                                const CUtensorMap& tb2, int M, int N, int K, int tiles_n,
                                const typename Epi::Params& ep) {
-  using L = GemmSmem<BN, STAGES>;
+  using L = GemmSmem<BN, STAGES, epi_stage_bytes<Epi>()>;
   auto kern = gemm_tc_kernel<BN, STAGES, A_MN, B_MN, B_DUAL, Epi, FP8>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL);
   if (e != cudaSuccess) return e;
@@ -36,7 +36,7 @@ template <int BN, int STAGES, bool A_MN, bool B_MN, bool B_DUAL, class Epi, bool
 cudaError_t launch_gemm2_kernel(const LaunchCtx& c, const CUtensorMap& ta, const CUtensorMap& tb,
                                 const CUtensorMap& tb2, int M, int N, int K, int tiles_n,
                                 const typename Epi::Params& ep) {
-  using L = Gemm2Smem<BN, STAGES>;
+  using L = Gemm2Smem<BN, STAGES, epi_stage_bytes<Epi>()>;
   auto kern = gemm_tc2_kernel<BN, STAGES, A_MN, B_MN, B_DUAL, Epi, FP8>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL);
   if (e != cudaSuccess) return e;

@@ -9,7 +9,12 @@ cudaError_t gemm_qkv_rope(const LaunchCtx& c, const __nv_bfloat16* X, const __nv
   // qkv[m, n] = sum_k X[m, k] Wqkv_t[n, k]: both operands K-major
   CUtensorMap ta, tb;
   if (!make_operand_maps(&ta, &tb, X, false, Wqkv_t, false, M, N, d, b_box_rows(c))) return cudaErrorInvalidValue;
-  EpiRope::Params ep{qkv, N, cos_t, sin_t, S, rot_cols};
+  EpiRope::Params ep{};
+  if (!make_tmap_store_bf16(&ep.out, qkv, N, M, N)) return cudaErrorInvalidValue;
+  ep.cos_t = cos_t;
+  ep.sin_t = sin_t;
+  ep.S = S;
+  ep.rot_cols = rot_cols;
   return run_gemm<false, false, false, EpiRope>(c, ta, tb, tb, M, N, d, (N + 255) / 256, ep);
 }
 

@@ -88,16 +88,27 @@ struct EpiCtx {
   int part;           // index of its half-tile partial along the row (tn * 2 + half)
   float acc_scale;    // multiply the accumulator by this (FP8 operand scales; 1 for bf16)
   uint32_t taddr;     // TMEM address of (first lane of quadrant, column 0 of this accumulator)
+  int m0;             // global row of this warp's lane 0 (the warp stores rows m0 .. m0 + 31)
+  uint32_t stage;     // shared address of this warp's store-staging slots
 };
 
-template <int BN, int STAGES>
+// Store staging: every epilogue warp owns Epi::kStoreSlots slots of
+// STORE_SLOT_BYTES in shared memory, after the operand ring.
+constexpr int STORE_SLOT_BYTES = 2048;
+template <class Epi>
+constexpr int epi_stage_bytes() { return Epi::kEpiWarps * Epi::kStoreSlots * STORE_SLOT_BYTES; }
+constexpr int MAX_DYN_SMEM = 232448;  // 227 KB per CTA
+
+template <int BN, int STAGES, int EPI_BYTES>
 struct GemmSmem {
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
+  static constexpr int STORE_BYTES = EPI_BYTES;                 // epilogue store staging
   static constexpr int BAR_BYTES = 256;
-  static constexpr int TOTAL = RING_BYTES + BAR_BYTES + 1024;  // + alignment slack
+  static constexpr int TOTAL = RING_BYTES + STORE_BYTES + BAR_BYTES + 1024;  // + alignment slack
+  static_assert(TOTAL <= MAX_DYN_SMEM, "shared memory budget");
   static constexpr int TMEM_COLS = 2 * BN;                      // double-buffered accumulator
   static_assert(TMEM_COLS <= 512, "TMEM has 512 columns");
   static_assert((2 * STAGES + 5) * 8 + 8 <= BAR_BYTES, "barrier area too small");
@@ -122,8 +133,8 @@ template <int BN, int STAGES, bool A_MN, bool B_MN, bool B_DUAL, class Epi, bool
 __global__ void __launch_bounds__(gemm_threads<Epi>(), 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmB2, const GemmShape sh, const KernelCtl ctl,
-                   const typename Epi::Params ep) {
-  using L = GemmSmem<BN, STAGES>;
+                   const __grid_constant__ typename Epi::Params ep) {
+  using L = GemmSmem<BN, STAGES, epi_stage_bytes<Epi>()>;
   static_assert(!(B_DUAL && B_MN), "dual-box B is K-major only");
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
   static_assert(!FP8 || (!A_MN && !B_MN), "FP8 operands are K-major");
@@ -132,7 +143,7 @@ __global__ void __launch_bounds__(gemm_threads<Epi>(), 1)
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::RING_BYTES);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::RING_BYTES + L::STORE_BYTES);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
@@ -286,6 +297,8 @@ __global__ void __launch_bounds__(gemm_threads<Epi>(), 1)
     const int quad = warp & 3;
     const int first_half = HALVES == 1 ? (warp - 2) >> 2 : 0;
     const int row = quad * 32 + lane;
+    const uint32_t stage_base = smem_u32(smem + L::RING_BYTES) +
+                                static_cast<uint32_t>((warp - 2) * Epi::kStoreSlots * STORE_SLOT_BYTES);
     int it = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
       int tm, tn;
@@ -306,10 +319,12 @@ __global__ void __launch_bounds__(gemm_threads<Epi>(), 1)
       c.tn = tn;
       c.row = row;
       c.m = tm * BM + row;
+      c.m0 = tm * BM + quad * 32;
       c.quad = quad;
       c.lane = lane;
       c.acc_scale = acc_scale;
       c.taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      c.stage = stage_base;
 #pragma unroll 1
       for (int hh = 0; hh < HALVES; ++hh) {
         const int half = first_half + hh;
@@ -321,6 +336,9 @@ __global__ void __launch_bounds__(gemm_threads<Epi>(), 1)
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
     }
+    // the last stores have landed before shared memory is released
+    if (lane == 0) bulk_wait_group0();
+    __syncwarp();
   }
 
   __syncthreads();
@@ -348,18 +366,53 @@ __device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* p, int nvalid,
   }
 }
 
-__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* p, int nvalid, const float (&f)[32]) {
+// ---------------------------------------------------------------------------
+// Staged TMA stores.  A warp's 32 rows x 32 columns of an output are written
+// row-per-lane into one of its shared-memory slots in the swizzled layout of
+// the output's tensor map, and one lane stores the block with a single TMA
+// copy (whole lines to L2; rows past M and columns past N are clipped by the
+// tensor map).  Per step:
+//   slots_acquire   lane 0 waits until the stores it issued before have read
+//                   the slots, then the warp syncs;
+//   stage_*         every lane writes its row;
+//   slots_publish   every lane fences its writes to the async proxy, then the
+//                   warp syncs; lane 0 issues the stores and commits them.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t slot_addr(const EpiCtx& c, int i) {
+  return c.stage + static_cast<uint32_t>(i * STORE_SLOT_BYTES);
+}
+
+// bf16 block, 64-byte rows, 64-byte swizzle: the 16-byte chunk q of row r
+// sits at chunk position q ^ ((r >> 1) & 3).
+__device__ __forceinline__ void stage_bf16x32(uint32_t slot, int lane, const float (&f)[32]) {
+  const uint32_t row = slot + static_cast<uint32_t>(lane) * 64u;
+  const uint32_t sw = (static_cast<uint32_t>(lane) >> 1) & 3u;
 #pragma unroll
-  for (int g = 0; g < 4; ++g) {
-    if (g * 8 < nvalid) {
-      uint4 q;
-      q.x = pack_bf16x2(f[g * 8 + 0], f[g * 8 + 1]);
-      q.y = pack_bf16x2(f[g * 8 + 2], f[g * 8 + 3]);
-      q.z = pack_bf16x2(f[g * 8 + 4], f[g * 8 + 5]);
-      q.w = pack_bf16x2(f[g * 8 + 6], f[g * 8 + 7]);
-      *reinterpret_cast<uint4*>(p + g * 8) = q;
-    }
-  }
+  for (int q = 0; q < 4; ++q)
+    st_shared_v4(row + ((static_cast<uint32_t>(q) ^ sw) << 4), pack_bf16x2(f[8 * q + 0], f[8 * q + 1]),
+                 pack_bf16x2(f[8 * q + 2], f[8 * q + 3]), pack_bf16x2(f[8 * q + 4], f[8 * q + 5]),
+                 pack_bf16x2(f[8 * q + 6], f[8 * q + 7]));
+}
+
+// fp32 block (two slots), 128-byte rows, 128-byte swizzle: chunk q of row r
+// sits at chunk position q ^ (r & 7).
+__device__ __forceinline__ void stage_f32x32(uint32_t slot, int lane, const float (&f)[32]) {
+  const uint32_t row = slot + static_cast<uint32_t>(lane) * 128u;
+  const uint32_t sw = static_cast<uint32_t>(lane) & 7u;
+#pragma unroll
+  for (int q = 0; q < 8; ++q)
+    st_shared_v4(row + ((static_cast<uint32_t>(q) ^ sw) << 4), __float_as_uint(f[4 * q + 0]),
+                 __float_as_uint(f[4 * q + 1]), __float_as_uint(f[4 * q + 2]), __float_as_uint(f[4 * q + 3]));
+}
+
+__device__ __forceinline__ void slots_acquire(int lane) {
+  if (lane == 0) bulk_wait_group_read0();
+  __syncwarp();
+}
+
+__device__ __forceinline__ void slots_publish() {
+  fence_proxy_async_shared();
+  __syncwarp();
 }
 
 // lane l ends with sum over the 32 lanes of v[l]  (31 shuffles)
@@ -397,9 +450,9 @@ __device__ __forceinline__ float rstd_from_psum(const float* psum, int T, float 
 // C = bf16(row_scale[m] * col_scale[n] * acc); both scales optional.
 struct EpiStore {
   static constexpr int kEpiWarps = 4;
+  static constexpr int kStoreSlots = 1;
   struct Params {
-    __nv_bfloat16* out;
-    int64_t ldo;
+    CUtensorMap out;  // [M][N] bf16
     const float* row_scale;
     const __nv_bfloat16* col_scale;
     // optional: the row scale from first-GEMM partial sums instead of row_scale
@@ -425,7 +478,7 @@ struct EpiStore {
       float v[32];
       tmem_ld32(c.taddr + cc, v);
       const int n0 = c.tn * BN + cc;
-      if (row_ok && n0 < c.N) {
+      if (n0 < c.N && c.m0 < c.M) {
         if (p.col_scale != nullptr) {
           float s[32];
           load_bf16x32(p.col_scale + n0, c.N - n0, s);
@@ -434,43 +487,44 @@ struct EpiStore {
         }
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] *= rs;
-        store_bf16x32(p.out + static_cast<int64_t>(c.m) * p.ldo + n0, c.N - n0, v);
+        slots_acquire(c.lane);
+        stage_bf16x32(slot_addr(c, 0), c.lane, v);
+        slots_publish();
+        if (c.lane == 0) {
+          tma_store_2d(&p.out, slot_addr(c, 0), n0, c.m0);
+          bulk_commit_group();
+        }
       }
     }
   }
 };
 
-// fp32 output, overwrite (beta = 0) or accumulate (beta = 1).
+// fp32 output, overwrite (beta = 0) or accumulate (beta = 1, a TMA
+// reduce-add: each element receives one add per launch).
 struct EpiStoreF32 {
   static constexpr int kEpiWarps = 4;
+  static constexpr int kStoreSlots = 2;  // one 4 KB fp32 block
   struct Params {
-    float* out;
-    int64_t ldo;
+    CUtensorMap out;  // [M][N] fp32
     int beta;
   };
   template <int BN>
   static __device__ __forceinline__ void run(const Params& p, const EpiCtx& c) {
-    const bool row_ok = c.m < c.M;
 #pragma unroll 1
     for (int cc = c.c0; cc < c.c1; cc += 32) {
       float v[32];
       tmem_ld32(c.taddr + cc, v);
       const int n0 = c.tn * BN + cc;
-      if (row_ok && n0 < c.N) {
-        float* o = p.out + static_cast<int64_t>(c.m) * p.ldo + n0;
-#pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          if (g * 4 < c.N - n0) {
-            float4 w = make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
-            if (p.beta) {
-              const float4 old = *reinterpret_cast<const float4*>(o + 4 * g);
-              w.x += old.x;
-              w.y += old.y;
-              w.z += old.z;
-              w.w += old.w;
-            }
-            *reinterpret_cast<float4*>(o + 4 * g) = w;
-          }
+      if (n0 < c.N && c.m0 < c.M) {
+        slots_acquire(c.lane);
+        stage_f32x32(slot_addr(c, 0), c.lane, v);
+        slots_publish();
+        if (c.lane == 0) {
+          if (p.beta)
+            tma_reduce_add_2d(&p.out, slot_addr(c, 0), n0, c.m0);
+          else
+            tma_store_2d(&p.out, slot_addr(c, 0), n0, c.m0);
+          bulk_commit_group();
         }
       }
     }
@@ -481,18 +535,18 @@ struct EpiStoreF32 {
 // tile's columns of h^2 (h as stored, i.e. after rounding to bf16).
 struct EpiResPrms {
   static constexpr int kEpiWarps = 4;
+  static constexpr int kStoreSlots = 2;
   struct Params {
+    CUtensorMap H;   // [M][d] bf16
+    CUtensorMap Hg;  // [M][d] bf16, used when g != null
     const __nv_bfloat16* R;
     int64_t ldr;
-    __nv_bfloat16* H;
-    int64_t ldh;
     float* psum;
     int T;  // psum columns
     // optional: the RMSNorm weight broadcast along the row (vector load) and
     // a second output Hg = bf16(H * g), the second GEMM's A operand when g is
     // applied on the activation side instead of being folded into W2
     const __nv_bfloat16* g;
-    __nv_bfloat16* Hg;
   };
   template <int BN>
   static __device__ __forceinline__ void run(const Params& p, const EpiCtx& c) {
@@ -503,21 +557,28 @@ struct EpiResPrms {
       float v[32];
       tmem_ld32(c.taddr + cc, v);
       const int n0 = c.tn * BN + cc;
-      if (row_ok && n0 < c.N) {
+      if (n0 < c.N && c.m0 < c.M) {
         float r[32];
-        load_bf16x32(p.R + static_cast<int64_t>(c.m) * p.ldr + n0, c.N - n0, r);
+        load_bf16x32(p.R + static_cast<int64_t>(c.m) * p.ldr + n0, row_ok ? c.N - n0 : 0, r);
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const float hb = bf16_round(fmaf(v[i], c.acc_scale, r[i]));
           v[i] = hb;
           ss = fmaf(hb, hb, ss);
         }
-        store_bf16x32(p.H + static_cast<int64_t>(c.m) * p.ldh + n0, c.N - n0, v);
-        if (p.Hg != nullptr) {
+        slots_acquire(c.lane);
+        stage_bf16x32(slot_addr(c, 0), c.lane, v);
+        if (p.g != nullptr) {
           load_bf16x32(p.g + n0, c.N - n0, r);
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] *= r[i];
-          store_bf16x32(p.Hg + static_cast<int64_t>(c.m) * p.ldh + n0, c.N - n0, v);
+          stage_bf16x32(slot_addr(c, 1), c.lane, v);
+        }
+        slots_publish();
+        if (c.lane == 0) {
+          tma_store_2d(&p.H, slot_addr(c, 0), n0, c.m0);
+          if (p.g != nullptr) tma_store_2d(&p.Hg, slot_addr(c, 1), n0, c.m0);
+          bulk_commit_group();
         }
       }
     }
@@ -527,17 +588,17 @@ struct EpiResPrms {
 
 // GEMM2 epilogue: the accumulator holds [gate | up] halves of BN/2 columns
 // (two B boxes).  z = rstd[m] * acc; out = silu(z_gate) * z_up; optionally
-// save z (bf16) for the backward.  In plain mode (swiglu == 0, single box)
-// out = rstd[m] * acc.
+// save z (bf16) for the backward.
 struct EpiRowscaleSwiglu {
   static constexpr int kEpiWarps = 4;
+  static constexpr int kStoreSlots = 3;  // out, z gate, z up
   struct Params {
+    CUtensorMap out;  // [M][F] bf16
+    CUtensorMap zg;   // gate half of z: [M][F] with the row pitch of z
+    CUtensorMap zu;   // up half of z
+    int save_z;
     const float* rstd;
-    __nv_bfloat16* out;
-    int64_t ldo;
-    __nv_bfloat16* zsave;  // may be null
-    int64_t ldz;
-    int F;                 // gate (= up) width; output columns
+    int F;            // gate (= up) width; output columns
     // optional: the row scale from first-GEMM partial sums instead of rstd
     const float* psum;
     int T;
@@ -558,21 +619,29 @@ struct EpiRowscaleSwiglu {
       tmem_ld32(c.taddr + cc, g);
       tmem_ld32(c.taddr + HB + cc, u);
       const int j0 = c.tn * HB + cc;
-      if (row_ok && j0 < p.F) {
-        const int nv = p.F - j0;
+      if (j0 < p.F && c.m0 < c.M) {
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           g[i] *= r;
           u[i] *= r;
         }
-        if (p.zsave != nullptr) {
-          store_bf16x32(p.zsave + static_cast<int64_t>(c.m) * p.ldz + j0, nv, g);
-          store_bf16x32(p.zsave + static_cast<int64_t>(c.m) * p.ldz + p.F + j0, nv, u);
+        slots_acquire(c.lane);
+        if (p.save_z) {
+          stage_bf16x32(slot_addr(c, 1), c.lane, g);
+          stage_bf16x32(slot_addr(c, 2), c.lane, u);
         }
-        float o[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] = silu_f(g[i]) * u[i];
-        store_bf16x32(p.out + static_cast<int64_t>(c.m) * p.ldo + j0, nv, o);
+        for (int i = 0; i < 32; ++i) g[i] = silu_f(g[i]) * u[i];
+        stage_bf16x32(slot_addr(c, 0), c.lane, g);
+        slots_publish();
+        if (c.lane == 0) {
+          tma_store_2d(&p.out, slot_addr(c, 0), j0, c.m0);
+          if (p.save_z) {
+            tma_store_2d(&p.zg, slot_addr(c, 1), j0, c.m0);
+            tma_store_2d(&p.zu, slot_addr(c, 2), j0, c.m0);
+          }
+          bulk_commit_group();
+        }
       }
     }
   }
@@ -583,13 +652,13 @@ struct EpiRowscaleSwiglu {
 //   sum over the warp's 32 rows of acc * h  (block reduction across lanes).
 struct EpiDgradRms {
   static constexpr int kEpiWarps = 4;
+  static constexpr int kStoreSlots = 1;
   struct Params {
+    CUtensorMap dH;  // [M][d] bf16
     const __nv_bfloat16* H;
     int64_t ldh;
     const __nv_bfloat16* g;
     const float* c;
-    __nv_bfloat16* dH;
-    int64_t lddh;
     float* dgpart;  // [4 * tiles_m, N]
     // optional: c from the SwiGLU-backward epilogue's partial sums,
     // c[m] = rstd[m]^2 * inv_d * sum_j cpart[m, j], instead of the c vector
@@ -622,11 +691,17 @@ struct EpiDgradRms {
         float h[32], gv[32];
         load_bf16x32(p.H + static_cast<int64_t>(c.m) * p.ldh + n0, row_ok ? c.N - n0 : 0, h);
         load_bf16x32(p.g + n0, c.N - n0, gv);
-        if (row_ok) {
+        if (c.m0 < c.M) {
           float dh[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) dh[i] = fmaf(gv[i], a[i], -cm * h[i]);
-          store_bf16x32(p.dH + static_cast<int64_t>(c.m) * p.lddh + n0, c.N - n0, dh);
+          slots_acquire(c.lane);
+          stage_bf16x32(slot_addr(c, 0), c.lane, dh);
+          slots_publish();
+          if (c.lane == 0) {
+            tma_store_2d(&p.dH, slot_addr(c, 0), n0, c.m0);
+            bulk_commit_group();
+          }
         }
 #pragma unroll
         for (int i = 0; i < 32; ++i) a[i] *= h[i];
@@ -650,10 +725,12 @@ struct EpiDgradRms {
 // never leaves the chip.
 struct EpiSwigluBwd {
   static constexpr int kEpiWarps = 8;  // loads z and stores dP: more loads in flight
+  static constexpr int kStoreSlots = 2;
   struct Params {
+    CUtensorMap dPg;  // gate half of dP: [M][F] with the row pitch of dP
+    CUtensorMap dPu;  // up half
     const __nv_bfloat16* z;  // [M, 2F]
     const float* rstd;
-    __nv_bfloat16* dP;       // [M, 2F]
     float* cpart;            // [M, T]
     int T;
     int F;
@@ -669,22 +746,29 @@ struct EpiSwigluBwd {
       float dy[32];
       tmem_ld32(c.taddr + cc, dy);
       const int j0 = c.tn * BN + cc;
-      if (row_ok && j0 < p.F) {
-        const int nv = p.F - j0;
+      if (j0 < p.F && c.m0 < c.M) {
+        const int nv = row_ok ? p.F - j0 : 0;
         float zg[32], zu[32];
         load_bf16x32(p.z + row + j0, nv, zg);
         load_bf16x32(p.z + row + p.F + j0, nv, zu);
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const float s = 1.0f / (1.0f + __expf(-zg[i]));
+          const float s = sigmoid_f(zg[i]);
           const float dzu = dy[i] * zg[i] * s;
           const float dzg = dy[i] * zu[i] * s * (1.0f + zg[i] * (1.0f - s));
           cp = fmaf(dzg, zg[i], fmaf(dzu, zu[i], cp));
           zg[i] = r * dzg;
           zu[i] = r * dzu;
         }
-        store_bf16x32(p.dP + row + j0, nv, zg);
-        store_bf16x32(p.dP + row + p.F + j0, nv, zu);
+        slots_acquire(c.lane);
+        stage_bf16x32(slot_addr(c, 0), c.lane, zg);
+        stage_bf16x32(slot_addr(c, 1), c.lane, zu);
+        slots_publish();
+        if (c.lane == 0) {
+          tma_store_2d(&p.dPg, slot_addr(c, 0), j0, c.m0);
+          tma_store_2d(&p.dPu, slot_addr(c, 1), j0, c.m0);
+          bulk_commit_group();
+        }
       }
     }
     if (row_ok && c.tn * BN + c.c0 < p.F) p.cpart[static_cast<int64_t>(c.m) * p.T + c.part] = cp;
@@ -698,9 +782,9 @@ struct EpiSwigluBwd {
 // (the vector-load primitive); v heads (columns >= rot_cols) pass through.
 struct EpiRope {
   static constexpr int kEpiWarps = 4;
+  static constexpr int kStoreSlots = 2;
   struct Params {
-    __nv_bfloat16* out;
-    int64_t ldo;
+    CUtensorMap out;     // [M][N] bf16
     const float* cos_t;  // [S, 64]
     const float* sin_t;  // [S, 64]
     int S;
@@ -713,32 +797,37 @@ struct EpiRope {
     const bool row_ok = c.m < c.M;
     const bool rot = nh < p.rot_cols;
     const int64_t tab = row_ok ? static_cast<int64_t>(c.m % p.S) * 64 : 0;
-    __nv_bfloat16* o = p.out + static_cast<int64_t>(c.m) * p.ldo + nh;
 #pragma unroll 1
     for (int cc = 0; cc < 64; cc += 32) {
       float x1[32], x2[32];
       tmem_ld32(c.taddr + c.c0 + cc, x1);
       tmem_ld32(c.taddr + c.c0 + 64 + cc, x2);
-      if (row_ok) {
-        if (rot) {
-          const float4* cs4 = reinterpret_cast<const float4*>(p.cos_t + tab + cc);
-          const float4* sn4 = reinterpret_cast<const float4*>(p.sin_t + tab + cc);
+      if (c.m0 >= c.M) continue;
+      if (rot) {
+        const float4* cs4 = reinterpret_cast<const float4*>(p.cos_t + tab + cc);
+        const float4* sn4 = reinterpret_cast<const float4*>(p.sin_t + tab + cc);
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const float4 cq = __ldg(cs4 + q), sq = __ldg(sn4 + q);
-            const float cv[4] = {cq.x, cq.y, cq.z, cq.w};
-            const float sv[4] = {sq.x, sq.y, sq.z, sq.w};
+        for (int q = 0; q < 8; ++q) {
+          const float4 cq = __ldg(cs4 + q), sq = __ldg(sn4 + q);
+          const float cv[4] = {cq.x, cq.y, cq.z, cq.w};
+          const float sv[4] = {sq.x, sq.y, sq.z, sq.w};
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const int i = 4 * q + k;
-              const float a = x1[i], b = x2[i];
-              x1[i] = fmaf(a, cv[k], -b * sv[k]);
-              x2[i] = fmaf(b, cv[k], a * sv[k]);
-            }
+          for (int k = 0; k < 4; ++k) {
+            const int i = 4 * q + k;
+            const float a = x1[i], b = x2[i];
+            x1[i] = fmaf(a, cv[k], -b * sv[k]);
+            x2[i] = fmaf(b, cv[k], a * sv[k]);
           }
         }
-        store_bf16x32(o + cc, c.N - (nh + cc), x1);
-        store_bf16x32(o + 64 + cc, c.N - (nh + 64 + cc), x2);
+      }
+      slots_acquire(c.lane);
+      stage_bf16x32(slot_addr(c, 0), c.lane, x1);
+      stage_bf16x32(slot_addr(c, 1), c.lane, x2);
+      slots_publish();
+      if (c.lane == 0) {
+        if (nh + cc < c.N) tma_store_2d(&p.out, slot_addr(c, 0), nh + cc, c.m0);
+        if (nh + 64 + cc < c.N) tma_store_2d(&p.out, slot_addr(c, 1), nh + 64 + cc, c.m0);
+        bulk_commit_group();
       }
     }
   }
@@ -750,6 +839,7 @@ struct EpiRope {
 // tile.  Columns >= N (vocabulary tail) are masked out.
 struct EpiCeStats {
   static constexpr int kEpiWarps = 4;
+  static constexpr int kStoreSlots = 0;
   struct Params {
     const int32_t* labels;
     float* pmax;
@@ -815,11 +905,11 @@ struct EpiCeStats {
 // into a vocabulary-chunk buffer (column n of the chunk = vocabulary v0 + n).
 struct EpiCeGrad {
   static constexpr int kEpiWarps = 4;
+  static constexpr int kStoreSlots = 1;
   struct Params {
+    CUtensorMap dL;  // [M][Vc] bf16
     const int32_t* labels;
     const float* lse;
-    __nv_bfloat16* dL;
-    int64_t ldd;
     float inv_M;
     int v0;
   };
@@ -833,13 +923,19 @@ struct EpiCeGrad {
       float v[32];
       tmem_ld32(c.taddr + cc, v);
       const int n0 = c.tn * BN + cc;
-      if (row_ok && n0 < c.N) {
+      if (n0 < c.N && c.m0 < c.M) {
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const float e = __expf(v[i] - l) - ((n0 + i == y) ? 1.f : 0.f);
           v[i] = e * p.inv_M;
         }
-        store_bf16x32(p.dL + static_cast<int64_t>(c.m) * p.ldd + n0, c.N - n0, v);
+        slots_acquire(c.lane);
+        stage_bf16x32(slot_addr(c, 0), c.lane, v);
+        slots_publish();
+        if (c.lane == 0) {
+          tma_store_2d(&p.dL, slot_addr(c, 0), n0, c.m0);
+          bulk_commit_group();
+        }
       }
     }
   }

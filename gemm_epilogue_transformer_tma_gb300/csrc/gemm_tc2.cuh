@@ -31,14 +31,16 @@ namespace coda {
 
 constexpr int BM2 = 256;  // output rows per CTA pair
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int EPI_BYTES>
 struct Gemm2Smem {
   static constexpr int A_BYTES = 128 * BK * 2;        // this CTA's 128 rows of A
   static constexpr int B_BYTES = (BN / 2) * BK * 2;   // this CTA's BN/2 rows of B
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
+  static constexpr int STORE_BYTES = EPI_BYTES;       // epilogue store staging
   static constexpr int BAR_BYTES = 512;
-  static constexpr int TOTAL = RING_BYTES + BAR_BYTES + 1024;
+  static constexpr int TOTAL = RING_BYTES + STORE_BYTES + BAR_BYTES + 1024;
+  static_assert(TOTAL <= MAX_DYN_SMEM, "shared memory budget");
   static constexpr int TMEM_COLS = 2 * BN;
   static_assert(TMEM_COLS <= 512, "TMEM has 512 columns");
   static_assert((2 * STAGES + 5) * 8 + 8 <= BAR_BYTES, "barrier area too small");
@@ -49,8 +51,8 @@ template <int BN, int STAGES, bool A_MN, bool B_MN, bool B_DUAL, class Epi, bool
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi>(), 1)
     gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmB2, const GemmShape sh, const KernelCtl ctl,
-                    const typename Epi::Params ep) {
-  using L = Gemm2Smem<BN, STAGES>;
+                    const __grid_constant__ typename Epi::Params ep) {
+  using L = Gemm2Smem<BN, STAGES, epi_stage_bytes<Epi>()>;
   static_assert(!(B_DUAL && B_MN), "dual-box B is K-major only");
   static_assert(BN == 256, "the pair kernel is instantiated for 256-column tiles");
   static_assert(!FP8 || (!A_MN && !B_MN), "FP8 operands are K-major");
@@ -60,7 +62,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi>(),
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::RING_BYTES);  // leader's counts both halves
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::RING_BYTES + L::STORE_BYTES);  // leader's counts both halves
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;  // leader only: both CTAs' epilogues released the buffer
@@ -238,6 +240,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi>(),
     const int first_half = HALVES == 1 ? (warp - 2) >> 2 : 0;
     const int row = quad * 32 + lane;
     const uint32_t leader_tempty = mapa_shared(smem_u32(tempty), 0);
+    const uint32_t stage_base = smem_u32(smem + L::RING_BYTES) +
+                                static_cast<uint32_t>((warp - 2) * Epi::kStoreSlots * STORE_SLOT_BYTES);
     int it = 0;
     for (int t = cluster_id; t < num_tiles; t += num_clusters, ++it) {
       int tm, tn;
@@ -258,10 +262,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi>(),
       c.tn = tn;
       c.row = row;
       c.m = c.tm * 128 + row;
+      c.m0 = c.tm * 128 + quad * 32;
       c.quad = quad;
       c.lane = lane;
       c.acc_scale = acc_scale;
       c.taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      c.stage = stage_base;
 #pragma unroll 1
       for (int hh = 0; hh < HALVES; ++hh) {
         const int half = first_half + hh;
@@ -274,6 +280,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi>(),
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(leader_tempty + static_cast<uint32_t>(acc * 8));
     }
+    // the last stores have landed before shared memory is released
+    if (lane == 0) bulk_wait_group0();
+    __syncwarp();
   }
 
   __syncwarp();

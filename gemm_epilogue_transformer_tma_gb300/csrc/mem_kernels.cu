@@ -112,7 +112,7 @@ __device__ __forceinline__ float swiglu_bwd_chunk(const uint4& dyq, const uint4&
   float dot = 0.f;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const float s = 1.0f / (1.0f + __expf(-zg[i]));
+    const float s = sigmoid_f(zg[i]);
     const float dzu = dy[i] * zg[i] * s;
     const float dzg = dy[i] * zu[i] * s * (1.0f + zg[i] * (1.0f - s));
     dot = fmaf(dzg, zg[i], fmaf(dzu, zu[i], dot));
@@ -447,7 +447,7 @@ __global__ void swiglu_bwd_plain_kernel(const __nv_bfloat16* __restrict__ dY, co
     unpack_bf16x8(reinterpret_cast<const uint4*>(z + m * 2 * F + F)[j], zu);
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      const float s = 1.0f / (1.0f + __expf(-zg[k]));
+      const float s = sigmoid_f(zg[k]);
       og[k] = dy[k] * zu[k] * s * (1.0f + zg[k] * (1.0f - s));
       ou[k] = dy[k] * zg[k] * s;
     }

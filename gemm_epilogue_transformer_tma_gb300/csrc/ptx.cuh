@@ -1,5 +1,5 @@
 // Thin inline-PTX layer for sm_103a: mbarriers with bounded waits, TMA tile
-// loads, and the tcgen05 family (TMEM allocation, MMA issue, commit, TMEM
+// loads and stores, and the tcgen05 family (TMEM allocation, MMA issue, commit, TMEM
 // loads, ordering fences).  Everything here is a one-to-one wrapper around a
 // single PTX instruction; the GEMM pipeline in gemm_tc.cuh composes them.
 #pragma once
@@ -160,6 +160,46 @@ __device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const CUtensorM
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(bar_cluster)
       : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// TMA stores: a 2-D box from shared memory to global memory (elements outside
+// the tensor map's extent are not written), tracked per thread in bulk
+// async-groups.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, uint32_t smem_src, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(smem_src), "r"(x), "r"(y)
+               : "memory");
+}
+
+// Element-wise add of the box into global memory (fp32 accumulate).
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* m, uint32_t smem_src, int32_t x, int32_t y) {
+  asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(smem_src), "r"(x), "r"(y)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Every bulk store this thread committed has finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_group_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Every bulk store this thread committed has completed.
+__device__ __forceinline__ void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Orders this thread's shared-memory writes before later async-proxy (TMA)
+// reads of them.
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
 // ---------------------------------------------------------------------------
@@ -368,6 +408,11 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4& q, float* f) {
   }
 }
 
-__device__ __forceinline__ float silu_f(float x) { return x / (1.0f + __expf(-x)); }
+// sigmoid and silu with the fast exponential and the fast (approximate
+// reciprocal) division: a few ulp of fp32, far below the bf16 rounding of
+// every value they feed.  For x < -88, exp(-x) overflows to inf and both
+// return 0 (silu's true value there is below 1e-36).
+__device__ __forceinline__ float sigmoid_f(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
+__device__ __forceinline__ float silu_f(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
 
 }  // namespace coda
