@@ -43,7 +43,8 @@ UNIT = "TFLOP/s"
 CONFIGS = {"7b": B7, "70b": B70, "1b": B1}  # 1b: forward only
 
 
-KERNEL_SOURCES = ["ptx.cuh", "gemm_tc.cuh", "gemm_tc2.cuh", "gemm_launch.cuh", "gemm_fwd.cu", "gemm_bwd.cu"]
+KERNEL_SOURCES = ["ptx.cuh", "gemm_tc.cuh", "gemm_tc2.cuh", "gemm_group.cuh", "gemm_launch.cuh", "gemm_fwd.cu",
+                  "gemm_bwd.cu", "gemm_group.cu"]
 
 
 def kernel_sources_sha256():
@@ -150,8 +151,8 @@ class FusedStep:
             gemm2: 2.0 * s.M * s.N2 * s.d,
             "dgrad2_rmsbwd": 2.0 * s.M * s.N2 * s.d,
             "wgrad2_gscale": 2.0 * s.M * s.N2 * s.d,
-            "dgrad1": 2.0 * s.M * s.d * s.K1,
-            "wgrad1": 2.0 * s.M * s.d * s.K1,
+            # dgrad1 and wgrad1 run as one grouped launch
+            "dgrad1_wgrad1": 2 * 2.0 * s.M * s.d * s.K1,
         }
         if g_on_activation:
             # g broadcast in GEMM1's epilogue (Hg), GEMM2 on the unfolded W2
@@ -177,8 +178,7 @@ class FusedStep:
             ("dgrad2_rmsbwd", lambda: C.coda_gemm_dgrad_rmsbwd(b.dP, b.W2t, b.H, b.g, b.c, b.dH, b.dgpart)),
             ("dg_combine", lambda: C.coda_dg_combine(b.dgpart, b.dg)),
             ("wgrad2_gscale", lambda: C.coda_gemm_wgrad_gscale(b.H, b.dP, b.g, b.dW2t)),
-            ("dgrad1", lambda: C.coda_gemm(b.dH, False, b.W1t, True, b.dX, b.M, b.K1, b.d)),
-            ("wgrad1", lambda: C.coda_gemm(b.dH, True, b.X, True, b.dW1t, b.d, b.K1, b.M)),
+            ("dgrad1_wgrad1", lambda: C.coda_gemm_res_prms_bwd(b.dH, b.X, b.W1t, b.dX, b.dW1t, b.dH)),
         ]
         self.stages = fwd + (bwd if b.with_backward else [])
 

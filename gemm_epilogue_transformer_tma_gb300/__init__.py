@@ -53,6 +53,7 @@ SIGNATURES = {
     "coda_sync_status": (_INT, [_P, _P, ctypes.POINTER(ctypes.c_int32)]),
     "coda_set_wait_timeout_ns": (_INT, [_P, _U64]),
     "coda_debug_skip_first_stage": (_INT, [_P, _INT]),
+    "coda_debug_group_schedule_violations": (_INT, [_INT, _INT, _INT, _INT, _INT]),
     "coda_set_sm_pairing": (_INT, [_P, _INT]),
     "coda_prms_num_tiles": (_I64, [_I64]),
     "coda_dgpart_rows": (_I64, [_I64]),
@@ -382,6 +383,11 @@ def coda_gemm_wgrad_gscale(H, dP, g, dW2t, stream=None):
     _check(load_library().coda_gemm_wgrad_gscale(_h(H), _ptr(H, BF, "H"), _ptr(dP, BF, "dP"), _ptr(g, BF, "g"),
                                                  _ptr(dW2t, BF, "dW2t"), M, N2, d, _stream(stream)),
            "coda_gemm_wgrad_gscale")
+
+
+def coda_debug_group_schedule_violations(P: int, heavy: int, nH: int, nL: int, q: int) -> int:
+    """Host check of the grouped launches' tile schedule (see include/coda.h)."""
+    return load_library().coda_debug_group_schedule_violations(P, heavy, nH, nL, q)
 
 
 def coda_bwd_workspace_bytes(M: int, d: int, N2: int) -> int:

@@ -460,6 +460,11 @@ size_t coda_bwd_workspace_bytes(int64_t M, int64_t d, int64_t N2) {
   return align256(size_t(M) * N2 * 2) + align256(size_t(M) * 4) + align256(size_t(coda_dgpart_rows(M)) * d * 4);
 }
 
+int coda_debug_group_schedule_violations(int P, int heavy, int nH, int nL, int q) {
+  if (P <= 0 || nH < 0 || nL < 0 || q < 0 || (heavy != 0 && heavy != 1)) return -1;
+  return group_schedule_violations(P, heavy, nH, nL, q);
+}
+
 coda_status_t coda_gemm_rowscale_swiglu_bwd(coda_handle_t h, const void* dY, const void* z, const float* rstd,
                                             const void* H, const void* W2t, const void* g, void* dH, void* dW2t,
                                             float* dg, void* ws, size_t ws_bytes, int64_t M, int64_t d, int64_t N2,
@@ -497,6 +502,8 @@ coda_status_t coda_gemm_rowscale_swiglu_bwd(coda_handle_t h, const void* dY, con
   const LaunchCtx cx = ctx_of(h, stream);
   CODA_CUDA(launch_swiglu_bwd(cx, static_cast<const bf16*>(dY), static_cast<const bf16*>(z), rstd, dP, c, M, N2 / 2,
                               d));
+  // The data and weight gradients stay two launches here: grouped into one
+  // (gemm_group.cuh) they measured 4-5 % slower at these sizes.
   CODA_CUDA(gemm_dgrad_rms(cx, dP, static_cast<const bf16*>(W2t), static_cast<const bf16*>(H),
                            static_cast<const bf16*>(g), c, static_cast<bf16*>(dH), dgpart, int(M), int(N2), int(d)));
   CODA_CUDA(launch_col_combine(cx, dgpart, coda_dgpart_rows(M), d, dg));
@@ -510,12 +517,11 @@ coda_status_t coda_gemm_res_prms_bwd(coda_handle_t h, const void* dH, const void
   CODA_TRY(Check().handle(h).rows(M).mptr(dH, M).mptr(X, M).ptr(W1t).mptr(dX, M).ptr(dW1t).opt_ptr(dR).cols(K1).cols(d).st);
   const LaunchCtx cx = ctx_of(h, stream);
   if (M == 0) return from_cuda(cudaMemsetAsync(dW1t, 0, size_t(d) * K1 * 2, cx.stream));
-  // dX[m][i] = sum_k dH[m][k] W1t[k][i]: A = dH [M][d], B = W1t stored [K][N]
-  CODA_CUDA(gemm_store(cx, static_cast<const bf16*>(dH), false, static_cast<const bf16*>(W1t), true,
-                       static_cast<bf16*>(dX), int(M), int(K1), int(d), nullptr, nullptr));
-  // dW1t[k][i] = sum_m dH[m][k] X[m][i]: M' = d, N' = K1, K' = M
-  CODA_CUDA(gemm_store(cx, static_cast<const bf16*>(dH), true, static_cast<const bf16*>(X), true,
-                       static_cast<bf16*>(dW1t), int(d), int(K1), int(M), nullptr, nullptr));
+  // dX[m][i] = sum_k dH[m][k] W1t[k][i] and dW1t[k][i] = sum_m dH[m][k] X[m][i],
+  // one grouped launch
+  CODA_CUDA(gemm_group_store(cx, static_cast<const bf16*>(dH), static_cast<const bf16*>(W1t),
+                             static_cast<const bf16*>(X), static_cast<bf16*>(dX), static_cast<bf16*>(dW1t), int(M),
+                             int(K1), int(d)));
   if (dR != nullptr && dR != dH)
     CODA_CUDA(cudaMemcpyAsync(dR, dH, size_t(M) * d * 2, cudaMemcpyDeviceToDevice, cx.stream));
   return CODA_OK;
@@ -707,11 +713,10 @@ coda_status_t coda_lmhead_ce(coda_handle_t h, const void* Hs, const void* Wt, co
     const bf16* Wc = Wb + v0 * d;
     // dL[:, chunk] = (softmax - onehot) / M, recomputing the logits
     CODA_CUDA(gemm_ce_grad(cx, Hb, Wc, labels, lse, w.dL, int(M), int(d), int(Vc), int(v0), inv_M));
-    // dH (+)= dL Wc : A = dL [M][Vc], B = Wc stored [Vc][d] = [K][N]
-    CODA_CUDA(gemm_store_f32(cx, w.dL, false, Wc, true, w.dH32, int(M), int(d), int(Vc), v0 > 0));
-    // dWt[v0 + v][k] = sum_m dL[m][v] Hs[m][k] : M' = Vc, N' = d, K' = M
-    CODA_CUDA(gemm_store(cx, w.dL, true, Hb, true, static_cast<bf16*>(dWt) + v0 * d, int(Vc), int(d), int(M),
-                         nullptr, nullptr));
+    // dH (+)= dL Wc (Wc stored [Vc][d]) and dWt[v0 + v][k] = sum_m dL[m][v]
+    // Hs[m][k], one grouped launch
+    CODA_CUDA(gemm_group_ce_bwd(cx, w.dL, Wc, Hb, w.dH32, v0 > 0, static_cast<bf16*>(dWt) + v0 * d, int(M), int(d),
+                                int(Vc)));
   }
   CODA_CUDA(launch_f32_to_bf16(cx, w.dH32, static_cast<bf16*>(dHs), M * d));
   return CODA_OK;
@@ -813,6 +818,9 @@ coda_status_t coda_unfused_bwd(coda_handle_t h, const void* dY, const void* X, c
   float* dgpart = reinterpret_cast<float*>(w);
   const int64_t parts = cdiv(M, kUnfusedDgRows);
   CODA_CUDA(launch_swiglu_bwd_plain(cx, static_cast<const bf16*>(dY), static_cast<const bf16*>(z), dZ, M, N2 / 2));
+  // the GEMM launches are those of the fused path (two for the second
+  // layer, one grouped launch for the first), so the comparison isolates
+  // the epilogue fusion
   // dN[m][k] = sum_n dZ[m][n] W2t[n][k]
   CODA_CUDA(gemm_store(cx, dZ, false, static_cast<const bf16*>(W2t), true, dN, int(M), int(d), int(N2), nullptr,
                        nullptr));
@@ -823,10 +831,9 @@ coda_status_t coda_unfused_bwd(coda_handle_t h, const void* dY, const void* X, c
   // dW2t[n][k] = sum_m dZ[m][n] Nrm[m][k]
   CODA_CUDA(gemm_store(cx, dZ, true, static_cast<const bf16*>(Nrm), true, static_cast<bf16*>(dW2t), int(N2), int(d),
                        int(M), nullptr, nullptr));
-  CODA_CUDA(gemm_store(cx, static_cast<const bf16*>(dH), false, static_cast<const bf16*>(W1t), true,
-                       static_cast<bf16*>(dX), int(M), int(K1), int(d), nullptr, nullptr));
-  CODA_CUDA(gemm_store(cx, static_cast<const bf16*>(dH), true, static_cast<const bf16*>(X), true,
-                       static_cast<bf16*>(dW1t), int(d), int(K1), int(M), nullptr, nullptr));
+  CODA_CUDA(gemm_group_store(cx, static_cast<const bf16*>(dH), static_cast<const bf16*>(W1t),
+                             static_cast<const bf16*>(X), static_cast<bf16*>(dX), static_cast<bf16*>(dW1t), int(M),
+                             int(K1), int(d)));
   return CODA_OK;
 }
 

@@ -126,6 +126,19 @@ cudaError_t gemm_rowscale_swiglu_fp8(const LaunchCtx& c, const uint8_t* Hq, cons
                                      const float* sW2, const float* rstd, __nv_bfloat16* out, __nv_bfloat16* zsave,
                                      int M, int d, int N2, bool swiglu);
 
+// Independent GEMM pairs in one launch (SM-pair kernel; two launches of the
+// 1-SM kernel when pairing is off):
+//   dX = dH W1t (W1t [d][K1]) and dW1t = dH^T X (any such pair: A [M][d]
+//   K-major with B [d][K1], and A^T with X [M][K1]);
+cudaError_t gemm_group_store(const LaunchCtx& c, const __nv_bfloat16* dH, const __nv_bfloat16* W1t,
+                             const __nv_bfloat16* X, __nv_bfloat16* dX, __nv_bfloat16* dW1t, int M, int K1, int d);
+//   LM-head chunk: dH32 (+)= dL Wc (Wc [Vc][d]) in fp32 and dWc = dL^T H.
+cudaError_t gemm_group_ce_bwd(const LaunchCtx& c, const __nv_bfloat16* dL, const __nv_bfloat16* Wc,
+                              const __nv_bfloat16* H, float* dH32, bool accumulate, __nv_bfloat16* dWc, int M, int d,
+                              int Vc);
+// Host check of the grouped tile schedule (0 = every tile visited once).
+int group_schedule_violations(int P, int heavy, int nH, int nL, int q);
+
 int ce_tile_cols();    // vocabulary columns per CE statistics tile
 int prms_tile_cols();  // columns per partial-RMS tile of GEMM1
 

@@ -22,7 +22,7 @@ def lib():
 
 def declared():
     src = open(HEADER).read()
-    return set(re.findall(r"^\s*(?:coda_status_t|const char\*|int64_t|size_t)\s+(coda_\w+)\s*\(", src, re.M))
+    return set(re.findall(r"^\s*(?:coda_status_t|const char\*|int64_t|size_t|int)\s+(coda_\w+)\s*\(", src, re.M))
 
 
 def test_header_declares_the_named_entry_points():
