@@ -77,8 +77,7 @@ class BlockBuffers:
             coda_gemm_res_prms_g(self.X, self.W1t, self.R, self.g, self.H, self.Hg, self.psum)
             A2, B2 = self.Hg, self.W2t
         else:
-            coda_fold_rmsnorm_weight(self.W2t, self.g, self.W2gt)
-            coda_gemm_res_prms(self.X, self.W1t, self.R, self.H, self.psum)
+            self.gemm1_and_fold()
             A2, B2 = self.H, self.W2gt
         if self.fuse_rstd:
             # the combine runs inside GEMM2's epilogue, which also stores rstd
@@ -92,6 +91,26 @@ class BlockBuffers:
             coda_gemm_rowscale_swiglu(A2, B2, self.rstd, self.out, self.z if save_z else None, CODA_EPI_SWIGLU)
         else:
             coda_gemm_rowscale_swiglu(A2, B2, self.rstd, self.z, None, CODA_EPI_PLAIN)
+
+    def gemm1_and_fold(self):
+        """GEMM1 + residual + partial RMS on the current stream, and the fold
+        W2g = g * W2 beside it on a second stream; returns with the current
+        stream ordered after both.  The fold reads only the weights and is
+        HBM-bound.  GEMM1 is tensor-bound and leaves shared memory, threads
+        and registers free on every SM, so the two share the SMs.  GEMM1 is
+        launched first: its persistent CTAs take their SMs before the fold's
+        CTAs fill them."""
+        main = torch.cuda.current_stream(self.X.device)
+        if getattr(self, "_side", None) is None:
+            self._side = torch.cuda.Stream(device=self.X.device)
+            self._ev_in = torch.cuda.Event()
+            self._ev_fold = torch.cuda.Event()
+        self._ev_in.record(main)
+        coda_gemm_res_prms(self.X, self.W1t, self.R, self.H, self.psum)
+        self._side.wait_event(self._ev_in)
+        coda_fold_rmsnorm_weight(self.W2t, self.g, self.W2gt, stream=self._side)
+        self._ev_fold.record(self._side)
+        main.wait_event(self._ev_fold)
 
     def backward_stages(self):
         """The backward as separate stage calls (dP, c, dgpart stay visible)."""
