@@ -17,7 +17,9 @@
 //                tcgen05.mma (M=128, N=BN, K=16) into one of two TMEM
 //                accumulator buffers and commits to mbarriers.
 //   warps 2..    epilogue: tcgen05.ld the accumulator (one row per thread),
-//                run the epilogue program, store to HBM, release the buffer.
+//                run the epilogue program, stage its outputs in shared memory
+//                and store them with TMA (32 x 32 blocks per warp), release
+//                the buffer.
 //                The program runs once per 128-column half of the tile: with
 //                8 warps, two per TMEM lane quadrant take one half each; with
 //                4 warps, each warp runs both halves in turn.  Block
