@@ -5,6 +5,7 @@
 //
 // All accesses are 16-byte vectors (8 bf16 or 4 fp32) along the contiguous
 // dimension; every extent on the boundary is a multiple of 8 elements.
+#include <algorithm>
 #include <cfloat>
 #include <cuda_fp8.h>
 
@@ -39,6 +40,35 @@ __device__ __forceinline__ float block_sum_256(float v, float* red) {
   __syncthreads();
   float t = (l < 8) ? red[l] : 0.f;
   return warp_sum(t);
+}
+
+// block-wide max for blockDim.x == 256; result valid in thread 0
+__device__ __forceinline__ float block_max_256(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (l == 0) red[w] = v;
+  __syncthreads();
+  float t = (l < 8) ? red[l] : 0.f;
+  if (w == 0) {
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, o));
+  }
+  return t;
+}
+
+// Grid for the column-chunk x row-block e4m3 quantisation kernels:
+// x covers the 8-column chunks in blocks of 256, y the blocks of `rows_per`
+// rows.  When there are more row blocks than fit in one wave (8 CTAs of 256
+// threads per SM), every CTA loops over the same number of them, so the
+// launch is a single, evenly loaded wave.
+dim3 chunk_rows_grid(const LaunchCtx& c, int64_t c8, int64_t rows, int rows_per) {
+  const int64_t gx = (c8 + 255) / 256;
+  const int64_t row_blocks = std::max<int64_t>(1, (rows + rows_per - 1) / rows_per);
+  const int64_t cap_y = std::max<int64_t>(1, static_cast<int64_t>(c.num_sms) * 8 / gx);
+  const int64_t iters = (row_blocks + cap_y - 1) / cap_y;
+  const int64_t gy = std::min<int64_t>((row_blocks + iters - 1) / iters, 65535);
+  return dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy));
 }
 
 int grid_for(const LaunchCtx& c, int64_t work_items, int threads) {
@@ -311,63 +341,91 @@ __global__ void rope_apply_kernel(__nv_bfloat16* __restrict__ qkv, const float* 
   }
 }
 
-// per-tensor amax of src (* g[col] when g is given): block maxima combined
-// with atomicMax on the bit patterns (non-negative floats order as integers)
-__global__ void amax_kernel(const uint4* __restrict__ src, const uint4* __restrict__ g8, int64_t n8, int64_t c8,
-                            unsigned int* __restrict__ amax_bits) {
+// Per-tensor e4m3 quantisation, two passes over src [rows][cols] (times
+// g[col] when g is given): the absolute maximum, then the codes.  Like the
+// fold, a thread owns one 8-column chunk (its g values in registers) and
+// kQuantRows rows of it, with all row loads issued before use.  Block maxima
+// are combined with atomicMax on the bit patterns (non-negative floats order
+// as integers).
+constexpr int kQuantRows = 8;
+
+__global__ void __launch_bounds__(256) amax_kernel(const uint4* __restrict__ src, const uint4* __restrict__ g8,
+                                                   int64_t rows, int64_t c8, unsigned int* __restrict__ amax_bits) {
   griddep_wait();
   griddep_launch_dependents();
-  __shared__ float red[32];
+  __shared__ float red[8];
+  const int64_t j = blockIdx.x * 256LL + threadIdx.x;
   float mx = 0.f;
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n8;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    float v[8], gg[8];
-    unpack_bf16x8(src[i], v);
+  if (j < c8) {
+    float gg[8];
     if (g8 != nullptr) {
-      unpack_bf16x8(__ldg(&g8[i % c8]), gg);
+      unpack_bf16x8(__ldg(&g8[j]), gg);
+    } else {
 #pragma unroll
-      for (int k = 0; k < 8; ++k) v[k] *= gg[k];
+      for (int k = 0; k < 8; ++k) gg[k] = 1.f;
     }
+    for (int64_t r0 = blockIdx.y * static_cast<int64_t>(kQuantRows); r0 < rows;
+         r0 += static_cast<int64_t>(gridDim.y) * kQuantRows) {
+      const int nr = static_cast<int>(rows - r0 < kQuantRows ? rows - r0 : kQuantRows);
+      uint4 q[kQuantRows];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) mx = fmaxf(mx, fabsf(v[k]));
+      for (int r = 0; r < kQuantRows; ++r)
+        if (r < nr) q[r] = src[(r0 + r) * c8 + j];
+#pragma unroll
+      for (int r = 0; r < kQuantRows; ++r) {
+        if (r < nr) {
+          float v[8];
+          unpack_bf16x8(q[r], v);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) mx = fmaxf(mx, fabsf(v[k] * gg[k]));
+        }
+      }
+    }
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
-  __syncthreads();
-  if (threadIdx.x < 32) {
-    float t = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, o));
-    if (threadIdx.x == 0) atomicMax(amax_bits, __float_as_uint(t));
-  }
+  const float t = block_max_256(mx, red);
+  if (threadIdx.x == 0) atomicMax(amax_bits, __float_as_uint(t));
 }
 
 // dst = e4m3(src * g / scale), scale = amax / 448 (1 for an all-zero tensor);
 // saturating round-to-nearest-even conversion.  ws[1] receives the scale.
-__global__ void fp8_quantize_kernel(const uint4* __restrict__ src, const uint4* __restrict__ g8, int64_t n8,
-                                    int64_t c8, float* __restrict__ ws, uint2* __restrict__ dst) {
+__global__ void __launch_bounds__(256) fp8_quantize_kernel(const uint4* __restrict__ src,
+                                                           const uint4* __restrict__ g8, int64_t rows, int64_t c8,
+                                                           float* __restrict__ ws, uint2* __restrict__ dst) {
   griddep_wait();
   griddep_launch_dependents();
   const float amax = ws[0];
   const float scale = amax > 0.f ? amax / 448.0f : 1.0f;
-  if (blockIdx.x == 0 && threadIdx.x == 0) ws[1] = scale;
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n8;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    float v[8], gg[8];
-    unpack_bf16x8(src[i], v);
-    if (g8 != nullptr) {
-      unpack_bf16x8(__ldg(&g8[i % c8]), gg);
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) ws[1] = scale;
+  const int64_t j = blockIdx.x * 256LL + threadIdx.x;
+  if (j >= c8) return;
+  float gg[8];
+  if (g8 != nullptr) {
+    unpack_bf16x8(__ldg(&g8[j]), gg);
+  } else {
 #pragma unroll
-      for (int k = 0; k < 8; ++k) v[k] *= gg[k];
-    }
-    uint32_t w[2] = {0u, 0u};
+    for (int k = 0; k < 8; ++k) gg[k] = 1.f;
+  }
+  for (int64_t r0 = blockIdx.y * static_cast<int64_t>(kQuantRows); r0 < rows;
+       r0 += static_cast<int64_t>(gridDim.y) * kQuantRows) {
+    const int nr = static_cast<int>(rows - r0 < kQuantRows ? rows - r0 : kQuantRows);
+    uint4 q[kQuantRows];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const uint32_t b = __nv_cvt_float_to_fp8(v[k] / scale, __NV_SATFINITE, __NV_E4M3);
-      w[k >> 2] |= (b & 0xFFu) << (8 * (k & 3));
+    for (int r = 0; r < kQuantRows; ++r)
+      if (r < nr) q[r] = src[(r0 + r) * c8 + j];
+#pragma unroll
+    for (int r = 0; r < kQuantRows; ++r) {
+      if (r < nr) {
+        float v[8];
+        unpack_bf16x8(q[r], v);
+        uint32_t w[2] = {0u, 0u};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t b = __nv_cvt_float_to_fp8((v[k] * gg[k]) / scale, __NV_SATFINITE, __NV_E4M3);
+          w[k >> 2] |= (b & 0xFFu) << (8 * (k & 3));
+        }
+        dst[(r0 + r) * c8 + j] = make_uint2(w[0], w[1]);
+      }
     }
-    dst[i] = make_uint2(w[0], w[1]);
   }
 }
 
@@ -525,6 +583,9 @@ __global__ void rmsnorm_bwd_dg_kernel(const __nv_bfloat16* __restrict__ dN, cons
 cudaError_t launch_fold(const LaunchCtx& c, const __nv_bfloat16* W2t, const __nv_bfloat16* g, __nv_bfloat16* W2gt,
                         int64_t N2, int64_t d) {
   const int64_t d8 = d / 8;
+  // one CTA per block of kFoldRows rows (not a single balanced wave): the
+  // fold usually runs beside GEMM1, where only a few of its CTAs fit per SM,
+  // and there the finer grid measured faster
   const int64_t row_blocks = (N2 + kFoldRows - 1) / kFoldRows;
   const dim3 grid(static_cast<unsigned>((d8 + 255) / 256), static_cast<unsigned>(row_blocks < 65535 ? row_blocks : 65535));
   return launch_chained(c, fold_kernel, grid, dim3(256), 0, reinterpret_cast<const uint4*>(W2t),
@@ -582,15 +643,16 @@ cudaError_t launch_rope_apply(const LaunchCtx& c, __nv_bfloat16* qkv, const floa
 
 cudaError_t launch_fp8_quantize(const LaunchCtx& c, const __nv_bfloat16* src, int64_t rows, int64_t cols,
                                 const __nv_bfloat16* g, float* ws, uint8_t* dst) {
-  const int64_t n8 = rows * cols / 8;
+  const int64_t c8 = cols / 8;
   cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(float), c.stream);
   if (e != cudaSuccess) return e;
   const uint4* g8 = reinterpret_cast<const uint4*>(g);
-  e = launch_chained(c, amax_kernel, dim3(grid_for(c, n8, 256)), dim3(256), 0, reinterpret_cast<const uint4*>(src), g8,
-                     n8, cols / 8, reinterpret_cast<unsigned int*>(ws));
+  const dim3 grid = chunk_rows_grid(c, c8, rows, kQuantRows);
+  e = launch_chained(c, amax_kernel, grid, dim3(256), 0, reinterpret_cast<const uint4*>(src), g8, rows, c8,
+                     reinterpret_cast<unsigned int*>(ws));
   if (e != cudaSuccess) return e;
-  return launch_chained(c, fp8_quantize_kernel, dim3(grid_for(c, n8, 256)), dim3(256), 0,
-                        reinterpret_cast<const uint4*>(src), g8, n8, cols / 8, ws, reinterpret_cast<uint2*>(dst));
+  return launch_chained(c, fp8_quantize_kernel, grid, dim3(256), 0, reinterpret_cast<const uint4*>(src), g8, rows,
+                        c8, ws, reinterpret_cast<uint2*>(dst));
 }
 
 cudaError_t launch_add_rmsnorm(const LaunchCtx& c, const __nv_bfloat16* A, const __nv_bfloat16* R,
