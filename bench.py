@@ -563,6 +563,31 @@ def main():
 
     launches = sum(fs.kernels.values()) * args.steps
     extras = {}
+    if not args.no_extras:
+        # end to end through the public API with host buffers: every rank runs
+        # its replica between barriers, the slowest rank's time counts
+        ins = ("X", "R", "dY") if shape.backward else ("X", "R")
+        res = "dX" if shape.backward else "out"
+        host = {k: torch.empty_like(x[k], device="cpu").pin_memory() for k in ins}
+        for k in host:
+            host[k].copy_(x[k])
+        host[res] = torch.empty_like(getattr(b, res), device="cpu").pin_memory()
+        pipe = E2EPipeline(C, b, host)
+        pipe.run(3)
+        n_e2e = max(3, args.steps // 2)
+        barrier()
+        t0 = time.perf_counter()
+        pipe.run(n_e2e)
+        barrier()
+        e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3 / n_e2e, dist, "cuda")
+        h2d = sum(host[k].numel() * host[k].element_size() for k in ins)
+        d2h = host[res].numel() * host[res].element_size()
+        extras["e2e"] = {"value": aggregate_value(step_flops, e2e_ms, world), "unit": UNIT, "ms_per_step": e2e_ms,
+                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                         "timing": "host wall clock over the whole run, synchronize (and barrier) at both ends; "
+                                   "copies of step i+1 (H2D) and i (D2H) overlap step i's compute; per-rank "
+                                   "bytes, value summed over ranks"}
+        del host, pipe
     if not args.no_extras and rank == 0:
         # the same step with g broadcast in GEMM1's epilogue (no fold pass over
         # W2) and the combine inside GEMM2's epilogue, timed the same way
@@ -592,27 +617,6 @@ def main():
             extras["next_swiglu_bwd_in_down_proj_dgrad"] = bench_down_proj_swiglu_bwd(C, b, shape, args.steps,
                                                                                     args.warmup)
             torch.cuda.empty_cache()
-        # end to end through the public API with host buffers
-        ins = ("X", "R", "dY") if shape.backward else ("X", "R")
-        res = "dX" if shape.backward else "out"
-        host = {k: torch.empty_like(x[k], device="cpu").pin_memory() for k in ins}
-        for k in host:
-            host[k].copy_(x[k])
-        host[res] = torch.empty_like(getattr(b, res), device="cpu").pin_memory()
-        pipe = E2EPipeline(C, b, host)
-        pipe.run(3)
-        n_e2e = max(3, args.steps // 2)
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        pipe.run(n_e2e)
-        e2e_ms = (time.perf_counter() - t0) * 1e3 / n_e2e
-        h2d = sum(host[k].numel() * host[k].element_size() for k in ins)
-        d2h = host[res].numel() * host[res].element_size()
-        extras["e2e"] = {"value": step_flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e2e_ms,
-                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                         "timing": "host wall clock over the whole run, synchronize at both ends; copies of "
-                                   "step i+1 (H2D) and i (D2H) overlap step i's compute"}
-        del host, pipe
         extras["next_fp8_forward"] = bench_fp8_forward(C, b, shape, args.steps, args.warmup, peak)
         torch.cuda.empty_cache()
         del b, x, fs, calls
