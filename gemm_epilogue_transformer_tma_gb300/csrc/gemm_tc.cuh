@@ -25,9 +25,10 @@
 //                4 warps, each warp runs both halves in turn.  Block
 //                reductions along a row (partial RMS, CE statistics,
 //                SwiGLU-backward partials) are therefore per half tile
-//                (PART_COLS columns).  Memory-heavy epilogues use 8 warps for
-//                more loads in flight; the others use 4, which leaves the
-//                producer's and MMA issuer's sub-partitions less crowded.
+//                (PART_COLS columns).  All programs use 4 warps, which leaves
+//                the producer's and MMA issuer's sub-partitions less crowded
+//                (8 measured slower for GEMM2 and no faster for the
+//                SwiGLU-backward epilogue once stores went through TMA).
 // Two TMEM buffers let the epilogue of tile i overlap the mainloop of i+1.
 //
 // Operand layouts (row-major storage, element = bf16):
@@ -726,7 +727,7 @@ struct EpiDgradRms {
 // (a block reduction the RMSNorm backward later merges into c).  dY itself
 // never leaves the chip.
 struct EpiSwigluBwd {
-  static constexpr int kEpiWarps = 8;  // loads z and stores dP: more loads in flight
+  static constexpr int kEpiWarps = 4;
   static constexpr int kStoreSlots = 2;
   struct Params {
     CUtensorMap dPg;  // gate half of dP: [M][F] with the row pitch of dP
