@@ -494,6 +494,8 @@ def main():
                     help="GEMMs on one SM per tile instead of SM pairs")
     ap.add_argument("--tokens", type=int, default=0,
                     help="override the token count M (smaller cases for profiler captures)")
+    ap.add_argument("--leg", default="", choices=["", "lmhead"],
+                    help="run only this extra leg and print its JSON (profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -508,6 +510,11 @@ def main():
 
     if args.impl == "reference":
         return run_reference(args, shape)
+    if args.leg == "lmhead":
+        import gemm_epilogue_transformer_tma_gb300 as C
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        print(json.dumps({"lmhead_ce": bench_lmhead(C, args.steps, args.warmup)}), flush=True)
+        return
 
     torch.cuda.set_device(local)
     dist = None
