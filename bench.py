@@ -179,6 +179,7 @@ class FusedStep:
             ("dgrad1_wgrad1", lambda: C.coda_gemm_res_prms_bwd(b.dH, b.X, b.W1t, b.dX, b.dW1t, b.dH)),
         ]
         self.stages = fwd + (bwd if b.with_backward else [])
+        self.n_fwd = len(fwd)
         # library kernels each stage launches (the fold + GEMM1 stage launches two)
         self.kernels = {name: (2 if name == "gemm1_res_prms+fold" else 1) for name, _ in self.stages}
 
@@ -329,7 +330,8 @@ def bench_fp8_forward(C, b, shape, steps, warmup, peak_bf16):
         lambda: C.coda_fp8_quantize(b.H, Hq, sc[3]),
         lambda: C.coda_gemm_rowscale_swiglu_fp8(Hq, sc[3, 1:], W2q, sc[2, 1:], b.rstd, b.out, b.z),
     ]
-    bf16 = FusedStep(C, b).calls()[:4]
+    fs = FusedStep(C, b)
+    bf16 = fs.calls()[:fs.n_fwd]  # the bf16 forward stages
     n = max(3, steps)
     t_w, _ = time_steps(weights, n, warmup, stage_events=False)
     t_8, per8 = time_steps(fp8, n, warmup, stage_events=True)
@@ -494,7 +496,7 @@ def main():
                     help="GEMMs on one SM per tile instead of SM pairs")
     ap.add_argument("--tokens", type=int, default=0,
                     help="override the token count M (smaller cases for profiler captures)")
-    ap.add_argument("--leg", default="", choices=["", "lmhead"],
+    ap.add_argument("--leg", default="", choices=["", "lmhead", "fp8"],
                     help="run only this extra leg and print its JSON (profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -510,10 +512,17 @@ def main():
 
     if args.impl == "reference":
         return run_reference(args, shape)
-    if args.leg == "lmhead":
+    if args.leg:
         import gemm_epilogue_transformer_tma_gb300 as C
+        from gemm_epilogue_transformer_tma_gb300.path import BlockBuffers
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
-        print(json.dumps({"lmhead_ce": bench_lmhead(C, args.steps, args.warmup)}), flush=True)
+        if args.leg == "lmhead":
+            out = {"lmhead_ce": bench_lmhead(C, args.steps, args.warmup)}
+        else:
+            b = BlockBuffers(block_inputs(shape, seed=0, device="cuda"), backward=False)
+            out = {"next_fp8_forward": bench_fp8_forward(C, b, shape, args.steps, args.warmup,
+                                                         load_peaks()["bf16_tflops"])}
+        print(json.dumps(out), flush=True)
         return
 
     torch.cuda.set_device(local)
