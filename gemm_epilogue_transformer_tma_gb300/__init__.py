@@ -79,6 +79,8 @@ SIGNATURES = {
     "coda_gemm_qkv_rope": (_INT, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64, _P]),
     "coda_rope_apply": (_INT, [_P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _P]),
     "coda_fp8_quantize": (_INT, [_P, _P, _P, _P, _P, _I64, _I64, _P]),
+    "coda_fp8_quantize_e5m2": (_INT, [_P, _P, _P, _P, _P, _I64, _I64, _P]),
+    "coda_gemm_fp8": (_INT, [_P, _P, _INT, _INT, _P, _P, _INT, _INT, _P, _P, _I64, _I64, _I64, _P, _P, _P]),
     "coda_gemm_res_prms_fp8": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "coda_gemm_rowscale_swiglu_fp8": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _U32, _P]),
     "coda_lmhead_ce_workspace_bytes": (_SZ, [_I64, _I64, _I64, _INT]),
@@ -473,6 +475,34 @@ def coda_fp8_quantize(src, dst, amax_scale, g=None, stream=None):
     _check(load_library().coda_fp8_quantize(_h(src), _ptr(src, BF, "src"), _ptr(g, BF, "g"),
                                             _ptr(amax_scale, F32, "amax_scale"), _ptr(dst, U8, "dst"), rows, cols,
                                             _stream(stream)), "coda_fp8_quantize")
+
+
+def coda_fp8_quantize_e5m2(src, dst, amax_scale, g=None, stream=None):
+    """Per-tensor e5m2 quantisation (scale = amax / 57344), like coda_fp8_quantize."""
+    rows, cols = src.shape
+    _shape(dst, (rows, cols), "dst")
+    _shape(amax_scale, (2,), "amax_scale")
+    if g is not None:
+        _shape(g, (cols,), "g")
+    _check(load_library().coda_fp8_quantize_e5m2(_h(src), _ptr(src, BF, "src"), _ptr(g, BF, "g"),
+                                                 _ptr(amax_scale, F32, "amax_scale"), _ptr(dst, U8, "dst"), rows,
+                                                 cols, _stream(stream)), "coda_fp8_quantize_e5m2")
+
+
+E4M3, E5M2 = 0, 1
+
+
+def coda_gemm_fp8(A, a_mn_major: bool, a_format: int, sA, B, b_mn_major: bool, b_format: int, sB, C,
+                  M: int, N: int, K: int, row_scale=None, col_scale=None, stream=None):
+    """C[M,N] = row_scale * col_scale * sA * sB * A B on 8-bit codes (see include/coda.h)."""
+    _shape(A, (K, M) if a_mn_major else (M, K), "A")
+    _shape(B, (K, N) if b_mn_major else (N, K), "B")
+    _shape(C, (M, N), "C")
+    _check(load_library().coda_gemm_fp8(_h(C), _ptr(A, U8, "A"), int(a_mn_major), int(a_format),
+                                        _ptr(sA, F32, "sA"), _ptr(B, U8, "B"), int(b_mn_major), int(b_format),
+                                        _ptr(sB, F32, "sB"), _ptr(C, BF, "C"), M, N, K,
+                                        _ptr(row_scale, F32, "row_scale"), _ptr(col_scale, BF, "col_scale"),
+                                        _stream(stream)), "coda_gemm_fp8")
 
 
 def coda_gemm_res_prms_fp8(Xq, sX, W1q, sW1, R, H, psum, stream=None):

@@ -51,6 +51,7 @@ LaunchCtx ctx_of(coda_handle_t h, void* stream) {
   c.pair = h->pair;
   c.scale_a = nullptr;
   c.scale_b = nullptr;
+  c.f8_fmt = 0;
   return c;
 }
 
@@ -72,6 +73,7 @@ struct Check {
     return *this;
   }
   Check& opt_ptr(const void* p) { return p == nullptr ? *this : ptr(p); }
+  Check& opt_sptr(const void* p) { return p == nullptr ? *this : sptr(p); }
   // a pointer to fp32 scalars: natural (4-byte) alignment
   Check& sptr(const void* p) {
     if (st != CODA_OK) return *this;
@@ -569,8 +571,9 @@ coda_status_t coda_rope_apply(coda_handle_t h, void* qkv, const float* cos_t, co
 }
 
 // ---------------------------------------------------------------------------
-coda_status_t coda_fp8_quantize(coda_handle_t h, const void* src, const void* g, float* amax_scale, void* dst,
-                                int64_t rows, int64_t cols, void* stream) {
+namespace {
+coda_status_t fp8_quantize_impl(coda_handle_t h, const void* src, const void* g, float* amax_scale, void* dst,
+                                int64_t rows, int64_t cols, void* stream, int e5m2) {
   CODA_TRY(Check().handle(h).rows(rows).mptr(src, rows).opt_ptr(g).sptr(amax_scale).mptr(dst, rows).cols(cols).st);
   if (cols % 16 != 0) return CODA_ERR_ALIGNMENT;
   if (rows == 0) {
@@ -579,7 +582,47 @@ coda_status_t coda_fp8_quantize(coda_handle_t h, const void* src, const void* g,
                                      static_cast<cudaStream_t>(stream)));
   }
   return from_cuda(launch_fp8_quantize(ctx_of(h, stream), static_cast<const bf16*>(src), rows, cols,
-                                       static_cast<const bf16*>(g), amax_scale, static_cast<uint8_t*>(dst)));
+                                       static_cast<const bf16*>(g), amax_scale, static_cast<uint8_t*>(dst), e5m2));
+}
+}  // namespace
+
+coda_status_t coda_fp8_quantize(coda_handle_t h, const void* src, const void* g, float* amax_scale, void* dst,
+                                int64_t rows, int64_t cols, void* stream) {
+  return fp8_quantize_impl(h, src, g, amax_scale, dst, rows, cols, stream, 0);
+}
+
+coda_status_t coda_fp8_quantize_e5m2(coda_handle_t h, const void* src, const void* g, float* amax_scale, void* dst,
+                                     int64_t rows, int64_t cols, void* stream) {
+  return fp8_quantize_impl(h, src, g, amax_scale, dst, rows, cols, stream, 1);
+}
+
+coda_status_t coda_gemm_fp8(coda_handle_t h, const void* A, int a_mn_major, int a_format, const float* sA,
+                            const void* B, int b_mn_major, int b_format, const float* sB, void* C, int64_t M,
+                            int64_t N, int64_t K, const float* row_scale, const void* col_scale, void* stream) {
+  CODA_TRY(Check()
+               .handle(h)
+               .rows(M)
+               .mptr(A, M)
+               .opt_sptr(sA)
+               .ptr(B)
+               .opt_sptr(sB)
+               .mptr(C, M)
+               .opt_ptr(row_scale)
+               .opt_ptr(col_scale)
+               .cols(N)
+               .cols(K)
+               .st);
+  if ((a_format != 0 && a_format != 1) || (b_format != 0 && b_format != 1)) return CODA_ERR_INVALID_ARG;
+  if (a_mn_major && !b_mn_major) return CODA_ERR_UNSUPPORTED;
+  // rows of 8-bit operands: 16-byte multiples along the contiguous extent
+  if ((!a_mn_major || !b_mn_major) && K % 16 != 0) return CODA_ERR_ALIGNMENT;
+  if (a_mn_major && M % 16 != 0) return CODA_ERR_ALIGNMENT;
+  if (b_mn_major && N % 16 != 0) return CODA_ERR_ALIGNMENT;
+  if (M == 0) return CODA_OK;
+  return from_cuda(gemm_store_fp8(ctx_of(h, stream), static_cast<const uint8_t*>(A), a_mn_major != 0, a_format, sA,
+                                  static_cast<const uint8_t*>(B), b_mn_major != 0, b_format, sB,
+                                  static_cast<bf16*>(C), int(M), int(N), int(K), row_scale,
+                                  static_cast<const bf16*>(col_scale)));
 }
 
 coda_status_t coda_gemm_res_prms_fp8(coda_handle_t h, const void* Xq, const float* sX, const void* W1q,

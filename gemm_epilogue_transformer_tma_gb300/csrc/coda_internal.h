@@ -19,6 +19,7 @@ struct LaunchCtx {
   int pair;              // 1: 2-SM GEMM kernel (CTA pairs), 0: 1-SM kernel
   const float* scale_a;  // FP8 operands: device pointers to the per-tensor scales
   const float* scale_b;
+  uint32_t f8_fmt;       // FP8 operands: format bits of A and B (f8_format_bits; 0 = both e4m3)
 };
 
 // 2-D bf16 tensor map with 128-byte swizzle.  The tensor is `outer` rows of
@@ -139,6 +140,13 @@ cudaError_t gemm_group_ce_bwd(const LaunchCtx& c, const __nv_bfloat16* dL, const
 // Host check of the grouped tile schedule (0 = every tile visited once).
 int group_schedule_violations(int P, int heavy, int nH, int nL, int q);
 
+// C = bf16(row_scale * col_scale * sA * sB * A B) on 8-bit operands: A
+// [M][K] (K-major) or [K][M] (MN-major), B [N][K] or [K][N]; formats 0 =
+// e4m3, 1 = e5m2; sA / sB device pointers to the scales (null = 1).
+cudaError_t gemm_store_fp8(const LaunchCtx& c, const uint8_t* A, bool a_mn, int a_fmt, const float* sA,
+                           const uint8_t* B, bool b_mn, int b_fmt, const float* sB, __nv_bfloat16* C, int M, int N,
+                           int K, const float* row_scale, const __nv_bfloat16* col_scale);
+
 int ce_tile_cols();    // vocabulary columns per CE statistics tile
 int prms_tile_cols();  // columns per partial-RMS tile of GEMM1
 
@@ -160,10 +168,11 @@ cudaError_t launch_rope_table(const LaunchCtx& c, float* cos_t, float* sin_t, in
 // RoPE in place on the first rot_cols columns of qkv [M, N] (standalone, unfused)
 cudaError_t launch_rope_apply(const LaunchCtx& c, __nv_bfloat16* qkv, const float* cos_t, const float* sin_t,
                               int64_t M, int64_t N, int64_t rot_cols, int64_t head_dim, int64_t S);
-// per-tensor e4m3 quantisation: ws[0] = amax of src (times g[col] if g),
-// ws[1] = scale = amax / 448 (1 if amax == 0); dst = e4m3(src * g / scale)
+// per-tensor fp8 quantisation: ws[0] = amax of src (times g[col] if g),
+// ws[1] = scale = amax / fmax (1 if amax == 0); dst = fp8(src * g / scale),
+// e4m3 (fmax 448) or, with e5m2 != 0, e5m2 (fmax 57344)
 cudaError_t launch_fp8_quantize(const LaunchCtx& c, const __nv_bfloat16* src, int64_t rows, int64_t cols,
-                                const __nv_bfloat16* g, float* ws, uint8_t* dst);
+                                const __nv_bfloat16* g, float* ws, uint8_t* dst, int e5m2 = 0);
 // unfused ablation kernels
 cudaError_t launch_add_rmsnorm(const LaunchCtx& c, const __nv_bfloat16* A, const __nv_bfloat16* R,
                                const __nv_bfloat16* g, __nv_bfloat16* H, float* rstd, __nv_bfloat16* Nrm, int64_t M,

@@ -1,7 +1,8 @@
-// FP8 (e4m3, per-tensor scaled) forms of the forward GEMMs with the same
+// FP8 (per-tensor scaled e4m3 / e5m2) forms of the GEMMs with the same
 // epilogue programs: GEMM1 + residual + partial RMS, GEMM2 + row scale +
-// SwiGLU.  kind::f8f6f4 MMAs, 128 e4m3 elements (128 bytes) per k-block row;
-// the product of the two operands' scales is applied in the epilogue.
+// SwiGLU, and the plain store used by the backward.  kind::f8f6f4 MMAs, 128
+// 8-bit elements (128 bytes) per k-block row; the product of the two
+// operands' scales is applied in the epilogue.
 #include "gemm_launch.cuh"
 
 namespace coda {
@@ -61,6 +62,34 @@ cudaError_t gemm_rowscale_swiglu_fp8(const LaunchCtx& c0, const uint8_t* Hq, con
   ep.F = F;
   return run_gemm<false, false, true, EpiRowscaleSwiglu, true>(c, ta, tb, tb2, M, F, d,
                                                                (F + kBN / 2 - 1) / (kBN / 2), ep);
+}
+
+// Tensor map of an 8-bit operand: K-major [rows][K] with boxes of 128 K x
+// box_rows, or MN-major [K][mn] with boxes of 128 (M/N) x 128 (K).
+bool make_f8_operand_map(CUtensorMap* m, const uint8_t* p, bool mn_major, int mn, int K, int box_rows) {
+  if (!mn_major) return make_tmap_u8(m, p, K, mn, K, 128, box_rows);
+  return make_tmap_u8(m, p, mn, K, mn, 128, 128);
+}
+
+cudaError_t gemm_store_fp8(const LaunchCtx& c0, const uint8_t* A, bool a_mn, int a_fmt, const float* sA,
+                           const uint8_t* B, bool b_mn, int b_fmt, const float* sB, __nv_bfloat16* C, int M, int N,
+                           int K, const float* row_scale, const __nv_bfloat16* col_scale) {
+  LaunchCtx c = c0;
+  c.scale_a = sA;
+  c.scale_b = sB;
+  c.f8_fmt = f8_format_bits(a_fmt, b_fmt);
+  CUtensorMap ta, tb;
+  if (!make_f8_operand_map(&ta, A, a_mn, M, K, BM)) return cudaErrorInvalidValue;
+  if (!make_f8_operand_map(&tb, B, b_mn, N, K, b_box_rows(c))) return cudaErrorInvalidValue;
+  EpiStore::Params ep{};
+  if (!make_tmap_store_bf16(&ep.out, C, N, M, N)) return cudaErrorInvalidValue;
+  ep.row_scale = row_scale;
+  ep.col_scale = col_scale;
+  const int tn = (N + kBN - 1) / kBN;
+  if (!a_mn && !b_mn) return run_gemm<false, false, false, EpiStore, true>(c, ta, tb, tb, M, N, K, tn, ep);
+  if (!a_mn && b_mn) return run_gemm<false, true, false, EpiStore, true>(c, ta, tb, tb, M, N, K, tn, ep);
+  if (a_mn && b_mn) return run_gemm<true, true, false, EpiStore, true>(c, ta, tb, tb, M, N, K, tn, ep);
+  return cudaErrorNotSupported;  // MN-major A with K-major B is not used on this path
 }
 
 }  // namespace coda

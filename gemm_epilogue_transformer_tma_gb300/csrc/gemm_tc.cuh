@@ -68,6 +68,7 @@ struct KernelCtl {
   int skip_first_stage;  // test hook: CTA 0's producer never fills its first stage
   const float* scale_a;  // FP8 operands: per-tensor dequantisation scales (null = 1)
   const float* scale_b;
+  uint32_t f8_fmt;       // FP8 operands: format bits of A and B (f8_format_bits)
 };
 
 // The accumulator's scale: the product of the operands' per-tensor scales
@@ -140,9 +141,13 @@ __global__ void __launch_bounds__(gemm_threads<Epi>(), 1)
   using L = GemmSmem<BN, STAGES, epi_stage_bytes<Epi>()>;
   static_assert(!(B_DUAL && B_MN), "dual-box B is K-major only");
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
-  static_assert(!FP8 || (!A_MN && !B_MN), "FP8 operands are K-major");
-  constexpr uint32_t IDESC = FP8 ? idesc_e4m3_f32(BM, BN) : idesc_bf16_f32(BM, BN, A_MN, B_MN);
-  constexpr int BKE = FP8 ? 128 : BK;  // elements per 128-byte k-block row
+  constexpr uint32_t IDESC0 = FP8 ? idesc_f8_f32(BM, BN, A_MN, B_MN) : idesc_bf16_f32(BM, BN, A_MN, B_MN);
+  constexpr int BKE = FP8 ? 128 : BK;         // K elements per 128-byte k-block row (K-major operands)
+  // MN-major operands: boxes of 128 bytes along M/N (64 bf16 or 128 e4m3) by
+  // BKE rows of K; one MMA's K slice is 16 (bf16) or 32 (8-bit) such rows
+  constexpr int MNB = FP8 ? 128 : 64;         // M/N elements per MN-major box
+  constexpr int MN_BOX = 128 * BKE;           // bytes per MN-major box
+  constexpr int MN_KSTEP = FP8 ? 4096 : 2048; // bytes per MMA K slice, MN-major
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -186,6 +191,7 @@ __global__ void __launch_bounds__(gemm_threads<Epi>(), 1)
   griddep_launch_dependents();
   griddep_wait();
   const float acc_scale = acc_scale_of(ctl);
+  const uint32_t idesc = FP8 ? (IDESC0 | ctl.f8_fmt) : IDESC0;
 
   const int num_tiles = sh.tiles_m * sh.tiles_n;
 
@@ -218,7 +224,8 @@ __global__ void __launch_bounds__(gemm_threads<Epi>(), 1)
               tma_load_2d(sa, &tmA, &full[stage], kb * BKE, tm * BM);
             } else {
 #pragma unroll
-              for (int i = 0; i < BM / 64; ++i) tma_load_2d(sa + i * 8192, &tmA, &full[stage], tm * BM + i * 64, kb * BK);
+              for (int i = 0; i < BM / MNB; ++i)
+                tma_load_2d(sa + i * MN_BOX, &tmA, &full[stage], tm * BM + i * MNB, kb * BKE);
             }
             if (B_DUAL) {
               tma_load_2d(sb, &tmB, &full[stage], kb * BKE, tn * (BN / 2));
@@ -227,7 +234,8 @@ __global__ void __launch_bounds__(gemm_threads<Epi>(), 1)
               tma_load_2d(sb, &tmB, &full[stage], kb * BKE, tn * BN);
             } else {
 #pragma unroll
-              for (int i = 0; i < BN / 64; ++i) tma_load_2d(sb + i * 8192, &tmB, &full[stage], tn * BN + i * 64, kb * BK);
+              for (int i = 0; i < BN / MNB; ++i)
+                tma_load_2d(sb + i * MN_BOX, &tmB, &full[stage], tn * BN + i * MNB, kb * BKE);
             }
             pending |= 1u << stage;
             parity = (parity & ~(1u << stage)) | (phase << stage);
@@ -274,12 +282,14 @@ __global__ void __launch_bounds__(gemm_threads<Epi>(), 1)
           const uint32_t sb = sa + L::A_BYTES;
 #pragma unroll
           for (int k = 0; k < BK / UMMA_K; ++k) {
-            const uint64_t ad = A_MN ? sdesc_sw128(sa + k * 2048, 8192, 1024) : sdesc_sw128(sa + k * 32, 16, 1024);
-            const uint64_t bd = B_MN ? sdesc_sw128(sb + k * 2048, 8192, 1024) : sdesc_sw128(sb + k * 32, 16, 1024);
+            const uint64_t ad =
+                A_MN ? sdesc_sw128(sa + k * MN_KSTEP, MN_BOX, 1024) : sdesc_sw128(sa + k * 32, 16, 1024);
+            const uint64_t bd =
+                B_MN ? sdesc_sw128(sb + k * MN_KSTEP, MN_BOX, 1024) : sdesc_sw128(sb + k * 32, 16, 1024);
             if (FP8)
-              umma_e4m3(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
+              umma_e4m3(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
             else
-              umma_bf16(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
+              umma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
           }
           umma_commit(&empty[stage]);
           if (++stage == STAGES) {

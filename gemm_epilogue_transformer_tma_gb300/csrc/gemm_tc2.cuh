@@ -55,10 +55,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi>(),
   using L = Gemm2Smem<BN, STAGES, epi_stage_bytes<Epi>()>;
   static_assert(!(B_DUAL && B_MN), "dual-box B is K-major only");
   static_assert(BN == 256, "the pair kernel is instantiated for 256-column tiles");
-  static_assert(!FP8 || (!A_MN && !B_MN), "FP8 operands are K-major");
   constexpr int HB = BN / 2;  // B rows held by one CTA
-  constexpr uint32_t IDESC = FP8 ? idesc_e4m3_f32(BM2, BN) : idesc_bf16_f32(BM2, BN, A_MN, B_MN);
-  constexpr int BKE = FP8 ? 128 : BK;  // elements per 128-byte k-block row
+  constexpr uint32_t IDESC0 = FP8 ? idesc_f8_f32(BM2, BN, A_MN, B_MN) : idesc_bf16_f32(BM2, BN, A_MN, B_MN);
+  constexpr int BKE = FP8 ? 128 : BK;         // K elements per 128-byte k-block row (K-major operands)
+  // MN-major operands: boxes of 128 bytes along M/N (64 bf16 or 128 e4m3) by
+  // BKE rows of K; one MMA's K slice is 16 (bf16) or 32 (8-bit) such rows
+  constexpr int MNB = FP8 ? 128 : 64;         // M/N elements per MN-major box
+  constexpr int MN_BOX = 128 * BKE;           // bytes per MN-major box
+  constexpr int MN_KSTEP = FP8 ? 4096 : 2048; // bytes per MMA K slice, MN-major
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -108,6 +112,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi>(),
   griddep_launch_dependents();
   griddep_wait();
   const float acc_scale = acc_scale_of(ctl);
+  const uint32_t idesc = FP8 ? (IDESC0 | ctl.f8_fmt) : IDESC0;
 
   const int num_tiles = sh.tiles_m * sh.tiles_n;
 
@@ -144,8 +149,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi>(),
             if (!A_MN) {
               tma_load_2d_pair(sa, &tmA, bar, kb * BKE, m0);
             } else {
-              tma_load_2d_pair(sa, &tmA, bar, m0, kb * BK);
-              tma_load_2d_pair(sa + 8192, &tmA, bar, m0 + 64, kb * BK);
+#pragma unroll
+              for (int i = 0; i < 128 / MNB; ++i) tma_load_2d_pair(sa + i * MN_BOX, &tmA, bar, m0 + i * MNB, kb * BKE);
             }
             if (B_DUAL) {
               // leader: gate rows of the tile, peer: the matching up rows
@@ -154,8 +159,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi>(),
               tma_load_2d_pair(sb, &tmB, bar, kb * BKE, tn * BN + static_cast<int>(rank) * HB);
             } else {
 #pragma unroll
-              for (int i = 0; i < HB / 64; ++i)
-                tma_load_2d_pair(sb + i * 8192, &tmB, bar, tn * BN + static_cast<int>(rank) * HB + i * 64, kb * BK);
+              for (int i = 0; i < HB / MNB; ++i)
+                tma_load_2d_pair(sb + i * MN_BOX, &tmB, bar, tn * BN + static_cast<int>(rank) * HB + i * MNB, kb * BKE);
             }
           }
           if (++stage == STAGES) {
@@ -209,12 +214,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi>(),
             const uint32_t sb = sa + L::A_BYTES;
 #pragma unroll
             for (int k = 0; k < BK / UMMA_K; ++k) {
-              const uint64_t ad = A_MN ? sdesc_sw128(sa + k * 2048, 8192, 1024) : sdesc_sw128(sa + k * 32, 16, 1024);
-              const uint64_t bd = B_MN ? sdesc_sw128(sb + k * 2048, 8192, 1024) : sdesc_sw128(sb + k * 32, 16, 1024);
+              const uint64_t ad =
+                  A_MN ? sdesc_sw128(sa + k * MN_KSTEP, MN_BOX, 1024) : sdesc_sw128(sa + k * 32, 16, 1024);
+              const uint64_t bd =
+                  B_MN ? sdesc_sw128(sb + k * MN_KSTEP, MN_BOX, 1024) : sdesc_sw128(sb + k * 32, 16, 1024);
               if (FP8)
-                umma_e4m3_pair(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
+                umma_e4m3_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
               else
-                umma_bf16_pair(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
+                umma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
             }
             issued_any = true;
             umma_commit_pair_multicast(&empty[stage], 0x3);

@@ -386,15 +386,18 @@ __global__ void __launch_bounds__(256) amax_kernel(const uint4* __restrict__ src
   if (threadIdx.x == 0) atomicMax(amax_bits, __float_as_uint(t));
 }
 
-// dst = e4m3(src * g / scale), scale = amax / 448 (1 for an all-zero tensor);
-// saturating round-to-nearest-even conversion.  ws[1] receives the scale.
+// dst = fp8(src * g / scale), scale = amax / fmax (1 for an all-zero
+// tensor), fp8 = e4m3 (fmax 448) or e5m2 (fmax 57344); saturating
+// round-to-nearest-even conversion.  ws[1] receives the scale.
 __global__ void __launch_bounds__(256) fp8_quantize_kernel(const uint4* __restrict__ src,
                                                            const uint4* __restrict__ g8, int64_t rows, int64_t c8,
-                                                           float* __restrict__ ws, uint2* __restrict__ dst) {
+                                                           int e5m2, float* __restrict__ ws,
+                                                           uint2* __restrict__ dst) {
   griddep_wait();
   griddep_launch_dependents();
   const float amax = ws[0];
-  const float scale = amax > 0.f ? amax / 448.0f : 1.0f;
+  const float scale = amax > 0.f ? amax / (e5m2 ? 57344.0f : 448.0f) : 1.0f;
+  const __nv_fp8_interpretation_t kind = e5m2 ? __NV_E5M2 : __NV_E4M3;
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) ws[1] = scale;
   const int64_t j = blockIdx.x * 256LL + threadIdx.x;
   if (j >= c8) return;
@@ -420,7 +423,7 @@ __global__ void __launch_bounds__(256) fp8_quantize_kernel(const uint4* __restri
         uint32_t w[2] = {0u, 0u};
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          const uint32_t b = __nv_cvt_float_to_fp8((v[k] * gg[k]) / scale, __NV_SATFINITE, __NV_E4M3);
+          const uint32_t b = __nv_cvt_float_to_fp8((v[k] * gg[k]) / scale, __NV_SATFINITE, kind);
           w[k >> 2] |= (b & 0xFFu) << (8 * (k & 3));
         }
         dst[(r0 + r) * c8 + j] = make_uint2(w[0], w[1]);
@@ -642,7 +645,7 @@ cudaError_t launch_rope_apply(const LaunchCtx& c, __nv_bfloat16* qkv, const floa
 }
 
 cudaError_t launch_fp8_quantize(const LaunchCtx& c, const __nv_bfloat16* src, int64_t rows, int64_t cols,
-                                const __nv_bfloat16* g, float* ws, uint8_t* dst) {
+                                const __nv_bfloat16* g, float* ws, uint8_t* dst, int e5m2) {
   const int64_t c8 = cols / 8;
   cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(float), c.stream);
   if (e != cudaSuccess) return e;
@@ -652,7 +655,7 @@ cudaError_t launch_fp8_quantize(const LaunchCtx& c, const __nv_bfloat16* src, in
                      reinterpret_cast<unsigned int*>(ws));
   if (e != cudaSuccess) return e;
   return launch_chained(c, fp8_quantize_kernel, grid, dim3(256), 0, reinterpret_cast<const uint4*>(src), g8, rows,
-                        c8, ws, reinterpret_cast<uint2*>(dst));
+                        c8, e5m2, ws, reinterpret_cast<uint2*>(dst));
 }
 
 cudaError_t launch_add_rmsnorm(const LaunchCtx& c, const __nv_bfloat16* A, const __nv_bfloat16* R,

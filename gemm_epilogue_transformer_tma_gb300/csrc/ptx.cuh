@@ -380,10 +380,17 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_ma
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-// Instruction descriptor for tcgen05.mma kind::f8f6f4 with e4m3 A/B (format
-// code 0) and fp32 D; both operands K-major.
-__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
-  return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+// Instruction descriptor for tcgen05.mma kind::f8f6f4 with fp32 D and 8-bit
+// A/B; the operand formats (bits 7-9 for A, 10-12 for B: 0 = e4m3,
+// 1 = e5m2) are OR-ed in at run time (f8_format_bits).
+__host__ __device__ constexpr uint32_t idesc_f8_f32(int M, int N, bool a_mn_major, bool b_mn_major) {
+  return (1u << 4) | (static_cast<uint32_t>(a_mn_major) << 15) | (static_cast<uint32_t>(b_mn_major) << 16) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Format bits of an 8-bit A and B for idesc_f8_f32 (0 = e4m3, 1 = e5m2).
+__host__ __device__ constexpr uint32_t f8_format_bits(int a_fmt, int b_fmt) {
+  return (static_cast<uint32_t>(a_fmt & 7) << 7) | (static_cast<uint32_t>(b_fmt & 7) << 10);
 }
 
 // ---------------------------------------------------------------------------

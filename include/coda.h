@@ -355,6 +355,24 @@ coda_status_t coda_rope_apply(coda_handle_t h, void* qkv, const float* cos_t, co
 coda_status_t coda_fp8_quantize(coda_handle_t h, const void* src, const void* g, float* amax_scale, void* dst,
                                 int64_t rows, int64_t cols, void* stream);
 
+/* The same quantisation to e5m2 (5 exponent, 2 mantissa bits): scale =
+ * amax / 57344, dst = e5m2( src * g / scale ), saturating at +-57344.  The
+ * wider range suits gradients. */
+coda_status_t coda_fp8_quantize_e5m2(coda_handle_t h, const void* src, const void* g, float* amax_scale, void* dst,
+                                     int64_t rows, int64_t cols, void* stream);
+
+/* Plain GEMM on 8-bit operands (the mainloop of the method with FP8 inputs):
+ *   C[m][n] = bf16( row_scale[m] * col_scale[n] * sA * sB * sum_k A[m][k] B[k][n] )
+ * A codes [M][K] (a_mn_major = 0) or [K][M] (1); B codes [N][K] (0) or [K][N]
+ * (1); a_format / b_format 0 = e4m3, 1 = e5m2 (mixed allowed); sA, sB device
+ * pointers to fp32 scales or NULL (1); row_scale fp32 [M], col_scale bf16 [N],
+ * both optional; C bf16 [M][N].  The contiguous extent of every 8-bit operand
+ * (K for K-major, M or N for MN-major) a multiple of 16, N a multiple of 8.
+ * MN-major A with K-major B returns CODA_ERR_UNSUPPORTED. */
+coda_status_t coda_gemm_fp8(coda_handle_t h, const void* A, int a_mn_major, int a_format, const float* sA,
+                            const void* B, int b_mn_major, int b_format, const float* sB, void* C, int64_t M,
+                            int64_t N, int64_t K, const float* row_scale, const void* col_scale, void* stream);
+
 /* coda_gemm_res_prms on e4m3 operands: H = bf16( sX * sW1 * sum_k Xq[m][k]
  * W1q[n][k] + R ), psum as before.  Xq codes [M][K1], W1q codes [d][K1], sX /
  * sW1 device pointers to the tensors' scales (amax_scale + 1 of

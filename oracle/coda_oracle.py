@@ -24,7 +24,7 @@ __all__ = [
     "lse_rows", "lse_tile_partials", "lse_combine", "ce_forward",
     "ce_backward", "argmax_lowest", "ce_weight_grad_given_lse", "down_proj_dgrad",
     "swiglu_c_partials", "rope_angles", "rope_rotate_half", "qkv_rope", "e4m3_round", "e4m3_encode",
-    "e4m3_decode", "fp8_scale", "fp8_quantize",
+    "e4m3_decode", "e5m2_round", "e5m2_encode", "e5m2_decode", "fp8_scale", "fp8_quantize", "fp8_decode",
 ]
 
 
@@ -436,15 +436,69 @@ def e4m3_decode(b):
     return sign * val
 
 
-def fp8_scale(x):
+E5M2_MAX = 57344.0
+
+
+def e5m2_round(x):
+    """Round to the nearest e5m2 value (sign, 5 exponent bits with bias 15, 2
+    mantissa bits), ties to even, saturating at +-57344.  Normal exponents
+    -14..15; below 2^-14 the subnormal quantum is 2^-16."""
+    x = np.asarray(x, np.float64)
+    a = np.abs(x)
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    e = np.clip(e, -14, 15)
+    quantum = np.exp2(e - 2)
+    q = np.round(a / quantum) * quantum         # np.round: half to even
+    q = np.minimum(q, E5M2_MAX)
+    return np.where(a > 0, np.sign(x) * q, 0.0 * x)
+
+
+def e5m2_encode(v):
+    """Byte encoding of e5m2 values (exactly representable, |v| <= 57344)."""
+    v = np.asarray(v, np.float64)
+    sign = (np.signbit(v)).astype(np.uint8) << 7
+    a = np.abs(v)
+    out = np.zeros(a.shape, np.uint8)
+    sub = (a > 0) & (a < 2.0 ** -14)
+    out[sub] = (a[sub] / 2.0 ** -16).astype(np.uint8)
+    nrm = a >= 2.0 ** -14
+    e = np.floor(np.log2(a[nrm]))
+    man = a[nrm] / np.exp2(e) - 1.0
+    out[nrm] = ((e + 15).astype(np.uint8) << 2) | np.round(man * 4).astype(np.uint8)
+    return out | sign
+
+
+def e5m2_decode(b):
+    """Value of e5m2 byte codes with a finite value (exponent field < 31; the
+    inf / NaN codes are not produced by a saturating conversion)."""
+    b = np.asarray(b, np.uint8).astype(np.int64)
+    sign = np.where(b & 0x80, -1.0, 1.0)
+    e = (b >> 2) & 0x1F
+    m = b & 0x3
+    val = np.where(e == 0, m * 2.0 ** -16, (1.0 + m / 4.0) * np.exp2(e - 15.0))
+    return sign * val
+
+
+FP8_FORMATS = {"e4m3": (E4M3_MAX, e4m3_round, e4m3_encode, e4m3_decode),
+               "e5m2": (E5M2_MAX, e5m2_round, e5m2_encode, e5m2_decode)}
+
+
+def fp8_scale(x, fmt="e4m3"):
     """Per-tensor scale that maps the tensor's largest magnitude onto the
-    top of the e4m3 range: amax / 448 (1 for an all-zero tensor), in fp32."""
+    top of the format's range: amax / 448 (e4m3) or amax / 57344 (e5m2), 1
+    for an all-zero tensor, in fp32."""
     amax = np.float32(np.max(np.abs(np.asarray(x, np.float32)))) if np.size(x) else np.float32(0)
-    return np.float32(amax / np.float32(E4M3_MAX)) if amax > 0 else np.float32(1.0)
+    return np.float32(amax / np.float32(FP8_FORMATS[fmt][0])) if amax > 0 else np.float32(1.0)
 
 
-def fp8_quantize(x, scale):
-    """Codes of x / scale rounded to e4m3; the division is done in fp32, the
-    precision the conversion sees."""
+def fp8_quantize(x, scale, fmt="e4m3"):
+    """Codes of x / scale rounded to the format; the division is done in
+    fp32, the precision the conversion sees."""
+    _, rnd, enc, _ = FP8_FORMATS[fmt]
     q = np.asarray(x, np.float32) / np.float32(scale)
-    return e4m3_encode(e4m3_round(q.astype(np.float64)))
+    return enc(rnd(q.astype(np.float64)))
+
+
+def fp8_decode(b, fmt="e4m3"):
+    """Values of fp8 byte codes in the given format."""
+    return FP8_FORMATS[fmt][3](b)

@@ -6,7 +6,9 @@ even.  The library's output must match bit for bit, for:
   * both kernel forms (SM pairs, one SM per tile);
   * power-of-two row / column scales (exact in fp32);
   * the grouped launch of the first layer's data and weight gradients;
-  * e4m3 operands with unit scales.
+  * e4m3 operands with unit scales;
+  * the generic 8-bit GEMM for every layout and every pair of formats
+    (e4m3 / e5m2), with power-of-two operand scales.
 Ragged sizes span several tiles in every dimension.
 
 Method: "CODA: Rewriting Transformer Blocks as GEMM-Epilogue Programs"
@@ -101,3 +103,24 @@ def test_fp8_operands_bit_exact(pairing):
     torch.cuda.synchronize()
     assert_device_ok()
     assert torch.equal(out.cpu(), exact_bf16(A, Bt))
+
+
+ENC = {0: O.e4m3_encode, 1: O.e5m2_encode}
+
+
+@pytest.mark.parametrize("a_mn,b_mn", [(False, False), (False, True), (True, True)])
+@pytest.mark.parametrize("a_fmt,b_fmt", [(0, 0), (1, 0), (0, 1), (1, 1)], ids=["e4e4", "e5e4", "e4e5", "e5e5"])
+def test_fp8_gemm_layouts_and_formats_bit_exact(a_mn, b_mn, a_fmt, b_fmt, pairing):
+    M, N, K = 528, 784, 1024       # ragged tiles in M and N, 8 k-blocks of 128
+    A = ints((M, K), -4, 4, 12)
+    Bt = ints((N, K), -4, 4, 13)
+    Aq = ENC[a_fmt]((A.T if a_mn else A).numpy().astype(np.float64))
+    Bq = ENC[b_fmt]((Bt.T if b_mn else Bt).numpy().astype(np.float64))
+    sA = torch.tensor([0.5], device="cuda")
+    sB = torch.tensor([4.0], device="cuda")
+    Cd = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    C.coda_gemm_fp8(torch.from_numpy(np.ascontiguousarray(Aq)).cuda(), a_mn, a_fmt, sA,
+                    torch.from_numpy(np.ascontiguousarray(Bq)).cuda(), b_mn, b_fmt, sB, Cd, M, N, K)
+    torch.cuda.synchronize()
+    assert_device_ok()
+    assert torch.equal(Cd.cpu(), exact_bf16(A, Bt, torch.full((M,), 2.0)))   # sA * sB = 2

@@ -65,6 +65,20 @@ def test_quantize_with_folded_weight_bit_exact():
     assert np.array_equal(q.cpu().numpy(), O.fp8_quantize(v, sc))
 
 
+@pytest.mark.parametrize("shape,scale", [((300, 528), 1.0), ((64, 4096), 1e-4), ((8, 16), 30.0)])
+def test_quantize_e5m2_codes_bit_exact(shape, scale):
+    g = torch.Generator().manual_seed(shape[0] + 1)
+    x = (torch.randn(*shape, generator=g) * scale).to(torch.bfloat16)
+    q = torch.empty(shape, dtype=torch.uint8, device="cuda")
+    s = torch.empty(2, device="cuda")
+    C.coda_fp8_quantize_e5m2(x.cuda(), q, s)
+    assert_device_ok()
+    xf = x.float().numpy()
+    sc = O.fp8_scale(xf, "e5m2")
+    assert np.float32(s[1].item()) == sc
+    assert np.array_equal(q.cpu().numpy(), O.fp8_quantize(xf, sc, "e5m2"))
+
+
 def test_quantize_zero_tensor():
     q, s = quantize(torch.zeros(16, 32, dtype=torch.bfloat16, device="cuda"))
     assert_device_ok()

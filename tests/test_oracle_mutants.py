@@ -167,3 +167,24 @@ def test_mutant_e4m3_ties_away_from_zero(monkeypatch):
     _patch(monkeypatch, "e4m3_round", bad)
     _fails(P.test_e4m3_rounding_rules)
     assert good is not bad
+
+
+def test_mutant_e5m2_ties_away_from_zero(monkeypatch):
+    def bad(x):
+        x = np.asarray(x, np.float64)
+        a = np.abs(x)
+        e = np.clip(np.floor(np.log2(np.where(a > 0, a, 1.0))), -14, 15)
+        quantum = np.exp2(e - 2)
+        q = np.minimum(np.floor(a / quantum + 0.5) * quantum, 57344.0)
+        return np.where(a > 0, np.sign(x) * q, 0.0 * x)
+    _patch(monkeypatch, "e5m2_round", bad)
+    _fails(P.test_e5m2_rounding_rules)
+
+
+def test_mutant_e5m2_exponent_bias(monkeypatch):
+    good = OC.e5m2_encode
+
+    def bad(v):
+        return good(np.asarray(v, np.float64) * 2.0)     # an exponent bias off by one
+    _patch(monkeypatch, "e5m2_encode", bad)
+    _fails(lambda: P.test_e5m2_known_encodings(1.0, 0x3C))

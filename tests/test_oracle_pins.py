@@ -468,6 +468,52 @@ def test_e4m3_rounding_rules():
         assert abs(O.e4m3_round(v) - v) <= abs(best - v) + 1e-15
 
 
+# --------------------------------------------------------------------------
+# e5m2 (FP8 for gradients) rounding and encoding, from the format's definition
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("v,code", [(1.0, 0x3C), (-1.0, 0xBC), (57344.0, 0x7B), (2.0 ** -14, 0x04),
+                                    (2.0 ** -16, 0x01), (3 * 2.0 ** -16, 0x03), (1.25, 0x3D), (3.0, 0x42),
+                                    (0.0, 0x00), (1536.0, 0x66)])
+def test_e5m2_known_encodings(v, code):
+    assert int(O.e5m2_encode(np.array([v]))[0]) == code
+    assert O.e5m2_decode(np.array([code], np.uint8))[0] == v
+
+
+def test_e5m2_every_code_round_trips():
+    codes = np.array([c for c in range(256) if ((c >> 2) & 0x1F) != 31], np.uint8)   # skip inf / NaN
+    vals = O.e5m2_decode(codes)
+    assert np.array_equal(O.e5m2_round(vals), vals)
+    back = O.e5m2_encode(vals)
+    nz = codes != 0x80
+    assert np.array_equal(back[nz], codes[nz])
+
+
+def test_e5m2_rounding_rules():
+    assert O.e5m2_round(1.125) == 1.0              # halfway 1 / 1.25 -> even mantissa 0
+    assert O.e5m2_round(1.375) == 1.5              # halfway 1.25 / 1.5 -> even mantissa 2
+    assert O.e5m2_round(2.0 ** -17) == 0.0          # half the smallest subnormal
+    assert O.e5m2_round(2.0 ** -17 * 1.001) == 2.0 ** -16
+    assert O.e5m2_round(60000.0) == 57344.0 and O.e5m2_round(-1e6) == -57344.0
+    x = np.random.default_rng(7).uniform(2.0 ** -14, 57344, 10000)
+    assert np.max(np.abs(O.e5m2_round(x) - x) / x) <= 2.0 ** -3 + 1e-15
+    grid = np.unique(np.abs(O.e5m2_decode(np.array([c for c in range(124)], np.uint8))))
+    for v in np.random.default_rng(8).uniform(0, 57344, 500):
+        best = grid[np.argmin(np.abs(grid - v))]
+        assert abs(O.e5m2_round(v) - v) <= abs(best - v) + 1e-12
+
+
+def test_fp8_scale_and_quantize_per_format():
+    x = np.array([[0.5, -3.0], [2.0, 0.25]], np.float32)
+    assert O.fp8_scale(x, "e4m3") == np.float32(3.0) / np.float32(448.0)
+    assert O.fp8_scale(x, "e5m2") == np.float32(3.0) / np.float32(57344.0)
+    for fmt, top in (("e4m3", 448.0), ("e5m2", 57344.0)):
+        codes = O.fp8_quantize(x, O.fp8_scale(x, fmt), fmt)
+        vals = O.fp8_decode(codes, fmt)
+        assert np.max(np.abs(vals)) == top               # the largest magnitude lands on the top code
+        assert O.fp8_scale(np.zeros((2, 2), np.float32), fmt) == 1.0
+
+
 def test_fp8_scale_and_quantize():
     x = np.array([[0.5, -3.0], [1.5, 0.25]], np.float32)
     s = O.fp8_scale(x)
