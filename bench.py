@@ -349,6 +349,20 @@ def bench_fp8_forward(C, b, shape, steps, warmup, peak_bf16):
             "peak_note": "fp8 dense peak taken as 2x the measured bf16 peak (nominal ratio 4.5 / 2.25 PFLOP/s)"}
 
 
+def bench_fp8_fwdbwd(C, b, shape, steps, warmup, peak_bf16):
+    """The block forward + backward with FP8 operands (e4m3 activations and
+    weights, e5m2 gradients; activation and gradient quantisation in the
+    step, weight quantisation timed apart) against the bf16 step."""
+    n = max(3, steps)
+    t_w, _ = time_steps([b.fp8_quantize_weights], n, warmup, stage_events=False)
+    t_8, _ = time_steps([b.forward_fp8, b.backward_fp8], n, warmup, stage_events=False)
+    t_16, _ = time_steps(FusedStep(C, b).calls(), n, warmup, stage_events=False)
+    fl = shape.fwdbwd_flops()
+    return {"workload": shape.name, "fp8_fwdbwd_ms": t_8 / n, "bf16_fwdbwd_ms": t_16 / n, "speedup": t_16 / t_8,
+            "fp8_fwdbwd_tflops": fl / (t_8 / n * 1e-3) / 1e12, "weight_quantize_ms": t_w / n,
+            "formats": "e4m3 activations and weights, e5m2 gradients (dP, dH), one fp32 scale per tensor"}
+
+
 def bench_qkv_rope(C, steps, warmup, M=8192, S=2048, d=4096, n_heads=32):
     """QKV projection of the 7B-size block (MHA, 32 heads of 128) with RoPE
     in the epilogue, against the plain GEMM followed by a standalone RoPE
@@ -519,9 +533,11 @@ def main():
         if args.leg == "lmhead":
             out = {"lmhead_ce": bench_lmhead(C, args.steps, args.warmup)}
         else:
-            b = BlockBuffers(block_inputs(shape, seed=0, device="cuda"), backward=False)
-            out = {"next_fp8_forward": bench_fp8_forward(C, b, shape, args.steps, args.warmup,
-                                                         load_peaks()["bf16_tflops"])}
+            b = BlockBuffers(block_inputs(shape, seed=0, device="cuda"), backward=shape.backward)
+            pk = load_peaks()["bf16_tflops"]
+            out = {"next_fp8_forward": bench_fp8_forward(C, b, shape, args.steps, args.warmup, pk)}
+            if shape.backward:
+                out["next_fp8_fwdbwd"] = bench_fp8_fwdbwd(C, b, shape, args.steps, args.warmup, pk)
         print(json.dumps(out), flush=True)
         return
 
@@ -635,6 +651,9 @@ def main():
             torch.cuda.empty_cache()
         extras["next_fp8_forward"] = bench_fp8_forward(C, b, shape, args.steps, args.warmup, peak)
         torch.cuda.empty_cache()
+        if shape.backward:
+            extras["next_fp8_fwdbwd"] = bench_fp8_fwdbwd(C, b, shape, args.steps, args.warmup, peak)
+            torch.cuda.empty_cache()
         del b, x, fs, calls
         torch.cuda.empty_cache()
         extras["plain_gemm_vs_cublas"] = bench_plain_vs_cublas(C, shape, args.steps, args.warmup)

@@ -81,6 +81,7 @@ SIGNATURES = {
     "coda_fp8_quantize": (_INT, [_P, _P, _P, _P, _P, _I64, _I64, _P]),
     "coda_fp8_quantize_e5m2": (_INT, [_P, _P, _P, _P, _P, _I64, _I64, _P]),
     "coda_gemm_fp8": (_INT, [_P, _P, _INT, _INT, _P, _P, _INT, _INT, _P, _P, _I64, _I64, _I64, _P, _P, _P]),
+    "coda_gemm_dgrad_rmsbwd_fp8": (_INT, [_P, _P, _INT, _P, _P, _INT, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "coda_gemm_res_prms_fp8": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "coda_gemm_rowscale_swiglu_fp8": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _U32, _P]),
     "coda_lmhead_ce_workspace_bytes": (_SZ, [_I64, _I64, _I64, _INT]),
@@ -503,6 +504,23 @@ def coda_gemm_fp8(A, a_mn_major: bool, a_format: int, sA, B, b_mn_major: bool, b
                                         _ptr(sB, F32, "sB"), _ptr(C, BF, "C"), M, N, K,
                                         _ptr(row_scale, F32, "row_scale"), _ptr(col_scale, BF, "col_scale"),
                                         _stream(stream)), "coda_gemm_fp8")
+
+
+def coda_gemm_dgrad_rmsbwd_fp8(dPq, dp_format: int, sdP, W2q, w_format: int, sW2, H, g, c, dH, dgpart,
+                               stream=None):
+    """dgrad2 with the RMSNorm-backward epilogue on 8-bit operands (see include/coda.h)."""
+    M, N2 = dPq.shape
+    d = W2q.shape[1]
+    _shape(W2q, (N2, d), "W2q")
+    _shape(H, (M, d), "H")
+    _shape(g, (d,), "g")
+    _shape(c, (M,), "c")
+    _shape(dH, (M, d), "dH")
+    _shape(dgpart, (coda_dgpart_rows(M), d), "dgpart")
+    _check(load_library().coda_gemm_dgrad_rmsbwd_fp8(
+        _h(dPq), _ptr(dPq, U8, "dPq"), int(dp_format), _ptr(sdP, F32, "sdP"), _ptr(W2q, U8, "W2q"), int(w_format),
+        _ptr(sW2, F32, "sW2"), _ptr(H, BF, "H"), _ptr(g, BF, "g"), _ptr(c, F32, "c"), _ptr(dH, BF, "dH"),
+        _ptr(dgpart, F32, "dgpart"), M, N2, d, _stream(stream)), "coda_gemm_dgrad_rmsbwd_fp8")
 
 
 def coda_gemm_res_prms_fp8(Xq, sX, W1q, sW1, R, H, psum, stream=None):

@@ -599,30 +599,65 @@ coda_status_t coda_fp8_quantize_e5m2(coda_handle_t h, const void* src, const voi
 coda_status_t coda_gemm_fp8(coda_handle_t h, const void* A, int a_mn_major, int a_format, const float* sA,
                             const void* B, int b_mn_major, int b_format, const float* sB, void* C, int64_t M,
                             int64_t N, int64_t K, const float* row_scale, const void* col_scale, void* stream) {
+  if ((a_format != 0 && a_format != 1) || (b_format != 0 && b_format != 1)) return CODA_ERR_INVALID_ARG;
+  if (a_mn_major && !b_mn_major) return CODA_ERR_UNSUPPORTED;
+  // With both operands MN-major K is their row count (a token count for the
+  // weight gradients): any K >= 0, the ragged last k-block zero-filled by TMA,
+  // and K == 0 an empty sum (A and B may then be NULL).  Otherwise K is a
+  // contiguous extent of 8-bit codes: a multiple of 16.
+  const bool k_rows = a_mn_major && b_mn_major;
+  const int64_t n_ops = k_rows && K == 0 ? 0 : M;  // operands present when M > 0 and K > 0
   CODA_TRY(Check()
                .handle(h)
                .rows(M)
-               .mptr(A, M)
+               .mptr(A, n_ops)
                .opt_sptr(sA)
-               .ptr(B)
+               .mptr(B, k_rows ? K : 1)
                .opt_sptr(sB)
                .mptr(C, M)
                .opt_ptr(row_scale)
                .opt_ptr(col_scale)
                .cols(N)
-               .cols(K)
                .st);
-  if ((a_format != 0 && a_format != 1) || (b_format != 0 && b_format != 1)) return CODA_ERR_INVALID_ARG;
-  if (a_mn_major && !b_mn_major) return CODA_ERR_UNSUPPORTED;
-  // rows of 8-bit operands: 16-byte multiples along the contiguous extent
-  if ((!a_mn_major || !b_mn_major) && K % 16 != 0) return CODA_ERR_ALIGNMENT;
+  CODA_TRY((k_rows ? Check().rows(K) : Check().cols(K)).st);
+  if (!k_rows && K % 16 != 0) return CODA_ERR_ALIGNMENT;
   if (a_mn_major && M % 16 != 0) return CODA_ERR_ALIGNMENT;
   if (b_mn_major && N % 16 != 0) return CODA_ERR_ALIGNMENT;
   if (M == 0) return CODA_OK;
+  if (K == 0)
+    return from_cuda(cudaMemsetAsync(C, 0, size_t(M) * N * 2, static_cast<cudaStream_t>(stream)));
   return from_cuda(gemm_store_fp8(ctx_of(h, stream), static_cast<const uint8_t*>(A), a_mn_major != 0, a_format, sA,
                                   static_cast<const uint8_t*>(B), b_mn_major != 0, b_format, sB,
                                   static_cast<bf16*>(C), int(M), int(N), int(K), row_scale,
                                   static_cast<const bf16*>(col_scale)));
+}
+
+coda_status_t coda_gemm_dgrad_rmsbwd_fp8(coda_handle_t h, const void* dPq, int dp_format, const float* sdP,
+                                         const void* W2q, int w_format, const float* sW2, const void* H,
+                                         const void* g, const float* c, void* dH, float* dgpart, int64_t M,
+                                         int64_t N2, int64_t d, void* stream) {
+  CODA_TRY(Check()
+               .handle(h)
+               .rows(M)
+               .mptr(dPq, M)
+               .sptr(sdP)
+               .ptr(W2q)
+               .sptr(sW2)
+               .mptr(H, M)
+               .ptr(g)
+               .mptr(c, M)
+               .mptr(dH, M)
+               .mptr(dgpart, M)
+               .cols(N2)
+               .cols(d)
+               .st);
+  if ((dp_format != 0 && dp_format != 1) || (w_format != 0 && w_format != 1)) return CODA_ERR_INVALID_ARG;
+  if (N2 % 16 != 0 || d % 16 != 0) return CODA_ERR_ALIGNMENT;
+  if (M == 0) return CODA_OK;
+  return from_cuda(gemm_dgrad_rms_fp8(ctx_of(h, stream), static_cast<const uint8_t*>(dPq), dp_format, sdP,
+                                      static_cast<const uint8_t*>(W2q), w_format, sW2, static_cast<const bf16*>(H),
+                                      static_cast<const bf16*>(g), c, static_cast<bf16*>(dH), dgpart, int(M),
+                                      int(N2), int(d)));
 }
 
 coda_status_t coda_gemm_res_prms_fp8(coda_handle_t h, const void* Xq, const float* sX, const void* W1q,

@@ -147,6 +147,14 @@ cudaError_t gemm_store_fp8(const LaunchCtx& c, const uint8_t* A, bool a_mn, int 
                            const uint8_t* B, bool b_mn, int b_fmt, const float* sB, __nv_bfloat16* C, int M, int N,
                            int K, const float* row_scale, const __nv_bfloat16* col_scale);
 
+// dgrad2 with the RMSNorm-backward epilogue (as gemm_dgrad_rms) on 8-bit
+// operands: dP codes [M][N2] (format dp_fmt, scale sdP), W2t codes [N2][d]
+// (format w_fmt, scale sW2).
+cudaError_t gemm_dgrad_rms_fp8(const LaunchCtx& c, const uint8_t* dPq, int dp_fmt, const float* sdP,
+                               const uint8_t* W2q, int w_fmt, const float* sW2, const __nv_bfloat16* H,
+                               const __nv_bfloat16* g, const float* cvec, __nv_bfloat16* dH, float* dgpart, int M,
+                               int N2, int d);
+
 int ce_tile_cols();    // vocabulary columns per CE statistics tile
 int prms_tile_cols();  // columns per partial-RMS tile of GEMM1
 

@@ -92,4 +92,28 @@ cudaError_t gemm_store_fp8(const LaunchCtx& c0, const uint8_t* A, bool a_mn, int
   return cudaErrorNotSupported;  // MN-major A with K-major B is not used on this path
 }
 
+cudaError_t gemm_dgrad_rms_fp8(const LaunchCtx& c0, const uint8_t* dPq, int dp_fmt, const float* sdP,
+                               const uint8_t* W2q, int w_fmt, const float* sW2, const __nv_bfloat16* H,
+                               const __nv_bfloat16* g, const float* cvec, __nv_bfloat16* dH, float* dgpart, int M,
+                               int N2, int d) {
+  LaunchCtx c = c0;
+  c.scale_a = sdP;
+  c.scale_b = sW2;
+  c.f8_fmt = f8_format_bits(dp_fmt, w_fmt);
+  // acc[m, k] = sum_n dP[m, n] W2t[n, k]: A = dP codes K-major (K = N2), B =
+  // W2t codes stored [K][N] (MN-major)
+  CUtensorMap ta, tb;
+  if (!make_f8_operand_map(&ta, dPq, false, M, N2, BM)) return cudaErrorInvalidValue;
+  if (!make_f8_operand_map(&tb, W2q, true, d, N2, b_box_rows(c))) return cudaErrorInvalidValue;
+  EpiDgradRms::Params ep{};
+  if (!make_tmap_store_bf16(&ep.dH, dH, d, M, d)) return cudaErrorInvalidValue;
+  ep.H = H;
+  ep.ldh = d;
+  ep.g = g;
+  ep.c = cvec;
+  ep.dgpart = dgpart;
+  ep.inv_d = 1.0f / static_cast<float>(d);
+  return run_gemm<false, true, false, EpiDgradRms, true>(c, ta, tb, tb, M, d, N2, (d + kBN - 1) / kBN, ep);
+}
+
 }  // namespace coda

@@ -81,6 +81,7 @@ cudaError_t launch_gemm2_kernel(const LaunchCtx& c, const CUtensorMap& ta, const
 template <bool A_MN, bool B_MN, bool B_DUAL, class Epi, bool FP8 = false>
 cudaError_t run_gemm(const LaunchCtx& c, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tb2, int M,
                      int N, int K, int tiles_n, const typename Epi::Params& ep) {
+  static_assert(!FP8 || Epi::kAccScale, "an epilogue on 8-bit operands must dequantise the accumulator");
   if (c.pair) return launch_gemm2_kernel<256, 6, A_MN, B_MN, B_DUAL, Epi, FP8>(c, ta, tb, tb2, M, N, K, tiles_n, ep);
   return launch_gemm_kernel<256, 4, A_MN, B_MN, B_DUAL, Epi, FP8>(c, ta, tb, tb2, M, N, K, tiles_n, ep);
 }

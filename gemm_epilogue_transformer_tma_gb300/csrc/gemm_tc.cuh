@@ -464,6 +464,7 @@ __device__ __forceinline__ float rstd_from_psum(const float* psum, int T, float 
 struct EpiStore {
   static constexpr int kEpiWarps = 4;
   static constexpr int kStoreSlots = 1;
+  static constexpr bool kAccScale = true;  // multiplies by EpiCtx::acc_scale: usable on FP8 operands
   struct Params {
     CUtensorMap out;  // [M][N] bf16
     const float* row_scale;
@@ -517,6 +518,7 @@ struct EpiStore {
 struct EpiStoreF32 {
   static constexpr int kEpiWarps = 4;
   static constexpr int kStoreSlots = 2;  // one 4 KB fp32 block
+  static constexpr bool kAccScale = false;  // ignores EpiCtx::acc_scale: bf16 operands only
   struct Params {
     CUtensorMap out;  // [M][N] fp32
     int beta;
@@ -549,6 +551,7 @@ struct EpiStoreF32 {
 struct EpiResPrms {
   static constexpr int kEpiWarps = 4;
   static constexpr int kStoreSlots = 2;
+  static constexpr bool kAccScale = true;  // multiplies by EpiCtx::acc_scale: usable on FP8 operands
   struct Params {
     CUtensorMap H;   // [M][d] bf16
     CUtensorMap Hg;  // [M][d] bf16, used when g != null
@@ -605,6 +608,7 @@ struct EpiResPrms {
 struct EpiRowscaleSwiglu {
   static constexpr int kEpiWarps = 4;
   static constexpr int kStoreSlots = 3;  // out, z gate, z up
+  static constexpr bool kAccScale = true;  // multiplies by EpiCtx::acc_scale: usable on FP8 operands
   struct Params {
     CUtensorMap out;  // [M][F] bf16
     CUtensorMap zg;   // gate half of z: [M][F] with the row pitch of z
@@ -666,6 +670,7 @@ struct EpiRowscaleSwiglu {
 struct EpiDgradRms {
   static constexpr int kEpiWarps = 4;
   static constexpr int kStoreSlots = 1;
+  static constexpr bool kAccScale = true;  // multiplies by EpiCtx::acc_scale: usable on FP8 operands
   struct Params {
     CUtensorMap dH;  // [M][d] bf16
     const __nv_bfloat16* H;
@@ -701,6 +706,9 @@ struct EpiDgradRms {
       tmem_ld32(c.taddr + cc, a);
       const int n0 = c.tn * BN + cc;
       if (n0 < c.N) {
+        // FP8 operands: dequantise the accumulator (acc_scale = 1 for bf16)
+#pragma unroll
+        for (int i = 0; i < 32; ++i) a[i] *= c.acc_scale;
         float h[32], gv[32];
         load_bf16x32(p.H + static_cast<int64_t>(c.m) * p.ldh + n0, row_ok ? c.N - n0 : 0, h);
         load_bf16x32(p.g + n0, c.N - n0, gv);
@@ -739,6 +747,7 @@ struct EpiDgradRms {
 struct EpiSwigluBwd {
   static constexpr int kEpiWarps = 4;
   static constexpr int kStoreSlots = 2;
+  static constexpr bool kAccScale = false;  // ignores EpiCtx::acc_scale: bf16 operands only
   struct Params {
     CUtensorMap dPg;  // gate half of dP: [M][F] with the row pitch of dP
     CUtensorMap dPu;  // up half
@@ -796,6 +805,7 @@ struct EpiSwigluBwd {
 struct EpiRope {
   static constexpr int kEpiWarps = 4;
   static constexpr int kStoreSlots = 2;
+  static constexpr bool kAccScale = false;  // ignores EpiCtx::acc_scale: bf16 operands only
   struct Params {
     CUtensorMap out;     // [M][N] bf16
     const float* cos_t;  // [S, 64]
@@ -853,6 +863,7 @@ struct EpiRope {
 struct EpiCeStats {
   static constexpr int kEpiWarps = 4;
   static constexpr int kStoreSlots = 0;
+  static constexpr bool kAccScale = false;  // ignores EpiCtx::acc_scale: bf16 operands only
   struct Params {
     const int32_t* labels;
     float* pmax;
@@ -919,6 +930,7 @@ struct EpiCeStats {
 struct EpiCeGrad {
   static constexpr int kEpiWarps = 4;
   static constexpr int kStoreSlots = 1;
+  static constexpr bool kAccScale = false;  // ignores EpiCtx::acc_scale: bf16 operands only
   struct Params {
     CUtensorMap dL;  // [M][Vc] bf16
     const int32_t* labels;

@@ -9,7 +9,9 @@ from __future__ import annotations
 
 import torch
 
-from . import (CODA_EPI_PLAIN, CODA_EPI_SWIGLU, coda_bwd_workspace_bytes, coda_dg_combine,
+from . import (CODA_EPI_PLAIN, CODA_EPI_SWIGLU, E4M3, E5M2, coda_bwd_workspace_bytes, coda_dg_combine,
+               coda_fp8_quantize, coda_fp8_quantize_e5m2, coda_gemm_dgrad_rmsbwd_fp8, coda_gemm_fp8,
+               coda_gemm_res_prms_fp8, coda_gemm_rowscale_swiglu_fp8,
                coda_dgpart_rows, coda_fold_rmsnorm_weight, coda_gemm_dgrad_rmsbwd, coda_gemm_prms_rowscale_swiglu,
                coda_gemm_dgrad_rmsbwd_cpart, coda_gemm_dgrad_swiglu_bwd, coda_gemm_res_prms, coda_gemm_res_prms_g,
                coda_gemm_res_prms_bwd, coda_gemm_rowscale_swiglu, coda_gemm_rowscale_swiglu_bwd,
@@ -149,6 +151,66 @@ class BlockBuffers:
         coda_dg_combine(self.dgpart, self.dg)
         coda_gemm_wgrad_gscale(self.H, self.dP, self.g, self.dW2t)
         coda_gemm_res_prms_bwd(self.dH, self.X, self.W1t, self.dX, self.dW1t, self.dH)
+
+    # -- FP8 operands: e4m3 activations and weights, e5m2 gradients -----------
+    def _fp8_buffers(self):
+        if getattr(self, "Xq", None) is not None:
+            return
+        M, K1, d, N2 = self.M, self.K1, self.d, self.N2
+        u8 = dict(dtype=torch.uint8, device=self.X.device)
+        self.Xq = torch.empty(M, K1, **u8)
+        self.Hq = torch.empty(M, d, **u8)
+        self.W1q = torch.empty(d, K1, **u8)
+        self.W2gq = torch.empty(N2, d, **u8)
+        self.W2q = torch.empty(N2, d, **u8)
+        # {amax, scale} per tensor: weights W1, W2*g, W2; activations X, H,
+        # gradients dP, dH
+        self.s_w = torch.empty(3, 2, dtype=F32, device=self.X.device)
+        self.s_a = torch.empty(4, 2, dtype=F32, device=self.X.device)
+        if self.with_backward:
+            self.dPq = torch.empty(M, N2, **u8)
+            self.dHq = torch.empty(M, d, **u8)
+
+    def fp8_quantize_weights(self):
+        """Per-tensor e4m3 codes of W1t, of W2t with g folded in (forward) and
+        of W2t alone (dgrad2); needed once per weight update."""
+        self._fp8_buffers()
+        coda_fp8_quantize(self.W1t, self.W1q, self.s_w[0])
+        coda_fp8_quantize(self.W2t, self.W2gq, self.s_w[1], self.g)
+        if self.with_backward:
+            coda_fp8_quantize(self.W2t, self.W2q, self.s_w[2])
+
+    def forward_fp8(self):
+        """The forward on e4m3 operands (X and H quantised in the step; the
+        weights by fp8_quantize_weights): the same epilogue programs."""
+        self._fp8_buffers()
+        coda_fp8_quantize(self.X, self.Xq, self.s_a[0])
+        coda_gemm_res_prms_fp8(self.Xq, self.s_a[0, 1:], self.W1q, self.s_w[0, 1:], self.R, self.H, self.psum)
+        coda_rstd_combine(self.psum, self.d, self.eps, self.rstd)
+        coda_fp8_quantize(self.H, self.Hq, self.s_a[1])
+        coda_gemm_rowscale_swiglu_fp8(self.Hq, self.s_a[1, 1:], self.W2gq, self.s_w[1, 1:], self.rstd, self.out,
+                                      self.z)
+
+    def backward_fp8(self):
+        """The backward with e5m2 gradients (dP, dH) against the e4m3 codes of
+        the forward's activations and weights: dgrad2 with the RMSNorm
+        backward in its epilogue, the weight gradients and the first layer's
+        data gradient as 8-bit GEMMs on the same codes read MN-major."""
+        M, K1, d, N2 = self.M, self.K1, self.d, self.N2
+        coda_swiglu_bwd(self.dY, self.z, self.rstd, self.dP, self.c, self.d)
+        coda_fp8_quantize_e5m2(self.dP, self.dPq, self.s_a[2])
+        coda_gemm_dgrad_rmsbwd_fp8(self.dPq, E5M2, self.s_a[2, 1:], self.W2q, E4M3, self.s_w[2, 1:], self.H, self.g,
+                                   self.c, self.dH, self.dgpart)
+        coda_dg_combine(self.dgpart, self.dg)
+        # dW2t[n][k] = g[k] sum_m dP[m][n] H[m][k]
+        coda_gemm_fp8(self.dPq, True, E5M2, self.s_a[2, 1:], self.Hq, True, E4M3, self.s_a[1, 1:], self.dW2t,
+                      N2, d, M, col_scale=self.g)
+        coda_fp8_quantize_e5m2(self.dH, self.dHq, self.s_a[3])
+        # dX = dH W1 (W1t codes [d][K1] read MN-major), dW1t = dH^T X
+        coda_gemm_fp8(self.dHq, False, E5M2, self.s_a[3, 1:], self.W1q, True, E4M3, self.s_w[0, 1:], self.dX,
+                      M, K1, d)
+        coda_gemm_fp8(self.dHq, True, E5M2, self.s_a[3, 1:], self.Xq, True, E4M3, self.s_a[0, 1:], self.dW1t,
+                      d, K1, M)
 
     # -- unfused ablation -----------------------------------------------------
     def forward_unfused(self):

@@ -368,10 +368,26 @@ coda_status_t coda_fp8_quantize_e5m2(coda_handle_t h, const void* src, const voi
  * pointers to fp32 scales or NULL (1); row_scale fp32 [M], col_scale bf16 [N],
  * both optional; C bf16 [M][N].  The contiguous extent of every 8-bit operand
  * (K for K-major, M or N for MN-major) a multiple of 16, N a multiple of 8.
- * MN-major A with K-major B returns CODA_ERR_UNSUPPORTED. */
+ * With both operands MN-major K is their row count and may take any value
+ * >= 0 (a token count for a weight gradient; K = 0 writes C = 0 and A, B may
+ * be NULL).  MN-major A with K-major B returns CODA_ERR_UNSUPPORTED. */
 coda_status_t coda_gemm_fp8(coda_handle_t h, const void* A, int a_mn_major, int a_format, const float* sA,
                             const void* B, int b_mn_major, int b_format, const float* sB, void* C, int64_t M,
                             int64_t N, int64_t K, const float* row_scale, const void* col_scale, void* stream);
+
+/* coda_gemm_dgrad_rmsbwd on 8-bit operands (the RMSNorm-backward epilogue
+ * with FP8 inputs):
+ *   acc = sdP * sW2 * sum_n dPq[m][n] W2q[n][k];  dH = bf16(g * acc - c * h);
+ *   dgpart as coda_gemm_dgrad_rmsbwd.
+ * dPq codes [M][N2] (dp_format: 0 = e4m3, 1 = e5m2, the usual choice for a
+ * gradient), W2q codes of W2t [N2][d] (w_format, without g), sdP / sW2 device
+ * pointers to the scales.  N2 and d multiples of 16.  The weight gradient
+ * dW2t = g * dP^T H and the first layer's dX / dW1t on FP8 operands are
+ * coda_gemm_fp8 calls with MN-major operands. */
+coda_status_t coda_gemm_dgrad_rmsbwd_fp8(coda_handle_t h, const void* dPq, int dp_format, const float* sdP,
+                                         const void* W2q, int w_format, const float* sW2, const void* H,
+                                         const void* g, const float* c, void* dH, float* dgpart, int64_t M,
+                                         int64_t N2, int64_t d, void* stream);
 
 /* coda_gemm_res_prms on e4m3 operands: H = bf16( sX * sW1 * sum_k Xq[m][k]
  * W1q[n][k] + R ), psum as before.  Xq codes [M][K1], W1q codes [d][K1], sX /

@@ -124,3 +124,20 @@ def test_fp8_gemm_layouts_and_formats_bit_exact(a_mn, b_mn, a_fmt, b_fmt, pairin
     torch.cuda.synchronize()
     assert_device_ok()
     assert torch.equal(Cd.cpu(), exact_bf16(A, Bt, torch.full((M,), 2.0)))   # sA * sB = 2
+
+
+@pytest.mark.parametrize("K", [300, 1, 0])
+def test_fp8_gemm_ragged_token_k_bit_exact(K, pairing):
+    """Both operands MN-major: K is their row count (a token count for a weight
+    gradient), ragged against the 128-deep k-block; K = 0 is an empty sum."""
+    M, N = 544, 336
+    A = ints((M, K), -4, 4, 14)
+    Bt = ints((N, K), -4, 4, 15)
+    Aq = np.ascontiguousarray(O.e5m2_encode(A.T.numpy().astype(np.float64)))
+    Bq = np.ascontiguousarray(O.e4m3_encode(Bt.T.numpy().astype(np.float64)))
+    Cd = torch.full((M, N), 7.0, dtype=torch.bfloat16, device="cuda")
+    C.coda_gemm_fp8(torch.from_numpy(Aq).cuda(), True, 1, None, torch.from_numpy(Bq).cuda(), True, 0, None,
+                    Cd, M, N, K)
+    torch.cuda.synchronize()
+    assert_device_ok()
+    assert torch.equal(Cd.cpu(), exact_bf16(A, Bt))

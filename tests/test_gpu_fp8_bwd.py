@@ -1,0 +1,94 @@
+"""FP8 forward and backward of the block (the FP8 operand variant of every
+epilogue program): e4m3 activations and weights, e5m2 gradients, each with
+one fp32 scale per tensor.
+
+Strict checks, stage by stage, against the oracle fed the GPU's own codes:
+  * the e5m2 codes and scales of dP and dH are bit-exact (the quantiser's
+    input is the bf16 tensor the GPU wrote);
+  * dgrad2 with the RMSNorm backward (dH, dg), wgrad2 (dW2t), dgrad1 (dX) and
+    wgrad1 (dW1t) meet the bf16 elementwise bar against the oracle fed the
+    dequantised codes (the GEMMs accumulate exact products in fp32).
+
+End to end against the fp64 oracle chained from the bf16 inputs, relative
+Frobenius bounds derived from the quantisation error.  Round to nearest in a
+format with p mantissa bits leaves an rms relative error of about
+2^-(p+1)/sqrt(3) per element: 3.6 % for e4m3 (p = 3) and 7.2 % for e5m2
+(p = 2).  Independent operand errors add in quadrature through a GEMM:
+  * out: two e4m3 operands per GEMM, two GEMMs: <= 8e-2;
+  * dP carries the forward's error (~5 %) and its e5m2 rounding (7.2 %),
+    about 9 %; dH = g acc - c h, dW2t and dg add an e4m3 operand (3.6 %):
+    about 10-11 %, bound 0.15;
+  * dX and dW1t take dH (about 11 %) rounded again to e5m2 (7.2 %) times
+    an e4m3 operand (3.6 %): about 14 %, bound 0.2.
+
+Method: "CODA: Rewriting Transformer Blocks as GEMM-Epilogue Programs"
+(Synced write-up, section 背景: FP8 makes the matmul faster and raises the
+share of the memory-bound work the epilogues absorb).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from coda_inputs import BlockShape, block_inputs
+from tests._parity import assert_device_ok, assert_elem, assert_frob, f64
+
+pytestmark = pytest.mark.gpu
+
+C = pytest.importorskip("gemm_epilogue_transformer_tma_gb300")
+from gemm_epilogue_transformer_tma_gb300.path import BlockBuffers  # noqa: E402
+from tests.test_gpu_parity import pairing  # noqa: E402,F401
+
+EPS = 1e-5
+SHAPES = {"ragged": BlockShape("ragged", 300, 208, 336, 544), "whole": BlockShape("whole", 384, 256, 512, 1024)}
+
+
+def deq(codes, scale_pair, fmt):
+    return O.fp8_decode(codes.cpu().numpy(), fmt) * float(scale_pair[1].item())
+
+
+def run_fp8(s):
+    x = {k: v.cuda() for k, v in block_inputs(s, 0, "cpu").items()}
+    b = BlockBuffers(x)
+    b.fp8_quantize_weights()
+    b.forward_fp8()
+    b.backward_fp8()
+    torch.cuda.synchronize()
+    assert_device_ok()
+    return x, b
+
+
+@pytest.mark.parametrize("name", ["ragged", "whole"])
+def test_fp8_backward_stages(name, pairing):
+    s = SHAPES[name]
+    x, b = run_fp8(s)
+    g, H, c = f64(x["g"]), f64(b.H), f64(b.c)
+    # gradient codes: bit-exact e5m2 of the bf16 tensors the GPU wrote
+    for src, q, sc in ((b.dP, b.dPq, b.s_a[2]), (b.dH, b.dHq, b.s_a[3])):
+        v = src.float().cpu().numpy()
+        ref_scale = O.fp8_scale(v, "e5m2")
+        assert np.float32(sc[1].item()) == ref_scale
+        assert np.array_equal(q.cpu().numpy(), O.fp8_quantize(v, ref_scale, "e5m2"))
+    dP = deq(b.dPq, b.s_a[2], "e5m2")
+    W2 = deq(b.W2q, b.s_w[2], "e4m3")
+    Hq = deq(b.Hq, b.s_a[1], "e4m3")
+    dH_ref, dg_ref = O.stage_dgrad2_rmsbwd(dP, W2, g, H, c)
+    assert_elem(b.dH, dH_ref, "dH (fp8 dgrad2)")
+    assert_elem(b.dg, dg_ref, "dg (fp8 dgrad2)")
+    assert_elem(b.dW2t, O.stage_wgrad2(Hq, dP, g), "dW2t (fp8 wgrad2)")
+    dHq = deq(b.dHq, b.s_a[3], "e5m2")
+    W1 = deq(b.W1q, b.s_w[0], "e4m3")
+    Xq = deq(b.Xq, b.s_a[0], "e4m3")
+    assert_elem(b.dX, O.stage_dgrad1(dHq, W1), "dX (fp8 dgrad1)")
+    assert_elem(b.dW1t, O.stage_wgrad1(dHq, Xq), "dW1t (fp8 wgrad1)")
+
+
+@pytest.mark.parametrize("name", ["ragged", "whole"])
+def test_fp8_forward_backward_end_to_end(name):
+    s = SHAPES[name]
+    x, b = run_fp8(s)
+    ref = O.block_backward(*(f64(x[k]) for k in ("X", "W1t", "R", "g", "W2t", "dY")), EPS, True)
+    bounds = {"out": 8e-2, "dR": 0.15, "dW2t": 0.15, "dg": 0.15, "dX": 0.2, "dW1t": 0.2}
+    for k_gpu, k_ref in (("out", "out"), ("dH", "dR"), ("dW2t", "dW2t"), ("dg", "dg"), ("dX", "dX"),
+                         ("dW1t", "dW1t")):
+        assert_frob(getattr(b, k_gpu), ref[k_ref], f"fp8 {k_gpu} e2e", tol=bounds[k_ref])
