@@ -354,12 +354,16 @@ def bench_fp8_fwdbwd(C, b, shape, steps, warmup, peak_bf16):
     weights, e5m2 gradients; activation and gradient quantisation in the
     step, weight quantisation timed apart) against the bf16 step."""
     n = max(3, steps)
+    named = b.fp8_forward_calls() + b.fp8_backward_calls()
+    calls = [f for _, f in named]
     t_w, _ = time_steps([b.fp8_quantize_weights], n, warmup, stage_events=False)
-    t_8, _ = time_steps([b.forward_fp8, b.backward_fp8], n, warmup, stage_events=False)
+    _, per8 = time_steps(calls, n, warmup, stage_events=True)
+    t_8, _ = time_steps(calls, n, 0, stage_events=False)
     t_16, _ = time_steps(FusedStep(C, b).calls(), n, warmup, stage_events=False)
     fl = shape.fwdbwd_flops()
     return {"workload": shape.name, "fp8_fwdbwd_ms": t_8 / n, "bf16_fwdbwd_ms": t_16 / n, "speedup": t_16 / t_8,
             "fp8_fwdbwd_tflops": fl / (t_8 / n * 1e-3) / 1e12, "weight_quantize_ms": t_w / n,
+            "stage_ms": {k: statistics.mean(v) for (k, _), v in zip(named, per8)},
             "formats": "e4m3 activations and weights, e5m2 gradients (dP, dH), one fp32 scale per tensor"}
 
 

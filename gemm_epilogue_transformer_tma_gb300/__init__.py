@@ -80,6 +80,7 @@ SIGNATURES = {
     "coda_rope_apply": (_INT, [_P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _P]),
     "coda_fp8_quantize": (_INT, [_P, _P, _P, _P, _P, _I64, _I64, _P]),
     "coda_fp8_quantize_e5m2": (_INT, [_P, _P, _P, _P, _P, _I64, _I64, _P]),
+    "coda_swiglu_bwd_fp8": (_INT, [_P, _P, _P, _P, _INT, _P, _P, _P, _I64, _I64, _I64, _P]),
     "coda_gemm_fp8": (_INT, [_P, _P, _INT, _INT, _P, _P, _INT, _INT, _P, _P, _I64, _I64, _I64, _P, _P, _P]),
     "coda_gemm_dgrad_rmsbwd_fp8": (_INT, [_P, _P, _INT, _P, _P, _INT, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "coda_gemm_res_prms_fp8": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
@@ -479,7 +480,8 @@ def coda_fp8_quantize(src, dst, amax_scale, g=None, stream=None):
 
 
 def coda_fp8_quantize_e5m2(src, dst, amax_scale, g=None, stream=None):
-    """Per-tensor e5m2 quantisation (scale = amax / 57344), like coda_fp8_quantize."""
+    """Per-tensor e5m2 quantisation (scale: the smallest power of two with
+    amax / scale <= 57344), like coda_fp8_quantize."""
     rows, cols = src.shape
     _shape(dst, (rows, cols), "dst")
     _shape(amax_scale, (2,), "amax_scale")
@@ -491,6 +493,20 @@ def coda_fp8_quantize_e5m2(src, dst, amax_scale, g=None, stream=None):
 
 
 E4M3, E5M2 = 0, 1
+
+
+def coda_swiglu_bwd_fp8(dY, z, rstd, fmt: int, dPq, amax_scale, c, d: int, stream=None):
+    """coda_swiglu_bwd with dP delivered as 8-bit codes (fmt E4M3 / E5M2) and
+    {amax, scale}; dP itself is never written (see include/coda.h)."""
+    M, F = dY.shape
+    _shape(z, (M, 2 * F), "z")
+    _shape(rstd, (M,), "rstd")
+    _shape(dPq, (M, 2 * F), "dPq")
+    _shape(amax_scale, (2,), "amax_scale")
+    _shape(c, (M,), "c")
+    _check(load_library().coda_swiglu_bwd_fp8(_h(dY), _ptr(dY, BF, "dY"), _ptr(z, BF, "z"), _ptr(rstd, F32, "rstd"),
+                                              int(fmt), _ptr(dPq, U8, "dPq"), _ptr(amax_scale, F32, "amax_scale"),
+                                              _ptr(c, F32, "c"), M, F, d, _stream(stream)), "coda_swiglu_bwd_fp8")
 
 
 def coda_gemm_fp8(A, a_mn_major: bool, a_format: int, sA, B, b_mn_major: bool, b_format: int, sB, C,

@@ -177,10 +177,16 @@ cudaError_t launch_rope_table(const LaunchCtx& c, float* cos_t, float* sin_t, in
 cudaError_t launch_rope_apply(const LaunchCtx& c, __nv_bfloat16* qkv, const float* cos_t, const float* sin_t,
                               int64_t M, int64_t N, int64_t rot_cols, int64_t head_dim, int64_t S);
 // per-tensor fp8 quantisation: ws[0] = amax of src (times g[col] if g),
-// ws[1] = scale = amax / fmax (1 if amax == 0); dst = fp8(src * g / scale),
-// e4m3 (fmax 448) or, with e5m2 != 0, e5m2 (fmax 57344)
+// ws[1] = scale = the smallest power of two with amax / scale <= fmax (1 if
+// amax == 0); dst = fp8(src * g / scale), e4m3 (fmax 448) or, with
+// e5m2 != 0, e5m2 (fmax 57344)
 cudaError_t launch_fp8_quantize(const LaunchCtx& c, const __nv_bfloat16* src, int64_t rows, int64_t cols,
                                 const __nv_bfloat16* g, float* ws, uint8_t* dst, int e5m2 = 0);
+// the SwiGLU backward straight to fp8 codes of bf16(dP) (two passes over dY
+// and z; ws as launch_fp8_quantize)
+cudaError_t launch_swiglu_bwd_fp8(const LaunchCtx& c, const __nv_bfloat16* dY, const __nv_bfloat16* z,
+                                  const float* rstd, float* ws, uint8_t* dPq, float* cvec, int64_t M, int64_t F,
+                                  int64_t d, int e5m2);
 // unfused ablation kernels
 cudaError_t launch_add_rmsnorm(const LaunchCtx& c, const __nv_bfloat16* A, const __nv_bfloat16* R,
                                const __nv_bfloat16* g, __nv_bfloat16* H, float* rstd, __nv_bfloat16* Nrm, int64_t M,

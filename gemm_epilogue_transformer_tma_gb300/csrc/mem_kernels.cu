@@ -133,9 +133,9 @@ __global__ void rstd_combine_kernel(const float* __restrict__ psum, int64_t M, i
 //   dP = bf16(r * dZ); c[m] = r^2/d * sum(dZg*zg + dZu*zu)
 // Each thread loads two 8-column chunks (six 16-byte loads) before computing
 // either, to keep enough bytes in flight.
-__device__ __forceinline__ float swiglu_bwd_chunk(const uint4& dyq, const uint4& zgq, const uint4& zuq, float r,
-                                                  uint4& pg, uint4& pu) {
-  float dy[8], zg[8], zu[8], og[8], ou[8];
+__device__ __forceinline__ float swiglu_bwd_vals(const uint4& dyq, const uint4& zgq, const uint4& zuq, float r,
+                                                 float* og, float* ou) {
+  float dy[8], zg[8], zu[8];
   unpack_bf16x8(dyq, dy);
   unpack_bf16x8(zgq, zg);
   unpack_bf16x8(zuq, zu);
@@ -149,6 +149,13 @@ __device__ __forceinline__ float swiglu_bwd_chunk(const uint4& dyq, const uint4&
     og[i] = r * dzg;
     ou[i] = r * dzu;
   }
+  return dot;
+}
+
+__device__ __forceinline__ float swiglu_bwd_chunk(const uint4& dyq, const uint4& zgq, const uint4& zuq, float r,
+                                                  uint4& pg, uint4& pu) {
+  float og[8], ou[8];
+  const float dot = swiglu_bwd_vals(dyq, zgq, zuq, r, og, ou);
   pg = pack8(og);
   pu = pack8(ou);
   return dot;
@@ -349,6 +356,39 @@ __global__ void rope_apply_kernel(__nv_bfloat16* __restrict__ qkv, const float* 
 // as integers).
 constexpr int kQuantRows = 8;
 
+// Per-tensor scale s = 2^k: the smallest power of two with amax / s <= fmax
+// (fmax = 448 = 0.875 * 2^9 for e4m3, 57344 = 0.875 * 2^16 for e5m2), k at
+// least -126; k = 0 for an all-zero tensor.  x / s = x * 2^-k is exact, so
+// every element is rounded once, by the conversion.
+template <bool E5M2>
+__device__ __forceinline__ int fp8_scale_exp(float amax) {
+  if (!(amax > 0.f)) return 0;
+  int ea;
+  const float ma = frexpf(amax, &ea);  // amax = ma * 2^ea, ma in [0.5, 1)
+  const int k = ea - (E5M2 ? 16 : 9) + (ma > 0.875f ? 1 : 0);
+  return k < -126 ? -126 : k;
+}
+
+// 2^k for -126 <= k <= 127
+__device__ __forceinline__ float pow2f(int k) { return __uint_as_float(static_cast<uint32_t>(k + 127) << 23); }
+
+// eight codes fp8(v[k] * inv), saturating round-to-nearest-even, packed in
+// column order (two conversions per instruction)
+template <bool E5M2>
+__device__ __forceinline__ uint2 fp8_codes8(const float* v, float inv) {
+  constexpr __nv_fp8_interpretation_t kind = E5M2 ? __NV_E5M2 : __NV_E4M3;
+  uint32_t w[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(v[4 * h] * inv, v[4 * h + 1] * inv), __NV_SATFINITE,
+                                                 kind);
+    const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(v[4 * h + 2] * inv, v[4 * h + 3] * inv),
+                                                 __NV_SATFINITE, kind);
+    w[h] = (lo & 0xFFFFu) | (hi << 16);
+  }
+  return make_uint2(w[0], w[1]);
+}
+
 __global__ void __launch_bounds__(256) amax_kernel(const uint4* __restrict__ src, const uint4* __restrict__ g8,
                                                    int64_t rows, int64_t c8, unsigned int* __restrict__ amax_bits) {
   griddep_wait();
@@ -386,19 +426,18 @@ __global__ void __launch_bounds__(256) amax_kernel(const uint4* __restrict__ src
   if (threadIdx.x == 0) atomicMax(amax_bits, __float_as_uint(t));
 }
 
-// dst = fp8(src * g / scale), scale = amax / fmax (1 for an all-zero
-// tensor), fp8 = e4m3 (fmax 448) or e5m2 (fmax 57344); saturating
-// round-to-nearest-even conversion.  ws[1] receives the scale.
+// dst = fp8(src * g / s), s the power-of-two scale of fp8_scale_exp (the
+// product src * g in fp32), fp8 = e4m3 or e5m2; saturating round-to-
+// nearest-even conversion.  ws[1] receives s.
+template <bool E5M2>
 __global__ void __launch_bounds__(256) fp8_quantize_kernel(const uint4* __restrict__ src,
                                                            const uint4* __restrict__ g8, int64_t rows, int64_t c8,
-                                                           int e5m2, float* __restrict__ ws,
-                                                           uint2* __restrict__ dst) {
+                                                           float* __restrict__ ws, uint2* __restrict__ dst) {
   griddep_wait();
   griddep_launch_dependents();
-  const float amax = ws[0];
-  const float scale = amax > 0.f ? amax / (e5m2 ? 57344.0f : 448.0f) : 1.0f;
-  const __nv_fp8_interpretation_t kind = e5m2 ? __NV_E5M2 : __NV_E4M3;
-  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) ws[1] = scale;
+  const int k = fp8_scale_exp<E5M2>(ws[0]);
+  const float inv = pow2f(-k);
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) ws[1] = pow2f(k);
   const int64_t j = blockIdx.x * 256LL + threadIdx.x;
   if (j >= c8) return;
   float gg[8];
@@ -420,14 +459,109 @@ __global__ void __launch_bounds__(256) fp8_quantize_kernel(const uint4* __restri
       if (r < nr) {
         float v[8];
         unpack_bf16x8(q[r], v);
-        uint32_t w[2] = {0u, 0u};
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t b = __nv_cvt_float_to_fp8((v[k] * gg[k]) / scale, __NV_SATFINITE, kind);
-          w[k >> 2] |= (b & 0xFFu) << (8 * (k & 3));
-        }
-        dst[(r0 + r) * c8 + j] = make_uint2(w[0], w[1]);
+        for (int q8 = 0; q8 < 8; ++q8) v[q8] *= gg[q8];
+        dst[(r0 + r) * c8 + j] = fp8_codes8<E5M2>(v, inv);
       }
+    }
+  }
+}
+
+// The SwiGLU backward straight to 8-bit codes of dP, in two passes over dY
+// and z so that the bf16 dP never reaches HBM (one CTA per row, as
+// swiglu_bwd_kernel).  Pass 1 writes c and folds max |bf16(dP)| into
+// amax_bits; pass 2 recomputes bf16(dP) and writes its codes.  The chunk
+// arithmetic is swiglu_bwd_vals and the conversion fp8_codes8, so the codes
+// equal those of swiglu_bwd_kernel's dP quantised by fp8_quantize_kernel.
+__device__ __forceinline__ float absmax8(const float* v, float mx) {
+#pragma unroll
+  for (int k = 0; k < 8; ++k) mx = fmaxf(mx, fabsf(v[k]));
+  return mx;
+}
+
+__global__ void __launch_bounds__(256) swiglu_bwd_amax_kernel(const __nv_bfloat16* __restrict__ dY,
+                                                              const __nv_bfloat16* __restrict__ z,
+                                                              const float* __restrict__ rstd,
+                                                              float* __restrict__ cvec, int64_t F, float inv_d,
+                                                              unsigned int* __restrict__ amax_bits) {
+  griddep_wait();
+  griddep_launch_dependents();
+  __shared__ float red[8];
+  __shared__ float red_max[8];
+  const int64_t m = blockIdx.x;
+  const float r = rstd[m];
+  const uint4* dy8 = reinterpret_cast<const uint4*>(dY + m * F);
+  const uint4* zg8 = reinterpret_cast<const uint4*>(z + m * 2 * F);
+  const uint4* zu8 = reinterpret_cast<const uint4*>(z + m * 2 * F + F);
+  const int64_t F8 = F / 8;
+  float dot = 0.f, mx = 0.f;
+  for (int64_t j0 = threadIdx.x; j0 < F8; j0 += 2 * 256) {
+    const int64_t j1 = j0 + 256;
+    const bool two = j1 < F8;
+    const uint4 a0 = dy8[j0], b0 = zg8[j0], c0 = zu8[j0];
+    uint4 a1 = a0, b1 = b0, c1 = c0;
+    if (two) {
+      a1 = dy8[j1];
+      b1 = zg8[j1];
+      c1 = zu8[j1];
+    }
+    float og[8], ou[8];
+    dot += swiglu_bwd_vals(a0, b0, c0, r, og, ou);
+    mx = absmax8(ou, absmax8(og, mx));
+    if (two) {
+      dot += swiglu_bwd_vals(a1, b1, c1, r, og, ou);
+      mx = absmax8(ou, absmax8(og, mx));
+    }
+  }
+  const float tot = block_sum_256(dot, red);
+  if (threadIdx.x == 0) cvec[m] = r * r * inv_d * tot;
+  const float t = block_max_256(mx, red_max);
+  // round-to-nearest-even is monotone and odd, so the bf16 of the largest
+  // fp32 magnitude is the largest magnitude of the bf16 dP
+  if (threadIdx.x == 0) atomicMax(amax_bits, __float_as_uint(__bfloat162float(__float2bfloat16_rn(t))));
+}
+
+template <bool E5M2>
+__global__ void __launch_bounds__(256) swiglu_bwd_fp8_kernel(const __nv_bfloat16* __restrict__ dY,
+                                                             const __nv_bfloat16* __restrict__ z,
+                                                             const float* __restrict__ rstd, int64_t F,
+                                                             float* __restrict__ ws, uint2* __restrict__ dPq) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int k = fp8_scale_exp<E5M2>(ws[0]);
+  const float inv = pow2f(-k);
+  if (blockIdx.x == 0 && threadIdx.x == 0) ws[1] = pow2f(k);
+  const int64_t m = blockIdx.x;
+  const float r = rstd[m];
+  const uint4* dy8 = reinterpret_cast<const uint4*>(dY + m * F);
+  const uint4* zg8 = reinterpret_cast<const uint4*>(z + m * 2 * F);
+  const uint4* zu8 = reinterpret_cast<const uint4*>(z + m * 2 * F + F);
+  const int64_t F8 = F / 8;
+  uint2* qg = dPq + m * 2 * F8;  // 8 codes per uint2: gate half, then up half
+  uint2* qu = qg + F8;
+  for (int64_t j0 = threadIdx.x; j0 < F8; j0 += 2 * 256) {
+    const int64_t j1 = j0 + 256;
+    const bool two = j1 < F8;
+    const uint4 a0 = dy8[j0], b0 = zg8[j0], c0 = zu8[j0];
+    uint4 a1 = a0, b1 = b0, c1 = c0;
+    if (two) {
+      a1 = dy8[j1];
+      b1 = zg8[j1];
+      c1 = zu8[j1];
+    }
+    uint4 pg, pu;
+    float v[8];
+    swiglu_bwd_chunk(a0, b0, c0, r, pg, pu);
+    unpack_bf16x8(pg, v);
+    qg[j0] = fp8_codes8<E5M2>(v, inv);
+    unpack_bf16x8(pu, v);
+    qu[j0] = fp8_codes8<E5M2>(v, inv);
+    if (two) {
+      swiglu_bwd_chunk(a1, b1, c1, r, pg, pu);
+      unpack_bf16x8(pg, v);
+      qg[j1] = fp8_codes8<E5M2>(v, inv);
+      unpack_bf16x8(pu, v);
+      qu[j1] = fp8_codes8<E5M2>(v, inv);
     }
   }
 }
@@ -654,8 +788,21 @@ cudaError_t launch_fp8_quantize(const LaunchCtx& c, const __nv_bfloat16* src, in
   e = launch_chained(c, amax_kernel, grid, dim3(256), 0, reinterpret_cast<const uint4*>(src), g8, rows, c8,
                      reinterpret_cast<unsigned int*>(ws));
   if (e != cudaSuccess) return e;
-  return launch_chained(c, fp8_quantize_kernel, grid, dim3(256), 0, reinterpret_cast<const uint4*>(src), g8, rows,
-                        c8, e5m2, ws, reinterpret_cast<uint2*>(dst));
+  return launch_chained(c, e5m2 ? fp8_quantize_kernel<true> : fp8_quantize_kernel<false>, grid, dim3(256), 0,
+                        reinterpret_cast<const uint4*>(src), g8, rows, c8, ws, reinterpret_cast<uint2*>(dst));
+}
+
+cudaError_t launch_swiglu_bwd_fp8(const LaunchCtx& c, const __nv_bfloat16* dY, const __nv_bfloat16* z,
+                                  const float* rstd, float* ws, uint8_t* dPq, float* cvec, int64_t M, int64_t F,
+                                  int64_t d, int e5m2) {
+  cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(float), c.stream);
+  if (e != cudaSuccess) return e;
+  const dim3 grid(static_cast<unsigned>(M));
+  e = launch_chained(c, swiglu_bwd_amax_kernel, grid, dim3(256), 0, dY, z, rstd, cvec, F,
+                     1.0f / static_cast<float>(d), reinterpret_cast<unsigned int*>(ws));
+  if (e != cudaSuccess) return e;
+  return launch_chained(c, e5m2 ? swiglu_bwd_fp8_kernel<true> : swiglu_bwd_fp8_kernel<false>, grid, dim3(256), 0, dY,
+                        z, rstd, F, ws, reinterpret_cast<uint2*>(dPq));
 }
 
 cudaError_t launch_add_rmsnorm(const LaunchCtx& c, const __nv_bfloat16* A, const __nv_bfloat16* R,

@@ -15,7 +15,7 @@ from . import (CODA_EPI_PLAIN, CODA_EPI_SWIGLU, E4M3, E5M2, coda_bwd_workspace_b
                coda_dgpart_rows, coda_fold_rmsnorm_weight, coda_gemm_dgrad_rmsbwd, coda_gemm_prms_rowscale_swiglu,
                coda_gemm_dgrad_rmsbwd_cpart, coda_gemm_dgrad_swiglu_bwd, coda_gemm_res_prms, coda_gemm_res_prms_g,
                coda_gemm_res_prms_bwd, coda_gemm_rowscale_swiglu, coda_gemm_rowscale_swiglu_bwd,
-               coda_gemm_wgrad_gscale, coda_prms_num_tiles, coda_rstd_combine, coda_swiglu_bwd,
+               coda_gemm_wgrad_gscale, coda_prms_num_tiles, coda_rstd_combine, coda_swiglu_bwd, coda_swiglu_bwd_fp8,
                coda_unfused_bwd, coda_unfused_fwd, coda_unfused_workspace_bytes)
 
 BF = torch.bfloat16
@@ -180,37 +180,54 @@ class BlockBuffers:
         if self.with_backward:
             coda_fp8_quantize(self.W2t, self.W2q, self.s_w[2])
 
-    def forward_fp8(self):
-        """The forward on e4m3 operands (X and H quantised in the step; the
-        weights by fp8_quantize_weights): the same epilogue programs."""
+    def fp8_forward_calls(self):
+        """The forward on e4m3 operands as named calls (X and H quantised in
+        the step, the weights by fp8_quantize_weights): the same epilogue
+        programs as the bf16 forward."""
         self._fp8_buffers()
-        coda_fp8_quantize(self.X, self.Xq, self.s_a[0])
-        coda_gemm_res_prms_fp8(self.Xq, self.s_a[0, 1:], self.W1q, self.s_w[0, 1:], self.R, self.H, self.psum)
-        coda_rstd_combine(self.psum, self.d, self.eps, self.rstd)
-        coda_fp8_quantize(self.H, self.Hq, self.s_a[1])
-        coda_gemm_rowscale_swiglu_fp8(self.Hq, self.s_a[1, 1:], self.W2gq, self.s_w[1, 1:], self.rstd, self.out,
-                                      self.z)
+        return [
+            ("quantize_X", lambda: coda_fp8_quantize(self.X, self.Xq, self.s_a[0])),
+            ("gemm1_res_prms_fp8", lambda: coda_gemm_res_prms_fp8(self.Xq, self.s_a[0, 1:], self.W1q,
+                                                                  self.s_w[0, 1:], self.R, self.H, self.psum)),
+            ("rstd_combine", lambda: coda_rstd_combine(self.psum, self.d, self.eps, self.rstd)),
+            ("quantize_H", lambda: coda_fp8_quantize(self.H, self.Hq, self.s_a[1])),
+            ("gemm2_rowscale_swiglu_fp8", lambda: coda_gemm_rowscale_swiglu_fp8(
+                self.Hq, self.s_a[1, 1:], self.W2gq, self.s_w[1, 1:], self.rstd, self.out, self.z)),
+        ]
+
+    def fp8_backward_calls(self):
+        """The backward as named calls, with e5m2 gradients (dP, dH) against
+        the e4m3 codes of the forward's activations and weights: the SwiGLU
+        backward writes dP's codes directly; dgrad2 runs the RMSNorm backward
+        in its epilogue; the weight gradients and the first layer's data
+        gradient are 8-bit GEMMs on the same codes read MN-major."""
+        self._fp8_buffers()
+        M, K1, d, N2 = self.M, self.K1, self.d, self.N2
+        return [
+            ("swiglu_bwd_e5m2", lambda: coda_swiglu_bwd_fp8(self.dY, self.z, self.rstd, E5M2, self.dPq,
+                                                            self.s_a[2], self.c, self.d)),
+            ("dgrad2_rmsbwd_fp8", lambda: coda_gemm_dgrad_rmsbwd_fp8(
+                self.dPq, E5M2, self.s_a[2, 1:], self.W2q, E4M3, self.s_w[2, 1:], self.H, self.g, self.c, self.dH,
+                self.dgpart)),
+            ("dg_combine", lambda: coda_dg_combine(self.dgpart, self.dg)),
+            # dW2t[n][k] = g[k] sum_m dP[m][n] H[m][k]
+            ("wgrad2_gscale_fp8", lambda: coda_gemm_fp8(self.dPq, True, E5M2, self.s_a[2, 1:], self.Hq, True, E4M3,
+                                                        self.s_a[1, 1:], self.dW2t, N2, d, M, col_scale=self.g)),
+            ("quantize_dH", lambda: coda_fp8_quantize_e5m2(self.dH, self.dHq, self.s_a[3])),
+            # dX = dH W1 (W1t codes [d][K1] read MN-major), dW1t = dH^T X
+            ("dgrad1_fp8", lambda: coda_gemm_fp8(self.dHq, False, E5M2, self.s_a[3, 1:], self.W1q, True, E4M3,
+                                                 self.s_w[0, 1:], self.dX, M, K1, d)),
+            ("wgrad1_fp8", lambda: coda_gemm_fp8(self.dHq, True, E5M2, self.s_a[3, 1:], self.Xq, True, E4M3,
+                                                 self.s_a[0, 1:], self.dW1t, d, K1, M)),
+        ]
+
+    def forward_fp8(self):
+        for _, f in self.fp8_forward_calls():
+            f()
 
     def backward_fp8(self):
-        """The backward with e5m2 gradients (dP, dH) against the e4m3 codes of
-        the forward's activations and weights: dgrad2 with the RMSNorm
-        backward in its epilogue, the weight gradients and the first layer's
-        data gradient as 8-bit GEMMs on the same codes read MN-major."""
-        M, K1, d, N2 = self.M, self.K1, self.d, self.N2
-        coda_swiglu_bwd(self.dY, self.z, self.rstd, self.dP, self.c, self.d)
-        coda_fp8_quantize_e5m2(self.dP, self.dPq, self.s_a[2])
-        coda_gemm_dgrad_rmsbwd_fp8(self.dPq, E5M2, self.s_a[2, 1:], self.W2q, E4M3, self.s_w[2, 1:], self.H, self.g,
-                                   self.c, self.dH, self.dgpart)
-        coda_dg_combine(self.dgpart, self.dg)
-        # dW2t[n][k] = g[k] sum_m dP[m][n] H[m][k]
-        coda_gemm_fp8(self.dPq, True, E5M2, self.s_a[2, 1:], self.Hq, True, E4M3, self.s_a[1, 1:], self.dW2t,
-                      N2, d, M, col_scale=self.g)
-        coda_fp8_quantize_e5m2(self.dH, self.dHq, self.s_a[3])
-        # dX = dH W1 (W1t codes [d][K1] read MN-major), dW1t = dH^T X
-        coda_gemm_fp8(self.dHq, False, E5M2, self.s_a[3, 1:], self.W1q, True, E4M3, self.s_w[0, 1:], self.dX,
-                      M, K1, d)
-        coda_gemm_fp8(self.dHq, True, E5M2, self.s_a[3, 1:], self.Xq, True, E4M3, self.s_a[0, 1:], self.dW1t,
-                      d, K1, M)
+        for _, f in self.fp8_backward_calls():
+            f()
 
     # -- unfused ablation -----------------------------------------------------
     def forward_unfused(self):

@@ -345,9 +345,11 @@ coda_status_t coda_rope_apply(coda_handle_t h, void* qkv, const float* cos_t, co
 
 /* Per-tensor e4m3 quantisation:
  *   amax = max |src[r][c] * g[c]|  (g = 1 when NULL; the product in fp32)
- *   scale = amax / 448 (1 when amax == 0)
+ *   scale = the smallest power of two 2^k with amax / 2^k <= 448 (k >= -126;
+ *           1 when amax == 0), so the largest element lands in (224, 448]
  *   dst[r][c] = e4m3( src[r][c] * g[c] / scale ), round to nearest even,
- *               saturating at +-448
+ *               saturating at +-448 (the division by a power of two is exact:
+ *               each element is rounded once, and code * scale is exact)
  * src bf16 [rows][cols], g bf16 [cols] or NULL (with g = the RMSNorm weight
  * and src = W2t this folds g into W2 while quantising), amax_scale fp32 [2]
  * receives {amax, scale}, dst e4m3 codes [rows][cols] (1 byte each).  cols a
@@ -355,11 +357,24 @@ coda_status_t coda_rope_apply(coda_handle_t h, void* qkv, const float* cos_t, co
 coda_status_t coda_fp8_quantize(coda_handle_t h, const void* src, const void* g, float* amax_scale, void* dst,
                                 int64_t rows, int64_t cols, void* stream);
 
-/* The same quantisation to e5m2 (5 exponent, 2 mantissa bits): scale =
- * amax / 57344, dst = e5m2( src * g / scale ), saturating at +-57344.  The
- * wider range suits gradients. */
+/* The same quantisation to e5m2 (5 exponent, 2 mantissa bits): scale = the
+ * smallest power of two with amax / scale <= 57344, dst = e5m2( src * g /
+ * scale ), saturating at +-57344.  The wider range suits gradients. */
 coda_status_t coda_fp8_quantize_e5m2(coda_handle_t h, const void* src, const void* g, float* amax_scale, void* dst,
                                      int64_t rows, int64_t cols, void* stream);
+
+/* coda_swiglu_bwd with dP delivered as per-tensor scaled 8-bit codes (the FP8
+ * backward's operand of dgrad2 and wgrad2): the codes, amax and scale equal
+ * those of coda_swiglu_bwd followed by coda_fp8_quantize (format 0, e4m3) or
+ * coda_fp8_quantize_e5m2 (format 1) on its bf16 dP, but dP is never written.
+ * Two passes over dY and z: the first writes c and the absolute maximum of
+ * bf16(dP), the second recomputes bf16(dP) and writes the codes.
+ * dY bf16 [M][F], z bf16 [M][2F], rstd fp32 [M]; dPq codes [M][2F] (gate
+ * half, then up half); amax_scale fp32 [2] receives {amax, scale} ({0, 1}
+ * when M == 0); c fp32 [M].  F and d multiples of 8. */
+coda_status_t coda_swiglu_bwd_fp8(coda_handle_t h, const void* dY, const void* z, const float* rstd, int format,
+                                  void* dPq, float* amax_scale, float* c, int64_t M, int64_t F, int64_t d,
+                                  void* stream);
 
 /* Plain GEMM on 8-bit operands (the mainloop of the method with FP8 inputs):
  *   C[m][n] = bf16( row_scale[m] * col_scale[n] * sA * sB * sum_k A[m][k] B[k][n] )

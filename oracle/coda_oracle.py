@@ -484,19 +484,28 @@ FP8_FORMATS = {"e4m3": (E4M3_MAX, e4m3_round, e4m3_encode, e4m3_decode),
 
 
 def fp8_scale(x, fmt="e4m3"):
-    """Per-tensor scale that maps the tensor's largest magnitude onto the
-    top of the format's range: amax / 448 (e4m3) or amax / 57344 (e5m2), 1
-    for an all-zero tensor, in fp32."""
-    amax = np.float32(np.max(np.abs(np.asarray(x, np.float32)))) if np.size(x) else np.float32(0)
-    return np.float32(amax / np.float32(FP8_FORMATS[fmt][0])) if amax > 0 else np.float32(1.0)
+    """Per-tensor scale: the smallest power of two s with amax / s <= fmax
+    (448 for e4m3, 57344 for e5m2), amax the largest magnitude of x in fp32,
+    so the largest element lands in (fmax / 2, fmax]; 1 for an all-zero
+    tensor; s >= 2^-126.  With a power of two, x / s and code * s are exact:
+    every element is rounded once, by the format.  (The method's pages name
+    FP8 only as a faster matmul and fix no scaling rule; this is the reading
+    taken.)"""
+    amax = float(np.max(np.abs(np.asarray(x, np.float32)))) if np.size(x) else 0.0
+    if amax == 0.0:
+        return np.float32(1.0)
+    ma, ea = np.frexp(amax)                     # amax = ma * 2^ea, ma in [0.5, 1)
+    mf, ef = np.frexp(FP8_FORMATS[fmt][0])      # fmax = 0.875 * 2^ef
+    k = int(ea) - int(ef) + (1 if ma > mf else 0)
+    return np.float32(2.0 ** max(k, -126))
 
 
 def fp8_quantize(x, scale, fmt="e4m3"):
-    """Codes of x / scale rounded to the format; the division is done in
-    fp32, the precision the conversion sees."""
+    """Codes of x / scale rounded to the format (x taken in fp32, as the
+    quantiser reads it; the division by a power-of-two scale is exact)."""
     _, rnd, enc, _ = FP8_FORMATS[fmt]
-    q = np.asarray(x, np.float32) / np.float32(scale)
-    return enc(rnd(q.astype(np.float64)))
+    q = np.asarray(x, np.float32).astype(np.float64) / float(scale)
+    return enc(rnd(q))
 
 
 def fp8_decode(b, fmt="e4m3"):

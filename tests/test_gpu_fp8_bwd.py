@@ -63,8 +63,16 @@ def test_fp8_backward_stages(name, pairing):
     s = SHAPES[name]
     x, b = run_fp8(s)
     g, H, c = f64(x["g"]), f64(b.H), f64(b.c)
+    # dP's codes come straight from the SwiGLU backward: they must equal the
+    # e5m2 codes of the bf16 dP that the unfused SwiGLU-backward kernel writes
+    # from the same z and rstd, with the same c
+    dP16 = torch.empty(s.M, s.N2, dtype=torch.bfloat16, device="cuda")
+    c16 = torch.empty(s.M, dtype=torch.float32, device="cuda")
+    C.coda_swiglu_bwd(b.dY, b.z, b.rstd, dP16, c16, s.d)
+    torch.cuda.synchronize()
+    assert torch.equal(b.c, c16)
     # gradient codes: bit-exact e5m2 of the bf16 tensors the GPU wrote
-    for src, q, sc in ((b.dP, b.dPq, b.s_a[2]), (b.dH, b.dHq, b.s_a[3])):
+    for src, q, sc in ((dP16, b.dPq, b.s_a[2]), (b.dH, b.dHq, b.s_a[3])):
         v = src.float().cpu().numpy()
         ref_scale = O.fp8_scale(v, "e5m2")
         assert np.float32(sc[1].item()) == ref_scale
@@ -92,3 +100,45 @@ def test_fp8_forward_backward_end_to_end(name):
     for k_gpu, k_ref in (("out", "out"), ("dH", "dR"), ("dW2t", "dW2t"), ("dg", "dg"), ("dX", "dX"),
                          ("dW1t", "dW1t")):
         assert_frob(getattr(b, k_gpu), ref[k_ref], f"fp8 {k_gpu} e2e", tol=bounds[k_ref])
+
+
+@pytest.mark.parametrize("fmt,name", [(C.E4M3, "e4m3"), (C.E5M2, "e5m2")])
+@pytest.mark.parametrize("M,F", [(300, 272), (1, 8), (64, 1040)])
+def test_swiglu_bwd_fp8_codes(fmt, name, M, F):
+    """coda_swiglu_bwd_fp8 against its unfused definition: the codes, amax
+    and scale of the bf16 dP that coda_swiglu_bwd writes, quantised by the
+    oracle; c bit-equal to coda_swiglu_bwd's; and dP against the oracle's
+    SwiGLU backward within the bf16 bar."""
+    g = torch.Generator().manual_seed(M * 7 + F)
+    dY = torch.randn(M, F, generator=g).to(torch.bfloat16).cuda()
+    z = (2.0 * torch.randn(M, 2 * F, generator=g)).to(torch.bfloat16).cuda()
+    rstd = (0.5 + torch.rand(M, generator=g)).cuda()
+    d = 256
+    dPq = torch.empty(M, 2 * F, dtype=torch.uint8, device="cuda")
+    sc = torch.empty(2, device="cuda")
+    c = torch.empty(M, device="cuda")
+    C.coda_swiglu_bwd_fp8(dY, z, rstd, fmt, dPq, sc, c, d)
+    dP16 = torch.empty(M, 2 * F, dtype=torch.bfloat16, device="cuda")
+    c16 = torch.empty(M, device="cuda")
+    C.coda_swiglu_bwd(dY, z, rstd, dP16, c16, d)
+    torch.cuda.synchronize()
+    assert_device_ok()
+    v = dP16.float().cpu().numpy()
+    ref_scale = O.fp8_scale(v, name)
+    assert np.float32(sc[0].item()) == np.float32(np.abs(v).max())
+    assert np.float32(sc[1].item()) == ref_scale
+    assert np.array_equal(dPq.cpu().numpy(), O.fp8_quantize(v, ref_scale, name))
+    assert torch.equal(c, c16)
+    dP_ref, c_ref = O.stage_swiglu_bwd(f64(dY), f64(z), f64(rstd), d)
+    assert_elem(dP16, dP_ref, "dP (bf16)")
+    assert_elem(c, c_ref, "c")
+
+
+def test_swiglu_bwd_fp8_empty():
+    z0 = torch.empty(0, 16, dtype=torch.bfloat16, device="cuda")
+    sc = torch.full((2,), 9.0, device="cuda")
+    C.coda_swiglu_bwd_fp8(torch.empty(0, 8, dtype=torch.bfloat16, device="cuda"), z0,
+                          torch.empty(0, device="cuda"), C.E5M2, torch.empty(0, 16, dtype=torch.uint8, device="cuda"),
+                          sc, torch.empty(0, device="cuda"), 64)
+    torch.cuda.synchronize()
+    assert sc.tolist() == [0.0, 1.0]

@@ -188,3 +188,28 @@ def test_mutant_e5m2_exponent_bias(monkeypatch):
         return good(np.asarray(v, np.float64) * 2.0)     # an exponent bias off by one
     _patch(monkeypatch, "e5m2_encode", bad)
     _fails(lambda: P.test_e5m2_known_encodings(1.0, 0x3C))
+
+
+def test_mutant_fp8_scale_one_binade_high(monkeypatch):
+    good = OC.fp8_scale
+    _patch(monkeypatch, "fp8_scale", lambda x, fmt="e4m3": np.float32(2.0 * good(x, fmt)))
+    _fails(P.test_fp8_scale_is_the_smallest_power_of_two, "e4m3", 448.0)
+
+
+def test_mutant_fp8_scale_edge_exclusive(monkeypatch):
+    """amax exactly fmax * 2^k must take s = 2^k, not 2^(k+1)."""
+    def bad(x, fmt="e4m3"):
+        amax = float(np.max(np.abs(np.asarray(x, np.float32))))
+        if amax == 0.0:
+            return np.float32(1.0)
+        k = int(np.floor(np.log2(amax / OC.FP8_FORMATS[fmt][0]))) + 1
+        return np.float32(2.0 ** k)
+    _patch(monkeypatch, "fp8_scale", bad)
+    _fails(P.test_fp8_scale_is_the_smallest_power_of_two, "e5m2", 57344.0)
+
+
+def test_mutant_fp8_scale_amax_over_fmax(monkeypatch):
+    """The plain ratio amax / fmax (not a power of two) fails the pins."""
+    _patch(monkeypatch, "fp8_scale", lambda x, fmt="e4m3": np.float32(
+        float(np.max(np.abs(np.asarray(x, np.float32)))) / OC.FP8_FORMATS[fmt][0]))
+    _fails(P.test_fp8_scale_and_quantize)

@@ -505,21 +505,51 @@ def test_e5m2_rounding_rules():
 
 def test_fp8_scale_and_quantize_per_format():
     x = np.array([[0.5, -3.0], [2.0, 0.25]], np.float32)
-    assert O.fp8_scale(x, "e4m3") == np.float32(3.0) / np.float32(448.0)
-    assert O.fp8_scale(x, "e5m2") == np.float32(3.0) / np.float32(57344.0)
+    # 3 / 448 lies in (2^-8, 2^-7]: 3 / 2^-7 = 384 <= 448 < 768
+    assert O.fp8_scale(x, "e4m3") == np.float32(2.0 ** -7)
+    # 3 / 57344 lies in (2^-15, 2^-14]: 3 / 2^-14 = 49152 <= 57344
+    assert O.fp8_scale(x, "e5m2") == np.float32(2.0 ** -14)
     for fmt, top in (("e4m3", 448.0), ("e5m2", 57344.0)):
-        codes = O.fp8_quantize(x, O.fp8_scale(x, fmt), fmt)
+        s = O.fp8_scale(x, fmt)
+        codes = O.fp8_quantize(x, s, fmt)
         vals = O.fp8_decode(codes, fmt)
-        assert np.max(np.abs(vals)) == top               # the largest magnitude lands on the top code
+        # the largest magnitude lands in the top binade, unsaturated
+        assert top / 2 < np.max(np.abs(vals)) <= top
+        # 0.5, 3, 2 and 0.25 are exact in both formats, and so is x / s
+        assert np.array_equal(vals * s, x.astype(np.float64))
         assert O.fp8_scale(np.zeros((2, 2), np.float32), fmt) == 1.0
+
+
+@pytest.mark.parametrize("fmt,top", [("e4m3", 448.0), ("e5m2", 57344.0)])
+def test_fp8_scale_is_the_smallest_power_of_two(fmt, top):
+    """Brute force over magnitudes spanning many binades, the exact edge
+    fmax * 2^k, and the values just beside it: s is a power of two with
+    amax / s <= fmax and amax / (s / 2) > fmax."""
+    rng = np.random.default_rng(9)
+    amaxes = np.concatenate([np.exp2(rng.uniform(-60, 60, 3000)),
+                             top * np.exp2(np.arange(-20, 21, dtype=np.float64))]).astype(np.float32)
+    amaxes = np.concatenate([amaxes, np.nextafter(amaxes, np.float32(np.inf)),
+                             np.nextafter(amaxes, np.float32(0))])
+    for a in amaxes:
+        s = float(O.fp8_scale(np.array([a, -a / 3], np.float32), fmt))
+        m, _ = np.frexp(s)
+        assert m == 0.5                                   # a power of two
+        assert float(a) / s <= top and float(a) / (s / 2) > top
+
+
+def test_fp8_scale_floor_for_tiny_tensors():
+    # amax = 2^-140 would want s = 2^-149 (e4m3): the floor 2^-126 keeps s
+    # normal and amax / s far below 448
+    x = np.array([2.0 ** -140], np.float32)
+    assert O.fp8_scale(x, "e4m3") == np.float32(2.0 ** -126)
 
 
 def test_fp8_scale_and_quantize():
     x = np.array([[0.5, -3.0], [1.5, 0.25]], np.float32)
     s = O.fp8_scale(x)
-    assert s == np.float32(3.0 / 448.0)
+    assert s == np.float32(2.0 ** -7)
     q = O.fp8_quantize(x, s)
-    # the largest magnitude maps to +-448
-    assert int(q[0, 1]) == 0xFE
-    np.testing.assert_allclose(O.e4m3_decode(q) * s, x, rtol=2.0 ** -4)
+    # -3 / 2^-7 = -384 = -1.5 * 2^8: sign 1, exponent field 15, mantissa 4
+    assert int(q[0, 1]) == 0xFC
+    np.testing.assert_array_equal(O.e4m3_decode(q) * s, x)
     assert O.fp8_scale(np.zeros((2, 2))) == 1.0
