@@ -96,6 +96,20 @@ struct EpiCtx {
   uint32_t stage;     // shared address of this warp's store-staging slots
 };
 
+// An epilogue program may declare
+//   static void prefetch(const Params&, int M, int N, int m, int n0, int bn);
+// the epilogue warps call it for their row m and the tile's columns
+// [n0, n0 + bn) before they wait for the tile's accumulator, so the
+// program's global inputs can be on their way to L2 during the mainloop.
+template <class E, class = void>
+struct EpiHasPrefetch {
+  static constexpr bool value = false;
+};
+template <class E>
+struct EpiHasPrefetch<E, decltype(void(&E::prefetch))> {
+  static constexpr bool value = true;
+};
+
 // Store staging: every epilogue warp owns Epi::kStoreSlots slots of
 // STORE_SLOT_BYTES in shared memory, after the operand ring.
 constexpr int STORE_SLOT_BYTES = 2048;
@@ -318,6 +332,8 @@ __global__ void __launch_bounds__(gemm_threads<Epi>(), 1)
       tile_coords(t, sh, tm, tn);
       const int acc = it & 1;
       const uint32_t acc_phase = (it >> 1) & 1;
+      if constexpr (EpiHasPrefetch<Epi>::value)
+        Epi::prefetch(ep, sh.M, sh.N, tm * BM + row, tn * BN + first_half * (BN / 2), HALVES * (BN / 2));
       bool ok = mbar_wait_bounded(&tfull[acc], acc_phase, abort_flag, ctl.timeout_ns);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) {
@@ -420,6 +436,21 @@ __device__ __forceinline__ void stage_f32x32(uint32_t slot, int lane, const floa
 
 __device__ __forceinline__ void slots_acquire(int lane) {
   if (lane == 0) bulk_wait_group_read0();
+  __syncwarp();
+}
+
+// Double-buffered form for a program with one output: before chunk j of a
+// run lane 0 waits until only the most recent store group (chunk j - 1, in
+// the other slot) may still be reading; at the start of a run (first) it
+// drains them all.  Within a run the stored chunks are a prefix of its
+// chunks, so consecutive stores always alternate slots.
+__device__ __forceinline__ void slots_acquire_db(int lane, bool first) {
+  if (lane == 0) {
+    if (first)
+      bulk_wait_group_read0();
+    else
+      bulk_wait_group_read1();
+  }
   __syncwarp();
 }
 
@@ -564,27 +595,52 @@ struct EpiResPrms {
     // applied on the activation side instead of being folded into W2
     const __nv_bfloat16* g;
   };
+  // the row's residual segment of the tile, line by line, into L2
+  static __device__ __forceinline__ void prefetch(const Params& p, int M, int N, int m, int n0, int bn) {
+    if (m >= M) return;
+    const __nv_bfloat16* row = p.R + static_cast<int64_t>(m) * p.ldr;
+    for (int n = n0; n < n0 + bn && n < N; n += 64) prefetch_l2(row + n);
+  }
+  // the residual's 32 columns from n0 as raw bf16 vectors (zero past nvalid)
+  static __device__ __forceinline__ void load_r(const __nv_bfloat16* row, int n0, int nvalid, uint4 (&q)[4]) {
+#pragma unroll
+    for (int g = 0; g < 4; ++g)
+      q[g] = g * 8 < nvalid ? __ldg(reinterpret_cast<const uint4*>(row + n0 + g * 8)) : make_uint4(0u, 0u, 0u, 0u);
+  }
   template <int BN>
   static __device__ __forceinline__ void run(const Params& p, const EpiCtx& c) {
     const bool row_ok = c.m < c.M;
+    const bool with_g = p.g != nullptr;
+    const __nv_bfloat16* rrow = p.R + static_cast<int64_t>(c.m) * p.ldr;
+    const int nb = c.tn * BN;
     float ss = 0.f;
+    // the residual is loaded one chunk ahead of its use
+    uint4 rq[4];
+    load_r(rrow, nb + c.c0, row_ok ? c.N - nb - c.c0 : 0, rq);
 #pragma unroll 1
     for (int cc = c.c0; cc < c.c1; cc += 32) {
       float v[32];
       tmem_ld32(c.taddr + cc, v);
-      const int n0 = c.tn * BN + cc;
+      const int n0 = nb + cc;
+      float r[32];
+#pragma unroll
+      for (int g = 0; g < 4; ++g) unpack_bf16x8(rq[g], &r[g * 8]);
+      if (cc + 32 < c.c1) load_r(rrow, n0 + 32, row_ok ? c.N - n0 - 32 : 0, rq);
       if (n0 < c.N && c.m0 < c.M) {
-        float r[32];
-        load_bf16x32(p.R + static_cast<int64_t>(c.m) * p.ldr + n0, row_ok ? c.N - n0 : 0, r);
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const float hb = bf16_round(fmaf(v[i], c.acc_scale, r[i]));
           v[i] = hb;
           ss = fmaf(hb, hb, ss);
         }
-        slots_acquire(c.lane);
-        stage_bf16x32(slot_addr(c, 0), c.lane, v);
-        if (p.g != nullptr) {
+        // H alone: two slots used alternately; H and Hg: one slot each
+        const int slot = with_g ? 0 : ((cc - c.c0) >> 5) & 1;
+        if (with_g)
+          slots_acquire(c.lane);
+        else
+          slots_acquire_db(c.lane, cc == c.c0);
+        stage_bf16x32(slot_addr(c, slot), c.lane, v);
+        if (with_g) {
           load_bf16x32(p.g + n0, c.N - n0, r);
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] *= r[i];
@@ -592,8 +648,8 @@ struct EpiResPrms {
         }
         slots_publish();
         if (c.lane == 0) {
-          tma_store_2d(&p.H, slot_addr(c, 0), n0, c.m0);
-          if (p.g != nullptr) tma_store_2d(&p.Hg, slot_addr(c, 1), n0, c.m0);
+          tma_store_2d(&p.H, slot_addr(c, slot), n0, c.m0);
+          if (with_g) tma_store_2d(&p.Hg, slot_addr(c, 1), n0, c.m0);
           bulk_commit_group();
         }
       }

@@ -255,6 +255,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi>(),
       tile_coords(t, sh, tm, tn);
       const int acc = it & 1;
       const uint32_t acc_phase = (it >> 1) & 1;
+      if constexpr (EpiHasPrefetch<Epi>::value)
+        Epi::prefetch(ep, sh.M, sh.N, (tm * 2 + static_cast<int>(rank)) * 128 + row,
+                      tn * BN + first_half * (BN / 2), HALVES * (BN / 2));
       bool ok = mbar_wait_bounded(&tfull[acc], acc_phase, abort_flag, ctl.timeout_ns);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) {
