@@ -36,7 +36,7 @@ sys.path.insert(0, ROOT)
 
 import torch  # noqa: E402
 
-from coda_inputs import B1, B7, B70, LMHEAD, BlockShape, block_inputs, ce_inputs, down_proj_inputs  # noqa: E402
+from coda_inputs import B1, B7, B70, LMHEAD, BlockShape, CEShape, block_inputs, ce_inputs, down_proj_inputs  # noqa: E402
 
 METRIC = "fused GEMM-RMSNorm-GEMM fwd+bwd TFLOP/s and % of GB300 bf16 dense peak"
 UNIT = "TFLOP/s"
@@ -418,8 +418,8 @@ def bench_plain_vs_cublas(C, shape, steps, warmup):
     return out
 
 
-def bench_lmhead(C, steps, warmup):
-    s = LMHEAD
+def bench_lmhead(C, steps, warmup, tokens=0):
+    s = LMHEAD if not tokens else CEShape(f"{LMHEAD.name}_m{tokens}", tokens, LMHEAD.d, LMHEAD.V)
     x = ce_inputs(s, 0, "cuda")
     ws = torch.empty(C.coda_lmhead_ce_workspace_bytes(s.M, s.d, s.V, True), dtype=torch.uint8, device="cuda")
     loss = torch.empty(1, device="cuda")
@@ -535,7 +535,7 @@ def main():
         from gemm_epilogue_transformer_tma_gb300.path import BlockBuffers
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
         if args.leg == "lmhead":
-            out = {"lmhead_ce": bench_lmhead(C, args.steps, args.warmup)}
+            out = {"lmhead_ce": bench_lmhead(C, args.steps, args.warmup, args.tokens)}
         else:
             b = BlockBuffers(block_inputs(shape, seed=0, device="cuda"), backward=shape.backward)
             pk = load_peaks()["bf16_tflops"]
