@@ -137,6 +137,33 @@ class BlockBuffers:
         if self.with_backward:
             self.backward()
 
+    def step_fp8(self):
+        """One pass with FP8 operands (weights quantised beforehand by
+        fp8_quantize_weights)."""
+        self.forward_fp8()
+        if self.with_backward:
+            self.backward_fp8()
+
+    # -- CUDA graphs ----------------------------------------------------------
+    def capture_step(self, fp8: bool = False):
+        """Record one step (step or step_fp8) into a CUDA graph and return
+        it; replay() then reruns it on whatever the input buffers hold.  One
+        eager step runs first, so that the library handle, tensor maps and
+        the fold's side stream exist before the capture (none of them may be
+        created inside it).  The fold's fork to the side stream and its join
+        back are recorded as graph edges."""
+        run = self.step_fp8 if fp8 else self.step
+        run()
+        torch.cuda.synchronize(self.X.device)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            run()
+        self._graph = graph
+        return graph
+
+    def replay(self):
+        self._graph.replay()
+
     # -- backward from the down projection's upstream gradient ---------------
     def backward_from_down_proj(self, dYb, W3t):
         """The backward when the block's output feeds a down projection

@@ -415,7 +415,9 @@ coda_status_t coda_gemm_res_prms_fp8(coda_handle_t h, const void* Xq, const floa
 
 /* coda_gemm_rowscale_swiglu on e4m3 operands: z = rstd[m] * sH * sW2 *
  * sum_k Hq[m][k] W2gq[n][k], then the same SwiGLU / PLAIN epilogue.  Hq codes
- * [M][d], W2gq codes [N2][d] (e.g. coda_fp8_quantize of W2t with g). */
+ * [M][d], W2gq codes [N2][d] (e.g. coda_fp8_quantize of W2t with g).  d a
+ * multiple of 16, and with SwiGLU N2 / 2 a multiple of 16 (CODA_ERR_ALIGNMENT
+ * otherwise). */
 coda_status_t coda_gemm_rowscale_swiglu_fp8(coda_handle_t h, const void* Hq, const float* sH, const void* W2gq,
                                             const float* sW2, const float* rstd, void* out, void* z_save, int64_t M,
                                             int64_t d, int64_t N2, uint32_t flags, void* stream);
