@@ -102,17 +102,27 @@ class BlockBuffers:
         and registers free on every SM, so the two share the SMs.  GEMM1 is
         launched first: its persistent CTAs take their SMs before the fold's
         CTAs fill them."""
+        self._beside(lambda: coda_gemm_res_prms(self.X, self.W1t, self.R, self.H, self.psum),
+                     lambda side: coda_fold_rmsnorm_weight(self.W2t, self.g, self.W2gt, stream=side))
+
+    def _beside(self, main_call, side_call):
+        """main_call on the current stream and side_call(side_stream) on a
+        second stream, both ordered after everything before on the current
+        stream; returns with the current stream ordered after both.  For a
+        tensor-bound persistent GEMM (launched first, its CTAs take their
+        SMs) with an independent HBM-bound kernel that fills the SMs'
+        remaining threads and registers."""
         main = torch.cuda.current_stream(self.X.device)
         if getattr(self, "_side", None) is None:
             self._side = torch.cuda.Stream(device=self.X.device)
             self._ev_in = torch.cuda.Event()
-            self._ev_fold = torch.cuda.Event()
+            self._ev_side = torch.cuda.Event()
         self._ev_in.record(main)
-        coda_gemm_res_prms(self.X, self.W1t, self.R, self.H, self.psum)
+        main_call()
         self._side.wait_event(self._ev_in)
-        coda_fold_rmsnorm_weight(self.W2t, self.g, self.W2gt, stream=self._side)
-        self._ev_fold.record(self._side)
-        main.wait_event(self._ev_fold)
+        side_call(self._side)
+        self._ev_side.record(self._side)
+        main.wait_event(self._ev_side)
 
     def backward_stages(self):
         """The backward as separate stage calls (dP, c, dgpart stay visible)."""
@@ -237,10 +247,12 @@ class BlockBuffers:
                 self.dPq, E5M2, self.s_a[2, 1:], self.W2q, E4M3, self.s_w[2, 1:], self.H, self.g, self.c, self.dH,
                 self.dgpart)),
             ("dg_combine", lambda: coda_dg_combine(self.dgpart, self.dg)),
-            # dW2t[n][k] = g[k] sum_m dP[m][n] H[m][k]
-            ("wgrad2_gscale_fp8", lambda: coda_gemm_fp8(self.dPq, True, E5M2, self.s_a[2, 1:], self.Hq, True, E4M3,
-                                                        self.s_a[1, 1:], self.dW2t, N2, d, M, col_scale=self.g)),
-            ("quantize_dH", lambda: coda_fp8_quantize_e5m2(self.dH, self.dHq, self.s_a[3])),
+            # dW2t[n][k] = g[k] sum_m dP[m][n] H[m][k]; dH's codes (needed
+            # only by the first layer's gradients) beside it
+            ("wgrad2_gscale_fp8+quantize_dH", lambda: self._beside(
+                lambda: coda_gemm_fp8(self.dPq, True, E5M2, self.s_a[2, 1:], self.Hq, True, E4M3, self.s_a[1, 1:],
+                                      self.dW2t, N2, d, M, col_scale=self.g),
+                lambda side: coda_fp8_quantize_e5m2(self.dH, self.dHq, self.s_a[3], stream=side))),
             # dX = dH W1 (W1t codes [d][K1] read MN-major), dW1t = dH^T X
             ("dgrad1_fp8", lambda: coda_gemm_fp8(self.dHq, False, E5M2, self.s_a[3, 1:], self.W1q, True, E4M3,
                                                  self.s_w[0, 1:], self.dX, M, K1, d)),
