@@ -553,3 +553,34 @@ def test_fp8_scale_and_quantize():
     assert int(q[0, 1]) == 0xFC
     np.testing.assert_array_equal(O.e4m3_decode(q) * s, x)
     assert O.fp8_scale(np.zeros((2, 2))) == 1.0
+
+
+def test_swiglu_backward_finite_difference():
+    """dZ of sum(swiglu(z) * dY) against central differences, element by
+    element, on both halves (a swapped half or a dropped silu' term fails)."""
+    rng = np.random.default_rng(21)
+    z = rng.normal(0, 2, (3, 8))
+    dY = rng.normal(0, 1, (3, 4))
+    dZ = O.swiglu_backward(dY, z)
+    h = 1e-6
+    for i in range(z.shape[0]):
+        for j in range(z.shape[1]):
+            zp, zm = z.copy(), z.copy()
+            zp[i, j] += h
+            zm[i, j] -= h
+            fd = (np.sum(O.swiglu(zp) * dY) - np.sum(O.swiglu(zm) * dY)) / (2 * h)
+            assert abs(dZ[i, j] - fd) <= 1e-7 * max(1.0, abs(fd))
+
+
+def test_argmax_lowest_brute_force():
+    """Small-integer rows with many ties: the first index of the row maximum,
+    found by a plain loop."""
+    rng = np.random.default_rng(22)
+    L = rng.integers(-3, 4, (200, 9)).astype(np.float64)
+    got = O.argmax_lowest(L)
+    for r in range(L.shape[0]):
+        best = 0
+        for j in range(1, L.shape[1]):
+            if L[r, j] > L[r, best]:
+                best = j
+        assert got[r] == best
