@@ -418,6 +418,41 @@ def bench_plain_vs_cublas(C, shape, steps, warmup):
     return out
 
 
+def bench_fp8_plain_vs_cublaslt(C, shape, steps, warmup):
+    """The library's plain 8-bit GEMM (e4m3 K-major operands, unit scales,
+    bf16 store) against cuBLASLt's (torch._scaled_mm) on the GEMM2 and dgrad2
+    shapes, same codes, interleaved: a measured library figure for the FP8
+    rate beside the nominal 2x of the bf16 peak."""
+    if not hasattr(torch, "_scaled_mm") or not hasattr(torch, "float8_e4m3fn"):
+        return {"unavailable": "torch has no float8 matmul"}
+    out = {}
+    n = max(3, steps // 2)
+    one = torch.ones((), device="cuda")
+    for name, (M, N, K) in {"gemm2": (shape.M, shape.N2, shape.d), "dgrad2": (shape.M, shape.d, shape.N2)}.items():
+        g = torch.Generator(device="cuda").manual_seed(0)
+        A = (torch.randn(M, K, device="cuda", generator=g) * 16).to(torch.float8_e4m3fn)
+        B = (torch.randn(N, K, device="cuda", generator=g) * 16).to(torch.float8_e4m3fn)
+        Cd = torch.empty(M, N, device="cuda", dtype=torch.bfloat16)
+        Au, Bu = A.view(torch.uint8), B.view(torch.uint8)
+        ours = [lambda: C.coda_gemm_fp8(Au, False, C.E4M3, None, Bu, False, C.E4M3, None, Cd, M, N, K)]
+        try:
+            torch._scaled_mm(A, B.t(), one, one, out_dtype=torch.bfloat16)
+        except Exception as e:  # noqa: BLE001 - report, do not fail the bench
+            return {"unavailable": f"torch._scaled_mm: {str(e).splitlines()[0][:160]}"}
+        lib = [lambda: torch._scaled_mm(A, B.t(), one, one, out_dtype=torch.bfloat16)]
+        t_o, t_l = [], []
+        for _ in range(2):
+            t_o.append(time_steps(ours, n, warmup, stage_events=False)[0] / n)
+            t_l.append(time_steps(lib, n, warmup, stage_events=False)[0] / n)
+        fl = 2.0 * M * N * K
+        out[name] = {"M": M, "N": N, "K": K, "coda_ms": min(t_o), "cublaslt_ms": min(t_l),
+                     "coda_tflops": fl / min(t_o) / 1e9, "cublaslt_tflops": fl / min(t_l) / 1e9,
+                     "ratio": min(t_l) / min(t_o)}
+        del A, B, Au, Bu, Cd
+        torch.cuda.empty_cache()
+    return out
+
+
 def bench_lmhead(C, steps, warmup, tokens=0):
     s = LMHEAD if not tokens else CEShape(f"{LMHEAD.name}_m{tokens}", tokens, LMHEAD.d, LMHEAD.V)
     x = ce_inputs(s, 0, "cuda")
@@ -463,7 +498,8 @@ class E2EPipeline:
         self.h2d = torch.cuda.Stream()
         self.d2h = torch.cuda.Stream()
         ev = lambda: [torch.cuda.Event(), torch.cuda.Event()]  # noqa: E731
-        self.ev_in, self.ev_comp, self.ev_out = ev(), ev(), ev()
+        # ev_in: the forward's inputs (X, R) landed; ev_in_bwd: dY landed
+        self.ev_in, self.ev_in_bwd, self.ev_comp, self.ev_out = ev(), ev(), ev(), ev()
         self.fresh = [True, True]
 
     def _load(self, slot):
@@ -471,9 +507,12 @@ class E2EPipeline:
         with torch.cuda.stream(self.h2d):
             if not self.fresh[slot]:
                 self.h2d.wait_event(self.ev_comp[slot])  # the previous step on this slot read it
-            for k in self.inputs:
+            for k in ("X", "R"):
                 getattr(b, k).copy_(self.host[k], non_blocking=True)
             self.ev_in[slot].record(self.h2d)
+            if "dY" in self.inputs:
+                b.dY.copy_(self.host["dY"], non_blocking=True)
+                self.ev_in_bwd[slot].record(self.h2d)
 
     def run(self, n):
         self._load(0)
@@ -485,6 +524,9 @@ class E2EPipeline:
                 self.compute.wait_event(self.ev_out[slot])  # dX of step i-2 read back
             b.forward()
             if b.with_backward:
+                # the upstream gradient is needed only now, as in a training
+                # loop where it arrives after the forward
+                self.compute.wait_event(self.ev_in_bwd[slot])
                 b.backward()
             self.ev_comp[slot].record(self.compute)
             self.fresh[slot] = False
@@ -542,6 +584,9 @@ def main():
             out = {"next_fp8_forward": bench_fp8_forward(C, b, shape, args.steps, args.warmup, pk)}
             if shape.backward:
                 out["next_fp8_fwdbwd"] = bench_fp8_fwdbwd(C, b, shape, args.steps, args.warmup, pk)
+            del b
+            torch.cuda.empty_cache()
+            out["fp8_plain_gemm_vs_cublaslt"] = bench_fp8_plain_vs_cublaslt(C, shape, args.steps, args.warmup)
         print(json.dumps(out), flush=True)
         return
 
@@ -624,9 +669,10 @@ def main():
                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                          "steps": n_e2e,
                          "timing": "host wall clock over the whole run, synchronize (and barrier) at both ends; "
-                                   "copies of step i+1 (H2D) and i (D2H) overlap step i's compute, the first "
-                                   "step's H2D and the last step's D2H overlap nothing; per-rank bytes, value "
-                                   "summed over ranks"}
+                                   "copies of step i+1 (H2D) and i (D2H) overlap step i's compute; each step's "
+                                   "backward waits for its dY copy, its forward for X and R only; the first "
+                                   "step's X / R copy and the last step's D2H overlap nothing; per-rank bytes, "
+                                   "value summed over ranks"}
         del host, pipe
     if not args.no_extras and rank == 0:
         # the same step with g broadcast in GEMM1's epilogue (no fold pass over
@@ -665,6 +711,8 @@ def main():
         del b, x, fs, calls
         torch.cuda.empty_cache()
         extras["plain_gemm_vs_cublas"] = bench_plain_vs_cublas(C, shape, args.steps, args.warmup)
+        extras["fp8_plain_gemm_vs_cublaslt"] = bench_fp8_plain_vs_cublaslt(C, shape, args.steps, args.warmup)
+        torch.cuda.empty_cache()
         extras["lmhead_ce"] = bench_lmhead(C, args.steps, args.warmup)
         torch.cuda.empty_cache()
         extras["next_qkv_rope"] = bench_qkv_rope(C, args.steps, args.warmup)
