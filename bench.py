@@ -233,6 +233,29 @@ def time_steps(calls, steps, warmup, stage_events=True):
     return total, per
 
 
+def interleave(a_calls, b_calls, n, warmup, rounds=3):
+    """Time two call sequences in alternating rounds (a, b, a, b, ...) of n
+    steps each, after warm-up of both: the part heats over a run, so two
+    sequences timed one after the other would see different clocks.
+    Returns (best a ms/step, best b ms/step, median per-round ratio b / a,
+    the per-round pairs)."""
+    for calls in (a_calls, b_calls):
+        for _ in range(warmup):
+            for f in calls:
+                f()
+    pairs = []
+    for _ in range(rounds):
+        t_a = time_steps(a_calls, n, 0, stage_events=False)[0] / n
+        t_b = time_steps(b_calls, n, 0, stage_events=False)[0] / n
+        pairs.append((t_a, t_b))
+    ratio = statistics.median(t_b / t_a for t_a, t_b in pairs)
+    return min(p[0] for p in pairs), min(p[1] for p in pairs), ratio, pairs
+
+
+def rounds_ms(pairs):
+    return [[round(a, 4), round(b, 4)] for a, b in pairs]
+
+
 def cpu_oracle_baseline(shape: BlockShape, target_s: float = 12.0, max_rows: int = 4096):
     """fp64 oracle fwd+bwd of the block on a row sample of the workload (full
     weights), timed on the host cores.  Returns a cpu_baseline dict."""
@@ -302,12 +325,12 @@ def bench_down_proj_swiglu_bwd(C, b, shape, steps, warmup):
         lambda: C.coda_gemm_dgrad_rmsbwd_cpart(b.dP, b.W2t, b.H, b.g, b.rstd, cpart, b.dH, b.dgpart),
     ]
     n = max(3, steps // 2)
-    t_hbm, _ = time_steps(through_hbm, n, warmup, stage_events=False)
-    t_chip, _ = time_steps(on_chip, n, warmup, stage_events=False)
+    t_chip, t_hbm, ratio, pairs = interleave(on_chip, through_hbm, n, warmup)
     flops = 2.0 * shape.M * shape.F * shape.d + 2.0 * shape.M * shape.N2 * shape.d
-    return {"what": "down-proj dgrad + SwiGLU bwd + dgrad2/RMSNorm bwd", "dY_through_hbm_ms": t_hbm / n,
-            "dY_on_chip_ms": t_chip / n, "speedup": t_hbm / t_chip,
-            "on_chip_tflops": flops / (t_chip / n * 1e-3) / 1e12}
+    return {"what": "down-proj dgrad + SwiGLU bwd + dgrad2/RMSNorm bwd", "dY_through_hbm_ms": t_hbm,
+            "dY_on_chip_ms": t_chip, "speedup": ratio, "on_chip_tflops": flops / (t_chip * 1e-3) / 1e12,
+            "rounds_ms": rounds_ms(pairs), "timing": "rounds of (on chip, through HBM) interleaved; speedup = "
+                                                   "median per-round time ratio"}
 
 
 def bench_fp8_forward(C, b, shape, steps, warmup, peak_bf16):
@@ -334,15 +357,16 @@ def bench_fp8_forward(C, b, shape, steps, warmup, peak_bf16):
     bf16 = fs.calls()[:fs.n_fwd]  # the bf16 forward stages
     n = max(3, steps)
     t_w, _ = time_steps(weights, n, warmup, stage_events=False)
-    t_8, per8 = time_steps(fp8, n, warmup, stage_events=True)
-    t_8, _ = time_steps(fp8, n, 0, stage_events=False)
-    t_16, _ = time_steps(bf16, n, warmup, stage_events=False)
+    _, per8 = time_steps(fp8, n, warmup, stage_events=True)
+    t_8, t_16, ratio, pairs = interleave(fp8, bf16, n, warmup)
     fl = shape.fwd_flops()
     names = ["quantize_X", "gemm1_res_prms_fp8", "rstd_combine", "quantize_H", "gemm2_rowscale_swiglu_fp8"]
     g2 = statistics.mean(per8[4])
-    return {"workload": shape.name + " forward", "fp8_fwd_ms": t_8 / n, "bf16_fwd_ms": t_16 / n,
-            "speedup": t_16 / t_8, "fp8_fwd_tflops": fl / (t_8 / n * 1e-3) / 1e12,
+    return {"workload": shape.name + " forward", "fp8_fwd_ms": t_8, "bf16_fwd_ms": t_16,
+            "speedup": ratio, "rounds_ms": rounds_ms(pairs), "fp8_fwd_tflops": fl / (t_8 * 1e-3) / 1e12,
             "weight_quantize_ms": t_w / n, "stage_ms": {k: statistics.mean(v) for k, v in zip(names, per8)},
+            "timing": "rounds of (fp8, bf16) interleaved; speedup = median per-round time ratio; stage_ms from "
+                      "a separate pass with an event between stages",
             "gemm2_fp8_tflops": 2.0 * shape.M * shape.N2 * shape.d / (g2 * 1e-3) / 1e12,
             "fp8_peak_tflops": 2 * peak_bf16,
             "gemm2_frac_of_fp8_peak": 2.0 * shape.M * shape.N2 * shape.d / (g2 * 1e-3) / 1e12 / (2 * peak_bf16),
@@ -358,12 +382,13 @@ def bench_fp8_fwdbwd(C, b, shape, steps, warmup, peak_bf16):
     calls = [f for _, f in named]
     t_w, _ = time_steps([b.fp8_quantize_weights], n, warmup, stage_events=False)
     _, per8 = time_steps(calls, n, warmup, stage_events=True)
-    t_8, _ = time_steps(calls, n, 0, stage_events=False)
-    t_16, _ = time_steps(FusedStep(C, b).calls(), n, warmup, stage_events=False)
+    t_8, t_16, ratio, pairs = interleave(calls, FusedStep(C, b).calls(), n, warmup)
     fl = shape.fwdbwd_flops()
-    return {"workload": shape.name, "fp8_fwdbwd_ms": t_8 / n, "bf16_fwdbwd_ms": t_16 / n, "speedup": t_16 / t_8,
-            "fp8_fwdbwd_tflops": fl / (t_8 / n * 1e-3) / 1e12, "weight_quantize_ms": t_w / n,
+    return {"workload": shape.name, "fp8_fwdbwd_ms": t_8, "bf16_fwdbwd_ms": t_16, "speedup": ratio,
+            "rounds_ms": rounds_ms(pairs), "fp8_fwdbwd_tflops": fl / (t_8 * 1e-3) / 1e12, "weight_quantize_ms": t_w / n,
             "stage_ms": {k: statistics.mean(v) for (k, _), v in zip(named, per8)},
+            "timing": "rounds of (fp8, bf16) interleaved; speedup = median per-round time ratio; stage_ms from a "
+                      "separate pass with an event between stages",
             "formats": "e4m3 activations and weights, e5m2 gradients (dP, dH), one fp32 scale per tensor"}
 
 
@@ -383,11 +408,12 @@ def bench_qkv_rope(C, steps, warmup, M=8192, S=2048, d=4096, n_heads=32):
     unfused = [lambda: C.coda_gemm(X, False, W, False, qkv, M, N, d),
                lambda: C.coda_rope_apply(qkv, cos_t, sin_t, n_heads, n_heads)]
     n = max(3, steps)
-    t_f, _ = time_steps(fused, n, warmup, stage_events=False)
-    t_u, _ = time_steps(unfused, n, warmup, stage_events=False)
+    t_f, t_u, ratio, pairs = interleave(fused, unfused, n, warmup)
     flops = 2.0 * M * N * d
-    return {"M": M, "d": d, "heads": n_heads, "head_dim": 128, "seq": S, "fused_ms": t_f / n,
-            "unfused_ms": t_u / n, "speedup": t_u / t_f, "fused_tflops": flops / (t_f / n * 1e-3) / 1e12}
+    return {"M": M, "d": d, "heads": n_heads, "head_dim": 128, "seq": S, "fused_ms": t_f,
+            "unfused_ms": t_u, "speedup": ratio, "fused_tflops": flops / (t_f * 1e-3) / 1e12,
+            "rounds_ms": rounds_ms(pairs), "timing": "rounds of (fused, unfused) interleaved; speedup = median "
+                                                   "per-round time ratio"}
 
 
 def bench_plain_vs_cublas(C, shape, steps, warmup):
@@ -675,28 +701,33 @@ def main():
                                    "value summed over ranks"}
         del host, pipe
     if not args.no_extras and rank == 0:
+        # Comparisons against the headline step are timed interleaved with it
+        # (rounds of fused / other, adjacent in time): the part heats over a
+        # run, and a leg timed once after the headline would see a hotter
+        # part than the headline did.
+        n_cmp = max(3, args.steps // 2)
+
         # the same step with g broadcast in GEMM1's epilogue (no fold pass over
-        # W2) and the combine inside GEMM2's epilogue, timed the same way
+        # W2) and the combine inside GEMM2's epilogue
         if not args.g_on_activation or not args.fuse_rstd:
             bv = BlockBuffers(x, backward=shape.backward, fuse_rstd=True, g_on_activation=True)
             vcalls = FusedStep(C, bv, fuse_rstd=True, g_on_activation=True).calls()
-            for _ in range(args.warmup):
-                for f in vcalls:
-                    f()
-            v_ms, _ = time_steps(vcalls, args.steps, 0, stage_events=False)
-            v_ms /= args.steps
+            _, v_ms, ratio, pairs = interleave(calls, vcalls, n_cmp, args.warmup)
             extras["variant_g_on_activation_fused_rstd"] = {
                 "ms_per_step": v_ms, "value": step_flops / (v_ms * 1e-3) / 1e12,
-                "pct_of_peak": 100.0 * step_flops / (v_ms * 1e-3) / 1e12 / peak, "launches_per_step": len(vcalls)}
+                "time_vs_headline_step": ratio, "rounds_ms": rounds_ms(pairs),
+                "timing": "rounds of (headline step, variant) interleaved; ratio = median per-round time ratio",
+                "launches_per_step": len(vcalls)}
             del bv, vcalls
             torch.cuda.empty_cache()
-        # unfused ablation, same workload and timing rules
+        # unfused ablation, same workload, interleaved the same way
         bu = BlockBuffers(x, unfused=True, backward=shape.backward)
         ucalls = [bu.forward_unfused, bu.backward_unfused] if shape.backward else [bu.forward_unfused]
-        u_ms, _ = time_steps(ucalls, max(3, args.steps // 2), args.warmup, stage_events=False)
-        u_ms /= max(3, args.steps // 2)
+        _, u_ms, ratio, pairs = interleave(calls, ucalls, n_cmp, args.warmup)
         extras["ablation_unfused"] = {"ms_per_step": u_ms, "tflops": step_flops / (u_ms * 1e-3) / 1e12,
-                                      "fused_speedup": u_ms / ms}
+                                      "fused_speedup": ratio, "rounds_ms": rounds_ms(pairs),
+                                      "timing": "rounds of (fused step, unfused step) interleaved; speedup = median "
+                                                "per-round time ratio"}
         del bu
         torch.cuda.empty_cache()
         if shape.backward:
