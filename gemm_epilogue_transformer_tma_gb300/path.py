@@ -60,7 +60,8 @@ class BlockBuffers:
         if backward:
             self.dP = torch.empty(M, N2, dtype=BF, **e)
             self.c = torch.empty(M, dtype=F32, **e)
-            self.dgpart = torch.empty(max(1, coda_dgpart_rows(M)), d, dtype=F32, **e)
+            # no rows for an empty batch: the dg combine then writes dg = 0
+            self.dgpart = torch.empty(coda_dgpart_rows(M), d, dtype=F32, **e)
             self.dH = torch.empty(M, d, dtype=BF, **e)
             self.dX = torch.empty(M, self.K1, dtype=BF, **e)
             self.dW1t = torch.empty(d, self.K1, dtype=BF, **e)

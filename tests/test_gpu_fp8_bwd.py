@@ -40,7 +40,8 @@ from gemm_epilogue_transformer_tma_gb300.path import BlockBuffers  # noqa: E402
 from tests.test_gpu_parity import pairing  # noqa: E402,F401
 
 EPS = 1e-5
-SHAPES = {"ragged": BlockShape("ragged", 300, 208, 336, 544), "whole": BlockShape("whole", 384, 256, 512, 1024)}
+SHAPES = {"ragged": BlockShape("ragged", 300, 208, 336, 544), "whole": BlockShape("whole", 384, 256, 512, 1024),
+          "one_row": BlockShape("one_row", 1, 64, 64, 128)}
 
 
 def deq(codes, scale_pair, fmt):
@@ -58,7 +59,7 @@ def run_fp8(s):
     return x, b
 
 
-@pytest.mark.parametrize("name", ["ragged", "whole"])
+@pytest.mark.parametrize("name", ["ragged", "whole", "one_row"])
 def test_fp8_backward_stages(name, pairing):
     s = SHAPES[name]
     x, b = run_fp8(s)
@@ -142,3 +143,20 @@ def test_swiglu_bwd_fp8_empty():
                           sc, torch.empty(0, device="cuda"), 64)
     torch.cuda.synchronize()
     assert sc.tolist() == [0.0, 1.0]
+
+
+def test_fp8_empty_batch():
+    """M = 0 through the whole FP8 step: the weight gradients are empty sums
+    (zero), dg is zero, and the activation / gradient scales are {0, 1}."""
+    s = BlockShape("empty", 0, 64, 64, 128)
+    b = BlockBuffers({k: v.cuda() for k, v in block_inputs(s, 0, "cpu").items()})
+    b.fp8_quantize_weights()
+    for t in (b.dW2t, b.dW1t, b.dg):
+        t.fill_(1.0)
+    b.s_a.fill_(7.0)
+    b.step_fp8()
+    torch.cuda.synchronize()
+    assert_device_ok()
+    for t in (b.dW2t, b.dW1t, b.dg):
+        assert torch.count_nonzero(t) == 0
+    assert b.s_a.tolist() == [[0.0, 1.0]] * 4

@@ -202,6 +202,13 @@ def test_empty_batch_is_a_no_op():
     b.step()
     assert_device_ok()
     assert torch.count_nonzero(b.dW2t) == 0 and torch.count_nonzero(b.dg) == 0
+    # the same through the stage calls (dgpart has no rows; the combine writes dg = 0)
+    b.dW2t.fill_(1.0)
+    b.dg.fill_(1.0)
+    b.forward()
+    b.backward_stages()
+    assert_device_ok()
+    assert torch.count_nonzero(b.dW2t) == 0 and torch.count_nonzero(b.dg) == 0
 
 
 def test_argument_errors():
