@@ -102,3 +102,29 @@ def test_ce_argmax_ties_pick_lowest_column():
     o = run_ce(H.cuda(), Wt.cuda(), lab.cuda(), grads=False)
     assert_device_ok()
     assert np.array_equal(o["argmax"].cpu().numpy(), O.argmax_lowest(L))
+
+
+def test_ce_large_logits_and_edge_labels(pairing):
+    """Logits of several hundred (exp overflows fp32 past about 88 unless the
+    running maximum is subtracted): the blocked statistics and the backward's
+    exp(L - lse) must stay finite and match the oracle; labels on the first
+    and last vocabulary columns (the last one in the ragged last tile)."""
+    s = CEShape("t", 96, 136, 1000)
+    x = ce_inputs(s, 3)
+    H = (x["H"].float() * 400).to(torch.bfloat16)
+    lab = x["labels"].clone()
+    lab[0], lab[1], lab[2] = 0, s.V - 1, s.V - 1
+    o = run_ce(H.cuda(), x["Wt"].cuda(), lab.cuda())
+    assert_device_ok()
+    Hf, Wt, y = f64(H), f64(x["Wt"]), lab.numpy()
+    L = O.logits_rows(Hf, Wt)
+    assert np.abs(L).max() > 200
+    fw = O.ce_forward(Hf, Wt, y)
+    bw = O.ce_backward(Hf, Wt, y)
+    for k in ("lse", "dH", "dW"):
+        assert torch.isfinite(o[k].float()).all(), k
+    assert_elem(o["lse"], fw["lse"], "lse (large logits)", tol=1e-4)
+    assert abs(o["loss"].item() - fw["loss"]) <= 1e-4 * abs(fw["loss"])
+    check_argmax(o["argmax"], Hf, Wt)
+    assert_frob(o["dH"], bw["dH"], "dH (large logits)")
+    assert_frob(o["dW"], bw["dWt"], "dW (large logits)")
