@@ -87,6 +87,7 @@ SIGNATURES = {
     "coda_gemm_rowscale_swiglu_fp8": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _U32, _P]),
     "coda_lmhead_ce_workspace_bytes": (_SZ, [_I64, _I64, _I64, _INT]),
     "coda_lmhead_ce": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I64, _I64, _I64, _P]),
+    "coda_lmhead_ce_fp8": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I64, _I64, _I64, _P]),
     "coda_unfused_workspace_bytes": (_SZ, [_I64, _I64, _I64]),
     "coda_unfused_fwd": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
                                 _I64, _I64, _I64, _I64, _F32, _U32, _P]),
@@ -589,6 +590,28 @@ def coda_lmhead_ce(Hs, Wt, labels, loss, lse, argmax, dHs, dWt, ws, stream=None)
         _h(Hs), _ptr(Hs, BF, "Hs"), _ptr(Wt, BF, "Wt"), _ptr(labels, I32, "labels"), _ptr(loss, F32, "loss"),
         _ptr(lse, F32, "lse"), _ptr(argmax, I32, "argmax"), _ptr(dHs, BF, "dHs"), _ptr(dWt, BF, "dWt"),
         _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), M, d, V, _stream(stream)), "coda_lmhead_ce")
+
+
+def coda_lmhead_ce_fp8(Hq, sH, Wq, sW, labels, loss, lse, argmax, dHs, dWt, ws, stream=None):
+    """coda_lmhead_ce on e4m3 codes of H and W (scales sH, sW: the scale
+    element of coda_fp8_quantize's {amax, scale}); dL kept as e5m2 codes in
+    the backward (see include/coda.h)."""
+    M, d = Hq.shape
+    V = Wq.shape[0]
+    _shape(Wq, (V, d), "Wq")
+    _shape(labels, (M,), "labels")
+    _shape(loss, (1,), "loss")
+    _shape(lse, (M,), "lse")
+    if argmax is not None:
+        _shape(argmax, (M,), "argmax")
+    if dHs is not None:
+        _shape(dHs, (M, d), "dHs")
+        _shape(dWt, (V, d), "dWt")
+    _check(load_library().coda_lmhead_ce_fp8(
+        _h(Hq), _ptr(Hq, U8, "Hq"), _ptr(sH, F32, "sH"), _ptr(Wq, U8, "Wq"), _ptr(sW, F32, "sW"),
+        _ptr(labels, I32, "labels"), _ptr(loss, F32, "loss"), _ptr(lse, F32, "lse"), _ptr(argmax, I32, "argmax"),
+        _ptr(dHs, BF, "dHs"), _ptr(dWt, BF, "dWt"), _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), M, d, V,
+        _stream(stream)), "coda_lmhead_ce_fp8")
 
 
 def coda_unfused_workspace_bytes(M: int, d: int, N2: int) -> int:

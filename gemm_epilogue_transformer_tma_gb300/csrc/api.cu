@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdint>
 #include <mutex>
 
@@ -52,6 +53,7 @@ LaunchCtx ctx_of(coda_handle_t h, void* stream) {
   c.scale_a = nullptr;
   c.scale_b = nullptr;
   c.f8_fmt = 0;
+  c.scale_host = 1.f;
   return c;
 }
 
@@ -143,6 +145,10 @@ bool make_tmap_store(CUtensorMap* m, CUtensorMapDataType type, uint32_t esize, C
 
 bool make_tmap_store_bf16(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t ld) {
   return make_tmap_store(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, CU_TENSOR_MAP_SWIZZLE_64B, base, cols, rows, ld);
+}
+
+bool make_tmap_store_u8_sw32(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t ld) {
+  return make_tmap_store(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, CU_TENSOR_MAP_SWIZZLE_32B, base, cols, rows, ld);
 }
 
 bool make_tmap_store_f32(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t ld) {
@@ -820,6 +826,64 @@ coda_status_t coda_lmhead_ce(coda_handle_t h, const void* Hs, const void* Wt, co
     // Hs[m][k], one grouped launch
     CODA_CUDA(gemm_group_ce_bwd(cx, w.dL, Wc, Hb, w.dH32, v0 > 0, static_cast<bf16*>(dWt) + v0 * d, int(M), int(d),
                                 int(Vc)));
+  }
+  CODA_CUDA(launch_f32_to_bf16(cx, w.dH32, static_cast<bf16*>(dHs), M * d));
+  return CODA_OK;
+}
+
+coda_status_t coda_lmhead_ce_fp8(coda_handle_t h, const void* Hq, const float* sH, const void* Wq, const float* sW,
+                                 const int32_t* labels, float* loss, float* lse, int32_t* argmax, void* dHs,
+                                 void* dWt, void* ws, size_t ws_bytes, int64_t M, int64_t d, int64_t V,
+                                 void* stream) {
+  CODA_TRY(Check()
+               .handle(h)
+               .ptr(Hq)
+               .sptr(sH)
+               .ptr(Wq)
+               .sptr(sW)
+               .ptr(labels)
+               .ptr(loss)
+               .ptr(lse)
+               .opt_ptr(argmax)
+               .opt_ptr(dHs)
+               .opt_ptr(dWt)
+               .ptr(ws)
+               .rows(M)
+               .cols(d)
+               .cols(V)
+               .st);
+  if (M == 0) return CODA_ERR_INVALID_ARG;  // the mean over no rows is undefined
+  if (d % 16 != 0 || V % 16 != 0) return CODA_ERR_ALIGNMENT;
+  const bool grads = dHs != nullptr;
+  if (grads != (dWt != nullptr)) return CODA_ERR_INVALID_ARG;
+  if (ws_bytes < coda_lmhead_ce_workspace_bytes(M, d, V, grads)) return CODA_ERR_WORKSPACE_TOO_SMALL;
+  const CeWs w = ce_layout(static_cast<uint8_t*>(ws), M, d, V, grads);
+  const int64_t T = cdiv(V, ce_tile_cols());
+  const LaunchCtx cx = ctx_of(h, stream);
+  const uint8_t* Hc = static_cast<const uint8_t*>(Hq);
+  const uint8_t* Wc8 = static_cast<const uint8_t*>(Wq);
+  CODA_CUDA(cudaMemsetAsync(w.zy, 0, size_t(M) * 4, cx.stream));
+  CODA_CUDA(gemm_ce_stats_fp8(cx, Hc, sH, Wc8, sW, labels, w.pmax, w.psum, w.parg, w.zy, int(M), int(d), int(V),
+                              int(T)));
+  CODA_CUDA(launch_ce_combine(cx, w.pmax, w.psum, w.parg, w.zy, labels, M, T, V, lse, argmax, w.row_loss));
+  CODA_CUDA(launch_mean(cx, w.row_loss, M, loss));
+  if (!grads) return CODA_OK;
+  const float inv_M = 1.0f / static_cast<float>(M);
+  // |dL| <= 1/M: the smallest power of two s with (1/M) / s <= 57344
+  // (= 0.875 * 2^16), so the e5m2 codes of dL / s never saturate
+  int ea = 0;
+  const float ma = std::frexp(inv_M, &ea);
+  const int k = std::max(-126, ea - 16 + (ma > 0.875f ? 1 : 0));
+  const float s_dL = std::ldexp(1.0f, k);
+  const float code_inv = std::ldexp(1.0f, -k);
+  uint8_t* dLq = reinterpret_cast<uint8_t*>(w.dL);  // the bf16 chunk buffer holds the 1-byte codes
+  for (int64_t v0 = 0; v0 < V; v0 += kCeChunk) {
+    const int64_t Vc = std::min<int64_t>(kCeChunk, V - v0);
+    const uint8_t* Wqc = Wc8 + v0 * d;
+    CODA_CUDA(gemm_ce_grad_fp8(cx, Hc, sH, Wqc, sW, labels, lse, dLq, code_inv, int(M), int(d), int(Vc), int(v0),
+                               inv_M));
+    CODA_CUDA(gemm_ce_bwd_fp8(cx, dLq, s_dL, Wqc, sW, Hc, sH, w.dH32, v0 > 0, static_cast<bf16*>(dWt) + v0 * d,
+                              int(M), int(d), int(Vc)));
   }
   CODA_CUDA(launch_f32_to_bf16(cx, w.dH32, static_cast<bf16*>(dHs), M * d));
   return CODA_OK;

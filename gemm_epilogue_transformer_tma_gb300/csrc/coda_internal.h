@@ -20,6 +20,7 @@ struct LaunchCtx {
   const float* scale_a;  // FP8 operands: device pointers to the per-tensor scales
   const float* scale_b;
   uint32_t f8_fmt;       // FP8 operands: format bits of A and B (f8_format_bits; 0 = both e4m3)
+  float scale_host;      // FP8 operands: a further accumulator scale known on the host (1 otherwise)
 };
 
 // 2-D bf16 tensor map with 128-byte swizzle.  The tensor is `outer` rows of
@@ -33,6 +34,8 @@ bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t o
 // 128-byte swizzle), matching the staging layout of the GEMM epilogue.
 bool make_tmap_store_bf16(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t ld);
 bool make_tmap_store_f32(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t ld);
+// 1-byte codes (32 x 32 boxes, 32-byte swizzle), matching stage_e5m2x32
+bool make_tmap_store_u8_sw32(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t ld);
 // The same for 1-byte elements (e4m3 codes): box_inner <= 128.
 bool make_tmap_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t ld, uint32_t box_inner,
                   uint32_t box_outer);
@@ -154,6 +157,19 @@ cudaError_t gemm_dgrad_rms_fp8(const LaunchCtx& c, const uint8_t* dPq, int dp_fm
                                const uint8_t* W2q, int w_fmt, const float* sW2, const __nv_bfloat16* H,
                                const __nv_bfloat16* g, const float* cvec, __nv_bfloat16* dH, float* dgpart, int M,
                                int N2, int d);
+
+// LM-head GEMMs on 8-bit operands: the statistics GEMM on e4m3 H and W
+// codes; the chunk's recomputed logits writing dL as e5m2 codes of
+// dL * code_inv; the chunk's dH (+)= and dW GEMMs on those codes (scale s_dL)
+cudaError_t gemm_ce_stats_fp8(const LaunchCtx& c, const uint8_t* Hq, const float* sH, const uint8_t* Wq,
+                              const float* sW, const int32_t* labels, float* pmax, float* psum, int32_t* parg,
+                              float* zy, int M, int d, int V, int T);
+cudaError_t gemm_ce_grad_fp8(const LaunchCtx& c, const uint8_t* Hq, const float* sH, const uint8_t* Wq_chunk,
+                             const float* sW, const int32_t* labels, const float* lse, uint8_t* dLq, float code_inv,
+                             int M, int d, int Vc, int v0, float inv_M);
+cudaError_t gemm_ce_bwd_fp8(const LaunchCtx& c, const uint8_t* dLq, float s_dL, const uint8_t* Wq_chunk,
+                            const float* sW, const uint8_t* Hq, const float* sH, float* dH32, bool accumulate,
+                            __nv_bfloat16* dWc, int M, int d, int Vc);
 
 int ce_tile_cols();    // vocabulary columns per CE statistics tile
 int prms_tile_cols();  // columns per partial-RMS tile of GEMM1

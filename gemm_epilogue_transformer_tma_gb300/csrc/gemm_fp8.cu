@@ -116,4 +116,70 @@ cudaError_t gemm_dgrad_rms_fp8(const LaunchCtx& c0, const uint8_t* dPq, int dp_f
   return run_gemm<false, true, false, EpiDgradRms, true>(c, ta, tb, tb, M, d, N2, (d + kBN - 1) / kBN, ep);
 }
 
+// LM-head statistics GEMM on e4m3 operands: logits = sH * sW * (Hq Wq^T),
+// the blocked log-sum-exp epilogue as in the bf16 form.
+cudaError_t gemm_ce_stats_fp8(const LaunchCtx& c0, const uint8_t* Hq, const float* sH, const uint8_t* Wq,
+                              const float* sW, const int32_t* labels, float* pmax, float* psum, int32_t* parg,
+                              float* zy, int M, int d, int V, int T) {
+  LaunchCtx c = c0;
+  c.scale_a = sH;
+  c.scale_b = sW;
+  c.f8_fmt = f8_format_bits(0, 0);
+  CUtensorMap ta, tb;
+  if (!make_fp8_maps(&ta, &tb, Hq, Wq, M, V, d, b_box_rows(c))) return cudaErrorInvalidValue;
+  EpiCeStats::Params ep{labels, pmax, psum, parg, zy, T, c.status};
+  return run_gemm<false, false, false, EpiCeStats, true>(c, ta, tb, tb, M, V, d, (V + kBN - 1) / kBN, ep);
+}
+
+// The recomputed logits of one vocabulary chunk on e4m3 operands, dL written
+// as e5m2 codes of dL * code_inv into dLq [M][Vc].
+cudaError_t gemm_ce_grad_fp8(const LaunchCtx& c0, const uint8_t* Hq, const float* sH, const uint8_t* Wq_chunk,
+                             const float* sW, const int32_t* labels, const float* lse, uint8_t* dLq, float code_inv,
+                             int M, int d, int Vc, int v0, float inv_M) {
+  LaunchCtx c = c0;
+  c.scale_a = sH;
+  c.scale_b = sW;
+  c.f8_fmt = f8_format_bits(0, 0);
+  CUtensorMap ta, tb;
+  if (!make_fp8_maps(&ta, &tb, Hq, Wq_chunk, M, Vc, d, b_box_rows(c))) return cudaErrorInvalidValue;
+  EpiCeGrad::Params ep{};
+  if (!make_tmap_store_u8_sw32(&ep.dL, dLq, Vc, M, Vc)) return cudaErrorInvalidValue;
+  ep.labels = labels;
+  ep.lse = lse;
+  ep.inv_M = inv_M;
+  ep.v0 = v0;
+  ep.codes = 1;
+  ep.code_inv = code_inv;
+  return run_gemm<false, false, false, EpiCeGrad, true>(c, ta, tb, tb, M, Vc, d, (Vc + kBN - 1) / kBN, ep);
+}
+
+// The chunk's two gradient GEMMs on the e5m2 dL codes (scale s_dL, known on
+// the host) and the e4m3 codes of W and H:
+//   dH32 [M][d] (+)= s_dL * sW * dLq Wq_chunk    (dLq K-major, Wq_chunk [Vc][d] read MN-major)
+//   dWc [Vc][d] = s_dL * sH * dLq^T Hq           (both read MN-major, K = M)
+cudaError_t gemm_ce_bwd_fp8(const LaunchCtx& c0, const uint8_t* dLq, float s_dL, const uint8_t* Wq_chunk,
+                            const float* sW, const uint8_t* Hq, const float* sH, float* dH32, bool accumulate,
+                            __nv_bfloat16* dWc, int M, int d, int Vc) {
+  LaunchCtx c = c0;
+  c.scale_a = nullptr;
+  c.scale_host = s_dL;
+  c.scale_b = sW;
+  c.f8_fmt = f8_format_bits(1, 0);
+  CUtensorMap ta, tb;
+  if (!make_f8_operand_map(&ta, dLq, false, M, Vc, BM)) return cudaErrorInvalidValue;
+  if (!make_f8_operand_map(&tb, Wq_chunk, true, d, Vc, b_box_rows(c))) return cudaErrorInvalidValue;
+  EpiStoreF32::Params e0{};
+  if (!make_tmap_store_f32(&e0.out, dH32, d, M, d)) return cudaErrorInvalidValue;
+  e0.beta = accumulate ? 1 : 0;
+  const int tn = (d + kBN - 1) / kBN;
+  cudaError_t e = run_gemm<false, true, false, EpiStoreF32, true>(c, ta, tb, tb, M, d, Vc, tn, e0);
+  if (e != cudaSuccess) return e;
+  c.scale_b = sH;
+  if (!make_f8_operand_map(&ta, dLq, true, Vc, M, BM)) return cudaErrorInvalidValue;
+  if (!make_f8_operand_map(&tb, Hq, true, d, M, b_box_rows(c))) return cudaErrorInvalidValue;
+  EpiStore::Params e1{};
+  if (!make_tmap_store_bf16(&e1.out, dWc, d, Vc, d)) return cudaErrorInvalidValue;
+  return run_gemm<true, true, false, EpiStore, true>(c, ta, tb, tb, Vc, d, M, tn, e1);
+}
+
 }  // namespace coda

@@ -69,7 +69,7 @@ cudaError_t launch_group(const LaunchCtx& c, GroupArgs<Epi0, Epi1>& g) {
   const int tiles = g.sh0.tiles_m * g.sh0.tiles_n + g.sh1.tiles_m * g.sh1.tiles_n;
   const int P = std::max(1, std::min(tiles, max_pairs[dev]));
   g.sched = make_sched(g.sh0, g.sh1, P);
-  KernelCtl ctl{c.status, c.timeout_ns, c.skip_first_stage, nullptr, nullptr, 0u};
+  KernelCtl ctl{c.status, c.timeout_ns, c.skip_first_stage, nullptr, nullptr, 0u, 1.f};
   return launch_chained(c, kern, dim3(2 * P), dim3(gemm_threads<Epi0>()), L::TOTAL, g, ctl);
 }
 }  // namespace

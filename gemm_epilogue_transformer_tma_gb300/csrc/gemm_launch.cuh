@@ -26,7 +26,7 @@ cudaError_t launch_gemm_kernel(const LaunchCtx& c, const CUtensorMap& ta, const 
   sh.tiles_n = tiles_n;
   sh.num_kb = (K + (FP8 ? 128 : BK) - 1) / (FP8 ? 128 : BK);
   sh.group_m = 8;
-  KernelCtl ctl{c.status, c.timeout_ns, c.skip_first_stage, c.scale_a, c.scale_b, c.f8_fmt};
+  KernelCtl ctl{c.status, c.timeout_ns, c.skip_first_stage, c.scale_a, c.scale_b, c.f8_fmt, c.scale_host};
   const int tiles = sh.tiles_m * sh.tiles_n;
   const int grid = std::max(1, std::min(tiles, c.num_sms));
   return launch_chained(c, kern, dim3(grid), dim3(gemm_threads<Epi>()), L::TOTAL, ta, tb, tb2, sh, ctl, ep);
@@ -48,7 +48,7 @@ cudaError_t launch_gemm2_kernel(const LaunchCtx& c, const CUtensorMap& ta, const
   sh.tiles_n = tiles_n;
   sh.num_kb = (K + (FP8 ? 128 : BK) - 1) / (FP8 ? 128 : BK);
   sh.group_m = 8;
-  KernelCtl ctl{c.status, c.timeout_ns, c.skip_first_stage, c.scale_a, c.scale_b, c.f8_fmt};
+  KernelCtl ctl{c.status, c.timeout_ns, c.skip_first_stage, c.scale_a, c.scale_b, c.f8_fmt, c.scale_host};
   // co-resident SM pairs for this kernel (not every TPC need have both SMs
   // enabled); queried once per instantiation and device
   static int max_pairs[64] = {};

@@ -43,6 +43,8 @@
 // returns.
 #pragma once
 
+#include <cuda_fp8.h>
+
 #include "ptx.cuh"
 
 namespace coda {
@@ -69,13 +71,14 @@ struct KernelCtl {
   const float* scale_a;  // FP8 operands: per-tensor dequantisation scales (null = 1)
   const float* scale_b;
   uint32_t f8_fmt;       // FP8 operands: format bits of A and B (f8_format_bits)
+  float scale_host;      // FP8 operands: a scale known on the host (1 otherwise)
 };
 
 // The accumulator's scale: the product of the operands' per-tensor scales
 // (1 for bf16 operands).  Read after griddep_wait (a previous kernel may have
 // produced the scales).
 __device__ __forceinline__ float acc_scale_of(const KernelCtl& ctl) {
-  float s = 1.f;
+  float s = ctl.scale_host;
   if (ctl.scale_a != nullptr) s *= *ctl.scale_a;
   if (ctl.scale_b != nullptr) s *= *ctl.scale_b;
   return s;
@@ -434,6 +437,28 @@ __device__ __forceinline__ void stage_f32x32(uint32_t slot, int lane, const floa
                  __float_as_uint(f[4 * q + 1]), __float_as_uint(f[4 * q + 2]), __float_as_uint(f[4 * q + 3]));
 }
 
+// e5m2 block: 32 rows x 32 codes of f * inv (saturating, round to nearest
+// even), 32-byte rows, 32-byte swizzle: the 16-byte chunk q of row r sits at
+// chunk position q ^ ((r >> 2) & 1).
+__device__ __forceinline__ void stage_e5m2x32(uint32_t slot, int lane, const float (&f)[32], float inv) {
+  const uint32_t row = slot + static_cast<uint32_t>(lane) * 32u;
+  const uint32_t sw = (static_cast<uint32_t>(lane) >> 2) & 1u;
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    uint32_t w[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int i = 16 * q + 4 * j;
+      const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(f[i] * inv, f[i + 1] * inv), __NV_SATFINITE,
+                                                   __NV_E5M2);
+      const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(f[i + 2] * inv, f[i + 3] * inv), __NV_SATFINITE,
+                                                   __NV_E5M2);
+      w[j] = (lo & 0xFFFFu) | (hi << 16);
+    }
+    st_shared_v4(row + ((static_cast<uint32_t>(q) ^ sw) << 4), w[0], w[1], w[2], w[3]);
+  }
+}
+
 __device__ __forceinline__ void slots_acquire(int lane) {
   if (lane == 0) bulk_wait_group_read0();
   __syncwarp();
@@ -549,7 +574,7 @@ struct EpiStore {
 struct EpiStoreF32 {
   static constexpr int kEpiWarps = 4;
   static constexpr int kStoreSlots = 2;  // one 4 KB fp32 block
-  static constexpr bool kAccScale = false;  // ignores EpiCtx::acc_scale: bf16 operands only
+  static constexpr bool kAccScale = true;  // multiplies by EpiCtx::acc_scale: usable on FP8 operands
   struct Params {
     CUtensorMap out;  // [M][N] fp32
     int beta;
@@ -562,6 +587,8 @@ struct EpiStoreF32 {
       tmem_ld32(c.taddr + cc, v);
       const int n0 = c.tn * BN + cc;
       if (n0 < c.N && c.m0 < c.M) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] *= c.acc_scale;
         slots_acquire(c.lane);
         stage_f32x32(slot_addr(c, 0), c.lane, v);
         slots_publish();
@@ -919,7 +946,7 @@ struct EpiRope {
 struct EpiCeStats {
   static constexpr int kEpiWarps = 4;
   static constexpr int kStoreSlots = 0;
-  static constexpr bool kAccScale = false;  // ignores EpiCtx::acc_scale: bf16 operands only
+  static constexpr bool kAccScale = true;  // multiplies by EpiCtx::acc_scale: usable on FP8 operands
   struct Params {
     const int32_t* labels;
     float* pmax;
@@ -943,6 +970,8 @@ struct EpiCeStats {
       tmem_ld32(c.taddr + cc, v);
       const int n0 = c.tn * BN + cc;
       if (row_ok && n0 < c.N) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] *= c.acc_scale;
         const int nv = c.N - n0;
         float cmax = -INFINITY;
         int carg = -1;
@@ -981,18 +1010,22 @@ struct EpiCeStats {
   }
 };
 
-// LM-head backward epilogue: dL = (exp(L - lse[m]) - [n == y_m]) / M as bf16
-// into a vocabulary-chunk buffer (column n of the chunk = vocabulary v0 + n).
+// LM-head backward epilogue: dL = (exp(L - lse[m]) - [n == y_m]) / M into a
+// vocabulary-chunk buffer (column n of the chunk = vocabulary v0 + n), as bf16
+// or, with FP8 operands, as e5m2 codes of dL * code_inv (|dL| <= 1/M, so a
+// power-of-two scale fixed in advance never saturates).
 struct EpiCeGrad {
   static constexpr int kEpiWarps = 4;
   static constexpr int kStoreSlots = 1;
-  static constexpr bool kAccScale = false;  // ignores EpiCtx::acc_scale: bf16 operands only
+  static constexpr bool kAccScale = true;  // multiplies by EpiCtx::acc_scale: usable on FP8 operands
   struct Params {
-    CUtensorMap dL;  // [M][Vc] bf16
+    CUtensorMap dL;  // [M][Vc] bf16, or e5m2 codes when codes != 0
     const int32_t* labels;
     const float* lse;
     float inv_M;
     int v0;
+    int codes;
+    float code_inv;  // the inverse of the codes' power-of-two scale
   };
   template <int BN>
   static __device__ __forceinline__ void run(const Params& p, const EpiCtx& c) {
@@ -1007,11 +1040,14 @@ struct EpiCeGrad {
       if (n0 < c.N && c.m0 < c.M) {
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const float e = __expf(v[i] - l) - ((n0 + i == y) ? 1.f : 0.f);
+          const float e = __expf(v[i] * c.acc_scale - l) - ((n0 + i == y) ? 1.f : 0.f);
           v[i] = e * p.inv_M;
         }
         slots_acquire(c.lane);
-        stage_bf16x32(slot_addr(c, 0), c.lane, v);
+        if (p.codes)
+          stage_e5m2x32(slot_addr(c, 0), c.lane, v, p.code_inv);
+        else
+          stage_bf16x32(slot_addr(c, 0), c.lane, v);
         slots_publish();
         if (c.lane == 0) {
           tma_store_2d(&p.dL, slot_addr(c, 0), n0, c.m0);

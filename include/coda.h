@@ -447,6 +447,22 @@ coda_status_t coda_lmhead_ce(coda_handle_t h, const void* Hs, const void* Wt, co
                              float* lse, int32_t* argmax, void* dHs, void* dWt, void* ws, size_t ws_bytes, int64_t M,
                              int64_t d, int64_t V, void* stream);
 
+/* coda_lmhead_ce on 8-bit operands (the FP8 variant of the same epilogue
+ * programs): Hq e4m3 codes [M][d] with scale *sH and Wq e4m3 codes [V][d]
+ * with scale *sW (coda_fp8_quantize), so L = sH * sW * Hq Wq^T; the
+ * statistics, loss, lse and argmax as coda_lmhead_ce.  The backward keeps the
+ * recomputed dL = (softmax - onehot)/M of each vocabulary chunk as e5m2 codes
+ * with the power-of-two scale s = 2^k fixed by |dL| <= 1/M (the smallest with
+ * (1/M) / s <= 57344, so no code saturates), and forms dHs = dL Wt and dWt =
+ * dL^T Hs from those codes and the e4m3 codes of W and H (fp32 accumulation
+ * across chunks for dHs).  Same outputs and workspace
+ * (coda_lmhead_ce_workspace_bytes) as coda_lmhead_ce; d and V multiples of 16
+ * (CODA_ERR_ALIGNMENT otherwise). */
+coda_status_t coda_lmhead_ce_fp8(coda_handle_t h, const void* Hq, const float* sH, const void* Wq, const float* sW,
+                                 const int32_t* labels, float* loss, float* lse, int32_t* argmax, void* dHs,
+                                 void* dWt, void* ws, size_t ws_bytes, int64_t M, int64_t d, int64_t V,
+                                 void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* unfused ablation: the same GEMM kernel with standalone memory-bound       */
 /* kernels in between (the "three separate operators" baseline of section    */

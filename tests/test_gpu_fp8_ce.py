@@ -1,0 +1,108 @@
+"""LM-head cross-entropy on FP8 operands (the FP8 variant of the blocked
+log-sum-exp and softmax-gradient epilogue programs): e4m3 codes of H and W,
+the recomputed dL of each vocabulary chunk kept as e5m2 codes with the
+power-of-two scale fixed by |dL| <= 1/M.
+
+  * against the oracle fed the GPU's own H / W codes: lse (elementwise),
+    loss, argmax; dH and dW against the oracle's dL (fp64, from the
+    dequantised logits) quantised to e5m2 with the same scale, then the two
+    contractions (Frobenius: a code that rounds the other way at a tie of
+    the fp32 and fp64 dL is invisible there);
+  * end to end against the oracle on the bf16 inputs, within bounds from the
+    formats' rounding error (e4m3 3.6 %, e5m2 7.2 % rms per element).
+
+Method: "CODA: Rewriting Transformer Blocks as GEMM-Epilogue Programs"
+(Synced write-up, sections 五种积木: block log-sum-exp; 背景: FP8).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from coda_inputs import CEShape, ce_inputs
+from tests._parity import assert_device_ok, assert_elem, assert_frob, f64
+from tests.test_gpu_ce import check_argmax, pairing  # noqa: F401
+
+pytestmark = pytest.mark.gpu
+
+C = pytest.importorskip("gemm_epilogue_transformer_tma_gb300")
+
+
+def quantize(x):
+    q = torch.empty(x.shape, dtype=torch.uint8, device="cuda")
+    s = torch.empty(2, device="cuda")
+    C.coda_fp8_quantize(x, q, s)
+    return q, s
+
+
+def deq(q, s, fmt="e4m3"):
+    return O.fp8_decode(q.cpu().numpy(), fmt) * float(s[1].item())
+
+
+def run_fp8_ce(Hq, sH, Wq, sW, labels, grads=True):
+    M, d = Hq.shape
+    V = Wq.shape[0]
+    ws = torch.empty(C.coda_lmhead_ce_workspace_bytes(M, d, V, grads), dtype=torch.uint8, device="cuda")
+    o = dict(loss=torch.empty(1, device="cuda"), lse=torch.empty(M, device="cuda"),
+             argmax=torch.empty(M, dtype=torch.int32, device="cuda"))
+    o["dH"] = torch.empty(M, d, dtype=torch.bfloat16, device="cuda") if grads else None
+    o["dW"] = torch.empty(V, d, dtype=torch.bfloat16, device="cuda") if grads else None
+    C.coda_lmhead_ce_fp8(Hq, sH[1:], Wq, sW[1:], labels, o["loss"], o["lse"], o["argmax"], o["dH"], o["dW"], ws)
+    return o
+
+
+@pytest.mark.parametrize("M,d,V", [(200, 144, 1008), (37, 256, 40000)])
+def test_fp8_ce_parity(M, d, V, pairing):
+    s = CEShape("t", M, d, V)
+    x = {k: v.cuda() for k, v in ce_inputs(s, 0).items()}
+    Hq, sH = quantize(x["H"])
+    Wq, sW = quantize(x["Wt"])
+    o = run_fp8_ce(Hq, sH, Wq, sW, x["labels"])
+    torch.cuda.synchronize()
+    assert_device_ok()
+    Hd, Wd, y = deq(Hq, sH), deq(Wq, sW), x["labels"].cpu().numpy()
+    fw = O.ce_forward(Hd, Wd, y)
+    assert_elem(o["lse"], fw["lse"], "lse (fp8)", tol=1e-4)
+    assert abs(o["loss"].item() - fw["loss"]) <= 1e-4 * abs(fw["loss"])
+    check_argmax(o["argmax"], Hd, Wd)
+    # the backward's dL as the GPU keeps it: e5m2 codes with the scale fixed
+    # by |dL| <= 1/M
+    L = O.logits_rows(Hd, Wd)
+    P = np.exp(L - fw["lse"][:, None])
+    P[np.arange(M), y] -= 1.0
+    dL = P / M
+    s_dL = O.fp8_scale(np.array([1.0 / M], np.float32), "e5m2")
+    assert np.max(np.abs(dL)) <= 1.0 / M
+    dLd = O.fp8_decode(O.fp8_quantize(dL, s_dL, "e5m2"), "e5m2") * float(s_dL)
+    assert_frob(o["dH"], dLd @ Wd, "dH (fp8, e5m2 dL)")
+    assert_frob(o["dW"], dLd.T @ Hd, "dW (fp8, e5m2 dL)")
+    # end to end against the bf16 inputs
+    Hb, Wb = f64(x["H"]), f64(x["Wt"])
+    fb = O.ce_forward(Hb, Wb, y)
+    bb = O.ce_backward(Hb, Wb, y)
+    assert abs(o["loss"].item() - fb["loss"]) <= 1e-2 * abs(fb["loss"])
+    assert_frob(o["dH"], bb["dH"], "dH fp8 e2e", tol=0.15)
+    assert_frob(o["dW"], bb["dWt"], "dW fp8 e2e", tol=0.15)
+
+
+def test_fp8_ce_forward_only_and_argument_errors():
+    s = CEShape("t", 64, 64, 512)
+    x = {k: v.cuda() for k, v in ce_inputs(s, 1).items()}
+    Hq, sH = quantize(x["H"])
+    Wq, sW = quantize(x["Wt"])
+    o = run_fp8_ce(Hq, sH, Wq, sW, x["labels"], grads=False)
+    torch.cuda.synchronize()
+    assert_device_ok()
+    fw = O.ce_forward(deq(Hq, sH), deq(Wq, sW), x["labels"].cpu().numpy())
+    assert_elem(o["lse"], fw["lse"], "lse (fp8, forward only)", tol=1e-4)
+    lib = C.load_library()
+    h = C.handle()
+    st = torch.cuda.current_stream().cuda_stream
+    ws = torch.empty(C.coda_lmhead_ce_workspace_bytes(64, 64, 512, 1), dtype=torch.uint8, device="cuda")
+    out = torch.empty(64, device="cuda")
+    args = [Hq.data_ptr(), sH[1:].data_ptr(), Wq.data_ptr(), sW[1:].data_ptr(), x["labels"].data_ptr(),
+            out.data_ptr(), out.data_ptr(), None, None, None, ws.data_ptr(), ws.numel()]
+    # d = 56: not a multiple of 16 (the 8-bit rows need 16-byte multiples)
+    assert lib.coda_lmhead_ce_fp8(h, *args, 64, 56, 512, st) == 2
+    # an empty batch has no mean
+    assert lib.coda_lmhead_ce_fp8(h, *args, 0, 64, 512, st) == 1
