@@ -970,28 +970,41 @@ struct EpiCeStats {
       tmem_ld32(c.taddr + cc, v);
       const int n0 = c.tn * BN + cc;
       if (row_ok && n0 < c.N) {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] *= c.acc_scale;
+        // one thread owns the row, so the chunk is reduced in registers: with
+        // one epilogue warp per scheduler the dependency chains set the pace,
+        // hence a pairwise tree for the maximum and four partial sums
         const int nv = c.N - n0;
-        float cmax = -INFINITY;
-        int carg = -1;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          if (i < nv && v[i] > cmax) {
-            cmax = v[i];
-            carg = n0 + i;
+        for (int i = 0; i < 32; ++i) v[i] = i < nv ? v[i] * c.acc_scale : -INFINITY;
+        // chunk maximum and its column: the left operand of every comparison
+        // holds the lower columns, so a tie keeps the lower one
+        float tv[16];
+        int ti[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const bool right = v[2 * i + 1] > v[2 * i];
+          tv[i] = right ? v[2 * i + 1] : v[2 * i];
+          ti[i] = right ? 2 * i + 1 : 2 * i;
+        }
+#pragma unroll
+        for (int w = 8; w >= 1; w >>= 1) {
+#pragma unroll
+          for (int i = 0; i < w; ++i) {
+            const bool right = tv[2 * i + 1] > tv[2 * i];
+            tv[i] = right ? tv[2 * i + 1] : tv[2 * i];
+            ti[i] = right ? ti[2 * i + 1] : ti[2 * i];
           }
         }
+        const float cmax = tv[0];
         if (cmax > mx) {
           se *= __expf(mx - cmax);
           mx = cmax;
-          am = carg;
+          am = n0 + ti[0];
         }
-        float s = 0.f;
+        float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (i < nv) s += __expf(v[i] - mx);
-        se += s;
+        for (int i = 0; i < 32; ++i) s4[i & 3] += __expf(v[i] - mx);
+        se += (s4[0] + s4[1]) + (s4[2] + s4[3]);
         if (y >= n0 && y < n0 + 32) {
 #pragma unroll
           for (int i = 0; i < 32; ++i)
