@@ -160,3 +160,30 @@ def test_fp8_empty_batch():
     for t in (b.dW2t, b.dW1t, b.dg):
         assert torch.count_nonzero(t) == 0
     assert b.s_a.tolist() == [[0.0, 1.0]] * 4
+
+
+def test_fp8_argument_errors():
+    """The 8-bit entry points reject what their header excludes, without
+    launching anything."""
+    lib = C.load_library()
+    h = C.handle()
+    st = torch.cuda.current_stream().cuda_stream
+    u = torch.empty(4096, dtype=torch.uint8, device="cuda")
+    bfb = torch.empty(4096, dtype=torch.bfloat16, device="cuda")
+    f = torch.empty(64, device="cuda")
+    p = u.data_ptr()
+    # coda_gemm_fp8: a format outside {0, 1}
+    assert lib.coda_gemm_fp8(h, p, 0, 2, None, p, 0, 0, None, bfb.data_ptr(), 32, 32, 32, None, None, st) == 1
+    # MN-major A with K-major B is not a supported combination
+    assert lib.coda_gemm_fp8(h, p, 1, 0, None, p, 0, 0, None, bfb.data_ptr(), 32, 32, 32, None, None, st) == 3
+    # K-major K not a multiple of 16 (8-bit rows are 16-byte multiples)
+    assert lib.coda_gemm_fp8(h, p, 0, 0, None, p, 0, 0, None, bfb.data_ptr(), 32, 32, 24, None, None, st) == 2
+    # MN-major M not a multiple of 16
+    assert lib.coda_gemm_fp8(h, p, 1, 0, None, p, 1, 0, None, bfb.data_ptr(), 24, 32, 32, None, None, st) == 2
+    # coda_swiglu_bwd_fp8: a format outside {0, 1}
+    assert lib.coda_swiglu_bwd_fp8(h, bfb.data_ptr(), bfb.data_ptr(), f.data_ptr(), 3, p, f.data_ptr(),
+                                   f.data_ptr(), 8, 16, 64, st) == 1
+    # coda_gemm_dgrad_rmsbwd_fp8: N2 not a multiple of 16
+    assert lib.coda_gemm_dgrad_rmsbwd_fp8(h, p, 1, f.data_ptr(), p, 0, f.data_ptr(), bfb.data_ptr(), bfb.data_ptr(),
+                                          f.data_ptr(), bfb.data_ptr(), f.data_ptr(), 8, 24, 64, st) == 2
+    assert_device_ok()
