@@ -112,7 +112,7 @@ def test_forward_parity(name, pairing):
 
 
 def test_tiny_config_plain(pairing):
-    """configs[0]-style tiny problem: X[256,512], W1, W2 [512,512], PLAIN
+    """The tiny forward workload: X[256,512], W1, W2 [512,512], PLAIN
     epilogue (row scale only), outputs h, rstd, out[256,512]."""
     x = dev_inputs(TINY)
     b = BlockBuffers(x, swiglu=False, backward=False)
