@@ -64,14 +64,21 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// Longest a waiting thread stays suspended inside one try_wait (it resumes at
+// once when the phase completes).  Waiting warps that sleep instead of
+// re-polling leave the power budget to the tensor cores: with the default
+// hint the 7B fwd+bwd step measured 3.97 ms, with this one 3.79 ms (same box,
+// alternated; 20 us gave 3.82 ms).
+constexpr uint32_t kWaitSuspendNs = 10000000u;
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}\n"
       : "=r"(ok)
-      : "r"(bar_addr), "r"(parity)
+      : "r"(bar_addr), "r"(parity), "n"(kWaitSuspendNs)
       : "memory");
   return ok != 0;
 }
@@ -80,10 +87,10 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar_addr, uint32_
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}\n"
       : "=r"(ok)
-      : "r"(bar_addr), "r"(parity)
+      : "r"(bar_addr), "r"(parity), "n"(kWaitSuspendNs)
       : "memory");
   return ok != 0;
 }
@@ -95,12 +102,11 @@ __device__ __forceinline__ bool mbar_wait_bounded_cluster(uint64_t* bar, uint32_
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait_cluster(a, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
+  for (;;) {
+    // each try may sleep up to kWaitSuspendNs: check after every one
     if (mbar_try_wait_cluster(a, parity)) return true;
-    if ((it & 31u) == 0) {
-      if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > timeout_ns) return false;
-    }
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > timeout_ns) return false;
   }
 }
 
@@ -113,12 +119,10 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
+  for (;;) {
     if (mbar_try_wait(a, parity)) return true;
-    if ((it & 31u) == 0) {
-      if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > timeout_ns) return false;
-    }
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > timeout_ns) return false;
   }
 }
 
@@ -128,9 +132,9 @@ __device__ __forceinline__ bool mbar_wait_timeout(uint64_t* bar, uint32_t parity
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
+  for (;;) {
     if (mbar_try_wait(a, parity)) return true;
-    if ((it & 31u) == 0 && globaltimer_ns() - t0 > timeout_ns) return false;
+    if (globaltimer_ns() - t0 > timeout_ns) return false;
   }
 }
 
