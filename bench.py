@@ -163,13 +163,15 @@ class FusedStep:
             # the fold runs on a second stream beside GEMM1 (BlockBuffers.gemm1_and_fold)
             fwd = [("gemm1_res_prms+fold", b.gemm1_and_fold)]
             A2, B2 = b.H, b.W2gt
+        # z is saved for the backward only: a forward-only workload has no use for it
+        zs = b.z if b.with_backward else None
         if fuse_rstd:
-            fwd.append((gemm2, lambda: C.coda_gemm_prms_rowscale_swiglu(A2, B2, b.psum, b.eps, b.rstd, b.out, b.z,
+            fwd.append((gemm2, lambda: C.coda_gemm_prms_rowscale_swiglu(A2, B2, b.psum, b.eps, b.rstd, b.out, zs,
                                                                         C.CODA_EPI_SWIGLU)))
         else:
             fwd += [
                 ("rstd_combine", lambda: C.coda_rstd_combine(b.psum, b.d, b.eps, b.rstd)),
-                (gemm2, lambda: C.coda_gemm_rowscale_swiglu(A2, B2, b.rstd, b.out, b.z, C.CODA_EPI_SWIGLU)),
+                (gemm2, lambda: C.coda_gemm_rowscale_swiglu(A2, B2, b.rstd, b.out, zs, C.CODA_EPI_SWIGLU)),
             ]
         bwd = [
             ("swiglu_bwd", lambda: C.coda_swiglu_bwd(b.dY, b.z, b.rstd, b.dP, b.c, b.d)),
@@ -351,7 +353,8 @@ def bench_fp8_forward(C, b, shape, steps, warmup, peak_bf16):
         lambda: C.coda_gemm_res_prms_fp8(Xq, sc[0, 1:], W1q, sc[1, 1:], b.R, b.H, b.psum),
         lambda: C.coda_rstd_combine(b.psum, b.d, b.eps, b.rstd),
         lambda: C.coda_fp8_quantize(b.H, Hq, sc[3]),
-        lambda: C.coda_gemm_rowscale_swiglu_fp8(Hq, sc[3, 1:], W2q, sc[2, 1:], b.rstd, b.out, b.z),
+        lambda: C.coda_gemm_rowscale_swiglu_fp8(Hq, sc[3, 1:], W2q, sc[2, 1:], b.rstd, b.out,
+                                                b.z if b.with_backward else None),
     ]
     fs = FusedStep(C, b)
     bf16 = fs.calls()[:fs.n_fwd]  # the bf16 forward stages
@@ -522,69 +525,6 @@ def bench_lmhead(C, steps, warmup, tokens=0):
     return out
 
 
-class E2EPipeline:
-    """The fused step through the public API with host buffers, as a training
-    loop would drive it: each step's activations and upstream gradient are
-    copied from pinned host memory and its dX is read back, with two device
-    buffer sets so that step i+1's H2D copy and step i's D2H read overlap
-    step i's compute (separate copy streams, event-ordered)."""
-
-    def __init__(self, C, b0, host):
-        from gemm_epilogue_transformer_tma_gb300.path import BlockBuffers
-        self.host = host
-        shared = {k: getattr(b0, k) for k in ("W1t", "g", "W2t")}
-        second = dict(shared, X=torch.empty_like(b0.X), R=torch.empty_like(b0.R))
-        if b0.with_backward:
-            second["dY"] = torch.empty_like(b0.dY)
-        self.bufs = [b0, BlockBuffers(second, backward=b0.with_backward, fuse_rstd=b0.fuse_rstd,
-                                      g_on_activation=b0.g_on_activation)]
-        self.inputs = ("X", "R", "dY") if b0.with_backward else ("X", "R")
-        self.result = "dX" if b0.with_backward else "out"
-        self.compute = torch.cuda.current_stream()
-        self.h2d = torch.cuda.Stream()
-        self.d2h = torch.cuda.Stream()
-        ev = lambda: [torch.cuda.Event(), torch.cuda.Event()]  # noqa: E731
-        # ev_in: the forward's inputs (X, R) landed; ev_in_bwd: dY landed
-        self.ev_in, self.ev_in_bwd, self.ev_comp, self.ev_out = ev(), ev(), ev(), ev()
-        self.fresh = [True, True]
-
-    def _load(self, slot):
-        b = self.bufs[slot]
-        with torch.cuda.stream(self.h2d):
-            if not self.fresh[slot]:
-                self.h2d.wait_event(self.ev_comp[slot])  # the previous step on this slot read it
-            for k in ("X", "R"):
-                getattr(b, k).copy_(self.host[k], non_blocking=True)
-            self.ev_in[slot].record(self.h2d)
-            if "dY" in self.inputs:
-                b.dY.copy_(self.host["dY"], non_blocking=True)
-                self.ev_in_bwd[slot].record(self.h2d)
-
-    def run(self, n):
-        self._load(0)
-        for i in range(n):
-            slot = i & 1
-            b = self.bufs[slot]
-            self.compute.wait_event(self.ev_in[slot])
-            if not self.fresh[slot]:
-                self.compute.wait_event(self.ev_out[slot])  # dX of step i-2 read back
-            b.forward()
-            if b.with_backward:
-                # the upstream gradient is needed only now, as in a training
-                # loop where it arrives after the forward
-                self.compute.wait_event(self.ev_in_bwd[slot])
-                b.backward()
-            self.ev_comp[slot].record(self.compute)
-            self.fresh[slot] = False
-            if i + 1 < n:
-                self._load(slot ^ 1)
-            with torch.cuda.stream(self.d2h):
-                self.d2h.wait_event(self.ev_comp[slot])
-                self.host[self.result].copy_(getattr(b, self.result), non_blocking=True)
-                self.ev_out[slot].record(self.d2h)
-        torch.cuda.synchronize()
-
-
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -643,7 +583,7 @@ def main():
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
 
     import gemm_epilogue_transformer_tma_gb300 as C
-    from gemm_epilogue_transformer_tma_gb300.path import BlockBuffers
+    from gemm_epilogue_transformer_tma_gb300.path import BlockBuffers, HostBlockStepper
     peaks = load_peaks()
     C.coda_set_sm_pairing(not args.single_sm)
 
@@ -691,22 +631,30 @@ def main():
     launches = sum(fs.kernels.values()) * args.steps
     extras = {}
     if not args.no_extras:
-        # end to end through the public API with host buffers: every rank runs
-        # its replica between barriers, the slowest rank's time counts
+        # end to end through the C ABI with host buffers: the library's block
+        # executor (coda_block_*) takes each step's inputs from page-locked
+        # host memory and reads its result back; every rank runs its replica
+        # between barriers, the slowest rank's time counts
         ins = ("X", "R", "dY") if shape.backward else ("X", "R")
         res = "dX" if shape.backward else "out"
         host = {k: torch.empty_like(x[k], device="cpu").pin_memory() for k in ins}
         for k in host:
             host[k].copy_(x[k])
-        host[res] = torch.empty_like(getattr(b, res), device="cpu").pin_memory()
-        pipe = E2EPipeline(C, b, host)
-        pipe.run(3)
+        stepper = HostBlockStepper(b.W1t, b.g, b.W2t, shape.M, shape.eps, backward=shape.backward)
+        host.update(stepper.host_buffers(out=not shape.backward, dX=shape.backward))
+
+        def e2e_steps(n):
+            for _ in range(n):
+                stepper.submit(host["X"], host["R"], host.get("dY"), out=host.get("out"), dX=host.get("dX"))
+            stepper.sync()
+
+        e2e_steps(3)
         # as many steps as the headline: the first step's H2D copy and the
         # last step's read-back overlap nothing and are timed in full
         n_e2e = max(3, args.steps)
         barrier()
         t0 = time.perf_counter()
-        pipe.run(n_e2e)
+        e2e_steps(n_e2e)
         barrier()
         e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3 / n_e2e, dist, "cuda")
         h2d = sum(host[k].numel() * host[k].element_size() for k in ins)
@@ -714,12 +662,14 @@ def main():
         extras["e2e"] = {"value": aggregate_value(step_flops, e2e_ms, world), "unit": UNIT, "ms_per_step": e2e_ms,
                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                          "steps": n_e2e,
+                         "api": "coda_block_create / coda_block_step_host / coda_block_sync (host buffers)",
                          "timing": "host wall clock over the whole run, synchronize (and barrier) at both ends; "
-                                   "copies of step i+1 (H2D) and i (D2H) overlap step i's compute; each step's "
-                                   "backward waits for its dY copy, its forward for X and R only; the first "
-                                   "step's X / R copy and the last step's D2H overlap nothing; per-rank bytes, "
-                                   "value summed over ranks"}
-        del host, pipe
+                                   "the executor overlaps step i+1's H2D copies and step i-1's D2H read-back "
+                                   "with step i's kernels; each step's backward waits for its dY copy, its "
+                                   "forward for X and R only; the first step's X / R copy and the last step's "
+                                   "D2H overlap nothing; per-rank bytes, value summed over ranks"}
+        stepper.close()
+        del host, stepper
     if not args.no_extras and rank == 0:
         # Comparisons against the headline step are timed interleaved with it
         # (rounds of fused / other, adjacent in time): the part heats over a

@@ -75,6 +75,14 @@ SIGNATURES = {
     "coda_gemm_rowscale_swiglu_bwd": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
                                              _I64, _I64, _I64, _P]),
     "coda_gemm_res_prms_bwd": (_INT, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
+    "coda_block_arena_bytes": (_SZ, [_I64, _I64, _I64, _I64, _INT]),
+    "coda_block_create": (_INT, [_P, _I64, _I64, _I64, _I64, _F32, _INT, _P, _P, _P, _P, _P, _P, _P, _SZ,
+                                 ctypes.POINTER(_P)]),
+    "coda_block_step_host": (_INT, [_P, _P, _P, _P, _P, _P, _P, ctypes.POINTER(_I64)]),
+    "coda_block_wait_step": (_INT, [_P, _I64]),
+    "coda_block_sync": (_INT, [_P, ctypes.POINTER(ctypes.c_int32)]),
+    "coda_block_stream": (_INT, [_P, ctypes.POINTER(_P)]),
+    "coda_block_destroy": (_INT, [_P]),
     "coda_rope_table": (_INT, [_P, _P, _P, _I64, _I64, _F32, _P]),
     "coda_gemm_qkv_rope": (_INT, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64, _P]),
     "coda_rope_apply": (_INT, [_P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _P]),
@@ -429,6 +437,82 @@ def coda_gemm_res_prms_bwd(dH, X, W1t, dX, dW1t, dR=None, stream=None):
     _check(load_library().coda_gemm_res_prms_bwd(_h(X), _ptr(dH, BF, "dH"), _ptr(X, BF, "X"), _ptr(W1t, BF, "W1t"),
                                                  _ptr(dX, BF, "dX"), _ptr(dW1t, BF, "dW1t"), _ptr(dR, BF, "dR"),
                                                  M, K1, d, _stream(stream)), "coda_gemm_res_prms_bwd")
+
+
+def _host_ptr(t: torch.Tensor | None, dtype, shape, name) -> int | None:
+    """A page-locked host tensor's address (the block executor's copy
+    engines read and write it asynchronously)."""
+    if t is None:
+        return None
+    if t.device.type != "cpu":
+        raise ValueError(f"{name} must be a host tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    _shape(t, shape, name)
+    if not t.is_pinned():
+        raise ValueError(f"{name} must be in page-locked memory (pin_memory())")
+    return t.data_ptr()
+
+
+def coda_block_arena_bytes(M: int, K1: int, d: int, N2: int, backward: bool) -> int:
+    return load_library().coda_block_arena_bytes(M, K1, d, N2, int(backward))
+
+
+def coda_block_create(M: int, K1: int, d: int, N2: int, eps: float, backward: bool, W1t, g, W2t,
+                      dW1t, dW2t, dg, arena) -> int:
+    """Create a block step executor (include/coda.h) on the weights' device;
+    returns its handle.  arena: a uint8 device tensor of at least
+    coda_block_arena_bytes bytes, kept alive by the caller."""
+    _shape(W1t, (d, K1), "W1t")
+    _shape(g, (d,), "g")
+    _shape(W2t, (N2, d), "W2t")
+    if backward:
+        _shape(dW1t, (d, K1), "dW1t")
+        _shape(dW2t, (N2, d), "dW2t")
+        _shape(dg, (d,), "dg")
+    out = _P()
+    with torch.cuda.device(W1t.device):
+        _check(load_library().coda_block_create(
+            _h(W1t), M, K1, d, N2, eps, int(backward), _ptr(W1t, BF, "W1t"), _ptr(g, BF, "g"), _ptr(W2t, BF, "W2t"),
+            _ptr(dW1t, BF, "dW1t"), _ptr(dW2t, BF, "dW2t"), _ptr(dg, F32, "dg"), _ptr(arena, torch.uint8, "arena"),
+            arena.numel(), ctypes.byref(out)), "coda_block_create")
+    return out.value
+
+
+def coda_block_step_host(blk: int, M: int, K1: int, d: int, F: int, X, R, dY=None, out=None, dX=None,
+                         dR=None) -> int:
+    """Enqueue one step on page-locked host tensors; returns the step index."""
+    sid = _I64(0)
+    _check(load_library().coda_block_step_host(
+        blk, _host_ptr(X, BF, (M, K1), "X"), _host_ptr(R, BF, (M, d), "R"), _host_ptr(dY, BF, (M, F), "dY"),
+        _host_ptr(out, BF, (M, F), "out"), _host_ptr(dX, BF, (M, K1), "dX"), _host_ptr(dR, BF, (M, d), "dR"),
+        ctypes.byref(sid)), "coda_block_step_host")
+    return sid.value
+
+
+def coda_block_wait_step(blk: int, step: int):
+    _check(load_library().coda_block_wait_step(blk, step), "coda_block_wait_step")
+
+
+def coda_block_sync(blk: int) -> tuple[int, int]:
+    """Wait for every submitted step; returns (status, raw_bits) like
+    coda_sync_status, without raising."""
+    bits = ctypes.c_int32(0)
+    st = load_library().coda_block_sync(blk, ctypes.byref(bits))
+    return st, bits.value
+
+
+def coda_block_stream(blk: int) -> int:
+    """The executor's compute stream, as a cudaStream_t value."""
+    s = _P()
+    _check(load_library().coda_block_stream(blk, ctypes.byref(s)), "coda_block_stream")
+    return s.value or 0
+
+
+def coda_block_destroy(blk: int):
+    _check(load_library().coda_block_destroy(blk), "coda_block_destroy")
 
 
 def coda_rope_table(cos_t, sin_t, base=10000.0, stream=None):

@@ -17,6 +17,8 @@ from . import (CODA_EPI_PLAIN, CODA_EPI_SWIGLU, E4M3, E5M2, coda_bwd_workspace_b
                coda_gemm_res_prms_bwd, coda_gemm_rowscale_swiglu, coda_gemm_rowscale_swiglu_bwd,
                coda_gemm_wgrad_gscale, coda_prms_num_tiles, coda_rstd_combine, coda_swiglu_bwd, coda_swiglu_bwd_fp8,
                coda_unfused_bwd, coda_unfused_fwd, coda_unfused_workspace_bytes)
+from . import (coda_block_arena_bytes, coda_block_create, coda_block_destroy, coda_block_step_host,
+               coda_block_stream, coda_block_sync, coda_block_wait_step, STATUS_NAMES)
 
 BF = torch.bfloat16
 F32 = torch.float32
@@ -277,3 +279,67 @@ class BlockBuffers:
     def backward_unfused(self):
         coda_unfused_bwd(self.dY, self.X, self.W1t, self.g, self.W2t, self.H, self.rstd, self.Nrm, self.z,
                          self.dH, self.dX, self.dW1t, self.dW2t, self.dg, self.ws_unfused)
+
+
+class HostBlockStepper:
+    """The fused step through the library's block executor (coda_block_*):
+    each step's X, R (and dY) come from page-locked host tensors and its
+    results go back to page-locked host tensors, with the copies of one step
+    overlapping the kernels of its neighbours.  The executor issues the
+    whole step natively; this class owns its device arena and the weight
+    gradients, nothing more.
+
+    W1t[d,K1], g[d], W2t[N2,d]: device bf16 weights, read by every step.
+    With backward, every step overwrites dW1t, dW2t and dg (device)."""
+
+    def __init__(self, W1t, g, W2t, M: int, eps: float = 1e-5, backward: bool = True):
+        dev = W1t.device
+        self.d, self.K1 = W1t.shape
+        self.N2 = W2t.shape[0]
+        self.F = self.N2 // 2
+        self.M = M
+        self.backward = backward
+        self.W1t, self.g, self.W2t = W1t, g, W2t
+        e = dict(device=dev)
+        self.dW1t = torch.empty(self.d, self.K1, dtype=BF, **e) if backward else None
+        self.dW2t = torch.empty(self.N2, self.d, dtype=BF, **e) if backward else None
+        self.dg = torch.empty(self.d, dtype=F32, **e) if backward else None
+        nbytes = coda_block_arena_bytes(M, self.K1, self.d, self.N2, backward)
+        self.arena = torch.empty(max(1, nbytes), dtype=torch.uint8, **e)
+        self.blk = coda_block_create(M, self.K1, self.d, self.N2, eps, backward, W1t, g, W2t,
+                                     self.dW1t, self.dW2t, self.dg, self.arena)
+
+    def host_buffers(self, out: bool = False, dX: bool = True, dR: bool = False) -> dict:
+        """Page-locked host tensors for the results a step should read back."""
+        M, K1, d, F = self.M, self.K1, self.d, self.F
+        want = {"out": (out, (M, F)), "dX": (dX and self.backward, (M, K1)), "dR": (dR and self.backward, (M, d))}
+        return {k: torch.empty(shape, dtype=BF).pin_memory() for k, (on, shape) in want.items() if on}
+
+    def submit(self, X, R, dY=None, out=None, dX=None, dR=None) -> int:
+        """Enqueue one step; returns its index.  The host inputs stay in use,
+        and the results are not ready, until wait(index) or sync()."""
+        return coda_block_step_host(self.blk, self.M, self.K1, self.d, self.F, X, R, dY, out, dX, dR)
+
+    def wait(self, step: int):
+        coda_block_wait_step(self.blk, step)
+
+    def sync(self):
+        """Wait for every submitted step; raises on a device-side error."""
+        st, bits = coda_block_sync(self.blk)
+        if st != 0:
+            raise RuntimeError(f"block executor: {STATUS_NAMES.get(st, st)} (device bits {bits:#x})")
+
+    def stream(self) -> torch.cuda.ExternalStream:
+        """The executor's compute stream, for work ordered between steps."""
+        return torch.cuda.ExternalStream(coda_block_stream(self.blk), device=self.W1t.device)
+
+    def close(self):
+        if getattr(self, "blk", None):
+            coda_block_destroy(self.blk)
+            self.blk = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

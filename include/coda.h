@@ -20,12 +20,12 @@
  *     SwiGLU, rows [0, F) of W2t are the gate projection and rows [F, 2F) the
  *     up projection (N2 = 2F).
  *   - Every pointer is caller-owned CUDA device memory on the handle's device
- *     (except the handle itself and the out-parameters of coda_create and
- *     coda_sync_status, which are host memory).  Device pointers must be
- *     16-byte aligned.  The library never allocates after coda_create and
- *     only reads or writes the buffers it is given; scratch space is passed
- *     in as a caller-owned workspace whose size a *_workspace_bytes call
- *     returns.
+ *     (except the handles, the out-parameters, and the step inputs and
+ *     results of coda_block_step_host, which are host memory).  Device
+ *     pointers must be 16-byte aligned.  The library allocates no device
+ *     memory after coda_create and only reads or writes the buffers it is
+ *     given; scratch space is passed in as a caller-owned workspace (or
+ *     arena) whose size a *_workspace_bytes (*_arena_bytes) call returns.
  *   - Extents are int64_t.  Every contiguous extent (K1, d, N2, F, V) must be
  *     a positive multiple of 8 and every extent below 2^31.  M == 0 is a
  *     valid empty problem: nothing is launched and CODA_OK is returned.
@@ -304,6 +304,79 @@ coda_status_t coda_gemm_rowscale_swiglu_bwd(coda_handle_t h, const void* dY, con
  * dR = dH), or a distinct bf16 [M][d] buffer that receives a copy of dH. */
 coda_status_t coda_gemm_res_prms_bwd(coda_handle_t h, const void* dH, const void* X, const void* W1t, void* dX,
                                      void* dW1t, void* dR, int64_t M, int64_t K1, int64_t d, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* block step executor: the whole step issued natively, with its inputs and  */
+/* results in host memory                                                    */
+/* ------------------------------------------------------------------------ */
+
+/* One executor runs the fused step of the write-up's flagship block (section
+ * 尾声: GEMM1 + residual + partial RMS with the fold of g beside it, the rstd
+ * combine, GEMM2 + row scale + SwiGLU, then, with backward = 1, the SwiGLU
+ * backward, dgrad2 with the RMSNorm backward, dg, wgrad2, dX and dW1) for
+ * inputs that live in page-locked host memory.  Each coda_block_step_host
+ * call enqueues the host-to-device copies of the step's X, R (and dY), the
+ * step's kernels and the read-back of the requested results, and returns
+ * without waiting.  Two device slots hold what the copies touch, so the
+ * copies of step n+1 and the read-back of step n-1 overlap step n's kernels;
+ * the kernels of successive steps run in submission order on one stream.
+ * The executor computes exactly what the separate calls compute (same
+ * kernels, same order): its results are bit-identical to theirs. */
+typedef struct coda_block_s* coda_block_t;
+
+/* Device bytes the executor needs for a problem (its arena): W2g [N2][d],
+ * H, psum, rstd, z and the backward workspace once, and X, R, out (and dY,
+ * dH, dX) in each of two slots, every buffer 256-byte aligned.  0 for an
+ * invalid shape. */
+size_t coda_block_arena_bytes(int64_t M, int64_t K1, int64_t d, int64_t N2, int backward);
+
+/* Create an executor on the current CUDA device, which must be the handle's.
+ * Shapes as coda_gemm_res_prms / coda_gemm_rowscale_swiglu with SwiGLU
+ * (N2 = 2F, F a multiple of 8); eps > 0 is the RMSNorm epsilon.
+ * Weights (device, bf16, caller-owned, read by every step): W1t [d][K1], g
+ * [d], W2t [N2][d].  With backward = 1 every step overwrites the weight
+ * gradients dW1t (bf16 [d][K1]), dW2t (bf16 [N2][d]) and dg (fp32 [d]),
+ * device buffers the caller owns; with backward = 0 they may be NULL.  arena:
+ * caller-owned device memory of at least coda_block_arena_bytes bytes,
+ * 16-byte aligned, used only by this executor until it is destroyed.  The
+ * executor creates four CUDA streams and its events; it allocates no device
+ * memory.  *out receives the executor. */
+coda_status_t coda_block_create(coda_handle_t h, int64_t M, int64_t K1, int64_t d, int64_t N2, float eps,
+                                int backward, const void* W1t, const void* g, const void* W2t, void* dW1t,
+                                void* dW2t, float* dg, void* arena, size_t arena_bytes, coda_block_t* out);
+
+/* Enqueue one step.  Host pointers, each page-locked (cudaHostAlloc) or
+ * registered (cudaHostRegister) memory, else CODA_ERR_INVALID_ARG:
+ *   X bf16 [M][K1], R bf16 [M][d] (required), dY bf16 [M][F] (required with
+ *   backward, NULL without);
+ *   out bf16 [M][F] receives the SwiGLU output, dX bf16 [M][K1] the input
+ *   gradient and dR bf16 [M][d] the residual gradient (= dH); each may be
+ *   NULL (not read back); dX and dR must be NULL without backward.
+ * The call returns once everything is enqueued.  The host inputs must stay
+ * unchanged, and the results are not valid, until coda_block_wait_step for
+ * this step (or coda_block_sync) has returned.  *step_id (may be NULL)
+ * receives the step's index, counted from 0 per executor. */
+coda_status_t coda_block_step_host(coda_block_t b, const void* X, const void* R, const void* dY, void* out, void* dX,
+                                   void* dR, int64_t* step_id);
+
+/* Block until step `step` has finished: its inputs have been read and its
+ * results written to host memory.  It may also wait for the next step that
+ * uses the same slot (step + 2) if that has been submitted. */
+coda_status_t coda_block_wait_step(coda_block_t b, int64_t step);
+
+/* Block until every submitted step has finished, then read and clear the
+ * handle's device status word as coda_sync_status does (its return value and
+ * device_bits have the same meaning). */
+coda_status_t coda_block_sync(coda_block_t b, int32_t* device_bits);
+
+/* *stream receives the executor's compute stream (a cudaStream_t): work the
+ * caller enqueues there (an optimizer update of the weights, say) runs after
+ * the steps submitted before it and before those submitted after it. */
+coda_status_t coda_block_stream(coda_block_t b, void** stream);
+
+/* Wait for the executor's streams, then destroy them and the executor.  NULL
+ * is accepted.  The arena is the caller's to free afterwards. */
+coda_status_t coda_block_destroy(coda_block_t b);
 
 /* ------------------------------------------------------------------------ */
 /* rotary position embedding on the QKV projection (section 五种积木: RoPE  */

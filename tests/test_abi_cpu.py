@@ -2,6 +2,7 @@
 point include/coda.h declares with the binding's signature table matching,
 and the pure host queries (tile counts, workspace sizes, status strings)
 answer without a GPU."""
+import ctypes
 import os
 import re
 import subprocess
@@ -53,6 +54,11 @@ def test_host_queries(lib):
     assert lib.coda_lmhead_ce_workspace_bytes(8192, 2048, 128256, 0) >= 3 * 8192 * 1002 * 4
     assert lib.coda_lmhead_ce_workspace_bytes(8192, 2048, 128256, 1) > lib.coda_lmhead_ce_workspace_bytes(
         8192, 2048, 128256, 0)
+    # the executor's arena: W2g alone for an empty batch, 0 for an invalid shape
+    assert lib.coda_block_arena_bytes(0, 64, 64, 128, 1) == 128 * 64 * 2
+    assert lib.coda_block_arena_bytes(8, 64, 64, 0, 1) == 0
+    assert lib.coda_block_arena_bytes(M, 4096, d, N2, 1) > lib.coda_block_arena_bytes(M, 4096, d, N2, 0) > \
+        2 * M * (4096 + d + N2 // 2) * 2
     assert lib.coda_status_string(0) == b"ok"
     assert b"time limit" in lib.coda_status_string(6)
 
@@ -62,3 +68,8 @@ def test_null_handle_is_rejected_without_a_gpu(lib):
     assert lib.coda_set_wait_timeout_ns(None, 1) == 1
     assert lib.coda_gemm(None, None, 0, None, 0, None, 8, 8, 8, None, None, None) == 1
     assert lib.coda_destroy(None) == 0
+    out = ctypes.c_void_p()
+    assert lib.coda_block_create(None, 8, 64, 64, 128, 1e-5, 1, *([None] * 7), 0, ctypes.byref(out)) == 1
+    assert lib.coda_block_step_host(None, None, None, None, None, None, None, None) == 1
+    assert lib.coda_block_sync(None, None) == 1
+    assert lib.coda_block_destroy(None) == 0
