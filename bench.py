@@ -285,6 +285,40 @@ def cpu_oracle_baseline(shape: BlockShape, target_s: float = 12.0, max_rows: int
             "rows": rows}
 
 
+_SINGLE_CORE = r"""
+import json, sys, time
+sys.path.insert(0, sys.argv[1])
+import oracle as O
+from coda_inputs import B1, TINY, BlockShape, block_inputs, to_f64
+res = {}
+for s, rows in ((TINY, TINY.M), (B1, 128)):
+    x = block_inputs(BlockShape(s.name, rows, s.K1, s.d, s.N2, swiglu=s.swiglu, w_std=s.w_std, x_std=s.x_std,
+                                backward=False), 0, "cpu")
+    a = {k: to_f64(v) for k, v in x.items()}
+    t = time.perf_counter()
+    O.block_forward(a["X"], a["W1t"], a["R"], a["g"], a["W2t"], s.eps, s.swiglu)
+    dt = time.perf_counter() - t
+    fl = 2.0 * rows * s.d * s.K1 + 2.0 * rows * s.N2 * s.d
+    res[s.name] = {"rows": rows, "of_rows": s.M, "seconds": dt, "gflops": fl / dt / 1e9}
+print(json.dumps(res))
+"""
+
+
+def cpu_oracle_single_core():
+    """The fp64 oracle's forward on one host core (the BLAS and OpenMP pools
+    limited to one thread in a child process): the tiny configuration whole
+    and a 128-row sample of the 1B one."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    try:
+        r = subprocess.run([sys.executable, "-c", _SINGLE_CORE, ROOT], env=env, capture_output=True, text=True,
+                           timeout=300)
+        out = json.loads(r.stdout.strip().splitlines()[-1])
+    except (subprocess.SubprocessError, ValueError, IndexError) as e:
+        return {"error": str(e)[:200]}
+    out["cores"] = 1
+    return out
+
+
 def run_reference(args, shape):
     """The oracle as the reference arm: timed on the host cores."""
     rank = int(os.environ.get("RANK", "0"))
@@ -307,6 +341,48 @@ def run_reference(args, shape):
                              "sample": res["sample"]},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def bench_memory_kernels(C, b, shape, hbm_gbs, warmup=10, iters=50):
+    """The memory-bound kernels of the step, each launched alone: warmup
+    untimed launches, then iters launches each preceded by a write of a
+    buffer twice the L2's size (so every launch starts with a cold L2) and
+    timed with CUDA events on the launching stream.  Algorithmic bytes per
+    launch: what the kernel must read and write once."""
+    M, d, N2, F = shape.M, shape.d, shape.N2, shape.N2 // 2
+    T = C.coda_prms_num_tiles(d)
+    rows = b.dgpart.shape[0] if shape.backward else 0
+    kernels = [
+        ("fold", 2 * N2 * d * 2, lambda: C.coda_fold_rmsnorm_weight(b.W2t, b.g, b.W2gt)),
+        ("rstd_combine", M * T * 4 + M * 4, lambda: C.coda_rstd_combine(b.psum, b.d, b.eps, b.rstd)),
+    ]
+    if shape.backward:
+        kernels += [
+            ("swiglu_bwd", M * F * 2 + 2 * M * N2 * 2 + 2 * M * 4,
+             lambda: C.coda_swiglu_bwd(b.dY, b.z, b.rstd, b.dP, b.c, b.d)),
+            ("dg_combine", rows * d * 4 + d * 4, lambda: C.coda_dg_combine(b.dgpart, b.dg)),
+        ]
+    flush = torch.empty(2 * 129 * 2 ** 20, dtype=torch.uint8, device="cuda")
+    out = {}
+    for name, nbytes, f in kernels:
+        for _ in range(warmup):
+            f()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+        for e0, e1 in evs:
+            flush.zero_()
+            e0.record()
+            f()
+            e1.record()
+        torch.cuda.synchronize()
+        us = sorted(e0.elapsed_time(e1) * 1e3 for e0, e1 in evs)
+        med = statistics.median(us)
+        out[name] = {"median_us": med, "min_us": us[0], "max_us": us[-1], "bytes": nbytes,
+                     "gbs": nbytes / (med * 1e-6) / 1e9, "frac_of_hbm": nbytes / (med * 1e-6) / 1e9 / hbm_gbs}
+    out["timing"] = (f"each kernel alone: {warmup} warm-up launches, then {iters} timed launches, each after a "
+                     f"{flush.numel() >> 20} MiB write that flushes the L2; median, min and max of the CUDA-event "
+                     "times; GB/s = algorithmic bytes / median (not meaningful for the latency-bound combines)")
+    out["peak_gbs"] = hbm_gbs
+    return out
 
 
 def bench_down_proj_swiglu_bwd(C, b, shape, steps, warmup):
@@ -700,6 +776,8 @@ def main():
                                                 "per-round time ratio"}
         del bu
         torch.cuda.empty_cache()
+        extras["memory_kernels"] = bench_memory_kernels(C, b, shape, peaks["hbm_gbs"])
+        torch.cuda.empty_cache()
         if shape.backward:
             extras["next_swiglu_bwd_in_down_proj_dgrad"] = bench_down_proj_swiglu_bwd(C, b, shape, args.steps,
                                                                                     args.warmup)
@@ -746,6 +824,7 @@ def main():
         line.update(extras)
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_oracle_baseline(shape)
+            line["cpu_baseline"]["single_core_fwd"] = cpu_oracle_single_core()
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.barrier()
