@@ -321,7 +321,8 @@ coda_status_t coda_gemm_res_prms_bwd(coda_handle_t h, const void* dH, const void
  * copies of step n+1 and the read-back of step n-1 overlap step n's kernels;
  * the kernels of successive steps run in submission order on one stream.
  * The executor computes exactly what the separate calls compute (same
- * kernels, same order): its results are bit-identical to theirs. */
+ * kernels, same order): its results are bit-identical to theirs.  An
+ * executor may be used from one host thread at a time. */
 typedef struct coda_block_s* coda_block_t;
 
 /* Device bytes the executor needs for a problem (its arena): W2g [N2][d],

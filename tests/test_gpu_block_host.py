@@ -160,3 +160,26 @@ def test_argument_errors():
     assert lib.coda_block_create(h, s.M, s.K1, s.d, s.N2, 0.0, 1, *args, need, ctypes.byref(out)) == 1
     assert lib.coda_block_create(h, s.M, s.K1, s.d, s.N2, s.eps, 1, *args, need, ctypes.byref(out)) == 0
     assert lib.coda_block_destroy(out) == 0
+
+
+def test_work_on_the_executor_stream_is_ordered_between_steps():
+    # a weight update enqueued on the executor's compute stream after step 0
+    # is seen by step 1 and not by step 0
+    s = SHAPES["ragged"]
+    w = {k: v.clone() for k, v in block_inputs(s, 0, "cuda").items() if k in WEIGHTS}
+    x = block_inputs(s, 1, "cuda")
+    st = HostBlockStepper(w["W1t"], w["g"], w["W2t"], s.M, s.eps)
+    hi = {k: pinned(x[k]) for k in ("X", "R", "dY")}
+    outs = [st.host_buffers(out=True, dX=True) for _ in range(2)]
+    st.submit(hi["X"], hi["R"], hi["dY"], **outs[0])
+    with torch.cuda.stream(st.stream()):
+        w["W1t"].mul_(2.0)
+        w["g"].mul_(0.5)
+    st.submit(hi["X"], hi["R"], hi["dY"], **outs[1])
+    st.sync()
+    w0 = {k: v for k, v in block_inputs(s, 0, "cuda").items() if k in WEIGHTS}
+    for o, weights in ((outs[0], w0), (outs[1], w)):
+        ref = reference(s, weights, x)
+        assert torch.equal(o["out"], ref.out.cpu())
+        assert torch.equal(o["dX"], ref.dX.cpu())
+    st.close()
