@@ -164,3 +164,33 @@ def test_lmhead_ce_full_size():
     vcols = np.unique(np.concatenate([sample(V, 24, 6), y[rows[:6]]]))
     dW_ref = O.ce_weight_grad_given_lse(Hall, Wt[vcols], vcols, y, f64(lse), M)
     assert_frob(rows_of(dW, vcols), dW_ref, "dW")
+
+
+def test_7b_block_executor_full_size():
+    """The block executor on host buffers at the 7B size, as the bench's
+    end-to-end figure drives it: two pipelined steps with different inputs,
+    each bit-identical to the separate calls on the same inputs (whose parity
+    with the oracle the tests above establish)."""
+    from gemm_epilogue_transformer_tma_gb300.path import HostBlockStepper
+    w = {k: v for k, v in block_inputs(B7, 0, "cuda").items() if k in ("W1t", "g", "W2t")}
+    steps = [block_inputs(B7, seed, "cuda") for seed in (1, 2)]
+    st = HostBlockStepper(w["W1t"], w["g"], w["W2t"], B7.M, B7.eps)
+    host_in = [{k: x[k].cpu().pin_memory() for k in ("X", "R", "dY")} for x in steps]
+    outs = [st.host_buffers(out=True, dX=True, dR=True) for _ in steps]
+    for hi, o in zip(host_in, outs):
+        st.submit(hi["X"], hi["R"], hi["dY"], **o)
+    st.sync()
+    del host_in
+    for i, (x, o) in enumerate(zip(steps, outs)):
+        b = BlockBuffers(dict(w, **{k: x[k] for k in ("X", "R", "dY")}))
+        b.step()
+        torch.cuda.synchronize()
+        assert_device_ok()
+        for k_host, k_ref in (("out", "out"), ("dX", "dX"), ("dR", "dH")):
+            assert torch.equal(o[k_host], getattr(b, k_ref).cpu()), (i, k_host)
+        if i == len(steps) - 1:
+            for k in ("dW1t", "dW2t", "dg"):
+                assert torch.equal(getattr(st, k), getattr(b, k)), k
+        del b
+        torch.cuda.empty_cache()
+    st.close()
