@@ -461,14 +461,28 @@ def bench_fp8_fwdbwd(C, b, shape, steps, warmup, peak_bf16):
     calls = [f for _, f in named]
     t_w, _ = time_steps([b.fp8_quantize_weights], n, warmup, stage_events=False)
     _, per8 = time_steps(calls, n, warmup, stage_events=True)
-    t_8, t_16, ratio, pairs = interleave(calls, FusedStep(C, b).calls(), n, warmup)
+    bf16 = FusedStep(C, b).calls()
+    t_8, t_16, ratio, pairs = interleave(calls, bf16, n, warmup)
     fl = shape.fwdbwd_flops()
+    # delayed scaling of dP's codes (the previous step's amax; one pass of the
+    # SwiGLU backward instead of two), against the exact form and bf16
+    dnamed = b.fp8_forward_calls() + b.fp8_backward_calls(delayed=True)
+    dcalls = [f for _, f in dnamed]
+    _, perd = time_steps(dcalls, n, warmup, stage_events=True)
+    t_d, _, ratio_d8, pairs_d8 = interleave(dcalls, calls, n, warmup)
+    _, _, ratio_d16, pairs_d16 = interleave(dcalls, bf16, n, warmup)
+    names = [k for k, _ in dnamed]
+    delayed = {"fp8_fwdbwd_ms": t_d, "fp8_fwdbwd_tflops": fl / (t_d * 1e-3) / 1e12,
+               "speedup_vs_exact_fp8": ratio_d8, "speedup_vs_bf16": ratio_d16,
+               "swiglu_bwd_e5m2_ms": statistics.mean(perd[names.index("swiglu_bwd_e5m2")]),
+               "rounds_ms_vs_exact_fp8": rounds_ms(pairs_d8), "rounds_ms_vs_bf16": rounds_ms(pairs_d16)}
     return {"workload": shape.name, "fp8_fwdbwd_ms": t_8, "bf16_fwdbwd_ms": t_16, "speedup": ratio,
             "rounds_ms": rounds_ms(pairs), "fp8_fwdbwd_tflops": fl / (t_8 * 1e-3) / 1e12, "weight_quantize_ms": t_w / n,
             "stage_ms": {k: statistics.mean(v) for (k, _), v in zip(named, per8)},
             "timing": "rounds of (fp8, bf16) interleaved; speedup = median per-round time ratio; stage_ms from a "
                       "separate pass with an event between stages",
-            "formats": "e4m3 activations and weights, e5m2 gradients (dP, dH), one fp32 scale per tensor"}
+            "formats": "e4m3 activations and weights, e5m2 gradients (dP, dH), one fp32 scale per tensor",
+            "delayed_dP_scaling": delayed}
 
 
 def bench_qkv_rope(C, steps, warmup, M=8192, S=2048, d=4096, n_heads=32):

@@ -89,6 +89,7 @@ SIGNATURES = {
     "coda_fp8_quantize": (_INT, [_P, _P, _P, _P, _P, _I64, _I64, _P]),
     "coda_fp8_quantize_e5m2": (_INT, [_P, _P, _P, _P, _P, _I64, _I64, _P]),
     "coda_swiglu_bwd_fp8": (_INT, [_P, _P, _P, _P, _INT, _P, _P, _P, _I64, _I64, _I64, _P]),
+    "coda_swiglu_bwd_fp8_delayed": (_INT, [_P, _P, _P, _P, _INT, _P, _P, _P, _I64, _I64, _I64, _P]),
     "coda_gemm_fp8": (_INT, [_P, _P, _INT, _INT, _P, _P, _INT, _INT, _P, _P, _I64, _I64, _I64, _P, _P, _P]),
     "coda_gemm_dgrad_rmsbwd_fp8": (_INT, [_P, _P, _INT, _P, _P, _INT, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "coda_gemm_res_prms_fp8": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
@@ -592,6 +593,22 @@ def coda_swiglu_bwd_fp8(dY, z, rstd, fmt: int, dPq, amax_scale, c, d: int, strea
     _check(load_library().coda_swiglu_bwd_fp8(_h(dY), _ptr(dY, BF, "dY"), _ptr(z, BF, "z"), _ptr(rstd, F32, "rstd"),
                                               int(fmt), _ptr(dPq, U8, "dPq"), _ptr(amax_scale, F32, "amax_scale"),
                                               _ptr(c, F32, "c"), M, F, d, _stream(stream)), "coda_swiglu_bwd_fp8")
+
+
+def coda_swiglu_bwd_fp8_delayed(dY, z, rstd, fmt: int, dPq, amax_scale, c, d: int, stream=None):
+    """coda_swiglu_bwd_fp8 with delayed scaling: amax_scale[0] holds the
+    previous dP's amax on entry; on exit {this dP's amax, the scale used}
+    (see include/coda.h)."""
+    M, F = dY.shape
+    _shape(z, (M, 2 * F), "z")
+    _shape(rstd, (M,), "rstd")
+    _shape(dPq, (M, 2 * F), "dPq")
+    _shape(amax_scale, (2,), "amax_scale")
+    _shape(c, (M,), "c")
+    _check(load_library().coda_swiglu_bwd_fp8_delayed(
+        _h(dY), _ptr(dY, BF, "dY"), _ptr(z, BF, "z"), _ptr(rstd, F32, "rstd"), int(fmt), _ptr(dPq, U8, "dPq"),
+        _ptr(amax_scale, F32, "amax_scale"), _ptr(c, F32, "c"), M, F, d, _stream(stream)),
+        "coda_swiglu_bwd_fp8_delayed")
 
 
 def coda_gemm_fp8(A, a_mn_major: bool, a_format: int, sA, B, b_mn_major: bool, b_format: int, sB, C,

@@ -627,6 +627,32 @@ coda_status_t coda_swiglu_bwd_fp8(coda_handle_t h, const void* dY, const void* z
                                          rstd, amax_scale, static_cast<uint8_t*>(dPq), c, M, F, d, format));
 }
 
+coda_status_t coda_swiglu_bwd_fp8_delayed(coda_handle_t h, const void* dY, const void* z, const float* rstd,
+                                          int format, void* dPq, float* amax_scale, float* c, int64_t M, int64_t F,
+                                          int64_t d, void* stream) {
+  CODA_TRY(Check()
+               .handle(h)
+               .rows(M)
+               .mptr(dY, M)
+               .mptr(z, M)
+               .mptr(rstd, M)
+               .mptr(dPq, M)
+               .sptr(amax_scale)
+               .mptr(c, M)
+               .cols(F)
+               .cols(d)
+               .st);
+  if (format != 0 && format != 1) return CODA_ERR_INVALID_ARG;
+  if (M == 0) {
+    const float init[2] = {0.f, 1.f};
+    return from_cuda(cudaMemcpyAsync(amax_scale, init, sizeof(init), cudaMemcpyHostToDevice,
+                                     static_cast<cudaStream_t>(stream)));
+  }
+  return from_cuda(launch_swiglu_bwd_fp8_delayed(ctx_of(h, stream), static_cast<const bf16*>(dY),
+                                                 static_cast<const bf16*>(z), rstd, amax_scale,
+                                                 static_cast<uint8_t*>(dPq), c, M, F, d, format));
+}
+
 coda_status_t coda_gemm_fp8(coda_handle_t h, const void* A, int a_mn_major, int a_format, const float* sA,
                             const void* B, int b_mn_major, int b_format, const float* sB, void* C, int64_t M,
                             int64_t N, int64_t K, const float* row_scale, const void* col_scale, void* stream) {

@@ -203,6 +203,11 @@ cudaError_t launch_fp8_quantize(const LaunchCtx& c, const __nv_bfloat16* src, in
 cudaError_t launch_swiglu_bwd_fp8(const LaunchCtx& c, const __nv_bfloat16* dY, const __nv_bfloat16* z,
                                   const float* rstd, float* ws, uint8_t* dPq, float* cvec, int64_t M, int64_t F,
                                   int64_t d, int e5m2);
+// the same with delayed scaling: state = {amax, scale}; on entry state[0] is
+// the previous dP's amax, on exit {this dP's amax, the scale used} (one pass)
+cudaError_t launch_swiglu_bwd_fp8_delayed(const LaunchCtx& c, const __nv_bfloat16* dY, const __nv_bfloat16* z,
+                                          const float* rstd, float* state, uint8_t* dPq, float* cvec, int64_t M,
+                                          int64_t F, int64_t d, int e5m2);
 // unfused ablation kernels
 cudaError_t launch_add_rmsnorm(const LaunchCtx& c, const __nv_bfloat16* A, const __nv_bfloat16* R,
                                const __nv_bfloat16* g, __nv_bfloat16* H, float* rstd, __nv_bfloat16* Nrm, int64_t M,

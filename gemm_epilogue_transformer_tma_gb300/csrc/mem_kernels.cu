@@ -566,6 +566,76 @@ __global__ void __launch_bounds__(256) swiglu_bwd_fp8_kernel(const __nv_bfloat16
   }
 }
 
+// Delayed scaling of dP's codes: the scale comes from the amax of the previous
+// step's dP (state[0] on entry), so a single pass over dY and z writes c, the
+// codes and this dP's amax (state[0] on exit, for the next step).  The codes
+// saturate where this dP exceeds the previous range.
+//   rotate: state[1] = 2^fp8_scale_exp(state[0]); state[0] = 0
+//   pass:   codes = fp8(bf16(dP) / state[1]); state[0] = max |bf16(dP)|
+template <bool E5M2>
+__global__ void fp8_delayed_rotate_kernel(float* __restrict__ state) {
+  griddep_wait();
+  griddep_launch_dependents();
+  if (threadIdx.x == 0) {
+    state[1] = pow2f(fp8_scale_exp<E5M2>(state[0]));
+    state[0] = 0.f;
+  }
+}
+
+template <bool E5M2>
+__global__ void __launch_bounds__(256) swiglu_bwd_fp8_delayed_kernel(const __nv_bfloat16* __restrict__ dY,
+                                                                     const __nv_bfloat16* __restrict__ z,
+                                                                     const float* __restrict__ rstd,
+                                                                     float* __restrict__ cvec, int64_t F,
+                                                                     float inv_d, float* __restrict__ state,
+                                                                     uint2* __restrict__ dPq) {
+  griddep_wait();
+  griddep_launch_dependents();
+  __shared__ float red[8];
+  __shared__ float red_max[8];
+  // the scale is a power of two: its exponent gives the exact inverse
+  int e;
+  (void)frexpf(state[1], &e);
+  const float inv = pow2f(1 - e);
+  const int64_t m = blockIdx.x;
+  const float r = rstd[m];
+  const uint4* dy8 = reinterpret_cast<const uint4*>(dY + m * F);
+  const uint4* zg8 = reinterpret_cast<const uint4*>(z + m * 2 * F);
+  const uint4* zu8 = reinterpret_cast<const uint4*>(z + m * 2 * F + F);
+  const int64_t F8 = F / 8;
+  uint2* qg = dPq + m * 2 * F8;
+  uint2* qu = qg + F8;
+  float dot = 0.f, mx = 0.f;
+  for (int64_t j0 = threadIdx.x; j0 < F8; j0 += 2 * 256) {
+    const int64_t j1 = j0 + 256;
+    const bool two = j1 < F8;
+    const uint4 a0 = dy8[j0], b0 = zg8[j0], c0 = zu8[j0];
+    uint4 a1 = a0, b1 = b0, c1 = c0;
+    if (two) {
+      a1 = dy8[j1];
+      b1 = zg8[j1];
+      c1 = zu8[j1];
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      if (h == 1 && !two) break;
+      const int64_t j = h == 0 ? j0 : j1;
+      float og[8], ou[8], v[8];
+      dot += swiglu_bwd_vals(h == 0 ? a0 : a1, h == 0 ? b0 : b1, h == 0 ? c0 : c1, r, og, ou);
+      mx = absmax8(ou, absmax8(og, mx));
+      unpack_bf16x8(pack8(og), v);
+      qg[j] = fp8_codes8<E5M2>(v, inv);
+      unpack_bf16x8(pack8(ou), v);
+      qu[j] = fp8_codes8<E5M2>(v, inv);
+    }
+  }
+  const float tot = block_sum_256(dot, red);
+  if (threadIdx.x == 0) cvec[m] = r * r * inv_d * tot;
+  const float t = block_max_256(mx, red_max);
+  if (threadIdx.x == 0)
+    atomicMax(reinterpret_cast<unsigned int*>(state), __float_as_uint(__bfloat162float(__float2bfloat16_rn(t))));
+}
+
 // ---------------------------------------------------------------------------
 // unfused ablation kernels
 
@@ -803,6 +873,17 @@ cudaError_t launch_swiglu_bwd_fp8(const LaunchCtx& c, const __nv_bfloat16* dY, c
   if (e != cudaSuccess) return e;
   return launch_chained(c, e5m2 ? swiglu_bwd_fp8_kernel<true> : swiglu_bwd_fp8_kernel<false>, grid, dim3(256), 0, dY,
                         z, rstd, F, ws, reinterpret_cast<uint2*>(dPq));
+}
+
+cudaError_t launch_swiglu_bwd_fp8_delayed(const LaunchCtx& c, const __nv_bfloat16* dY, const __nv_bfloat16* z,
+                                          const float* rstd, float* state, uint8_t* dPq, float* cvec, int64_t M,
+                                          int64_t F, int64_t d, int e5m2) {
+  cudaError_t e = launch_chained(c, e5m2 ? fp8_delayed_rotate_kernel<true> : fp8_delayed_rotate_kernel<false>,
+                                 dim3(1), dim3(32), 0, state);
+  if (e != cudaSuccess) return e;
+  return launch_chained(c, e5m2 ? swiglu_bwd_fp8_delayed_kernel<true> : swiglu_bwd_fp8_delayed_kernel<false>,
+                        dim3(static_cast<unsigned>(M)), dim3(256), 0, dY, z, rstd, cvec, F,
+                        1.0f / static_cast<float>(d), state, reinterpret_cast<uint2*>(dPq));
 }
 
 cudaError_t launch_add_rmsnorm(const LaunchCtx& c, const __nv_bfloat16* A, const __nv_bfloat16* R,

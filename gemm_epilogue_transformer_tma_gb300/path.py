@@ -11,6 +11,7 @@ import torch
 
 from . import (CODA_EPI_PLAIN, CODA_EPI_SWIGLU, E4M3, E5M2, coda_bwd_workspace_bytes, coda_dg_combine,
                coda_fp8_quantize, coda_fp8_quantize_e5m2, coda_gemm_dgrad_rmsbwd_fp8, coda_gemm_fp8,
+               coda_swiglu_bwd_fp8_delayed,
                coda_gemm_res_prms_fp8, coda_gemm_rowscale_swiglu_fp8,
                coda_dgpart_rows, coda_fold_rmsnorm_weight, coda_gemm_dgrad_rmsbwd, coda_gemm_prms_rowscale_swiglu,
                coda_gemm_dgrad_rmsbwd_cpart, coda_gemm_dgrad_swiglu_bwd, coda_gemm_res_prms, coda_gemm_res_prms_g,
@@ -150,22 +151,23 @@ class BlockBuffers:
         if self.with_backward:
             self.backward()
 
-    def step_fp8(self):
+    def step_fp8(self, delayed: bool = False):
         """One pass with FP8 operands (weights quantised beforehand by
-        fp8_quantize_weights)."""
+        fp8_quantize_weights); delayed: dP's codes scaled by the previous
+        step's amax (one pass instead of two)."""
         self.forward_fp8()
         if self.with_backward:
-            self.backward_fp8()
+            self.backward_fp8(delayed)
 
     # -- CUDA graphs ----------------------------------------------------------
-    def capture_step(self, fp8: bool = False):
+    def capture_step(self, fp8: bool = False, delayed: bool = False):
         """Record one step (step or step_fp8) into a CUDA graph and return
         it; replay() then reruns it on whatever the input buffers hold.  One
         eager step runs first, so that the library handle, tensor maps and
         the fold's side stream exist before the capture (none of them may be
         created inside it).  The fold's fork to the side stream and its join
         back are recorded as graph edges."""
-        run = self.step_fp8 if fp8 else self.step
+        run = (lambda: self.step_fp8(delayed)) if fp8 else self.step
         run()
         torch.cuda.synchronize(self.X.device)
         graph = torch.cuda.CUDAGraph()
@@ -207,6 +209,7 @@ class BlockBuffers:
         # gradients dP, dH
         self.s_w = torch.empty(3, 2, dtype=F32, device=self.X.device)
         self.s_a = torch.empty(4, 2, dtype=F32, device=self.X.device)
+        self._dp_amax_ready = False  # s_a[2] holds an amax of dP (delayed scaling)
         if self.with_backward:
             self.dPq = torch.empty(M, N2, **u8)
             self.dHq = torch.empty(M, d, **u8)
@@ -235,17 +238,27 @@ class BlockBuffers:
                 self.Hq, self.s_a[1, 1:], self.W2gq, self.s_w[1, 1:], self.rstd, self.out, self.z)),
         ]
 
-    def fp8_backward_calls(self):
+    def _swiglu_bwd_codes(self, delayed: bool):
+        """dP's e5m2 codes and c.  Delayed: scaled by the previous step's
+        amax of dP, one pass (the first step of a run, with no previous amax,
+        takes the exact two-pass form)."""
+        if delayed and self._dp_amax_ready:
+            coda_swiglu_bwd_fp8_delayed(self.dY, self.z, self.rstd, E5M2, self.dPq, self.s_a[2], self.c, self.d)
+        else:
+            coda_swiglu_bwd_fp8(self.dY, self.z, self.rstd, E5M2, self.dPq, self.s_a[2], self.c, self.d)
+        self._dp_amax_ready = True
+
+    def fp8_backward_calls(self, delayed: bool = False):
         """The backward as named calls, with e5m2 gradients (dP, dH) against
         the e4m3 codes of the forward's activations and weights: the SwiGLU
-        backward writes dP's codes directly; dgrad2 runs the RMSNorm backward
-        in its epilogue; the weight gradients and the first layer's data
-        gradient are 8-bit GEMMs on the same codes read MN-major."""
+        backward writes dP's codes directly (with delayed, scaled by the
+        previous step's amax of dP, in one pass); dgrad2 runs the RMSNorm
+        backward in its epilogue; the weight gradients and the first layer's
+        data gradient are 8-bit GEMMs on the same codes read MN-major."""
         self._fp8_buffers()
         M, K1, d, N2 = self.M, self.K1, self.d, self.N2
         return [
-            ("swiglu_bwd_e5m2", lambda: coda_swiglu_bwd_fp8(self.dY, self.z, self.rstd, E5M2, self.dPq,
-                                                            self.s_a[2], self.c, self.d)),
+            ("swiglu_bwd_e5m2", lambda: self._swiglu_bwd_codes(delayed)),
             ("dgrad2_rmsbwd_fp8", lambda: coda_gemm_dgrad_rmsbwd_fp8(
                 self.dPq, E5M2, self.s_a[2, 1:], self.W2q, E4M3, self.s_w[2, 1:], self.H, self.g, self.c, self.dH,
                 self.dgpart)),
@@ -267,8 +280,8 @@ class BlockBuffers:
         for _, f in self.fp8_forward_calls():
             f()
 
-    def backward_fp8(self):
-        for _, f in self.fp8_backward_calls():
+    def backward_fp8(self, delayed: bool = False):
+        for _, f in self.fp8_backward_calls(delayed):
             f()
 
     # -- unfused ablation -----------------------------------------------------

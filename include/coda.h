@@ -450,6 +450,21 @@ coda_status_t coda_swiglu_bwd_fp8(coda_handle_t h, const void* dY, const void* z
                                   void* dPq, float* amax_scale, float* c, int64_t M, int64_t F, int64_t d,
                                   void* stream);
 
+/* coda_swiglu_bwd_fp8 with delayed scaling: the scale of dP's codes comes from
+ * the absolute maximum of the previous step's dP instead of this one's, so a
+ * single pass over dY and z writes c, the codes and this dP's maximum.
+ * amax_scale fp32 [2]: on entry amax_scale[0] holds the previous maximum (as
+ * left by coda_swiglu_bwd_fp8 or by this call on the previous step); on exit
+ * it holds {max |bf16(dP)| of this step, the scale used}, the scale being the
+ * power of two that coda_fp8_quantize(_e5m2) derives from the entry maximum.
+ * Codes of elements beyond the previous range saturate (+-448 e4m3, +-57344
+ * e5m2 times the scale).  The first step of a run, with no previous maximum,
+ * uses coda_swiglu_bwd_fp8.  Other arguments as coda_swiglu_bwd_fp8; M == 0
+ * writes {0, 1}. */
+coda_status_t coda_swiglu_bwd_fp8_delayed(coda_handle_t h, const void* dY, const void* z, const float* rstd,
+                                          int format, void* dPq, float* amax_scale, float* c, int64_t M, int64_t F,
+                                          int64_t d, void* stream);
+
 /* Plain GEMM on 8-bit operands (the mainloop of the method with FP8 inputs):
  *   C[m][n] = bf16( row_scale[m] * col_scale[n] * sA * sB * sum_k A[m][k] B[k][n] )
  * A codes [M][K] (a_mn_major = 0) or [K][M] (1); B codes [N][K] (0) or [K][N]

@@ -135,6 +135,90 @@ def test_swiglu_bwd_fp8_codes(fmt, name, M, F):
     assert_elem(c, c_ref, "c")
 
 
+def _swiglu_case(M, F, seed, dy_scale=1.0):
+    g = torch.Generator().manual_seed(seed)
+    dY = (dy_scale * torch.randn(M, F, generator=g)).to(torch.bfloat16).cuda()
+    z = (2.0 * torch.randn(M, 2 * F, generator=g)).to(torch.bfloat16).cuda()
+    rstd = (0.5 + torch.rand(M, generator=g)).cuda()
+    return dY, z, rstd
+
+
+@pytest.mark.parametrize("fmt,name", [(C.E4M3, "e4m3"), (C.E5M2, "e5m2")])
+@pytest.mark.parametrize("M,F", [(300, 272), (64, 1040)])
+@pytest.mark.parametrize("dy_scale", [1.0, 3000.0], ids=["in_range", "saturating"])
+def test_swiglu_bwd_fp8_delayed_codes(fmt, name, M, F, dy_scale):
+    """Delayed scaling: step A (exact, two passes) leaves its amax in the
+    state; step B's single pass quantises its bf16 dP with the scale the
+    oracle derives from A's amax (saturating where B exceeds A's range, the
+    second case), reports B's own amax for the next step, and writes the c
+    of coda_swiglu_bwd bit for bit."""
+    d = 256
+    dPq = torch.empty(M, 2 * F, dtype=torch.uint8, device="cuda")
+    sc = torch.empty(2, device="cuda")
+    c = torch.empty(M, device="cuda")
+    dP16 = torch.empty(M, 2 * F, dtype=torch.bfloat16, device="cuda")
+    c16 = torch.empty(M, device="cuda")
+    dYa, za, ra = _swiglu_case(M, F, 11)
+    C.coda_swiglu_bwd_fp8(dYa, za, ra, fmt, dPq, sc, c, d)
+    C.coda_swiglu_bwd(dYa, za, ra, dP16, c16, d)
+    torch.cuda.synchronize()
+    prev_scale = O.fp8_scale(dP16.float().cpu().numpy(), name)
+    dYb, zb, rb = _swiglu_case(M, F, 12, dy_scale)
+    C.coda_swiglu_bwd_fp8_delayed(dYb, zb, rb, fmt, dPq, sc, c, d)
+    C.coda_swiglu_bwd(dYb, zb, rb, dP16, c16, d)
+    torch.cuda.synchronize()
+    assert_device_ok()
+    v = dP16.float().cpu().numpy()
+    assert np.float32(sc[1].item()) == prev_scale
+    assert np.float32(sc[0].item()) == np.float32(np.abs(v).max())
+    codes = dPq.cpu().numpy()
+    assert np.array_equal(codes, O.fp8_quantize(v, prev_scale, name))
+    fmax = 448.0 if name == "e4m3" else 57344.0
+    if dy_scale > 1.0:   # B far outside A's range: the codes saturate (and still match)
+        assert (np.abs(v) / prev_scale > fmax).any()
+    assert torch.equal(c, c16)
+
+
+def test_fp8_delayed_scaling_end_to_end_and_graph():
+    """Steps with delayed dP scaling: after an exact first step, a delayed
+    step on new inputs meets the FP8 end-to-end bounds against the oracle;
+    a CUDA graph of the delayed step replays bit-identically to the same
+    eager sequence."""
+    s = SHAPES["ragged"]
+    xa = {k: v.cuda() for k, v in block_inputs(s, 0, "cpu").items()}
+    xb = {k: v.cuda() for k, v in block_inputs(s, 1, "cpu").items()}
+    ins = ("X", "R", "dY")
+    b = BlockBuffers({k: v.clone() for k, v in xa.items()})
+    b.fp8_quantize_weights()
+    b.step_fp8(delayed=True)             # the first step takes the exact form
+    eager = []
+    for x in (xb, xa, xb):
+        for k in ins:
+            getattr(b, k).copy_(x[k])
+        b.step_fp8(delayed=True)
+        torch.cuda.synchronize()
+        eager.append({k: getattr(b, k).clone() for k in ("out", "dH", "dX", "dW1t", "dW2t", "dg")})
+    assert_device_ok()
+    ref = O.block_backward(*(f64(xa[k]) if k in ("W1t", "g", "W2t") else f64(xb[k])
+                             for k in ("X", "W1t", "R", "g", "W2t", "dY")), EPS, True)
+    bounds = {"out": 8e-2, "dR": 0.15, "dW2t": 0.15, "dg": 0.15, "dX": 0.2, "dW1t": 0.2}
+    for k_gpu, k_ref in (("out", "out"), ("dH", "dR"), ("dW2t", "dW2t"), ("dg", "dg"), ("dX", "dX"),
+                         ("dW1t", "dW1t")):
+        assert_frob(eager[2][k_gpu], ref[k_ref], f"fp8 delayed {k_gpu} e2e", tol=bounds[k_ref])
+
+    g = BlockBuffers({k: v.clone() for k, v in xa.items()})
+    g.fp8_quantize_weights()
+    g.capture_step(fp8=True, delayed=True)   # its eager step is the exact first step
+    for x, want in zip((xb, xa, xb), eager):
+        for k in ins:
+            getattr(g, k).copy_(x[k])
+        g.replay()
+        torch.cuda.synchronize()
+        for k, v in want.items():
+            assert torch.equal(getattr(g, k), v), k
+    assert_device_ok()
+
+
 def test_swiglu_bwd_fp8_empty():
     z0 = torch.empty(0, 16, dtype=torch.bfloat16, device="cuda")
     sc = torch.full((2,), 9.0, device="cuda")
