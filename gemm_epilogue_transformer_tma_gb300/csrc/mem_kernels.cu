@@ -139,17 +139,28 @@ __device__ __forceinline__ float swiglu_bwd_vals(const uint4& dyq, const uint4& 
   unpack_bf16x8(dyq, dy);
   unpack_bf16x8(zgq, zg);
   unpack_bf16x8(zuq, zu);
-  float dot = 0.f;
+  // columns in pairs, on packed fp32 pairs; the two lanes' dot products stay
+  // apart until the end
+  const float2 one = make_float2(1.0f, 1.0f), neg_one = make_float2(-1.0f, -1.0f), r2 = make_float2(r, r);
+  float2 dot = make_float2(0.f, 0.f);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float s = sigmoid_f(zg[i]);
-    const float dzu = dy[i] * zg[i] * s;
-    const float dzg = dy[i] * zu[i] * s * (1.0f + zg[i] * (1.0f - s));
-    dot = fmaf(dzg, zg[i], fmaf(dzu, zu[i], dot));
-    og[i] = r * dzg;
-    ou[i] = r * dzu;
+  for (int i = 0; i < 8; i += 2) {
+    const float2 y = make_float2(dy[i], dy[i + 1]);
+    const float2 g = make_float2(zg[i], zg[i + 1]);
+    const float2 u = make_float2(zu[i], zu[i + 1]);
+    const float2 s = make_float2(sigmoid_f(g.x), sigmoid_f(g.y));
+    const float2 ys = f2_mul(y, s);
+    const float2 dzu = f2_mul(ys, g);                       // dY zg s
+    const float2 w = f2_fma(g, f2_fma(s, neg_one, one), one);  // 1 + zg (1 - s)
+    const float2 dzg = f2_mul(f2_mul(ys, u), w);            // dY zu s (1 + zg (1 - s))
+    dot = f2_fma(dzg, g, f2_fma(dzu, u, dot));
+    const float2 pg = f2_mul(r2, dzg), pu = f2_mul(r2, dzu);
+    og[i] = pg.x;
+    og[i + 1] = pg.y;
+    ou[i] = pu.x;
+    ou[i + 1] = pu.y;
   }
-  return dot;
+  return dot.x + dot.y;
 }
 
 __device__ __forceinline__ float swiglu_bwd_chunk(const uint4& dyq, const uint4& zgq, const uint4& zuq, float r,
