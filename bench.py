@@ -840,7 +840,8 @@ def main():
         if "e2e" in extras:
             line["e2e"] = extras.pop("e2e")
         line.update(extras)
-        if not args.no_cpu_baseline:
+        if not args.no_cpu_baseline and world == 1:
+            # the oracle's host-core baseline: rank 0 of a single-GPU run only
             line["cpu_baseline"] = cpu_oracle_baseline(shape)
             line["cpu_baseline"]["single_core_fwd"] = cpu_oracle_single_core()
         print(json.dumps(line), flush=True)
