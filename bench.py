@@ -473,6 +473,25 @@ def bench_fp8_fwdbwd(C, b, shape, steps, warmup, peak_bf16):
     t_d, _, ratio_d8, pairs_d8 = interleave(dcalls, calls, n, warmup)
     _, _, ratio_d16, pairs_d16 = interleave(dcalls, bf16, n, warmup)
     names = [k for k, _ in dnamed]
+    # the FP8 step end to end through the C ABI with host buffers (the block
+    # executor in FP8 mode, weights quantised once beforehand)
+    from gemm_epilogue_transformer_tma_gb300.path import HostBlockStepper
+    st = HostBlockStepper(b.W1t, b.g, b.W2t, shape.M, shape.eps, fp8=True)
+    host = {k: getattr(b, k).cpu().pin_memory() for k in ("X", "R", "dY")}
+    host.update(st.host_buffers(dX=True))
+    for _ in range(3):
+        st.submit(host["X"], host["R"], host["dY"], dX=host["dX"])
+    st.sync()
+    t0 = time.perf_counter()
+    for _ in range(n):
+        st.submit(host["X"], host["R"], host["dY"], dX=host["dX"])
+    st.sync()
+    e2e_ms = (time.perf_counter() - t0) * 1e3 / n
+    st.close()
+    del st, host
+    e2e = {"value": fl / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e2e_ms, "steps": n,
+           "api": "coda_block_create(CODA_BLOCK_FP8) / coda_block_step_host / coda_block_sync (host buffers)",
+           "timing": "host wall clock, synchronize at both ends; H2D of X, R, dY and D2H of dX inside"}
     delayed = {"fp8_fwdbwd_ms": t_d, "fp8_fwdbwd_tflops": fl / (t_d * 1e-3) / 1e12,
                "speedup_vs_exact_fp8": ratio_d8, "speedup_vs_bf16": ratio_d16,
                "swiglu_bwd_e5m2_ms": statistics.mean(perd[names.index("swiglu_bwd_e5m2")]),
@@ -483,7 +502,7 @@ def bench_fp8_fwdbwd(C, b, shape, steps, warmup, peak_bf16):
             "timing": "rounds of (fp8, bf16) interleaved; speedup = median per-round time ratio; stage_ms from a "
                       "separate pass with an event between stages",
             "formats": "e4m3 activations and weights, e5m2 gradients (dP, dH), one fp32 scale per tensor",
-            "delayed_dP_scaling": delayed}
+            "delayed_dP_scaling": delayed, "e2e": e2e}
 
 
 def bench_qkv_rope(C, steps, warmup, M=8192, S=2048, d=4096, n_heads=32):

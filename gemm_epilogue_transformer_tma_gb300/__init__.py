@@ -75,9 +75,10 @@ SIGNATURES = {
     "coda_gemm_rowscale_swiglu_bwd": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
                                              _I64, _I64, _I64, _P]),
     "coda_gemm_res_prms_bwd": (_INT, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
-    "coda_block_arena_bytes": (_SZ, [_I64, _I64, _I64, _I64, _INT]),
-    "coda_block_create": (_INT, [_P, _I64, _I64, _I64, _I64, _F32, _INT, _P, _P, _P, _P, _P, _P, _P, _SZ,
+    "coda_block_arena_bytes": (_SZ, [_I64, _I64, _I64, _I64, _U32]),
+    "coda_block_create": (_INT, [_P, _I64, _I64, _I64, _I64, _F32, _U32, _P, _P, _P, _P, _P, _P, _P, _SZ,
                                  ctypes.POINTER(_P)]),
+    "coda_block_quantize_weights": (_INT, [_P]),
     "coda_block_step_host": (_INT, [_P, _P, _P, _P, _P, _P, _P, ctypes.POINTER(_I64)]),
     "coda_block_wait_step": (_INT, [_P, _I64]),
     "coda_block_sync": (_INT, [_P, ctypes.POINTER(ctypes.c_int32)]),
@@ -457,15 +458,22 @@ def _host_ptr(t: torch.Tensor | None, dtype, shape, name) -> int | None:
     return t.data_ptr()
 
 
-def coda_block_arena_bytes(M: int, K1: int, d: int, N2: int, backward: bool) -> int:
-    return load_library().coda_block_arena_bytes(M, K1, d, N2, int(backward))
+CODA_BLOCK_BACKWARD = 1
+CODA_BLOCK_FP8 = 2
+CODA_BLOCK_FP8_DELAYED = 4
 
 
-def coda_block_create(M: int, K1: int, d: int, N2: int, eps: float, backward: bool, W1t, g, W2t,
+def coda_block_arena_bytes(M: int, K1: int, d: int, N2: int, flags: int) -> int:
+    return load_library().coda_block_arena_bytes(M, K1, d, N2, int(flags))
+
+
+def coda_block_create(M: int, K1: int, d: int, N2: int, eps: float, flags: int, W1t, g, W2t,
                       dW1t, dW2t, dg, arena) -> int:
     """Create a block step executor (include/coda.h) on the weights' device;
-    returns its handle.  arena: a uint8 device tensor of at least
-    coda_block_arena_bytes bytes, kept alive by the caller."""
+    returns its handle.  flags: CODA_BLOCK_* bits.  arena: a uint8 device
+    tensor of at least coda_block_arena_bytes bytes, kept alive by the
+    caller."""
+    backward = bool(flags & CODA_BLOCK_BACKWARD)
     _shape(W1t, (d, K1), "W1t")
     _shape(g, (d,), "g")
     _shape(W2t, (N2, d), "W2t")
@@ -476,7 +484,7 @@ def coda_block_create(M: int, K1: int, d: int, N2: int, eps: float, backward: bo
     out = _P()
     with torch.cuda.device(W1t.device):
         _check(load_library().coda_block_create(
-            _h(W1t), M, K1, d, N2, eps, int(backward), _ptr(W1t, BF, "W1t"), _ptr(g, BF, "g"), _ptr(W2t, BF, "W2t"),
+            _h(W1t), M, K1, d, N2, eps, int(flags), _ptr(W1t, BF, "W1t"), _ptr(g, BF, "g"), _ptr(W2t, BF, "W2t"),
             _ptr(dW1t, BF, "dW1t"), _ptr(dW2t, BF, "dW2t"), _ptr(dg, F32, "dg"), _ptr(arena, torch.uint8, "arena"),
             arena.numel(), ctypes.byref(out)), "coda_block_create")
     return out.value
@@ -491,6 +499,11 @@ def coda_block_step_host(blk: int, M: int, K1: int, d: int, F: int, X, R, dY=Non
         _host_ptr(out, BF, (M, F), "out"), _host_ptr(dX, BF, (M, K1), "dX"), _host_ptr(dR, BF, (M, d), "dR"),
         ctypes.byref(sid)), "coda_block_step_host")
     return sid.value
+
+
+def coda_block_quantize_weights(blk: int):
+    """FP8 executors: enqueue the e4m3 quantisation of the weights."""
+    _check(load_library().coda_block_quantize_weights(blk), "coda_block_quantize_weights")
 
 
 def coda_block_wait_step(blk: int, step: int):

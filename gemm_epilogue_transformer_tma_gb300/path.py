@@ -18,7 +18,8 @@ from . import (CODA_EPI_PLAIN, CODA_EPI_SWIGLU, E4M3, E5M2, coda_bwd_workspace_b
                coda_gemm_res_prms_bwd, coda_gemm_rowscale_swiglu, coda_gemm_rowscale_swiglu_bwd,
                coda_gemm_wgrad_gscale, coda_prms_num_tiles, coda_rstd_combine, coda_swiglu_bwd, coda_swiglu_bwd_fp8,
                coda_unfused_bwd, coda_unfused_fwd, coda_unfused_workspace_bytes)
-from . import (coda_block_arena_bytes, coda_block_create, coda_block_destroy, coda_block_step_host,
+from . import (CODA_BLOCK_BACKWARD, CODA_BLOCK_FP8, CODA_BLOCK_FP8_DELAYED, coda_block_arena_bytes,
+               coda_block_create, coda_block_destroy, coda_block_quantize_weights, coda_block_step_host,
                coda_block_stream, coda_block_sync, coda_block_wait_step, STATUS_NAMES)
 
 BF = torch.bfloat16
@@ -303,9 +304,13 @@ class HostBlockStepper:
     gradients, nothing more.
 
     W1t[d,K1], g[d], W2t[N2,d]: device bf16 weights, read by every step.
-    With backward, every step overwrites dW1t, dW2t and dg (device)."""
+    With backward, every step overwrites dW1t, dW2t and dg (device).  With
+    fp8, the steps run on 8-bit operands (delayed: dP's codes scaled by the
+    previous step's amax); quantize_weights() must follow every weight
+    update (the constructor calls it once)."""
 
-    def __init__(self, W1t, g, W2t, M: int, eps: float = 1e-5, backward: bool = True):
+    def __init__(self, W1t, g, W2t, M: int, eps: float = 1e-5, backward: bool = True, fp8: bool = False,
+                 delayed: bool = False):
         dev = W1t.device
         self.d, self.K1 = W1t.shape
         self.N2 = W2t.shape[0]
@@ -317,10 +322,20 @@ class HostBlockStepper:
         self.dW1t = torch.empty(self.d, self.K1, dtype=BF, **e) if backward else None
         self.dW2t = torch.empty(self.N2, self.d, dtype=BF, **e) if backward else None
         self.dg = torch.empty(self.d, dtype=F32, **e) if backward else None
-        nbytes = coda_block_arena_bytes(M, self.K1, self.d, self.N2, backward)
+        flags = (CODA_BLOCK_BACKWARD if backward else 0) | (CODA_BLOCK_FP8 if fp8 else 0) | \
+            (CODA_BLOCK_FP8_DELAYED if delayed else 0)
+        nbytes = coda_block_arena_bytes(M, self.K1, self.d, self.N2, flags)
         self.arena = torch.empty(max(1, nbytes), dtype=torch.uint8, **e)
-        self.blk = coda_block_create(M, self.K1, self.d, self.N2, eps, backward, W1t, g, W2t,
+        self.blk = coda_block_create(M, self.K1, self.d, self.N2, eps, flags, W1t, g, W2t,
                                      self.dW1t, self.dW2t, self.dg, self.arena)
+        self.fp8 = fp8
+        if fp8:
+            self.quantize_weights()
+
+    def quantize_weights(self):
+        """FP8: enqueue the weights' e4m3 quantisation on the executor's
+        stream (after every weight update)."""
+        coda_block_quantize_weights(self.blk)
 
     def host_buffers(self, out: bool = False, dX: bool = True, dR: bool = False) -> dict:
         """Page-locked host tensors for the results a step should read back."""

@@ -325,28 +325,48 @@ coda_status_t coda_gemm_res_prms_bwd(coda_handle_t h, const void* dH, const void
  * executor may be used from one host thread at a time. */
 typedef struct coda_block_s* coda_block_t;
 
-/* Device bytes the executor needs for a problem (its arena): W2g [N2][d],
- * H, psum, rstd, z and the backward workspace once, and X, R, out (and dY,
- * dH, dX) in each of two slots, every buffer 256-byte aligned.  0 for an
- * invalid shape. */
-size_t coda_block_arena_bytes(int64_t M, int64_t K1, int64_t d, int64_t N2, int backward);
+/* flags of coda_block_create */
+#define CODA_BLOCK_BACKWARD 1u    /* forward + backward (else forward only) */
+#define CODA_BLOCK_FP8 2u         /* 8-bit operands: e4m3 activations and weights, e5m2 gradients */
+#define CODA_BLOCK_FP8_DELAYED 4u /* with FP8 and backward: dP's codes scaled by the previous step's
+                                     amax (coda_swiglu_bwd_fp8_delayed) after the first step */
+
+/* Device bytes the executor needs for a problem (its arena): H, psum, rstd
+ * and z once; W2g and the backward workspace (bf16), or the weight,
+ * activation and gradient codes with their scales, c and the dg partials
+ * (FP8); and X, R, out (and dY, dH, dX) in each of two slots, every buffer
+ * 256-byte aligned.  0 for an invalid shape. */
+size_t coda_block_arena_bytes(int64_t M, int64_t K1, int64_t d, int64_t N2, uint32_t flags);
 
 /* Create an executor on the current CUDA device, which must be the handle's.
  * Shapes as coda_gemm_res_prms / coda_gemm_rowscale_swiglu with SwiGLU
- * (N2 = 2F, F a multiple of 8); eps > 0 is the RMSNorm epsilon.
+ * (N2 = 2F, F a multiple of 8; with CODA_BLOCK_FP8 K1 and d multiples of 16
+ * and F of 16); eps > 0 is the RMSNorm epsilon; flags a combination of
+ * CODA_BLOCK_* (CODA_ERR_INVALID_ARG for unknown bits, or for
+ * CODA_BLOCK_FP8_DELAYED without FP8 and BACKWARD).
  * Weights (device, bf16, caller-owned, read by every step): W1t [d][K1], g
- * [d], W2t [N2][d].  With backward = 1 every step overwrites the weight
- * gradients dW1t (bf16 [d][K1]), dW2t (bf16 [N2][d]) and dg (fp32 [d]),
- * device buffers the caller owns; with backward = 0 they may be NULL.  arena:
+ * [d], W2t [N2][d].  With CODA_BLOCK_BACKWARD every step overwrites the
+ * weight gradients dW1t (bf16 [d][K1]), dW2t (bf16 [N2][d]) and dg (fp32
+ * [d]), device buffers the caller owns; without it they may be NULL.  arena:
  * caller-owned device memory of at least coda_block_arena_bytes bytes,
  * 16-byte aligned, used only by this executor until it is destroyed.  The
  * executor creates four CUDA streams and its events; it allocates no device
  * memory.  *out receives the executor. */
 coda_status_t coda_block_create(coda_handle_t h, int64_t M, int64_t K1, int64_t d, int64_t N2, float eps,
-                                int backward, const void* W1t, const void* g, const void* W2t, void* dW1t,
+                                uint32_t flags, const void* W1t, const void* g, const void* W2t, void* dW1t,
                                 void* dW2t, float* dg, void* arena, size_t arena_bytes, coda_block_t* out);
 
-/* Enqueue one step.  Host pointers, each page-locked (cudaHostAlloc) or
+/* FP8 executors: enqueue, on the executor's compute stream, the e4m3
+ * quantisation of the weights the steps use (W1, W2 with g folded in, and
+ * W2 alone for the backward), as coda_fp8_quantize does.  Call it after
+ * coda_block_create and after every update of W1t, g or W2t; an FP8 step
+ * before the first call is refused with CODA_ERR_INVALID_ARG.  A no-op for
+ * bf16 executors. */
+coda_status_t coda_block_quantize_weights(coda_block_t b);
+
+/* Enqueue one step (bf16, or FP8 per the executor's flags: X and H quantised
+ * in the step, the FP8 backward of coda_swiglu_bwd_fp8 and the 8-bit GEMMs).
+ * Host pointers, each page-locked (cudaHostAlloc) or
  * registered (cudaHostRegister) memory, else CODA_ERR_INVALID_ARG:
  *   X bf16 [M][K1], R bf16 [M][d] (required), dY bf16 [M][F] (required with
  *   backward, NULL without);

@@ -59,6 +59,8 @@ def test_host_queries(lib):
     assert lib.coda_block_arena_bytes(8, 64, 64, 0, 1) == 0
     assert lib.coda_block_arena_bytes(M, 4096, d, N2, 1) > lib.coda_block_arena_bytes(M, 4096, d, N2, 0) > \
         2 * M * (4096 + d + N2 // 2) * 2
+    # FP8: codes instead of W2g and the bf16 workspace, so a smaller arena
+    assert 0 < lib.coda_block_arena_bytes(M, 4096, d, N2, 3) < lib.coda_block_arena_bytes(M, 4096, d, N2, 1)
     assert lib.coda_status_string(0) == b"ok"
     assert b"time limit" in lib.coda_status_string(6)
 
@@ -70,6 +72,7 @@ def test_null_handle_is_rejected_without_a_gpu(lib):
     assert lib.coda_destroy(None) == 0
     out = ctypes.c_void_p()
     assert lib.coda_block_create(None, 8, 64, 64, 128, 1e-5, 1, *([None] * 7), 0, ctypes.byref(out)) == 1
+    assert lib.coda_block_quantize_weights(None) == 1
     assert lib.coda_block_step_host(None, None, None, None, None, None, None, None) == 1
     assert lib.coda_block_sync(None, None) == 1
     assert lib.coda_block_destroy(None) == 0

@@ -145,7 +145,7 @@ def test_argument_errors():
     fw.close()
 
     # an arena one byte short, and a non-SwiGLU-sized N2
-    need = C.coda_block_arena_bytes(s.M, s.K1, s.d, s.N2, True)
+    need = C.coda_block_arena_bytes(s.M, s.K1, s.d, s.N2, C.CODA_BLOCK_BACKWARD)
     arena = torch.empty(need, dtype=torch.uint8, device="cuda")
     dW1t = torch.empty(s.d, s.K1, dtype=torch.bfloat16, device="cuda")
     dW2t = torch.empty(s.N2, s.d, dtype=torch.bfloat16, device="cuda")
@@ -158,6 +158,8 @@ def test_argument_errors():
     assert out.value is None
     assert lib.coda_block_create(h, s.M, s.K1, s.d, 520, s.eps, 1, *args, need, ctypes.byref(out)) == 2
     assert lib.coda_block_create(h, s.M, s.K1, s.d, s.N2, 0.0, 1, *args, need, ctypes.byref(out)) == 1
+    assert lib.coda_block_create(h, s.M, s.K1, s.d, s.N2, s.eps, 8, *args, need, ctypes.byref(out)) == 1
+    assert lib.coda_block_create(h, s.M, s.K1, s.d, s.N2, s.eps, 1 | 4, *args, need, ctypes.byref(out)) == 1
     assert lib.coda_block_create(h, s.M, s.K1, s.d, s.N2, s.eps, 1, *args, need, ctypes.byref(out)) == 0
     assert lib.coda_block_destroy(out) == 0
 
@@ -183,3 +185,59 @@ def test_work_on_the_executor_stream_is_ordered_between_steps():
         assert torch.equal(o["out"], ref.out.cpu())
         assert torch.equal(o["dX"], ref.dX.cpu())
     st.close()
+
+
+FP8_SHAPE = BlockShape("ragged_fp8", 300, 208, 336, 544)
+
+
+@pytest.mark.parametrize("delayed", [False, True], ids=["exact", "delayed"])
+def test_fp8_steps_match_separate_calls(delayed):
+    """FP8 executor steps on host buffers bit-identical to BlockBuffers'
+    FP8 steps on the same inputs in the same order (with delayed scaling
+    the dP state carries from step to step on both sides)."""
+    s = FP8_SHAPE
+    w = {k: v for k, v in block_inputs(s, 0, "cuda").items() if k in WEIGHTS}
+    steps = [block_inputs(s, seed, "cuda") for seed in (1, 2, 3, 4)]
+    st = HostBlockStepper(w["W1t"], w["g"], w["W2t"], s.M, s.eps, fp8=True, delayed=delayed)
+    host_in = [{k: pinned(x[k]) for k in ("X", "R", "dY")} for x in steps]
+    outs = [st.host_buffers(out=True, dX=True, dR=True) for _ in steps]
+    for hi, o in zip(host_in, outs):
+        st.submit(hi["X"], hi["R"], hi["dY"], **o)
+    st.sync()
+    ref = BlockBuffers(dict(w, **{k: steps[0][k].clone() for k in ("X", "R", "dY")}))
+    ref.fp8_quantize_weights()
+    for i, x in enumerate(steps):
+        for k in ("X", "R", "dY"):
+            getattr(ref, k).copy_(x[k])
+        ref.step_fp8(delayed=delayed)
+        torch.cuda.synchronize()
+        for k_host, k_ref in (("out", "out"), ("dX", "dX"), ("dR", "dH")):
+            assert torch.equal(outs[i][k_host], getattr(ref, k_ref).cpu()), (i, k_host)
+    assert_device_ok()
+    for k in ("dW1t", "dW2t", "dg"):
+        assert torch.equal(getattr(st, k), getattr(ref, k)), k
+    st.close()
+
+
+def test_fp8_step_needs_quantised_weights():
+    s = FP8_SHAPE
+    x = block_inputs(s, 0, "cuda")
+    lib = C.load_library()
+    flags = C.CODA_BLOCK_BACKWARD | C.CODA_BLOCK_FP8
+    need = C.coda_block_arena_bytes(s.M, s.K1, s.d, s.N2, flags)
+    arena = torch.empty(need, dtype=torch.uint8, device="cuda")
+    grads = [torch.empty(s.d, s.K1, dtype=torch.bfloat16, device="cuda"),
+             torch.empty(s.N2, s.d, dtype=torch.bfloat16, device="cuda"),
+             torch.empty(s.d, dtype=torch.float32, device="cuda")]
+    out = ctypes.c_void_p()
+    assert lib.coda_block_create(C.handle(), s.M, s.K1, s.d, s.N2, s.eps, flags, x["W1t"].data_ptr(),
+                                 x["g"].data_ptr(), x["W2t"].data_ptr(), *(t.data_ptr() for t in grads),
+                                 arena.data_ptr(), need, ctypes.byref(out)) == 0
+    hi = {k: pinned(x[k]) for k in ("X", "R", "dY")}
+    assert lib.coda_block_step_host(out, hi["X"].data_ptr(), hi["R"].data_ptr(), hi["dY"].data_ptr(), None, None,
+                                    None, None) == 1
+    assert lib.coda_block_quantize_weights(out) == 0
+    assert lib.coda_block_step_host(out, hi["X"].data_ptr(), hi["R"].data_ptr(), hi["dY"].data_ptr(), None, None,
+                                    None, None) == 0
+    assert lib.coda_block_sync(out, None) == 0
+    assert lib.coda_block_destroy(out) == 0
