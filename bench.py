@@ -207,6 +207,20 @@ def aggregate_value(step_flops: float, ms: float, world: int) -> float:
     return world * step_flops / (ms * 1e-3) / 1e12
 
 
+class nvtx:
+    """An NVTX range around a region of the bench (a profiler can restrict a
+    capture to it, e.g. ncu --nvtx --nvtx-include "stage_pass/")."""
+
+    def __init__(self, name):
+        self.name = name
+
+    def __enter__(self):
+        torch.cuda.nvtx.range_push(self.name)
+
+    def __exit__(self, *exc):
+        torch.cuda.nvtx.range_pop()
+
+
 def time_steps(calls, steps, warmup, stage_events=True):
     """Run warmup + timed steps; return (total_ms, per-stage ms lists)."""
     stream = torch.cuda.current_stream()
@@ -716,9 +730,11 @@ def main():
         # headline: events only around the whole region, so nothing sits
         # between launches (an event between kernels would also stop the
         # next kernel's prologue from overlapping the previous one's tail)
-        total_ms, _ = time_steps(calls, args.steps, 0, stage_events=False)
+        with nvtx("headline"):
+            total_ms, _ = time_steps(calls, args.steps, 0, stage_events=False)
         # per-stage breakdown: a second pass with an event between stages
-        _, per = time_steps(calls, args.steps, 0, stage_events=True)
+        with nvtx("stage_pass"):
+            _, per = time_steps(calls, args.steps, 0, stage_events=True)
     barrier()
     st, bits = C.coda_sync_status()
     if st != 0:
@@ -765,7 +781,8 @@ def main():
         n_e2e = max(3, args.steps)
         barrier()
         t0 = time.perf_counter()
-        e2e_steps(n_e2e)
+        with nvtx("e2e"):
+            e2e_steps(n_e2e)
         barrier()
         e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3 / n_e2e, dist, "cuda")
         h2d = sum(host[k].numel() * host[k].element_size() for k in ins)
@@ -811,25 +828,33 @@ def main():
                                                 "per-round time ratio"}
         del bu
         torch.cuda.empty_cache()
-        extras["memory_kernels"] = bench_memory_kernels(C, b, shape, peaks["hbm_gbs"])
+        with nvtx("memory_kernels"):
+            extras["memory_kernels"] = bench_memory_kernels(C, b, shape, peaks["hbm_gbs"])
         torch.cuda.empty_cache()
         if shape.backward:
-            extras["next_swiglu_bwd_in_down_proj_dgrad"] = bench_down_proj_swiglu_bwd(C, b, shape, args.steps,
-                                                                                    args.warmup)
+            with nvtx("next_swiglu_bwd_in_down_proj_dgrad"):
+                extras["next_swiglu_bwd_in_down_proj_dgrad"] = bench_down_proj_swiglu_bwd(C, b, shape, args.steps,
+                                                                                        args.warmup)
             torch.cuda.empty_cache()
-        extras["next_fp8_forward"] = bench_fp8_forward(C, b, shape, args.steps, args.warmup, peak)
+        with nvtx("next_fp8_forward"):
+            extras["next_fp8_forward"] = bench_fp8_forward(C, b, shape, args.steps, args.warmup, peak)
         torch.cuda.empty_cache()
         if shape.backward:
-            extras["next_fp8_fwdbwd"] = bench_fp8_fwdbwd(C, b, shape, args.steps, args.warmup, peak)
+            with nvtx("next_fp8_fwdbwd"):
+                extras["next_fp8_fwdbwd"] = bench_fp8_fwdbwd(C, b, shape, args.steps, args.warmup, peak)
             torch.cuda.empty_cache()
         del b, x, fs, calls
         torch.cuda.empty_cache()
-        extras["plain_gemm_vs_cublas"] = bench_plain_vs_cublas(C, shape, args.steps, args.warmup)
-        extras["fp8_plain_gemm_vs_cublaslt"] = bench_fp8_plain_vs_cublaslt(C, shape, args.steps, args.warmup)
+        with nvtx("plain_gemm_vs_cublas"):
+            extras["plain_gemm_vs_cublas"] = bench_plain_vs_cublas(C, shape, args.steps, args.warmup)
+        with nvtx("fp8_plain_gemm_vs_cublaslt"):
+            extras["fp8_plain_gemm_vs_cublaslt"] = bench_fp8_plain_vs_cublaslt(C, shape, args.steps, args.warmup)
         torch.cuda.empty_cache()
-        extras["lmhead_ce"] = bench_lmhead(C, args.steps, args.warmup)
+        with nvtx("lmhead_ce"):
+            extras["lmhead_ce"] = bench_lmhead(C, args.steps, args.warmup)
         torch.cuda.empty_cache()
-        extras["next_qkv_rope"] = bench_qkv_rope(C, args.steps, args.warmup)
+        with nvtx("next_qkv_rope"):
+            extras["next_qkv_rope"] = bench_qkv_rope(C, args.steps, args.warmup)
 
     if rank == 0:
         line = {
