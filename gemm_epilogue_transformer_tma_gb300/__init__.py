@@ -92,6 +92,7 @@ SIGNATURES = {
     "coda_swiglu_bwd_fp8": (_INT, [_P, _P, _P, _P, _INT, _P, _P, _P, _I64, _I64, _I64, _P]),
     "coda_swiglu_bwd_fp8_delayed": (_INT, [_P, _P, _P, _P, _INT, _P, _P, _P, _I64, _I64, _I64, _P]),
     "coda_gemm_fp8": (_INT, [_P, _P, _INT, _INT, _P, _P, _INT, _INT, _P, _P, _I64, _I64, _I64, _P, _P, _P]),
+    "coda_gemm_res_prms_bwd_fp8": (_INT, [_P, _P, _INT, _P, _P, _P, _P, _P, _INT, _P, _P, _I64, _I64, _I64, _P]),
     "coda_gemm_dgrad_rmsbwd_fp8": (_INT, [_P, _P, _INT, _P, _P, _INT, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "coda_gemm_res_prms_fp8": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "coda_gemm_rowscale_swiglu_fp8": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _U32, _P]),
@@ -635,6 +636,22 @@ def coda_gemm_fp8(A, a_mn_major: bool, a_format: int, sA, B, b_mn_major: bool, b
                                         _ptr(sB, F32, "sB"), _ptr(C, BF, "C"), M, N, K,
                                         _ptr(row_scale, F32, "row_scale"), _ptr(col_scale, BF, "col_scale"),
                                         _stream(stream)), "coda_gemm_fp8")
+
+
+def coda_gemm_res_prms_bwd_fp8(dHq, dh_format: int, sdH, Xq, sX, W1q, sW1, w_format: int, dX, dW1t,
+                               stream=None):
+    """dX = sdH sW1 dHq W1q and dW1t = sdH sX dHq^T Xq on 8-bit codes, one
+    grouped launch (see include/coda.h)."""
+    M, d = dHq.shape
+    K1 = W1q.shape[1]
+    _shape(W1q, (d, K1), "W1q")
+    _shape(Xq, (M, K1), "Xq")
+    _shape(dX, (M, K1), "dX")
+    _shape(dW1t, (d, K1), "dW1t")
+    _check(load_library().coda_gemm_res_prms_bwd_fp8(
+        _h(dW1t), _ptr(dHq, U8, "dHq"), int(dh_format), _ptr(sdH, F32, "sdH"), _ptr(Xq, U8, "Xq"),
+        _ptr(sX, F32, "sX"), _ptr(W1q, U8, "W1q"), _ptr(sW1, F32, "sW1"), int(w_format), _ptr(dX, BF, "dX"),
+        _ptr(dW1t, BF, "dW1t"), M, K1, d, _stream(stream)), "coda_gemm_res_prms_bwd_fp8")
 
 
 def coda_gemm_dgrad_rmsbwd_fp8(dPq, dp_format: int, sdP, W2q, w_format: int, sW2, H, g, c, dH, dgpart,

@@ -689,6 +689,35 @@ coda_status_t coda_gemm_fp8(coda_handle_t h, const void* A, int a_mn_major, int 
                                   static_cast<const bf16*>(col_scale)));
 }
 
+coda_status_t coda_gemm_res_prms_bwd_fp8(coda_handle_t h, const void* dHq, int dh_format, const float* sdH,
+                                         const void* Xq, const float* sX, const void* W1q, const float* sW1,
+                                         int w_format, void* dX, void* dW1t, int64_t M, int64_t K1, int64_t d,
+                                         void* stream) {
+  CODA_TRY(Check()
+               .handle(h)
+               .rows(M)
+               .mptr(dHq, M)
+               .opt_sptr(sdH)
+               .mptr(Xq, M)
+               .opt_sptr(sX)
+               .ptr(W1q)
+               .opt_sptr(sW1)
+               .mptr(dX, M)
+               .ptr(dW1t)
+               .cols(K1)
+               .cols(d)
+               .st);
+  if ((dh_format != 0 && dh_format != 1) || (w_format != 0 && w_format != 1)) return CODA_ERR_INVALID_ARG;
+  if (K1 % 16 != 0 || d % 16 != 0) return CODA_ERR_ALIGNMENT;
+  const LaunchCtx cx = ctx_of(h, stream);
+  // an empty batch: dW1t is an empty sum
+  if (M == 0) return from_cuda(cudaMemsetAsync(dW1t, 0, size_t(d) * K1 * 2, cx.stream));
+  return from_cuda(gemm_group_store_fp8(cx, static_cast<const uint8_t*>(dHq), dh_format, sdH,
+                                        static_cast<const uint8_t*>(W1q), sW1, static_cast<const uint8_t*>(Xq), sX,
+                                        w_format, static_cast<bf16*>(dX), static_cast<bf16*>(dW1t), int(M), int(K1),
+                                        int(d)));
+}
+
 coda_status_t coda_gemm_dgrad_rmsbwd_fp8(coda_handle_t h, const void* dPq, int dp_format, const float* sdP,
                                          const void* W2q, int w_format, const float* sW2, const void* H,
                                          const void* g, const float* c, void* dH, float* dgpart, int64_t M,

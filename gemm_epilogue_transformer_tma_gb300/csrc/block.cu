@@ -240,7 +240,8 @@ coda_status_t forward_fp8(coda_block_s* b, Slot& sl) {
 
 // The FP8 backward: dP's e5m2 codes from the SwiGLU backward (delayed
 // scaling after the first step if requested), dgrad2 with the RMSNorm
-// backward, dg, wgrad2 with dH's e5m2 codes quantised beside it, dX and dW1.
+// backward, dg, wgrad2 with dH's e5m2 codes quantised beside it, then dX and
+// dW1 in one grouped launch.
 coda_status_t backward_fp8(coda_block_s* b, Slot& sl) {
   void* cs = b->compute;
   const int64_t F = b->N2 / 2;
@@ -262,10 +263,8 @@ coda_status_t backward_fp8(coda_block_s* b, Slot& sl) {
   BLK_TRY(coda_fp8_quantize_e5m2(b->h, sl.dH, nullptr, b->s_a + 6, b->dHq, b->M, b->d, b->side));
   BLK_TRY(cu(cudaEventRecord(b->ev_join, b->side)));
   BLK_TRY(cu(cudaStreamWaitEvent(b->compute, b->ev_join, 0)));
-  BLK_TRY(coda_gemm_fp8(b->h, b->dHq, 0, 1, b->s_a + 7, b->W1q, 1, 0, b->s_w + 1, sl.dX, b->M, b->K1, b->d, nullptr,
-                        nullptr, cs));
-  return coda_gemm_fp8(b->h, b->dHq, 1, 1, b->s_a + 7, b->Xq, 1, 0, b->s_a + 1, b->dW1t, b->d, b->K1, b->M, nullptr,
-                       nullptr, cs);
+  return coda_gemm_res_prms_bwd_fp8(b->h, b->dHq, 1, b->s_a + 7, b->Xq, b->s_a + 1, b->W1q, b->s_w + 1, 0, sl.dX,
+                                    b->dW1t, b->M, b->K1, b->d, cs);
 }
 
 }  // namespace

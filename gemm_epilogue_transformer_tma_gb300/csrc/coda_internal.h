@@ -140,8 +140,17 @@ cudaError_t gemm_group_store(const LaunchCtx& c, const __nv_bfloat16* dH, const 
 cudaError_t gemm_group_ce_bwd(const LaunchCtx& c, const __nv_bfloat16* dL, const __nv_bfloat16* Wc,
                               const __nv_bfloat16* H, float* dH32, bool accumulate, __nv_bfloat16* dWc, int M, int d,
                               int Vc);
+//   the same first-layer pair on 8-bit codes: dX = sdH sW1 dHq W1q and
+//   dW1t = sdH sX dHq^T Xq (dH format dh_fmt; W1 and X in w_fmt); two
+//   launches when pairing is off.
+cudaError_t gemm_group_store_fp8(const LaunchCtx& c, const uint8_t* dHq, int dh_fmt, const float* sdH,
+                                 const uint8_t* W1q, const float* sW1, const uint8_t* Xq, const float* sX, int w_fmt,
+                                 __nv_bfloat16* dX, __nv_bfloat16* dW1t, int M, int K1, int d);
 // Host check of the grouped tile schedule (0 = every tile visited once).
 int group_schedule_violations(int P, int heavy, int nH, int nL, int q);
+// Tensor map of an 8-bit operand: K-major [rows][K] (boxes of 128 K x
+// box_rows) or MN-major [K][mn] (boxes of 128 x 128).
+bool make_f8_operand_map(CUtensorMap* m, const uint8_t* p, bool mn_major, int mn, int K, int box_rows);
 
 // C = bf16(row_scale * col_scale * sA * sB * A B) on 8-bit operands: A
 // [M][K] (K-major) or [K][M] (MN-major), B [N][K] or [K][N]; formats 0 =

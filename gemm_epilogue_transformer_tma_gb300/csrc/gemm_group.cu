@@ -1,6 +1,6 @@
 // Grouped launches of independent GEMM pairs (the data and the weight
-// gradient of one layer: the first layer of the block, the LM-head chunks) on
-// the SM-pair kernel of gemm_group.cuh.  With SM pairing switched off they run
+// gradient of one layer: the first layer of the block, in bf16 or on 8-bit
+// codes, and the LM-head chunks) on the SM-pair kernel of gemm_group.cuh.  With SM pairing switched off they run
 // as two launches of the 1-SM kernel.
 #include <vector>
 
@@ -12,14 +12,16 @@ namespace coda {
 namespace {
 constexpr int kStages = 6;
 
-GemmShape pair_shape(int M, int N, int K) {
+// k-blocks of 128 bytes of K per row: 64 bf16 or 128 8-bit codes
+GemmShape pair_shape(int M, int N, int K, bool fp8 = false) {
+  const int bke = fp8 ? 128 : BK;
   GemmShape sh;
   sh.M = M;
   sh.N = N;
   sh.K = K;
   sh.tiles_m = (M + BM2 - 1) / BM2;
   sh.tiles_n = (N + 255) / 256;
-  sh.num_kb = (K + BK - 1) / BK;
+  sh.num_kb = (K + bke - 1) / bke;
   sh.group_m = 8;
   return sh;
 }
@@ -39,17 +41,18 @@ GroupSched make_sched(const GemmShape& a, const GemmShape& b, int P) {
   return s;
 }
 
-template <bool A_MN0, bool B_MN0, bool A_MN1, bool B_MN1, class Epi0, class Epi1>
+template <bool A_MN0, bool B_MN0, bool A_MN1, bool B_MN1, class Epi0, class Epi1, bool FP8 = false>
 cudaError_t launch_group(const LaunchCtx& c, GroupArgs<Epi0, Epi1>& g) {
   using L = Gemm2Smem<256, kStages, group_stage_bytes<Epi0, Epi1>()>;
-  auto kern = gemm_tc2_group_kernel<kStages, A_MN0, B_MN0, A_MN1, B_MN1, Epi0, Epi1>;
+  auto kern = gemm_tc2_group_kernel<kStages, A_MN0, B_MN0, A_MN1, B_MN1, Epi0, Epi1, FP8>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL);
   if (e != cudaSuccess) return e;
-  static int max_pairs[64] = {};
+  static int max_pairs[2][64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (max_pairs[dev] == 0) {
+  int* mp = &max_pairs[FP8 ? 1 : 0][dev];
+  if (*mp == 0) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * (c.num_sms / 2), 1, 1);
     cfg.blockDim = dim3(gemm_threads<Epi0>(), 1, 1);
@@ -64,12 +67,12 @@ cudaError_t launch_group(const LaunchCtx& c, GroupArgs<Epi0, Epi1>& g) {
     int n = 0;
     e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
     if (e != cudaSuccess) return e;
-    max_pairs[dev] = std::max(1, std::min(n, c.num_sms / 2));
+    *mp = std::max(1, std::min(n, c.num_sms / 2));
   }
   const int tiles = g.sh0.tiles_m * g.sh0.tiles_n + g.sh1.tiles_m * g.sh1.tiles_n;
-  const int P = std::max(1, std::min(tiles, max_pairs[dev]));
+  const int P = std::max(1, std::min(tiles, *mp));
   g.sched = make_sched(g.sh0, g.sh1, P);
-  KernelCtl ctl{c.status, c.timeout_ns, c.skip_first_stage, nullptr, nullptr, 0u, 1.f};
+  KernelCtl ctl{c.status, c.timeout_ns, c.skip_first_stage, nullptr, nullptr, FP8 ? c.f8_fmt : 0u, 1.f};
   return launch_chained(c, kern, dim3(2 * P), dim3(gemm_threads<Epi0>()), L::TOTAL, g, ctl);
 }
 }  // namespace
@@ -94,6 +97,38 @@ cudaError_t gemm_group_store(const LaunchCtx& c, const __nv_bfloat16* dH, const 
   if (!make_tmap_store_bf16(&ga.ep0.out, dX, K1, M, K1)) return cudaErrorInvalidValue;
   if (!make_tmap_store_bf16(&ga.ep1.out, dW1t, K1, d, K1)) return cudaErrorInvalidValue;
   return launch_group<false, true, true, true, EpiStore, EpiStore>(c, ga);
+}
+
+cudaError_t gemm_group_store_fp8(const LaunchCtx& c0, const uint8_t* dHq, int dh_fmt, const float* sdH,
+                                 const uint8_t* W1q, const float* sW1, const uint8_t* Xq, const float* sX, int w_fmt,
+                                 __nv_bfloat16* dX, __nv_bfloat16* dW1t, int M, int K1, int d) {
+  if (!c0.pair) {
+    cudaError_t e = gemm_store_fp8(c0, dHq, false, dh_fmt, sdH, W1q, true, w_fmt, sW1, dX, M, K1, d, nullptr, nullptr);
+    if (e != cudaSuccess) return e;
+    return gemm_store_fp8(c0, dHq, true, dh_fmt, sdH, Xq, true, w_fmt, sX, dW1t, d, K1, M, nullptr, nullptr);
+  }
+  LaunchCtx c = c0;
+  c.f8_fmt = f8_format_bits(dh_fmt, w_fmt);
+  GroupArgs<EpiStore, EpiStore> ga{};
+  // problem 0, dgrad: dX[M, K1] from dH codes [M][d] (K-major) and W1t codes
+  // [d][K1] (MN-major)
+  if (!make_f8_operand_map(&ga.tmA0, dHq, false, M, d, BM) ||
+      !make_f8_operand_map(&ga.tmB0, W1q, true, K1, d, b_box_rows(c)))
+    return cudaErrorInvalidValue;
+  // problem 1, wgrad: dW1t[d, K1] = dH^T X; K' = M, A' = dH codes [M][d] and
+  // B' = X codes [M][K1], both MN-major
+  if (!make_f8_operand_map(&ga.tmA1, dHq, true, d, M, BM) ||
+      !make_f8_operand_map(&ga.tmB1, Xq, true, K1, M, b_box_rows(c)))
+    return cudaErrorInvalidValue;
+  ga.sh0 = pair_shape(M, K1, d, true);
+  ga.sh1 = pair_shape(d, K1, M, true);
+  if (!make_tmap_store_bf16(&ga.ep0.out, dX, K1, M, K1)) return cudaErrorInvalidValue;
+  if (!make_tmap_store_bf16(&ga.ep1.out, dW1t, K1, d, K1)) return cudaErrorInvalidValue;
+  ga.scale_a0 = sdH;
+  ga.scale_b0 = sW1;
+  ga.scale_a1 = sdH;
+  ga.scale_b1 = sX;
+  return launch_group<false, true, true, true, EpiStore, EpiStore, true>(c, ga);
 }
 
 cudaError_t gemm_group_ce_bwd(const LaunchCtx& c, const __nv_bfloat16* dL, const __nv_bfloat16* Wc,

@@ -13,7 +13,9 @@
 // them buys little.
 //
 // Problem 0 has A K-major or MN-major and B MN-major; problem 1 likewise
-// (template flags), each with its own epilogue program.  The pipeline (TMA
+// (template flags), each with its own epilogue program.  With FP8 both
+// problems take 8-bit operands of the same formats (kind::f8f6f4), each with
+// its own pair of per-tensor scales.  The pipeline (TMA
 // producer, 2-SM MMA issuer, epilogue warps, bounded waits, abort and drain)
 // is that of gemm_tc2_kernel; only the tile sequence and the per-tile choice
 // of operands, descriptors and epilogue differ.
@@ -79,36 +81,53 @@ struct GroupArgs {
   GroupSched sched;
   typename Epi0::Params ep0;
   typename Epi1::Params ep1;
+  // FP8 operands: each problem's per-tensor dequantisation scales (null = 1)
+  const float* scale_a0;
+  const float* scale_b0;
+  const float* scale_a1;
+  const float* scale_b1;
 };
 
 // This CTA's halves of one k-block of a 256 x 256 pair tile (B MN-major or
-// K-major, A either), completing on the leader's barrier.
-template <bool A_MN, bool B_MN>
+// K-major, A either), completing on the leader's barrier.  A k-block is 128
+// bytes of K per row: 64 bf16 or 128 8-bit codes.  MN-major halves are 128
+// (M/N) wide: two 64-wide bf16 boxes or one 128-wide box of codes.
+template <bool A_MN, bool B_MN, bool FP8>
 __device__ __forceinline__ void pair_load_kblock(uint8_t* sa, uint8_t* sb, const CUtensorMap* ta,
                                                  const CUtensorMap* tb, uint32_t bar, int kb, int m0, int n0) {
+  constexpr int BKE = FP8 ? 128 : BK;     // K elements per k-block
+  constexpr int MNB = FP8 ? 128 : 64;     // M/N elements per MN-major box
+  constexpr int MN_BOX = 128 * BKE;       // bytes per MN-major box
   if (!A_MN) {
-    tma_load_2d_pair(sa, ta, bar, kb * BK, m0);
+    tma_load_2d_pair(sa, ta, bar, kb * BKE, m0);
   } else {
-    tma_load_2d_pair(sa, ta, bar, m0, kb * BK);
-    tma_load_2d_pair(sa + 8192, ta, bar, m0 + 64, kb * BK);
+#pragma unroll
+    for (int i = 0; i < 128 / MNB; ++i) tma_load_2d_pair(sa + i * MN_BOX, ta, bar, m0 + i * MNB, kb * BKE);
   }
   if (!B_MN) {
-    tma_load_2d_pair(sb, tb, bar, kb * BK, n0);
+    tma_load_2d_pair(sb, tb, bar, kb * BKE, n0);
   } else {
-    tma_load_2d_pair(sb, tb, bar, n0, kb * BK);
-    tma_load_2d_pair(sb + 8192, tb, bar, n0 + 64, kb * BK);
+#pragma unroll
+    for (int i = 0; i < 128 / MNB; ++i) tma_load_2d_pair(sb + i * MN_BOX, tb, bar, n0 + i * MNB, kb * BKE);
   }
 }
 
-// The four K=16 MMAs of one k-block.
-template <bool A_MN, bool B_MN>
-__device__ __forceinline__ void pair_mma_kblock(uint32_t d_tmem, uint32_t sa, uint32_t sb, bool first) {
-  constexpr uint32_t IDESC = idesc_bf16_f32(BM2, 256, A_MN, B_MN);
+// The four MMAs of one k-block (K = 16 bf16 or 32 8-bit codes each).
+template <bool A_MN, bool B_MN, bool FP8>
+__device__ __forceinline__ void pair_mma_kblock(uint32_t d_tmem, uint32_t sa, uint32_t sb, bool first,
+                                                uint32_t f8_fmt) {
+  constexpr uint32_t IDESC0 = FP8 ? idesc_f8_f32(BM2, 256, A_MN, B_MN) : idesc_bf16_f32(BM2, 256, A_MN, B_MN);
+  constexpr int MN_BOX = FP8 ? 16384 : 8192;
+  constexpr int MN_KSTEP = FP8 ? 4096 : 2048;  // bytes per MMA K slice, MN-major
+  const uint32_t idesc = FP8 ? (IDESC0 | f8_fmt) : IDESC0;
 #pragma unroll
   for (int k = 0; k < BK / UMMA_K; ++k) {
-    const uint64_t ad = A_MN ? sdesc_sw128(sa + k * 2048, 8192, 1024) : sdesc_sw128(sa + k * 32, 16, 1024);
-    const uint64_t bd = B_MN ? sdesc_sw128(sb + k * 2048, 8192, 1024) : sdesc_sw128(sb + k * 32, 16, 1024);
-    umma_bf16_pair(d_tmem, ad, bd, IDESC, (first && k == 0) ? 0u : 1u);
+    const uint64_t ad = A_MN ? sdesc_sw128(sa + k * MN_KSTEP, MN_BOX, 1024) : sdesc_sw128(sa + k * 32, 16, 1024);
+    const uint64_t bd = B_MN ? sdesc_sw128(sb + k * MN_KSTEP, MN_BOX, 1024) : sdesc_sw128(sb + k * 32, 16, 1024);
+    if (FP8)
+      umma_e4m3_pair(d_tmem, ad, bd, idesc, (first && k == 0) ? 0u : 1u);
+    else
+      umma_bf16_pair(d_tmem, ad, bd, idesc, (first && k == 0) ? 0u : 1u);
   }
 }
 
@@ -118,10 +137,11 @@ constexpr int group_stage_bytes() {
          STORE_SLOT_BYTES;
 }
 
-template <int STAGES, bool A_MN0, bool B_MN0, bool A_MN1, bool B_MN1, class Epi0, class Epi1>
+template <int STAGES, bool A_MN0, bool B_MN0, bool A_MN1, bool B_MN1, class Epi0, class Epi1, bool FP8 = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi0>(), 1)
     gemm_tc2_group_kernel(const __grid_constant__ GroupArgs<Epi0, Epi1> g, const KernelCtl ctl) {
   static_assert(Epi0::kEpiWarps == Epi1::kEpiWarps, "both epilogue programs use the same warps");
+  static_assert(!FP8 || (Epi0::kAccScale && Epi1::kAccScale), "8-bit operands need the accumulator scale");
   constexpr int BN = 256;
   constexpr int HB = BN / 2;
   using L = Gemm2Smem<BN, STAGES, group_stage_bytes<Epi0, Epi1>()>;
@@ -206,9 +226,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi0>()
               parity = (parity & ~(1u << stage)) | (phase << stage);
             }
             if (prob == 0)
-              pair_load_kblock<A_MN0, B_MN0>(sa, sb, &g.tmA0, &g.tmB0, bar, kb, m0, n0);
+              pair_load_kblock<A_MN0, B_MN0, FP8>(sa, sb, &g.tmA0, &g.tmB0, bar, kb, m0, n0);
             else
-              pair_load_kblock<A_MN1, B_MN1>(sa, sb, &g.tmA1, &g.tmB1, bar, kb, m0, n0);
+              pair_load_kblock<A_MN1, B_MN1, FP8>(sa, sb, &g.tmA1, &g.tmB1, bar, kb, m0, n0);
           }
           if (++stage == STAGES) {
             stage = 0;
@@ -258,9 +278,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi0>()
           const uint32_t sa = smem_u32(smem + stage * L::STAGE_BYTES);
           const uint32_t sb = sa + L::A_BYTES;
           if (prob == 0)
-            pair_mma_kblock<A_MN0, B_MN0>(d_tmem, sa, sb, kb == 0);
+            pair_mma_kblock<A_MN0, B_MN0, FP8>(d_tmem, sa, sb, kb == 0, ctl.f8_fmt);
           else
-            pair_mma_kblock<A_MN1, B_MN1>(d_tmem, sa, sb, kb == 0);
+            pair_mma_kblock<A_MN1, B_MN1, FP8>(d_tmem, sa, sb, kb == 0, ctl.f8_fmt);
           issued_any = true;
           umma_commit_pair_multicast(&empty[stage], 0x3);
           if (++stage == STAGES) {
@@ -285,6 +305,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi0>()
     const uint32_t leader_tempty = mapa_shared(smem_u32(tempty), 0);
     const uint32_t stage_base =
         smem_u32(smem + L::RING_BYTES) + static_cast<uint32_t>((warp - 2) * SLOTS * STORE_SLOT_BYTES);
+    // each problem's accumulator scale (1 for bf16 operands)
+    float acc_scale[2] = {1.f, 1.f};
+    if (FP8) {
+      acc_scale[0] = (g.scale_a0 ? *g.scale_a0 : 1.f) * (g.scale_b0 ? *g.scale_b0 : 1.f);
+      acc_scale[1] = (g.scale_a1 ? *g.scale_a1 : 1.f) * (g.scale_b1 ? *g.scale_b1 : 1.f);
+    }
     int prob, t;
     for (int it = 0; group_tile(g.sched, cluster_id, it, prob, t); ++it) {
       const GemmShape& sh = prob == 0 ? g.sh0 : g.sh1;
@@ -309,7 +335,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi0>()
       c.m0 = c.tm * 128 + quad * 32;
       c.quad = quad;
       c.lane = lane;
-      c.acc_scale = 1.f;
+      c.acc_scale = acc_scale[prob];
       c.taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN);
       c.stage = stage_base;
 #pragma unroll 1

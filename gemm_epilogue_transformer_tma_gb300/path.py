@@ -11,7 +11,7 @@ import torch
 
 from . import (CODA_EPI_PLAIN, CODA_EPI_SWIGLU, E4M3, E5M2, coda_bwd_workspace_bytes, coda_dg_combine,
                coda_fp8_quantize, coda_fp8_quantize_e5m2, coda_gemm_dgrad_rmsbwd_fp8, coda_gemm_fp8,
-               coda_swiglu_bwd_fp8_delayed,
+               coda_swiglu_bwd_fp8_delayed, coda_gemm_res_prms_bwd_fp8,
                coda_gemm_res_prms_fp8, coda_gemm_rowscale_swiglu_fp8,
                coda_dgpart_rows, coda_fold_rmsnorm_weight, coda_gemm_dgrad_rmsbwd, coda_gemm_prms_rowscale_swiglu,
                coda_gemm_dgrad_rmsbwd_cpart, coda_gemm_dgrad_swiglu_bwd, coda_gemm_res_prms, coda_gemm_res_prms_g,
@@ -270,11 +270,11 @@ class BlockBuffers:
                 lambda: coda_gemm_fp8(self.dPq, True, E5M2, self.s_a[2, 1:], self.Hq, True, E4M3, self.s_a[1, 1:],
                                       self.dW2t, N2, d, M, col_scale=self.g),
                 lambda side: coda_fp8_quantize_e5m2(self.dH, self.dHq, self.s_a[3], stream=side))),
-            # dX = dH W1 (W1t codes [d][K1] read MN-major), dW1t = dH^T X
-            ("dgrad1_fp8", lambda: coda_gemm_fp8(self.dHq, False, E5M2, self.s_a[3, 1:], self.W1q, True, E4M3,
-                                                 self.s_w[0, 1:], self.dX, M, K1, d)),
-            ("wgrad1_fp8", lambda: coda_gemm_fp8(self.dHq, True, E5M2, self.s_a[3, 1:], self.Xq, True, E4M3,
-                                                 self.s_a[0, 1:], self.dW1t, d, K1, M)),
+            # dX = dH W1 (W1t codes [d][K1] read MN-major) and dW1t = dH^T X,
+            # one grouped launch
+            ("dgrad1_wgrad1_fp8", lambda: coda_gemm_res_prms_bwd_fp8(
+                self.dHq, E5M2, self.s_a[3, 1:], self.Xq, self.s_a[0, 1:], self.W1q, self.s_w[0, 1:], E4M3, self.dX,
+                self.dW1t)),
         ]
 
     def forward_fp8(self):

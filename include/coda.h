@@ -499,6 +499,22 @@ coda_status_t coda_gemm_fp8(coda_handle_t h, const void* A, int a_mn_major, int 
                             const void* B, int b_mn_major, int b_format, const float* sB, void* C, int64_t M,
                             int64_t N, int64_t K, const float* row_scale, const void* col_scale, void* stream);
 
+/* coda_gemm_res_prms_bwd on 8-bit operands: the first layer's data and
+ * weight gradients from dH's codes,
+ *   dX[m][i]   = bf16( sdH * sW1 * sum_k dHq[m][k] W1q[k][i] )
+ *   dW1t[k][i] = bf16( sdH * sX  * sum_m dHq[m][k] Xq[m][i] )
+ * with SM pairing in one persistent launch (the schedule of
+ * coda_gemm_res_prms_bwd), otherwise two launches; the results equal those
+ * of the two coda_gemm_fp8 calls bit for bit.  dHq codes [M][d] (dh_format: 0
+ * = e4m3, 1 = e5m2), Xq codes [M][K1] and W1q codes [d][K1] (both w_format),
+ * sdH / sX / sW1 device pointers to fp32 scales (NULL = 1); dX bf16 [M][K1],
+ * dW1t bf16 [d][K1].  K1 and d multiples of 16; any M >= 0 (M == 0 writes
+ * dW1t = 0). */
+coda_status_t coda_gemm_res_prms_bwd_fp8(coda_handle_t h, const void* dHq, int dh_format, const float* sdH,
+                                         const void* Xq, const float* sX, const void* W1q, const float* sW1,
+                                         int w_format, void* dX, void* dW1t, int64_t M, int64_t K1, int64_t d,
+                                         void* stream);
+
 /* coda_gemm_dgrad_rmsbwd on 8-bit operands (the RMSNorm-backward epilogue
  * with FP8 inputs):
  *   acc = sdP * sW2 * sum_n dPq[m][n] W2q[n][k];  dH = bf16(g * acc - c * h);

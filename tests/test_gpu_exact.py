@@ -41,7 +41,7 @@ def exact_bf16(A, Bt, row=None, col=None):
         v = v * row.to(torch.float64)[:, None]
     if col is not None:
         v = v * col.to(torch.float64)[None, :]
-    assert float(v.abs().max()) < 2 ** 24
+    assert v.numel() == 0 or float(v.abs().max()) < 2 ** 24
     return v.to(torch.float32).to(torch.bfloat16)
 
 
@@ -141,3 +141,26 @@ def test_fp8_gemm_ragged_token_k_bit_exact(K, pairing):
     torch.cuda.synchronize()
     assert_device_ok()
     assert torch.equal(Cd.cpu(), exact_bf16(A, Bt))
+
+
+@pytest.mark.parametrize("M,K1,d", [(1000, 528, 336), (300, 256, 512), (1, 256, 256), (0, 256, 256),
+                                    (4096, 1024, 1024)])
+def test_fp8_grouped_first_layer_backward_bit_exact(M, K1, d, pairing):
+    """dX = sdH sW1 dH W1 and dW1t = sdH sX dH^T X from e5m2 dH and e4m3 W1 / X
+    codes, one grouped launch with SM pairing (two launches without): the
+    exact products times the power-of-two scales, rounded once (ragged tiles,
+    ragged token count, one row, an empty batch)."""
+    dH = ints((M, d), -4, 4, 16)
+    X = ints((M, K1), -4, 4, 17)
+    W1t = ints((d, K1), -4, 4, 18)
+    dHq = torch.from_numpy(np.ascontiguousarray(O.e5m2_encode(dH.numpy().astype(np.float64)))).cuda()
+    Xq = torch.from_numpy(np.ascontiguousarray(O.e4m3_encode(X.numpy().astype(np.float64)))).cuda()
+    W1q = torch.from_numpy(np.ascontiguousarray(O.e4m3_encode(W1t.numpy().astype(np.float64)))).cuda()
+    sdH, sX, sW1 = (torch.tensor([v], device="cuda") for v in (0.5, 2.0, 0.25))
+    dX = torch.full((M, K1), 7.0, dtype=torch.bfloat16, device="cuda")
+    dW1t = torch.full((d, K1), 7.0, dtype=torch.bfloat16, device="cuda")
+    C.coda_gemm_res_prms_bwd_fp8(dHq, C.E5M2, sdH, Xq, sX, W1q, sW1, C.E4M3, dX, dW1t)
+    torch.cuda.synchronize()
+    assert_device_ok()
+    assert torch.equal(dX.cpu(), exact_bf16(dH, W1t.T.contiguous(), torch.full((M,), 0.125)))   # sdH * sW1
+    assert torch.equal(dW1t.cpu(), exact_bf16(dH.T.contiguous(), X.T.contiguous(), torch.full((d,), 1.0)))  # sdH * sX
