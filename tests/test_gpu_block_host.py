@@ -102,10 +102,11 @@ def test_forward_only():
     st.close()
 
 
-def test_empty_batch_zeroes_the_weight_gradients():
+@pytest.mark.parametrize("fp8", [False, True], ids=["bf16", "fp8"])
+def test_empty_batch_zeroes_the_weight_gradients(fp8):
     s = BlockShape("empty", 0, 64, 64, 128)
     x = block_inputs(s, 0, "cuda")
-    st = HostBlockStepper(x["W1t"], x["g"], x["W2t"], 0, s.eps)
+    st = HostBlockStepper(x["W1t"], x["g"], x["W2t"], 0, s.eps, fp8=fp8)
     for t in (st.dW1t, st.dW2t, st.dg):
         t.fill_(1.0)
     st.submit(None, None, None)
