@@ -268,6 +268,23 @@ def interleave(a_calls, b_calls, n, warmup, rounds=3):
     return min(p[0] for p in pairs), min(p[1] for p in pairs), ratio, pairs
 
 
+def interleave_many(seqs, n, warmup, rounds=6):
+    """Time several call sequences in rounds, each round running every
+    sequence for n steps, the order reversed on every other round so that
+    drift within a round (the part heating) falls on each sequence alike.
+    Returns per-sequence lists of ms/step, one entry per round."""
+    for calls in seqs:
+        for _ in range(warmup):
+            for f in calls:
+                f()
+    out = [[] for _ in seqs]
+    for r in range(rounds):
+        order = range(len(seqs)) if r % 2 == 0 else reversed(range(len(seqs)))
+        for i in order:
+            out[i].append(time_steps(seqs[i], n, 0, stage_events=False)[0] / n)
+    return out
+
+
 def rounds_ms(pairs):
     return [[round(a, 4), round(b, 4)] for a, b in pairs]
 
@@ -355,6 +372,76 @@ def run_reference(args, shape):
                              "sample": res["sample"]},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def bench_block_workload(C, shape, steps, warmup, peaks, device_index, g_on_activation=False):
+    """Another block workload on the same line: its fused step timed like the
+    headline (events around `steps` steps after `warmup`), the dominant
+    kernel's roofline from a second pass with events between stages, the
+    unfused ablation and the other placement of the RMSNorm weight each in
+    interleaved rounds with it, and the clocks sampled meanwhile."""
+    from gemm_epilogue_transformer_tma_gb300.path import BlockBuffers
+    x = block_inputs(shape, seed=0, device="cuda")
+    b = BlockBuffers(x, backward=shape.backward, g_on_activation=g_on_activation)
+    fs = FusedStep(C, b, g_on_activation=g_on_activation)
+    calls = fs.calls()
+    for _ in range(warmup):
+        for f in calls:
+            f()
+    torch.cuda.synchronize()
+    with ClockSampler(device_index) as clk:
+        total_ms, _ = time_steps(calls, steps, 0, stage_events=False)
+        _, per = time_steps(calls, steps, 0, stage_events=True)
+    st, bits = C.coda_sync_status()
+    if st != 0:
+        raise RuntimeError(f"device status {C.STATUS_NAMES.get(st)} bits={bits:#x}")
+    ms = total_ms / steps
+    step_flops = shape.fwdbwd_flops() if shape.backward else shape.fwd_flops()
+    stage_ms = {name: statistics.mean(per[i]) for i, name in enumerate(fs.names())}
+    dom = max((k for k in fs.flops if k in stage_ms), key=lambda k: stage_ms[k])
+    dom_ach = fs.flops[dom] / (stage_ms[dom] * 1e-3) / 1e12
+    clocks = clk.summary()
+    n_cmp = max(3, steps // 2)
+    out = {
+        "workload": shape.name, "M": shape.M, "K1": shape.K1, "d": shape.d, "ffn": shape.N2 // 2,
+        "pass": "forward+backward" if shape.backward else "forward (no z store)",
+        "g": "on the activation (GEMM1 epilogue)" if g_on_activation else "folded into W2",
+        "ms_per_step": ms, "value": step_flops / (ms * 1e-3) / 1e12, "unit": UNIT,
+        "pct_of_peak": 100.0 * step_flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
+        "steps": steps, "warmup": warmup, "stage_ms": stage_ms,
+        "roofline": {"kernel": dom, "bound": "tensor", "achieved": dom_ach, "peak": peaks["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": dom_ach / peaks["bf16_tflops"],
+                     "frac_of_sustained": dom_ach / peaks["bf16_tflops_sustained"],
+                     "traffic": measured_traffic(shape.name, dom),
+                     "note": "peak = burst bf16 of %s: the kernel is timed inside a sub-second step loop" %
+                             peaks["source"]},
+        "clocks": clocks,
+    }
+    # this step, the other placement of the RMSNorm weight and the unfused
+    # ablation, in interleaved rounds (order alternating between rounds)
+    bo = BlockBuffers(x, backward=shape.backward, g_on_activation=not g_on_activation)
+    ocalls = FusedStep(C, bo, g_on_activation=not g_on_activation).calls()
+    bu = BlockBuffers(x, unfused=True, backward=shape.backward)
+    ucalls = [bu.forward_unfused, bu.backward_unfused] if shape.backward else [bu.forward_unfused]
+    t_this, t_other, t_unf = interleave_many([calls, ocalls, ucalls], n_cmp, warmup)
+    med = statistics.median
+    out["other_g_placement"] = {
+        "g": "folded into W2" if g_on_activation else "on the activation (GEMM1 epilogue)",
+        "ms_per_step": min(t_other), "time_vs_this_step": med(o / t for o, t in zip(t_other, t_this)),
+        "vs_unfused_speedup": med(u / o for u, o in zip(t_unf, t_other)),
+        "rounds_ms": [round(v, 4) for v in t_other]}
+    out["ablation_unfused"] = {"ms_per_step": min(t_unf), "tflops": step_flops / (min(t_unf) * 1e-3) / 1e12,
+                               "fused_speedup": med(u / t for u, t in zip(t_unf, t_this)),
+                               "rounds_ms": [round(v, 4) for v in t_unf],
+                               "fused_rounds_ms": [round(v, 4) for v in t_this],
+                               "timing": "rounds of (this step, other g placement, unfused step), order reversed "
+                                         "every other round; speedups = median per-round time ratios"}
+    st, bits = C.coda_sync_status()
+    if st != 0:
+        raise RuntimeError(f"device status {C.STATUS_NAMES.get(st)} bits={bits:#x}")
+    del bu, ucalls, bo, ocalls, b, fs, calls, x
+    torch.cuda.empty_cache()
+    return out
 
 
 def bench_memory_kernels(C, b, shape, hbm_gbs, warmup=10, iters=50):
@@ -463,7 +550,7 @@ def bench_fp8_forward(C, b, shape, steps, warmup, peak_bf16):
             "gemm2_fp8_tflops": 2.0 * shape.M * shape.N2 * shape.d / (g2 * 1e-3) / 1e12,
             "fp8_peak_tflops": 2 * peak_bf16,
             "gemm2_frac_of_fp8_peak": 2.0 * shape.M * shape.N2 * shape.d / (g2 * 1e-3) / 1e12 / (2 * peak_bf16),
-            "peak_note": "fp8 dense peak taken as 2x the measured sustained bf16 peak (nominal ratio 4.5 / 2.25 "
+            "peak_note": "fp8 dense peak taken as 2x the measured burst bf16 peak (nominal ratio 4.5 / 2.25 "
                          "PFLOP/s); GEMM2 timed in a stage pass inside the step loop"}
 
 
@@ -746,14 +833,12 @@ def main():
     dom = max((k for k in fs.flops if k in stage_ms), key=lambda k: stage_ms[k])
     dom_ach = fs.flops[dom] / (stage_ms[dom] * 1e-3) / 1e12
     clocks = clk.summary()
-    # The dominant kernel is timed in the stage pass, inside the step loop,
-    # after the warm-up and headline passes: a kernel timed inside a long run,
-    # whose denominator is the sustained (power-capped) cuBLAS figure; under
-    # tensor load the SMs run below the clock nvidia-smi reports.  Its
-    # fraction of the burst figure is reported beside it.  The whole step's
-    # percentage is given against both.
-    peak = peaks["bf16_tflops_sustained"]
-    peak_kind = "sustained"
+    # The dominant kernel is timed in the stage pass, inside a step loop of
+    # well under a second: its denominator is the burst cuBLAS figure (the
+    # sustained one is for kernels timed inside seconds-long runs), with its
+    # fraction of the sustained figure reported beside it.
+    peak = peaks["bf16_tflops"]
+    peak_kind = "burst"
 
     launches = sum(fs.kernels.values()) * args.steps
     extras = {}
@@ -855,6 +940,17 @@ def main():
         torch.cuda.empty_cache()
         with nvtx("next_qkv_rope"):
             extras["next_qkv_rope"] = bench_qkv_rope(C, args.steps, args.warmup)
+        torch.cuda.empty_cache()
+        # the other block workloads of the method's experiments: 70B-size
+        # forward+backward (d = 8192) and 1B-size forward, each with its own
+        # roofline, ablation and clocks
+        for key, other in (("bench_70b", B70), ("bench_1b", B1)):
+            if other.name == shape.name:
+                continue
+            with nvtx(key):
+                extras[key] = bench_block_workload(C, other, args.steps, args.warmup, peaks, local,
+                                                   g_on_activation=args.g_on_activation)
+            torch.cuda.empty_cache()
 
     if rank == 0:
         line = {
@@ -869,10 +965,10 @@ def main():
                        "l2": "inputs larger than L2 (W2 alone is %d MB), no flush" % (shape.N2 * shape.d * 2 >> 20)},
             "pct_of_peak": 100.0 * value / world / peaks["bf16_tflops"],
             "pct_of_sustained_peak": 100.0 * value / world / peaks["bf16_tflops_sustained"],
-            "peak": {"used": "burst for pct_of_peak; sustained for the roofline", "bf16_tflops_burst": peaks["bf16_tflops"],
+            "peak": {"used": "burst for pct_of_peak and the roofline", "bf16_tflops_burst": peaks["bf16_tflops"],
                      "bf16_tflops_sustained": peaks["bf16_tflops_sustained"], "source": peaks["source"]},
             "roofline": {"kernel": dom, "bound": "tensor", "achieved": dom_ach, "peak": peak, "unit": "TFLOP/s",
-                         "frac": dom_ach / peak, "frac_of_burst": dom_ach / peaks["bf16_tflops"],
+                         "frac": dom_ach / peak, "frac_of_sustained": dom_ach / peaks["bf16_tflops_sustained"],
                          "traffic": measured_traffic(shape.name, dom),
                          "note": "peak = %s bf16 of %s: the kernel is timed inside the step loop (stage pass); "
                                  "nvidia-smi SM clock %s of max %s MHz" % (

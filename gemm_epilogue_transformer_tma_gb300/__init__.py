@@ -97,6 +97,7 @@ SIGNATURES = {
     "coda_gemm_res_prms_fp8": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P]),
     "coda_gemm_rowscale_swiglu_fp8": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _U32, _P]),
     "coda_lmhead_ce_workspace_bytes": (_SZ, [_I64, _I64, _I64, _INT]),
+    "coda_lmhead_ce_row_offsets": (_INT, [_I64, _I64, _I64, _INT, ctypes.POINTER(_SZ), ctypes.POINTER(_SZ)]),
     "coda_lmhead_ce": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I64, _I64, _I64, _P]),
     "coda_lmhead_ce_fp8": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I64, _I64, _I64, _P]),
     "coda_unfused_workspace_bytes": (_SZ, [_I64, _I64, _I64]),
@@ -703,6 +704,23 @@ def coda_gemm_rowscale_swiglu_fp8(Hq, sH, W2gq, sW2, rstd, out, z_save=None, fla
 
 def coda_lmhead_ce_workspace_bytes(M: int, d: int, V: int, with_grads: bool) -> int:
     return load_library().coda_lmhead_ce_workspace_bytes(M, d, V, int(with_grads))
+
+
+def coda_lmhead_ce_row_offsets(M: int, d: int, V: int, with_grads: bool):
+    """Byte offsets (label logits, row losses) of the per-row fp32 results
+    that coda_lmhead_ce / coda_lmhead_ce_fp8 leave in their workspace."""
+    a, b = _SZ(0), _SZ(0)
+    _check(load_library().coda_lmhead_ce_row_offsets(M, d, V, int(with_grads), ctypes.byref(a), ctypes.byref(b)),
+           "coda_lmhead_ce_row_offsets")
+    return a.value, b.value
+
+
+def coda_lmhead_ce_row_results(ws, M: int, d: int, V: int, with_grads: bool):
+    """Views (label logits [M], row losses [M], fp32) into a workspace that a
+    completed coda_lmhead_ce call with these sizes has filled."""
+    a, b = coda_lmhead_ce_row_offsets(M, d, V, with_grads)
+    flat = ws.view(torch.uint8).reshape(-1)
+    return (flat[a:a + 4 * M].view(torch.float32), flat[b:b + 4 * M].view(torch.float32))
 
 
 def coda_lmhead_ce(Hs, Wt, labels, loss, lse, argmax, dHs, dWt, ws, stream=None):

@@ -34,7 +34,7 @@ def sources():
 
 def _deps():
     return sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h")) + \
-        [os.path.join(INCLUDE, "coda.h"), __file__]
+        glob.glob(os.path.join(INCLUDE, "*.h")) + [__file__]
 
 
 def up_to_date() -> bool:

@@ -11,6 +11,7 @@
 #include <mutex>
 
 #include "../../include/coda.h"
+#include "../../include/coda_testing.h"
 #include "coda_internal.h"
 #include "ptx.cuh"
 
@@ -21,6 +22,7 @@ struct coda_handle_s {
   uint64_t timeout_ns;
   int skip_first_stage;  // test hook for the bounded waits (coda_debug_skip_first_stage)
   int pair;              // GEMMs on SM pairs (coda_set_sm_pairing)
+  void* noalloc_scratch;  // device address of the allocation-free call's scratch, looked up on its first use
 };
 
 namespace coda {
@@ -161,6 +163,8 @@ LaunchCtx launch_ctx_of_handle(void* handle, void* stream) {
 
 int device_of_handle(void* handle) { return static_cast<coda_handle_t>(handle)->device; }
 
+void** noalloc_scratch_slot(void* handle) { return &static_cast<coda_handle_t>(handle)->noalloc_scratch; }
+
 bool make_tmap_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t ld, uint32_t box_inner,
                   uint32_t box_outer) {
   std::call_once(g_encode_once, resolve_encode);
@@ -205,6 +209,7 @@ coda_status_t coda_create(coda_handle_t* out, int device) {
   h->skip_first_stage = 0;
   h->pair = 1;
   h->status = nullptr;
+  h->noalloc_scratch = nullptr;
   coda_status_t st = CODA_OK;
   if (cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
       cudaMalloc(&h->status, sizeof(int)) != cudaSuccess || cudaMemset(h->status, 0, sizeof(int)) != cudaSuccess)
@@ -837,6 +842,17 @@ CeWs ce_layout(uint8_t* base, int64_t M, int64_t d, int64_t V, bool grads) {
 size_t coda_lmhead_ce_workspace_bytes(int64_t M, int64_t d, int64_t V, int with_grads) {
   if (M <= 0 || d <= 0 || V <= 0) return 0;
   return ce_layout(nullptr, M, d, V, with_grads != 0).bytes;
+}
+
+coda_status_t coda_lmhead_ce_row_offsets(int64_t M, int64_t d, int64_t V, int with_grads, size_t* label_logit_off,
+                                         size_t* row_loss_off) {
+  if (M <= 0 || d <= 0 || V <= 0) return CODA_ERR_INVALID_ARG;
+  // carve the layout from a stand-in base (a null base gives null pointers)
+  uint8_t* const base = reinterpret_cast<uint8_t*>(uintptr_t(256));
+  const CeWs w = ce_layout(base, M, d, V, with_grads != 0);
+  if (label_logit_off) *label_logit_off = size_t(reinterpret_cast<uint8_t*>(w.zy) - base);
+  if (row_loss_off) *row_loss_off = size_t(reinterpret_cast<uint8_t*>(w.row_loss) - base);
+  return CODA_OK;
 }
 
 coda_status_t coda_lmhead_ce(coda_handle_t h, const void* Hs, const void* Wt, const int32_t* labels, float* loss,

@@ -64,6 +64,9 @@ cudaError_t launch_chained(const LaunchCtx& c, void (*kern)(KArgs...), dim3 grid
 // opaque coda_handle_t.
 LaunchCtx launch_ctx_of_handle(void* handle, void* stream);
 int device_of_handle(void* handle);
+// The handle's slot for the device address of the allocation-free call's
+// scratch array (noalloc.cu); null until that call first runs on the handle.
+void** noalloc_scratch_slot(void* handle);
 
 // ---- GEMM launchers (gemm_*.cu) --------------------------------------------
 // Operand majors: A K-major = [M][K], MN-major = [K][M]; B K-major = [N][K],

@@ -176,8 +176,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi>(),
               if (!mbar_wait_timeout(&full[st], (parity >> st) & 1u, ctl.timeout_ns))
                 atomicOr(ctl.status, DEV_ERR_TIMEOUT_DRAIN);
         } else {
-          // the peer's copies complete on the leader's barrier: give any that
-          // are still in flight a grace period (copies take microseconds)
+          // The peer's copies complete on the leader's barrier, which this
+          // CTA cannot wait on, so it waits out a fixed grace period instead.
+          // 2 ms bounds them with a wide margin: the bytes in flight on the
+          // whole GPU cannot exceed the operand rings of the resident CTAs
+          // (152 SMs x 6 stages x 32 KB = 29 MB), which HBM delivers in
+          // about 5 us; a copy is bounded by that queue, not by a wait on
+          // anything this kernel controls.
           const uint64_t t0 = globaltimer_ns();
           while (globaltimer_ns() - t0 < 2000000ull) {
           }

@@ -12,26 +12,30 @@
 #include "../../include/coda.h"
 #include "coda_internal.h"
 
+// Scratch for the dg partial sums: 8 MiB, reserved on a device once this
+// file's module is loaded there (at the latest on the first call on that
+// device) and held until the process exits.  It covers coda_dgpart_rows(M)
+// * d <= 2 Mi floats, e.g. M = 8192 tokens at d = 8192 or M = 16384 at
+// d = 4096.
+static constexpr size_t kScratchBytes = size_t(8) << 20;
+static __device__ __align__(256) float g_dgpart_scratch[kScratchBytes / sizeof(float)];
+
 namespace coda {
 namespace {
 
-// Scratch for the dg partial sums: 8 MiB per device, held by every GPU that
-// loads the library until the process exits.  It covers coda_dgpart_rows(M)
-// * d <= 2 Mi floats, e.g. M = 8192 tokens at d = 8192 or M = 16384 at d = 4096.
-constexpr size_t kScratchBytes = size_t(8) << 20;
-__device__ __align__(256) float g_dgpart_scratch[kScratchBytes / sizeof(float)];
-
-constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-float* g_scratch_addr[kMaxDevices] = {};
 
-// Device address of g_dgpart_scratch on `dev`.  In host code the array's name
-// is only a host-side stand-in, so the address is looked up once per device,
-// with that device current, and cached.
-coda_status_t scratch_on_device(int dev, float** out) {
-  if (dev < 0 || dev >= kMaxDevices) return CODA_ERR_UNSUPPORTED;
+// Device address of g_dgpart_scratch for the handle's device and context.
+// In host code the array's name is only a host-side stand-in, so the address
+// is looked up with the handle's device current, on the first call with that
+// handle, and kept in the handle.  A handle belongs to one context (its status
+// word does too), so a handle created after a device reset looks the address
+// up afresh instead of reusing one from the destroyed context.
+coda_status_t scratch_of_handle(void* h, float** out) {
   std::lock_guard<std::mutex> lock(g_mu);
-  if (g_scratch_addr[dev] == nullptr) {
+  void** slot = noalloc_scratch_slot(h);
+  if (*slot == nullptr) {
+    const int dev = device_of_handle(h);
     int prev = 0;
     if (cudaGetDevice(&prev) != cudaSuccess) return CODA_ERR_CUDA;
     if (prev != dev && cudaSetDevice(dev) != cudaSuccess) return CODA_ERR_CUDA;
@@ -39,9 +43,9 @@ coda_status_t scratch_on_device(int dev, float** out) {
     const cudaError_t e = cudaGetSymbolAddress(&p, g_dgpart_scratch);
     if (prev != dev) cudaSetDevice(prev);
     if (e != cudaSuccess || p == nullptr) return CODA_ERR_CUDA;
-    g_scratch_addr[dev] = static_cast<float*>(p);
+    *slot = p;
   }
-  *out = g_scratch_addr[dev];
+  *out = static_cast<float*>(*slot);
   return CODA_OK;
 }
 
@@ -76,7 +80,7 @@ extern "C" coda_status_t coda_gemm_dgrad_rmsbwd_noalloc(coda_handle_t h, const v
     return cudaMemsetAsync(dg, 0, size_t(d) * sizeof(float), cx.stream) == cudaSuccess ? CODA_OK : CODA_ERR_CUDA;
   }
   float* scratch = nullptr;
-  const coda_status_t st = scratch_on_device(device_of_handle(h), &scratch);
+  const coda_status_t st = scratch_of_handle(h, &scratch);
   if (st != CODA_OK) return st;
   // The GEMM epilogue writes every partial the combine reads (all
   // coda_dgpart_rows(M) x d entries), so nothing left by an earlier call is

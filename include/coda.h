@@ -98,21 +98,6 @@ coda_status_t coda_set_wait_timeout_ns(coda_handle_t h, uint64_t ns);
  * inside the tensor core; the choice only affects speed. */
 coda_status_t coda_set_sm_pairing(coda_handle_t h, int enable);
 
-/* Failure-detection test hook.  While enabled, every GEMM launched through
- * this handle leaves the first shared-memory stage of its first CTA unfilled,
- * so that CTA's MMA wait cannot complete and must hit the wait limit: the
- * launch then records CODA_ERR_TIMEOUT (reported by coda_sync_status), its
- * results are invalid, and the context stays usable.  Pair it with a short
- * coda_set_wait_timeout_ns.  Not for production use. */
-coda_status_t coda_debug_skip_first_stage(coda_handle_t h, int enable);
-
-/* Host-side check of the tile schedule of the grouped launches (no GPU
- * needed): P clusters, the heavy problem's index (0 or 1), its tile count nH,
- * the light problem's tile count nL, q catch-up tiles.  Returns 0 when every
- * tile of both problems is assigned to exactly one cluster, the number of
- * violations otherwise, -1 for invalid arguments.  Not for production use. */
-int coda_debug_group_schedule_violations(int P, int heavy, int nH, int nL, int q);
-
 /* Columns of a block-reduction partial buffer over n columns: ceil(n / 128).
  * Partial j of a row covers columns [128 j, 128 j + 128) (half of a 256-column
  * output tile).  Used for the partial RMS (n = d), the SwiGLU-backward c
@@ -237,11 +222,15 @@ coda_status_t coda_gemm_dgrad_rmsbwd(coda_handle_t h, const void* dP, const void
  *   Limit: coda_dgpart_rows(M) * d * 4 bytes must not exceed 8 MiB (e.g. M up
  *   to 8192 at d = 8192, or 16384 at d = 4096); larger problems are rejected
  *   with CODA_ERR_WORKSPACE_TOO_SMALL before anything is launched.  The 8 MiB
- *   array is held on every GPU that loads the library until the process
- *   exits.
- *   The first call on a device looks up the array's device address (with that
- *   device current) and caches it; make that first call before any stream
- *   capture.
+ *   array is a file-scope static __device__ array: it is reserved on a device
+ *   once the library's module holding it is loaded there (with the CUDA
+ *   runtime's lazy loading, at the latest on the first call on that device)
+ *   and held until the process exits.
+ *   The first call with a given handle looks up the array's device address
+ *   (with the handle's device current) and keeps it in the handle; make that
+ *   first call before any stream capture.  Handles do not outlive their
+ *   context: after a device reset, create a new handle, which looks the
+ *   address up again.
  *   All calls share the one array per device: calls that may overlap on the
  *   GPU (different streams, or different host threads) race on it and must be
  *   serialised by the caller.  Every partial a call reads is written earlier
@@ -251,8 +240,8 @@ coda_status_t coda_gemm_dgrad_rmsbwd_noalloc(coda_handle_t h, const void* dP, co
                                              int64_t N2, int64_t d, void* stream);
 
 /* SwiGLU backward in the epilogue of the down projection's data gradient
- * (the first "next" row: the upstream gradient dY of the SwiGLU output is
- * never written to HBM).  With the down projection y = out W3 (nn.Linear
+ * (the upstream gradient dY of the SwiGLU output stays on chip and is never
+ * written to HBM).  With the down projection y = out W3 (nn.Linear
  * layout W3t[d][F]) and its upstream gradient dYb:
  *   dY[m][j] = sum_k dYb[m][k] W3t[k][j]                 (mainloop, on chip)
  *   dP = bf16(rstd[m] * dZ), dZ = d(silu(z_gate) * z_up) applied to dY
@@ -554,6 +543,21 @@ coda_status_t coda_gemm_rowscale_swiglu_fp8(coda_handle_t h, const void* Hq, con
 
 /* Workspace of coda_lmhead_ce (with_grads = 0: forward only). */
 size_t coda_lmhead_ce_workspace_bytes(int64_t M, int64_t d, int64_t V, int with_grads);
+
+/* Per-row results that coda_lmhead_ce and coda_lmhead_ce_fp8 leave in their
+ * workspace (the per-token losses behind the mean, e.g. for masking or
+ * logging).  Writes the byte offsets, from the workspace's start, of:
+ *   *label_logit_off: fp32 [M], L[m][y_m], the logit of row m's label,
+ *                     gathered by the epilogue of the vocabulary tile that
+ *                     holds column y_m (0 for a label outside [0, V));
+ *   *row_loss_off:    fp32 [M], lse[m] - L[m][y_m] (0 for a label outside
+ *                     [0, V)); the loss output is their mean.
+ * Both offsets are multiples of 256.  The values are those of the last call
+ * on that workspace with the same M, d, V and with_grads, once it has
+ * completed on its stream.  Either output pointer may be NULL.  Returns
+ * CODA_ERR_INVALID_ARG for M, d or V <= 0. */
+coda_status_t coda_lmhead_ce_row_offsets(int64_t M, int64_t d, int64_t V, int with_grads, size_t* label_logit_off,
+                                         size_t* row_loss_off);
 
 /* Mean softmax cross-entropy of the logits L = Hs Wt^T against labels,
  * without ever writing an [M][V] logits tensor:

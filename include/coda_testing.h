@@ -1,0 +1,31 @@
+/* Test hooks of libcoda.  These entry points exist so that the library's own
+ * tests can exercise failure detection and check host-side scheduling logic
+ * without a GPU fault; they are exported by libcoda.so beside the entry
+ * points of coda.h but are not part of the library's interface for users,
+ * and no computation of the block path depends on them. */
+#pragma once
+
+#include "coda.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Failure-detection test hook.  While enabled, every GEMM launched through
+ * this handle leaves the first shared-memory stage of its first CTA unfilled,
+ * so that CTA's MMA wait cannot complete and must hit the wait limit: the
+ * launch then records CODA_ERR_TIMEOUT (reported by coda_sync_status), its
+ * results are invalid, and the context stays usable.  Pair it with a short
+ * coda_set_wait_timeout_ns.  Not for production use. */
+coda_status_t coda_debug_skip_first_stage(coda_handle_t h, int enable);
+
+/* Host-side check of the tile schedule of the grouped launches (no GPU
+ * needed): P clusters, the heavy problem's index (0 or 1), its tile count nH,
+ * the light problem's tile count nL, q catch-up tiles.  Returns 0 when every
+ * tile of both problems is assigned to exactly one cluster, the number of
+ * violations otherwise, -1 for invalid arguments.  Not for production use. */
+int coda_debug_group_schedule_violations(int P, int heavy, int nH, int nL, int q);
+
+#ifdef __cplusplus
+}
+#endif

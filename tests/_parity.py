@@ -1,17 +1,28 @@
 """Tolerances and comparison helpers shared by the GPU parity tests.
 
 Bars (bf16 inputs/outputs, fp32 accumulation):
-  * elementwise  max |gpu - ref| / (|ref| + 1e-3 * s) <= 2e-2, graded per
-    stage against the oracle fed the GPU's own stage inputs, where
-    s = max(1, rms(ref)): the absolute floor is in units of the tensor's own
-    scale (identical to a 1e-3 floor for unit-scale data).  A fixed floor
-    cannot hold for larger-scale outputs: at the 70B size a bf16 cuBLAS GEMM
-    on the same inputs misses it by the same margin as this library;
+  * elementwise  max |gpu - ref| / (|ref| + 1e-3) <= 2e-2, graded per stage
+    against the oracle fed the GPU's own stage inputs.  The 1e-3 floor is
+    absolute.  For a few named (test, tensor) pairs whose values are far from
+    unit scale (listed in SCALED_FLOOR with the reason), that fixed floor is
+    below what any fp32-accumulating GEMM reaches near zero crossings; there
+    the test must show instead that cuBLAS on the same inputs (bf16 GEMM,
+    fp32 accumulation) misses the fixed floor about as badly: fixed-floor
+    error no worse than 1.25x cuBLAS's.  Every other tensor is held to the
+    fixed floor.  The error with the floor scaled to 1e-3 * max(1, rms(ref))
+    is reported beside it;
   * relative Frobenius ||gpu - ref|| / ||ref|| <= 5e-3, graded end to end
     against the oracle chained from the seeded inputs;
-  * integer outputs (argmax) exact wherever the oracle's top-2 gap is wider
-    than the fp32 accumulation error, else either index may win.
+  * integer outputs (argmax, label logits' indices) exact wherever the
+    oracle's top-2 gap is wider than the fp32 accumulation error, else either
+    index may win.
+
+Setting CODA_PARITY_LOG to a file path appends one JSON line per graded
+tensor (test, tensor, strict and scaled-floor errors) to that file.
 """
+import json
+import os
+
 import numpy as np
 import torch
 
@@ -19,19 +30,61 @@ from coda_inputs import to_f64
 
 ELEM_TOL = 2e-2
 FROB_TOL = 5e-3
+FLOOR = 1e-3
+
+# (test function, tensor name) -> why the fixed floor cannot hold there.
+# Each entry's test passes the same quantity computed by cuBLAS on the same
+# inputs (its bf16 GEMM with fp32 accumulation, the epilogue arithmetic in
+# fp32 on its fp32 result); that pair then passes when its fixed-floor error
+# is no worse than 1.25x cuBLAS's.  The scaled-floor error is reported beside.
+# The measured fixed-floor errors (library = cuBLAS to the digits shown)
+# come from full-size runs on a GB300.
+_K7 = "7B backward: long-K tensor-core sums (K = 28672 or M = 8192) far from unit scale"
+_K70 = "70B: long-K tensor-core sums (K = 8192 to 57344) far from unit scale"
+CUBLAS_RELATIVE = {
+    ("test_7b_forward_backward_full_size", "dH"): _K7 + "; 1.21e-1, cuBLAS 1.21e-1",
+    ("test_7b_forward_backward_full_size", "dg"): _K7 + "; rms 261, 1.50e-1",
+    ("test_7b_forward_backward_full_size", "dW2t columns"): _K7 + "; rms 79, 3.83e-1, cuBLAS 3.83e-1",
+    ("test_7b_forward_backward_full_size", "dW2t rows"): _K7 + "; rms 79, 3.81e-1, cuBLAS 3.81e-1",
+    ("test_7b_forward_backward_full_size", "dW1t rows"): _K7 + "; rms 165, 4.13e-1, cuBLAS 4.13e-1",
+    ("test_7b_forward_backward_full_size", "dW1t columns"): _K7 + "; rms 166, 3.10e-1, cuBLAS 3.10e-1",
+    ("test_70b_forward_backward_full_size", "H"): _K70 + "; 3.70e-2, cuBLAS 3.70e-2",
+    ("test_70b_forward_backward_full_size", "z"): _K70 + "; 3.13e-2, cuBLAS 3.13e-2",
+    ("test_70b_forward_backward_full_size", "out"): _K70 + "; 7.31e-2, cuBLAS 7.31e-2",
+    ("test_70b_forward_backward_full_size", "dH"): _K70 + "; 3.50e-1, cuBLAS 3.50e-1",
+    ("test_70b_forward_backward_full_size", "dg"): _K70 + "; rms 387, 9.97e-1",
+    ("test_70b_forward_backward_full_size", "dX"): _K70 + "; 5.20e-2, cuBLAS 5.20e-2",
+    ("test_70b_forward_backward_full_size", "dW2t columns"): _K70 + "; rms 85, 5.53e-1, cuBLAS 5.53e-1",
+    ("test_70b_forward_backward_full_size", "dW2t rows"): _K70 + "; rms 84, 2.11e-1, cuBLAS 2.11e-1",
+    ("test_70b_forward_backward_full_size", "dW1t rows"): _K70 + "; rms 195, 3.10e-1, cuBLAS 3.10e-1",
+    ("test_70b_forward_backward_full_size", "dW1t columns"): _K70 + "; rms 196, 3.33e-1, cuBLAS 3.33e-1",
+    ("test_gemm2_epilogue_saturation", "out (saturating)"):
+        "row scale 60-120 and silu ~ 100 amplify the accumulator's error near z_up's zero crossings; "
+        "rms 6.4e3, 6.15e-2",
+}
 
 
 def f64(t):
     return to_f64(t) if isinstance(t, torch.Tensor) else np.asarray(t, np.float64)
 
 
-def elem_err(gpu, ref):
-    g, r = f64(gpu), f64(ref)
+def _elem(g, r, floor):
     assert g.shape == r.shape, (g.shape, r.shape)
     if g.size == 0:
         return 0.0
-    scale = max(1.0, float(np.sqrt(np.mean(r * r))))
-    return float(np.max(np.abs(g - r) / (np.abs(r) + 1e-3 * scale)))
+    return float(np.max(np.abs(g - r) / (np.abs(r) + floor)))
+
+
+def elem_err(gpu, ref):
+    """max |gpu - ref| / (|ref| + 1e-3): the fixed-floor elementwise error."""
+    return _elem(f64(gpu), f64(ref), FLOOR)
+
+
+def elem_err_scaled(gpu, ref):
+    """The same with the floor in units of the reference's rms (>= 1e-3)."""
+    g, r = f64(gpu), f64(ref)
+    scale = max(1.0, float(np.sqrt(np.mean(r * r)))) if r.size else 1.0
+    return _elem(g, r, FLOOR * scale)
 
 
 def frob_err(gpu, ref):
@@ -41,14 +94,75 @@ def frob_err(gpu, ref):
     return float(np.linalg.norm(g - r) / (n if n > 0 else 1.0))
 
 
-def assert_elem(gpu, ref, name, tol=ELEM_TOL):
-    e = elem_err(gpu, ref)
-    assert e <= tol, f"{name}: elementwise err {e:.3e} > {tol:.1e}"
-    return e
+def _current_test():
+    cur = os.environ.get("PYTEST_CURRENT_TEST", "")
+    node = cur.split(" ")[0]
+    func = node.split("::")[-1].split("[")[0] if node else ""
+    return node, func
+
+
+def _log(rec):
+    path = os.environ.get("CODA_PARITY_LOG")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps(rec) + "\n")
+
+
+def _grade(diff, absref, name, tol, e_cub):
+    """Shared verdict of assert_elem / assert_elem_chunks on |gpu - ref| and
+    |ref| (flat float64 arrays of one tensor); e_cub: cuBLAS's fixed-floor
+    error on the same inputs, or None."""
+    if diff.size == 0:
+        return 0.0
+    strict = float(np.max(diff / (absref + FLOOR)))
+    scale = max(1.0, float(np.sqrt(np.mean(absref * absref))))
+    scaled = float(np.max(diff / (absref + FLOOR * scale)))
+    node, func = _current_test()
+    _log({"test": node, "tensor": name, "strict": strict, "scaled": scaled, "rms_ref": scale, "tol": tol,
+          "cublas_strict": e_cub, "n": int(diff.size)})
+    msg = (f"{name}: elementwise err {strict:.3e} (fixed 1e-3 floor), {scaled:.3e} (floor x rms {scale:.3g}); "
+           f"bar {tol:.1e}" + ("" if e_cub is None else f"; cuBLAS on the same inputs {e_cub:.3e}"))
+    if strict <= tol:
+        return strict
+    assert (func, name) in CUBLAS_RELATIVE, msg
+    assert e_cub is not None, f"{msg}; listed as cuBLAS-relative but no cuBLAS result given"
+    assert strict <= 1.25 * e_cub, msg
+    return strict
+
+
+def _strict(g, r):
+    return float(np.max(np.abs(g - r) / (np.abs(r) + FLOOR))) if r.size else 0.0
+
+
+def assert_elem(gpu, ref, name, tol=ELEM_TOL, cublas=None):
+    """Grade `gpu` against `ref` elementwise; returns the fixed-floor error.
+
+    `cublas`: the same quantity from cuBLAS on the same inputs; it is graded
+    beside, and it decides the bar for the pairs in CUBLAS_RELATIVE."""
+    g, r = f64(gpu), f64(ref)
+    assert g.shape == r.shape, (g.shape, r.shape)
+    e_cub = _strict(f64(cublas), r) if cublas is not None else None
+    return _grade(np.abs(g - r).ravel(), np.abs(r).ravel(), name, tol, e_cub)
+
+
+def assert_elem_chunks(parts, name, tol=ELEM_TOL):
+    """assert_elem over one tensor handed in as (gpu, ref) or (gpu, ref,
+    cublas) chunks (e.g. row blocks of an output too large to hold twice in
+    fp64)."""
+    diffs, refs, e_cub = [], [], None
+    for part in parts:
+        g, r = f64(part[0]), f64(part[1])
+        assert g.shape == r.shape, (g.shape, r.shape)
+        diffs.append(np.abs(g - r).ravel())
+        refs.append(np.abs(r).ravel())
+        if len(part) > 2 and part[2] is not None:
+            e_cub = max(e_cub or 0.0, _strict(f64(part[2]), r))
+    return _grade(np.concatenate(diffs), np.concatenate(refs), name, tol, e_cub)
 
 
 def assert_frob(gpu, ref, name, tol=FROB_TOL):
     e = frob_err(gpu, ref)
+    _log({"test": _current_test()[0], "tensor": name, "frob": e, "tol": tol})
     assert e <= tol, f"{name}: relative Frobenius err {e:.3e} > {tol:.1e}"
     return e
 

@@ -10,7 +10,7 @@ import subprocess
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "coda.h")
+HEADERS = [os.path.join(ROOT, "include", n) for n in ("coda.h", "coda_testing.h")]
 
 
 @pytest.fixture(scope="module")
@@ -22,7 +22,7 @@ def lib():
 
 
 def declared():
-    src = open(HEADER).read()
+    src = "".join(open(h).read() for h in HEADERS)
     return set(re.findall(r"^\s*(?:coda_status_t|const char\*|int64_t|size_t|int)\s+(coda_\w+)\s*\(", src, re.M))
 
 
@@ -61,6 +61,16 @@ def test_host_queries(lib):
         2 * M * (4096 + d + N2 // 2) * 2
     # FP8: codes instead of W2g and the bf16 workspace, so a smaller arena
     assert 0 < lib.coda_block_arena_bytes(M, 4096, d, N2, 3) < lib.coda_block_arena_bytes(M, 4096, d, N2, 1)
+    # per-row CE results: label logits then row losses, after the three
+    # [M][ceil(V/128)] partial arrays, inside the workspace
+    M, d, V = 8192, 2048, 128256
+    a, b = ctypes.c_size_t(), ctypes.c_size_t()
+    for grads in (0, 1):
+        assert lib.coda_lmhead_ce_row_offsets(M, d, V, grads, ctypes.byref(a), ctypes.byref(b)) == 0
+        part = -(-(M * (V // 128) * 4) // 256) * 256
+        assert a.value == 3 * part and b.value == a.value + M * 4
+        assert b.value + M * 4 <= lib.coda_lmhead_ce_workspace_bytes(M, d, V, grads)
+    assert lib.coda_lmhead_ce_row_offsets(0, d, V, 0, None, None) == 1
     assert lib.coda_status_string(0) == b"ok"
     assert b"time limit" in lib.coda_status_string(6)
 

@@ -1,15 +1,20 @@
 """LM-head cross-entropy with the blocked log-sum-exp epilogue vs the fp64
 oracle (Synced write-up, section 五种积木: block reduction "block
-log-sum-exp" and the stateful max / sum-exp statistics).
+log-sum-exp" and the stateful max / sum-exp statistics; the label logit is
+gathered by the epilogue of the vocabulary tile that holds the label).
 
 Small vocabularies that still span several 256-column tiles with a ragged
-last tile, plus several 16384-column backward chunks."""
+last tile, plus several 16384-column backward chunks.  Every row's label
+logit and row loss is read back from the workspace and graded, with labels
+placed on the 128- and 256-column tile edges, the backward chunk edges and
+the last (ragged) tile."""
 import numpy as np
 import pytest
 import torch
 
 import oracle as O
 from coda_inputs import CEShape, ce_inputs
+from tests._ce import check_argmax, check_label_rows, check_row_loss, known_answer_ce, with_edge_labels
 from tests._parity import assert_device_ok, assert_elem, assert_frob, f64
 
 pytestmark = pytest.mark.gpu
@@ -34,26 +39,15 @@ def run_ce(H, Wt, labels, grads=True):
     dW = torch.empty(V, d, dtype=torch.bfloat16, device="cuda") if grads else None
     C.coda_lmhead_ce(H, Wt, labels, out["loss"], out["lse"], out["argmax"], dH, dW, ws)
     out["dH"], out["dW"] = dH, dW
+    out["zy"], out["row_loss"] = C.coda_lmhead_ce_row_results(ws, M, d, V, grads)
     return out
-
-
-def check_argmax(gpu_am, H, Wt, tol_gap=1e-3):
-    L = O.logits_rows(H, Wt)
-    ref = O.argmax_lowest(L)
-    srt = np.sort(L, axis=1)
-    gap = srt[:, -1] - srt[:, -2]
-    decided = gap > tol_gap
-    got = gpu_am.cpu().numpy().astype(np.int64)
-    assert np.array_equal(got[decided], ref[decided])
-    # undecided rows: the GPU's choice must be a maximal column within the gap
-    for m in np.where(~decided)[0]:
-        assert L[m, got[m]] >= srt[m, -1] - tol_gap
 
 
 @pytest.mark.parametrize("M,d,V", [(200, 136, 1000), (128, 64, 256), (37, 256, 40000)])
 def test_ce_parity(M, d, V, pairing):
     s = CEShape("t", M, d, V)
     x = {k: v.cuda() for k, v in ce_inputs(s, 0).items()}
+    x["labels"] = with_edge_labels(x["labels"], V)
     o = run_ce(x["H"], x["Wt"], x["labels"])
     assert_device_ok()
     H, Wt, y = f64(x["H"]), f64(x["Wt"]), x["labels"].cpu().numpy()
@@ -61,7 +55,9 @@ def test_ce_parity(M, d, V, pairing):
     bw = O.ce_backward(H, Wt, y)
     assert_elem(o["lse"], fw["lse"], "lse", tol=1e-4)
     assert abs(o["loss"].item() - fw["loss"]) <= 1e-4 * abs(fw["loss"])
-    check_argmax(o["argmax"], H, Wt)
+    L = O.logits_rows(H, Wt)
+    check_argmax(o["argmax"], H, Wt, L=L)
+    check_label_rows(o["zy"], o["row_loss"], L, y, fw["lse"])
     assert_frob(o["dH"], bw["dH"], "dH")
     assert_frob(o["dW"], bw["dWt"], "dW")
 
@@ -84,6 +80,10 @@ def test_ce_forward_only_and_label_range():
     yy = lab.cpu().numpy()
     per_row = np.where(ok, lse - L[np.arange(64), np.clip(yy, 0, 511)], 0.0)
     assert abs(o["loss"].item() - per_row.mean()) <= 1e-4 * abs(per_row.mean())
+    # rows with a label outside [0, V) gather nothing and contribute 0
+    zy, rl = f64(o["zy"]), f64(o["row_loss"])
+    assert zy[3] == 0.0 and zy[5] == 0.0 and rl[3] == 0.0 and rl[5] == 0.0
+    check_label_rows(zy[ok], rl[ok], L[ok], yy[ok], lse[ok])
     assert_device_ok()
 
 
@@ -125,6 +125,26 @@ def test_ce_large_logits_and_edge_labels(pairing):
         assert torch.isfinite(o[k].float()).all(), k
     assert_elem(o["lse"], fw["lse"], "lse (large logits)", tol=1e-4)
     assert abs(o["loss"].item() - fw["loss"]) <= 1e-4 * abs(fw["loss"])
-    check_argmax(o["argmax"], Hf, Wt)
+    check_argmax(o["argmax"], Hf, Wt, L=L)
+    # logits of several hundred: the fp32 accumulation error is ~1e-5 of them
+    check_label_rows(o["zy"], o["row_loss"], L, y, fw["lse"], tol_gap=0.05)
     assert_frob(o["dH"], bw["dH"], "dH (large logits)")
     assert_frob(o["dW"], bw["dWt"], "dW (large logits)")
+
+
+@pytest.mark.parametrize("M,d,V", [(200, 64, 1000), (37, 256, 40000), (256, 16, 128256)])
+def test_ce_label_logit_and_argmax_known_answer(M, d, V, pairing):
+    """Label indexing and argmax bit-exact on every row: integer logits
+    L[m, v] = +-pi(v) for a fixed permutation pi (exact in any fp32
+    summation order), labels on the tile and chunk edges."""
+    H, Wt, lab, zy_ref, am_ref = known_answer_ce(M, d, V, seed=M + V)
+    o = run_ce(H.cuda(), Wt.cuda(), lab.cuda(), grads=False)
+    assert_device_ok()
+    assert np.array_equal(f64(o["zy"]), zy_ref)
+    assert np.array_equal(o["argmax"].cpu().numpy().astype(np.int64), am_ref)
+    # lse = max + log sum exp(L - max) of the integer logits; the row loss
+    piv = f64(Wt)[:, 0] + 128 * f64(Wt)[:, 1] + 16384 * f64(Wt)[:, 2]
+    L = np.where(np.arange(M) % 2 == 0, 1.0, -1.0)[:, None] * piv[None, :]
+    lse_ref = O.lse_rows(L)
+    assert_elem(o["lse"], lse_ref, "lse (integer logits)", tol=1e-5)
+    check_row_loss(o["row_loss"], lse_ref, zy_ref)

@@ -1,10 +1,16 @@
 """Parity at the full workload sizes, in the launch configuration the bench
-times (same entry points, persistent grids), on sampled outputs the fp64
-oracle can compute row by row or column by column.
+times (same entry points, persistent grids), on whole rows and whole columns
+the fp64 oracle computes in seconds.
 
 Each stage is graded elementwise against the oracle fed the GPU's own stage
-inputs; the forward output is also graded end to end (Frobenius) against the
-oracle chained from the seeded inputs on the sampled rows.  Workloads: the 1B
+inputs: whole rows (every column) of H, z, out, dP and dX on at least 256
+rows, taken from the first and last row tiles, both sides of the 128- and
+256-row tile edges and at random; every row of psum, rstd, c and dH (dH and
+dg from a full row-blocked oracle pass of the second GEMM's data gradient);
+all of dg; at least 64 whole columns and 64 whole rows of dW2t and dW1t,
+including the first and last column tiles and the gate/up boundary.  The
+forward output is also graded end to end (Frobenius) against the oracle
+chained from the seeded inputs on the sampled rows.  Workloads: the 1B
 forward, the 7B and 70B forward+backward, and the LM-head cross-entropy
 (Synced write-up, sections 尾声 / 五种积木 / 实验结果: GEMM-RMSNorm-GEMM at
 the 1B, 7B and 70B hidden sizes).
@@ -15,17 +21,32 @@ import torch
 
 import oracle as O
 from coda_inputs import B1, B7, B70, LMHEAD, block_inputs, ce_inputs
-from tests._parity import assert_device_ok, assert_elem, assert_frob, elem_err, f64
+from tests._ce import check_argmax, check_label_rows, edge_labels, known_answer_ce
+from tests._parity import assert_device_ok, assert_elem, assert_elem_chunks, assert_frob, f64
 
 pytestmark = pytest.mark.gpu
 
 C = pytest.importorskip("gemm_epilogue_transformer_tma_gb300")
 from gemm_epilogue_transformer_tma_gb300.path import BlockBuffers  # noqa: E402
 
+CHUNK = 1024  # rows per oracle block for the whole-tensor passes
 
-def sample(n, k, seed):
+
+def edge_sample(n, k, seed, tiles=(128, 256), extra=()):
+    """At least k sorted indices in [0, n): the first and last four, both
+    sides of every multiple of the tile sizes within the first two and the
+    last two tiles, any `extra` edges, and random others."""
+    idx = set(range(min(4, n))) | set(range(max(0, n - 4), n))
+    for t in tiles:
+        for e in (t, 2 * t, ((n - 1) // t) * t, ((n - 1) // t - 1) * t):
+            idx |= {e - 2, e - 1, e, e + 1}
+    for e in extra:
+        idx |= {e - 1, e, e + 1}
+    idx = {i for i in idx if 0 <= i < n}
     r = np.random.default_rng(seed)
-    idx = set(r.choice(n, size=min(k, n), replace=False).tolist()) | {0, n - 1}
+    rest = np.setdiff1d(np.arange(n), np.fromiter(idx, int))
+    need = max(0, k - len(idx))
+    idx |= set(r.choice(rest, size=min(need, rest.size), replace=False).tolist())
     return np.array(sorted(idx))
 
 
@@ -37,18 +58,15 @@ def cols_of(t, idx):
     return f64(t[:, torch.as_tensor(idx, device=t.device)])
 
 
-def dgrad2_sampled(b, kcols, rows, chunk=1024):
-    """Oracle dH[rows][:, kcols] and dg[kcols] from the GPU's stage inputs
-    (dP, c, H), summing the oracle's dg over row chunks."""
-    W2k = cols_of(b.W2t, kcols)
-    gk = f64(b.g)[kcols]
-    dg = np.zeros(len(kcols))
-    for s in range(0, b.M, chunk):
-        e = min(b.M, s + chunk)
-        _, part = O.stage_dgrad2_rmsbwd(f64(b.dP[s:e]), W2k, gk, cols_of(b.H[s:e], kcols), f64(b.c[s:e]))
-        dg += part
-    dh, _ = O.stage_dgrad2_rmsbwd(rows_of(b.dP, rows), W2k, gk, rows_of(b.H, rows)[:, kcols], f64(b.c)[rows])
-    return dh, dg
+def row_blocks(M):
+    return [(s, min(M, s + CHUNK)) for s in range(0, M, CHUNK)]
+
+
+def mm_f32(A, B):
+    """cuBLAS bf16 GEMM A B with its fp32 result (fp32 accumulation, no
+    rounding of the product to bf16): the library's counterpart where an
+    epilogue consumes the fp32 accumulator."""
+    return torch.mm(A, B, out_dtype=torch.float32)
 
 
 def check_block(shape, backward: bool):
@@ -58,57 +76,87 @@ def check_block(shape, backward: bool):
     if backward:
         b.backward_stages()
     assert_device_ok()
-    M, d, F = shape.M, shape.d, shape.F
-    rows = sample(M, 12, 1)
-    jcols = sample(F, 16, 2)
-    kcols = sample(d, 16, 3)
-    ncols = np.concatenate([jcols, F + jcols])
+    M, d, F, K1 = shape.M, shape.d, shape.F, shape.K1
+    rows = edge_sample(M, 256, 1)
+    jcols = edge_sample(F, 32, 2)
+    ncols = np.concatenate([jcols, F + jcols])          # gate and matching up rows of W2t
+    kcols = edge_sample(d, 64, 3)
+    icols = edge_sample(K1, 64, 4)
+    ri, ni, ki, ii = (torch.as_tensor(v, device="cuda") for v in (rows, ncols, kcols, icols))
+    bf = torch.bfloat16
     W1t = f64(b.W1t)
+    W2t = f64(b.W2t)
     g = f64(b.g)
-    # a1 fold
-    assert_elem(rows_of(b.W2gt, ncols), O.fold_weight(rows_of(b.W2t, ncols), g), "W2gt")
-    # a2 GEMM1 + residual, partial RMS
+    # a1 fold: whole rows of W2gt (gate and up)
+    assert_elem(rows_of(b.W2gt, ncols), O.fold_weight(W2t[ncols], g), "W2gt")
+    # a2 GEMM1 + residual (whole rows), partial RMS (every row)
     H = rows_of(b.H, rows)
-    assert_elem(H, O.gemm_residual(rows_of(b.X, rows), W1t, rows_of(b.R, rows)), "H")
-    assert_elem(rows_of(b.psum, rows), O.partial_sumsq(H, C.PARTIAL_COLS), "psum", tol=1e-4)
-    # a3 combine
+    cub = (mm_f32(b.X[ri], b.W1t.t()) + b.R[ri].float()).to(bf)
+    assert_elem(H, O.gemm_residual(rows_of(b.X, rows), W1t, rows_of(b.R, rows)), "H", cublas=cub)
+    Hall = f64(b.H)
+    psum_all = f64(b.psum)
+    assert_elem(psum_all, O.partial_sumsq(Hall, C.PARTIAL_COLS), "psum", tol=1e-4)
+    # a3 combine, every row
+    assert_elem(b.rstd, O.rstd_from_partials(psum_all, d, shape.eps), "rstd", tol=1e-5)
     rstd = f64(b.rstd)[rows]
-    assert_elem(rstd, O.rstd_from_partials(rows_of(b.psum, rows), d, shape.eps), "rstd", tol=1e-5)
-    # a4 GEMM2 + row scale + SwiGLU on sampled gate/up columns
-    z_ref = O.rowscale_gemm(H, rows_of(b.W2gt, ncols), rstd)
-    assert_elem(rows_of(b.z, rows)[:, ncols], z_ref, "z")
+    # a4 GEMM2 + row scale + SwiGLU, whole rows
+    z_ref = O.rowscale_gemm(H, f64(b.W2gt), rstd)
+    z32 = b.rstd[ri, None] * mm_f32(b.H[ri], b.W2gt.t())
+    assert_elem(rows_of(b.z, rows), z_ref, "z", cublas=z32.to(bf))
     out_ref = O.swiglu(z_ref)
-    assert_elem(rows_of(b.out, rows)[:, jcols], out_ref, "out")
-    # end to end on the sampled rows and columns
-    full = O.block_forward(rows_of(b.X, rows), W1t, rows_of(b.R, rows), g, rows_of(b.W2t, ncols), shape.eps, True)
-    assert_frob(rows_of(b.out, rows)[:, jcols], full["out"], "out e2e")
+    zg, zu = z32[:, :F], z32[:, F:]
+    assert_elem(rows_of(b.out, rows), out_ref, "out", cublas=(zg * torch.sigmoid(zg) * zu).to(bf))
+    del z32, zg, zu
+    # end to end on the sampled rows
+    full = O.block_forward(rows_of(b.X, rows), W1t, rows_of(b.R, rows), g, W2t, shape.eps, True)
+    assert_frob(rows_of(b.out, rows), full["out"], "out e2e")
     assert_frob(H, full["h"], "H e2e")
+    del full, z_ref, out_ref
     if not backward:
         return
-    # a5 SwiGLU backward
-    dP_ref, c_ref = O.stage_swiglu_bwd(rows_of(b.dY, rows), rows_of(b.z, rows), rstd, d)
+    # a5 SwiGLU backward: dP on whole rows, c on every row
+    dP_ref, _ = O.stage_swiglu_bwd(rows_of(b.dY, rows), rows_of(b.z, rows), rstd, d)
     assert_elem(rows_of(b.dP, rows), dP_ref, "dP")
-    assert_elem(f64(b.c)[rows], c_ref, "c")
-    # a6 + a7 dgrad2 with the RMSNorm backward, dg
-    dh_ref, dg_ref = dgrad2_sampled(b, kcols, rows)
-    assert_elem(rows_of(b.dH, rows)[:, kcols], dh_ref, "dH")
-    assert_elem(f64(b.dg)[kcols], dg_ref, "dg")
-    # a8 wgrad2
-    dW2_ref = O.stage_wgrad2(cols_of(b.H, kcols), cols_of(b.dP, ncols), g[kcols])
-    e_ours = assert_elem(rows_of(b.dW2t, ncols)[:, kcols], dW2_ref, "dW2t")
-    ni, ki = torch.as_tensor(ncols, device="cuda"), torch.as_tensor(kcols, device="cuda")
-    cub = torch.matmul(b.dP[:, ni].t(), b.H[:, ki]).float() * b.g[ki].float()
-    assert e_ours <= 1.25 * elem_err(cub, dW2_ref) + 1e-3
-    # a9 dgrad1, a10 wgrad1; dgrad1 also against cuBLAS (bf16 in, fp32
-    # accumulate, bf16 out) on the same inputs: no worse than it
+    rstd_all = f64(b.rstd)
+    c_ref = np.concatenate([O.stage_swiglu_bwd(f64(b.dY[s:e]), f64(b.z[s:e]), rstd_all[s:e], d)[1]
+                            for s, e in row_blocks(M)])
+    assert_elem(b.c, c_ref, "c")
+    # a6 + a7 dgrad2 with the RMSNorm backward: dH on every row, all of dg
+    c_all = f64(b.c)
+    dg_ref = np.zeros(d)
+    gf = b.g.float()
+    dg_cub = np.zeros(d)
+    parts = []
+    for s, e in row_blocks(M):
+        dh, part = O.stage_dgrad2_rmsbwd(f64(b.dP[s:e]), W2t, g, Hall[s:e], c_all[s:e])
+        dg_ref += part
+        acc = mm_f32(b.dP[s:e], b.W2t)
+        cub = (gf * acc - b.c[s:e, None] * b.H[s:e].float()).to(bf)
+        dg_cub += f64((acc * b.H[s:e].float()).sum(0))
+        parts.append((b.dH[s:e], dh, cub))
+        del acc
+    assert_elem_chunks(parts, "dH")
+    del parts
+    assert_elem(b.dg, dg_ref, "dg", cublas=dg_cub)
+    # a8 wgrad2: whole columns (fixed k) and whole rows (fixed n) of dW2t
+    dP_all = f64(b.dP)
+    cub = (mm_f32(b.dP.t(), b.H[:, ki]) * gf[ki]).to(bf)
+    assert_elem(cols_of(b.dW2t, kcols), O.stage_wgrad2(Hall[:, kcols], dP_all, g[kcols]), "dW2t columns",
+                cublas=cub)
+    cub = (mm_f32(b.dP[:, ni].t(), b.H) * gf).to(bf)
+    assert_elem(rows_of(b.dW2t, ncols), O.stage_wgrad2(Hall, dP_all[:, ncols], g), "dW2t rows", cublas=cub)
+    del dP_all, cub
+    # a9 dgrad1 (whole rows)
     dX_ref = O.stage_dgrad1(rows_of(b.dH, rows), W1t)
-    e_ours = assert_elem(rows_of(b.dX, rows), dX_ref, "dX")
-    ri = torch.as_tensor(rows, device="cuda")
-    e_cublas = elem_err(torch.matmul(b.dH[ri], b.W1t), dX_ref)
-    assert e_ours <= 1.25 * e_cublas + 1e-3, (e_ours, e_cublas)
-    icols = sample(shape.K1, 16, 4)
-    assert_elem(rows_of(b.dW1t, kcols)[:, icols], O.stage_wgrad1(cols_of(b.dH, kcols), cols_of(b.X, icols)),
-                "dW1t")
+    assert_elem(rows_of(b.dX, rows), dX_ref, "dX", cublas=torch.matmul(b.dH[ri], b.W1t))
+    # a10 wgrad1: whole rows (fixed k) and whole columns (fixed i) of dW1t
+    dH_all = f64(b.dH)
+    X_all = f64(b.X)
+    assert_elem(rows_of(b.dW1t, kcols), O.stage_wgrad1(dH_all[:, kcols], X_all), "dW1t rows",
+                cublas=torch.matmul(b.dH[:, ki].t(), b.X))
+    assert_elem(cols_of(b.dW1t, icols), O.stage_wgrad1(dH_all, X_all[:, icols]), "dW1t columns",
+                cublas=torch.matmul(b.dH.t(), b.X[:, ii]))
+    del dH_all, X_all
     # the composite backward reproduces the stage calls exactly
     ref = {k: getattr(b, k).clone() for k in ("dH", "dW2t", "dg", "dX", "dW1t")}
     b.backward()
@@ -130,40 +178,69 @@ def test_70b_forward_backward_full_size():
 
 
 def test_lmhead_ce_full_size():
+    """Every row's label logit; lse, argmax, row loss and the label's column
+    on at least 256 whole rows (all 128256 logits each), with labels placed
+    on the 128- and 256-column tile edges, the backward chunk edges and the
+    last vocabulary columns; dH and dW by Frobenius."""
     s = LMHEAD
     x = ce_inputs(s, 0, "cuda")
     M, d, V = s.M, s.d, s.V
+    rows = edge_sample(M, 256, 5)
+    edges = edge_labels(V)
+    assert len(edges) <= len(rows)
+    labels = x["labels"].clone()
+    labels[torch.as_tensor(rows[:len(edges)], device="cuda")] = torch.tensor(edges, dtype=labels.dtype,
+                                                                             device="cuda")
     ws = torch.empty(C.coda_lmhead_ce_workspace_bytes(M, d, V, True), dtype=torch.uint8, device="cuda")
     loss = torch.empty(1, device="cuda")
     lse = torch.empty(M, device="cuda")
     am = torch.empty(M, dtype=torch.int32, device="cuda")
     dH = torch.empty(M, d, dtype=torch.bfloat16, device="cuda")
     dW = torch.empty(V, d, dtype=torch.bfloat16, device="cuda")
-    C.coda_lmhead_ce(x["H"], x["Wt"], x["labels"], loss, lse, am, dH, dW, ws)
+    C.coda_lmhead_ce(x["H"], x["Wt"], labels, loss, lse, am, dH, dW, ws)
     assert_device_ok()
-    rows = sample(M, 12, 5)
-    y = x["labels"].cpu().numpy().astype(np.int64)
-    Hs = rows_of(x["H"], rows)
-    Wt = f64(x["Wt"])
+    zy_gpu, row_loss_gpu = C.coda_lmhead_ce_row_results(ws, M, d, V, True)
+    y = labels.cpu().numpy().astype(np.int64)
     Hall = f64(x["H"])
-    fw = O.ce_forward(Hs, Wt, y[rows])
-    assert_elem(f64(lse)[rows], fw["lse"], "lse", tol=1e-4)
-    # argmax on the sampled rows (ties within the fp32 error may go either way)
+    Wt = f64(x["Wt"])
+    # the label logit of every row: L[m, y_m] = H[m] . W[y_m]
+    zy_ref = np.einsum("md,md->m", Hall, Wt[y])
+    assert_elem(zy_gpu, zy_ref, "label logit (all rows)")
+    # whole rows of logits on the sample: lse, argmax, row loss, label column
+    Hs = Hall[rows]
     L = O.logits_rows(Hs, Wt)
-    srt = np.sort(L, axis=1)
-    decided = srt[:, -1] - srt[:, -2] > 1e-3
-    got = am.cpu().numpy()[rows]
-    assert np.array_equal(got[decided], O.argmax_lowest(L)[decided])
-    # mean loss = mean(lse - L[y]); the label logits for every row from the oracle
-    zy = np.einsum("md,md->m", Hall, Wt[y])
-    assert abs(loss.item() - float(np.mean(f64(lse) - zy))) <= 1e-4 * abs(loss.item())
+    lse_ref = O.lse_rows(L)
+    assert_elem(f64(lse)[rows], lse_ref, "lse", tol=1e-4)
+    assert check_argmax(am.cpu()[rows], Hs, Wt, L=L) >= len(rows) - 4
+    check_label_rows(zy_gpu, row_loss_gpu, L, y[rows], lse_ref, rows=rows)
+    # mean loss = mean(lse - L[y]) over every row
+    assert abs(loss.item() - float(np.mean(f64(lse) - zy_ref))) <= 1e-4 * abs(loss.item())
     # dH on sampled rows: the oracle's per-row gradient rescaled from 1/len(rows) to 1/M
     bw = O.ce_backward(Hs, Wt, y[rows])
     assert_frob(rows_of(dH, rows), bw["dH"] * (len(rows) / M), "dH")
-    # dW on sampled vocabulary rows (including some labels) given the GPU's lse
-    vcols = np.unique(np.concatenate([sample(V, 24, 6), y[rows[:6]]]))
+    # dW on sampled vocabulary rows (the edge labels among them) given the GPU's lse
+    vcols = np.unique(np.concatenate([edge_sample(V, 48, 6), np.asarray(edges)]))
     dW_ref = O.ce_weight_grad_given_lse(Hall, Wt[vcols], vcols, y, f64(lse), M)
     assert_frob(rows_of(dW, vcols), dW_ref, "dW")
+
+
+def test_lmhead_ce_known_answer_full_size():
+    """Label logit and argmax bit-exact on all 8192 rows at the full
+    vocabulary (integer logits +-pi(v), see tests/_ce.py), labels on every
+    tile and chunk edge."""
+    s = LMHEAD
+    H, Wt, lab, zy_ref, am_ref = known_answer_ce(s.M, s.d, s.V, seed=7)
+    Hd, Wd, ld = H.cuda(), Wt.cuda(), lab.cuda()
+    del H, Wt
+    ws = torch.empty(C.coda_lmhead_ce_workspace_bytes(s.M, s.d, s.V, False), dtype=torch.uint8, device="cuda")
+    loss = torch.empty(1, device="cuda")
+    lse = torch.empty(s.M, device="cuda")
+    am = torch.empty(s.M, dtype=torch.int32, device="cuda")
+    C.coda_lmhead_ce(Hd, Wd, ld, loss, lse, am, None, None, ws)
+    assert_device_ok()
+    zy_gpu, _ = C.coda_lmhead_ce_row_results(ws, s.M, s.d, s.V, False)
+    assert np.array_equal(f64(zy_gpu), zy_ref)
+    assert np.array_equal(am.cpu().numpy().astype(np.int64), am_ref)
 
 
 def test_7b_block_executor_full_size():

@@ -1,4 +1,4 @@
-"""The "next" rows built on the hot path, against the fp64 oracle:
+"""Further epilogue programs on the block's path, against the fp64 oracle:
 
 * the SwiGLU backward in the epilogue of the down projection's data-gradient
   GEMM (dY stays on chip; c is formed from per-tile partial sums inside the
