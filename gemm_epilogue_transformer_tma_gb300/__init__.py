@@ -54,7 +54,11 @@ SIGNATURES = {
     "coda_set_wait_timeout_ns": (_INT, [_P, _U64]),
     "coda_debug_skip_first_stage": (_INT, [_P, _INT]),
     "coda_debug_group_schedule_violations": (_INT, [_INT, _INT, _INT, _INT, _INT]),
+    "coda_debug_split_schedule_violations": (_INT, [_INT, _INT, _INT]),
+    "coda_debug_split_first_tile": (_INT, [_INT, _INT, _INT]),
     "coda_set_sm_pairing": (_INT, [_P, _INT]),
+    "coda_split_workspace_bytes": (_SZ, [_P]),
+    "coda_set_split_workspace": (_INT, [_P, _P, _SZ, _P]),
     "coda_prms_num_tiles": (_I64, [_I64]),
     "coda_dgpart_rows": (_I64, [_I64]),
     "coda_gemm": (_INT, [_P, _P, _INT, _P, _INT, _P, _I64, _I64, _I64, _P, _P, _P]),
@@ -200,8 +204,26 @@ def coda_set_sm_pairing(enable: bool, device: int | None = None):
     _check(load_library().coda_set_sm_pairing(handle(device), int(enable)), "coda_set_sm_pairing")
 
 
+def coda_split_workspace_bytes(device: int | None = None) -> int:
+    """Bytes of the split-tile scratch coda_set_split_workspace takes."""
+    return load_library().coda_split_workspace_bytes(handle(device))
+
+
+def coda_set_split_workspace(ws, device: int | None = None, stream=None):
+    """Give the device's handle a split-tile scratch (a uint8 CUDA tensor of at
+    least coda_split_workspace_bytes()), or None to stop splitting tiles.
+    The caller keeps ws alive while it is set (see include/coda.h)."""
+    if ws is None:
+        _check(load_library().coda_set_split_workspace(handle(device), None, 0, _stream(stream)),
+               "coda_set_split_workspace")
+        return
+    _check(load_library().coda_set_split_workspace(handle(device), _ptr(ws, torch.uint8, "ws"),
+                                                   ws.numel() * ws.element_size(), _stream(stream)),
+           "coda_set_split_workspace")
+
+
 def coda_debug_skip_first_stage(enable: bool, device: int | None = None):
-    """Failure-detection test hook (see include/coda.h)."""
+    """Failure-detection test hook (see include/coda_testing.h)."""
     _check(load_library().coda_debug_skip_first_stage(handle(device), int(enable)), "coda_debug_skip_first_stage")
 
 
@@ -403,8 +425,18 @@ def coda_gemm_wgrad_gscale(H, dP, g, dW2t, stream=None):
 
 
 def coda_debug_group_schedule_violations(P: int, heavy: int, nH: int, nL: int, q: int) -> int:
-    """Host check of the grouped launches' tile schedule (see include/coda.h)."""
+    """Host check of the grouped launches' tile schedule (see include/coda_testing.h)."""
     return load_library().coda_debug_group_schedule_violations(P, heavy, nH, nL, q)
+
+
+def coda_debug_split_schedule_violations(tiles: int, num_kb: int, clusters: int) -> int:
+    """Host check of the split-tile schedule (see include/coda_testing.h)."""
+    return load_library().coda_debug_split_schedule_violations(tiles, num_kb, clusters)
+
+
+def coda_debug_split_first_tile(tiles: int, num_kb: int, clusters: int) -> int:
+    """First split tile the launcher would choose, tiles if none (see include/coda_testing.h)."""
+    return load_library().coda_debug_split_first_tile(tiles, num_kb, clusters)
 
 
 def coda_bwd_workspace_bytes(M: int, d: int, N2: int) -> int:

@@ -23,6 +23,8 @@ struct coda_handle_s {
   int skip_first_stage;  // test hook for the bounded waits (coda_debug_skip_first_stage)
   int pair;              // GEMMs on SM pairs (coda_set_sm_pairing)
   void* noalloc_scratch;  // device address of the allocation-free call's scratch, looked up on its first use
+  float* sk_parts;        // split-tile scratch (coda_set_split_workspace), or null
+  int* sk_flags;
 };
 
 namespace coda {
@@ -56,8 +58,16 @@ LaunchCtx ctx_of(coda_handle_t h, void* stream) {
   c.scale_b = nullptr;
   c.f8_fmt = 0;
   c.scale_host = 1.f;
+  c.sk_parts = h->sk_parts;
+  c.sk_flags = h->sk_flags;
+  c.sk_slots = h->num_sms / 2;
   return c;
 }
+
+// Split-tile scratch: one 256 x 256 fp32 partial per SM pair, then one flag
+// per (pair, CTA of the pair, epilogue warp).
+size_t split_parts_bytes(int num_sms) { return size_t(num_sms / 2) * 256 * 256 * sizeof(float); }
+size_t split_flags_bytes(int num_sms) { return size_t(num_sms / 2) * 2 * 8 * sizeof(int); }
 
 coda_status_t from_cuda(cudaError_t e) {
   if (e == cudaSuccess) return CODA_OK;
@@ -210,6 +220,8 @@ coda_status_t coda_create(coda_handle_t* out, int device) {
   h->pair = 1;
   h->status = nullptr;
   h->noalloc_scratch = nullptr;
+  h->sk_parts = nullptr;
+  h->sk_flags = nullptr;
   coda_status_t st = CODA_OK;
   if (cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
       cudaMalloc(&h->status, sizeof(int)) != cudaSuccess || cudaMemset(h->status, 0, sizeof(int)) != cudaSuccess)
@@ -269,6 +281,34 @@ coda_status_t coda_set_wait_timeout_ns(coda_handle_t h, uint64_t ns) {
 coda_status_t coda_set_sm_pairing(coda_handle_t h, int enable) {
   CODA_TRY(Check().handle(h).st);
   h->pair = enable != 0;
+  return CODA_OK;
+}
+
+size_t coda_split_workspace_bytes(coda_handle_t h) {
+  if (h == nullptr) return 0;
+  return split_parts_bytes(h->num_sms) + split_flags_bytes(h->num_sms);
+}
+
+coda_status_t coda_set_split_workspace(coda_handle_t h, void* ws, size_t ws_bytes, void* stream) {
+  if (h == nullptr) return CODA_ERR_INVALID_ARG;
+  if (ws == nullptr) {
+    h->sk_parts = nullptr;
+    h->sk_flags = nullptr;
+    return CODA_OK;
+  }
+  if (reinterpret_cast<uintptr_t>(ws) % 256 != 0) return CODA_ERR_ALIGNMENT;
+  if (ws_bytes < coda_split_workspace_bytes(h)) return CODA_ERR_WORKSPACE_TOO_SMALL;
+  float* parts = static_cast<float*>(ws);
+  int* flags = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + split_parts_bytes(h->num_sms));
+  int prev = 0;
+  if (cudaGetDevice(&prev) != cudaSuccess) return CODA_ERR_CUDA;
+  if (prev != h->device && cudaSetDevice(h->device) != cudaSuccess) return CODA_ERR_CUDA;
+  const cudaError_t e =
+      cudaMemsetAsync(flags, 0, split_flags_bytes(h->num_sms), static_cast<cudaStream_t>(stream));
+  if (prev != h->device) cudaSetDevice(prev);
+  if (e != cudaSuccess) return CODA_ERR_CUDA;
+  h->sk_parts = parts;
+  h->sk_flags = flags;
   return CODA_OK;
 }
 

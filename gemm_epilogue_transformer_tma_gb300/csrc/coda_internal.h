@@ -21,6 +21,9 @@ struct LaunchCtx {
   const float* scale_b;
   uint32_t f8_fmt;       // FP8 operands: format bits of A and B (f8_format_bits; 0 = both e4m3)
   float scale_host;      // FP8 operands: a further accumulator scale known on the host (1 otherwise)
+  float* sk_parts;       // split-tile scratch (coda_set_split_workspace), or null: no tile is split
+  int* sk_flags;
+  int sk_slots;          // clusters the scratch has slots for
 };
 
 // 2-D bf16 tensor map with 128-byte swizzle.  The tensor is `outer` rows of

@@ -1,5 +1,7 @@
 // Forward GEMM instantiations: GEMM1 with the residual + partial-RMS epilogue,
 // GEMM2 with the deferred row scale + SwiGLU epilogue, and the plain GEMM.
+#include <vector>
+
 #include "gemm_launch.cuh"
 
 namespace coda {
@@ -94,3 +96,66 @@ cudaError_t gemm_store_f32(const LaunchCtx& c, const __nv_bfloat16* A, bool a_mn
 }
 
 }  // namespace coda
+
+// Host-side check of the split-tile schedule of the SM-pair kernel, run with
+// the kernel's own iterator (coda_debug_split_schedule_violations in
+// include/coda_testing.h).
+extern "C" int coda_debug_split_schedule_violations(int tiles, int num_kb, int clusters) {
+  using namespace coda;
+  if (tiles < 1 || num_kb < 1 || clusters < 1) return -1;
+  GemmShape sh{};
+  sh.tiles_m = tiles;
+  sh.tiles_n = 1;
+  sh.num_kb = num_kb;
+  sh.sk_first = split_first_tile(tiles, num_kb, clusters, clusters);
+  if (sh.sk_first == tiles) return 0;  // not split: nothing to check
+  std::vector<int> cover(static_cast<size_t>(tiles) * num_kb, 0);
+  int bad = 0;
+  for (int cid = 0; cid < clusters; ++cid) {
+    SplitWork wk(sh, cid, clusters);
+    TilePiece pc;
+    int n_split = 0, n_partial = 0, n_owner = 0, last_owner = -1, first_partial = -1;
+    while (wk.next(pc)) {
+      for (int k = pc.kb0; k < pc.kb1; ++k) cover[static_cast<size_t>(pc.tile) * num_kb + k]++;
+      if (pc.tile < sh.sk_first) continue;
+      if (pc.partial) {
+        ++n_partial;
+        if (n_split != 0) ++bad;  // a partial piece is always the first of the range
+        first_partial = pc.tile;
+      }
+      if (pc.owner) {
+        ++n_owner;
+        last_owner = n_split;
+        // the clusters whose ranges start inside the tile hold k-blocks
+        // [pc.kb1, num_kb): each one's first piece is a partial there, and
+        // together they cover the rest of the tile without a gap
+        const int64_t tile_end = (static_cast<int64_t>(pc.tile) + 1) * num_kb;
+        int pos = pc.kb1, n_contrib = 0;
+        for (int q = cid + 1; q < clusters && wk.start_of(q) < tile_end; ++q) {
+          SplitWork wq(sh, q, clusters);
+          TilePiece f;
+          while (wq.next(f) && f.tile < sh.sk_first) {
+          }
+          if (f.tile != pc.tile || !f.partial || f.kb0 != pos) ++bad;
+          pos = f.kb1;
+          ++n_contrib;
+        }
+        if (pos != num_kb || n_contrib > kMaxSplitParts) ++bad;
+      }
+      ++n_split;
+    }
+    (void)first_partial;
+    if (n_split == 0 || n_partial > 1 || n_owner > 1) ++bad;
+    if (n_owner == 1 && last_owner != n_split - 1) ++bad;  // the owner piece ends the range
+  }
+  for (int v : cover)
+    if (v != 1) ++bad;
+  return bad;
+}
+
+// First tile of the split region the SM-pair launcher would choose
+// (coda_debug_split_first_tile in include/coda_testing.h).
+extern "C" int coda_debug_split_first_tile(int tiles, int num_kb, int clusters) {
+  if (tiles < 1 || num_kb < 1 || clusters < 1) return -1;
+  return coda::split_first_tile(tiles, num_kb, clusters, clusters);
+}

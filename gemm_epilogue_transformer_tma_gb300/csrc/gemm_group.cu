@@ -23,6 +23,7 @@ GemmShape pair_shape(int M, int N, int K, bool fp8 = false) {
   sh.tiles_n = (N + 255) / 256;
   sh.num_kb = (K + bke - 1) / bke;
   sh.group_m = 8;
+  sh.sk_first = sh.tiles_m * sh.tiles_n;  // grouped launches never split tiles
   return sh;
 }
 

@@ -338,6 +338,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi0>()
       c.acc_scale = acc_scale[prob];
       c.taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN);
       c.stage = stage_base;
+      c.nsplit = 0;
 #pragma unroll 1
       for (int hh = 0; hh < HALVES; ++hh) {
         const int half = first_half + hh;

@@ -28,8 +28,25 @@ cudaError_t launch_gemm_kernel(const LaunchCtx& c, const CUtensorMap& ta, const 
   sh.group_m = 8;
   KernelCtl ctl{c.status, c.timeout_ns, c.skip_first_stage, c.scale_a, c.scale_b, c.f8_fmt, c.scale_host};
   const int tiles = sh.tiles_m * sh.tiles_n;
+  sh.sk_first = tiles;  // the 1-SM kernel never splits tiles
   const int grid = std::max(1, std::min(tiles, c.num_sms));
   return launch_chained(c, kern, dim3(grid), dim3(gemm_threads<Epi>()), L::TOTAL, ta, tb, tb2, sh, ctl, ep);
+}
+
+// First tile of the split region of an SM-pair launch (stream-K over the
+// last partial wave and the full wave before it), or `tiles` for no split.
+// Split only when the scratch has a slot for every cluster, the last wave is
+// partial, a tile has at least kSplitMinKb k-blocks, and every split tile has
+// at most kMaxSplitParts contributing clusters besides its owner.
+constexpr int kSplitMinKb = 16;
+inline int split_first_tile(int tiles, int num_kb, int clusters, int slots) {
+  if (slots < clusters || clusters < 2 || num_kb < kSplitMinKb || tiles % clusters == 0) return tiles;
+  const int full = tiles / clusters;
+  const int first = full >= 1 ? (full - 1) * clusters : 0;
+  const int64_t per = static_cast<int64_t>(tiles - first) * num_kb / clusters;  // k-blocks per cluster (floor)
+  // starts of other clusters strictly inside one tile: at most ceil((num_kb - 1) / per)
+  if (per < 1 || (num_kb - 1 + per - 1) / per > kMaxSplitParts) return tiles;
+  return first;
 }
 
 template <int BN, int STAGES, bool A_MN, bool B_MN, bool B_DUAL, class Epi, bool FP8 = false>
@@ -73,7 +90,16 @@ cudaError_t launch_gemm2_kernel(const LaunchCtx& c, const CUtensorMap& ta, const
     max_pairs[dev] = std::max(1, std::min(n, c.num_sms / 2));
   }
   const int tiles = sh.tiles_m * sh.tiles_n;
-  const int clusters = std::max(1, std::min(tiles, max_pairs[dev]));
+  int clusters = std::max(1, std::min(tiles, max_pairs[dev]));
+  // the partials are written per TMEM lane quadrant by one warp each: split
+  // tiles only under 4-warp epilogue programs
+  const int slots = (c.sk_parts != nullptr && c.sk_flags != nullptr && Epi::kEpiWarps == 4) ? c.sk_slots : 0;
+  sh.sk_first = split_first_tile(tiles, sh.num_kb, max_pairs[dev], slots);
+  if (sh.sk_first < tiles) {
+    clusters = max_pairs[dev];
+    ctl.sk_parts = c.sk_parts;
+    ctl.sk_flags = c.sk_flags;
+  }
   return launch_chained(c, kern, dim3(2 * clusters), dim3(gemm_threads<Epi>()), L::TOTAL, ta, tb, tb2, sh, ctl, ep);
 }
 

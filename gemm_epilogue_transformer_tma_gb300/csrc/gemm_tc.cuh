@@ -56,12 +56,16 @@ constexpr int UMMA_K = 16;
 template <class Epi>
 constexpr int gemm_threads() { return 64 + 32 * Epi::kEpiWarps; }
 constexpr int PART_COLS = 128;     // columns per block-reduction partial (half a tile)
+constexpr int kMaxSplitParts = 3;  // other clusters' K ranges a split tile may have
 
 struct GemmShape {
   int M, N, K;        // logical problem (N = output columns the epilogue sees)
   int tiles_m, tiles_n;
   int num_kb;
   int group_m;        // tile raster: groups of group_m M-tiles sweep all N-tiles
+  // SM-pair kernel only: tiles [sk_first, tiles) are split along K across
+  // clusters (stream-K); sk_first = tiles_m * tiles_n means no split
+  int sk_first;
 };
 
 struct KernelCtl {
@@ -72,6 +76,11 @@ struct KernelCtl {
   const float* scale_b;
   uint32_t f8_fmt;       // FP8 operands: format bits of A and B (f8_format_bits)
   float scale_host;      // FP8 operands: a scale known on the host (1 otherwise)
+  // split tiles (SM-pair kernel): one partial-accumulator slot per cluster
+  // ([cluster][rank][quad][32 rows x 256 columns] fp32) and one flag per
+  // (cluster, rank, epilogue warp); null when tiles are not split
+  float* sk_parts;
+  int* sk_flags;
 };
 
 // The accumulator's scale: the product of the operands' per-tensor scales
@@ -97,7 +106,38 @@ struct EpiCtx {
   uint32_t taddr;     // TMEM address of (first lane of quadrant, column 0 of this accumulator)
   int m0;             // global row of this warp's lane 0 (the warp stores rows m0 .. m0 + 31)
   uint32_t stage;     // shared address of this warp's store-staging slots
+  // a split tile: fp32 partial accumulators of the tile's other K ranges,
+  // added to the TMEM accumulator as it is read (acc_ld32)
+  int nsplit;
+  const float* split[kMaxSplitParts];
 };
+
+// Layout of one warp's partial accumulator: 32 rows x 256 columns, stored as
+// [column / 4][row][4] so that a warp's 32 lanes (rows) touch 512 contiguous
+// bytes per 4-column group.
+__device__ __forceinline__ int split_part_f4_index(int col, int lane) { return (col >> 2) * 32 + lane; }
+constexpr int SPLIT_PART_FLOATS = 32 * 256;  // per (cluster, rank, quad)
+
+// 32 accumulator columns from `col` for this thread's row: TMEM, plus the
+// partial sums of a split tile's other K ranges.
+__device__ __forceinline__ void acc_ld32(const EpiCtx& c, int col, float (&v)[32]) {
+  tmem_ld32(c.taddr + static_cast<uint32_t>(col), v);
+  if (c.nsplit == 0) return;
+#pragma unroll
+  for (int q = 0; q < kMaxSplitParts; ++q) {
+    if (q < c.nsplit) {
+      const float4* src = reinterpret_cast<const float4*>(c.split[q]) + split_part_f4_index(col, c.lane);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float4 x = ld_cg_f4(src + j * 32);
+        v[4 * j] += x.x;
+        v[4 * j + 1] += x.y;
+        v[4 * j + 2] += x.z;
+        v[4 * j + 3] += x.w;
+      }
+    }
+  }
+}
 
 // An epilogue program may declare
 //   static void prefetch(const Params&, int M, int N, int m, int n0, int bn);
@@ -357,6 +397,7 @@ __global__ void __launch_bounds__(gemm_threads<Epi>(), 1)
       c.acc_scale = acc_scale;
       c.taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN);
       c.stage = stage_base;
+      c.nsplit = 0;
 #pragma unroll 1
       for (int hh = 0; hh < HALVES; ++hh) {
         const int half = first_half + hh;
@@ -546,7 +587,7 @@ struct EpiStore {
 #pragma unroll 1
     for (int cc = c.c0; cc < c.c1; cc += 32) {
       float v[32];
-      tmem_ld32(c.taddr + cc, v);
+      acc_ld32(c, cc, v);
       const int n0 = c.tn * BN + cc;
       if (n0 < c.N && c.m0 < c.M) {
         if (p.col_scale != nullptr) {
@@ -584,7 +625,7 @@ struct EpiStoreF32 {
 #pragma unroll 1
     for (int cc = c.c0; cc < c.c1; cc += 32) {
       float v[32];
-      tmem_ld32(c.taddr + cc, v);
+      acc_ld32(c, cc, v);
       const int n0 = c.tn * BN + cc;
       if (n0 < c.N && c.m0 < c.M) {
 #pragma unroll
@@ -647,7 +688,7 @@ struct EpiResPrms {
 #pragma unroll 1
     for (int cc = c.c0; cc < c.c1; cc += 32) {
       float v[32];
-      tmem_ld32(c.taddr + cc, v);
+      acc_ld32(c, cc, v);
       const int n0 = nb + cc;
       float r[32];
 #pragma unroll
@@ -716,8 +757,8 @@ struct EpiRowscaleSwiglu {
 #pragma unroll 1
     for (int cc = c.c0 / 2; cc < c.c1 / 2; cc += 32) {
       float g[32], u[32];
-      tmem_ld32(c.taddr + cc, g);
-      tmem_ld32(c.taddr + HB + cc, u);
+      acc_ld32(c, cc, g);
+      acc_ld32(c, HB + cc, u);
       const int j0 = c.tn * HB + cc;
       if (j0 < p.F && c.m0 < c.M) {
 #pragma unroll
@@ -786,7 +827,7 @@ struct EpiDgradRms {
 #pragma unroll 1
     for (int cc = c.c0; cc < c.c1; cc += 32) {
       float a[32];
-      tmem_ld32(c.taddr + cc, a);
+      acc_ld32(c, cc, a);
       const int n0 = c.tn * BN + cc;
       if (n0 < c.N) {
         // FP8 operands: dequantise the accumulator (acc_scale = 1 for bf16)
@@ -849,7 +890,7 @@ struct EpiSwigluBwd {
 #pragma unroll 1
     for (int cc = c.c0; cc < c.c1; cc += 32) {
       float dy[32];
-      tmem_ld32(c.taddr + cc, dy);
+      acc_ld32(c, cc, dy);
       const int j0 = c.tn * BN + cc;
       if (j0 < p.F && c.m0 < c.M) {
         const int nv = row_ok ? p.F - j0 : 0;
@@ -906,8 +947,8 @@ struct EpiRope {
 #pragma unroll 1
     for (int cc = 0; cc < 64; cc += 32) {
       float x1[32], x2[32];
-      tmem_ld32(c.taddr + c.c0 + cc, x1);
-      tmem_ld32(c.taddr + c.c0 + 64 + cc, x2);
+      acc_ld32(c, c.c0 + cc, x1);
+      acc_ld32(c, c.c0 + 64 + cc, x2);
       if (c.m0 >= c.M) continue;
       if (rot) {
         const float4* cs4 = reinterpret_cast<const float4*>(p.cos_t + tab + cc);
@@ -967,7 +1008,7 @@ struct EpiCeStats {
 #pragma unroll 1
     for (int cc = c.c0; cc < c.c1; cc += 32) {
       float v[32];
-      tmem_ld32(c.taddr + cc, v);
+      acc_ld32(c, cc, v);
       const int n0 = c.tn * BN + cc;
       if (row_ok && n0 < c.N) {
         // one thread owns the row, so the chunk is reduced in registers: with
@@ -1048,7 +1089,7 @@ struct EpiCeGrad {
 #pragma unroll 1
     for (int cc = c.c0; cc < c.c1; cc += 32) {
       float v[32];
-      tmem_ld32(c.taddr + cc, v);
+      acc_ld32(c, cc, v);
       const int n0 = c.tn * BN + cc;
       if (n0 < c.N && c.m0 < c.M) {
 #pragma unroll

@@ -31,6 +31,72 @@ namespace coda {
 
 constexpr int BM2 = 256;  // output rows per CTA pair
 
+// Work of one cluster: whole tiles first (tiles cluster, cluster + P, ...
+// below sh.sk_first), then its share of the split region.  The split region
+// (tiles sk_first .. tiles - 1, the last partial wave and the full wave
+// before it) is a run of (tile, k-block) units dealt in P equal contiguous
+// ranges, one per cluster (stream-K).  A cluster's range may start inside a
+// tile: that first piece is a partial accumulator, which goes to the
+// cluster's scratch slot.  Every later piece of the range starts at k-block 0
+// of its tile and is that tile's owner: when it ends before the tile's last
+// k-block, the clusters whose ranges start inside the tile hold the rest, and
+// the owner's epilogue adds their partials before it runs.  Owners come last
+// in a range and partial pieces first, so no cluster ever waits on a cluster
+// that is waiting.  Producer, MMA issuer and epilogue walk the same sequence.
+struct TilePiece {
+  int tile, kb0, kb1;
+  bool partial;  // kb0 > 0: accumulator to the scratch slot, no epilogue program
+  bool owner;    // kb0 == 0 and kb1 < num_kb: other clusters hold the tile's remaining k-blocks
+};
+
+struct SplitWork {
+  int next_whole, first_split, P, nkb;
+  int64_t base, W, u, u_end;
+  __host__ __device__ SplitWork(const GemmShape& sh, int cluster, int num_clusters) {
+    next_whole = cluster;
+    first_split = sh.sk_first;
+    P = num_clusters;
+    nkb = sh.num_kb;
+    base = static_cast<int64_t>(sh.sk_first) * nkb;
+    W = static_cast<int64_t>(sh.tiles_m * sh.tiles_n - sh.sk_first) * nkb;
+    u = start_of(cluster);
+    u_end = start_of(cluster + 1);
+  }
+  // first (tile, k-block) unit of cluster q's split range
+  __host__ __device__ int64_t start_of(int q) const { return base + W * q / P; }
+  __host__ __device__ bool next(TilePiece& pc) {
+    if (next_whole < first_split) {
+      pc.tile = next_whole;
+      pc.kb0 = 0;
+      pc.kb1 = nkb;
+      pc.partial = pc.owner = false;
+      next_whole += P;
+      return true;
+    }
+    if (u >= u_end) return false;
+    pc.tile = static_cast<int>(u / nkb);
+    pc.kb0 = static_cast<int>(u - static_cast<int64_t>(pc.tile) * nkb);
+    const int64_t rest = pc.kb0 + (u_end - u);
+    pc.kb1 = static_cast<int>(rest < nkb ? rest : nkb);
+    pc.partial = pc.kb0 > 0;
+    pc.owner = pc.kb0 == 0 && pc.kb1 < nkb;
+    u += pc.kb1 - pc.kb0;
+    return true;
+  }
+};
+
+// Wait (bounded, like the mbarrier waits) for a split partial's flag.
+__device__ __forceinline__ bool split_flag_wait(const int* f, const volatile int* abort_flag, uint64_t timeout_ns) {
+  if (ld_acquire_gpu(f) != 0) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    __nanosleep(200);
+    if (ld_acquire_gpu(f) != 0) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > timeout_ns) return false;
+  }
+}
+
 template <int BN, int STAGES, int EPI_BYTES>
 struct Gemm2Smem {
   static constexpr int A_BYTES = 128 * BK * 2;        // this CTA's 128 rows of A
@@ -125,11 +191,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi>(),
       uint32_t pending = 0, parity = 0;  // leader: stages it armed
       bool ok = true;
       bool skip = ctl.skip_first_stage != 0 && cluster_id == 0 && leader;
-      for (int t = cluster_id; t < num_tiles && ok; t += num_clusters) {
+      SplitWork wk(sh, cluster_id, num_clusters);
+      TilePiece pc;
+      while (ok && wk.next(pc)) {
         int tm, tn;
-        tile_coords(t, sh, tm, tn);
+        tile_coords(pc.tile, sh, tm, tn);
         const int m0 = tm * BM2 + static_cast<int>(rank) * 128;  // this CTA's A rows
-        for (int kb = 0; kb < sh.num_kb; ++kb) {
+        for (int kb = pc.kb0; kb < pc.kb1; ++kb) {
           if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, ctl.timeout_ns)) {
             if (!*abort_flag) raise_error(ctl, abort_flag, DEV_ERR_TIMEOUT_PRODUCER);
             ok = false;
@@ -198,7 +266,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi>(),
         int it = 0;
         bool ok = true;
         bool issued_any = false;
-        for (int t = cluster_id; t < num_tiles && ok; t += num_clusters, ++it) {
+        SplitWork wk(sh, cluster_id, num_clusters);
+        TilePiece pc;
+        for (; ok && wk.next(pc); ++it) {
           const int acc = it & 1;
           const uint32_t acc_phase = (it >> 1) & 1;
           if (!mbar_wait_bounded_cluster(&tempty[acc], acc_phase ^ 1u, abort_flag, ctl.timeout_ns)) {
@@ -208,7 +278,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi>(),
           }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-          for (int kb = 0; kb < sh.num_kb; ++kb) {
+          for (int kb = pc.kb0; kb < pc.kb1; ++kb) {
             if (!mbar_wait_bounded_cluster(&full[stage], phase, abort_flag, ctl.timeout_ns)) {
               if (!*abort_flag) raise_error(ctl, abort_flag, DEV_ERR_TIMEOUT_MMA);
               ok = false;
@@ -223,10 +293,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi>(),
                   A_MN ? sdesc_sw128(sa + k * MN_KSTEP, MN_BOX, 1024) : sdesc_sw128(sa + k * 32, 16, 1024);
               const uint64_t bd =
                   B_MN ? sdesc_sw128(sb + k * MN_KSTEP, MN_BOX, 1024) : sdesc_sw128(sb + k * 32, 16, 1024);
+              const uint32_t accumulate = (kb != pc.kb0 || k != 0) ? 1u : 0u;
               if (FP8)
-                umma_e4m3_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                umma_e4m3_pair(d_tmem, ad, bd, idesc, accumulate);
               else
-                umma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                umma_bf16_pair(d_tmem, ad, bd, idesc, accumulate);
             }
             issued_any = true;
             umma_commit_pair_multicast(&empty[stage], 0x3);
@@ -254,15 +325,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi>(),
     const uint32_t leader_tempty = mapa_shared(smem_u32(tempty), 0);
     const uint32_t stage_base = smem_u32(smem + L::RING_BYTES) +
                                 static_cast<uint32_t>((warp - 2) * Epi::kStoreSlots * STORE_SLOT_BYTES);
+    const int ew = warp - 2;  // epilogue warp index: its split flag
     int it = 0;
-    for (int t = cluster_id; t < num_tiles; t += num_clusters, ++it) {
+    SplitWork wk(sh, cluster_id, num_clusters);
+    TilePiece pc;
+    for (; wk.next(pc); ++it) {
       int tm, tn;
-      tile_coords(t, sh, tm, tn);
+      tile_coords(pc.tile, sh, tm, tn);
       const int acc = it & 1;
       const uint32_t acc_phase = (it >> 1) & 1;
       if constexpr (EpiHasPrefetch<Epi>::value)
-        Epi::prefetch(ep, sh.M, sh.N, (tm * 2 + static_cast<int>(rank)) * 128 + row,
-                      tn * BN + first_half * (BN / 2), HALVES * (BN / 2));
+        if (!pc.partial)
+          Epi::prefetch(ep, sh.M, sh.N, (tm * 2 + static_cast<int>(rank)) * 128 + row,
+                        tn * BN + first_half * (BN / 2), HALVES * (BN / 2));
       bool ok = mbar_wait_bounded(&tfull[acc], acc_phase, abort_flag, ctl.timeout_ns);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) {
@@ -270,26 +345,83 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi>(),
         break;
       }
       tc_fence_after();
-      EpiCtx c;
-      c.M = sh.M;
-      c.N = sh.N;
-      c.tm = tm * 2 + static_cast<int>(rank);
-      c.tn = tn;
-      c.row = row;
-      c.m = c.tm * 128 + row;
-      c.m0 = c.tm * 128 + quad * 32;
-      c.quad = quad;
-      c.lane = lane;
-      c.acc_scale = acc_scale;
-      c.taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN);
-      c.stage = stage_base;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      if (pc.partial) {
+        // the first piece of this cluster's split range: the raw accumulator
+        // of this warp's rows to the cluster's slot, then its flag
+        float4* dst = reinterpret_cast<float4*>(
+            ctl.sk_parts + static_cast<int64_t>((cluster_id * 2 + static_cast<int>(rank)) * 4 + quad) *
+                               SPLIT_PART_FLOATS);
 #pragma unroll 1
-      for (int hh = 0; hh < HALVES; ++hh) {
-        const int half = first_half + hh;
-        c.c0 = half * (BN / 2);
-        c.c1 = c.c0 + BN / 2;
-        c.part = tn * 2 + half;
-        Epi::template run<BN>(ep, c);
+        for (int cc = first_half * (BN / 2); cc < (first_half + HALVES) * (BN / 2); cc += 32) {
+          float v[32];
+          tmem_ld32(taddr + static_cast<uint32_t>(cc), v);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            st_cg_f4(dst + split_part_f4_index(cc, lane) + j * 32,
+                     make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+        }
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) st_release_gpu(&ctl.sk_flags[(cluster_id * 2 + static_cast<int>(rank)) * 8 + ew], 1);
+      } else {
+        EpiCtx c;
+        c.M = sh.M;
+        c.N = sh.N;
+        c.tm = tm * 2 + static_cast<int>(rank);
+        c.tn = tn;
+        c.row = row;
+        c.m = c.tm * 128 + row;
+        c.m0 = c.tm * 128 + quad * 32;
+        c.quad = quad;
+        c.lane = lane;
+        c.acc_scale = acc_scale;
+        c.taddr = taddr;
+        c.stage = stage_base;
+        c.nsplit = 0;
+        int q_end = cluster_id + 1;  // contributors are clusters cluster_id + 1 .. q_end - 1
+        if (pc.owner) {
+          // the clusters whose split ranges start inside this tile hold its
+          // remaining k-blocks; wait for each one's partial of these rows
+          const int64_t tile_end = (static_cast<int64_t>(pc.tile) + 1) * wk.nkb;
+          while (q_end < num_clusters && wk.start_of(q_end) < tile_end) ++q_end;
+          bool got = q_end - cluster_id - 1 <= kMaxSplitParts;
+#pragma unroll
+          for (int j = 0; j < kMaxSplitParts; ++j) {
+            const int q = cluster_id + 1 + j;
+            if (got && q < q_end) {
+              const int* f = &ctl.sk_flags[(q * 2 + static_cast<int>(rank)) * 8 + ew];
+              bool seen = true;
+              if (lane == 0) seen = split_flag_wait(f, abort_flag, ctl.timeout_ns);
+              got = __shfl_sync(0xffffffffu, seen, 0);
+              if (got) {
+                (void)ld_acquire_gpu(f);  // every lane: its partial loads come after the flag
+                c.split[j] = ctl.sk_parts +
+                             static_cast<int64_t>((q * 2 + static_cast<int>(rank)) * 4 + quad) * SPLIT_PART_FLOATS;
+                c.nsplit = j + 1;
+              }
+            }
+          }
+          if (!got) {
+            if (lane == 0 && !*abort_flag) raise_error(ctl, abort_flag, DEV_ERR_TIMEOUT_EPILOGUE);
+            break;
+          }
+        }
+#pragma unroll 1
+        for (int hh = 0; hh < HALVES; ++hh) {
+          const int half = first_half + hh;
+          c.c0 = half * (BN / 2);
+          c.c1 = c.c0 + BN / 2;
+          c.part = tn * 2 + half;
+          Epi::template run<BN>(ep, c);
+        }
+        if (pc.owner) {
+          // every lane has read the partials: clear the flags for the next launch
+          __syncwarp();
+          if (lane == 0)
+            for (int q = cluster_id + 1; q < q_end; ++q)
+              st_relaxed_gpu(&ctl.sk_flags[(q * 2 + static_cast<int>(rank)) * 8 + ew], 0);
+        }
       }
       tc_fence_before();
       __syncwarp();

@@ -98,6 +98,33 @@ coda_status_t coda_set_wait_timeout_ns(coda_handle_t h, uint64_t ns);
  * inside the tensor core; the choice only affects speed. */
 coda_status_t coda_set_sm_pairing(coda_handle_t h, int enable);
 
+/* Scratch that lets this handle's SM-pair GEMMs keep every SM pair busy in
+ * their last, partial wave (stream-K).  Without it (the default) each SM pair
+ * computes whole 256 x 256 tiles, and when the tile count is not a multiple
+ * of the pairs the last wave leaves some pairs idle.  With it, the tiles of
+ * the last wave and of the full wave before it are dealt as one run of
+ * (tile, 64-deep k-block) units in equal contiguous shares to all pairs.  A
+ * tile whose k-blocks span two or more pairs is finished by the pair that
+ * holds its first k-block: the others leave fp32 partial accumulators in this
+ * scratch, and its epilogue adds them before running.  Only launches whose
+ * tiles have at least 16 k-blocks, and whose shares leave at most three other
+ * pairs per split tile, are split; grouped launches never are.  Results
+ * differ from unsplit runs only in the fp32 summation order of the split
+ * tiles, and a split launch is deterministic.
+ * coda_split_workspace_bytes: bytes needed (one 256 KB partial per SM pair
+ * plus flags).  coda_set_split_workspace: ws (256-byte aligned, at least that
+ * many bytes, caller-owned device memory) becomes the handle's scratch; its
+ * flags are cleared on `stream`, so set it in stream order before the GEMMs
+ * that use it; ws = NULL switches splitting off.  The library allocates
+ * nothing.  While it is set, GEMMs issued through the handle must not run
+ * concurrently with each other on the GPU (they share the scratch): issue
+ * them on one stream, or give each stream its own handle.  Keep ws alive until
+ * it is replaced and the GEMMs that used it have completed.  After a call
+ * reports CODA_ERR_TIMEOUT, set the workspace again before the next GEMM (the
+ * aborted launch may have left flags raised). */
+size_t coda_split_workspace_bytes(coda_handle_t h);
+coda_status_t coda_set_split_workspace(coda_handle_t h, void* ws, size_t ws_bytes, void* stream);
+
 /* Columns of a block-reduction partial buffer over n columns: ceil(n / 128).
  * Partial j of a row covers columns [128 j, 128 j + 128) (half of a 256-column
  * output tile).  Used for the partial RMS (n = d), the SwiGLU-backward c

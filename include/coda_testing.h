@@ -26,6 +26,22 @@ coda_status_t coda_debug_skip_first_stage(coda_handle_t h, int enable);
  * violations otherwise, -1 for invalid arguments.  Not for production use. */
 int coda_debug_group_schedule_violations(int P, int heavy, int nH, int nL, int q);
 
+/* Host-side check of the split-tile schedule (coda_set_split_workspace) of
+ * the SM-pair GEMM, run with the kernel's own work iterator (no GPU needed):
+ * `tiles` output tiles of `num_kb` k-blocks on `clusters` SM pairs.  Returns
+ * 0 when the launch would not split or when every (tile, k-block) is computed
+ * exactly once, each pair's range has at most one partial piece (its first)
+ * and one owner piece (its last), and each owner's contributors cover the
+ * rest of its tile contiguously, at most three of them; the number of
+ * violations otherwise, -1 for invalid arguments.  Not for production use. */
+int coda_debug_split_schedule_violations(int tiles, int num_kb, int clusters);
+
+/* The first tile of the split region that an SM-pair launch of `tiles` tiles
+ * of `num_kb` k-blocks on `clusters` pairs would use with a split workspace
+ * set (tiles when it would not split), -1 for invalid arguments.  Not for
+ * production use. */
+int coda_debug_split_first_tile(int tiles, int num_kb, int clusters);
+
 #ifdef __cplusplus
 }
 #endif

@@ -76,24 +76,29 @@ def check_row_loss(row_loss, lse_ref, zy_ref):
     assert not bad.any(), f"row loss off on {int(bad.sum())} rows, first {np.flatnonzero(bad)[:5]}"
 
 
-def known_answer_ce(M, d, V, seed):
+def known_answer_ce(M, d, V, seed, base=128):
     """Integer logits with a known label logit and argmax on every row.
 
-    A fixed permutation pi of [0, V) is written in base 128 into the first
-    three columns of W (digits <= 127, exact in bf16), and row m of H holds
-    a_m * (1, 128, 16384) there (a_m = +1 on even rows, -1 on odd ones;
-    powers of two, exact), zeros elsewhere.  Every logit is then the exact
-    integer L[m, v] = a_m pi(v) (|L| < 2^17, so any fp32 summation order is
-    exact): the label logit must be a_m pi(y_m) bit for bit, and the argmax
+    A fixed permutation pi of [0, V) is written in base `base` into the
+    first columns of W (one digit per column, digits < base exact in bf16 for
+    base 128, and in e4m3 for base 8 after its power-of-two scale), and row m
+    of H holds a_m * base^i there (a_m = +1 on even rows, -1 on odd ones;
+    powers of two), zeros elsewhere.  Every logit is then the exact integer
+    L[m, v] = a_m pi(v) (|L| < 2^18, so any fp32 summation order is exact):
+    the label logit must be a_m pi(y_m) bit for bit, and the argmax
     pi^-1(V - 1) on even rows, pi^-1(0) on odd ones, with no ties."""
-    assert V <= 128 * 128 * 128 and d >= 3
+    nd = 1
+    while base ** nd < V:
+        nd += 1
+    assert d >= nd and V <= 2 ** 18
     r = np.random.default_rng(seed)
     pi = r.permutation(V)
     W = np.zeros((V, d), np.float32)
-    W[:, 0], W[:, 1], W[:, 2] = pi % 128, (pi // 128) % 128, pi // 16384
     a = np.where(np.arange(M) % 2 == 0, 1.0, -1.0).astype(np.float32)
     H = np.zeros((M, d), np.float32)
-    H[:, 0], H[:, 1], H[:, 2] = a, 128 * a, 16384 * a
+    for i in range(nd):
+        W[:, i] = (pi // base ** i) % base
+        H[:, i] = a * float(base ** i)
     labels = r.integers(0, V, size=M)
     e = edge_labels(V)
     labels[:min(M, len(e))] = e[:min(M, len(e))]
@@ -103,3 +108,14 @@ def known_answer_ce(M, d, V, seed):
     bf = torch.bfloat16
     return (torch.from_numpy(H).to(bf), torch.from_numpy(W).to(bf), torch.from_numpy(labels.astype(np.int32)),
             zy, am)
+
+
+def known_answer_logits(Wt, M, base=128):
+    """The integer logits a_m pi(v) of known_answer_ce, read back from W's
+    digit columns."""
+    Wf = f64(Wt)
+    nd = 1
+    while base ** nd < Wf.shape[0]:
+        nd += 1
+    piv = sum(Wf[:, i] * base ** i for i in range(nd))
+    return np.where(np.arange(M) % 2 == 0, 1.0, -1.0)[:, None] * piv[None, :]

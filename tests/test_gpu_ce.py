@@ -14,7 +14,8 @@ import torch
 
 import oracle as O
 from coda_inputs import CEShape, ce_inputs
-from tests._ce import check_argmax, check_label_rows, check_row_loss, known_answer_ce, with_edge_labels
+from tests._ce import (check_argmax, check_label_rows, check_row_loss, known_answer_ce, known_answer_logits,
+                      with_edge_labels)
 from tests._parity import assert_device_ok, assert_elem, assert_frob, f64
 
 pytestmark = pytest.mark.gpu
@@ -143,8 +144,6 @@ def test_ce_label_logit_and_argmax_known_answer(M, d, V, pairing):
     assert np.array_equal(f64(o["zy"]), zy_ref)
     assert np.array_equal(o["argmax"].cpu().numpy().astype(np.int64), am_ref)
     # lse = max + log sum exp(L - max) of the integer logits; the row loss
-    piv = f64(Wt)[:, 0] + 128 * f64(Wt)[:, 1] + 16384 * f64(Wt)[:, 2]
-    L = np.where(np.arange(M) % 2 == 0, 1.0, -1.0)[:, None] * piv[None, :]
-    lse_ref = O.lse_rows(L)
+    lse_ref = O.lse_rows(known_answer_logits(Wt, M))
     assert_elem(o["lse"], lse_ref, "lse (integer logits)", tol=1e-5)
     check_row_loss(o["row_loss"], lse_ref, zy_ref)

@@ -20,6 +20,7 @@ import torch
 
 import oracle as O
 from coda_inputs import CEShape, ce_inputs
+from tests._ce import check_label_rows, check_row_loss, known_answer_ce, known_answer_logits, with_edge_labels
 from tests._parity import assert_device_ok, assert_elem, assert_frob, f64
 from tests.test_gpu_ce import check_argmax, pairing  # noqa: F401
 
@@ -48,6 +49,7 @@ def run_fp8_ce(Hq, sH, Wq, sW, labels, grads=True):
     o["dH"] = torch.empty(M, d, dtype=torch.bfloat16, device="cuda") if grads else None
     o["dW"] = torch.empty(V, d, dtype=torch.bfloat16, device="cuda") if grads else None
     C.coda_lmhead_ce_fp8(Hq, sH[1:], Wq, sW[1:], labels, o["loss"], o["lse"], o["argmax"], o["dH"], o["dW"], ws)
+    o["zy"], o["row_loss"] = C.coda_lmhead_ce_row_results(ws, M, d, V, grads)
     return o
 
 
@@ -55,6 +57,7 @@ def run_fp8_ce(Hq, sH, Wq, sW, labels, grads=True):
 def test_fp8_ce_parity(M, d, V, pairing):
     s = CEShape("t", M, d, V)
     x = {k: v.cuda() for k, v in ce_inputs(s, 0).items()}
+    x["labels"] = with_edge_labels(x["labels"], V)
     Hq, sH = quantize(x["H"])
     Wq, sW = quantize(x["Wt"])
     o = run_fp8_ce(Hq, sH, Wq, sW, x["labels"])
@@ -64,10 +67,11 @@ def test_fp8_ce_parity(M, d, V, pairing):
     fw = O.ce_forward(Hd, Wd, y)
     assert_elem(o["lse"], fw["lse"], "lse (fp8)", tol=1e-4)
     assert abs(o["loss"].item() - fw["loss"]) <= 1e-4 * abs(fw["loss"])
-    check_argmax(o["argmax"], Hd, Wd)
+    L = O.logits_rows(Hd, Wd)
+    check_argmax(o["argmax"], Hd, Wd, L=L)
+    check_label_rows(o["zy"], o["row_loss"], L, y, fw["lse"])
     # the backward's dL as the GPU keeps it: e5m2 codes with the scale fixed
     # by |dL| <= 1/M
-    L = O.logits_rows(Hd, Wd)
     P = np.exp(L - fw["lse"][:, None])
     P[np.arange(M), y] -= 1.0
     dL = P / M
@@ -106,3 +110,23 @@ def test_fp8_ce_forward_only_and_argument_errors():
     assert lib.coda_lmhead_ce_fp8(h, *args, 64, 56, 512, st) == 2
     # an empty batch has no mean
     assert lib.coda_lmhead_ce_fp8(h, *args, 0, 64, 512, st) == 1
+
+
+@pytest.mark.parametrize("M,d,V", [(200, 64, 1008), (37, 256, 40000)])
+def test_fp8_ce_label_logit_and_argmax_known_answer(M, d, V, pairing):
+    """Label indexing and argmax bit-exact on every row with 8-bit operands:
+    integer logits +-pi(v) written in base 8 (digits and powers of two exact
+    in e4m3 under the power-of-two scales), labels on the tile and chunk
+    edges."""
+    H, Wt, lab, zy_ref, am_ref = known_answer_ce(M, d, V, seed=M + V, base=8)
+    Hq, sH = quantize(H.cuda())
+    Wq, sW = quantize(Wt.cuda())
+    assert np.array_equal(deq(Hq, sH), f64(H)) and np.array_equal(deq(Wq, sW), f64(Wt))
+    o = run_fp8_ce(Hq, sH, Wq, sW, lab.cuda(), grads=False)
+    torch.cuda.synchronize()
+    assert_device_ok()
+    assert np.array_equal(f64(o["zy"]), zy_ref)
+    assert np.array_equal(o["argmax"].cpu().numpy().astype(np.int64), am_ref)
+    lse_ref = O.lse_rows(known_answer_logits(Wt, M, base=8))
+    assert_elem(o["lse"], lse_ref, "lse (fp8, integer logits)", tol=1e-5)
+    check_row_loss(o["row_loss"], lse_ref, zy_ref)
