@@ -43,7 +43,7 @@ _K7 = "7B backward: long-K tensor-core sums (K = 28672 or M = 8192) far from uni
 _K70 = "70B: long-K tensor-core sums (K = 8192 to 57344) far from unit scale"
 CUBLAS_RELATIVE = {
     ("test_7b_forward_backward_full_size", "dH"): _K7 + "; 1.21e-1, cuBLAS 1.21e-1",
-    ("test_7b_forward_backward_full_size", "dg"): _K7 + "; rms 261, 1.50e-1",
+    ("test_7b_forward_backward_full_size", "dg"): _K7 + "; rms 261, 1.50e-1, cuBLAS 1.50e-1",
     ("test_7b_forward_backward_full_size", "dW2t columns"): _K7 + "; rms 79, 3.83e-1, cuBLAS 3.83e-1",
     ("test_7b_forward_backward_full_size", "dW2t rows"): _K7 + "; rms 79, 3.81e-1, cuBLAS 3.81e-1",
     ("test_7b_forward_backward_full_size", "dW1t rows"): _K7 + "; rms 165, 4.13e-1, cuBLAS 4.13e-1",
@@ -52,17 +52,19 @@ CUBLAS_RELATIVE = {
     ("test_70b_forward_backward_full_size", "z"): _K70 + "; 3.13e-2, cuBLAS 3.13e-2",
     ("test_70b_forward_backward_full_size", "out"): _K70 + "; 7.31e-2, cuBLAS 7.31e-2",
     ("test_70b_forward_backward_full_size", "dH"): _K70 + "; 3.50e-1, cuBLAS 3.50e-1",
-    ("test_70b_forward_backward_full_size", "dg"): _K70 + "; rms 387, 9.97e-1",
+    ("test_70b_forward_backward_full_size", "dg"): _K70 + "; rms 387, 9.97e-1, cuBLAS 9.97e-1",
     ("test_70b_forward_backward_full_size", "dX"): _K70 + "; 5.20e-2, cuBLAS 5.20e-2",
     ("test_70b_forward_backward_full_size", "dW2t columns"): _K70 + "; rms 85, 5.53e-1, cuBLAS 5.53e-1",
     ("test_70b_forward_backward_full_size", "dW2t rows"): _K70 + "; rms 84, 2.11e-1, cuBLAS 2.11e-1",
     ("test_70b_forward_backward_full_size", "dW1t rows"): _K70 + "; rms 195, 3.10e-1, cuBLAS 3.10e-1",
     ("test_70b_forward_backward_full_size", "dW1t columns"): _K70 + "; rms 196, 3.33e-1, cuBLAS 3.33e-1",
-    ("test_split_block_stages_against_oracle", "dW2t"): "split tiles, M = 2048 rows summed, rms 26; 8.27e-2",
-    ("test_split_block_stages_against_oracle", "dW1t"): "split tiles, M = 2048 rows summed, rms 25; 5.06e-2",
+    ("test_split_block_stages_against_oracle", "dW2t"):
+        "split tiles, M = 2048 rows summed, rms 26; 8.27e-2, cuBLAS 7.95e-2",
+    ("test_split_block_stages_against_oracle", "dW1t"):
+        "split tiles, M = 2048 rows summed, rms 25; 5.06e-2, cuBLAS 5.06e-2",
     ("test_gemm2_epilogue_saturation", "out (saturating)"):
         "row scale 60-120 and silu ~ 100 amplify the accumulator's error near z_up's zero crossings; "
-        "rms 6.4e3, 6.15e-2",
+        "rms 6.4e3, 6.15e-2, cuBLAS 6.15e-2",
 }
 
 
