@@ -49,12 +49,43 @@ inline int split_first_tile(int tiles, int num_kb, int clusters, int slots) {
   return first;
 }
 
+// Co-resident SM pairs of one pair-kernel instantiation on the current
+// device (not every TPC need have both SMs enabled), queried once into
+// `cached` (one slot per device, owned by the calling launcher instantiation).
+inline cudaError_t pair_capacity(const void* kern, int threads, int smem, int num_sms, int (&cached)[64], int* pairs) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (cached[dev] == 0) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
+    cfg.blockDim = dim3(threads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    cached[dev] = std::max(1, std::min(n, num_sms / 2));
+  }
+  *pairs = cached[dev];
+  return cudaSuccess;
+}
+
 template <int BN, int STAGES, bool A_MN, bool B_MN, bool B_DUAL, class Epi, bool FP8 = false>
 cudaError_t launch_gemm2_kernel(const LaunchCtx& c, const CUtensorMap& ta, const CUtensorMap& tb,
                                 const CUtensorMap& tb2, int M, int N, int K, int tiles_n,
                                 const typename Epi::Params& ep) {
   using L = Gemm2Smem<BN, STAGES, epi_stage_bytes<Epi>()>;
-  auto kern = gemm_tc2_kernel<BN, STAGES, A_MN, B_MN, B_DUAL, Epi, FP8>;
+  auto kern = gemm_tc2_kernel<BN, STAGES, A_MN, B_MN, B_DUAL, Epi, FP8, false>;
+  auto kern_split = gemm_tc2_kernel<BN, STAGES, A_MN, B_MN, B_DUAL, Epi, FP8, true>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL);
   if (e != cudaSuccess) return e;
   GemmShape sh;
@@ -66,40 +97,29 @@ cudaError_t launch_gemm2_kernel(const LaunchCtx& c, const CUtensorMap& ta, const
   sh.num_kb = (K + (FP8 ? 128 : BK) - 1) / (FP8 ? 128 : BK);
   sh.group_m = 8;
   KernelCtl ctl{c.status, c.timeout_ns, c.skip_first_stage, c.scale_a, c.scale_b, c.f8_fmt, c.scale_host};
-  // co-resident SM pairs for this kernel (not every TPC need have both SMs
-  // enabled); queried once per instantiation and device
-  static int max_pairs[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (max_pairs[dev] == 0) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * (c.num_sms / 2), 1, 1);
-    cfg.blockDim = dim3(gemm_threads<Epi>(), 1, 1);
-    cfg.dynamicSmemBytes = L::TOTAL;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = 2;
-    attr.val.clusterDim.y = 1;
-    attr.val.clusterDim.z = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
-    if (e != cudaSuccess) return e;
-    max_pairs[dev] = std::max(1, std::min(n, c.num_sms / 2));
-  }
+  static int cap[64] = {};        // per device, for this instantiation
+  static int cap_split[64] = {};
+  int pairs = 0;
+  e = pair_capacity(reinterpret_cast<const void*>(kern), gemm_threads<Epi>(), L::TOTAL, c.num_sms, cap, &pairs);
+  if (e != cudaSuccess) return e;
   const int tiles = sh.tiles_m * sh.tiles_n;
-  int clusters = std::max(1, std::min(tiles, max_pairs[dev]));
-  // the partials are written per TMEM lane quadrant by one warp each: split
-  // tiles only under 4-warp epilogue programs
-  const int slots = (c.sk_parts != nullptr && c.sk_flags != nullptr && Epi::kEpiWarps == 4) ? c.sk_slots : 0;
-  sh.sk_first = split_first_tile(tiles, sh.num_kb, max_pairs[dev], slots);
-  if (sh.sk_first < tiles) {
-    clusters = max_pairs[dev];
-    ctl.sk_parts = c.sk_parts;
-    ctl.sk_flags = c.sk_flags;
+  sh.sk_first = tiles;
+  // split tiles only when a scratch is set, and only under 4-warp epilogue
+  // programs (the partials are written per TMEM lane quadrant by one warp)
+  if (c.sk_parts != nullptr && c.sk_flags != nullptr && Epi::kEpiWarps == 4) {
+    int split_pairs = 0;
+    e = pair_capacity(reinterpret_cast<const void*>(kern_split), gemm_threads<Epi>(), L::TOTAL, c.num_sms, cap_split,
+                      &split_pairs);
+    if (e != cudaSuccess) return e;
+    sh.sk_first = split_first_tile(tiles, sh.num_kb, split_pairs, c.sk_slots);
+    if (sh.sk_first < tiles) {
+      ctl.sk_parts = c.sk_parts;
+      ctl.sk_flags = c.sk_flags;
+      return launch_chained(c, kern_split, dim3(2 * split_pairs), dim3(gemm_threads<Epi>()), L::TOTAL, ta, tb, tb2,
+                            sh, ctl, ep);
+    }
   }
+  const int clusters = std::max(1, std::min(tiles, pairs));
   return launch_chained(c, kern, dim3(2 * clusters), dim3(gemm_threads<Epi>()), L::TOTAL, ta, tb, tb2, sh, ctl, ep);
 }
 

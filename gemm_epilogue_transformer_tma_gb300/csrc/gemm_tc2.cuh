@@ -113,7 +113,10 @@ struct Gemm2Smem {
   static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "1 KB aligned halves");
 };
 
-template <int BN, int STAGES, bool A_MN, bool B_MN, bool B_DUAL, class Epi, bool FP8 = false>
+// SPLIT: the instantiation that can split tiles (launched only when the
+// launch's split region is not empty); without it the partial and owner paths
+// are compiled out and the epilogue reads the accumulator from TMEM alone.
+template <int BN, int STAGES, bool A_MN, bool B_MN, bool B_DUAL, class Epi, bool FP8 = false, bool SPLIT = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi>(), 1)
     gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmB2, const GemmShape sh, const KernelCtl ctl,
@@ -334,8 +337,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi>(),
       tile_coords(pc.tile, sh, tm, tn);
       const int acc = it & 1;
       const uint32_t acc_phase = (it >> 1) & 1;
+      const bool partial = SPLIT && pc.partial;
+      const bool owner = SPLIT && pc.owner;
       if constexpr (EpiHasPrefetch<Epi>::value)
-        if (!pc.partial)
+        if (!partial)
           Epi::prefetch(ep, sh.M, sh.N, (tm * 2 + static_cast<int>(rank)) * 128 + row,
                         tn * BN + first_half * (BN / 2), HALVES * (BN / 2));
       bool ok = mbar_wait_bounded(&tfull[acc], acc_phase, abort_flag, ctl.timeout_ns);
@@ -346,7 +351,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi>(),
       }
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN);
-      if (pc.partial) {
+      if (partial) {
         // the first piece of this cluster's split range: the raw accumulator
         // of this warp's rows to the cluster's slot, then its flag
         float4* dst = reinterpret_cast<float4*>(
@@ -380,7 +385,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi>(),
         c.stage = stage_base;
         c.nsplit = 0;
         int q_end = cluster_id + 1;  // contributors are clusters cluster_id + 1 .. q_end - 1
-        if (pc.owner) {
+        if (owner) {
           // the clusters whose split ranges start inside this tile hold its
           // remaining k-blocks; wait for each one's partial of these rows
           const int64_t tile_end = (static_cast<int64_t>(pc.tile) + 1) * wk.nkb;
@@ -415,7 +420,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi>(),
           c.part = tn * 2 + half;
           Epi::template run<BN>(ep, c);
         }
-        if (pc.owner) {
+        if (owner) {
           // every lane has read the partials: clear the flags for the next launch
           __syncwarp();
           if (lane == 0)
