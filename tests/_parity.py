@@ -113,7 +113,7 @@ def _log(rec):
 
 
 def _grade(diff, absref, name, tol, e_cub):
-    """Shared verdict of assert_elem / assert_elem_chunks on |gpu - ref| and
+    """Shared decision of assert_elem / assert_elem_chunks on |gpu - ref| and
     |ref| (flat float64 arrays of one tensor); e_cub: cuBLAS's fixed-floor
     error on the same inputs, or None."""
     if diff.size == 0:
