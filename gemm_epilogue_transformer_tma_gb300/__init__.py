@@ -56,6 +56,7 @@ SIGNATURES = {
     "coda_debug_group_schedule_violations": (_INT, [_INT, _INT, _INT, _INT, _INT]),
     "coda_debug_split_schedule_violations": (_INT, [_INT, _INT, _INT]),
     "coda_debug_split_first_tile": (_INT, [_INT, _INT, _INT]),
+    "coda_debug_split_ranges": (_INT, [_INT, _INT, _INT]),
     "coda_set_sm_pairing": (_INT, [_P, _INT]),
     "coda_split_workspace_bytes": (_SZ, [_P]),
     "coda_set_split_workspace": (_INT, [_P, _P, _SZ, _P]),
@@ -437,6 +438,11 @@ def coda_debug_split_schedule_violations(tiles: int, num_kb: int, clusters: int)
 def coda_debug_split_first_tile(tiles: int, num_kb: int, clusters: int) -> int:
     """First split tile the launcher would choose, tiles if none (see include/coda_testing.h)."""
     return load_library().coda_debug_split_first_tile(tiles, num_kb, clusters)
+
+
+def coda_debug_split_ranges(tiles: int, num_kb: int, clusters: int) -> int:
+    """k-ranges per split tile the launcher would choose, 1 if none (see include/coda_testing.h)."""
+    return load_library().coda_debug_split_ranges(tiles, num_kb, clusters)
 
 
 def coda_bwd_workspace_bytes(M: int, d: int, N2: int) -> int:

@@ -60,14 +60,17 @@ LaunchCtx ctx_of(coda_handle_t h, void* stream) {
   c.scale_host = 1.f;
   c.sk_parts = h->sk_parts;
   c.sk_flags = h->sk_flags;
-  c.sk_slots = h->num_sms / 2;
+  c.sk_slots = split_scratch_slots(h->num_sms);
   return c;
 }
 
-// Split-tile scratch: one 256 x 256 fp32 partial per SM pair, then one flag
-// per (pair, CTA of the pair, epilogue warp).
-size_t split_parts_bytes(int num_sms) { return size_t(num_sms / 2) * 256 * 256 * sizeof(float); }
-size_t split_flags_bytes(int num_sms) { return size_t(num_sms / 2) * 2 * 8 * sizeof(int); }
+// Split-tile scratch: slots for the partials of the earlier k-ranges of a
+// launch's split tiles (at most pairs - 1 split tiles, kSplitMaxRanges - 1
+// partials each), a 256 x 256 fp32 accumulator per slot, then one flag per
+// (slot, CTA of the pair, epilogue warp).
+int split_slots(int num_sms) { return split_scratch_slots(num_sms); }
+size_t split_parts_bytes(int num_sms) { return size_t(split_slots(num_sms)) * 256 * 256 * sizeof(float); }
+size_t split_flags_bytes(int num_sms) { return size_t(split_slots(num_sms)) * 2 * 8 * sizeof(int); }
 
 coda_status_t from_cuda(cudaError_t e) {
   if (e == cudaSuccess) return CODA_OK;

@@ -67,6 +67,9 @@ cudaError_t launch_chained(const LaunchCtx& c, void (*kern)(KArgs...), dim3 grid
 // opaque coda_handle_t.
 LaunchCtx launch_ctx_of_handle(void* handle, void* stream);
 int device_of_handle(void* handle);
+// Partial-accumulator slots the split-tile scratch needs on a GPU with
+// num_sms SMs (gemm_fwd.cu, beside the split plan it serves).
+int split_scratch_slots(int num_sms);
 // The handle's slot for the device address of the allocation-free call's
 // scratch array (noalloc.cu); null until that call first runs on the handle.
 void** noalloc_scratch_slot(void* handle);

@@ -97,57 +97,75 @@ cudaError_t gemm_store_f32(const LaunchCtx& c, const __nv_bfloat16* A, bool a_mn
 
 }  // namespace coda
 
+int coda::split_scratch_slots(int num_sms) { return (num_sms / 2 - 1) * (kSplitMaxRanges - 1); }
+
 // Host-side check of the split-tile schedule of the SM-pair kernel, run with
 // the kernel's own iterator (coda_debug_split_schedule_violations in
 // include/coda_testing.h).
 extern "C" int coda_debug_split_schedule_violations(int tiles, int num_kb, int clusters) {
   using namespace coda;
   if (tiles < 1 || num_kb < 1 || clusters < 1) return -1;
+  const int slots = (clusters - 1) * (kSplitMaxRanges - 1);
+  const SplitPlan plan = split_plan(tiles, num_kb, clusters, slots);
+  if (plan.first == tiles) return 0;  // not split: nothing to check
   GemmShape sh{};
   sh.tiles_m = tiles;
   sh.tiles_n = 1;
   sh.num_kb = num_kb;
-  sh.sk_first = split_first_tile(tiles, num_kb, clusters, clusters);
-  if (sh.sk_first == tiles) return 0;  // not split: nothing to check
-  std::vector<int> cover(static_cast<size_t>(tiles) * num_kb, 0);
+  sh.sk_first = plan.first;
+  sh.sk_ranges = plan.ranges;
+  const int S = plan.ranges;
+  const int rem = tiles - plan.first;
   int bad = 0;
+  if (S < 2 || S > kSplitMaxRanges || rem >= clusters || rem * (S - 1) > slots) ++bad;
+  std::vector<int> cover(static_cast<size_t>(tiles) * num_kb, 0);
+  // which (tile, k-range) wrote each slot, and in which order each cluster met its pieces
+  std::vector<int> slot_tile(static_cast<size_t>(rem) * (S - 1), -1), slot_kb0(slot_tile.size(), -1);
+  std::vector<std::vector<TilePiece>> owners(clusters);
   for (int cid = 0; cid < clusters; ++cid) {
     SplitWork wk(sh, cid, clusters);
     TilePiece pc;
-    int n_split = 0, n_partial = 0, n_owner = 0, last_owner = -1, first_partial = -1;
+    bool seen_owner = false;
     while (wk.next(pc)) {
+      if (pc.kb0 >= pc.kb1) ++bad;  // an empty range
       for (int k = pc.kb0; k < pc.kb1; ++k) cover[static_cast<size_t>(pc.tile) * num_kb + k]++;
-      if (pc.tile < sh.sk_first) continue;
+      if (pc.tile < sh.sk_first) {
+        if (pc.partial || pc.owner || pc.kb0 != 0 || pc.kb1 != num_kb) ++bad;
+        continue;
+      }
+      if (pc.partial == pc.owner) ++bad;  // every split piece is exactly one of the two
       if (pc.partial) {
-        ++n_partial;
-        if (n_split != 0) ++bad;  // a partial piece is always the first of the range
-        first_partial = pc.tile;
+        if (seen_owner) ++bad;  // partial pieces come before the cluster's owner pieces
+        if (pc.slot < 0 || pc.slot >= static_cast<int>(slot_tile.size()) || slot_tile[pc.slot] != -1) {
+          ++bad;
+        } else {
+          slot_tile[pc.slot] = pc.tile;
+          slot_kb0[pc.slot] = pc.kb0;
+        }
       }
       if (pc.owner) {
-        ++n_owner;
-        last_owner = n_split;
-        // the clusters whose ranges start inside the tile hold k-blocks
-        // [pc.kb1, num_kb): each one's first piece is a partial there, and
-        // together they cover the rest of the tile without a gap
-        const int64_t tile_end = (static_cast<int64_t>(pc.tile) + 1) * num_kb;
-        int pos = pc.kb1, n_contrib = 0;
-        for (int q = cid + 1; q < clusters && wk.start_of(q) < tile_end; ++q) {
-          SplitWork wq(sh, q, clusters);
-          TilePiece f;
-          while (wq.next(f) && f.tile < sh.sk_first) {
-          }
-          if (f.tile != pc.tile || !f.partial || f.kb0 != pos) ++bad;
-          pos = f.kb1;
-          ++n_contrib;
-        }
-        if (pos != num_kb || n_contrib > kMaxSplitParts) ++bad;
+        seen_owner = true;
+        if (pc.kb1 != num_kb) ++bad;  // the owner holds the tile's last k-range
+        owners[cid].push_back(pc);
       }
-      ++n_split;
     }
-    (void)first_partial;
-    if (n_split == 0 || n_partial > 1 || n_owner > 1) ++bad;
-    if (n_owner == 1 && last_owner != n_split - 1) ++bad;  // the owner piece ends the range
   }
+  // each owner's slots hold its tile's earlier k-ranges, in order, covering
+  // k-blocks [0, owner's first k-block) without a gap
+  for (int cid = 0; cid < clusters; ++cid)
+    for (const TilePiece& o : owners[cid]) {
+      int pos = 0;
+      for (int j = 0; j < S - 1; ++j) {
+        const int sl = o.slot + j;
+        if (sl < 0 || sl >= static_cast<int>(slot_tile.size()) || slot_tile[sl] != o.tile || slot_kb0[sl] != pos) {
+          ++bad;
+          break;
+        }
+        SplitWork probe(sh, 0, clusters);
+        pos = probe.kb_begin(j + 1);
+      }
+      if (pos != o.kb0) ++bad;
+    }
   for (int v : cover)
     if (v != 1) ++bad;
   return bad;
@@ -157,5 +175,11 @@ extern "C" int coda_debug_split_schedule_violations(int tiles, int num_kb, int c
 // (coda_debug_split_first_tile in include/coda_testing.h).
 extern "C" int coda_debug_split_first_tile(int tiles, int num_kb, int clusters) {
   if (tiles < 1 || num_kb < 1 || clusters < 1) return -1;
-  return coda::split_first_tile(tiles, num_kb, clusters, clusters);
+  return coda::split_plan(tiles, num_kb, clusters, (clusters - 1) * (coda::kSplitMaxRanges - 1)).first;
+}
+
+// k-ranges per split tile the launcher would choose (1: no split).
+extern "C" int coda_debug_split_ranges(int tiles, int num_kb, int clusters) {
+  if (tiles < 1 || num_kb < 1 || clusters < 1) return -1;
+  return coda::split_plan(tiles, num_kb, clusters, (clusters - 1) * (coda::kSplitMaxRanges - 1)).ranges;
 }

@@ -24,6 +24,7 @@ GemmShape pair_shape(int M, int N, int K, bool fp8 = false) {
   sh.num_kb = (K + bke - 1) / bke;
   sh.group_m = 8;
   sh.sk_first = sh.tiles_m * sh.tiles_n;  // grouped launches never split tiles
+  sh.sk_ranges = 1;
   return sh;
 }
 

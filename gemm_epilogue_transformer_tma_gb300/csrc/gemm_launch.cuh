@@ -29,24 +29,43 @@ cudaError_t launch_gemm_kernel(const LaunchCtx& c, const CUtensorMap& ta, const 
   KernelCtl ctl{c.status, c.timeout_ns, c.skip_first_stage, c.scale_a, c.scale_b, c.f8_fmt, c.scale_host};
   const int tiles = sh.tiles_m * sh.tiles_n;
   sh.sk_first = tiles;  // the 1-SM kernel never splits tiles
+  sh.sk_ranges = 1;
   const int grid = std::max(1, std::min(tiles, c.num_sms));
   return launch_chained(c, kern, dim3(grid), dim3(gemm_threads<Epi>()), L::TOTAL, ta, tb, tb2, sh, ctl, ep);
 }
 
-// First tile of the split region of an SM-pair launch (stream-K over the
-// last partial wave and the full wave before it), or `tiles` for no split.
-// Split only when the scratch has a slot for every cluster, the last wave is
-// partial, a tile has at least kSplitMinKb k-blocks, and every split tile has
-// at most kMaxSplitParts contributing clusters besides its owner.
-constexpr int kSplitMinKb = 16;
-inline int split_first_tile(int tiles, int num_kb, int clusters, int slots) {
-  if (slots < clusters || clusters < 2 || num_kb < kSplitMinKb || tiles % clusters == 0) return tiles;
-  const int full = tiles / clusters;
-  const int first = full >= 1 ? (full - 1) * clusters : 0;
-  const int64_t per = static_cast<int64_t>(tiles - first) * num_kb / clusters;  // k-blocks per cluster (floor)
-  // starts of other clusters strictly inside one tile: at most ceil((num_kb - 1) / per)
-  if (per < 1 || (num_kb - 1 + per - 1) / per > kMaxSplitParts) return tiles;
-  return first;
+// The split of an SM-pair launch: the remainder tiles after the full waves
+// (the last, partial wave) are each cut into `ranges` k-ranges, dealt
+// range-major and round-robin to all clusters.  The count is the one that
+// finishes the remainder in the fewest rounds, ceil(rem * ranges / clusters)
+// k-ranges' time, against one whole round unsplit.  Ranges of fewer than
+// kSplitMinRangeKb k-blocks are not used (the owner's reads of the other
+// ranges' partials at the end of the launch would eat the gain), nor more
+// than kSplitMaxRanges, nor more partial slots than the scratch has.
+constexpr int kSplitMaxRanges = kMaxSplitParts + 1;
+constexpr int kSplitMinRangeKb = 48;
+struct SplitPlan {
+  int first;   // first split tile (tiles: no split)
+  int ranges;  // k-ranges per split tile (1: no split)
+};
+inline SplitPlan split_plan(int tiles, int num_kb, int clusters, int slots) {
+  SplitPlan plan{tiles, 1};
+  if (clusters < 2 || tiles < 1) return plan;
+  const int rem = tiles % clusters;
+  if (rem == 0) return plan;
+  // rounds of ranges for the remainder, compared as best_rounds / best
+  int best = 1, best_rounds = 1;
+  for (int r = 2; r <= kSplitMaxRanges && num_kb / r >= kSplitMinRangeKb; ++r) {
+    const int rounds = (rem * r + clusters - 1) / clusters;  // in units of 1/r of a round
+    if (rounds * best < best_rounds * r) {
+      best = r;
+      best_rounds = rounds;
+    }
+  }
+  if (best < 2 || rem * (best - 1) > slots) return plan;
+  plan.first = tiles - rem;
+  plan.ranges = best;
+  return plan;
 }
 
 // Co-resident SM pairs of one pair-kernel instantiation on the current
@@ -104,6 +123,7 @@ cudaError_t launch_gemm2_kernel(const LaunchCtx& c, const CUtensorMap& ta, const
   if (e != cudaSuccess) return e;
   const int tiles = sh.tiles_m * sh.tiles_n;
   sh.sk_first = tiles;
+  sh.sk_ranges = 1;
   // split tiles only when a scratch is set, and only under 4-warp epilogue
   // programs (the partials are written per TMEM lane quadrant by one warp)
   if (c.sk_parts != nullptr && c.sk_flags != nullptr && Epi::kEpiWarps == 4) {
@@ -111,7 +131,9 @@ cudaError_t launch_gemm2_kernel(const LaunchCtx& c, const CUtensorMap& ta, const
     e = pair_capacity(reinterpret_cast<const void*>(kern_split), gemm_threads<Epi>(), L::TOTAL, c.num_sms, cap_split,
                       &split_pairs);
     if (e != cudaSuccess) return e;
-    sh.sk_first = split_first_tile(tiles, sh.num_kb, split_pairs, c.sk_slots);
+    const SplitPlan plan = split_plan(tiles, sh.num_kb, split_pairs, c.sk_slots);
+    sh.sk_first = plan.first;
+    sh.sk_ranges = plan.ranges;
     if (sh.sk_first < tiles) {
       ctl.sk_parts = c.sk_parts;
       ctl.sk_flags = c.sk_flags;

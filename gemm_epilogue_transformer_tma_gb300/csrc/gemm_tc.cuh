@@ -56,16 +56,18 @@ constexpr int UMMA_K = 16;
 template <class Epi>
 constexpr int gemm_threads() { return 64 + 32 * Epi::kEpiWarps; }
 constexpr int PART_COLS = 128;     // columns per block-reduction partial (half a tile)
-constexpr int kMaxSplitParts = 3;  // other clusters' K ranges a split tile may have
+constexpr int kMaxSplitParts = 5;  // earlier k-ranges (partials) a split tile may have
 
 struct GemmShape {
   int M, N, K;        // logical problem (N = output columns the epilogue sees)
   int tiles_m, tiles_n;
   int num_kb;
   int group_m;        // tile raster: groups of group_m M-tiles sweep all N-tiles
-  // SM-pair kernel only: tiles [sk_first, tiles) are split along K across
-  // clusters (stream-K); sk_first = tiles_m * tiles_n means no split
+  // SM-pair kernel only: tiles [sk_first, tiles) (the last, partial wave)
+  // are each split into sk_ranges k-ranges run by different clusters;
+  // sk_first = tiles_m * tiles_n (and sk_ranges = 1) means no split
   int sk_first;
+  int sk_ranges;
 };
 
 struct KernelCtl {
@@ -76,9 +78,9 @@ struct KernelCtl {
   const float* scale_b;
   uint32_t f8_fmt;       // FP8 operands: format bits of A and B (f8_format_bits)
   float scale_host;      // FP8 operands: a scale known on the host (1 otherwise)
-  // split tiles (SM-pair kernel): one partial-accumulator slot per cluster
-  // ([cluster][rank][quad][32 rows x 256 columns] fp32) and one flag per
-  // (cluster, rank, epilogue warp); null when tiles are not split
+  // split tiles (SM-pair kernel): partial-accumulator slots, one per (split
+  // tile, earlier k-range) ([slot][rank][quad][32 rows x 256 columns] fp32),
+  // and one flag per (slot, rank, epilogue warp); null when tiles are not split
   float* sk_parts;
   int* sk_flags;
 };

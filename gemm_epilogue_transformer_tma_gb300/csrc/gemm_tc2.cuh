@@ -31,56 +31,61 @@ namespace coda {
 
 constexpr int BM2 = 256;  // output rows per CTA pair
 
-// Work of one cluster: whole tiles first (tiles cluster, cluster + P, ...
-// below sh.sk_first), then its share of the split region.  The split region
-// (tiles sk_first .. tiles - 1, the last partial wave and the full wave
-// before it) is a run of (tile, k-block) units dealt in P equal contiguous
-// ranges, one per cluster (stream-K).  A cluster's range may start inside a
-// tile: that first piece is a partial accumulator, which goes to the
-// cluster's scratch slot.  Every later piece of the range starts at k-block 0
-// of its tile and is that tile's owner: when it ends before the tile's last
-// k-block, the clusters whose ranges start inside the tile hold the rest, and
-// the owner's epilogue adds their partials before it runs.  Owners come last
-// in a range and partial pieces first, so no cluster ever waits on a cluster
-// that is waiting.  Producer, MMA issuer and epilogue walk the same sequence.
+// Work of one cluster.  Whole tiles first: tiles cluster, cluster + P, ...
+// below sh.sk_first (every full wave).  The tiles from sk_first on, the last
+// and partial wave, are each cut into sh.sk_ranges equal k-ranges.  Those
+// units (k-range j of tile t) are taken range-major -- every split tile's
+// first range, then every second range, ... -- and dealt round-robin, so the
+// units that run at the same time cover the same k-range and read the same
+// k-slices of their operand panels, as the whole tiles of one wave do.  A
+// unit of a tile's last range owns the tile: its epilogue adds the fp32
+// partials that the tile's earlier ranges left in their scratch slots
+// (written by whichever clusters ran them) and runs the epilogue program.
+// Every cluster meets all its partial units before its owner units, and
+// partial units never wait, so no cluster waits on a waiting cluster.
+// Producer, MMA issuer and epilogue walk the same sequence.
 struct TilePiece {
   int tile, kb0, kb1;
-  bool partial;  // kb0 > 0: accumulator to the scratch slot, no epilogue program
-  bool owner;    // kb0 == 0 and kb1 < num_kb: other clusters hold the tile's remaining k-blocks
+  int slot;      // partial: its scratch slot; owner: the tile's first slot
+  bool partial;  // an earlier k-range: accumulator to the slot, no epilogue program
+  bool owner;    // the last k-range: the earlier ranges' partials are added before the epilogue
 };
 
 struct SplitWork {
-  int next_whole, first_split, P, nkb;
-  int64_t base, W, u, u_end;
+  int next_whole, first_split, P, nkb, S, rem, u;
   __host__ __device__ SplitWork(const GemmShape& sh, int cluster, int num_clusters) {
     next_whole = cluster;
     first_split = sh.sk_first;
     P = num_clusters;
     nkb = sh.num_kb;
-    base = static_cast<int64_t>(sh.sk_first) * nkb;
-    W = static_cast<int64_t>(sh.tiles_m * sh.tiles_n - sh.sk_first) * nkb;
-    u = start_of(cluster);
-    u_end = start_of(cluster + 1);
+    S = sh.sk_ranges;
+    rem = sh.tiles_m * sh.tiles_n - sh.sk_first;
+    u = cluster;
   }
-  // first (tile, k-block) unit of cluster q's split range
-  __host__ __device__ int64_t start_of(int q) const { return base + W * q / P; }
+  // first k-block of k-range j of a split tile
+  __host__ __device__ int kb_begin(int j) const {
+    return static_cast<int>(static_cast<int64_t>(nkb) * j / S);
+  }
   __host__ __device__ bool next(TilePiece& pc) {
     if (next_whole < first_split) {
       pc.tile = next_whole;
       pc.kb0 = 0;
       pc.kb1 = nkb;
+      pc.slot = -1;
       pc.partial = pc.owner = false;
       next_whole += P;
       return true;
     }
-    if (u >= u_end) return false;
-    pc.tile = static_cast<int>(u / nkb);
-    pc.kb0 = static_cast<int>(u - static_cast<int64_t>(pc.tile) * nkb);
-    const int64_t rest = pc.kb0 + (u_end - u);
-    pc.kb1 = static_cast<int>(rest < nkb ? rest : nkb);
-    pc.partial = pc.kb0 > 0;
-    pc.owner = pc.kb0 == 0 && pc.kb1 < nkb;
-    u += pc.kb1 - pc.kb0;
+    if (S < 2 || u >= S * rem) return false;
+    const int j = u / rem;
+    const int i = u - j * rem;
+    pc.tile = first_split + i;
+    pc.kb0 = kb_begin(j);
+    pc.kb1 = kb_begin(j + 1);
+    pc.partial = j < S - 1;
+    pc.owner = j == S - 1;
+    pc.slot = i * (S - 1) + (pc.partial ? j : 0);
+    u += P;
     return true;
   }
 };
@@ -355,7 +360,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi>(),
         // the first piece of this cluster's split range: the raw accumulator
         // of this warp's rows to the cluster's slot, then its flag
         float4* dst = reinterpret_cast<float4*>(
-            ctl.sk_parts + static_cast<int64_t>((cluster_id * 2 + static_cast<int>(rank)) * 4 + quad) *
+            ctl.sk_parts + static_cast<int64_t>((pc.slot * 2 + static_cast<int>(rank)) * 4 + quad) *
                                SPLIT_PART_FLOATS);
 #pragma unroll 1
         for (int cc = first_half * (BN / 2); cc < (first_half + HALVES) * (BN / 2); cc += 32) {
@@ -368,7 +373,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi>(),
         }
         __threadfence();
         __syncwarp();
-        if (lane == 0) st_release_gpu(&ctl.sk_flags[(cluster_id * 2 + static_cast<int>(rank)) * 8 + ew], 1);
+        if (lane == 0) st_release_gpu(&ctl.sk_flags[(pc.slot * 2 + static_cast<int>(rank)) * 8 + ew], 1);
       } else {
         EpiCtx c;
         c.M = sh.M;
@@ -384,25 +389,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi>(),
         c.taddr = taddr;
         c.stage = stage_base;
         c.nsplit = 0;
-        int q_end = cluster_id + 1;  // contributors are clusters cluster_id + 1 .. q_end - 1
+        const int n_parts = owner ? wk.S - 1 : 0;  // the tile's earlier k-ranges, one slot each
         if (owner) {
-          // the clusters whose split ranges start inside this tile hold its
-          // remaining k-blocks; wait for each one's partial of these rows
-          const int64_t tile_end = (static_cast<int64_t>(pc.tile) + 1) * wk.nkb;
-          while (q_end < num_clusters && wk.start_of(q_end) < tile_end) ++q_end;
-          bool got = q_end - cluster_id - 1 <= kMaxSplitParts;
+          // wait for each earlier k-range's partial of these rows
+          bool got = n_parts <= kMaxSplitParts;
 #pragma unroll
           for (int j = 0; j < kMaxSplitParts; ++j) {
-            const int q = cluster_id + 1 + j;
-            if (got && q < q_end) {
-              const int* f = &ctl.sk_flags[(q * 2 + static_cast<int>(rank)) * 8 + ew];
+            if (got && j < n_parts) {
+              const int slot = pc.slot + j;
+              const int* f = &ctl.sk_flags[(slot * 2 + static_cast<int>(rank)) * 8 + ew];
               bool seen = true;
               if (lane == 0) seen = split_flag_wait(f, abort_flag, ctl.timeout_ns);
               got = __shfl_sync(0xffffffffu, seen, 0);
               if (got) {
                 (void)ld_acquire_gpu(f);  // every lane: its partial loads come after the flag
                 c.split[j] = ctl.sk_parts +
-                             static_cast<int64_t>((q * 2 + static_cast<int>(rank)) * 4 + quad) * SPLIT_PART_FLOATS;
+                             static_cast<int64_t>((slot * 2 + static_cast<int>(rank)) * 4 + quad) * SPLIT_PART_FLOATS;
                 c.nsplit = j + 1;
               }
             }
@@ -424,8 +426,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi>(),
           // every lane has read the partials: clear the flags for the next launch
           __syncwarp();
           if (lane == 0)
-            for (int q = cluster_id + 1; q < q_end; ++q)
-              st_relaxed_gpu(&ctl.sk_flags[(q * 2 + static_cast<int>(rank)) * 8 + ew], 0);
+            for (int j = 0; j < n_parts; ++j)
+              st_relaxed_gpu(&ctl.sk_flags[((pc.slot + j) * 2 + static_cast<int>(rank)) * 8 + ew], 0);
         }
       }
       tc_fence_before();

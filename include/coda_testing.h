@@ -29,11 +29,13 @@ int coda_debug_group_schedule_violations(int P, int heavy, int nH, int nL, int q
 /* Host-side check of the split-tile schedule (coda_set_split_workspace) of
  * the SM-pair GEMM, run with the kernel's own work iterator (no GPU needed):
  * `tiles` output tiles of `num_kb` k-blocks on `clusters` SM pairs.  Returns
- * 0 when the launch would not split or when every (tile, k-block) is computed
- * exactly once, each pair's range has at most one partial piece (its first)
- * and one owner piece (its last), and each owner's contributors cover the
- * rest of its tile contiguously, at most three of them; the number of
- * violations otherwise, -1 for invalid arguments.  Not for production use. */
+ * 0 when the launch would not split, or when every (tile, k-block) is
+ * computed exactly once, every split piece is either a partial (an earlier
+ * k-range, written to a slot no other piece writes) or the owner (the last
+ * k-range), each cluster meets all its partial pieces before its owner
+ * pieces, and each owner's slots hold its tile's earlier k-ranges in order
+ * without a gap; the number of violations otherwise, -1 for invalid
+ * arguments.  Not for production use. */
 int coda_debug_split_schedule_violations(int tiles, int num_kb, int clusters);
 
 /* The first tile of the split region that an SM-pair launch of `tiles` tiles
@@ -41,6 +43,10 @@ int coda_debug_split_schedule_violations(int tiles, int num_kb, int clusters);
  * set (tiles when it would not split), -1 for invalid arguments.  Not for
  * production use. */
 int coda_debug_split_first_tile(int tiles, int num_kb, int clusters);
+
+/* The k-ranges per split tile of that launch (1 when it would not split),
+ * -1 for invalid arguments.  Not for production use. */
+int coda_debug_split_ranges(int tiles, int num_kb, int clusters);
 
 #ifdef __cplusplus
 }

@@ -58,10 +58,12 @@ CUBLAS_RELATIVE = {
     ("test_70b_forward_backward_full_size", "dW2t rows"): _K70 + "; rms 84, 2.11e-1, cuBLAS 2.11e-1",
     ("test_70b_forward_backward_full_size", "dW1t rows"): _K70 + "; rms 195, 3.10e-1, cuBLAS 3.10e-1",
     ("test_70b_forward_backward_full_size", "dW1t columns"): _K70 + "; rms 196, 3.33e-1, cuBLAS 3.33e-1",
+    ("test_split_block_stages_against_oracle", "dH"):
+        "split dgrad2, K = 16384; 5.02e-2, cuBLAS 5.23e-2",
     ("test_split_block_stages_against_oracle", "dW2t"):
-        "split tiles, M = 2048 rows summed, rms 26; 8.27e-2, cuBLAS 7.95e-2",
+        "M = 2048 rows summed, rms 40; 1.22e-1, cuBLAS 1.22e-1",
     ("test_split_block_stages_against_oracle", "dW1t"):
-        "split tiles, M = 2048 rows summed, rms 25; 5.06e-2, cuBLAS 5.06e-2",
+        "M = 2048 rows summed, rms 76; 1.94e-1, cuBLAS 1.94e-1",
     ("test_gemm2_epilogue_saturation", "out (saturating)"):
         "row scale 60-120 and silu ~ 100 amplify the accumulator's error near z_up's zero crossings; "
         "rms 6.4e3, 6.15e-2, cuBLAS 6.15e-2",

@@ -1,7 +1,8 @@
 """GEMMs whose last, partial wave is split along K across all SM pairs
-(coda_set_split_workspace): the tiles of the last wave and of the full wave
-before it are dealt as equal runs of k-blocks, and the pair holding a split
-tile's first k-block adds the others' fp32 partials before its epilogue.
+(coda_set_split_workspace): the remainder tiles after the full waves are
+each cut into equal k-ranges, dealt range-major to all pairs, and the pair
+that runs a tile's last range adds the earlier ranges' fp32 partials before
+its epilogue.
 
 Checked with splitting on, at sizes where the launcher splits (asked of the
 library's own rule through its test hook):
@@ -10,7 +11,8 @@ library's own rule through its test hook):
   * the block forward and backward stages (every epilogue program of the
     path) elementwise against the oracle fed the GPU's own stage inputs, and
     close to the unsplit run;
-  * the LM-head cross-entropy statistics and gradient programs;
+  * the LM-head cross-entropy statistics and gradient programs (at a hidden
+    width long enough to split);
   * two runs bit-identical (the split is a fixed schedule).
 
 Method: "CODA: Rewriting Transformer Blocks as GEMM-Epilogue Programs"
@@ -24,7 +26,7 @@ import torch
 import oracle as O
 from coda_inputs import BlockShape, CEShape, block_inputs, ce_inputs
 from tests._parity import assert_device_ok, assert_elem, assert_frob, f64
-from tests.test_gpu_exact import exact_bf16, ints
+from tests.test_gpu_exact import ints
 
 pytestmark = pytest.mark.gpu
 
@@ -36,7 +38,15 @@ def splits(M, N, K, kb=64):
     tiles, kb-deep k-blocks) on this GPU's SM pairs."""
     tiles = -(-M // 256) * -(-N // 256)
     pairs = torch.cuda.get_device_properties(0).multi_processor_count // 2
-    return C.coda_debug_split_first_tile(tiles, -(-K // kb), pairs) < tiles
+    return C.coda_debug_split_ranges(tiles, -(-K // kb), pairs) > 1
+
+
+def exact(A, Bt, scale=1.0):
+    """bf16 of the exact integer product A Bt^T (float64 BLAS: every partial
+    sum is an integer below 2^53), times an exact power of two."""
+    v = (A.to(torch.float64) @ Bt.to(torch.float64).T) * scale
+    assert float(v.abs().max()) < 2 ** 24
+    return v.to(torch.float32).to(torch.bfloat16)
 
 
 @pytest.fixture
@@ -50,7 +60,7 @@ def split_on():
 
 
 @pytest.mark.parametrize("a_mn,b_mn", [(False, False), (False, True), (True, True)])
-@pytest.mark.parametrize("M,N,K", [(2048, 2048, 2048), (1000, 1800, 6000), (8192, 4096, 1024)])
+@pytest.mark.parametrize("M,N,K", [(2048, 4096, 16384), (1800, 3904, 13000)])
 def test_split_gemm_bit_exact(a_mn, b_mn, M, N, K, split_on):
     assert splits(M, N, K)
     A = ints((M, K), -3, 3, 21)
@@ -61,12 +71,12 @@ def test_split_gemm_bit_exact(a_mn, b_mn, M, N, K, split_on):
     C.coda_gemm(Ad, a_mn, Bd, b_mn, Cd, M, N, K)
     torch.cuda.synchronize()
     assert_device_ok()
-    assert torch.equal(Cd.cpu(), exact_bf16(A, Bt))
+    assert torch.equal(Cd.cpu(), exact(A, Bt))
 
 
 @pytest.mark.parametrize("a_mn,b_mn", [(False, False), (True, True)])
 def test_split_fp8_gemm_bit_exact(a_mn, b_mn, split_on):
-    M, N, K = 2048, 2304, 4096         # 8 x 9 tiles, 32 k-blocks of 128 codes
+    M, N, K = 2048, 4096, 24576        # 8 x 16 tiles, 192 k-blocks of 128 codes
     assert splits(M, N, K, kb=128)
     A = ints((M, K), -4, 4, 23)
     Bt = ints((N, K), -4, 4, 24)
@@ -79,18 +89,19 @@ def test_split_fp8_gemm_bit_exact(a_mn, b_mn, split_on):
                     torch.from_numpy(np.ascontiguousarray(Bq)).cuda(), b_mn, 0, sB, Cd, M, N, K)
     torch.cuda.synchronize()
     assert_device_ok()
-    assert torch.equal(Cd.cpu(), exact_bf16(A, Bt, torch.full((M,), 2.0)))
+    assert torch.equal(Cd.cpu(), exact(A, Bt, 2.0))   # sA * sB = 2
 
 
-SPLIT_BLOCK = BlockShape("split", 2048, 2048, 2048, 4096)
+# dgrad2 (M x d x 2F = 2048 x 4096 x 16384, 256 k-blocks) splits; the
+# step's shorter-K GEMMs do not
+SPLIT_BLOCK = BlockShape("split", 2048, 2048, 4096, 16384)
 
 
 def test_split_block_stages_against_oracle(split_on):
-    """Every GEMM of the step splits at this shape except the grouped first
-    layer's backward; each stage against the oracle on the GPU's own inputs."""
+    """The block at a size whose dgrad2 (the RMSNorm-backward epilogue)
+    splits; every stage against the oracle on the GPU's own inputs."""
     s = SPLIT_BLOCK
-    for M, N, K in ((s.M, s.d, s.K1), (s.M, s.N2, s.d), (s.M, s.d, s.N2), (s.N2, s.d, s.M)):
-        assert splits(M, N, K)
+    assert splits(s.M, s.d, s.N2)
     x = block_inputs(s, 0, "cuda")
     b = BlockBuffers(x)
     b.forward()
@@ -103,14 +114,20 @@ def test_split_block_stages_against_oracle(split_on):
     z_ref = O.rowscale_gemm(H, f64(b.W2gt), f64(b.rstd))
     assert_elem(b.z, z_ref, "z")
     assert_elem(b.out, O.swiglu(z_ref), "out")
+    # dgrad2 sums K = 16384 terms: dH and dg are compared with cuBLAS on the
+    # same inputs as at full size
     dH_ref, dg_ref = O.stage_dgrad2_rmsbwd(f64(b.dP), W2t, g, H, f64(b.c))
-    assert_elem(b.dH, dH_ref, "dH")
-    assert_elem(b.dg, dg_ref, "dg")
+    acc = torch.mm(b.dP, b.W2t, out_dtype=torch.float32)
+    dH_cub = (b.g.float() * acc - b.c[:, None] * b.H.float()).to(torch.bfloat16)
+    dg_cub = (acc * b.H.float()).sum(0)
+    del acc
+    assert_elem(b.dH, dH_ref, "dH", cublas=dH_cub)
+    assert_elem(b.dg, dg_ref, "dg", cublas=dg_cub)
     # the weight gradients sum M = 2048 rows (rms ~ 26): compared with cuBLAS
     # on the same inputs as at full size
     cub = (torch.mm(b.dP.t(), b.H, out_dtype=torch.float32) * b.g.float()).to(torch.bfloat16)
     assert_elem(b.dW2t, O.stage_wgrad2(H, f64(b.dP), g), "dW2t", cublas=cub)
-    assert_elem(b.dX, O.stage_dgrad1(f64(b.dH), W1t), "dX")
+    assert_elem(b.dX, O.stage_dgrad1(f64(b.dH), W1t), "dX", cublas=torch.matmul(b.dH, b.W1t))
     assert_elem(b.dW1t, O.stage_wgrad1(f64(b.dH), X), "dW1t", cublas=torch.matmul(b.dH.t(), b.X))
     full = O.block_forward(X, W1t, R, g, W2t, s.eps, True)
     assert_frob(b.out, full["out"], "out e2e")
@@ -142,10 +159,11 @@ def test_split_is_deterministic(split_on):
 
 
 def test_split_lmhead_ce(split_on):
-    """Statistics (628 tiles of 32 k-blocks) and per-chunk gradient
-    recompute (256 tiles per chunk) both split; lse, loss and argmax against
-    the oracle, dH and dW by Frobenius."""
-    s = CEShape("split_ce", 1024, 2048, 40000)
+    """At a hidden width of 12288 (192 k-blocks) the statistics GEMM (314
+    tiles) and each vocabulary chunk's gradient recompute (128 tiles) split;
+    lse, loss, label logits and argmax against the oracle, dH and dW by
+    Frobenius."""
+    s = CEShape("split_ce", 512, 12288, 40000)
     assert splits(s.M, s.V, s.d) and splits(s.M, 16384, s.d)
     x = {k: v.cuda() for k, v in ce_inputs(s, 0).items()}
     M, d, V = s.M, s.d, s.V
