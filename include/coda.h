@@ -99,29 +99,31 @@ coda_status_t coda_set_wait_timeout_ns(coda_handle_t h, uint64_t ns);
 coda_status_t coda_set_sm_pairing(coda_handle_t h, int enable);
 
 /* Scratch that lets this handle's SM-pair GEMMs keep every SM pair busy in
- * their last, partial wave (stream-K).  Without it (the default) each SM pair
- * computes whole 256 x 256 tiles, and when the tile count is not a multiple
- * of the pairs the last wave leaves some pairs idle.  With it, the tiles of
- * the last wave and of the full wave before it are dealt as one run of
- * (tile, 64-deep k-block) units in equal contiguous shares to all pairs.  A
- * tile whose k-blocks span two or more pairs is finished by the pair that
- * holds its first k-block: the others leave fp32 partial accumulators in this
- * scratch, and its epilogue adds them before running.  Only launches whose
- * tiles have at least 16 k-blocks, and whose shares leave at most three other
- * pairs per split tile, are split; grouped launches never are.  Results
- * differ from unsplit runs only in the fp32 summation order of the split
- * tiles, and a split launch is deterministic.
- * coda_split_workspace_bytes: bytes needed (one 256 KB partial per SM pair
- * plus flags).  coda_set_split_workspace: ws (256-byte aligned, at least that
- * many bytes, caller-owned device memory) becomes the handle's scratch; its
- * flags are cleared on `stream`, so set it in stream order before the GEMMs
- * that use it; ws = NULL switches splitting off.  The library allocates
- * nothing.  While it is set, GEMMs issued through the handle must not run
- * concurrently with each other on the GPU (they share the scratch): issue
- * them on one stream, or give each stream its own handle.  Keep ws alive until
- * it is replaced and the GEMMs that used it have completed.  After a call
- * reports CODA_ERR_TIMEOUT, set the workspace again before the next GEMM (the
- * aborted launch may have left flags raised). */
+ * their last, partial wave.  Without it (the default) each SM pair computes
+ * whole 256 x 256 tiles, and when the tile count is not a multiple of the
+ * pairs the last wave leaves some pairs idle.  With it, each tile of that
+ * last wave is cut into S equal k-ranges (2 <= S <= 6, the count that
+ * finishes them in the fewest rounds), and the units are dealt range-major to
+ * all pairs, so the units that run together cover the same k-range.  A unit
+ * of an earlier range leaves its fp32 partial accumulator in this scratch;
+ * the pair that runs the tile's last range adds the partials and runs the
+ * epilogue.  Only launches whose ranges have at least 48 k-blocks are split,
+ * and grouped launches never are.  Results differ from unsplit runs only in
+ * the fp32 summation order of the split tiles, and a split launch is
+ * deterministic.  Measured on the block step's long-K data gradient, it
+ * neither gains nor loses beyond run-to-run noise under the power cap.
+ * coda_split_workspace_bytes: bytes needed (one 256 KB partial per split
+ * tile and earlier range, for the most a launch can need, plus flags; about
+ * 94 MiB on a 152-SM GPU).  coda_set_split_workspace: ws (256-byte aligned,
+ * at least that many bytes, caller-owned device memory) becomes the handle's
+ * scratch; its flags are cleared on `stream`, so set it in stream order
+ * before the GEMMs that use it; ws = NULL switches splitting off.  The
+ * library allocates nothing.  While it is set, GEMMs issued through the
+ * handle must not run concurrently with each other on the GPU (they share the
+ * scratch): issue them on one stream, or give each stream its own handle.
+ * Keep ws alive until it is replaced and the GEMMs that used it have
+ * completed.  After a call reports CODA_ERR_TIMEOUT, set the workspace again
+ * before the next GEMM (the aborted launch may have left flags raised). */
 size_t coda_split_workspace_bytes(coda_handle_t h);
 coda_status_t coda_set_split_workspace(coda_handle_t h, void* ws, size_t ws_bytes, void* stream);
 
