@@ -444,6 +444,28 @@ def bench_block_workload(C, shape, steps, warmup, peaks, device_index, g_on_acti
     return out
 
 
+def host_link_gbs(nbytes: int = 256 << 20, reps: int = 3) -> dict:
+    """Copy bandwidth between page-locked host memory and the device on this
+    box (GB/s, best of `reps`), measured beside the end-to-end figure: the
+    host-buffer step is bound by it once a step's copies outlast its kernels."""
+    host = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    dev = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+    best = {"h2d": 0.0, "d2h": 0.0}
+    with torch.cuda.stream(s):
+        dev.copy_(host, non_blocking=True)
+        for _ in range(reps):
+            for key, (dst, src) in (("h2d", (dev, host)), ("d2h", (host, dev))):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(s)
+                dst.copy_(src, non_blocking=True)
+                e1.record(s)
+                e1.synchronize()
+                best[key] = max(best[key], nbytes / (e0.elapsed_time(e1) * 1e-3) / 1e9)
+    torch.cuda.synchronize()
+    return {k: round(v, 1) for k, v in best.items()}
+
+
 def bench_memory_kernels(C, b, shape, hbm_gbs, warmup=10, iters=50):
     """The memory-bound kernels of the step, each launched alone: warmup
     untimed launches, then iters launches each preceded by a write of a
@@ -875,12 +897,16 @@ def main():
         extras["e2e"] = {"value": aggregate_value(step_flops, e2e_ms, world), "unit": UNIT, "ms_per_step": e2e_ms,
                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                          "steps": n_e2e,
+                         "host_link_gbs": host_link_gbs(),
+                         "h2d_ms_per_step_at_link_rate": None,
                          "api": "coda_block_create / coda_block_step_host / coda_block_sync (host buffers)",
                          "timing": "host wall clock over the whole run, synchronize (and barrier) at both ends; "
                                    "the executor overlaps step i+1's H2D copies and step i-1's D2H read-back "
                                    "with step i's kernels; each step's backward waits for its dY copy, its "
                                    "forward for X and R only; the first step's X / R copy and the last step's "
                                    "D2H overlap nothing; per-rank bytes, value summed over ranks"}
+        link = extras["e2e"]["host_link_gbs"]
+        extras["e2e"]["h2d_ms_per_step_at_link_rate"] = h2d / (link["h2d"] * 1e9) * 1e3 if link["h2d"] else None
         stepper.close()
         del host, stepper
     if not args.no_extras and rank == 0:
