@@ -4,7 +4,7 @@ Bars (bf16 inputs/outputs, fp32 accumulation):
   * elementwise  max |gpu - ref| / (|ref| + 1e-3) <= 2e-2, graded per stage
     against the oracle fed the GPU's own stage inputs.  The 1e-3 floor is
     absolute.  For a few named (test, tensor) pairs whose values are far from
-    unit scale (listed in SCALED_FLOOR with the reason), that fixed floor is
+    unit scale (listed in CUBLAS_RELATIVE with the reason), that fixed floor is
     below what any fp32-accumulating GEMM reaches near zero crossings; there
     the test must show instead that cuBLAS on the same inputs (bf16 GEMM,
     fp32 accumulation) misses the fixed floor about as badly: fixed-floor
@@ -41,6 +41,10 @@ FLOOR = 1e-3
 # come from full-size runs on a GB300.
 _K7 = "7B backward: long-K tensor-core sums (K = 28672 or M = 8192) far from unit scale"
 _K70 = "70B: long-K tensor-core sums (K = 8192 to 57344) far from unit scale"
+# The FP8 step's pairs: the comparator is cuBLASLt's FP8 GEMM (torch._scaled_mm,
+# fp32 output) on the same codes and per-tensor scales
+_F7 = "7B FP8 backward: long-K sums (K = 28672 or M = 8192) of e5m2 x e4m3 codes far from unit scale"
+_F70 = "70B FP8 backward: long-K sums (K = 57344 or M = 4096) of e5m2 x e4m3 codes far from unit scale"
 CUBLAS_RELATIVE = {
     ("test_7b_forward_backward_full_size", "dH"): _K7 + "; 1.21e-1, cuBLAS 1.21e-1",
     ("test_7b_forward_backward_full_size", "dg"): _K7 + "; rms 261, 1.50e-1, cuBLAS 1.50e-1",
@@ -58,6 +62,12 @@ CUBLAS_RELATIVE = {
     ("test_70b_forward_backward_full_size", "dW2t rows"): _K70 + "; rms 84, 2.11e-1, cuBLAS 2.11e-1",
     ("test_70b_forward_backward_full_size", "dW1t rows"): _K70 + "; rms 195, 3.10e-1, cuBLAS 3.10e-1",
     ("test_70b_forward_backward_full_size", "dW1t columns"): _K70 + "; rms 196, 3.33e-1, cuBLAS 3.33e-1",
+    ("test_7b_fp8_forward_backward_full_size", "dH (fp8)"): _F7 + "; 2.63e-2, cuBLASLt 2.63e-2",
+    ("test_7b_fp8_forward_backward_full_size", "dW2t columns (fp8)"): _F7 + "; rms 80, 1.30e-1, cuBLASLt 1.30e-1",
+    ("test_7b_fp8_forward_backward_full_size", "dW2t rows (fp8)"): _F7 + "; rms 79, 3.20e-2, cuBLASLt 3.20e-2",
+    ("test_70b_fp8_forward_backward_full_size", "dH (fp8)"): _F70 + "; 1.27e-1, cuBLASLt 1.27e-1",
+    ("test_70b_fp8_forward_backward_full_size", "dg (fp8)"): _F70 + "; rms 386, 1.07e-1, cuBLASLt 1.16e-1",
+    ("test_70b_fp8_forward_backward_full_size", "dW2t columns (fp8)"): _F70 + "; rms 85, 6.04e-2, cuBLASLt 6.04e-2",
     ("test_split_block_stages_against_oracle", "dH"):
         "split dgrad2, K = 16384; 5.02e-2, cuBLAS 5.23e-2",
     ("test_split_block_stages_against_oracle", "dW2t"):
@@ -68,6 +78,24 @@ CUBLAS_RELATIVE = {
         "row scale 60-120 and silu ~ 100 amplify the accumulator's error near z_up's zero crossings; "
         "rms 6.4e3, 6.15e-2, cuBLAS 6.15e-2",
 }
+
+
+def edge_sample(n, k, seed, tiles=(128, 256), extra=()):
+    """At least k sorted indices in [0, n): the first and last four, both
+    sides of every multiple of the tile sizes within the first two and the
+    last two tiles, any `extra` edges, and random others."""
+    idx = set(range(min(4, n))) | set(range(max(0, n - 4), n))
+    for t in tiles:
+        for e in (t, 2 * t, ((n - 1) // t) * t, ((n - 1) // t - 1) * t):
+            idx |= {e - 2, e - 1, e, e + 1}
+    for e in extra:
+        idx |= {e - 1, e, e + 1}
+    idx = {i for i in idx if 0 <= i < n}
+    r = np.random.default_rng(seed)
+    rest = np.setdiff1d(np.arange(n), np.fromiter(idx, int))
+    need = max(0, k - len(idx))
+    idx |= set(r.choice(rest, size=min(need, rest.size), replace=False).tolist())
+    return np.array(sorted(idx))
 
 
 def f64(t):

@@ -1,13 +1,19 @@
 """FP8 forward and backward at the full workload sizes (7B and 70B blocks),
-in the launch configuration the bench times, on sampled outputs.
+in the launch configuration the bench times, on whole rows and columns.
 
   * scales: the GPU's scale of every quantised tensor equals the oracle's
     fp8_scale of the whole tensor (its amax taken on the host);
-  * codes: sampled rows of every code tensor are bit-exact against the
-    oracle's quantisation with that scale;
-  * GEMM stages: sampled rows / columns of H, z, out, dH, dg, dW2t, dX and
-    dW1t meet the bf16 elementwise bar against the oracle fed the GPU's own
-    codes, dequantised (the products are exact and accumulate in fp32);
+  * codes: at least 256 whole rows of every activation code tensor (first
+    and last row tiles, both sides of the tile edges, random others) and
+    whole rows of the weight codes are bit-exact against the oracle's
+    quantisation with that scale;
+  * GEMM stages against the oracle fed the GPU's own codes, dequantised (the
+    products are exact and accumulate in fp32), at the bf16 elementwise bar:
+    whole rows of H, z, out and dX; every row of dH and all of dg; at least
+    64 whole rows and 64 whole columns of dW2t and dW1t.  Each GEMM output is
+    also computed by cuBLASLt on the same codes and scales (torch._scaled_mm,
+    fp32 result, the epilogue's arithmetic in fp32): the long-K sums named in
+    tests/_parity.py pass when no worse than 1.25x cuBLASLt;
   * end to end on the sampled rows against the oracle chained from the bf16
     inputs: the forward output within the e4m3 bound (Frobenius 8e-2), the
     row-local data gradients dR and dX within 0.15 and 0.2 (the bounds of
@@ -24,18 +30,15 @@ import torch
 
 import oracle as O
 from coda_inputs import B7, B70, block_inputs
-from tests._parity import assert_device_ok, assert_elem, assert_frob, f64
+from tests._parity import assert_device_ok, assert_elem, assert_elem_chunks, assert_frob, edge_sample, f64
 
 pytestmark = pytest.mark.gpu
 
 C = pytest.importorskip("gemm_epilogue_transformer_tma_gb300")
 from gemm_epilogue_transformer_tma_gb300.path import BlockBuffers  # noqa: E402
 
-
-def sample(n, k, seed):
-    r = np.random.default_rng(seed)
-    idx = set(r.choice(n, size=min(k, n), replace=False).tolist()) | {0, n - 1}
-    return np.array(sorted(idx))
+CHUNK = 1024
+E4M3, E5M2 = torch.float8_e4m3fn, torch.float8_e5m2
 
 
 def idx(a):
@@ -52,12 +55,27 @@ def deq(codes, pair, fmt):
 
 
 def check_codes(src_f32, codes, pair, fmt, rows, name):
-    """The scale from the whole tensor, the codes of the sampled rows."""
+    """The scale from the whole tensor, the codes of whole rows."""
     v = src_f32.cpu().numpy()
     s = O.fp8_scale(v, fmt)
     assert scale_of(pair) == s, f"{name}: scale {scale_of(pair)} != {s}"
     got = codes[idx(rows)].cpu().numpy()
     assert np.array_equal(got, O.fp8_quantize(v[rows], s, fmt)), f"{name}: codes"
+
+
+def pad16(ix):
+    """Indices padded (with their first) to a multiple of 16, as cuBLASLt's
+    8-bit GEMM wants; the comparator's extra columns are sliced off."""
+    ix = np.asarray(ix)
+    return np.concatenate([ix, np.full((-len(ix)) % 16, ix[0])])
+
+
+def lt(a_codes, a_fmt, a_pair, b_codes_kn, b_fmt, b_pair):
+    """cuBLASLt: sa * sb * A B in fp32, A [m][k] row-major codes, B given as
+    [k][n] (made column-major here)."""
+    a = a_codes.contiguous().view(a_fmt)
+    b = b_codes_kn.t().contiguous().t().view(b_fmt)
+    return torch._scaled_mm(a, b, a_pair[1], b_pair[1], out_dtype=torch.float32)
 
 
 def check_fp8_block(shape):
@@ -69,62 +87,92 @@ def check_fp8_block(shape):
     torch.cuda.synchronize()
     assert_device_ok()
     M, d, F, K1 = shape.M, shape.d, shape.F, shape.K1
-    rows = sample(M, 10, 11)
-    jcols = sample(F, 16, 12)
-    kcols = sample(d, 16, 13)
-    icols = sample(K1, 16, 14)
-    ncols = np.concatenate([jcols, F + jcols])
+    rows = pad16(edge_sample(M, 256, 11))
+    jcols = edge_sample(F, 32, 12)
+    kcols = pad16(edge_sample(d, 64, 13))
+    icols = pad16(edge_sample(K1, 64, 14))
+    ncols = pad16(np.concatenate([jcols, F + jcols]))
+    ri, ki, ii, ni = idx(rows), idx(kcols), idx(icols), idx(ncols)
+    bf = torch.bfloat16
     g = f64(b.g)
+    gf = b.g.float()
+    sX, sH, sdP, sdH = b.s_a
+    sW1, sW2g, sW2 = b.s_w
 
     # codes and scales (the folded weight quantises fp32(W2t * g))
-    check_codes(b.X.float(), b.Xq, b.s_a[0], "e4m3", rows, "Xq")
-    check_codes(b.H.float(), b.Hq, b.s_a[1], "e4m3", rows, "Hq")
-    check_codes(b.W1t.float(), b.W1q, b.s_w[0], "e4m3", sample(d, 10, 15), "W1q")
-    check_codes(x["W2t"].cpu().float() * x["g"].cpu().float(), b.W2gq, b.s_w[1], "e4m3", ncols, "W2gq")
-    check_codes(b.W2t.float(), b.W2q, b.s_w[2], "e4m3", ncols, "W2q")
-    check_codes(b.dH.float(), b.dHq, b.s_a[3], "e5m2", rows, "dHq")
+    check_codes(b.X.float(), b.Xq, sX, "e4m3", rows, "Xq")
+    check_codes(b.H.float(), b.Hq, sH, "e4m3", rows, "Hq")
+    check_codes(b.W1t.float(), b.W1q, sW1, "e4m3", kcols, "W1q")
+    check_codes(x["W2t"].cpu().float() * x["g"].cpu().float(), b.W2gq, sW2g, "e4m3", ncols, "W2gq")
+    check_codes(b.W2t.float(), b.W2q, sW2, "e4m3", ncols, "W2q")
+    check_codes(b.dH.float(), b.dHq, sdH, "e5m2", rows, "dHq")
     # dP's codes against the bf16 dP the unfused SwiGLU backward writes
     C.coda_swiglu_bwd(b.dY, b.z, b.rstd, b.dP, torch.empty_like(b.c), b.d)
     torch.cuda.synchronize()
-    check_codes(b.dP.float(), b.dPq, b.s_a[2], "e5m2", rows, "dPq")
+    check_codes(b.dP.float(), b.dPq, sdP, "e5m2", rows, "dPq")
 
-    # forward GEMMs on the codes
-    W1 = deq(b.W1q, b.s_w[0], "e4m3")
-    H = f64(b.H[idx(rows)])
-    assert_elem(H, O.gemm_residual(deq(b.Xq[idx(rows)], b.s_a[0], "e4m3"), W1, f64(b.R[idx(rows)])), "H (fp8)")
+    # forward GEMMs on the codes: whole rows
+    W1 = deq(b.W1q, sW1, "e4m3")
+    H = f64(b.H[ri])
+    cub = (lt(b.Xq[ri], E4M3, sX, b.W1q.t(), E4M3, sW1) + b.R[ri].float()).to(bf)
+    assert_elem(H, O.gemm_residual(deq(b.Xq[ri], sX, "e4m3"), W1, f64(b.R[ri])), "H (fp8)", cublas=cub)
+    assert_elem(b.rstd, O.rstd_from_partials(f64(b.psum), d, shape.eps), "rstd", tol=1e-5)
     rstd = f64(b.rstd)[rows]
-    assert_elem(rstd, O.rstd_from_partials(f64(b.psum[idx(rows)]), d, shape.eps), "rstd", tol=1e-5)
-    z_ref = O.rowscale_gemm(deq(b.Hq[idx(rows)], b.s_a[1], "e4m3"), deq(b.W2gq[idx(ncols)], b.s_w[1], "e4m3"), rstd)
-    assert_elem(f64(b.z[idx(rows)])[:, ncols], z_ref, "z (fp8)")
-    assert_elem(f64(b.out[idx(rows)])[:, jcols], O.swiglu(z_ref), "out (fp8)")
+    z_ref = O.rowscale_gemm(deq(b.Hq[ri], sH, "e4m3"), deq(b.W2gq, sW2g, "e4m3"), rstd)
+    z32 = b.rstd[ri, None] * lt(b.Hq[ri], E4M3, sH, b.W2gq.t(), E4M3, sW2g)
+    assert_elem(f64(b.z[ri]), z_ref, "z (fp8)", cublas=z32.to(bf))
+    zg, zu = z32[:, :F], z32[:, F:]
+    assert_elem(f64(b.out[ri]), O.swiglu(z_ref), "out (fp8)", cublas=(zg * torch.sigmoid(zg) * zu).to(bf))
+    del z_ref, z32, zg, zu
     # the forward output end to end, from the bf16 inputs
-    full = O.block_forward(f64(b.X[idx(rows)]), f64(b.W1t), f64(b.R[idx(rows)]), g, f64(b.W2t[idx(ncols)]),
-                           shape.eps, True)
-    assert_frob(f64(b.out[idx(rows)])[:, jcols], full["out"], "out fp8 e2e", tol=8e-2)
+    full = O.block_forward(f64(b.X[ri]), f64(b.W1t), f64(b.R[ri]), g, f64(b.W2t), shape.eps, True)
+    assert_frob(f64(b.out[ri]), full["out"], "out fp8 e2e", tol=8e-2)
+    del full
 
-    # backward GEMMs on the codes
-    W2k = deq(b.W2q[:, idx(kcols)], b.s_w[2], "e4m3")
-    dg = np.zeros(len(kcols))
-    for s0 in range(0, M, 1024):
-        e = min(M, s0 + 1024)
-        _, part = O.stage_dgrad2_rmsbwd(deq(b.dPq[s0:e], b.s_a[2], "e5m2"), W2k, g[kcols],
-                                        f64(b.H[s0:e])[:, kcols], f64(b.c[s0:e]))
+    # dgrad2 + RMSNorm backward: every row of dH, all of dg
+    W2 = deq(b.W2q, sW2, "e4m3")
+    Hall = f64(b.H)
+    c_all = f64(b.c)
+    dg = np.zeros(d)
+    dg_cub = np.zeros(d)
+    parts = []
+    for s0 in range(0, M, CHUNK):
+        e = min(M, s0 + CHUNK)
+        dh, part = O.stage_dgrad2_rmsbwd(deq(b.dPq[s0:e], sdP, "e5m2"), W2, g, Hall[s0:e], c_all[s0:e])
         dg += part
-    dh_ref, _ = O.stage_dgrad2_rmsbwd(deq(b.dPq[idx(rows)], b.s_a[2], "e5m2"), W2k, g[kcols],
-                                      f64(b.H[idx(rows)])[:, kcols], f64(b.c)[rows])
-    assert_elem(f64(b.dH[idx(rows)])[:, kcols], dh_ref, "dH (fp8)")
-    assert_elem(f64(b.dg)[kcols], dg, "dg (fp8)")
-    dW2_ref = O.stage_wgrad2(deq(b.Hq[:, idx(kcols)], b.s_a[1], "e4m3"), deq(b.dPq[:, idx(ncols)], b.s_a[2], "e5m2"),
-                             g[kcols])
-    assert_elem(f64(b.dW2t[idx(ncols)])[:, kcols], dW2_ref, "dW2t (fp8)")
-    assert_elem(f64(b.dX[idx(rows)]), O.stage_dgrad1(deq(b.dHq[idx(rows)], b.s_a[3], "e5m2"), W1), "dX (fp8)")
-    dW1_ref = O.stage_wgrad1(deq(b.dHq[:, idx(kcols)], b.s_a[3], "e5m2"), deq(b.Xq[:, idx(icols)], b.s_a[0], "e4m3"))
-    assert_elem(f64(b.dW1t[idx(kcols)])[:, icols], dW1_ref, "dW1t (fp8)")
+        acc = lt(b.dPq[s0:e], E5M2, sdP, b.W2q, E4M3, sW2)
+        dg_cub += f64((acc * b.H[s0:e].float()).sum(0))
+        parts.append((b.dH[s0:e], dh, (gf * acc - b.c[s0:e, None] * b.H[s0:e].float()).to(bf)))
+        del acc
+    assert_elem_chunks(parts, "dH (fp8)")
+    del parts, W2
+    assert_elem(b.dg, dg, "dg (fp8)", cublas=dg_cub)
+    # wgrad2: whole columns (fixed k) and whole rows (fixed n) of dW2t
+    dP_all = deq(b.dPq, sdP, "e5m2")
+    Hq_all = deq(b.Hq, sH, "e4m3")
+    dPqT = b.dPq.t().contiguous()
+    cub = (lt(dPqT, E5M2, sdP, b.Hq[:, ki], E4M3, sH) * gf[ki]).to(bf)
+    assert_elem(f64(b.dW2t[:, ki]), O.stage_wgrad2(Hq_all[:, kcols], dP_all, g[kcols]), "dW2t columns (fp8)",
+                cublas=cub)
+    cub = (lt(dPqT[ni], E5M2, sdP, b.Hq, E4M3, sH) * gf).to(bf)
+    assert_elem(f64(b.dW2t[ni]), O.stage_wgrad2(Hq_all, dP_all[:, ncols], g), "dW2t rows (fp8)", cublas=cub)
+    del dP_all, dPqT, cub
+    # dgrad1 (whole rows) and wgrad1 (whole rows and columns of dW1t)
+    dHq_rows = deq(b.dHq[ri], sdH, "e5m2")
+    assert_elem(f64(b.dX[ri]), O.stage_dgrad1(dHq_rows, W1), "dX (fp8)",
+                cublas=lt(b.dHq[ri], E5M2, sdH, b.W1q, E4M3, sW1).to(bf))
+    dH_all = deq(b.dHq, sdH, "e5m2")
+    X_all = deq(b.Xq, sX, "e4m3")
+    dHqT = b.dHq.t().contiguous()
+    assert_elem(f64(b.dW1t[ki]), O.stage_wgrad1(dH_all[:, kcols], X_all), "dW1t rows (fp8)",
+                cublas=lt(dHqT[ki], E5M2, sdH, b.Xq, E4M3, sX).to(bf))
+    assert_elem(f64(b.dW1t[:, ii]), O.stage_wgrad1(dH_all, X_all[:, icols]), "dW1t columns (fp8)",
+                cublas=lt(dHqT, E5M2, sdH, b.Xq[:, ii], E4M3, sX).to(bf))
+    del dH_all, X_all, dHqT, Hq_all
     # the data gradients end to end: a row's dR and dX depend on that row alone
-    ref = O.block_backward(f64(b.X[idx(rows)]), f64(b.W1t), f64(b.R[idx(rows)]), g, f64(b.W2t),
-                           f64(b.dY[idx(rows)]), shape.eps, True)
-    assert_frob(f64(b.dH[idx(rows)]), ref["dR"], "dR fp8 e2e", tol=0.15)
-    assert_frob(f64(b.dX[idx(rows)]), ref["dX"], "dX fp8 e2e", tol=0.2)
+    ref = O.block_backward(f64(b.X[ri]), f64(b.W1t), f64(b.R[ri]), g, f64(b.W2t), f64(b.dY[ri]), shape.eps, True)
+    assert_frob(f64(b.dH[ri]), ref["dR"], "dR fp8 e2e", tol=0.15)
+    assert_frob(f64(b.dX[ri]), ref["dX"], "dX fp8 e2e", tol=0.2)
 
 
 def test_7b_fp8_forward_backward_full_size():

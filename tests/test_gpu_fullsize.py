@@ -22,7 +22,7 @@ import torch
 import oracle as O
 from coda_inputs import B1, B7, B70, LMHEAD, block_inputs, ce_inputs
 from tests._ce import check_argmax, check_label_rows, edge_labels, known_answer_ce
-from tests._parity import assert_device_ok, assert_elem, assert_elem_chunks, assert_frob, f64
+from tests._parity import assert_device_ok, assert_elem, assert_elem_chunks, assert_frob, edge_sample, f64
 
 pytestmark = pytest.mark.gpu
 
@@ -30,24 +30,6 @@ C = pytest.importorskip("gemm_epilogue_transformer_tma_gb300")
 from gemm_epilogue_transformer_tma_gb300.path import BlockBuffers  # noqa: E402
 
 CHUNK = 1024  # rows per oracle block for the whole-tensor passes
-
-
-def edge_sample(n, k, seed, tiles=(128, 256), extra=()):
-    """At least k sorted indices in [0, n): the first and last four, both
-    sides of every multiple of the tile sizes within the first two and the
-    last two tiles, any `extra` edges, and random others."""
-    idx = set(range(min(4, n))) | set(range(max(0, n - 4), n))
-    for t in tiles:
-        for e in (t, 2 * t, ((n - 1) // t) * t, ((n - 1) // t - 1) * t):
-            idx |= {e - 2, e - 1, e, e + 1}
-    for e in extra:
-        idx |= {e - 1, e, e + 1}
-    idx = {i for i in idx if 0 <= i < n}
-    r = np.random.default_rng(seed)
-    rest = np.setdiff1d(np.arange(n), np.fromiter(idx, int))
-    need = max(0, k - len(idx))
-    idx |= set(r.choice(rest, size=min(need, rest.size), replace=False).tolist())
-    return np.array(sorted(idx))
 
 
 def rows_of(t, idx):
