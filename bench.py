@@ -652,6 +652,20 @@ def bench_qkv_rope(C, steps, warmup, M=8192, S=2048, d=4096, n_heads=32):
                                                    "per-round time ratio"}
 
 
+def _vs_library(ours, lib, lib_name, flops, n, warmup, rounds=4):
+    """The library's GEMM against a vendor library's on the same operands:
+    rounds of n launches each, the order reversed every other round (the part
+    heats over a run).  Medians over rounds; ratio = median per-round time
+    ratio (vendor / ours, above 1 when ours is faster)."""
+    t_o, t_l = interleave_many([ours, lib], n, warmup, rounds=rounds)
+    mo, ml = statistics.median(t_o), statistics.median(t_l)
+    return {"coda_ms": mo, f"{lib_name}_ms": ml, "coda_tflops": flops / mo / 1e9,
+            f"{lib_name}_tflops": flops / ml / 1e9,
+            "ratio": statistics.median(b / a for a, b in zip(t_o, t_l)),
+            "rounds_ms": rounds_ms(zip(t_o, t_l)),
+            "timing": "rounds of n launches, order alternating; medians over rounds"}
+
+
 def bench_plain_vs_cublas(C, shape, steps, warmup):
     """The library's plain GEMM (K-major operands, bf16 store, no epilogue
     work) against cuBLAS (torch.matmul) on the GEMM shapes of the step, same
@@ -667,14 +681,7 @@ def bench_plain_vs_cublas(C, shape, steps, warmup):
         Cd = torch.empty(M, N, device="cuda", dtype=torch.bfloat16)
         ours = [lambda: C.coda_gemm(A, False, B, False, Cd, M, N, K)]
         lib = [lambda: torch.matmul(A, B.t(), out=Cd)]
-        t_o, t_l = [], []
-        for _ in range(2):
-            t_o.append(time_steps(ours, n, warmup, stage_events=False)[0] / n)
-            t_l.append(time_steps(lib, n, warmup, stage_events=False)[0] / n)
-        fl = 2.0 * M * N * K
-        out[name] = {"M": M, "N": N, "K": K, "coda_ms": min(t_o), "cublas_ms": min(t_l),
-                     "coda_tflops": fl / min(t_o) / 1e9, "cublas_tflops": fl / min(t_l) / 1e9,
-                     "ratio": min(t_l) / min(t_o)}
+        out[name] = {"M": M, "N": N, "K": K, **_vs_library(ours, lib, "cublas", 2.0 * M * N * K, n, warmup)}
         del A, B, Cd
         torch.cuda.empty_cache()
     return out
@@ -702,14 +709,7 @@ def bench_fp8_plain_vs_cublaslt(C, shape, steps, warmup):
         except Exception as e:  # noqa: BLE001 - report, do not fail the bench
             return {"unavailable": f"torch._scaled_mm: {str(e).splitlines()[0][:160]}"}
         lib = [lambda: torch._scaled_mm(A, B.t(), one, one, out_dtype=torch.bfloat16)]
-        t_o, t_l = [], []
-        for _ in range(2):
-            t_o.append(time_steps(ours, n, warmup, stage_events=False)[0] / n)
-            t_l.append(time_steps(lib, n, warmup, stage_events=False)[0] / n)
-        fl = 2.0 * M * N * K
-        out[name] = {"M": M, "N": N, "K": K, "coda_ms": min(t_o), "cublaslt_ms": min(t_l),
-                     "coda_tflops": fl / min(t_o) / 1e9, "cublaslt_tflops": fl / min(t_l) / 1e9,
-                     "ratio": min(t_l) / min(t_o)}
+        out[name] = {"M": M, "N": N, "K": K, **_vs_library(ours, lib, "cublaslt", 2.0 * M * N * K, n, warmup)}
         del A, B, Au, Bu, Cd
         torch.cuda.empty_cache()
     return out
