@@ -428,6 +428,14 @@ __global__ void __launch_bounds__(gemm_threads<Epi>(), 1)
 // epilogue helpers: 32-column row segments, groups of 8 bf16 (16 bytes);
 // every extent on the boundary is a multiple of 8 so groups are all-or-none.
 // ---------------------------------------------------------------------------
+// 32 bf16 of a row from column n0 as raw vectors, zero past nvalid: issued
+// one chunk ahead of their use, unpacked with unpack_bf16x8 when needed.
+__device__ __forceinline__ void load_bf16x32_raw(const __nv_bfloat16* row, int n0, int nvalid, uint4 (&q)[4]) {
+#pragma unroll
+  for (int g = 0; g < 4; ++g)
+    q[g] = g * 8 < nvalid ? __ldg(reinterpret_cast<const uint4*>(row + n0 + g * 8)) : make_uint4(0u, 0u, 0u, 0u);
+}
+
 __device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* p, int nvalid, float (&f)[32]) {
 #pragma unroll
   for (int g = 0; g < 4; ++g) {
@@ -562,7 +570,7 @@ __device__ __forceinline__ float rstd_from_psum(const float* psum, int T, float 
 // C = bf16(row_scale[m] * col_scale[n] * acc); both scales optional.
 struct EpiStore {
   static constexpr int kEpiWarps = 4;
-  static constexpr int kStoreSlots = 1;
+  static constexpr int kStoreSlots = 2;  // two slots used alternately
   static constexpr bool kAccScale = true;  // multiplies by EpiCtx::acc_scale: usable on FP8 operands
   struct Params {
     CUtensorMap out;  // [M][N] bf16
@@ -600,11 +608,12 @@ struct EpiStore {
         }
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] *= rs;
-        slots_acquire(c.lane);
-        stage_bf16x32(slot_addr(c, 0), c.lane, v);
+        const int slot = ((cc - c.c0) >> 5) & 1;
+        slots_acquire_db(c.lane, cc == c.c0);
+        stage_bf16x32(slot_addr(c, slot), c.lane, v);
         slots_publish();
         if (c.lane == 0) {
-          tma_store_2d(&p.out, slot_addr(c, 0), n0, c.m0);
+          tma_store_2d(&p.out, slot_addr(c, slot), n0, c.m0);
           bulk_commit_group();
         }
       }
@@ -671,12 +680,6 @@ struct EpiResPrms {
     const __nv_bfloat16* row = p.R + static_cast<int64_t>(m) * p.ldr;
     for (int n = n0; n < n0 + bn && n < N; n += 64) prefetch_l2(row + n);
   }
-  // the residual's 32 columns from n0 as raw bf16 vectors (zero past nvalid)
-  static __device__ __forceinline__ void load_r(const __nv_bfloat16* row, int n0, int nvalid, uint4 (&q)[4]) {
-#pragma unroll
-    for (int g = 0; g < 4; ++g)
-      q[g] = g * 8 < nvalid ? __ldg(reinterpret_cast<const uint4*>(row + n0 + g * 8)) : make_uint4(0u, 0u, 0u, 0u);
-  }
   template <int BN>
   static __device__ __forceinline__ void run(const Params& p, const EpiCtx& c) {
     const bool row_ok = c.m < c.M;
@@ -686,7 +689,7 @@ struct EpiResPrms {
     float ss = 0.f;
     // the residual is loaded one chunk ahead of its use
     uint4 rq[4];
-    load_r(rrow, nb + c.c0, row_ok ? c.N - nb - c.c0 : 0, rq);
+    load_bf16x32_raw(rrow, nb + c.c0, row_ok ? c.N - nb - c.c0 : 0, rq);
 #pragma unroll 1
     for (int cc = c.c0; cc < c.c1; cc += 32) {
       float v[32];
@@ -695,7 +698,7 @@ struct EpiResPrms {
       float r[32];
 #pragma unroll
       for (int g = 0; g < 4; ++g) unpack_bf16x8(rq[g], &r[g * 8]);
-      if (cc + 32 < c.c1) load_r(rrow, n0 + 32, row_ok ? c.N - n0 - 32 : 0, rq);
+      if (cc + 32 < c.c1) load_bf16x32_raw(rrow, n0 + 32, row_ok ? c.N - n0 - 32 : 0, rq);
       if (n0 < c.N && c.m0 < c.M) {
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
@@ -795,7 +798,7 @@ struct EpiRowscaleSwiglu {
 //   sum over the warp's 32 rows of acc * h  (block reduction across lanes).
 struct EpiDgradRms {
   static constexpr int kEpiWarps = 4;
-  static constexpr int kStoreSlots = 1;
+  static constexpr int kStoreSlots = 2;  // dH chunks, two slots used alternately
   static constexpr bool kAccScale = true;  // multiplies by EpiCtx::acc_scale: usable on FP8 operands
   struct Params {
     CUtensorMap dH;  // [M][d] bf16
@@ -811,9 +814,20 @@ struct EpiDgradRms {
     const float* rstd;
     float inv_d;
   };
+  // the row's segment of h for the tile, line by line, into L2
+  static __device__ __forceinline__ void prefetch(const Params& p, int M, int N, int m, int n0, int bn) {
+    if (m >= M) return;
+    const __nv_bfloat16* row = p.H + static_cast<int64_t>(m) * p.ldh;
+    for (int n = n0; n < n0 + bn && n < N; n += 64) prefetch_l2(row + n);
+  }
   template <int BN>
   static __device__ __forceinline__ void run(const Params& p, const EpiCtx& c) {
     const bool row_ok = c.m < c.M;
+    const __nv_bfloat16* hrow = p.H + static_cast<int64_t>(c.m) * p.ldh;
+    const int nb = c.tn * BN;
+    // h is loaded one chunk ahead of its use
+    uint4 hq[4];
+    load_bf16x32_raw(hrow, nb + c.c0, row_ok ? c.N - nb - c.c0 : 0, hq);
     float cm = 0.f;
     if (row_ok) {
       if (p.cpart != nullptr) {
@@ -830,23 +844,27 @@ struct EpiDgradRms {
     for (int cc = c.c0; cc < c.c1; cc += 32) {
       float a[32];
       acc_ld32(c, cc, a);
-      const int n0 = c.tn * BN + cc;
+      const int n0 = nb + cc;
+      float h[32];
+#pragma unroll
+      for (int g = 0; g < 4; ++g) unpack_bf16x8(hq[g], &h[g * 8]);
+      if (cc + 32 < c.c1) load_bf16x32_raw(hrow, n0 + 32, row_ok ? c.N - n0 - 32 : 0, hq);
       if (n0 < c.N) {
         // FP8 operands: dequantise the accumulator (acc_scale = 1 for bf16)
 #pragma unroll
         for (int i = 0; i < 32; ++i) a[i] *= c.acc_scale;
-        float h[32], gv[32];
-        load_bf16x32(p.H + static_cast<int64_t>(c.m) * p.ldh + n0, row_ok ? c.N - n0 : 0, h);
+        float gv[32];
         load_bf16x32(p.g + n0, c.N - n0, gv);
         if (c.m0 < c.M) {
           float dh[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) dh[i] = fmaf(gv[i], a[i], -cm * h[i]);
-          slots_acquire(c.lane);
-          stage_bf16x32(slot_addr(c, 0), c.lane, dh);
+          const int slot = ((cc - c.c0) >> 5) & 1;
+          slots_acquire_db(c.lane, cc == c.c0);
+          stage_bf16x32(slot_addr(c, slot), c.lane, dh);
           slots_publish();
           if (c.lane == 0) {
-            tma_store_2d(&p.dH, slot_addr(c, 0), n0, c.m0);
+            tma_store_2d(&p.dH, slot_addr(c, slot), n0, c.m0);
             bulk_commit_group();
           }
         }

@@ -188,8 +188,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi>(),
   const float acc_scale = acc_scale_of(ctl);
   const uint32_t idesc = FP8 ? (IDESC0 | ctl.f8_fmt) : IDESC0;
 
-  const int num_tiles = sh.tiles_m * sh.tiles_n;
-
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA
     if (lane == 0) {
