@@ -43,7 +43,7 @@ UNIT = "TFLOP/s"
 CONFIGS = {"7b": B7, "70b": B70, "1b": B1}  # 1b: forward only
 
 
-KERNEL_SOURCES = ["ptx.cuh", "gemm_tc.cuh", "gemm_tc2.cuh", "gemm_group.cuh", "gemm_launch.cuh", "gemm_fwd.cu",
+KERNEL_SOURCES = ["ptx.cuh", "gemm_tc.cuh", "gemm_tc2.cuh", "gemm_tc2w.cuh", "gemm_group.cuh", "gemm_launch.cuh", "gemm_fwd.cu",
                   "gemm_bwd.cu", "gemm_group.cu"]
 
 
@@ -773,6 +773,8 @@ def main():
                     help="apply the RMSNorm weight in GEMM1's epilogue (Hg) instead of folding it into W2")
     ap.add_argument("--single-sm", action="store_true",
                     help="GEMMs on one SM per tile instead of SM pairs")
+    ap.add_argument("--wide-tiles", type=int, default=0, metavar="J",
+                    help="256 x 512 pair tiles with lead J for the long-K backward GEMMs (coda_set_wide_tiles)")
     ap.add_argument("--tokens", type=int, default=0,
                     help="override the token count M (smaller cases for profiler captures)")
     ap.add_argument("--leg", default="", choices=["", "lmhead", "fp8"],
@@ -819,6 +821,7 @@ def main():
     from gemm_epilogue_transformer_tma_gb300.path import BlockBuffers, HostBlockStepper
     peaks = load_peaks()
     C.coda_set_sm_pairing(not args.single_sm)
+    C.coda_set_wide_tiles(args.wide_tiles)
 
     x = block_inputs(shape, seed=rank, device="cuda")
     b = BlockBuffers(x, backward=shape.backward, fuse_rstd=args.fuse_rstd, g_on_activation=args.g_on_activation)
@@ -987,7 +990,9 @@ def main():
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1)/N(0,0.02)/U(0.5,1.5))",
             "config": {"workload": shape.name, "M": shape.M, "K1": shape.K1, "d": shape.d, "ffn": shape.N2 // 2,
                        "eps": shape.eps, "parallelism": "replicas" if world > 1 else "single-gpu",
-                       "gemm": "1-SM tiles" if args.single_sm else "SM-pair tiles",
+                       "gemm": "1-SM tiles" if args.single_sm else (
+                           f"SM-pair tiles, 256 x 512 on the long-K backward GEMMs (lead {args.wide_tiles})"
+                           if args.wide_tiles else "SM-pair tiles"),
                        "rstd": "in GEMM2's epilogue" if args.fuse_rstd else "separate combine kernel",
                        "g": "on the activation (GEMM1 epilogue)" if args.g_on_activation else "folded into W2",
                        "l2": "inputs larger than L2 (W2 alone is %d MB), no flush" % (shape.N2 * shape.d * 2 >> 20)},

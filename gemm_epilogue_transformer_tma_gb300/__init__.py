@@ -57,7 +57,10 @@ SIGNATURES = {
     "coda_debug_split_schedule_violations": (_INT, [_INT, _INT, _INT]),
     "coda_debug_split_first_tile": (_INT, [_INT, _INT, _INT]),
     "coda_debug_split_ranges": (_INT, [_INT, _INT, _INT]),
+    "coda_debug_wide_schedule_violations": (_INT, [_INT, _INT, _INT, _INT, _INT]),
+    "coda_debug_wide_applies": (_INT, [_P, _INT, _INT, _INT]),
     "coda_set_sm_pairing": (_INT, [_P, _INT]),
+    "coda_set_wide_tiles": (_INT, [_P, _INT]),
     "coda_split_workspace_bytes": (_SZ, [_P]),
     "coda_set_split_workspace": (_INT, [_P, _P, _SZ, _P]),
     "coda_prms_num_tiles": (_I64, [_I64]),
@@ -203,6 +206,12 @@ def coda_set_wait_timeout_ns(ns: int, device: int | None = None):
 def coda_set_sm_pairing(enable: bool, device: int | None = None):
     """GEMMs on SM pairs (2-SM MMA, default) or one SM per tile."""
     _check(load_library().coda_set_sm_pairing(handle(device), int(enable)), "coda_set_sm_pairing")
+
+
+def coda_set_wide_tiles(lead_kblocks: int, device: int | None = None):
+    """256 x 512 pair tiles for the long-K backward GEMMs with lead J =
+    lead_kblocks k-blocks; 0 turns them off (see include/coda.h)."""
+    _check(load_library().coda_set_wide_tiles(handle(device), int(lead_kblocks)), "coda_set_wide_tiles")
 
 
 def coda_split_workspace_bytes(device: int | None = None) -> int:
@@ -443,6 +452,17 @@ def coda_debug_split_first_tile(tiles: int, num_kb: int, clusters: int) -> int:
 def coda_debug_split_ranges(tiles: int, num_kb: int, clusters: int) -> int:
     """k-ranges per split tile the launcher would choose, 1 if none (see include/coda_testing.h)."""
     return load_library().coda_debug_split_ranges(tiles, num_kb, clusters)
+
+
+def coda_debug_wide_schedule_violations(M: int, N: int, K: int, clusters: int, lead: int) -> int:
+    """Host-side check of the wide-tile schedule (see include/coda_testing.h)."""
+    return load_library().coda_debug_wide_schedule_violations(M, N, K, clusters, lead)
+
+
+def coda_debug_wide_applies(M: int, N: int, K: int, device: int | None = None) -> int:
+    """1 if a long-K backward GEMM of this size would take wide tiles on the
+    device's handle now (see include/coda_testing.h)."""
+    return load_library().coda_debug_wide_applies(handle(device), M, N, K)
 
 
 def coda_bwd_workspace_bytes(M: int, d: int, N2: int) -> int:

@@ -25,6 +25,7 @@ struct coda_handle_s {
   void* noalloc_scratch;  // device address of the allocation-free call's scratch, looked up on its first use
   float* sk_parts;        // split-tile scratch (coda_set_split_workspace), or null
   int* sk_flags;
+  int wide_lead;          // wide pair tiles for long-K GEMMs (coda_set_wide_tiles): lead J, 0 = off
 };
 
 namespace coda {
@@ -61,6 +62,7 @@ LaunchCtx ctx_of(coda_handle_t h, void* stream) {
   c.sk_parts = h->sk_parts;
   c.sk_flags = h->sk_flags;
   c.sk_slots = split_scratch_slots(h->num_sms);
+  c.wide_lead = h->wide_lead;
   return c;
 }
 
@@ -225,6 +227,7 @@ coda_status_t coda_create(coda_handle_t* out, int device) {
   h->noalloc_scratch = nullptr;
   h->sk_parts = nullptr;
   h->sk_flags = nullptr;
+  h->wide_lead = 0;
   coda_status_t st = CODA_OK;
   if (cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
       cudaMalloc(&h->status, sizeof(int)) != cudaSuccess || cudaMemset(h->status, 0, sizeof(int)) != cudaSuccess)
@@ -285,6 +288,18 @@ coda_status_t coda_set_sm_pairing(coda_handle_t h, int enable) {
   CODA_TRY(Check().handle(h).st);
   h->pair = enable != 0;
   return CODA_OK;
+}
+
+coda_status_t coda_set_wide_tiles(coda_handle_t h, int lead_kblocks) {
+  CODA_TRY(Check().handle(h).st);
+  if (lead_kblocks < 0 || lead_kblocks > 64) return CODA_ERR_INVALID_ARG;
+  h->wide_lead = lead_kblocks;
+  return CODA_OK;
+}
+
+int coda_debug_wide_applies(coda_handle_t h, int M, int N, int K) {
+  if (h == nullptr || M < 1 || N < 1 || K < 1) return -1;
+  return wide_tiles_fit(ctx_of(h, nullptr), K, (N + 255) / 256) ? 1 : 0;
 }
 
 size_t coda_split_workspace_bytes(coda_handle_t h) {

@@ -24,7 +24,21 @@ struct LaunchCtx {
   float* sk_parts;       // split-tile scratch (coda_set_split_workspace), or null: no tile is split
   int* sk_flags;
   int sk_slots;          // clusters the scratch has slots for
+  int wide_lead;         // > 0: long-K launches take 256 x 512 pair tiles with this lead J (coda_set_wide_tiles)
 };
+
+// Whether a bf16 GEMM over K with tiles_n 256-column output tiles takes the
+// wide-tile pair kernel: the handle asks for it (a lead J > 0), the pair
+// kernel is on, the column tiles pair up, and K is long: at least
+// kWideMinKb k-blocks of 64 (K >= 16384), and enough that the 2J single-half
+// k-blocks of a tile are at most a quarter of its 2 nkb half k-blocks.  Only
+// the long-K backward programs are compiled for it.  Each tile boundary
+// exposes part of an accumulator half's drain, so short-K GEMMs, with many
+// tiles per SM pair, lose more there than the smaller operand traffic gains:
+// measured, the 7B / 70B weight gradient (K = 8192 / 4096) ran 1-9 % slower
+// on wide tiles and the data gradient (K = 28672 / 57344) 3 % faster.
+constexpr int kWideMinKb = 256;
+bool wide_tiles_fit(const LaunchCtx& c, int K, int tiles_n);
 
 // 2-D bf16 tensor map with 128-byte swizzle.  The tensor is `outer` rows of
 // `inner` contiguous elements with a row pitch of `ld` elements; the box is

@@ -97,6 +97,11 @@ cudaError_t gemm_store_f32(const LaunchCtx& c, const __nv_bfloat16* A, bool a_mn
 
 }  // namespace coda
 
+bool coda::wide_tiles_fit(const LaunchCtx& c, int K, int tiles_n) {
+  const int nkb = (K + BK - 1) / BK;
+  return c.pair && c.wide_lead > 0 && tiles_n % 2 == 0 && nkb >= 4 * c.wide_lead && nkb >= kWideMinKb;
+}
+
 int coda::split_scratch_slots(int num_sms) { return (num_sms / 2 - 1) * (kSplitMaxRanges - 1); }
 
 // Host-side check of the split-tile schedule of the SM-pair kernel, run with
@@ -182,4 +187,72 @@ extern "C" int coda_debug_split_first_tile(int tiles, int num_kb, int clusters) 
 extern "C" int coda_debug_split_ranges(int tiles, int num_kb, int clusters) {
   if (tiles < 1 || num_kb < 1 || clusters < 1) return -1;
   return coda::split_plan(tiles, num_kb, clusters, (clusters - 1) * (coda::kSplitMaxRanges - 1)).ranges;
+}
+
+// Host-side check of the wide-tile schedule of the SM-pair kernel, run with
+// the kernel's own iterators (coda_debug_wide_schedule_violations in
+// include/coda_testing.h).
+extern "C" int coda_debug_wide_schedule_violations(int M, int N, int K, int clusters, int lead) {
+  using namespace coda;
+  if (M < 1 || N < 1 || K < 1 || clusters < 1 || lead < 0) return -1;
+  GemmShape sh{};
+  sh.M = M;
+  sh.N = N;
+  sh.K = K;
+  sh.tiles_m = (M + BM2 - 1) / BM2;
+  sh.tiles_n = (N + 255) / 256;
+  if (sh.tiles_n % 2 != 0) return -1;  // the launcher takes wide tiles only for an even count
+  sh.num_kb = (K + BK - 1) / BK;
+  sh.group_m = 8;
+  sh.w_lead = lead;
+  const int tiles_w = sh.tiles_m * sh.tiles_n / 2;
+  sh.w_single_from = wide_single_from(tiles_w, clusters);
+  int bad = 0;
+  std::vector<int> cover(static_cast<size_t>(sh.tiles_m) * sh.tiles_n, 0);
+  std::vector<int> kcover(static_cast<size_t>(sh.num_kb));
+  for (int cid = 0; cid < clusters; ++cid) {
+    WideWork wk(sh, cid, clusters);
+    WideUnit u;
+    bool single_seen = false;
+    while (wk.next(u)) {
+      if (u.tm < 0 || u.tm >= sh.tiles_m || u.tv < 0 || u.tv + (u.wide ? 1 : 0) >= sh.tiles_n) {
+        ++bad;
+        continue;
+      }
+      // wide units first (the producer switches rings once), on even columns
+      if (u.wide && (single_seen || u.tv % 2 != 0)) ++bad;
+      if (!u.wide) single_seen = true;
+      for (int j = 0; j < (u.wide ? 2 : 1); ++j) cover[static_cast<size_t>(u.tm) * sh.tiles_n + u.tv + j]++;
+      // each half sees every k-block exactly once; its first block starts
+      // the sum and its last block is where the kernel commits it
+      const WidePhases ph(u, sh.num_kb, sh.w_lead);
+      for (int h = 0; h < (u.wide ? 2 : 1); ++h) {
+        std::fill(kcover.begin(), kcover.end(), 0);
+        int first = -1, last = -1;
+        for (int i = 0; i < ph.nblocks; ++i) {
+          int kb;
+          bool f0, f1;
+          ph.block(i, kb, f0, f1);
+          if (kb < 0 || kb >= sh.num_kb) {
+            ++bad;
+            continue;
+          }
+          if (!u.wide && f1) ++bad;  // a half tile feeds one half only
+          if (h == 0 ? f0 : f1) {
+            kcover[kb]++;
+            if (first < 0) first = i;
+            last = i;
+          }
+        }
+        for (int v : kcover)
+          if (v != 1) ++bad;
+        if (first != (h == 0 ? 0 : ph.first_h1())) ++bad;
+        if (last != (h == 0 ? ph.last_h0() : ph.last_h1())) ++bad;
+      }
+      if (u.wide && ph.J != (lead < sh.num_kb / 2 ? lead : sh.num_kb / 2)) ++bad;
+    }
+  }
+  for (int v : cover)
+    if (v != 1) ++bad;
+  return bad;
 }

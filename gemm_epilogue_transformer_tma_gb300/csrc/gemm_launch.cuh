@@ -7,6 +7,7 @@
 #include "coda_internal.h"
 #include "gemm_tc.cuh"
 #include "gemm_tc2.cuh"
+#include "gemm_tc2w.cuh"
 
 namespace coda {
 
@@ -145,11 +146,70 @@ cudaError_t launch_gemm2_kernel(const LaunchCtx& c, const CUtensorMap& ta, const
   return launch_chained(c, kern, dim3(2 * clusters), dim3(gemm_threads<Epi>()), L::TOTAL, ta, tb, tb2, sh, ctl, ep);
 }
 
+// The wide-tile pair kernel (256 x 512 tiles, gemm_tc2w.cuh) on a persistent
+// grid of all co-resident SM pairs.  tiles_n counts 256-column tiles and must
+// be even.  When the last wave holds at most half as many wide tiles as there
+// are pairs, its tiles run as 256-column halves.
+template <bool A_MN, bool B_MN, class Epi>
+cudaError_t launch_gemm2w_kernel(const LaunchCtx& c, const CUtensorMap& ta, const CUtensorMap& tb, int M, int N,
+                                 int K, int tiles_n, const typename Epi::Params& ep) {
+  constexpr int STAGES = 4;
+  using L = Gemm2wSmem<STAGES, epi_stage_bytes<Epi>()>;
+  auto kern = gemm_tc2w_kernel<STAGES, A_MN, B_MN, Epi>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL);
+  if (e != cudaSuccess) return e;
+  GemmShape sh;
+  sh.M = M;
+  sh.N = N;
+  sh.K = K;
+  sh.tiles_m = (M + BM2 - 1) / BM2;
+  sh.tiles_n = tiles_n;
+  sh.num_kb = (K + BK - 1) / BK;
+  sh.group_m = 8;
+  sh.sk_first = sh.tiles_m * sh.tiles_n;
+  sh.sk_ranges = 1;
+  sh.w_lead = c.wide_lead;
+  static int cap[64] = {};  // per device, for this instantiation
+  int pairs = 0;
+  e = pair_capacity(reinterpret_cast<const void*>(kern), gemm_threads<Epi>(), L::TOTAL, c.num_sms, cap, &pairs);
+  if (e != cudaSuccess) return e;
+  sh.w_single_from = wide_single_from(sh.tiles_m * (tiles_n / 2), pairs);
+  KernelCtl ctl{c.status, c.timeout_ns, 0, c.scale_a, c.scale_b, c.f8_fmt, c.scale_host};
+  return launch_chained(c, kern, dim3(2 * pairs), dim3(gemm_threads<Epi>()), L::TOTAL, ta, tb, sh, ctl, ep);
+}
+
+// An epilogue program run by 8 warps, two per TMEM lane quadrant, each on
+// half of a tile's columns: the wide-tile kernel drains one accumulator half
+// while the other accumulates, so the drain must be short.
+template <class E>
+struct Epi8 : E {
+  static constexpr int kEpiWarps = 8;
+};
+
+// Epilogue programs the wide-tile kernel is instantiated for: those of the
+// long-K backward GEMMs (dgrad2's RMSNorm backward, the weight gradients'
+// store).
+template <class Epi>
+struct WideTiles {
+  static constexpr bool value = false;
+};
+template <>
+struct WideTiles<EpiStore> {
+  static constexpr bool value = true;
+};
+template <>
+struct WideTiles<EpiDgradRms> {
+  static constexpr bool value = true;
+};
+
 // The 2-SM pair kernel (default) or the 1-SM kernel, 256-column tiles.
 template <bool A_MN, bool B_MN, bool B_DUAL, class Epi, bool FP8 = false>
 cudaError_t run_gemm(const LaunchCtx& c, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tb2, int M,
                      int N, int K, int tiles_n, const typename Epi::Params& ep) {
   static_assert(!FP8 || Epi::kAccScale, "an epilogue on 8-bit operands must dequantise the accumulator");
+  if constexpr (!FP8 && !B_DUAL && WideTiles<Epi>::value && Epi::kEpiWarps == 4)
+    if (wide_tiles_fit(c, K, tiles_n))
+      return launch_gemm2w_kernel<A_MN, B_MN, Epi8<Epi>>(c, ta, tb, M, N, K, tiles_n, ep);
   if (c.pair) return launch_gemm2_kernel<256, 6, A_MN, B_MN, B_DUAL, Epi, FP8>(c, ta, tb, tb2, M, N, K, tiles_n, ep);
   return launch_gemm_kernel<256, 4, A_MN, B_MN, B_DUAL, Epi, FP8>(c, ta, tb, tb2, M, N, K, tiles_n, ep);
 }

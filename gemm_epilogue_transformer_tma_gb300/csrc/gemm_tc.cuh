@@ -68,6 +68,12 @@ struct GemmShape {
   // sk_first = tiles_m * tiles_n (and sk_ranges = 1) means no split
   int sk_first;
   int sk_ranges;
+  // wide-tile SM-pair kernel only (gemm_tc2w.cuh): tiles_n counts 256-column
+  // tiles (even); w_lead = J, the single-half k-blocks before and after a
+  // wide tile's shared ones; wide tiles from w_single_from on run as two
+  // 256-column half tiles
+  int w_lead;
+  int w_single_from;
 };
 
 struct KernelCtl {

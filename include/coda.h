@@ -98,6 +98,20 @@ coda_status_t coda_set_wait_timeout_ns(coda_handle_t h, uint64_t ns);
  * inside the tensor core; the choice only affects speed. */
 coda_status_t coda_set_sm_pairing(coda_handle_t h, int enable);
 
+/* Wide tiles for the long-K GEMMs of the backward (the RMSNorm-backward
+ * data gradient coda_gemm_dgrad_rmsbwd and the weight gradients of
+ * coda_gemm_wgrad_gscale / coda_gemm), SM pairs only.  lead_kblocks = J > 0:
+ * such a GEMM whose output has an even number of 256-column tiles and at
+ * least max(4J, 256) k-blocks of 64 (K >= 16384) computes 256 x 512 tiles, two 256-column
+ * halves per A tile, so each SM loads three quarters of the operand bytes
+ * per MAC and the operand panels are re-read from memory less often.  The
+ * tile's accumulator fills all of tensor memory; the first J k-blocks feed
+ * only the first half and are repeated at the end for the second half, so
+ * that the epilogue of one half runs while the other accumulates.  0 (the
+ * default) turns wide tiles off.  Results equal the 256-column tiles' up to
+ * fp32 summation order.  Returns CODA_ERR_INVALID_ARG outside [0, 64]. */
+coda_status_t coda_set_wide_tiles(coda_handle_t h, int lead_kblocks);
+
 /* Scratch that lets this handle's SM-pair GEMMs keep every SM pair busy in
  * their last, partial wave.  Without it (the default) each SM pair computes
  * whole 256 x 256 tiles, and when the tile count is not a multiple of the

@@ -48,6 +48,24 @@ int coda_debug_split_first_tile(int tiles, int num_kb, int clusters);
  * -1 for invalid arguments.  Not for production use. */
 int coda_debug_split_ranges(int tiles, int num_kb, int clusters);
 
+/* Host-side check of the wide-tile schedule (coda_set_wide_tiles) of the
+ * SM-pair GEMM, run with the kernel's own iterators (no GPU needed): an M x N
+ * output (N with an even number of 256-column tiles) over K on `clusters` SM
+ * pairs with lead `lead`.  Returns 0 when every 256 x 256 output tile is
+ * computed by exactly one unit, every cluster meets its wide units before its
+ * half-tile units, and each accumulator half of a unit sees every k-block
+ * exactly once, starting and ending at the blocks where the kernel starts the
+ * sum and commits it; the number of violations otherwise, -1 for invalid
+ * arguments or an odd tile count.  Not for production use. */
+int coda_debug_wide_schedule_violations(int M, int N, int K, int clusters, int lead);
+
+/* 1 when a long-K backward GEMM (coda_gemm_dgrad_rmsbwd, or coda_gemm /
+ * coda_gemm_wgrad_gscale with bf16 operands) with an M x N output over K
+ * would take wide tiles on this handle now (coda_set_wide_tiles), 0 when it
+ * would take 256-column tiles, -1 for invalid arguments.  Not for
+ * production use. */
+int coda_debug_wide_applies(coda_handle_t h, int M, int N, int K);
+
 #ifdef __cplusplus
 }
 #endif
