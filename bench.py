@@ -932,6 +932,21 @@ def main():
                 "launches_per_step": len(vcalls)}
             del bv, vcalls
             torch.cuda.empty_cache()
+        # the same step with 256 x 512 pair tiles for its long-K GEMMs (dgrad2):
+        # the handle option is set before and cleared after each variant step
+        if not args.wide_tiles and shape.backward:
+            lead = 8
+            wcalls = [lambda: C.coda_set_wide_tiles(lead)] + list(calls) + [lambda: C.coda_set_wide_tiles(0)]
+            t_h, t_w = interleave_many([calls, wcalls], n_cmp, args.warmup, rounds=4)
+            C.coda_set_wide_tiles(0)
+            w_ms = statistics.median(t_w)
+            extras["variant_wide_tiles"] = {
+                "lead": lead, "ms_per_step": w_ms, "value": step_flops / (w_ms * 1e-3) / 1e12,
+                "time_vs_headline_step": statistics.median(w / h for h, w in zip(t_h, t_w)),
+                "rounds_ms": rounds_ms(zip(t_h, t_w)),
+                "gemms": "dgrad2 (K = 2F) on 256 x 512 tiles; the other GEMMs as in the headline step",
+                "timing": "rounds of (headline step, variant), the order reversed every other round; "
+                          "ratio = median per-round time ratio"}
         # unfused ablation, same workload, interleaved the same way
         bu = BlockBuffers(x, unfused=True, backward=shape.backward)
         ucalls = [bu.forward_unfused, bu.backward_unfused] if shape.backward else [bu.forward_unfused]
