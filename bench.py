@@ -249,20 +249,25 @@ def time_steps(calls, steps, warmup, stage_events=True):
     return total, per
 
 
-def interleave(a_calls, b_calls, n, warmup, rounds=3):
-    """Time two call sequences in alternating rounds (a, b, a, b, ...) of n
-    steps each, after warm-up of both: the part heats over a run, so two
-    sequences timed one after the other would see different clocks.
-    Returns (best a ms/step, best b ms/step, median per-round ratio b / a,
-    the per-round pairs)."""
+def interleave(a_calls, b_calls, n, warmup, rounds=4):
+    """Time two call sequences in rounds of n steps each, after warm-up of
+    both: a then b, then b then a, and so on (an even number of rounds).  The
+    part heats over a run, so two sequences timed one after the other would
+    see different clocks, and the one timed second in every round would run
+    hotter.  Returns (best a ms/step, best b ms/step, median per-round ratio
+    b / a, the per-round pairs (a, b))."""
     for calls in (a_calls, b_calls):
         for _ in range(warmup):
             for f in calls:
                 f()
     pairs = []
-    for _ in range(rounds):
-        t_a = time_steps(a_calls, n, 0, stage_events=False)[0] / n
-        t_b = time_steps(b_calls, n, 0, stage_events=False)[0] / n
+    for r in range(rounds):
+        if r % 2 == 0:
+            t_a = time_steps(a_calls, n, 0, stage_events=False)[0] / n
+            t_b = time_steps(b_calls, n, 0, stage_events=False)[0] / n
+        else:
+            t_b = time_steps(b_calls, n, 0, stage_events=False)[0] / n
+            t_a = time_steps(a_calls, n, 0, stage_events=False)[0] / n
         pairs.append((t_a, t_b))
     ratio = statistics.median(t_b / t_a for t_a, t_b in pairs)
     return min(p[0] for p in pairs), min(p[1] for p in pairs), ratio, pairs
@@ -530,7 +535,7 @@ def bench_down_proj_swiglu_bwd(C, b, shape, steps, warmup):
     flops = 2.0 * shape.M * shape.F * shape.d + 2.0 * shape.M * shape.N2 * shape.d
     return {"what": "down-proj dgrad + SwiGLU bwd + dgrad2/RMSNorm bwd", "dY_through_hbm_ms": t_hbm,
             "dY_on_chip_ms": t_chip, "speedup": ratio, "on_chip_tflops": flops / (t_chip * 1e-3) / 1e12,
-            "rounds_ms": rounds_ms(pairs), "timing": "rounds of (on chip, through HBM) interleaved; speedup = "
+            "rounds_ms": rounds_ms(pairs), "timing": "rounds of (on chip, through HBM), the order reversed every other round; speedup = "
                                                    "median per-round time ratio"}
 
 
@@ -567,7 +572,7 @@ def bench_fp8_forward(C, b, shape, steps, warmup, peak_bf16):
     return {"workload": shape.name + " forward", "fp8_fwd_ms": t_8, "bf16_fwd_ms": t_16,
             "speedup": ratio, "rounds_ms": rounds_ms(pairs), "fp8_fwd_tflops": fl / (t_8 * 1e-3) / 1e12,
             "weight_quantize_ms": t_w / n, "stage_ms": {k: statistics.mean(v) for k, v in zip(names, per8)},
-            "timing": "rounds of (fp8, bf16) interleaved; speedup = median per-round time ratio; stage_ms from "
+            "timing": "rounds of (fp8, bf16), the order reversed every other round; speedup = median per-round time ratio; stage_ms from "
                       "a separate pass with an event between stages",
             "gemm2_fp8_tflops": 2.0 * shape.M * shape.N2 * shape.d / (g2 * 1e-3) / 1e12,
             "fp8_peak_tflops": 2 * peak_bf16,
@@ -622,7 +627,7 @@ def bench_fp8_fwdbwd(C, b, shape, steps, warmup, peak_bf16):
     return {"workload": shape.name, "fp8_fwdbwd_ms": t_8, "bf16_fwdbwd_ms": t_16, "speedup": ratio,
             "rounds_ms": rounds_ms(pairs), "fp8_fwdbwd_tflops": fl / (t_8 * 1e-3) / 1e12, "weight_quantize_ms": t_w / n,
             "stage_ms": {k: statistics.mean(v) for (k, _), v in zip(named, per8)},
-            "timing": "rounds of (fp8, bf16) interleaved; speedup = median per-round time ratio; stage_ms from a "
+            "timing": "rounds of (fp8, bf16), the order reversed every other round; speedup = median per-round time ratio; stage_ms from a "
                       "separate pass with an event between stages",
             "formats": "e4m3 activations and weights, e5m2 gradients (dP, dH), one fp32 scale per tensor",
             "delayed_dP_scaling": delayed, "e2e": e2e}
@@ -648,7 +653,7 @@ def bench_qkv_rope(C, steps, warmup, M=8192, S=2048, d=4096, n_heads=32):
     flops = 2.0 * M * N * d
     return {"M": M, "d": d, "heads": n_heads, "head_dim": 128, "seq": S, "fused_ms": t_f,
             "unfused_ms": t_u, "speedup": ratio, "fused_tflops": flops / (t_f * 1e-3) / 1e12,
-            "rounds_ms": rounds_ms(pairs), "timing": "rounds of (fused, unfused) interleaved; speedup = median "
+            "rounds_ms": rounds_ms(pairs), "timing": "rounds of (fused, unfused), the order reversed every other round; speedup = median "
                                                    "per-round time ratio"}
 
 
@@ -753,7 +758,7 @@ def bench_lmhead(C, steps, warmup, tokens=0):
                   "fwdbwd_tflops_executed": 4 * g / t8 / 1e9, "weight_quantize_ms": t_wq / max(1, steps // 2),
                   "loss": loss8.item(),
                   "formats": "e4m3 H and W (per-tensor power-of-two scales), e5m2 dL (scale fixed by |dL| <= 1/M)",
-                  "timing": "rounds of (fp8, bf16) interleaved; speedup = median per-round time ratio"}
+                  "timing": "rounds of (fp8, bf16), the order reversed every other round; speedup = median per-round time ratio"}
     del x, ws, dH, dW, Hq, Wq, dH8, dW8
     return out
 
@@ -928,7 +933,7 @@ def main():
             extras["variant_g_on_activation_fused_rstd"] = {
                 "ms_per_step": v_ms, "value": step_flops / (v_ms * 1e-3) / 1e12,
                 "time_vs_headline_step": ratio, "rounds_ms": rounds_ms(pairs),
-                "timing": "rounds of (headline step, variant) interleaved; ratio = median per-round time ratio",
+                "timing": "rounds of (headline step, variant), the order reversed every other round; ratio = median per-round time ratio",
                 "launches_per_step": len(vcalls)}
             del bv, vcalls
             torch.cuda.empty_cache()
@@ -953,7 +958,7 @@ def main():
         _, u_ms, ratio, pairs = interleave(calls, ucalls, n_cmp, args.warmup)
         extras["ablation_unfused"] = {"ms_per_step": u_ms, "tflops": step_flops / (u_ms * 1e-3) / 1e12,
                                       "fused_speedup": ratio, "rounds_ms": rounds_ms(pairs),
-                                      "timing": "rounds of (fused step, unfused step) interleaved; speedup = median "
+                                      "timing": "rounds of (fused step, unfused step), the order reversed every other round; speedup = median "
                                                 "per-round time ratio"}
         del bu
         torch.cuda.empty_cache()
