@@ -232,7 +232,7 @@ def coda_set_split_workspace(ws, device: int | None = None, stream=None):
            "coda_set_split_workspace")
 
 
-def coda_debug_skip_first_stage(enable: bool, device: int | None = None):
+def coda_debug_skip_first_stage(enable: int, device: int | None = None):
     """Failure-detection test hook (see include/coda_testing.h)."""
     _check(load_library().coda_debug_skip_first_stage(handle(device), int(enable)), "coda_debug_skip_first_stage")
 

@@ -332,7 +332,7 @@ coda_status_t coda_set_split_workspace(coda_handle_t h, void* ws, size_t ws_byte
 
 coda_status_t coda_debug_skip_first_stage(coda_handle_t h, int enable) {
   CODA_TRY(Check().handle(h).st);
-  h->skip_first_stage = enable != 0;
+  h->skip_first_stage = enable == 2 ? 2 : (enable != 0 ? 1 : 0);
   return CODA_OK;
 }
 

@@ -156,6 +156,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi0>()
   uint64_t* drain = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  uint32_t* fill_report = reinterpret_cast<uint32_t*>(tmem_slot + 2);  // leader: the peer's fills + 1
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -174,6 +175,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi0>()
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
+    *fill_report = 0;
     fence_mbar_init();
     tma_prefetch_desc(&g.tmA0);
     tma_prefetch_desc(&g.tmB0);
@@ -198,9 +200,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi0>()
       const uint32_t leader_full = mapa_shared(smem_u32(full), 0);
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t pending = 0, parity = 0;
+      int issued = 0, skipped = -1;  // k-block fills so far; the one the test hook left unarmed
       bool ok = true;
-      bool skip = ctl.skip_first_stage != 0 && cluster_id == 0 && leader;
+      bool skip = ctl.skip_first_stage == 1 && cluster_id == 0 && leader;
+      // test hook: the first pair's second CTA stops before its first copy
+      if (ctl.skip_first_stage == 2 && cluster_id == 0 && !leader) ok = false;
       int prob, t;
       for (int k = 0; ok && group_tile(g.sched, cluster_id, k, prob, t); ++k) {
         const GemmShape& sh = prob == 0 ? g.sh0 : g.sh1;
@@ -216,36 +220,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi0>()
           }
           if (skip) {
             skip = false;  // test hook: the leader never arms this stage
+            skipped = issued;
           } else {
             uint8_t* sa = smem + stage * L::STAGE_BYTES;
             uint8_t* sb = sa + L::A_BYTES;
             const uint32_t bar = leader_full + static_cast<uint32_t>(stage * 8);
-            if (leader) {
-              mbar_arrive_expect_tx(&full[stage], 2 * L::STAGE_BYTES);
-              pending |= 1u << stage;
-              parity = (parity & ~(1u << stage)) | (phase << stage);
-            }
+            if (leader) mbar_arrive_expect_tx(&full[stage], 2 * L::STAGE_BYTES);
             if (prob == 0)
               pair_load_kblock<A_MN0, B_MN0, FP8>(sa, sb, &g.tmA0, &g.tmB0, bar, kb, m0, n0);
             else
               pair_load_kblock<A_MN1, B_MN1, FP8>(sa, sb, &g.tmA1, &g.tmB1, bar, kb, m0, n0);
           }
+          ++issued;
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
-      if (!ok) {
-        if (leader) {
-          for (int st = 0; st < STAGES; ++st)
-            if ((pending >> st) & 1u)
-              if (!mbar_wait_timeout(&full[st], (parity >> st) & 1u, ctl.timeout_ns))
-                atomicOr(ctl.status, DEV_ERR_TIMEOUT_DRAIN);
-        } else {
-          const uint64_t t0 = globaltimer_ns();
-          while (globaltimer_ns() - t0 < 2000000ull) {
-          }
+      // every fill of both CTAs observed landed (as in gemm_tc2_kernel)
+      if (!pair_fills_landed(leader, issued, skipped, full, STAGES, L::STAGE_BYTES, fill_report, ctl.timeout_ns)) {
+        atomicOr(ctl.status, DEV_ERR_TIMEOUT_DRAIN);
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 2000000ull) {
         }
       }
     }

@@ -174,7 +174,7 @@ cudaError_t launch_gemm2w_kernel(const LaunchCtx& c, const CUtensorMap& ta, cons
   e = pair_capacity(reinterpret_cast<const void*>(kern), gemm_threads<Epi>(), L::TOTAL, c.num_sms, cap, &pairs);
   if (e != cudaSuccess) return e;
   sh.w_single_from = wide_single_from(sh.tiles_m * (tiles_n / 2), pairs);
-  KernelCtl ctl{c.status, c.timeout_ns, 0, c.scale_a, c.scale_b, c.f8_fmt, c.scale_host};
+  KernelCtl ctl{c.status, c.timeout_ns, c.skip_first_stage, c.scale_a, c.scale_b, c.f8_fmt, c.scale_host};
   return launch_chained(c, kern, dim3(2 * pairs), dim3(gemm_threads<Epi>()), L::TOTAL, ta, tb, sh, ctl, ep);
 }
 

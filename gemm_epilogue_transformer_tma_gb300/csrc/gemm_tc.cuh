@@ -79,7 +79,8 @@ struct GemmShape {
 struct KernelCtl {
   int* status;        // device status word (atomicOr of DEV_ERR_* bits)
   uint64_t timeout_ns;
-  int skip_first_stage;  // test hook: CTA 0's producer never fills its first stage
+  int skip_first_stage;  // test hook: 1: CTA 0's producer never fills its first stage;
+                         // 2 (SM-pair kernels): the first pair's second CTA issues no copy
   const float* scale_a;  // FP8 operands: per-tensor dequantisation scales (null = 1)
   const float* scale_b;
   uint32_t f8_fmt;       // FP8 operands: format bits of A and B (f8_format_bits)

@@ -19,10 +19,12 @@
 //   warps 2..    epilogue on this CTA's 128 rows (4 or 8 warps, see
 //                gemm_tc.cuh); release the accumulator by
 //                arriving on the leader's tempty[].
-// All waits are bounded as in the 1-SM kernel.  After an abort the leader
-// waits (bounded) for every stage it armed, which counts the peer's bytes
-// too; the peer cannot observe its own copies, so it waits a fixed grace
-// period far longer than a copy's latency before releasing its memory.
+// All waits are bounded as in the 1-SM kernel.  At the end of the producers,
+// finished or stopped early, the peer reports how many stage fills it issued
+// and the leader observes the last fill of every stage land, arming or
+// trimming the barrier where only one CTA's copies were issued
+// (pair_fills_landed); the peer's memory stays allocated until the final
+// cluster barrier, which the leader's producer reaches only after that.
 #pragma once
 
 #include "gemm_tc.cuh"
@@ -90,6 +92,69 @@ struct SplitWork {
   }
 };
 
+// End of both producers of a CTA pair, whether their loops finished or
+// stopped early.  The leader's full barriers count both CTAs' bytes and the
+// peer cannot wait on them, so the peer reports how many fills it issued (a
+// store into the leader's report word), and the leader makes sure that the
+// last fill of every stage has landed before its producer goes on; the
+// peer's shared memory stays allocated until the kernel's final cluster
+// barrier, which the leader's producer reaches only after this.
+//
+// pair_report_wait: the leader's bounded wait for the peer's report (the
+// count + 1, so that 0 means "not yet").  The limit is twice the wait limit
+// plus the 10 ms a sleeping try_wait may overrun it: the peer's producer
+// stops at most one expired wait after the leader's.
+__device__ __forceinline__ bool pair_report_wait(const uint32_t* report, uint64_t timeout_ns, uint32_t& r) {
+  r = ld_acquire_cluster_u32(report);
+  if (r != 0) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while ((r = ld_acquire_cluster_u32(report)) == 0)
+    if (globaltimer_ns() - t0 > 2 * timeout_ns + 20000000ull) return false;
+  return true;
+}
+
+// pair_ring_landed: the leader's walk over one ring.  Fill i goes to stage
+// i % stages in lap i / stages; the leader armed fills [0, issued) except
+// `skipped`, the peer issued [0, peer).  Only the last `stages` fills can be
+// in flight: any older one was consumed before its stage was filled again.
+// Where the leader never armed a fill that the peer issued (it stopped
+// first, or the test hook skipped it), it arms the barrier for the peer's
+// bytes alone; where the peer never issued a fill that the leader armed, it
+// takes the peer's share off the expected bytes; then it waits for the
+// phase.  peer_bytes(i, leader_armed) gives the peer's share of fill i.
+template <class PeerBytes>
+__device__ __forceinline__ bool pair_ring_landed(int issued, int skipped, int peer, uint64_t* full, int stages,
+                                                 PeerBytes peer_bytes, uint64_t timeout_ns) {
+  const int last = issued > peer ? issued : peer;
+  bool ok = true;
+  for (int i = last > stages ? last - stages : 0; i < last; ++i) {
+    const bool armed = i < issued && i != skipped;
+    const bool loaded = i < peer;
+    if (!armed && !loaded) continue;
+    uint64_t* bar = &full[i % stages];
+    if (!armed)
+      mbar_arrive_expect_tx(bar, peer_bytes(i, false));
+    else if (!loaded)
+      mbar_complete_tx(bar, peer_bytes(i, true));
+    if (!mbar_wait_timeout(bar, static_cast<uint32_t>((i / stages) & 1), timeout_ns)) ok = false;
+  }
+  return ok;
+}
+
+// The hand-off for a kernel with one ring of equal fills.  Returns false
+// when the report or a phase did not come in time.
+__device__ __forceinline__ bool pair_fills_landed(bool leader, int issued, int skipped, uint64_t* full, int stages,
+                                                  uint32_t peer_bytes, uint32_t* report, uint64_t timeout_ns) {
+  if (!leader) {
+    st_release_cluster_u32(mapa_shared(smem_u32(report), 0), static_cast<uint32_t>(issued) + 1u);
+    return true;
+  }
+  uint32_t r;
+  if (!pair_report_wait(report, timeout_ns, r)) return false;
+  return pair_ring_landed(issued, skipped, static_cast<int>(r) - 1, full, stages,
+                          [peer_bytes](int, bool) { return peer_bytes; }, timeout_ns);
+}
+
 // Wait (bounded, like the mbarrier waits) for a split partial's flag.
 __device__ __forceinline__ bool split_flag_wait(const int* f, const volatile int* abort_flag, uint64_t timeout_ns) {
   if (ld_acquire_gpu(f) != 0) return true;
@@ -114,7 +179,7 @@ struct Gemm2Smem {
   static_assert(TOTAL <= MAX_DYN_SMEM, "shared memory budget");
   static constexpr int TMEM_COLS = 2 * BN;
   static_assert(TMEM_COLS <= 512, "TMEM has 512 columns");
-  static_assert((2 * STAGES + 5) * 8 + 8 <= BAR_BYTES, "barrier area too small");
+  static_assert((2 * STAGES + 5) * 8 + 12 <= BAR_BYTES, "barrier area too small");
   static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "1 KB aligned halves");
 };
 
@@ -147,6 +212,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi>(),
   uint64_t* drain = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  uint32_t* fill_report = reinterpret_cast<uint32_t*>(tmem_slot + 2);  // leader: the peer's fills + 1
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -166,6 +232,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi>(),
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
+    *fill_report = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
@@ -194,9 +261,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi>(),
       const uint32_t leader_full = mapa_shared(smem_u32(full), 0);
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t pending = 0, parity = 0;  // leader: stages it armed
+      int issued = 0, skipped = -1;  // k-block fills so far; the one the test hook left unarmed
       bool ok = true;
-      bool skip = ctl.skip_first_stage != 0 && cluster_id == 0 && leader;
+      bool skip = ctl.skip_first_stage == 1 && cluster_id == 0 && leader;
+      // test hook: the first pair's second CTA stops before its first copy
+      if (ctl.skip_first_stage == 2 && cluster_id == 0 && !leader) ok = false;
       SplitWork wk(sh, cluster_id, num_clusters);
       TilePiece pc;
       while (ok && wk.next(pc)) {
@@ -211,15 +280,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi>(),
           }
           if (skip) {
             skip = false;  // test hook: the leader never arms this stage
+            skipped = issued;
           } else {
             uint8_t* sa = smem + stage * L::STAGE_BYTES;
             uint8_t* sb = sa + L::A_BYTES;
             const uint32_t bar = leader_full + static_cast<uint32_t>(stage * 8);
-            if (leader) {
-              mbar_arrive_expect_tx(&full[stage], 2 * L::STAGE_BYTES);
-              pending |= 1u << stage;
-              parity = (parity & ~(1u << stage)) | (phase << stage);
-            }
+            if (leader) mbar_arrive_expect_tx(&full[stage], 2 * L::STAGE_BYTES);
             if (!A_MN) {
               tma_load_2d_pair(sa, &tmA, bar, kb * BKE, m0);
             } else {
@@ -237,29 +303,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi>(),
                 tma_load_2d_pair(sb + i * MN_BOX, &tmB, bar, tn * BN + static_cast<int>(rank) * HB + i * MNB, kb * BKE);
             }
           }
+          ++issued;
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
-      if (!ok) {
-        if (leader) {
-          for (int st = 0; st < STAGES; ++st)
-            if ((pending >> st) & 1u)
-              if (!mbar_wait_timeout(&full[st], (parity >> st) & 1u, ctl.timeout_ns))
-                atomicOr(ctl.status, DEV_ERR_TIMEOUT_DRAIN);
-        } else {
-          // The peer's copies complete on the leader's barrier, which this
-          // CTA cannot wait on, so it waits out a fixed grace period instead.
-          // 2 ms bounds them with a wide margin: the bytes in flight on the
-          // whole GPU cannot exceed the operand rings of the resident CTAs
-          // (152 SMs x 6 stages x 32 KB = 29 MB), which HBM delivers in
-          // about 5 us; a copy is bounded by that queue, not by a wait on
-          // anything this kernel controls.
-          const uint64_t t0 = globaltimer_ns();
-          while (globaltimer_ns() - t0 < 2000000ull) {
-          }
+      // every fill of both CTAs observed landed before shared memory can be
+      // released (the leader's producer holds the final cluster barrier)
+      if (!pair_fills_landed(leader, issued, skipped, full, STAGES, L::STAGE_BYTES, fill_report, ctl.timeout_ns)) {
+        atomicOr(ctl.status, DEV_ERR_TIMEOUT_DRAIN);
+        // a fill could not be observed: wait out a grace period far longer
+        // than any copy's latency (the bytes in flight on the whole GPU, at
+        // most the rings of the resident CTAs, 152 SMs x 6 stages x 32 KB =
+        // 29 MB, take HBM about 5 us) before the peer can exit
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 2000000ull) {
         }
       }
     }

@@ -169,7 +169,8 @@ struct Gemm2wSmem {
   static constexpr int TOTAL = RING_BYTES + STORE_BYTES + BAR_BYTES + 1024;
   static_assert(TOTAL <= MAX_DYN_SMEM, "shared memory budget");
   static constexpr int TMEM_COLS = 512;
-  static_assert((2 * STAGES + 5) * 8 + 8 <= BAR1_OFFSET, "barrier area too small");
+  static_assert((2 * STAGES + 5) * 8 + 20 <= BAR1_OFFSET, "barrier area too small");
+  static_assert(STAGES <= 16, "the producer's per-stage B-half counts are 2 bits each in one word");
   static_assert(BAR1_OFFSET + 2 * STAGES1 * 8 <= BAR_BYTES, "barrier area too small");
   static_assert(STAGES1 * STAGE1_BYTES == RING_BYTES, "both rings cover the same bytes");
 };
@@ -195,6 +196,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi>(),
   uint64_t* drain = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // leader: the peer's fills of the wide ring + 1, of the half-tile ring, and
+  // the B halves (0..2) of its last fill into each wide stage, 2 bits each
+  uint32_t* fill_report = tmem_slot + 2;
   constexpr int S1 = L::STAGES1;
   uint64_t* full1 = reinterpret_cast<uint64_t*>(smem + L::RING_BYTES + L::STORE_BYTES + L::BAR1_OFFSET);
   uint64_t* empty1 = full1 + S1;
@@ -221,6 +225,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi>(),
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
+    fill_report[0] = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
@@ -245,8 +250,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi>(),
       const uint32_t leader_full1 = mapa_shared(smem_u32(full1), 0);
       int stage = 0, stage1 = 0;  // wide ring / half-tile ring cursors
       uint32_t phase = 0, phase1 = 0;
-      uint32_t pending = 0, parity = 0, pending1 = 0, parity1 = 0;  // leader: stages it armed
-      bool ok = true;
+      int issued = 0, issued1 = 0;  // fills of the wide / half-tile ring so far
+      uint32_t halves = 0;          // B halves of the last fill into each wide stage, 2 bits each
+      // test hook: one CTA of the first pair stops before its first copy
+      // (1: the leader, 2: the peer)
+      bool ok = !(cluster_id == 0 && ctl.skip_first_stage == (leader ? 1 : 2));
       bool ring1 = false;  // switched to the half-tile ring
       int ff = 0;          // TMEM half that frees first
       WideWork wk(sh, cluster_id, num_clusters);
@@ -285,12 +293,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi>(),
             }
             uint8_t* sa = smem + stage * L::STAGE_BYTES;
             const uint32_t bar = leader_full + static_cast<uint32_t>(stage * 8);
-            if (leader) {
-              const int bytes = L::A_BYTES + (f0 ? L::HB_BYTES : 0) + (f1 ? L::HB_BYTES : 0);
-              mbar_arrive_expect_tx(&full[stage], 2 * bytes);
-              pending |= 1u << stage;
-              parity = (parity & ~(1u << stage)) | (phase << stage);
-            }
+            const uint32_t nh = (f0 ? 1u : 0u) + (f1 ? 1u : 0u);
+            halves = (halves & ~(3u << (2 * stage))) | (nh << (2 * stage));
+            if (leader) mbar_arrive_expect_tx(&full[stage], 2 * (L::A_BYTES + nh * L::HB_BYTES));
             if (!A_MN) {
               tma_load_2d_pair(sa, &tmA, bar, kb * BK, m0);
             } else {
@@ -310,6 +315,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi>(),
                   tma_load_2d_pair(sb + j * MN_BOX, &tmB, bar, n0 + j * MNB, kb * BK);
               }
             }
+            ++issued;
             if (++stage == STAGES) {
               stage = 0;
               phase ^= 1u;
@@ -326,11 +332,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi>(),
             uint8_t* sa = smem + stage1 * L::STAGE1_BYTES;
             uint8_t* sb = sa + L::A_BYTES;
             const uint32_t bar = leader_full1 + static_cast<uint32_t>(stage1 * 8);
-            if (leader) {
-              mbar_arrive_expect_tx(&full1[stage1], 2 * L::STAGE1_BYTES);
-              pending1 |= 1u << stage1;
-              parity1 = (parity1 & ~(1u << stage1)) | (phase1 << stage1);
-            }
+            if (leader) mbar_arrive_expect_tx(&full1[stage1], 2 * L::STAGE1_BYTES);
             if (!A_MN) {
               tma_load_2d_pair(sa, &tmA, bar, kb * BK, m0);
             } else {
@@ -344,6 +346,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi>(),
               for (int j = 0; j < HB / MNB; ++j)
                 tma_load_2d_pair(sb + j * MN_BOX, &tmB, bar, n_first + j * MNB, kb * BK);
             }
+            ++issued1;
             if (++stage1 == S1) {
               stage1 = 0;
               phase1 ^= 1u;
@@ -352,23 +355,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi>(),
         }
         if (!u.wide) ff ^= 1;
       }
-      if (!ok) {
-        if (leader) {
-          for (int st = 0; st < STAGES; ++st)
-            if ((pending >> st) & 1u)
-              if (!mbar_wait_timeout(&full[st], (parity >> st) & 1u, ctl.timeout_ns))
-                atomicOr(ctl.status, DEV_ERR_TIMEOUT_DRAIN);
-          for (int st = 0; st < S1; ++st)
-            if ((pending1 >> st) & 1u)
-              if (!mbar_wait_timeout(&full1[st], (parity1 >> st) & 1u, ctl.timeout_ns))
-                atomicOr(ctl.status, DEV_ERR_TIMEOUT_DRAIN);
-        } else {
-          // as in gemm_tc2_kernel: the peer's copies complete on the leader's
-          // barrier, so it waits out a fixed grace period (2 ms, far above
-          // the time HBM takes to deliver every ring of the GPU)
-          const uint64_t t0 = globaltimer_ns();
-          while (globaltimer_ns() - t0 < 2000000ull) {
-          }
+      // the hand-off of gemm_tc2_kernel, over both rings: every fill of both
+      // CTAs observed landed before shared memory can be released
+      bool landed = true;
+      if (!leader) {
+        const uint32_t lead_report = mapa_shared(smem_u32(fill_report), 0);
+        st_release_cluster_u32(lead_report + 4, static_cast<uint32_t>(issued1));
+        st_release_cluster_u32(lead_report + 8, halves);
+        st_release_cluster_u32(lead_report, static_cast<uint32_t>(issued) + 1u);
+      } else {
+        uint32_t r;
+        landed = pair_report_wait(fill_report, ctl.timeout_ns, r);
+        if (landed) {
+          const int peer1 = static_cast<int>(ld_acquire_cluster_u32(fill_report + 1));
+          const uint32_t peer_halves = ld_acquire_cluster_u32(fill_report + 2);
+          const auto wide_bytes = [halves, peer_halves](int i, bool leader_armed) {
+            const uint32_t nh = ((leader_armed ? halves : peer_halves) >> (2 * (i % STAGES))) & 3u;
+            return static_cast<uint32_t>(L::A_BYTES) + nh * static_cast<uint32_t>(L::HB_BYTES);
+          };
+          landed = pair_ring_landed(issued, -1, static_cast<int>(r) - 1, full, STAGES, wide_bytes, ctl.timeout_ns);
+          landed = pair_ring_landed(issued1, -1, peer1, full1, S1,
+                                    [](int, bool) { return static_cast<uint32_t>(L::STAGE1_BYTES); },
+                                    ctl.timeout_ns) && landed;
+        }
+      }
+      if (!landed) {
+        atomicOr(ctl.status, DEV_ERR_TIMEOUT_DRAIN);
+        // as in gemm_tc2_kernel: a fill could not be observed, so wait out a
+        // grace period far longer than any copy's latency
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 2000000ull) {
         }
       }
     }

@@ -64,6 +64,13 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// Count `bytes` of the current phase's expected transaction bytes as done
+// without a copy (bytes that were expected but will never be sent).
+__device__ __forceinline__ void mbar_complete_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.complete_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
 // Longest a waiting thread stays suspended inside one try_wait (it resumes at
 // once when the phase completes).  Waiting warps that sleep instead of
 // re-polling leave the power budget to the tensor cores: with the default
@@ -332,6 +339,20 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
 }
 
 // Shared::cluster address of the variable at local address `addr` in CTA `rank`.
+// A 32-bit store to shared memory of another CTA of the cluster (address
+// from mapa_shared), ordered after this thread's earlier memory operations.
+__device__ __forceinline__ void st_release_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.release.cluster.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+
+// A 32-bit load of this CTA's shared memory, ordered before this thread's
+// later memory operations, seeing stores released at cluster scope.
+__device__ __forceinline__ uint32_t ld_acquire_cluster_u32(const void* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.cluster.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));

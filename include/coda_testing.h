@@ -11,12 +11,17 @@
 extern "C" {
 #endif
 
-/* Failure-detection test hook.  While enabled, every GEMM launched through
- * this handle leaves the first shared-memory stage of its first CTA unfilled,
- * so that CTA's MMA wait cannot complete and must hit the wait limit: the
- * launch then records CODA_ERR_TIMEOUT (reported by coda_sync_status), its
- * results are invalid, and the context stays usable.  Pair it with a short
- * coda_set_wait_timeout_ns.  Not for production use. */
+/* Failure-detection test hook.  enable = 1: every GEMM launched through this
+ * handle leaves the first shared-memory stage of its first CTA unfilled, so
+ * that CTA's MMA wait cannot complete and must hit the wait limit (in the
+ * 256 x 512 pair-tile kernel of coda_set_wide_tiles, the first CTA issues no
+ * copy at all).  enable = 2 (SM-pair GEMMs): the second CTA of the first SM
+ * pair issues no copy at all, so the pair's stages never fill; on single
+ * SMs it acts as 1.  Either way the launch records
+ * CODA_ERR_TIMEOUT (reported by coda_sync_status), its results are invalid,
+ * every copy that was issued is still observed to land before shared memory
+ * is released, and the context stays usable.  0 turns the hook off.  Pair it
+ * with a short coda_set_wait_timeout_ns.  Not for production use. */
 coda_status_t coda_debug_skip_first_stage(coda_handle_t h, int enable);
 
 /* Host-side check of the tile schedule of the grouped launches (no GPU

@@ -1,9 +1,10 @@
 """Failure detection without a GPU fault: every wait inside the GEMM kernels
-is time-bounded.  The test hook leaves one shared-memory stage unfilled, so
-the MMA warp's wait can never complete; the wait must expire after the short
-limit, the kernel must record CODA_ERR_TIMEOUT in the device status word,
-drain its own in-flight copies and return, and the context must stay usable
-(a normal GEMM right after is checked against the oracle)."""
+is time-bounded.  The test hook leaves a shared-memory stage unfilled, or
+stops one CTA of an SM pair before its first copy, so the MMA warp's wait
+can never complete; the wait must expire after the short limit, the kernel
+must record CODA_ERR_TIMEOUT in the device status word, observe every copy
+it issued land and return, and the context must stay usable (a normal GEMM
+right after is checked against the oracle)."""
 import pytest
 import torch
 
@@ -27,17 +28,22 @@ def _gemm(M, N, K, seed):
     return A, B, Cd
 
 
-@pytest.mark.parametrize("pair", [True, False], ids=["sm_pair", "single_sm"])
-def test_expired_wait_is_reported_and_the_context_survives(pair):
+@pytest.mark.parametrize("pair,mode", [(True, 1), (True, 2), (False, 1)],
+                         ids=["sm_pair_leader_skips", "sm_pair_peer_stops", "single_sm"])
+def test_expired_wait_is_reported_and_the_context_survives(pair, mode):
+    """mode 1: the first CTA never arms its first stage (the second CTA's
+    copies for it land unobserved by any MMA); mode 2: the first pair's second
+    CTA issues no copy (the first CTA's stages expect bytes that never come).
+    Both leave copies that only the end-of-producer hand-off observes."""
     assert_device_ok()
     C.coda_set_sm_pairing(pair)
     C.coda_set_wait_timeout_ns(50_000_000)  # 50 ms
-    C.coda_debug_skip_first_stage(True)
+    C.coda_debug_skip_first_stage(mode)
     try:
         _gemm(256, 256, 512, 1)
         st, bits = C.coda_sync_status()
     finally:
-        C.coda_debug_skip_first_stage(False)
+        C.coda_debug_skip_first_stage(0)
         C.coda_set_wait_timeout_ns(0)
         C.coda_set_sm_pairing(True)
     assert st == 6, f"expected CODA_ERR_TIMEOUT, got {C.STATUS_NAMES.get(st)} bits={bits:#x}"
@@ -51,3 +57,42 @@ def test_expired_wait_is_reported_and_the_context_survives(pair):
     C.coda_set_sm_pairing(True)
     assert_device_ok()
     assert_elem(Cd, O.matmul_nt(f64(A), f64(B)), "C after timeout")
+
+
+@pytest.mark.parametrize("mode", [1, 2], ids=["leader_stops", "peer_stops"])
+def test_wide_tiles_expired_wait(mode):
+    """The 256 x 512 pair-tile kernel, whose producers fill two rings (wide
+    stages of one or two B halves, then half-tile stages): one CTA of the
+    first pair issues no copy (1: the first CTA, so every fill of the second
+    lands on a stage only the end-of-producer hand-off arms; 2: the second
+    CTA, so the first CTA's stages wait for bytes that never come).  The
+    wait must expire, no drain may, and a wide GEMM right after is exact."""
+    from tests.test_gpu_exact import ints
+    assert_device_ok()
+    C.coda_set_sm_pairing(True)
+    C.coda_set_wide_tiles(8)
+    try:
+        assert C.coda_debug_wide_applies(256, 512, 16384) == 1
+        C.coda_set_wait_timeout_ns(50_000_000)  # 50 ms
+        C.coda_debug_skip_first_stage(mode)
+        try:
+            _gemm(256, 512, 16384, 3)
+            st, bits = C.coda_sync_status()
+        finally:
+            C.coda_debug_skip_first_stage(0)
+            C.coda_set_wait_timeout_ns(0)
+        assert st == 6, f"expected CODA_ERR_TIMEOUT, got {C.STATUS_NAMES.get(st)} bits={bits:#x}"
+        assert bits & TIMEOUT_BITS, f"a bounded wait should have expired (bits={bits:#x})"
+        assert not bits & DRAIN_BIT, f"in-flight copies did not drain (bits={bits:#x})"
+        # integer operands: one exact result whatever the summation order
+        M, N, K = 1024, 4096, 16384
+        assert C.coda_debug_wide_applies(M, N, K) == 1
+        A, Bt = ints((M, K), -3, 3, 51), ints((N, K), -3, 3, 52)
+        Cd = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+        C.coda_gemm(A.to(torch.bfloat16).cuda(), False, Bt.to(torch.bfloat16).cuda(), False, Cd, M, N, K)
+        torch.cuda.synchronize()
+    finally:
+        C.coda_set_wide_tiles(0)
+    assert_device_ok()
+    ref = (A.to(torch.float64) @ Bt.to(torch.float64).T).to(torch.float32).to(torch.bfloat16)
+    assert torch.equal(Cd.cpu(), ref)
