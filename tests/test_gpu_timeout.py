@@ -96,3 +96,38 @@ def test_wide_tiles_expired_wait(mode):
     assert_device_ok()
     ref = (A.to(torch.float64) @ Bt.to(torch.float64).T).to(torch.float32).to(torch.bfloat16)
     assert torch.equal(Cd.cpu(), ref)
+
+
+@pytest.mark.parametrize("mode", [1, 2], ids=["leader_skips", "peer_stops"])
+def test_grouped_launch_expired_wait(mode):
+    """The grouped SM-pair launch (dX and dW1 of the first layer in one
+    persistent kernel) under both hook modes: the wait must expire, no drain
+    may, and the grouped launch right after must equal two separate GEMMs."""
+    assert_device_ok()
+    M, K1, d = 1280, 512, 256
+    g = torch.Generator(device="cuda").manual_seed(7)
+    dH = torch.randn(M, d, device="cuda", generator=g).to(torch.bfloat16)
+    X = torch.randn(M, K1, device="cuda", generator=g).to(torch.bfloat16)
+    W1t = (torch.randn(d, K1, device="cuda", generator=g) / d ** 0.5).to(torch.bfloat16)
+    dX = torch.empty(M, K1, device="cuda", dtype=torch.bfloat16)
+    dW1t = torch.empty(d, K1, device="cuda", dtype=torch.bfloat16)
+    C.coda_set_sm_pairing(True)
+    C.coda_set_wait_timeout_ns(50_000_000)  # 50 ms
+    C.coda_debug_skip_first_stage(mode)
+    try:
+        C.coda_gemm_res_prms_bwd(dH, X, W1t, dX, dW1t, None)
+        st, bits = C.coda_sync_status()
+    finally:
+        C.coda_debug_skip_first_stage(0)
+        C.coda_set_wait_timeout_ns(0)
+    assert st == 6, f"expected CODA_ERR_TIMEOUT, got {C.STATUS_NAMES.get(st)} bits={bits:#x}"
+    assert bits & TIMEOUT_BITS, f"a bounded wait should have expired (bits={bits:#x})"
+    assert not bits & DRAIN_BIT, f"in-flight copies did not drain (bits={bits:#x})"
+    C.coda_gemm_res_prms_bwd(dH, X, W1t, dX, dW1t, None)
+    rX, rW = torch.empty_like(dX), torch.empty_like(dW1t)
+    C.coda_gemm(dH, False, W1t, True, rX, M, K1, d)
+    C.coda_gemm(dH, True, X, True, rW, d, K1, M)
+    torch.cuda.synchronize()
+    assert_device_ok()
+    assert torch.equal(dX, rX)
+    assert torch.equal(dW1t, rW)
