@@ -11,7 +11,8 @@ all of dg; at least 64 whole columns and 64 whole rows of dW2t and dW1t,
 including the first and last column tiles and the gate/up boundary.  The
 forward output is also graded end to end (Frobenius) against the oracle
 chained from the seeded inputs on the sampled rows.  Workloads: the 1B
-forward, the 7B and 70B forward+backward, and the LM-head cross-entropy
+forward, the 7B and 70B forward+backward (each on the default 256 x 256 pair
+tiles and on the opt-in 256 x 512 tiles), and the LM-head cross-entropy
 (Synced write-up, sections 尾声 / 五种积木 / 实验结果: GEMM-RMSNorm-GEMM at
 the 1B, 7B and 70B hidden sizes).
 """
@@ -151,11 +152,26 @@ def test_1b_forward_full_size():
     check_block(B1, backward=False)
 
 
-def test_7b_forward_backward_full_size():
+@pytest.fixture(params=[0, 8], ids=["tiles_256", "wide_tiles"])
+def wide_lead(request):
+    """The default 256 x 256 pair tiles, and the opt-in 256 x 512 pair tiles
+    (coda_set_wide_tiles, lead 8), which the data gradient of the second GEMM
+    (K = 2F) takes at both block sizes."""
+    C.coda_set_wide_tiles(request.param)
+    yield request.param
+    torch.cuda.synchronize()
+    C.coda_set_wide_tiles(0)
+
+
+def test_7b_forward_backward_full_size(wide_lead):
+    if wide_lead:
+        assert C.coda_debug_wide_applies(B7.M, B7.d, B7.N2) == 1
     check_block(B7, backward=True)
 
 
-def test_70b_forward_backward_full_size():
+def test_70b_forward_backward_full_size(wide_lead):
+    if wide_lead:
+        assert C.coda_debug_wide_applies(B70.M, B70.d, B70.N2) == 1
     check_block(B70, backward=True)
 
 
