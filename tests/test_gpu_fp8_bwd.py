@@ -48,8 +48,8 @@ def deq(codes, scale_pair, fmt):
     return O.fp8_decode(codes.cpu().numpy(), fmt) * float(scale_pair[1].item())
 
 
-def run_fp8(s):
-    x = {k: v.cuda() for k, v in block_inputs(s, 0, "cpu").items()}
+def run_fp8(s, seed=0):
+    x = {k: v.cuda() for k, v in block_inputs(s, seed, "cpu").items()}
     b = BlockBuffers(x)
     b.fp8_quantize_weights()
     b.forward_fp8()
@@ -63,6 +63,29 @@ def run_fp8(s):
 def test_fp8_backward_stages(name, pairing):
     s = SHAPES[name]
     x, b = run_fp8(s)
+    check_fp8_backward_stages(s, x, b)
+
+
+def check_fp8_forward_stages(s, x, b):
+    """The FP8 forward of BlockBuffers stage by stage: the codes and scales
+    of X and H bit-exact (the oracle's quantiser on the bf16 tensors), H,
+    psum, rstd, z and out against the oracle fed the dequantised codes."""
+    for src, q, sc in ((x["X"], b.Xq, b.s_a[0]), (b.H, b.Hq, b.s_a[1])):
+        v = src.float().cpu().numpy()
+        ref_scale = O.fp8_scale(v, "e4m3")
+        assert np.float32(sc[1].item()) == ref_scale
+        assert np.array_equal(q.cpu().numpy(), O.fp8_quantize(v, ref_scale, "e4m3"))
+    Xd, W1d = deq(b.Xq, b.s_a[0], "e4m3"), deq(b.W1q, b.s_w[0], "e4m3")
+    assert_elem(b.H, O.gemm_residual(Xd, W1d, f64(x["R"])), "H (fp8 gemm1)")
+    H = f64(b.H)
+    assert_elem(b.psum, O.partial_sumsq(H, C.PARTIAL_COLS), "psum (fp8 gemm1)", tol=1e-4)
+    assert_elem(b.rstd, O.rstd_from_partials(f64(b.psum), s.d, EPS), "rstd", tol=1e-5)
+    z_ref = O.rowscale_gemm(deq(b.Hq, b.s_a[1], "e4m3"), deq(b.W2gq, b.s_w[1], "e4m3"), f64(b.rstd))
+    assert_elem(b.z, z_ref, "z (fp8 gemm2)")
+    assert_elem(b.out, O.swiglu(z_ref), "out (fp8 gemm2)")
+
+
+def check_fp8_backward_stages(s, x, b):
     g, H, c = f64(x["g"]), f64(b.H), f64(b.c)
     # dP's codes come straight from the SwiGLU backward: they must equal the
     # e5m2 codes of the bf16 dP that the unfused SwiGLU-backward kernel writes

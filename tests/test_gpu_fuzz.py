@@ -1,0 +1,124 @@
+"""Seeded random shapes through the whole block and the LM-head cross-entropy,
+against the fp64 oracle fed the GPU's own stage inputs.
+
+The hand-picked shapes of the other parity tests sit on chosen tile edges;
+these draw M, K1, d, F and V from a fixed seed (extents multiples of 8, the
+boundary's rule; M any positive size), so that tails of every width
+against the 128-row / 256-column tiles, the 64-deep k-blocks, the 128-column
+partial sums and the 16384-column vocabulary chunks come up without being
+chosen.  Every stage is graded as in the hand-picked tests, the block also on
+8-bit operands (extents multiples of 16 there); each shape runs on SM pairs
+or on single SMs, alternately.
+
+Method: "CODA: Rewriting Transformer Blocks as GEMM-Epilogue Programs"
+(Synced write-up, sections 尾声 and 五种积木).
+"""
+import numpy as np
+import pytest
+
+import oracle as O
+from coda_inputs import BlockShape, CEShape, block_inputs, ce_inputs
+from tests._ce import check_argmax, check_label_rows, with_edge_labels
+from tests._parity import assert_device_ok, assert_elem, assert_frob, f64
+
+pytestmark = pytest.mark.gpu
+
+C = pytest.importorskip("gemm_epilogue_transformer_tma_gb300")
+from gemm_epilogue_transformer_tma_gb300.path import BlockBuffers  # noqa: E402
+from tests.test_gpu_ce import run_ce  # noqa: E402
+from tests.test_gpu_fp8_bwd import check_fp8_backward_stages, check_fp8_forward_stages, run_fp8  # noqa: E402
+from tests.test_gpu_parity import check_backward_stages, check_forward  # noqa: E402
+
+
+def block_shapes(n=32, seed=2024):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        M = int(rng.integers(1, 1100))
+        K1 = 8 * int(rng.integers(1, 80))
+        d = 8 * int(rng.integers(1, 96))
+        F = 8 * int(rng.integers(1, 72))
+        out.append(BlockShape(f"fuzz{i}", M, K1, d, 2 * F))
+    return out
+
+
+def fp8_block_shapes(n=8, seed=2026):
+    """8-bit operands: extents multiples of 16 (TMA rows of 16 bytes)."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        M = int(rng.integers(1, 900))
+        K1 = 16 * int(rng.integers(1, 40))
+        d = 16 * int(rng.integers(1, 48))
+        F = 16 * int(rng.integers(1, 36))
+        out.append(BlockShape(f"fuzz_fp8_{i}", M, K1, d, 2 * F))
+    return out
+
+
+def ce_shapes(n=12, seed=2025):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        M = int(rng.integers(1, 400))
+        d = 8 * int(rng.integers(1, 48))
+        V = 8 * int(rng.integers(1, 5000))
+        out.append(CEShape(f"fuzz{i}", M, d, V))
+    return out
+
+
+BLOCKS = block_shapes()
+FP8_BLOCKS = fp8_block_shapes()
+CES = ce_shapes()
+
+
+@pytest.mark.parametrize("i", range(len(BLOCKS)), ids=[f"M{s.M}_K{s.K1}_d{s.d}_N{s.N2}" for s in BLOCKS])
+def test_block_random_shape(i):
+    s = BLOCKS[i]
+    C.coda_set_sm_pairing(i % 2 == 0)
+    try:
+        x = {k: v.cuda() for k, v in block_inputs(s, i, "cpu").items()}
+        b = BlockBuffers(x)
+        b.forward()
+        b.backward_stages()
+        assert_device_ok()
+    finally:
+        C.coda_set_sm_pairing(True)
+    check_forward(s, b, x)
+    check_backward_stages(s, b, x)
+
+
+@pytest.mark.parametrize("i", range(len(FP8_BLOCKS)),
+                         ids=[f"M{s.M}_K{s.K1}_d{s.d}_N{s.N2}" for s in FP8_BLOCKS])
+def test_fp8_block_random_shape(i):
+    """The block on e4m3 activations and weights and e5m2 gradients."""
+    s = FP8_BLOCKS[i]
+    C.coda_set_sm_pairing(i % 2 == 0)
+    try:
+        x, b = run_fp8(s, seed=100 + i)
+    finally:
+        C.coda_set_sm_pairing(True)
+    check_fp8_forward_stages(s, x, b)
+    check_fp8_backward_stages(s, x, b)
+
+
+@pytest.mark.parametrize("i", range(len(CES)), ids=[f"M{s.M}_d{s.d}_V{s.V}" for s in CES])
+def test_ce_random_shape(i):
+    s = CES[i]
+    C.coda_set_sm_pairing(i % 2 == 0)
+    try:
+        x = {k: v.cuda() for k, v in ce_inputs(s, i).items()}
+        x["labels"] = with_edge_labels(x["labels"], s.V)
+        o = run_ce(x["H"], x["Wt"], x["labels"])
+        assert_device_ok()
+    finally:
+        C.coda_set_sm_pairing(True)
+    H, Wt, y = f64(x["H"]), f64(x["Wt"]), x["labels"].cpu().numpy()
+    fw = O.ce_forward(H, Wt, y)
+    bw = O.ce_backward(H, Wt, y)
+    assert_elem(o["lse"], fw["lse"], "lse", tol=1e-4)
+    assert abs(o["loss"].item() - fw["loss"]) <= 1e-4 * abs(fw["loss"])
+    L = O.logits_rows(H, Wt)
+    check_argmax(o["argmax"], H, Wt, L=L)
+    check_label_rows(o["zy"], o["row_loss"], L, y, fw["lse"])
+    assert_frob(o["dH"], bw["dH"], "dH")
+    assert_frob(o["dW"], bw["dWt"], "dW")
