@@ -7,7 +7,9 @@ boundary's rule; M any positive size), so that tails of every width
 against the 128-row / 256-column tiles, the 64-deep k-blocks, the 128-column
 partial sums and the 16384-column vocabulary chunks come up without being
 chosen.  Every stage is graded as in the hand-picked tests, the block also on
-8-bit operands (extents multiples of 16 there); each shape runs on SM pairs
+8-bit operands (extents multiples of 16 there), and the further epilogue
+programs (the SwiGLU backward in the down projection's data gradient, RoPE
+in the QKV projection) on shapes of their own; each shape runs on SM pairs
 or on single SMs, alternately.
 
 Method: "CODA: Rewriting Transformer Blocks as GEMM-Epilogue Programs"
@@ -15,9 +17,10 @@ Method: "CODA: Rewriting Transformer Blocks as GEMM-Epilogue Programs"
 """
 import numpy as np
 import pytest
+import torch
 
 import oracle as O
-from coda_inputs import BlockShape, CEShape, block_inputs, ce_inputs
+from coda_inputs import BlockShape, CEShape, block_inputs, ce_inputs, down_proj_inputs
 from tests._ce import check_argmax, check_label_rows, with_edge_labels
 from tests._parity import assert_device_ok, assert_elem, assert_frob, f64
 
@@ -122,3 +125,73 @@ def test_ce_random_shape(i):
     check_label_rows(o["zy"], o["row_loss"], L, y, fw["lse"])
     assert_frob(o["dH"], bw["dH"], "dH")
     assert_frob(o["dW"], bw["dWt"], "dW")
+
+
+# the next epilogue programs on the same kind of random shapes: the SwiGLU
+# backward inside the down projection's data-gradient GEMM with dgrad2 on its
+# c partials, and RoPE in the QKV projection's epilogue
+NEXT_BLOCKS = block_shapes(n=8, seed=2027)
+
+
+@pytest.mark.parametrize("i", range(len(NEXT_BLOCKS)),
+                         ids=[f"M{s.M}_K{s.K1}_d{s.d}_N{s.N2}" for s in NEXT_BLOCKS])
+def test_down_proj_swiglu_bwd_random_shape(i):
+    s = NEXT_BLOCKS[i]
+    C.coda_set_sm_pairing(i % 2 == 0)
+    try:
+        x = {k: v.cuda() for k, v in block_inputs(s, i, "cpu", with_dy=False).items()}
+        dp = {k: v.cuda() for k, v in down_proj_inputs(s, i, "cpu").items()}
+        b = BlockBuffers(dict(x, dY=torch.empty(s.M, s.F, dtype=torch.bfloat16, device="cuda")))
+        b.forward()
+        cpart = torch.empty(s.M, C.coda_prms_num_tiles(s.F), device="cuda")
+        C.coda_gemm_dgrad_swiglu_bwd(dp["dYb"], dp["W3t"], b.z, b.rstd, b.dP, cpart)
+        C.coda_gemm_dgrad_rmsbwd_cpart(b.dP, b.W2t, b.H, b.g, b.rstd, cpart, b.dH, b.dgpart)
+        C.coda_dg_combine(b.dgpart, b.dg)
+        assert_device_ok()
+    finally:
+        C.coda_set_sm_pairing(True)
+    dY = O.down_proj_dgrad(f64(dp["dYb"]), f64(dp["W3t"]))
+    z, rstd = f64(b.z), f64(b.rstd)
+    dP_ref, c_ref = O.stage_swiglu_bwd(dY, z, rstd, s.d)
+    assert_elem(b.dP, dP_ref, "dP")
+    assert_elem(cpart, O.swiglu_c_partials(dY, z, C.PARTIAL_COLS), "cpart")
+    c = f64(cpart).sum(axis=1) * rstd ** 2 / s.d
+    dH_ref, dg_ref = O.stage_dgrad2_rmsbwd(f64(b.dP), f64(x["W2t"]), f64(x["g"]), f64(b.H), c)
+    assert_elem(b.dH, dH_ref, "dH")
+    assert_elem(b.dg, dg_ref, "dg")
+
+
+def rope_shapes(n=8, seed=2028):
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        M = int(rng.integers(1, 1100))
+        d = 8 * int(rng.integers(1, 80))
+        hq = int(rng.integers(1, 6))
+        hkv = int(rng.integers(0, hq + 1))
+        S = int(rng.integers(1, 700))
+        out.append((M, d, hq, hkv, S))
+    return out
+
+
+ROPES = rope_shapes()
+
+
+@pytest.mark.parametrize("i", range(len(ROPES)), ids=[f"M{m}_d{d}_q{q}_kv{k}_S{s}" for m, d, q, k, s in ROPES])
+def test_qkv_rope_random_shape(i):
+    M, d, hq, hkv, S = ROPES[i]
+    g = torch.Generator().manual_seed(500 + i)
+    X = torch.randn(M, d, generator=g).to(torch.bfloat16).cuda()
+    W = (torch.randn((hq + 2 * hkv) * 128, d, generator=g) * 0.02).to(torch.bfloat16).cuda()
+    cos_t = torch.empty(S, 64, device="cuda")
+    sin_t = torch.empty(S, 64, device="cuda")
+    qkv = torch.empty(M, (hq + 2 * hkv) * 128, dtype=torch.bfloat16, device="cuda")
+    C.coda_set_sm_pairing(i % 2 == 0)
+    try:
+        C.coda_rope_table(cos_t, sin_t, 10000.0)
+        C.coda_gemm_qkv_rope(X, W, cos_t, sin_t, qkv, hq, hkv)
+        assert_device_ok()
+    finally:
+        C.coda_set_sm_pairing(True)
+    ref = O.qkv_rope(f64(X), f64(W), hq, hkv, 128, S)
+    assert_elem(qkv, ref, "qkv")
