@@ -195,3 +195,87 @@ def test_qkv_rope_random_shape(i):
         C.coda_set_sm_pairing(True)
     ref = O.qkv_rope(f64(X), f64(W), hq, hkv, 128, S)
     assert_elem(qkv, ref, "qkv")
+
+
+# the opt-in schedules on random shapes, with integer operands (one exact
+# result whatever the summation order): 256 x 512 pair tiles (K of at least
+# 16384 and an even number of 256-column tiles) and split last waves
+def exact_product(A, Bt):
+    v = A.to(torch.float64) @ Bt.to(torch.float64).T
+    assert float(v.abs().max()) < 2 ** 24
+    return v.to(torch.float32).to(torch.bfloat16)
+
+
+def wide_shapes(n=5, seed=2029):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        M = int(rng.integers(1, 2600))
+        if i % 3 == 2:
+            M = 8 * max(1, M // 8)  # A read MN-major: its rows of M elements obey the 8-element rule
+        N = 512 * int(rng.integers(1, 9)) - 8 * int(rng.integers(0, 32))
+        K = 16384 + 8 * int(rng.integers(0, 512))
+        out.append((M, N, K))
+    return out
+
+
+def split_shapes(n=5, seed=2030, pairs=76):
+    """Random shapes that the launcher splits on a GPU of `pairs` SM pairs
+    (asked of the library's own rule, which runs on the host)."""
+    rng = np.random.default_rng(seed)
+    out = []
+    while len(out) < n:
+        M = int(rng.integers(300, 2600))
+        if len(out) % 3 == 2:
+            M = 8 * (M // 8)  # A read MN-major (see wide_shapes)
+        N = 8 * int(rng.integers(40, 560))
+        K = 8 * int(rng.integers(400, 2000))
+        tiles = -(-M // 256) * -(-N // 256)
+        if C.coda_debug_split_ranges(tiles, -(-K // 64), pairs) > 1:
+            out.append((M, N, K))
+    return out
+
+
+WIDES = wide_shapes()
+SPLITS = split_shapes()
+
+
+def _int_gemm(M, N, K, a_mn, b_mn, seed):
+    from tests.test_gpu_exact import ints
+    A, Bt = ints((M, K), -3, 3, seed), ints((N, K), -3, 3, seed + 1)
+    Ad = (A.T.contiguous() if a_mn else A).to(torch.bfloat16).cuda()
+    Bd = (Bt.T.contiguous() if b_mn else Bt).to(torch.bfloat16).cuda()
+    Cd = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    C.coda_gemm(Ad, a_mn, Bd, b_mn, Cd, M, N, K)
+    torch.cuda.synchronize()
+    assert_device_ok()
+    return Cd.cpu(), exact_product(A, Bt)
+
+
+@pytest.mark.parametrize("i", range(len(WIDES)), ids=[f"M{m}_N{n}_K{k}" for m, n, k in WIDES])
+def test_wide_tiles_random_shape(i):
+    M, N, K = WIDES[i]
+    C.coda_set_sm_pairing(True)
+    C.coda_set_wide_tiles(8)
+    try:
+        assert C.coda_debug_wide_applies(M, N, K) == 1
+        got, ref = _int_gemm(M, N, K, i % 3 == 2, i % 3 != 0, 700 + 2 * i)
+    finally:
+        C.coda_set_wide_tiles(0)
+    assert torch.equal(got, ref)
+
+
+@pytest.mark.parametrize("i", range(len(SPLITS)), ids=[f"M{m}_N{n}_K{k}" for m, n, k in SPLITS])
+def test_split_tiles_random_shape(i):
+    M, N, K = SPLITS[i]
+    ws = torch.empty(C.coda_split_workspace_bytes(), dtype=torch.uint8, device="cuda")
+    C.coda_set_sm_pairing(True)
+    C.coda_set_split_workspace(ws)
+    try:
+        tiles = -(-M // 256) * -(-N // 256)
+        pairs = torch.cuda.get_device_properties(0).multi_processor_count // 2
+        assert C.coda_debug_split_ranges(tiles, -(-K // 64), pairs) > 1
+        got, ref = _int_gemm(M, N, K, i % 3 == 2, i % 3 != 0, 800 + 2 * i)
+    finally:
+        C.coda_set_split_workspace(None)
+    assert torch.equal(got, ref)
