@@ -61,6 +61,7 @@ SIGNATURES = {
     "coda_debug_wide_applies": (_INT, [_P, _INT, _INT, _INT]),
     "coda_set_sm_pairing": (_INT, [_P, _INT]),
     "coda_set_wide_tiles": (_INT, [_P, _INT]),
+    "coda_set_lmhead_chunk": (_INT, [_P, _I64]),
     "coda_split_workspace_bytes": (_SZ, [_P]),
     "coda_set_split_workspace": (_INT, [_P, _P, _SZ, _P]),
     "coda_prms_num_tiles": (_I64, [_I64]),
@@ -212,6 +213,12 @@ def coda_set_wide_tiles(lead_kblocks: int, device: int | None = None):
     """256 x 512 pair tiles for the long-K backward GEMMs with lead J =
     lead_kblocks k-blocks; 0 turns them off (see include/coda.h)."""
     _check(load_library().coda_set_wide_tiles(handle(device), int(lead_kblocks)), "coda_set_wide_tiles")
+
+
+def coda_set_lmhead_chunk(cols: int, device: int | None = None):
+    """Vocabulary columns per LM-head backward chunk (a multiple of 256 up to
+    32768; 0 = the default, 32768); see include/coda.h."""
+    _check(load_library().coda_set_lmhead_chunk(handle(device), int(cols)), "coda_set_lmhead_chunk")
 
 
 def coda_split_workspace_bytes(device: int | None = None) -> int:

@@ -112,6 +112,16 @@ coda_status_t coda_set_sm_pairing(coda_handle_t h, int enable);
  * fp32 summation order.  Returns CODA_ERR_INVALID_ARG outside [0, 64]. */
 coda_status_t coda_set_wide_tiles(coda_handle_t h, int lead_kblocks);
 
+/* Width of the vocabulary chunks of the LM-head backward (coda_lmhead_ce,
+ * coda_lmhead_ce_fp8): the logits are recomputed and dL written for one
+ * chunk of `cols` vocabulary columns at a time, then dH and that chunk's dW
+ * rows are computed from it.  Narrower chunks shrink the dL buffer that
+ * passes between the two launches, at the price of more and smaller launches
+ * (measured slower at every width below the default).  cols: a multiple of 256 in [256, 32768]; 0
+ * restores the default, 32768.  The workspace size does not depend on it.  Results equal across widths up to fp32 summation order
+ * of dH.  Returns CODA_ERR_INVALID_ARG otherwise. */
+coda_status_t coda_set_lmhead_chunk(coda_handle_t h, int64_t cols);
+
 /* Scratch that lets this handle's SM-pair GEMMs keep every SM pair busy in
  * their last, partial wave.  Without it (the default) each SM pair computes
  * whole 256 x 256 tiles, and when the tile count is not a multiple of the

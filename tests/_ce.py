@@ -10,22 +10,22 @@ import torch
 import oracle as O
 from tests._parity import assert_elem, f64
 
-CHUNK = 16384  # vocabulary columns per backward chunk
+CHUNK = 32768  # vocabulary columns per backward chunk (the library's default)
 
 
-def edge_labels(V):
+def edge_labels(V, chunk=CHUNK):
     """Vocabulary columns on the edges the kernels split at: the 128-column
     partials, the 256-column tiles, the backward chunks, and the last tile."""
     cols = {0, 1, 127, 128, 129, 255, 256, 257, V - 1, V - 2, V - 128, V - 129, ((V - 1) // 256) * 256,
             ((V - 1) // 256) * 256 - 1}
-    for c0 in range(CHUNK, V, CHUNK):
+    for c0 in range(chunk, V, chunk):
         cols |= {c0 - 1, c0, c0 + 1}
     return sorted(c for c in cols if 0 <= c < V)
 
 
-def with_edge_labels(labels, V):
+def with_edge_labels(labels, V, chunk=CHUNK):
     lab = labels.clone()
-    e = edge_labels(V)
+    e = edge_labels(V, chunk)
     n = min(len(e), lab.numel())
     lab[:n] = torch.tensor(e[:n], dtype=lab.dtype)
     return lab

@@ -4,7 +4,8 @@ log-sum-exp" and the stateful max / sum-exp statistics; the label logit is
 gathered by the epilogue of the vocabulary tile that holds the label).
 
 Small vocabularies that still span several 256-column tiles with a ragged
-last tile, plus several 16384-column backward chunks.  Every row's label
+last tile, plus two 32768-column backward chunks (and ten of 4096 columns
+with the chunk width set narrower).  Every row's label
 logit and row loss is read back from the workspace and graded, with labels
 placed on the 128- and 256-column tile edges, the backward chunk edges and
 the last (ragged) tile."""
@@ -61,6 +62,35 @@ def test_ce_parity(M, d, V, pairing):
     check_label_rows(o["zy"], o["row_loss"], L, y, fw["lse"])
     assert_frob(o["dH"], bw["dH"], "dH")
     assert_frob(o["dW"], bw["dWt"], "dW")
+
+
+@pytest.mark.parametrize("chunk,V", [(4096, 40000), (256, 5000)])
+def test_ce_narrower_backward_chunks(chunk, V):
+    """coda_set_lmhead_chunk: the backward in narrower vocabulary chunks (ten
+    of 4096 columns; twenty of 256, one tile each) against the oracle, with
+    labels on the chunk edges; dW equal to the default chunks' bit for bit
+    (its tiles do not change), dH within its fp32 summation order."""
+    lib = C.load_library()
+    h = C.handle()
+    for bad in (-256, 100, 255, 32768 + 256):
+        assert lib.coda_set_lmhead_chunk(h, bad) == 1  # CODA_ERR_INVALID_ARG
+    s = CEShape("t", 200, 136, V)
+    x = {k: v.cuda() for k, v in ce_inputs(s, 3).items()}
+    x["labels"] = with_edge_labels(x["labels"], V, chunk)
+    base = run_ce(x["H"], x["Wt"], x["labels"])
+    C.coda_set_lmhead_chunk(chunk)
+    try:
+        o = run_ce(x["H"], x["Wt"], x["labels"])
+        assert_device_ok()
+    finally:
+        C.coda_set_lmhead_chunk(0)
+    H, Wt, y = f64(x["H"]), f64(x["Wt"]), x["labels"].cpu().numpy()
+    bw = O.ce_backward(H, Wt, y)
+    assert torch.equal(o["lse"], base["lse"]) and torch.equal(o["loss"], base["loss"])
+    assert torch.equal(o["dW"], base["dW"])
+    assert_frob(o["dH"], bw["dH"], "dH")
+    assert_frob(o["dW"], bw["dWt"], "dW")
+    assert_frob(o["dH"], f64(base["dH"]), "dH vs default chunks", tol=2 ** -8)
 
 
 def test_ce_forward_only_and_label_range():
