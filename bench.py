@@ -900,29 +900,42 @@ def main():
         e2e_steps(3)
         # as many steps as the headline: the first step's H2D copy and the
         # last step's read-back overlap nothing and are timed in full.  The
-        # run is timed three times and the median taken: a host wall clock
-        # also counts any stall of the host thread (one run of a default
-        # bench once took 17 % longer than the runs before and after it).
+        # run is timed three times, each beside a run of the same number of
+        # device-resident steps (the order alternating), and the medians
+        # taken: a host wall clock also counts any stall of the host thread,
+        # and the part heats over the bench, so this leg, which runs after
+        # the headline, is compared with device steps timed at the same
+        # point rather than with the headline.
         n_e2e = max(3, args.steps)
-        runs = []
-        for _ in range(E2E_REPEATS):
-            barrier()
-            t0 = time.perf_counter()
-            with nvtx("e2e"):
-                e2e_steps(n_e2e)
-            barrier()
-            runs.append(max_over_ranks((time.perf_counter() - t0) * 1e3 / n_e2e, dist, "cuda"))
+        runs, dev_runs = [], []
+        for r in range(E2E_REPEATS):
+            for leg in (("e2e", "dev") if r % 2 == 0 else ("dev", "e2e")):
+                if leg == "dev":
+                    barrier()
+                    dev_runs.append(max_over_ranks(time_steps(calls, n_e2e, 0, stage_events=False)[0] / n_e2e,
+                                                   dist, "cuda"))
+                    continue
+                barrier()
+                t0 = time.perf_counter()
+                with nvtx("e2e"):
+                    e2e_steps(n_e2e)
+                barrier()
+                runs.append(max_over_ranks((time.perf_counter() - t0) * 1e3 / n_e2e, dist, "cuda"))
         e2e_ms = statistics.median(runs)
         h2d = sum(host[k].numel() * host[k].element_size() for k in ins)
         d2h = host[res].numel() * host[res].element_size()
         extras["e2e"] = {"value": aggregate_value(step_flops, e2e_ms, world), "unit": UNIT, "ms_per_step": e2e_ms,
                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                          "steps": n_e2e, "runs_ms_per_step": runs,
+                         "device_runs_ms_per_step": dev_runs,
+                         "vs_device_same_rounds": statistics.median(d / e for d, e in zip(dev_runs, runs)),
                          "host_link_gbs": host_link_gbs(),
                          "h2d_ms_per_step_at_link_rate": None,
                          "api": "coda_block_create / coda_block_step_host / coda_block_sync (host buffers)",
                          "timing": "host wall clock over the whole run, synchronize (and barrier) at both ends, "
-                                   "median of three runs; the executor overlaps step i+1's H2D copies and step i-1's D2H read-back "
+                                   "median of three runs, each beside a run of device-resident steps "
+                                   "(vs_device_same_rounds: median per-round device / e2e time); the "
+                                   "executor overlaps step i+1's H2D copies and step i-1's D2H read-back "
                                    "with step i's kernels; each step's backward waits for its dY copy, its "
                                    "forward for X and R only; the first step's X / R copy and the last step's "
                                    "D2H overlap nothing; per-rank bytes, value summed over ranks"}
