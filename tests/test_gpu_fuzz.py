@@ -6,7 +6,8 @@ these draw M, K1, d, F and V from a fixed seed (extents multiples of 8, the
 boundary's rule; M any positive size), so that tails of every width
 against the 128-row / 256-column tiles, the 64-deep k-blocks, the 128-column
 partial sums and the 16384-column vocabulary chunks come up without being
-chosen.  Every stage is graded as in the hand-picked tests, the block also on
+chosen.  Every stage is graded as in the hand-picked tests (and the block's
+outputs are bit-identical over two runs), the block also on
 8-bit operands (extents multiples of 16 there), and the further epilogue
 programs (the SwiGLU backward in the down projection's data gradient, RoPE
 in the QKV projection) on shapes of their own; each shape runs on SM pairs
@@ -70,6 +71,7 @@ def ce_shapes(n=12, seed=2025):
 
 
 BLOCKS = block_shapes()
+OUTPUTS = ("H", "psum", "rstd", "z", "out", "dP", "c", "dgpart", "dH", "dg", "dW2t", "dX", "dW1t")
 FP8_BLOCKS = fp8_block_shapes()
 CES = ce_shapes()
 
@@ -84,8 +86,16 @@ def test_block_random_shape(i):
         b.forward()
         b.backward_stages()
         assert_device_ok()
+        first = {k: getattr(b, k).clone() for k in OUTPUTS}
+        # a second run: every reduction is a fixed-order combine, so the
+        # results must be bit-identical
+        b.forward()
+        b.backward_stages()
+        assert_device_ok()
     finally:
         C.coda_set_sm_pairing(True)
+    for k in OUTPUTS:
+        assert torch.equal(getattr(b, k), first[k]), f"{k} differs between two runs"
     check_forward(s, b, x)
     check_backward_stages(s, b, x)
 
