@@ -594,7 +594,10 @@ coda_status_t coda_gemm_rowscale_swiglu_fp8(coda_handle_t h, const void* Hq, con
 /* block reduction "block log-sum-exp", stateful max / sum-exp)              */
 /* ------------------------------------------------------------------------ */
 
-/* Workspace of coda_lmhead_ce (with_grads = 0: forward only). */
+/* Workspace of coda_lmhead_ce (with_grads = 0: forward only): the per-tile
+ * statistics partials (3 x M x ceil(V / 128) x 4 bytes), the per-row label
+ * logits and losses, and with gradients the fp32 dH accumulator (M x d x 4)
+ * and one vocabulary chunk of dL (M x min(V, 32768) x 2 bytes). */
 size_t coda_lmhead_ce_workspace_bytes(int64_t M, int64_t d, int64_t V, int with_grads);
 
 /* Per-row results that coda_lmhead_ce and coda_lmhead_ce_fp8 leave in their
