@@ -1028,8 +1028,9 @@ coda_status_t coda_lmhead_ce_fp8(coda_handle_t h, const void* Hq, const float* s
     const uint8_t* Wqc = Wc8 + v0 * d;
     CODA_CUDA(gemm_ce_grad_fp8(cx, Hc, sH, Wqc, sW, labels, lse, dLq, code_inv, int(M), int(d), int(Vc), int(v0),
                                inv_M));
-    CODA_CUDA(gemm_ce_bwd_fp8(cx, dLq, s_dL, Wqc, sW, Hc, sH, w.dH32, v0 > 0, static_cast<bf16*>(dWt) + v0 * d,
-                              int(M), int(d), int(Vc)));
+    // dH (+)= dL W and the chunk's dW rows from the codes, one grouped launch
+    CODA_CUDA(gemm_group_ce_bwd_fp8(cx, dLq, s_dL, Wqc, sW, Hc, sH, w.dH32, v0 > 0,
+                                    static_cast<bf16*>(dWt) + v0 * d, int(M), int(d), int(Vc)));
   }
   CODA_CUDA(launch_f32_to_bf16(cx, w.dH32, static_cast<bf16*>(dHs), M * d));
   return CODA_OK;

@@ -202,6 +202,11 @@ cudaError_t gemm_ce_grad_fp8(const LaunchCtx& c, const uint8_t* Hq, const float*
 cudaError_t gemm_ce_bwd_fp8(const LaunchCtx& c, const uint8_t* dLq, float s_dL, const uint8_t* Wq_chunk,
                             const float* sW, const uint8_t* Hq, const float* sH, float* dH32, bool accumulate,
                             __nv_bfloat16* dWc, int M, int d, int Vc);
+// the same two GEMMs in one grouped SM-pair launch (the two launches above
+// on single SMs)
+cudaError_t gemm_group_ce_bwd_fp8(const LaunchCtx& c, const uint8_t* dLq, float s_dL, const uint8_t* Wq_chunk,
+                                  const float* sW, const uint8_t* Hq, const float* sH, float* dH32, bool accumulate,
+                                  __nv_bfloat16* dWc, int M, int d, int Vc);
 
 int ce_tile_cols();    // vocabulary columns per CE statistics tile
 int prms_tile_cols();  // columns per partial-RMS tile of GEMM1

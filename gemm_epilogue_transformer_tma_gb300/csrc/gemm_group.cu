@@ -74,7 +74,8 @@ cudaError_t launch_group(const LaunchCtx& c, GroupArgs<Epi0, Epi1>& g) {
   const int tiles = g.sh0.tiles_m * g.sh0.tiles_n + g.sh1.tiles_m * g.sh1.tiles_n;
   const int P = std::max(1, std::min(tiles, *mp));
   g.sched = make_sched(g.sh0, g.sh1, P);
-  KernelCtl ctl{c.status, c.timeout_ns, c.skip_first_stage, nullptr, nullptr, FP8 ? c.f8_fmt : 0u, 1.f};
+  KernelCtl ctl{c.status, c.timeout_ns, c.skip_first_stage, nullptr, nullptr, FP8 ? c.f8_fmt : 0u,
+                FP8 ? c.scale_host : 1.f};
   return launch_chained(c, kern, dim3(2 * P), dim3(gemm_threads<Epi0>()), L::TOTAL, g, ctl);
 }
 }  // namespace
@@ -155,6 +156,36 @@ cudaError_t gemm_group_ce_bwd(const LaunchCtx& c, const __nv_bfloat16* dL, const
   ga.ep0.beta = accumulate ? 1 : 0;
   if (!make_tmap_store_bf16(&ga.ep1.out, dWc, d, Vc, d)) return cudaErrorInvalidValue;
   return launch_group<false, true, true, true, EpiStoreF32, EpiStore>(c, ga);
+}
+
+cudaError_t gemm_group_ce_bwd_fp8(const LaunchCtx& c0, const uint8_t* dLq, float s_dL, const uint8_t* Wq_chunk,
+                                  const float* sW, const uint8_t* Hq, const float* sH, float* dH32, bool accumulate,
+                                  __nv_bfloat16* dWc, int M, int d, int Vc) {
+  if (!c0.pair) return gemm_ce_bwd_fp8(c0, dLq, s_dL, Wq_chunk, sW, Hq, sH, dH32, accumulate, dWc, M, d, Vc);
+  LaunchCtx c = c0;
+  c.scale_host = s_dL;               // dL's power-of-two scale, common to both problems
+  c.f8_fmt = f8_format_bits(1, 0);   // e5m2 dL codes against e4m3 W / H codes
+  GroupArgs<EpiStoreF32, EpiStore> ga{};
+  // problem 0: dH32[M, d] (+)= dL codes [M][Vc] (K-major) W codes [Vc][d]
+  // (MN-major), scale s_dL * sW
+  if (!make_f8_operand_map(&ga.tmA0, dLq, false, M, Vc, BM) ||
+      !make_f8_operand_map(&ga.tmB0, Wq_chunk, true, d, Vc, b_box_rows(c)))
+    return cudaErrorInvalidValue;
+  // problem 1: dWc[Vc, d] = dL^T H; K' = M, A' = dL codes [M][Vc] and B' = H
+  // codes [M][d], both MN-major, scale s_dL * sH
+  if (!make_f8_operand_map(&ga.tmA1, dLq, true, Vc, M, BM) ||
+      !make_f8_operand_map(&ga.tmB1, Hq, true, d, M, b_box_rows(c)))
+    return cudaErrorInvalidValue;
+  ga.sh0 = pair_shape(M, d, Vc, true);
+  ga.sh1 = pair_shape(Vc, d, M, true);
+  if (!make_tmap_store_f32(&ga.ep0.out, dH32, d, M, d)) return cudaErrorInvalidValue;
+  ga.ep0.beta = accumulate ? 1 : 0;
+  if (!make_tmap_store_bf16(&ga.ep1.out, dWc, d, Vc, d)) return cudaErrorInvalidValue;
+  ga.scale_a0 = nullptr;
+  ga.scale_b0 = sW;
+  ga.scale_a1 = nullptr;
+  ga.scale_b1 = sH;
+  return launch_group<false, true, true, true, EpiStoreF32, EpiStore, true>(c, ga);
 }
 
 // Host check of the grouped schedule: every tile of both problems is visited

@@ -302,11 +302,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<Epi0>()
     const uint32_t leader_tempty = mapa_shared(smem_u32(tempty), 0);
     const uint32_t stage_base =
         smem_u32(smem + L::RING_BYTES) + static_cast<uint32_t>((warp - 2) * SLOTS * STORE_SLOT_BYTES);
-    // each problem's accumulator scale (1 for bf16 operands)
+    // each problem's accumulator scale (1 for bf16 operands): its operands'
+    // scales times a host-given factor common to both problems
     float acc_scale[2] = {1.f, 1.f};
     if (FP8) {
-      acc_scale[0] = (g.scale_a0 ? *g.scale_a0 : 1.f) * (g.scale_b0 ? *g.scale_b0 : 1.f);
-      acc_scale[1] = (g.scale_a1 ? *g.scale_a1 : 1.f) * (g.scale_b1 ? *g.scale_b1 : 1.f);
+      acc_scale[0] = ctl.scale_host * (g.scale_a0 ? *g.scale_a0 : 1.f) * (g.scale_b0 ? *g.scale_b0 : 1.f);
+      acc_scale[1] = ctl.scale_host * (g.scale_a1 ? *g.scale_a1 : 1.f) * (g.scale_b1 ? *g.scale_b1 : 1.f);
     }
     int prob, t;
     for (int it = 0; group_tile(g.sched, cluster_id, it, prob, t); ++it) {
