@@ -89,6 +89,38 @@ def test_fp8_ce_parity(M, d, V, pairing):
     assert_frob(o["dW"], bb["dWt"], "dW fp8 e2e", tol=0.15)
 
 
+def test_fp8_ce_narrower_backward_chunks():
+    """The 8-bit backward in 4096-column chunks (ten at V = 40000, each one
+    grouped dH / dW launch): dW bit-equal to the default chunks' (its tiles do
+    not change), dH within its fp32 summation order, and both against the
+    oracle fed the same codes."""
+    M, d, V = 37, 256, 40000
+    s = CEShape("t", M, d, V)
+    x = {k: v.cuda() for k, v in ce_inputs(s, 4).items()}
+    x["labels"] = with_edge_labels(x["labels"], V, 4096)
+    Hq, sH = quantize(x["H"])
+    Wq, sW = quantize(x["Wt"])
+    base = run_fp8_ce(Hq, sH, Wq, sW, x["labels"])
+    C.coda_set_lmhead_chunk(4096)
+    try:
+        o = run_fp8_ce(Hq, sH, Wq, sW, x["labels"])
+        torch.cuda.synchronize()
+    finally:
+        C.coda_set_lmhead_chunk(0)
+    assert_device_ok()
+    assert torch.equal(o["dW"], base["dW"])
+    assert_frob(o["dH"], f64(base["dH"]), "dH vs default chunks (fp8)", tol=2 ** -8)
+    Hd, Wd, y = deq(Hq, sH), deq(Wq, sW), x["labels"].cpu().numpy()
+    L = O.logits_rows(Hd, Wd)
+    lse = O.ce_forward(Hd, Wd, y)["lse"]
+    P = np.exp(L - lse[:, None])
+    P[np.arange(M), y] -= 1.0
+    s_dL = O.fp8_scale(np.array([1.0 / M], np.float32), "e5m2")
+    dLd = O.fp8_decode(O.fp8_quantize(P / M, s_dL, "e5m2"), "e5m2") * float(s_dL)
+    assert_frob(o["dH"], dLd @ Wd, "dH (fp8, 4096-column chunks)")
+    assert_frob(o["dW"], dLd.T @ Hd, "dW (fp8, 4096-column chunks)")
+
+
 def test_fp8_ce_forward_only_and_argument_errors():
     s = CEShape("t", 64, 64, 512)
     x = {k: v.cuda() for k, v in ce_inputs(s, 1).items()}
